@@ -1,0 +1,146 @@
+"""Double-precision CPU oracle for the selective state-space scan (S6).
+
+TEST INFRASTRUCTURE ONLY.  The library never imports this package.  The tests,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` are its only
+users.  It shares no code with the CUDA path: the arithmetic lives in
+``ssm_oracle.c`` (compiled with plain gcc, no fast-math) and, as an independent
+second restatement, in ``numpy_oracle.py``.
+
+What it computes (the plain definition, sequential over t, in float64):
+
+    Δ_t   = softplus(Δraw_t + bias)
+    Ā     = exp(Δ_t A),  B̄ = (Δ_t A)^-1 (exp(Δ_t A) - I) Δ_t B_t
+    h_t   = Ā h_{t-1} + B̄ x_t            (h_0 = 0 unless h0 is given)
+    y_t   = C_t h_t + D x_t
+    out_t = y_t · silu(z_t)
+
+Sources: "State Space Models（SSM）とMamba" §2.2 離散化 and §4.2 Selective SSM;
+"Mambaとは？Transformer以外の系列モデル", sections 状態空間モデルを一つの式から理解する,
+固定SSMには「再帰」と「畳み込み」の二つの顔がある and Mamba blockのarchitecture.
+
+Parity pinned: every function here is checked against the pages' worked
+example, closed forms, brute-force convolution and invariants in
+``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssm_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libssm_oracle.so")
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile ssm_oracle.c into a shared library (plain gcc, IEEE math)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-std=c11", "-shared", "-fPIC",
+             "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, dp = ctypes.c_int64, ctypes.c_void_p
+            lib.oracle_scan.argtypes = [i64, i64, i64, i64] + [dp] * 11 + [i64, i64]
+            lib.oracle_scan.restype = None
+            lib.oracle_step.argtypes = [i64, i64, i64] + [dp] * 10 + [i64, i64]
+            lib.oracle_step.restype = None
+            _lib = lib
+    return _lib
+
+
+def _f64(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _row_ranges(rows: int, threads: int):
+    threads = max(1, min(threads, rows))
+    step = (rows + threads - 1) // threads
+    return [(s, min(rows, s + step)) for s in range(0, rows, step)]
+
+
+def default_threads() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def scan(u, delta, A, B, C, D=None, z=None, bias=None, h0=None, threads: int | None = None):
+    """Parallel-mode selective scan, sequential loop in float64.
+
+    u, delta, z: [batch, d_inner, L]; B, C: [batch, L, N]; A: [d_inner, N];
+    D, bias: [d_inner]; h0: [batch, d_inner, N] or None (zero state).
+    Returns (out [batch, d_inner, L], hT [batch, d_inner, N]) as float64 arrays.
+    Rows (batch, channel) are independent, so they are split between threads;
+    each row is one plain sequential loop.
+    """
+    u, delta, A, B, C = (_f64(x) for x in (u, delta, A, B, C))
+    D, z, bias, h0 = (_f64(x) for x in (D, z, bias, h0))
+    batch, d_inner, L = u.shape
+    N = A.shape[1]
+    assert delta.shape == u.shape and A.shape == (d_inner, N)
+    assert B.shape == (batch, L, N) and C.shape == (batch, L, N)
+    assert z is None or z.shape == u.shape
+    assert D is None or D.shape == (d_inner,)
+    assert bias is None or bias.shape == (d_inner,)
+    assert h0 is None or h0.shape == (batch, d_inner, N)
+    out = np.empty((batch, d_inner, L), np.float64)
+    hT = np.empty((batch, d_inner, N), np.float64)
+    lib = _load()
+    args = [batch, d_inner, N, L] + [_ptr(x) for x in (u, delta, A, B, C, D, z, bias, h0, out, hT)]
+    ranges = _row_ranges(batch * d_inner, threads or default_threads())
+    if len(ranges) == 1:
+        lib.oracle_scan(*args, *ranges[0])
+    else:
+        with ThreadPoolExecutor(len(ranges)) as ex:
+            list(ex.map(lambda rg: lib.oracle_scan(*args, *rg), ranges))
+    return out, hT
+
+
+def step(state, x, delta, A, B, C, D=None, z=None, bias=None, threads: int | None = None):
+    """Recurrent-mode single token for every (batch, channel) row.
+
+    state: [batch, d_inner, N] (not modified; the new state is returned);
+    x, delta, z: [batch, d_inner]; B, C: [batch, N]; A: [d_inner, N].
+    Returns (out [batch, d_inner], new_state [batch, d_inner, N]).
+    """
+    st = _f64(state).copy()
+    x, delta, A, B, C = (_f64(v) for v in (x, delta, A, B, C))
+    D, z, bias = (_f64(v) for v in (D, z, bias))
+    batch, d_inner, N = st.shape
+    assert x.shape == (batch, d_inner) and delta.shape == (batch, d_inner)
+    assert A.shape == (d_inner, N) and B.shape == (batch, N) and C.shape == (batch, N)
+    out = np.empty((batch, d_inner), np.float64)
+    lib = _load()
+    args = [batch, d_inner, N] + [_ptr(v) for v in (st, x, delta, A, B, C, D, z, bias, out)]
+    ranges = _row_ranges(batch * d_inner, threads or 1)
+    if len(ranges) == 1:
+        lib.oracle_step(*args, *ranges[0])
+    else:
+        with ThreadPoolExecutor(len(ranges)) as ex:
+            list(ex.map(lambda rg: lib.oracle_step(*args, *rg), ranges))
+    return out, st
