@@ -1,0 +1,502 @@
+#!/usr/bin/env python3
+"""Benchmark of the B300 selective scan.
+
+One step = one ssm_scan_fwd call over the 1M-token workload (batch 1,
+d_inner 2048, d_state 16, L = 1,048,576; bf16 u/Δraw/z/B/C/out, fp32 state):
+softplus, ZOH discretisation, recurrence, readout, D skip and SiLU gate, fused.
+Prints one JSON line.  Also reported in the same line: the decode step
+(ssm_step, batch 256 × d_inner 5120 × 16 states, 1000 steps), the end-to-end
+throughput through the C ABI with inputs copied from pinned host memory and
+the output read back, and the CPU oracle timed on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 run under torchrun (one process per GPU); each rank scans its own
+workload-sized problem (independent rows, no collective): weak scaling.
+``--impl reference`` times the CPU oracle (the slow plain definition) on the
+host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "scan GB/s & channel·tokens/s (fraction of HBM roofline); ssm_step tokens/s"
+WORKLOAD = "long_1m"
+HBM_PEAK_FALLBACK = 6400.0
+FP32_LANES_PER_SM = 128
+# FP32 lane operations of one state update (b, c, t, n) on the minimal path:
+# Δ·A, Ā-1, x·(1/A), (x/A)·B + h, (Ā-1)·s + h, C·h accumulate (the exp is on the MUFU pipe).
+FP32_OPS_PER_UPDATE = 6
+# ncu DRAM bytes (read + write) per launch of the scan kernel on this workload;
+# None until a capture of the current kernel is recorded (see profiles/).
+SCAN_DRAM_BYTES_PER_LAUNCH = None
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+def scan_alg_bytes(shape: W.ScanShape) -> int:
+    """Bytes the scan must move: u, Δraw, z read and out written once per
+    (batch, channel, token); B and C once per (batch, token); final state,
+    A, D and bias once."""
+    e = 2 if shape.dtype == torch.bfloat16 else 4
+    ct = shape.batch * shape.d_inner * shape.seqlen
+    return (4 * ct * e + 2 * shape.batch * shape.seqlen * shape.d_state * e
+            + 4 * shape.batch * shape.d_inner * shape.d_state
+            + 4 * shape.d_inner * shape.d_state + 8 * shape.d_inner)
+
+
+def step_alg_bytes(shape: W.DecodeShape) -> int:
+    e = 2 if shape.dtype == torch.bfloat16 else 4
+    rows = shape.batch * shape.d_inner
+    return (8 * rows * shape.d_state + 4 * rows * e + 2 * shape.batch * shape.d_state * e
+            + 4 * shape.d_inner * shape.d_state + 8 * shape.d_inner)
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        rank = int(os.environ["RANK"])
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return rank, world, local
+    return 0, 1, 0
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank scans its own workload-sized problem drawn from its own seed."""
+    return rank
+
+
+def aggregate_throughput(units_per_rank_per_step: int, world: int, steps: int, max_secs: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_rank_per_step * steps / max_secs
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    mhz.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "samples": len(mhz), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- timing helpers
+def flush_l2(buf):
+    buf.zero_()
+
+
+def time_steps(fn, steps, warmup, world, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / 1e3  # seconds
+
+
+# ---------------------------------------------------------------- our arm
+def bench_scan(args, rank, world, dev):
+    import selective_state_space_154_b300 as ssm
+    shape = W.SCAN_SHAPES[WORKLOAD]
+    inp = W.scan_inputs(shape, device=dev, seed=rank_seed(rank))
+    out = torch.empty_like(inp["u"])
+    fs = torch.empty((shape.batch, shape.d_inner, shape.d_state), dtype=torch.float32, device=dev)
+    ws_bytes = ssm.ssm_scan_workspace_bytes(shape.batch, shape.d_inner, shape.d_state, shape.seqlen, shape.dtype)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                         inp["bias"], out, fs, workspace=ws, stream=stream)
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        secs = time_steps(step, args.steps, args.warmup, world, stream)
+    status = ssm.ssm_scan_check(ws)
+    if status != ssm.SSM_OK:
+        raise RuntimeError(f"scan reported {ssm.ssm_status_string(status)}")
+    return shape, inp, out, secs, clk.summary()
+
+
+def bench_e2e(args, shape, inp, out, dev, world):
+    """Same workload through the public API, with the inputs copied from pinned
+    host memory and the output read back inside the timed region."""
+    import selective_state_space_154_b300 as ssm
+    names = ["u", "delta", "z", "B", "C"]
+    host = {k: torch.empty(inp[k].shape, dtype=inp[k].dtype, pin_memory=True) for k in names}
+    for k in names:
+        host[k].copy_(inp[k])
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    ws = torch.empty(max(16, ssm.ssm_scan_workspace_bytes(shape.batch, shape.d_inner, shape.d_state,
+                                                          shape.seqlen, shape.dtype)), dtype=torch.uint8,
+                     device=dev)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    d2h = out_host.numel() * out_host.element_size()
+    stream = torch.cuda.current_stream(dev)
+    steps = max(1, min(args.steps, 5))
+
+    def one():
+        for k in names:
+            inp[k].copy_(host[k], non_blocking=True)
+        ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                         inp["bias"], out, None, workspace=ws, stream=stream)
+        out_host.copy_(out, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    secs = time.perf_counter() - t0
+    secs = max_over_ranks(secs, world, dev)
+    del host, out_host
+    return steps, secs, h2d, d2h
+
+
+def bench_decode(dev):
+    """ssm_step on the decode workload: each timed step starts with L2 flushed
+    (in a model, the other layers evict this layer's state between its steps);
+    also the same 1000 steps back to back in one CUDA graph (state warm in L2)."""
+    import selective_state_space_154_b300 as ssm
+    shape = W.DECODE_SHAPE
+    inp = W.decode_inputs(shape, device=dev, seed=0)
+    state = torch.zeros((shape.batch, shape.d_inner, shape.d_state), dtype=torch.float32, device=dev)
+    out = torch.empty((shape.batch, shape.d_inner), dtype=shape.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def step(s):
+        ssm.ssm_step(state, inp["x"][s], inp["delta"][s], inp["A"], inp["B"][s], inp["C"][s], inp["D"],
+                     inp["z"][s], inp["bias"], out, stream=stream)
+
+    for s in range(5):
+        step(s)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(shape.steps)]
+    for s in range(shape.steps):
+        flush_l2(l2)
+        evs[s][0].record(stream)
+        step(s)
+        evs[s][1].record(stream)
+    torch.cuda.synchronize()
+    cold = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+    # warm: the whole 1000-step decode captured once as a graph
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step(0)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            for s in range(shape.steps):
+                ssm.ssm_step(state, inp["x"][s], inp["delta"][s], inp["A"], inp["B"][s], inp["C"][s], inp["D"],
+                             inp["z"][s], inp["bias"], out, stream=side)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    warm = e0.elapsed_time(e1) / 1e3
+    per_step_bytes = step_alg_bytes(shape)
+    return {
+        "metric": "ssm_step tokens/s", "unit": "tokens/s",
+        "value": shape.batch * shape.steps / cold,
+        "us_per_step": cold / shape.steps * 1e6,
+        "gbs": per_step_bytes * shape.steps / cold / 1e9,
+        "alg_bytes_per_step": per_step_bytes,
+        "l2": "flushed (512 MiB write) before every timed step; steps timed one by one with CUDA events",
+        "warm_l2_graph": {"value": shape.batch * shape.steps / warm, "us_per_step": warm / shape.steps * 1e6,
+                          "gbs": per_step_bytes * shape.steps / warm / 1e9,
+                          "note": "1000 steps replayed back to back as one CUDA graph; the 84 MB state stays in L2"},
+        "config": {"workload": "decode", "batch": shape.batch, "d_inner": shape.d_inner,
+                   "d_state": shape.d_state, "steps": shape.steps, "io": "bf16", "state": "fp32"},
+        "gpu_launches": shape.steps,
+    }
+
+
+# ---------------------------------------------------------------- CPU oracle
+def cpu_threads():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def make_oracle_rows(shape, rows, length, seed=0):
+    """Host float64 inputs of `rows` channels × `length` tokens of the workload
+    (drawn on the GPU when available, else on the CPU, then rounded as the GPU sees them)."""
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    sub = W.ScanShape("sample", 1, rows, shape.d_state, length, shape.dtype)
+    inp = W.scan_inputs(sub, device=dev, seed=seed)
+    f = lambda t: None if t is None else t.detach().to("cpu", torch.float64).numpy()
+    return [f(inp["u"]), f(inp["delta"]), f(inp["A"]), f(inp["B"]), f(inp["C"]), f(inp["D"]), f(inp["z"]),
+            f(inp["bias"])]
+
+
+def _oracle_call(args_list, threads):
+    import oracle
+    u, delta, A, B, C, D, z, bias = args_list
+    t0 = time.perf_counter()
+    oracle.scan(u, delta, A, B, C, D=D, z=z, bias=bias, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(target_s=15.0):
+    """The oracle as it stands, on all host cores, over a bounded sample of the
+    workload: full-length rows are too slow, so the sample is `rows` channels ×
+    `length` tokens sized from a short calibration run to about target_s."""
+    shape = W.SCAN_SHAPES[WORKLOAD]
+    threads = cpu_threads()
+    calib_len = 1 << 16
+    cal = make_oracle_rows(shape, threads, calib_len)
+    _oracle_call(cal, threads)  # warm (thread pool, page faults)
+    dt = _oracle_call(cal, threads)
+    rate = threads * calib_len / max(dt, 1e-6)  # channel·tokens/s
+    length = shape.seqlen if rate * target_s >= threads * shape.seqlen else max(calib_len, int(rate * target_s / threads) // 1024 * 1024)
+    rows = threads * max(1, int(rate * target_s / (threads * length)))
+    sample = make_oracle_rows(shape, rows, length, seed=1)
+    dt = _oracle_call(sample, threads)
+    return {"value": rows * length / dt, "unit": "channel·tokens/s", "cores": threads, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"{rows} channels x {length} tokens of the {WORKLOAD} workload (d_state {shape.d_state}, "
+                      f"bf16-rounded inputs, float64 arithmetic), oracle.scan threaded over channels"}
+
+
+# ---------------------------------------------------------------- arms
+def run_ours(args):
+    rank, world, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the reference arm runs on CPU: --impl reference)")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks = measured_peaks()
+    shape, inp, out, secs, clocks = bench_scan(args, rank, world, dev)
+    secs = max_over_ranks(secs, world, dev)
+    ct = shape.channel_tokens
+    value = aggregate_throughput(ct, world, args.steps, secs)
+    ms = secs / args.steps * 1e3
+    alg = scan_alg_bytes(shape)
+    gbs = alg / (secs / args.steps) / 1e9
+    sm_mhz = clocks.get("sm_mhz") or peaks.get("sm_max_mhz", 2032.0)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = sms * FP32_LANES_PER_SM * sm_mhz * 1e6 / 1e12
+    alu_achieved = FP32_OPS_PER_UPDATE * ct * shape.d_state / (secs / args.steps) / 1e12
+    hbm_peak = peaks.get("hbm_gbs")
+    hbm_note = "of measured" if hbm_peak else "of fallback"
+    hbm_peak = hbm_peak or HBM_PEAK_FALLBACK
+
+    e2e_steps, e2e_secs, h2d, d2h = bench_e2e(args, shape, inp, out, dev, world)
+    del inp, out
+    torch.cuda.empty_cache()
+    decode = bench_decode(dev) if rank == 0 else None
+    cpu = cpu_baseline() if (rank == 0 and world == 1) else None
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "channel·tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD} scan: batch {shape.batch}, d_inner {shape.d_inner}, "
+                                   f"d_state {shape.d_state}, L {shape.seqlen}; bf16 u/delta/z/B/C/out, "
+                                   "fp32 A/D/bias/state, softplus+ZOH+recurrence+readout+D+silu gate fused",
+                       "batch": shape.batch, "d_inner": shape.d_inner, "d_state": shape.d_state,
+                       "seq_len": shape.seqlen, "io_dtype": "bf16",
+                       "parallelism": "one independent problem per GPU, no collective" if world > 1 else "single GPU",
+                       "l2": "inputs 17.2 GB > 126 MB L2 (no flush needed)"},
+            "gbs": gbs,
+            "roofline": {"bound": "alu", "achieved": alu_achieved, "peak": alu_peak, "unit": "FP32 Tops/s",
+                         "frac": alu_achieved / alu_peak, "traffic": SCAN_DRAM_BYTES_PER_LAUNCH,
+                         "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x {sm_mhz:.0f} MHz (median SM clock sampled during the timed region)",
+                         "achieved_basis": f"{FP32_OPS_PER_UPDATE} FP32 ops per state update x {ct * shape.d_state} updates per launch",
+                         "hbm": {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                                 "peak_note": hbm_note, "alg_bytes_per_launch": alg}},
+            "e2e": {"value": world * ct * e2e_steps / e2e_secs, "unit": "channel·tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "note": "public API: pinned host -> device copies of u, delta, z, B, C, ssm_scan_fwd, out -> pinned host; wall clock"},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "decode": decode,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_profile_case(args):
+    """A short run of one kernel for ncu captures (prints timing, not the JSON line)."""
+    import selective_state_space_154_b300 as ssm
+    dev = torch.device("cuda", 0)
+    if args.only == "scan":
+        base = W.SCAN_SHAPES[WORKLOAD]
+        shape = W.ScanShape(base.name, base.batch, base.d_inner, base.d_state, args.seqlen or base.seqlen, base.dtype)
+        inp = W.scan_inputs(shape, device=dev, seed=0)
+        out = torch.empty_like(inp["u"])
+        ws = torch.empty(max(16, ssm.ssm_scan_workspace_bytes(shape.batch, shape.d_inner, shape.d_state,
+                                                              shape.seqlen, shape.dtype)), dtype=torch.uint8, device=dev)
+        fn = lambda: ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                      inp["bias"], out, None, workspace=ws)
+        units = shape.channel_tokens
+    else:
+        shape = W.DECODE_SHAPE
+        inp = W.decode_inputs(shape, device=dev, seed=0, steps=8)
+        state = torch.zeros((shape.batch, shape.d_inner, shape.d_state), device=dev)
+        out = torch.empty((shape.batch, shape.d_inner), dtype=shape.dtype, device=dev)
+        fn = lambda: ssm.ssm_step(state, inp["x"][0], inp["delta"][0], inp["A"], inp["B"][0], inp["C"][0],
+                                  inp["D"], inp["z"][0], inp["bias"], out)
+        units = shape.batch
+    secs = time_steps(fn, args.steps, args.warmup, 1, torch.cuda.current_stream(dev))
+    print(f"{args.only}: {secs / args.steps * 1e3:.4f} ms per call, {units * args.steps / secs:.4e} units/s")
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    shape = W.SCAN_SHAPES[WORKLOAD]
+    threads = cpu_threads()
+    length = 1 << 17
+    rows = threads * 4
+    sample = make_oracle_rows(shape, rows, length, seed=0)
+    for _ in range(args.warmup):
+        _oracle_call(sample, threads)
+    total = 0.0
+    for _ in range(args.steps):
+        total += _oracle_call(sample, threads)
+    value = rows * length * args.steps / total
+    desc = (f"each step: {rows} channels x {length} tokens of the {WORKLOAD} workload "
+            f"(d_state {shape.d_state}), oracle.scan in float64 on {threads} host threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "channel·tokens/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} scan (bounded sample, see cpu_baseline)", "batch": shape.batch,
+                   "d_inner": shape.d_inner, "d_state": shape.d_state, "seq_len": shape.seqlen},
+        "cpu_baseline": {"value": value, "unit": "channel·tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "channel·tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only", choices=["all", "scan", "decode"], default="all",
+                    help="profiling aid: run only the scan or only the decode part (no JSON line)")
+    ap.add_argument("--seqlen", type=int, default=None,
+                    help="profiling aid: scan a shorter sequence of the same workload")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.only != "all":
+        run_profile_case(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

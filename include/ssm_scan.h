@@ -1,0 +1,138 @@
+/*
+ * ssm_scan.h — C ABI of a B300 (sm_103a) selective state-space scan (S6).
+ *
+ * The operation (per batch b, channel c, state n; diagonal A):
+ *
+ *   Δ_t   = softplus(Δraw[b,c,t] + bias[c])
+ *   Ā_t   = exp(Δ_t · A[c,n])                                  zero-order hold
+ *   B̄_t   = (Δ_t A)^-1 (exp(Δ_t A) - 1) Δ_t B[b,t,n]
+ *         = expm1(Δ_t A[c,n]) / A[c,n] · B[b,t,n]   (Δ_t · B[b,t,n] when A[c,n] = 0)
+ *   h_t   = Ā_t h_{t-1} + B̄_t u[b,c,t]                           h_0 = 0
+ *   y_t   = Σ_n C[b,t,n] h_t[n] + D[c] u[b,c,t]
+ *   out   = y_t · silu(z[b,c,t])          silu(z) = z / (1 + exp(-z))
+ *
+ * Sources: "State Space Models（SSM）とMamba" §2.2 離散化 (ZOH formulas, the
+ * discrete recurrence), §2.4 二つのモード (parallel training mode, recurrent
+ * fixed-memory inference mode), §4.2 Selective SSM (Δ, B, C per token, A fixed);
+ * "Mambaとは？Transformer以外の系列モデル", sections 状態空間モデルを一つの式から
+ * 理解する (readout with the D skip term), Mamba blockのarchitecture (SiLU gate
+ * multiplies the SSM branch) and training、prefill、decodeでは計算の姿が違う
+ * (prefill runs the scan over the prompt, decode updates the state once per
+ * token).  softplus(Δraw + bias) is this library's parameterisation of the
+ * positive step size, which the pages leave open.
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    keeps no global state, allocates nothing and never frees caller memory.
+ *  - Layouts are dense row-major:
+ *        u, delta, z, out          [batch][d_inner][seqlen]   (act dtype)
+ *        B, C                      [batch][seqlen][d_state]   (act dtype)
+ *        A                         [d_inner][d_state]         (float32)
+ *        D, delta_bias             [d_inner]                  (float32)
+ *        final_state / state       [batch][d_inner][d_state]  (float32)
+ *    (for ssm_step, seqlen is 1: x, delta, z, out are [batch][d_inner] and
+ *    B, C are [batch][d_state].)
+ *  - act dtype is float32 or bfloat16 (ssm_dims.act); outputs of the act dtype
+ *    are rounded to nearest even.  State and all arithmetic are float32.
+ *  - Work is enqueued on `stream` and runs asynchronously; the call returns
+ *    once the work is queued.  Arguments are validated on the host before any
+ *    launch, and a failed validation queues nothing.
+ *  - Inputs are never written.  out must not overlap any input.
+ *  - NaN / Inf inputs are not checked and propagate.
+ *  - Limits: 1 ≤ d_state ≤ 64; batch, d_inner, seqlen ≥ 1;
+ *    batch·d_inner·seqlen < 2^62.  Pointers must be 16-byte aligned.
+ */
+#ifndef SSM_SCAN_H_
+#define SSM_SCAN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* ssm_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  SSM_OK = 0,
+  SSM_ERR_INVALID_ARG = 1, /* null required pointer, non-positive size, bad dtype */
+  SSM_ERR_UNSUPPORTED = 2, /* d_state > 64, or a size beyond the limits above */
+  SSM_ERR_ALIGNMENT = 3,   /* a pointer not aligned as required (see Conventions) */
+  SSM_ERR_WORKSPACE = 4,   /* workspace missing or smaller than ssm_scan_workspace_bytes() */
+  SSM_ERR_CUDA = 5,        /* a CUDA runtime call or a launch failed */
+  SSM_ERR_TIMEOUT = 6      /* a device-side wait between chunks gave up (see ssm_scan_check) */
+} ssm_status;
+
+typedef enum { SSM_DTYPE_F32 = 0, SSM_DTYPE_BF16 = 1 } ssm_dtype;
+
+typedef struct {
+  int64_t batch;
+  int64_t d_inner;
+  int64_t d_state; /* N */
+  int64_t seqlen;  /* L; ignored by ssm_step */
+  int32_t act;     /* ssm_dtype of u, delta, z, B, C, out */
+  int32_t reserved;
+} ssm_dims;
+
+/*
+ * Bytes of device workspace ssm_scan_fwd needs for `dims` on the current
+ * device (0 means none is needed and workspace may be NULL).  Long sequences
+ * with few (batch, channel) rows are split into chunks along the sequence;
+ * the workspace then carries each chunk's state summary to the next chunk.
+ * Returns 0 for invalid dims as well (ssm_scan_fwd reports those).
+ */
+SSM_API size_t ssm_scan_workspace_bytes(const ssm_dims* dims);
+
+/*
+ * Parallel (training / prefill) mode over the whole sequence, initial state 0.
+ *   u, delta (= Δraw), A, B, C, out, dims: required.
+ *   D, z, delta_bias: may be NULL (no skip term / no gate / zero bias).
+ *   final_state: may be NULL; otherwise receives h_L.
+ *   workspace: device memory of at least ssm_scan_workspace_bytes(dims) bytes,
+ *     caller-owned, contents on entry irrelevant, not shared with a concurrent
+ *     call.  It also holds a device error word read by ssm_scan_check.
+ * Returns SSM_OK when the work was queued.
+ */
+SSM_API ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                        const void* C, const float* D, const void* z, const float* delta_bias,
+                        void* out, float* final_state, const ssm_dims* dims, void* workspace,
+                        size_t workspace_bytes, ssm_stream_t stream);
+
+/*
+ * Recurrent (decode) mode: one token for every (batch, channel) row, updating
+ * `state` in place (h ← Ā h + B̄ x) and writing out = (C·h + D x) · silu(z).
+ *   state, x, delta, A, B, C, out, dims: required (dims->seqlen is ignored).
+ *   D, z, delta_bias: may be NULL.
+ * A and delta_bias are needed to discretise (A enters Ā and B̄; the bias is
+ * part of the step size), so they are arguments of the step as of the scan.
+ */
+SSM_API ssm_status ssm_step(float* state, const void* x, const void* delta, const float* A,
+                    const void* B, const void* C, const float* D, const void* z,
+                    const float* delta_bias, void* out, const ssm_dims* dims,
+                    ssm_stream_t stream);
+
+/*
+ * After the stream that ran ssm_scan_fwd has been synchronised: reads the
+ * device error word in `workspace` (synchronous device-to-host copy of 4
+ * bytes) and returns SSM_ERR_TIMEOUT if a wait between chunks gave up,
+ * SSM_OK otherwise (also when workspace is NULL).  Each ssm_scan_fwd call
+ * clears the word before its kernel runs.
+ */
+SSM_API ssm_status ssm_scan_check(const void* workspace, size_t workspace_bytes);
+
+/* Static, human-readable name of a status. */
+SSM_API const char* ssm_status_string(ssm_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H_ */

@@ -1,0 +1,205 @@
+"""B300-native selective state-space scan (S6): Python binding of the C ABI.
+
+The compute path is entirely in ``_lib/libssm_b300.so`` (CUDA, sm_103a); this
+module only marshals torch tensors into pointers, sizes and the current CUDA
+stream.  The functions named like the C entry points take the same arguments
+(see ``include/ssm_scan.h``) and raise ``SsmError`` on a non-OK status.
+``scan_fwd`` / ``step`` are conveniences that allocate outputs with torch.
+
+There is no fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "SsmError", "ssm_scan_workspace_bytes", "ssm_scan_fwd", "ssm_step", "ssm_scan_check",
+    "ssm_status_string", "scan_fwd", "step", "library_path", "load_library",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_lib", "libssm_b300.so")
+
+SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_ALIGNMENT, SSM_ERR_WORKSPACE, \
+    SSM_ERR_CUDA, SSM_ERR_TIMEOUT = range(7)
+SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
+_DTYPES = {torch.float32: SSM_DTYPE_F32, torch.bfloat16: SSM_DTYPE_BF16}
+
+
+class SsmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {ssm_status_string(status)}")
+
+
+class ssm_dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("d_inner", ctypes.c_int64), ("d_state", ctypes.c_int64),
+                ("seqlen", ctypes.c_int64), ("act", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with `python -m selective_state_space_154_b300.build`")
+            lib = ctypes.CDLL(_LIB_PATH)
+            vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            dp = ctypes.POINTER(ssm_dims)
+            lib.ssm_scan_workspace_bytes.argtypes = [dp]
+            lib.ssm_scan_workspace_bytes.restype = sz
+            lib.ssm_scan_fwd.argtypes = [vp] * 10 + [dp, vp, sz, vp]
+            lib.ssm_scan_fwd.restype = i32
+            lib.ssm_step.argtypes = [vp] * 10 + [dp, vp]
+            lib.ssm_step.restype = i32
+            lib.ssm_scan_check.argtypes = [vp, sz]
+            lib.ssm_scan_check.restype = i32
+            lib.ssm_status_string.argtypes = [i32]
+            lib.ssm_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def ssm_status_string(status: int) -> str:
+    return load_library().ssm_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype, shape, device, required=True):
+    if t is None:
+        if required:
+            raise ValueError(f"{name} is required")
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _dims(batch, d_inner, d_state, seqlen, dtype):
+    if dtype not in _DTYPES:
+        raise TypeError(f"activation dtype must be float32 or bfloat16, got {dtype}")
+    return ssm_dims(int(batch), int(d_inner), int(d_state), int(seqlen), _DTYPES[dtype], 0)
+
+
+def ssm_scan_workspace_bytes(batch, d_inner, d_state, seqlen, dtype=torch.bfloat16) -> int:
+    d = _dims(batch, d_inner, d_state, seqlen, dtype)
+    return int(load_library().ssm_scan_workspace_bytes(ctypes.byref(d)))
+
+
+def ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, out, final_state, workspace=None, stream=None):
+    """Parallel-mode scan into caller-provided ``out`` (and ``final_state``)."""
+    lib = load_library()
+    if not isinstance(u, torch.Tensor) or u.dim() != 3:
+        raise ValueError("u must be a [batch, d_inner, seqlen] tensor")
+    batch, d_inner, L = u.shape
+    if not isinstance(A, torch.Tensor) or A.dim() != 2:
+        raise ValueError("A must be a [d_inner, d_state] tensor")
+    N = A.shape[1]
+    act, dev = u.dtype, u.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    _check(u, "u", act, (batch, d_inner, L), dev)
+    _check(delta, "delta", act, (batch, d_inner, L), dev)
+    _check(A, "A", torch.float32, (d_inner, N), dev)
+    _check(B, "B", act, (batch, L, N), dev)
+    _check(C, "C", act, (batch, L, N), dev)
+    _check(D, "D", torch.float32, (d_inner,), dev, required=False)
+    _check(z, "z", act, (batch, d_inner, L), dev, required=False)
+    _check(delta_bias, "delta_bias", torch.float32, (d_inner,), dev, required=False)
+    _check(out, "out", act, (batch, d_inner, L), dev)
+    _check(final_state, "final_state", torch.float32, (batch, d_inner, N), dev, required=False)
+    dims = _dims(batch, d_inner, N, L, act)
+    with torch.cuda.device(dev):
+        need = int(lib.ssm_scan_workspace_bytes(ctypes.byref(dims)))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = lib.ssm_scan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                              _ptr(delta_bias), _ptr(out), _ptr(final_state), ctypes.byref(dims),
+                              _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
+    if st != SSM_OK:
+        raise SsmError(st, "ssm_scan_fwd")
+    return workspace
+
+
+def ssm_step(state, x, delta, A, B, C, D, z, delta_bias, out, stream=None):
+    """Recurrent-mode single token; ``state`` is updated in place."""
+    lib = load_library()
+    if not isinstance(state, torch.Tensor) or state.dim() != 3:
+        raise ValueError("state must be a [batch, d_inner, d_state] tensor")
+    batch, d_inner, N = state.shape
+    act, dev = x.dtype, state.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    _check(state, "state", torch.float32, (batch, d_inner, N), dev)
+    _check(x, "x", act, (batch, d_inner), dev)
+    _check(delta, "delta", act, (batch, d_inner), dev)
+    _check(A, "A", torch.float32, (d_inner, N), dev)
+    _check(B, "B", act, (batch, N), dev)
+    _check(C, "C", act, (batch, N), dev)
+    _check(D, "D", torch.float32, (d_inner,), dev, required=False)
+    _check(z, "z", act, (batch, d_inner), dev, required=False)
+    _check(delta_bias, "delta_bias", torch.float32, (d_inner,), dev, required=False)
+    _check(out, "out", act, (batch, d_inner), dev)
+    dims = _dims(batch, d_inner, N, 1, act)
+    with torch.cuda.device(dev):
+        st = lib.ssm_step(_ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                          _ptr(delta_bias), _ptr(out), ctypes.byref(dims), _stream_handle(stream, dev))
+    if st != SSM_OK:
+        raise SsmError(st, "ssm_step")
+
+
+def ssm_scan_check(workspace) -> int:
+    """Status of the device error word after the scan's stream was synchronised."""
+    if workspace is None:
+        return SSM_OK
+    return int(load_library().ssm_scan_check(_ptr(workspace), workspace.numel() * workspace.element_size()))
+
+
+def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, return_final_state=False,
+             workspace=None, stream=None):
+    """Allocate ``out`` (and ``final_state``) and run ``ssm_scan_fwd``."""
+    out = torch.empty_like(u)
+    fs = None
+    if return_final_state:
+        fs = torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
+    ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, out, fs, workspace=workspace, stream=stream)
+    return (out, fs) if return_final_state else out
+
+
+def step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, out=None, stream=None):
+    """Run ``ssm_step`` (state updated in place) and return the output."""
+    if out is None:
+        out = torch.empty_like(x)
+    ssm_step(state, x, delta, A, B, C, D, z, delta_bias, out, stream=stream)
+    return out

@@ -1,0 +1,161 @@
+// C ABI of the selective-scan library: argument validation, launch planning,
+// status codes.  Declarations and the meaning of every argument are in
+// include/ssm_scan.h.
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "../../include/ssm_scan.h"
+#include "ssm_internal.h"
+
+namespace ssm {
+
+// Read on every call (a getenv per launch) so that tests can change them per call.
+RuntimeKnobs runtime_knobs() {
+  return [] {
+    RuntimeKnobs r{};
+    r.lookback_timeout_ns = 0;  // 0: 1 s + 100 ns per token of a chunk (set at launch)
+    if (const char* s = std::getenv("SSM_LOOKBACK_TIMEOUT_MS")) {
+      const long long ms = std::atoll(s);
+      if (ms > 0) r.lookback_timeout_ns = ms * 1000ll * 1000;
+    }
+    const char* f = std::getenv("SSM_FAULT");
+    r.fault_lookback = f && std::strcmp(f, "lookback") == 0;
+    if (const char* c = std::getenv("SSM_FORCE_CHUNKS")) r.force_chunks = std::atoi(c);
+    return r;
+  }();
+}
+
+}  // namespace ssm
+
+namespace {
+
+bool aligned(const void* p, unsigned bytes) { return (reinterpret_cast<uintptr_t>(p) & (bytes - 1u)) == 0; }
+bool aligned16(const void* p) { return aligned(p, 16); }
+
+// Common validation of dims; seqlen is checked only for the scan.
+ssm_status check_dims(const ssm_dims* d, bool need_len) {
+  if (!d) return SSM_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->d_inner < 1 || d->d_state < 1) return SSM_ERR_INVALID_ARG;
+  if (need_len && d->seqlen < 1) return SSM_ERR_INVALID_ARG;
+  if (d->act != SSM_DTYPE_F32 && d->act != SSM_DTYPE_BF16) return SSM_ERR_INVALID_ARG;
+  if (d->d_state > 64) return SSM_ERR_UNSUPPORTED;
+  const int64_t lim = int64_t(1) << 62;
+  const int64_t len = need_len ? d->seqlen : 1;
+  if (d->batch > lim / d->d_inner) return SSM_ERR_UNSUPPORTED;
+  const int64_t rows = d->batch * d->d_inner;
+  if (len > lim / rows) return SSM_ERR_UNSUPPORTED;
+  if (rows > lim / d->d_state) return SSM_ERR_UNSUPPORTED;
+  // grid limits: the scan launches nchunks * batch * ctiles CTAs, the step rows * 16 / 256
+  if (rows > (int64_t(1) << 35)) return SSM_ERR_UNSUPPORTED;
+  return SSM_OK;
+}
+
+ssm::ScanArgs scan_args(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* bias, void* out, float* fs,
+                        const ssm_dims* d, void* ws) {
+  ssm::ScanArgs a{};
+  a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.bias = bias;
+  a.out = out; a.final_state = fs;
+  a.batch = d->batch; a.d_inner = d->d_inner; a.N = d->d_state; a.L = d->seqlen;
+  a.act = d->act;
+  a.ws = static_cast<unsigned char*>(ws);
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_scan_workspace_bytes(const ssm_dims* dims) {
+  if (check_dims(dims, true) != SSM_OK) return 0;
+  ssm::ScanArgs a = scan_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                              nullptr, nullptr, dims, nullptr);
+  a.z = reinterpret_cast<const void*>(uintptr_t(16));  // the plan does not depend on z for sizing
+  ssm::ScanPlan plan;
+  if (!ssm::scan_make_plan(a, &plan)) return 0;
+  // the z / no-z variants may differ in occupancy; size for the larger plan
+  ssm::ScanArgs a2 = a;
+  a2.z = nullptr;
+  ssm::ScanPlan plan2;
+  if (!ssm::scan_make_plan(a2, &plan2)) return 0;
+  return plan.ws_bytes > plan2.ws_bytes ? plan.ws_bytes : plan2.ws_bytes;
+}
+
+ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* delta_bias, void* out,
+                        float* final_state, const ssm_dims* dims, void* workspace, size_t workspace_bytes,
+                        ssm_stream_t stream) {
+  const ssm_status ds = check_dims(dims, true);
+  if (ds != SSM_OK) return ds;
+  if (!u || !delta || !A || !B || !C || !out) return SSM_ERR_INVALID_ARG;
+  // element alignment is required; 16-byte alignment only selects the vector path
+  const unsigned esz = dims->act == SSM_DTYPE_BF16 ? 2u : 4u;
+  const void* act_ptrs[] = {u, delta, B, C, z, out};
+  for (const void* p : act_ptrs)
+    if (p && !aligned(p, esz)) return SSM_ERR_ALIGNMENT;
+  const void* f32_ptrs[] = {A, D, delta_bias, final_state};
+  for (const void* p : f32_ptrs)
+    if (p && !aligned(p, 4)) return SSM_ERR_ALIGNMENT;
+  ssm::ScanArgs a = scan_args(u, delta, A, B, C, D, z, delta_bias, out, final_state, dims, workspace);
+  ssm::ScanPlan plan;
+  if (!ssm::scan_make_plan(a, &plan)) return SSM_ERR_UNSUPPORTED;
+  if (plan.ws_bytes > 0) {
+    if (!workspace || workspace_bytes < plan.ws_bytes) return SSM_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return SSM_ERR_ALIGNMENT;
+  }
+  if (plan.ws_bytes == 0 && workspace && workspace_bytes >= sizeof(unsigned) * 2) {
+    // clear the error word so ssm_scan_check on this workspace reports this call
+    if (cudaMemsetAsync(workspace, 0, sizeof(unsigned) * 2, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return SSM_ERR_CUDA;
+  }
+  const cudaError_t e = ssm::scan_launch(a, plan, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_step(float* state, const void* x, const void* delta, const float* A, const void* B,
+                    const void* C, const float* D, const void* z, const float* delta_bias, void* out,
+                    const ssm_dims* dims, ssm_stream_t stream) {
+  const ssm_status ds = check_dims(dims, false);
+  if (ds != SSM_OK) return ds;
+  if (!state || !x || !delta || !A || !B || !C || !out) return SSM_ERR_INVALID_ARG;
+  const unsigned esz = dims->act == SSM_DTYPE_BF16 ? 2u : 4u;
+  const void* act_ptrs[] = {x, delta, B, C, z, out};
+  for (const void* p : act_ptrs)
+    if (p && !aligned(p, esz)) return SSM_ERR_ALIGNMENT;
+  const void* f32_ptrs[] = {D, delta_bias};
+  for (const void* p : f32_ptrs)
+    if (p && !aligned(p, 4)) return SSM_ERR_ALIGNMENT;
+  // state and A are read as float4 rows
+  if (!aligned16(state) || !aligned16(A)) return SSM_ERR_ALIGNMENT;
+  ssm::StepArgs a{};
+  a.state = state; a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
+  a.bias = delta_bias; a.out = out;
+  a.batch = dims->batch; a.d_inner = dims->d_inner; a.N = dims->d_state; a.act = dims->act;
+  const cudaError_t e = ssm::step_launch(a, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_scan_check(const void* workspace, size_t workspace_bytes) {
+  if (!workspace || workspace_bytes < sizeof(unsigned) * 2) return SSM_OK;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, static_cast<const unsigned char*>(workspace) + sizeof(unsigned), sizeof(word),
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  return (word & ssm::kErrTimeout) ? SSM_ERR_TIMEOUT : SSM_OK;
+}
+
+const char* ssm_status_string(ssm_status s) {
+  switch (s) {
+    case SSM_OK: return "SSM_OK";
+    case SSM_ERR_INVALID_ARG: return "SSM_ERR_INVALID_ARG";
+    case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED";
+    case SSM_ERR_ALIGNMENT: return "SSM_ERR_ALIGNMENT";
+    case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE";
+    case SSM_ERR_CUDA: return "SSM_ERR_CUDA";
+    case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT";
+  }
+  return "SSM_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import selective_state_space_154_b300 as ssm
+from selective_state_space_154_b300 import build as ssm_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ssm_build.build()
+    return ssm.load_library()
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"SSM_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for required in ("ssm_scan_fwd", "ssm_step", "ssm_scan_workspace_bytes", "ssm_scan_check",
+                     "ssm_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["SSM_OK", "SSM_ERR_INVALID_ARG", "SSM_ERR_UNSUPPORTED", "SSM_ERR_ALIGNMENT",
+                                 "SSM_ERR_WORKSPACE", "SSM_ERR_CUDA", "SSM_ERR_TIMEOUT"]):
+        assert ssm.ssm_status_string(code) == name
+    assert ssm.ssm_status_string(99) == "SSM_ERR_UNKNOWN"
+
+
+def _dims(batch=2, d_inner=8, d_state=16, seqlen=64, act=ssm.SSM_DTYPE_BF16):
+    return ssm.ssm_dims(batch, d_inner, d_state, seqlen, act, 0)
+
+
+FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced (validation fails first)
+
+
+def _scan(lib, dims, ptrs=None, ws=None, ws_bytes=0):
+    p = dict(u=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, bias=None, out=FAKE, fs=None)
+    p.update(ptrs or {})
+    args = [ctypes.c_void_p(p[k]) if p[k] else None for k in ("u", "delta", "A", "B", "C", "D", "z", "bias", "out", "fs")]
+    return lib.ssm_scan_fwd(*args, ctypes.byref(dims), ws, ws_bytes, None)
+
+
+def _step(lib, dims, ptrs=None):
+    p = dict(state=FAKE, x=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, bias=None, out=FAKE)
+    p.update(ptrs or {})
+    args = [ctypes.c_void_p(p[k]) if p[k] else None for k in ("state", "x", "delta", "A", "B", "C", "D", "z", "bias", "out")]
+    return lib.ssm_step(*args, ctypes.byref(dims), None)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("batch", 0, ssm.SSM_ERR_INVALID_ARG), ("d_inner", -1, ssm.SSM_ERR_INVALID_ARG),
+    ("d_state", 0, ssm.SSM_ERR_INVALID_ARG), ("seqlen", 0, ssm.SSM_ERR_INVALID_ARG),
+    ("act", 7, ssm.SSM_ERR_INVALID_ARG), ("d_state", 65, ssm.SSM_ERR_UNSUPPORTED),
+    ("seqlen", 1 << 61, ssm.SSM_ERR_UNSUPPORTED),
+])
+def test_scan_rejects_bad_dims(lib, field, value, status):
+    d = _dims()
+    setattr(d, field, value)
+    assert _scan(lib, d) == status
+    assert lib.ssm_scan_workspace_bytes(ctypes.byref(d)) == 0
+
+
+def test_scan_rejects_null_dims(lib):
+    args = [ctypes.c_void_p(FAKE)] * 5 + [None] * 3 + [ctypes.c_void_p(FAKE), None]
+    assert lib.ssm_scan_fwd(*args, None, None, 0, None) == ssm.SSM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("missing", ["u", "delta", "A", "B", "C", "out"])
+def test_scan_rejects_null_required_pointer(lib, missing):
+    assert _scan(lib, _dims(), {missing: None}) == ssm.SSM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("which", ["u", "delta", "B", "C", "z", "out"])
+def test_scan_rejects_misaligned_activation_pointer(lib, which):
+    assert _scan(lib, _dims(), {which: FAKE + 1}) == ssm.SSM_ERR_ALIGNMENT          # bf16: 2-byte
+    assert _scan(lib, _dims(act=ssm.SSM_DTYPE_F32), {which: FAKE + 2}) == ssm.SSM_ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("which", ["A", "D", "bias", "fs"])
+def test_scan_rejects_misaligned_fp32_pointer(lib, which):
+    assert _scan(lib, _dims(), {which: FAKE + 2}) == ssm.SSM_ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("missing", ["state", "x", "delta", "A", "B", "C", "out"])
+def test_step_rejects_null_required_pointer(lib, missing):
+    assert _step(lib, _dims(), {missing: None}) == ssm.SSM_ERR_INVALID_ARG
+
+
+def test_step_rejects_bad_dims_and_alignment(lib):
+    d = _dims(d_state=100)
+    assert _step(lib, d) == ssm.SSM_ERR_UNSUPPORTED
+    d = _dims(d_inner=0)
+    assert _step(lib, d) == ssm.SSM_ERR_INVALID_ARG
+    assert _step(lib, _dims(), {"state": FAKE + 4}) == ssm.SSM_ERR_ALIGNMENT   # state: 16-byte
+    assert _step(lib, _dims(), {"A": FAKE + 8}) == ssm.SSM_ERR_ALIGNMENT
+    assert _step(lib, _dims(), {"x": FAKE + 1}) == ssm.SSM_ERR_ALIGNMENT
+
+
+def test_long_sequence_needs_workspace(lib):
+    """A long sequence over few rows is split into chunks, which needs workspace;
+    without it the call is rejected before any launch."""
+    d = _dims(batch=1, d_inner=64, d_state=16, seqlen=1 << 20)
+    need = lib.ssm_scan_workspace_bytes(ctypes.byref(d))
+    assert need > 0
+    assert _scan(lib, d) == ssm.SSM_ERR_WORKSPACE
+    assert _scan(lib, d, ws=ctypes.c_void_p(FAKE), ws_bytes=need - 1) == ssm.SSM_ERR_WORKSPACE
+
+
+def test_short_sequence_needs_no_workspace(lib):
+    d = _dims(batch=64, d_inner=4096, d_state=16, seqlen=256)
+    assert lib.ssm_scan_workspace_bytes(ctypes.byref(d)) == 0
+
+
+def test_check_without_workspace_is_ok(lib):
+    assert lib.ssm_scan_check(None, 0) == ssm.SSM_OK
+
+
+def test_binding_fails_loudly_without_cuda_tensors():
+    import torch
+    u = torch.zeros(1, 1, 8)
+    with pytest.raises(ValueError):
+        ssm.scan_fwd(u, u, torch.zeros(1, 4), torch.zeros(1, 8, 4), torch.zeros(1, 8, 4))

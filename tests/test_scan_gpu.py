@@ -1,0 +1,186 @@
+"""GPU parity of ssm_scan_fwd against the CPU oracle on the same seeded inputs.
+
+Small problems are compared element by element over the whole output; the
+Mamba-shaped workloads at full size are run exactly as the benchmark runs
+them and compared on sampled (batch, channel) rows over the full length.
+Tolerance (see parity.rel_err): 1e-4 for fp32 activations, 2e-2 for bf16
+activations with fp32 state, against the oracle fed the same rounded inputs.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import selective_state_space_154_b300 as ssm
+import workloads as W
+from parity import TOL, oracle_rows, rel_err, spread_rows, to_np
+import oracle
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run_scan(inp, guard=False):
+    u = inp["u"]
+    b, d, L = u.shape
+    N = inp["A"].shape[1]
+    if guard:
+        # out placed inside a larger buffer; the guard bands must stay untouched
+        pad = 4096
+        buf = torch.full((2 * pad + b * d * L,), 7.0, dtype=u.dtype, device=DEV)
+        out = buf[pad:pad + b * d * L].view(b, d, L)
+        fsbuf = torch.full((2 * pad + b * d * N,), 7.0, dtype=torch.float32, device=DEV)
+        fs = fsbuf[pad:pad + b * d * N].view(b, d, N)
+    else:
+        out = torch.empty_like(u)
+        fs = torch.empty((b, d, N), dtype=torch.float32, device=DEV)
+    ws = ssm.ssm_scan_fwd(u, inp["delta"], inp["A"], inp["B"], inp["C"], inp.get("D"), inp.get("z"),
+                          inp.get("bias"), out, fs)
+    torch.cuda.synchronize()
+    assert ssm.ssm_scan_check(ws) == ssm.SSM_OK
+    if guard:
+        assert torch.all(buf[:pad] == 7.0) and torch.all(buf[pad + b * d * L:] == 7.0)
+        assert torch.all(fsbuf[:pad] == 7.0) and torch.all(fsbuf[pad + b * d * N:] == 7.0)
+    return out, fs
+
+
+def full_compare(inp, tol):
+    out, fs = run_scan(inp, guard=True)
+    ref, href = oracle.scan(*(to_np(inp[k]) for k in ("u", "delta", "A", "B", "C")),
+                            D=to_np(inp.get("D")), z=to_np(inp.get("z")), bias=to_np(inp.get("bias")))
+    e_out = rel_err(to_np(out), ref)
+    e_fs = rel_err(to_np(fs), href)
+    assert e_out <= tol, f"out rel err {e_out:.3e} > {tol}"
+    assert e_fs <= tol, f"final_state rel err {e_fs:.3e} > {tol}"
+    return e_out, e_fs
+
+
+def test_tiny_fp32_workload():
+    inp = W.scan_inputs(W.SCAN_SHAPES["tiny_fp32"], device=DEV)
+    full_compare(inp, TOL[torch.float32])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("L", [1, 7, 8, 9, 31, 32, 33, 255, 256, 257, 1000])
+def test_ragged_lengths(dtype, L):
+    inp = W.random_scan_inputs(2, 37, 16, L, dtype=dtype, device=DEV, seed=L, a_kind="random")
+    full_compare(inp, TOL[dtype])
+
+
+@pytest.mark.parametrize("N", [1, 3, 4, 8, 13, 16, 17, 32, 48, 64])
+def test_state_sizes(N):
+    inp = W.random_scan_inputs(2, 40, N, 100, dtype=torch.bfloat16, device=DEV, seed=N, a_kind="random")
+    full_compare(inp, TOL[torch.bfloat16])
+
+
+@pytest.mark.parametrize("opt", ["none", "no_D", "no_z", "no_bias", "all_off"])
+def test_optional_inputs(opt):
+    inp = W.random_scan_inputs(3, 33, 16, 96, dtype=torch.bfloat16, device=DEV, seed=5, a_kind="random",
+                               gate=opt not in ("no_z", "all_off"), skip=opt not in ("no_D", "all_off"),
+                               with_bias=opt not in ("no_bias", "all_off"))
+    full_compare(inp, TOL[torch.bfloat16])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+def test_zero_and_tiny_A(dtype):
+    """A = 0 (running sum through ΔB) and |A| below 2^-60 take the exact-limit path."""
+    inp = W.random_scan_inputs(1, 35, 16, 300, dtype=dtype, device=DEV, seed=3, a_kind="random")
+    A = inp["A"].clone()
+    A[::3, 0] = 0.0
+    A[1::5, 5] = -1e-30
+    A[2::7, :] = 0.0
+    inp["A"] = A
+    full_compare(inp, TOL[dtype])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("chunks", [2, 3, 7])
+def test_chunked_carry(dtype, chunks, monkeypatch):
+    """Force the split along L so the look-back carry and the correction run on
+    a problem the oracle checks in full (ragged last chunk, ragged channels)."""
+    monkeypatch.setenv("SSM_FORCE_CHUNKS", str(chunks))
+    inp = W.random_scan_inputs(2, 45, 16, 32 * 41 + 5, dtype=dtype, device=DEV, seed=chunks,
+                               a_kind="random")
+    full_compare(inp, TOL[dtype])
+
+
+def test_chunked_carry_slow_decay(monkeypatch):
+    """Tiny |A|·Δ keeps the carry alive across whole chunks (correction never stops early)."""
+    monkeypatch.setenv("SSM_FORCE_CHUNKS", "4")
+    inp = W.random_scan_inputs(1, 33, 16, 2048, dtype=torch.float32, device=DEV, seed=8, a_kind="random")
+    inp["A"] = inp["A"] * 1e-3
+    full_compare(inp, TOL[torch.float32])
+
+
+def test_lookback_timeout_is_reported_and_context_survives(monkeypatch):
+    """Test hook: every chunk after the first waits on a flag nothing sets; the
+    bounded wait gives up, the error word reads SSM_ERR_TIMEOUT and the device
+    stays usable."""
+    monkeypatch.setenv("SSM_FORCE_CHUNKS", "2")
+    monkeypatch.setenv("SSM_FAULT", "lookback")
+    monkeypatch.setenv("SSM_LOOKBACK_TIMEOUT_MS", "200")
+    inp = W.random_scan_inputs(1, 32, 16, 512, dtype=torch.bfloat16, device=DEV, seed=1)
+    out = torch.empty_like(inp["u"])
+    ws = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                          inp["bias"], out, None)
+    torch.cuda.synchronize()
+    assert ssm.ssm_scan_check(ws) == ssm.SSM_ERR_TIMEOUT
+    monkeypatch.delenv("SSM_FAULT")
+    full_compare(inp, TOL[torch.bfloat16])  # same workspace layout, clean run
+
+
+def _workload_rows(name, k, seed=0):
+    shape = W.SCAN_SHAPES[name]
+    inp = W.scan_inputs(shape, device=DEV, seed=seed)
+    out, fs = run_scan(inp)
+    rows = spread_rows(shape.batch, shape.d_inner, k, seed)
+    ref, href = oracle_rows(inp, rows)
+    idx_b = torch.tensor([b for b, _ in rows], device=DEV)
+    idx_c = torch.tensor([c for _, c in rows], device=DEV)
+    got = to_np(out[idx_b, idx_c])
+    got_h = to_np(fs[idx_b, idx_c])
+    tol = TOL[shape.dtype]
+    e, eh = rel_err(got, ref), rel_err(got_h, href)
+    assert e <= tol, f"{name}: out rel err {e:.3e}"
+    assert eh <= tol, f"{name}: final_state rel err {eh:.3e}"
+    assert torch.isfinite(out.float()).all()
+    return e, eh
+
+
+def test_mamba130m_layer_sampled():
+    _workload_rows("mamba130m_layer", 48)
+
+
+def test_mamba2p8b_layer_sampled():
+    _workload_rows("mamba2p8b_layer", 32)
+
+
+def test_long_1m_sampled():
+    """The 1M-token workload runs chunked with the carry between chunks."""
+    _workload_rows("long_1m", 12)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+def test_unaligned_views(dtype):
+    """Element-aligned but not 16-byte aligned tensors take the element-copy path."""
+    b, d, N, L = 2, 35, 16, 200
+    src = W.random_scan_inputs(b, d, N, L, dtype=dtype, device=DEV, seed=21, a_kind="random")
+    inp = dict(src)
+    for k in ("u", "delta", "z", "B", "C"):
+        t = src[k]
+        buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=DEV)
+        v = buf[1:].view(t.shape)
+        v.copy_(t)
+        inp[k] = v
+    assert inp["u"].data_ptr() % 16 != 0
+    full_compare(inp, TOL[dtype])
+
+
+def test_repeat_calls_are_identical():
+    """Same inputs, same launch configuration → bitwise identical outputs, also
+    when the sequence is split into chunks (the carry is chained in chunk order)."""
+    inp = W.random_scan_inputs(1, 64, 16, 1 << 16, dtype=torch.bfloat16, device=DEV, seed=2)
+    o1, f1 = run_scan(inp)
+    o2, f2 = run_scan(inp)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
