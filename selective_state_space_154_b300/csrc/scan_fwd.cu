@@ -508,9 +508,74 @@ int occupancy_t(const ScanPlan& plan) {
 
 }  // namespace
 
+namespace {
+
+int device_sms() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+    return v;
+  return 148;
+}
+
+// Chunks along L: enough (rows x chunks) work items to fill the resident slots,
+// each chunk at least min_chunk tokens (the carry correction is paid per chunk).
+int64_t pick_chunks(int64_t items, int64_t slots, int64_t L, int64_t min_chunk, int64_t granule, int force) {
+  int64_t nch = 1;
+  if (items < slots) nch = std::min<int64_t>(slots / items, L / min_chunk);
+  if (force > 0) nch = force;
+  nch = std::max<int64_t>(1, std::min<int64_t>(nch, (L + granule - 1) / granule));
+  return nch;
+}
+
+void finish_chunks(ScanPlan& pl, int64_t L, int64_t nch, int64_t granule, int64_t items, size_t state_bytes_per_item) {
+  int64_t clen = (L + nch - 1) / nch;
+  clen = (clen + granule - 1) / granule * granule;
+  nch = (L + clen - 1) / clen;
+  pl.chunk_len = clen;
+  pl.nchunks = (int)nch;
+  if (nch > 1) {
+    pl.ws_flags_off = kWsHeaderBytes;
+    const size_t flags_bytes = align16((size_t)nch * items * 4);
+    pl.ws_agg_off = pl.ws_flags_off + ((flags_bytes + 255) & ~size_t(255));
+    pl.ws_bytes = pl.ws_agg_off + (size_t)nch * items * state_bytes_per_item;
+  } else {
+    pl.ws_flags_off = pl.ws_agg_off = pl.ws_bytes = 0;
+  }
+}
+
+}  // namespace
+
 bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
   if (a.N < 1 || a.N > 64) return false;
+  const RuntimeKnobs knobs = runtime_knobs();
+  const int sms = device_sms();
   ScanPlan pl{};
+  // The row kernel (one thread per row) does the least work per state update
+  // but needs many rows or a long sequence to fill the GPU; the tile kernel
+  // splits a row's states over 4 threads and suits short sequences.
+  const int64_t rows = a.batch * a.d_inner;
+  int kind = kScanTiles;
+  if (a.N <= 16) {
+    const int occ_r = knobs.ctas_per_sm > 0 ? knobs.ctas_per_sm : rows_resident_ctas(a.act, a.z != nullptr);
+    const int64_t row_slots = (int64_t)sms * occ_r * kRowsPerRowCta;
+    if (rows >= row_slots || a.L >= 65536) kind = kScanRows;
+  }
+  if (knobs.force_kind >= 0 && !(knobs.force_kind == kScanRows && a.N > 16)) kind = knobs.force_kind;
+  pl.kind = kind;
+  if (kind == kScanRows) {
+    pl.npad = 16;
+    pl.groups = 1;
+    pl.threads = kRowsPerRowCta;
+    pl.ctiles = (int)((a.d_inner + kRowsPerRowCta - 1) / kRowsPerRowCta);
+    pl.smem_bytes = 0;
+    const int occ = knobs.ctas_per_sm > 0 ? knobs.ctas_per_sm : rows_resident_ctas(a.act, a.z != nullptr);
+    const int64_t items = a.batch * pl.ctiles;
+    const int64_t nch = pick_chunks(items, (int64_t)sms * occ, a.L, 8192, kRowTokensPerStage, knobs.force_chunks);
+    finish_chunks(pl, a.L, nch, kRowTokensPerStage, items, (size_t)kRowsPerRowCta * 16 * 4);
+    *plan = pl;
+    return true;
+  }
   pl.npad = (int)((a.N + 15) / 16) * 16;
   pl.groups = pl.npad / G;
   pl.threads = RT * pl.groups;
@@ -518,11 +583,6 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
   const int esize = a.act == 1 ? 2 : 4;
   const Layout lay = make_layout(esize, (int)a.N, pl.npad, pl.groups);
   pl.smem_bytes = lay.total;
-
-  int dev = 0, sms = 148, v = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess &&
-      cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-    sms = v;
   // resident CTAs per SM for this kernel variant (cached; host-only query, no launch)
   int& occ = g_occupancy_cache[a.act == 1][pl.npad / 16 - 1][a.z != nullptr];
   if (occ == 0) {
@@ -531,34 +591,15 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
     else
       occ = a.z ? occupancy_t<float, true>(pl) : occupancy_t<float, false>(pl);
   }
-  const int64_t slots = (int64_t)sms * occ;
   const int64_t items = a.batch * pl.ctiles;
-  // Split L into chunks only when the rows alone cannot fill the resident slots
-  // and the chunks stay long (the carry correction is paid at each chunk start).
-  const int64_t min_chunk = 8192;
-  int64_t nch = 1;
-  if (items < slots) nch = std::min<int64_t>(slots / items, a.L / min_chunk);
-  const RuntimeKnobs knobs = runtime_knobs();
-  if (knobs.force_chunks > 0) nch = knobs.force_chunks;
-  nch = std::max<int64_t>(1, std::min<int64_t>(nch, (a.L + TT - 1) / TT));
-  int64_t clen = (a.L + nch - 1) / nch;
-  clen = (clen + TT - 1) / TT * TT;
-  nch = (a.L + clen - 1) / clen;
-  pl.chunk_len = clen;
-  pl.nchunks = (int)nch;
-  if (nch > 1) {
-    pl.ws_flags_off = kWsHeaderBytes;
-    const size_t flags_bytes = align16((size_t)nch * items * 4);
-    pl.ws_agg_off = pl.ws_flags_off + ((flags_bytes + 255) & ~size_t(255));
-    pl.ws_bytes = pl.ws_agg_off + (size_t)nch * items * RT * pl.npad * 4;
-  } else {
-    pl.ws_flags_off = pl.ws_agg_off = pl.ws_bytes = 0;
-  }
+  const int64_t nch = pick_chunks(items, (int64_t)sms * occ, a.L, 8192, TT, knobs.force_chunks);
+  finish_chunks(pl, a.L, nch, TT, items, (size_t)RT * pl.npad * 4);
   *plan = pl;
   return true;
 }
 
 cudaError_t scan_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream) {
+  if (plan.kind == kScanRows) return scan_rows_launch(a, plan, stream);
   KParams p{};
   p.a = a;
   p.npad = plan.npad;

@@ -5,7 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 
-#include "../../include/ssm_scan.h"
+#include "ssm_scan.h"
 #include "ssm_internal.h"
 
 namespace ssm {
@@ -22,6 +22,12 @@ RuntimeKnobs runtime_knobs() {
     const char* f = std::getenv("SSM_FAULT");
     r.fault_lookback = f && std::strcmp(f, "lookback") == 0;
     if (const char* c = std::getenv("SSM_FORCE_CHUNKS")) r.force_chunks = std::atoi(c);
+    r.force_kind = -1;
+    if (const char* k = std::getenv("SSM_FORCE_KERNEL")) {
+      if (std::strcmp(k, "tiles") == 0) r.force_kind = kScanTiles;
+      if (std::strcmp(k, "rows") == 0) r.force_kind = kScanRows;
+    }
+    if (const char* c = std::getenv("SSM_CTAS_PER_SM")) r.ctas_per_sm = std::atoi(c);
     return r;
   }();
 }

@@ -10,7 +10,11 @@ namespace ssm {
 // Rows of a scan CTA (channels of one batch) and tokens of one staged tile.
 constexpr int kRowsPerCta = 32;
 constexpr int kTileTokens = 32;
-constexpr int kStatesPerThread = 4;  // G: states of one row held by one thread
+constexpr int kStatesPerThread = 4;  // G: states of one row held by one thread (tile kernel)
+constexpr int kRowsPerRowCta = 128;     // row kernel: rows per CTA (one thread per row, d_state <= 16)
+constexpr int kRowTokensPerStage = 32;  // row kernel: tokens per stage
+
+enum ScanKind { kScanTiles = 0, kScanRows = 1 };
 
 // Workspace header (bytes): [0] ticket counter, [1] error word.
 constexpr size_t kWsHeaderBytes = 256;
@@ -20,10 +24,11 @@ constexpr unsigned kErrTimeout = 1u;
 
 // Launch plan of one scan call, a pure function of the dims and the device.
 struct ScanPlan {
+  int kind;           // ScanKind
   int npad;           // states per row rounded up to a multiple of 16 (16, 32, 48 or 64)
   int groups;         // npad / kStatesPerThread: threads per row
   int threads;        // kRowsPerCta * groups
-  int ctiles;         // channel tiles per batch
+  int ctiles;         // channel tiles per batch (32 channels for kScanTiles, 128 for kScanRows)
   int64_t chunk_len;  // tokens per chunk (multiple of kTileTokens unless one chunk)
   int nchunks;        // chunks along the sequence (1: no carry between chunks)
   size_t smem_bytes;  // dynamic shared memory per CTA
@@ -51,11 +56,15 @@ struct RuntimeKnobs {
   long long lookback_timeout_ns;  // device-side wait limit between chunks (0: default)
   bool fault_lookback;            // test hook: chunk waits on a flag nothing sets
   int force_chunks;               // >0: override the chunk count (tests)
+  int force_kind;                 // -1: choose by shape; else a ScanKind (tests)
+  int ctas_per_sm;                // >0: resident CTAs per SM assumed when splitting into chunks
 };
 RuntimeKnobs runtime_knobs();
 
 bool scan_make_plan(const ScanArgs& a, ScanPlan* plan);  // false: unsupported dims
 cudaError_t scan_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream);
+int rows_resident_ctas(int act, bool has_z);
+cudaError_t scan_rows_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream);
 
 struct StepArgs {
   float* state;

@@ -21,6 +21,14 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
+@pytest.fixture(params=["tiles", "rows"])
+def kernel(request, monkeypatch):
+    """Run the test through each scan kernel (the row kernel serves d_state <= 16;
+    larger d_state falls back to the tile kernel)."""
+    monkeypatch.setenv("SSM_FORCE_KERNEL", request.param)
+    return request.param
+
+
 def run_scan(inp, guard=False):
     u = inp["u"]
     b, d, L = u.shape
@@ -56,26 +64,26 @@ def full_compare(inp, tol):
     return e_out, e_fs
 
 
-def test_tiny_fp32_workload():
+def test_tiny_fp32_workload(kernel):
     inp = W.scan_inputs(W.SCAN_SHAPES["tiny_fp32"], device=DEV)
     full_compare(inp, TOL[torch.float32])
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
 @pytest.mark.parametrize("L", [1, 7, 8, 9, 31, 32, 33, 255, 256, 257, 1000])
-def test_ragged_lengths(dtype, L):
+def test_ragged_lengths(dtype, L, kernel):
     inp = W.random_scan_inputs(2, 37, 16, L, dtype=dtype, device=DEV, seed=L, a_kind="random")
     full_compare(inp, TOL[dtype])
 
 
 @pytest.mark.parametrize("N", [1, 3, 4, 8, 13, 16, 17, 32, 48, 64])
-def test_state_sizes(N):
+def test_state_sizes(N, kernel):
     inp = W.random_scan_inputs(2, 40, N, 100, dtype=torch.bfloat16, device=DEV, seed=N, a_kind="random")
     full_compare(inp, TOL[torch.bfloat16])
 
 
 @pytest.mark.parametrize("opt", ["none", "no_D", "no_z", "no_bias", "all_off"])
-def test_optional_inputs(opt):
+def test_optional_inputs(opt, kernel):
     inp = W.random_scan_inputs(3, 33, 16, 96, dtype=torch.bfloat16, device=DEV, seed=5, a_kind="random",
                                gate=opt not in ("no_z", "all_off"), skip=opt not in ("no_D", "all_off"),
                                with_bias=opt not in ("no_bias", "all_off"))
@@ -83,7 +91,7 @@ def test_optional_inputs(opt):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
-def test_zero_and_tiny_A(dtype):
+def test_zero_and_tiny_A(dtype, kernel):
     """A = 0 (running sum through ΔB) and |A| below 2^-60 take the exact-limit path."""
     inp = W.random_scan_inputs(1, 35, 16, 300, dtype=dtype, device=DEV, seed=3, a_kind="random")
     A = inp["A"].clone()
@@ -96,16 +104,16 @@ def test_zero_and_tiny_A(dtype):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
 @pytest.mark.parametrize("chunks", [2, 3, 7])
-def test_chunked_carry(dtype, chunks, monkeypatch):
+def test_chunked_carry(dtype, chunks, kernel, monkeypatch):
     """Force the split along L so the look-back carry and the correction run on
     a problem the oracle checks in full (ragged last chunk, ragged channels)."""
     monkeypatch.setenv("SSM_FORCE_CHUNKS", str(chunks))
-    inp = W.random_scan_inputs(2, 45, 16, 32 * 41 + 5, dtype=dtype, device=DEV, seed=chunks,
+    inp = W.random_scan_inputs(2, 45, 16, 64 * 23 + 5, dtype=dtype, device=DEV, seed=chunks,
                                a_kind="random")
     full_compare(inp, TOL[dtype])
 
 
-def test_chunked_carry_slow_decay(monkeypatch):
+def test_chunked_carry_slow_decay(kernel, monkeypatch):
     """Tiny |A|·Δ keeps the carry alive across whole chunks (correction never stops early)."""
     monkeypatch.setenv("SSM_FORCE_CHUNKS", "4")
     inp = W.random_scan_inputs(1, 33, 16, 2048, dtype=torch.float32, device=DEV, seed=8, a_kind="random")
@@ -113,14 +121,14 @@ def test_chunked_carry_slow_decay(monkeypatch):
     full_compare(inp, TOL[torch.float32])
 
 
-def test_lookback_timeout_is_reported_and_context_survives(monkeypatch):
+def test_lookback_timeout_is_reported_and_context_survives(kernel, monkeypatch):
     """Test hook: every chunk after the first waits on a flag nothing sets; the
     bounded wait gives up, the error word reads SSM_ERR_TIMEOUT and the device
     stays usable."""
     monkeypatch.setenv("SSM_FORCE_CHUNKS", "2")
     monkeypatch.setenv("SSM_FAULT", "lookback")
     monkeypatch.setenv("SSM_LOOKBACK_TIMEOUT_MS", "200")
-    inp = W.random_scan_inputs(1, 32, 16, 512, dtype=torch.bfloat16, device=DEV, seed=1)
+    inp = W.random_scan_inputs(1, 32, 16, 1024, dtype=torch.bfloat16, device=DEV, seed=1)
     out = torch.empty_like(inp["u"])
     ws = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
                           inp["bias"], out, None)
@@ -161,8 +169,16 @@ def test_long_1m_sampled():
     _workload_rows("long_1m", 12)
 
 
+@pytest.mark.parametrize("name", ["mamba130m_layer", "long_1m"])
+def test_workload_through_other_kernel(name, monkeypatch):
+    """The kernel not chosen by the planner for a workload gives the same result."""
+    other = "rows" if name == "mamba130m_layer" else "tiles"
+    monkeypatch.setenv("SSM_FORCE_KERNEL", other)
+    _workload_rows(name, 8, seed=3)
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
-def test_unaligned_views(dtype):
+def test_unaligned_views(dtype, kernel):
     """Element-aligned but not 16-byte aligned tensors take the element-copy path."""
     b, d, N, L = 2, 35, 16, 200
     src = W.random_scan_inputs(b, d, N, L, dtype=dtype, device=DEV, seed=21, a_kind="random")
@@ -177,7 +193,7 @@ def test_unaligned_views(dtype):
     full_compare(inp, TOL[dtype])
 
 
-def test_repeat_calls_are_identical():
+def test_repeat_calls_are_identical(kernel):
     """Same inputs, same launch configuration → bitwise identical outputs, also
     when the sequence is split into chunks (the carry is chained in chunk order)."""
     inp = W.random_scan_inputs(1, 64, 16, 1 << 16, dtype=torch.bfloat16, device=DEV, seed=2)
