@@ -131,6 +131,35 @@ SSM_API ssm_status ssm_scan_check(const void* workspace, size_t workspace_bytes)
 /* Static, human-readable name of a status. */
 SSM_API const char* ssm_status_string(ssm_status s);
 
+/*
+ * ssm_scan_fwd for callers that cannot allocate device memory: a plug-in whose
+ * host framework owns every allocation, a serving loop that may not call
+ * cudaMalloc after start-up, or any caller with a fixed device-memory budget.
+ * (This entry point has no counterpart in the pages; it is a property of the
+ * library, not of the method.)
+ *
+ * Same arguments and results as ssm_scan_fwd without the workspace.  The scratch
+ * that long sequences need (the carry between chunks) comes from one static
+ * device array of SSM_NOALLOC_SCRATCH_BYTES inside this library, which exists
+ * on every device that loads the library until the process exits.  The call
+ * allocates nothing and frees nothing.
+ *  - Returns SSM_ERR_WORKSPACE when ssm_scan_workspace_bytes(dims) exceeds
+ *    SSM_NOALLOC_SCRATCH_BYTES; use ssm_scan_fwd with your own workspace then.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture.
+ *  - All calls share the one array, and each call resets what must start at
+ *    zero.  Calls whose work overlaps on the GPU (concurrent streams, or other
+ *    threads) race on the array: serialise them.
+ *  - A wait between chunks that gives up sets its error bit in the shared
+ *    array, where ssm_scan_check cannot see it; callers who need that report
+ *    use ssm_scan_fwd.
+ */
+#define SSM_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+SSM_API ssm_status ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* A, const void* B,
+                                const void* C, const float* D, const void* z, const float* delta_bias,
+                                void* out, float* final_state, const ssm_dims* dims, ssm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,7 +18,8 @@ import torch
 
 __all__ = [
     "SsmError", "ssm_scan_workspace_bytes", "ssm_scan_fwd", "ssm_step", "ssm_scan_check",
-    "ssm_status_string", "scan_fwd", "step", "library_path", "load_library",
+    "ssm_status_string", "scan_fwd", "step", "library_path", "load_library", "ssm_scan_fwd_noalloc",
+    "SSM_NOALLOC_SCRATCH_BYTES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -27,6 +28,7 @@ _LIB_PATH = os.path.join(_PKG, "_lib", "libssm_b300.so")
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_ALIGNMENT, SSM_ERR_WORKSPACE, \
     SSM_ERR_CUDA, SSM_ERR_TIMEOUT = range(7)
 SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
+SSM_NOALLOC_SCRATCH_BYTES = 8 << 20  # size of the library's static scratch (include/ssm_scan.h)
 _DTYPES = {torch.float32: SSM_DTYPE_F32, torch.bfloat16: SSM_DTYPE_BF16}
 
 
@@ -68,6 +70,8 @@ def load_library():
             lib.ssm_step.restype = i32
             lib.ssm_scan_check.argtypes = [vp, sz]
             lib.ssm_scan_check.restype = i32
+            lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 10 + [dp, vp]
+            lib.ssm_scan_fwd_noalloc.restype = i32
             lib.ssm_status_string.argtypes = [i32]
             lib.ssm_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -150,6 +154,34 @@ def ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, out, final_state, workspac
     if st != SSM_OK:
         raise SsmError(st, "ssm_scan_fwd")
     return workspace
+
+
+def ssm_scan_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, out, final_state, stream=None):
+    """ssm_scan_fwd using the library's static device scratch instead of a workspace
+    (for callers that cannot allocate device memory; see include/ssm_scan.h)."""
+    lib = load_library()
+    batch, d_inner, L = u.shape
+    N = A.shape[1]
+    act, dev = u.dtype, u.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    _check(u, "u", act, (batch, d_inner, L), dev)
+    _check(delta, "delta", act, (batch, d_inner, L), dev)
+    _check(A, "A", torch.float32, (d_inner, N), dev)
+    _check(B, "B", act, (batch, L, N), dev)
+    _check(C, "C", act, (batch, L, N), dev)
+    _check(D, "D", torch.float32, (d_inner,), dev, required=False)
+    _check(z, "z", act, (batch, d_inner, L), dev, required=False)
+    _check(delta_bias, "delta_bias", torch.float32, (d_inner,), dev, required=False)
+    _check(out, "out", act, (batch, d_inner, L), dev)
+    _check(final_state, "final_state", torch.float32, (batch, d_inner, N), dev, required=False)
+    dims = _dims(batch, d_inner, N, L, act)
+    with torch.cuda.device(dev):
+        st = lib.ssm_scan_fwd_noalloc(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                      _ptr(delta_bias), _ptr(out), _ptr(final_state), ctypes.byref(dims),
+                                      _stream_handle(stream, dev))
+    if st != SSM_OK:
+        raise SsmError(st, "ssm_scan_fwd_noalloc")
 
 
 def ssm_step(state, x, delta, A, B, C, D, z, delta_bias, out, stream=None):
