@@ -426,7 +426,8 @@ def run_profile_case(args):
     dev = torch.device("cuda", 0)
     if args.only == "scan":
         base = W.SCAN_SHAPES[WORKLOAD]
-        shape = W.ScanShape(base.name, base.batch, base.d_inner, base.d_state, args.seqlen or base.seqlen, base.dtype)
+        shape = W.ScanShape(base.name, base.batch, args.dinner or base.d_inner, base.d_state, args.seqlen or base.seqlen,
+                            base.dtype)
         inp = W.scan_inputs(shape, device=dev, seed=0)
         out = torch.empty_like(inp["u"])
         ws = torch.empty(max(16, ssm.ssm_scan_workspace_bytes(shape.batch, shape.d_inner, shape.d_state,
@@ -487,7 +488,9 @@ def main(argv=None):
     ap.add_argument("--only", choices=["all", "scan", "decode"], default="all",
                     help="profiling aid: run only the scan or only the decode part (no JSON line)")
     ap.add_argument("--seqlen", type=int, default=None,
-                    help="profiling aid: scan a shorter sequence of the same workload")
+                    help="profiling aid: scan another sequence length of the same workload")
+    ap.add_argument("--dinner", type=int, default=None,
+                    help="profiling aid: scan another number of channels of the same workload")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":

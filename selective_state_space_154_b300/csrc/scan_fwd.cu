@@ -557,22 +557,27 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
   const int64_t rows = a.batch * a.d_inner;
   int kind = kScanTiles;
   if (a.N <= 16) {
-    const int occ_r = knobs.ctas_per_sm > 0 ? knobs.ctas_per_sm : rows_resident_ctas(a.act, a.z != nullptr);
-    const int64_t row_slots = (int64_t)sms * occ_r * kRowsPerRowCta;
+    const int64_t row_slots = (int64_t)sms * 4 * kRowsPerRowCta;
     if (rows >= row_slots || a.L >= 65536) kind = kScanRows;
   }
   if (knobs.force_kind >= 0 && !(knobs.force_kind == kScanRows && a.N > 16)) kind = knobs.force_kind;
   pl.kind = kind;
   if (kind == kScanRows) {
+    // Long sequences over wide layers: one CTA per SM holding rows_big_cta_rows() rows,
+    // so that chunks advance in lock-step and the carry between them resolves at once.
+    // Otherwise 128-row CTAs, four per SM, for finer load balance.
+    const int big = rows_big_cta_rows(a.act);
+    const int rb = (a.d_inner >= big && a.L >= 65536 && knobs.ctas_per_sm <= 0) ? big : kRowsPerRowCta;
+    const int occ = rb == kRowsPerRowCta ? 4 : 1;
     pl.npad = 16;
     pl.groups = 1;
-    pl.threads = kRowsPerRowCta;
-    pl.ctiles = (int)((a.d_inner + kRowsPerRowCta - 1) / kRowsPerRowCta);
+    pl.threads = rb;
+    pl.ctiles = (int)((a.d_inner + rb - 1) / rb);
     pl.smem_bytes = 0;
-    const int occ = knobs.ctas_per_sm > 0 ? knobs.ctas_per_sm : rows_resident_ctas(a.act, a.z != nullptr);
+    const int occ_k = knobs.ctas_per_sm > 0 ? knobs.ctas_per_sm : occ;
     const int64_t items = a.batch * pl.ctiles;
-    const int64_t nch = pick_chunks(items, (int64_t)sms * occ, a.L, 8192, kRowTokensPerStage, knobs.force_chunks);
-    finish_chunks(pl, a.L, nch, kRowTokensPerStage, items, (size_t)kRowsPerRowCta * 16 * 4);
+    const int64_t nch = pick_chunks(items, (int64_t)sms * occ_k, a.L, 8192, kRowTokensPerStage, knobs.force_chunks);
+    finish_chunks(pl, a.L, nch, kRowTokensPerStage, items, (size_t)rb * 16 * 4);
     *plan = pl;
     return true;
   }

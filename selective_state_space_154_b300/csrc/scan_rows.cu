@@ -26,7 +26,6 @@
 namespace ssm {
 namespace {
 
-constexpr int RB = kRowsPerRowCta;      // rows (threads) per CTA
 constexpr int TS = kRowTokensPerStage;  // tokens per stage
 constexpr int NS = 16;                  // states per row held by one thread
 
@@ -46,45 +45,52 @@ __device__ __forceinline__ int64_t min64r(int64_t a, int64_t b) { return a < b ?
 
 // Shared memory of one CTA.  A row tile holds TS tokens of RB rows; granule g
 // (16 bytes) of row r sits at granule index g ^ swz(r) of that row.
-template <typename T>
+template <typename T, int RB>
 struct Smem {
   static constexpr int kRowBytes = TS * (int)sizeof(T);  // 64 (bf16) or 128 (fp32)
   static constexpr int kGran = kRowBytes / 16;           // 16-byte granules per row and stage
   uint4 tile[2][3][RB][kGran];                           // [stage][u|delta|z][row][granule]
   uint4 raw_bc[2][2 * TS * NS * sizeof(T) / 16];         // [stage][B|C][TS][N] raw
   float bcf[TS * 2 * NS];                                // converted stage, [TS][B|C][16]
-  int misc[2];
+  // two ints used outside the passes (ticket, wait result) share bcf's storage,
+  // which keeps the CTA at 56 KB of shared memory (four CTAs per SM)
+  __device__ int* misc() { return reinterpret_cast<int*>(bcf); }
 };
 
 // XOR swizzle of the granule index: lanes r..r+7 reading the same granule of
 // their rows then hit eight different 16-byte bank groups.
 template <typename T>
 __device__ __forceinline__ int swz(int r) {
-  return (r / (128 / Smem<T>::kRowBytes)) & (Smem<T>::kGran - 1);
+  constexpr int kRowBytes = TS * (int)sizeof(T), kGran = kRowBytes / 16;
+  return (r / (128 / kRowBytes)) & (kGran - 1);
 }
 
 // Issue the copies of stage [t0, t0 + TS) ∩ [t0, t_end): three row tiles and B, C.
-template <typename T, bool VEC, int MODE>
-__device__ __forceinline__ void issue_stage(Smem<T>& sm, int buf, const RowParams& p, int64_t b, int64_t row0, int nrows,
+template <typename T, int RB, bool VEC, int MODE>
+__device__ __forceinline__ void issue_stage(Smem<T, RB>& sm, int buf, const RowParams& p, int64_t b, int64_t row0, int nrows,
                                             int64_t t0, int64_t t_end) {
-  constexpr int G = Smem<T>::kGran;
+  constexpr int G = Smem<T, RB>::kGran;
   constexpr int E = sizeof(T);
   const int64_t L = p.a.L;
   const T* srcs[3] = {static_cast<const T*>(MODE == 0 ? p.a.u : p.a.out), static_cast<const T*>(p.a.delta),
                       static_cast<const T*>(p.a.z)};
   const int ntens = p.a.z ? 3 : 2;
+  const int g = threadIdx.x % G;
+  const int r_first = threadIdx.x / G;
+  const int64_t t = t0 + (int64_t)g * (16 / E);
   for (int w = 0; w < ntens; ++w) {
-    for (int i = threadIdx.x; i < RB * G; i += RB) {
-      const int r = i / G, g = i % G;
-      const int64_t t = t0 + (int64_t)g * (16 / E);
+    const T* base = srcs[w] + (row0 + r_first) * L + t;
+    for (int k = 0; k < G; ++k) {
+      const int r = r_first + k * (RB / G);
       uint4* dst = &sm.tile[buf][w][r][g ^ swz<T>(r)];
       const bool ok = r < nrows && t < t_end;
       if (VEC) {
-        const T* s = ok ? srcs[w] + (row0 + r) * L + t : srcs[w];
-        cp_async16(dst, s, ok ? 16 : 0);
+        cp_async16(dst, ok ? static_cast<const void*>(base + (int64_t)k * (RB / G) * L) : static_cast<const void*>(srcs[w]),
+                   ok ? 16 : 0);
       } else {
         // element copies for rows that are not 16-byte aligned
         unsigned wv[4] = {0u, 0u, 0u, 0u};
+        static_assert(RB % G == 0, "rows per stage split evenly over granules");
         if (ok) {
           const T* s = srcs[w] + (row0 + r) * L;
           for (int e = 0; e < 16 / E; ++e) {
@@ -122,7 +128,7 @@ __device__ __forceinline__ void issue_stage(Smem<T>& sm, int buf, const RowParam
   }
 }
 
-template <typename T>
+template <typename T, int RB>
 __device__ __forceinline__ void convert_bc(float* bc, const T* raw, int N) {
   for (int i = threadIdx.x; i < TS * 2 * NS; i += RB) {
     const int t = i / (2 * NS), w = (i / NS) & 1, n = i % NS;
@@ -199,8 +205,8 @@ enum PassMode { kScanPass = 0, kCorrPass = 1 };
 //   kScanPass: the local scan from the registers' h; writes out.
 //   kCorrPass: h holds h_in; adds Σ_n C exp(A S) h_in to out until the term is
 //              zero for every row of the CTA.
-template <typename T, bool HAS_Z, bool VEC, int MODE>
-__device__ __forceinline__ void row_pass(Smem<T>& sm, const RowParams& p, int64_t b, int64_t row0, int nrows,
+template <typename T, int RB, bool HAS_Z, bool VEC, int MODE>
+__device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, int64_t b, int64_t row0, int nrows,
                                          int64_t t_lo, int64_t t_hi, float (&h)[NS], const float (&a2)[NS],
                                          const float (&ia)[NS], const float* arow, bool precise, float Dc,
                                          float biasc, float& S) {
@@ -213,17 +219,17 @@ __device__ __forceinline__ void row_pass(Smem<T>& sm, const RowParams& p, int64_
   T* orow = static_cast<T*>(p.a.out) + (row0 + (row_ok ? r : 0)) * p.a.L;
   const int nst = (int)((t_hi - t_lo + TS - 1) / TS);
   if (nst <= 0) return;
-  issue_stage<T, VEC, MODE>(sm, 0, p, b, row0, nrows, t_lo, t_hi);
+  issue_stage<T, RB, VEC, MODE>(sm, 0, p, b, row0, nrows, t_lo, t_hi);
   cp_async_commit();
   float comp = 0.f;  // Kahan compensation of S
   for (int st = 0; st < nst; ++st) {
     const int64_t ts = t_lo + (int64_t)st * TS;
     const int buf = st & 1;
-    if (st + 1 < nst) issue_stage<T, VEC, MODE>(sm, buf ^ 1, p, b, row0, nrows, ts + TS, t_hi);
+    if (st + 1 < nst) issue_stage<T, RB, VEC, MODE>(sm, buf ^ 1, p, b, row0, nrows, ts + TS, t_hi);
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();  // stage st landed for every thread
-    convert_bc<T>(sm.bcf, reinterpret_cast<const T*>(sm.raw_bc[buf]), N);
+    convert_bc<T, RB>(sm.bcf, reinterpret_cast<const T*>(sm.raw_bc[buf]), N);
     __syncthreads();
     const int64_t t_valid = row_ok ? t_hi : ts;  // rows past d_inner compute nothing useful
     bool any = false;
@@ -353,20 +359,24 @@ __device__ __forceinline__ void row_pass(Smem<T>& sm, const RowParams& p, int64_
   __syncthreads();
 }
 
-template <typename T, bool HAS_Z, bool VEC>
-__global__ void __launch_bounds__(RB, 4) scan_rows_kernel(const RowParams p) {
+// RB rows (threads) per CTA: 128 (four CTAs per SM) or 512 / 256 (one CTA per SM
+// for bf16 / fp32).  With one CTA per SM all of an SM's rows advance in lock-step
+// through the per-stage barriers, so chunks finish together; co-resident CTAs
+// with equal work were seen to finish up to 1.6x apart.
+template <typename T, int RB, bool HAS_Z, bool VEC>
+__global__ void __launch_bounds__(RB, 512 / RB) scan_rows_kernel(const RowParams p) {
   using AT = Act<T>;
   constexpr bool FAST = AT::kFast;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  Smem<T>& sm = *reinterpret_cast<Smem<T>*>(smem_raw);
+  Smem<T, RB>& sm = *reinterpret_cast<Smem<T, RB>*>(smem_raw);
 
   const int N = (int)p.a.N;
   const int per_chunk = (int)p.a.batch * p.rtiles;
   int item;
   if (p.nchunks > 1) {
-    if (threadIdx.x == 0) sm.misc[0] = (int)atomicAdd(p.hdr, 1u);
+    if (threadIdx.x == 0) sm.misc()[0] = (int)atomicAdd(p.hdr, 1u);
     __syncthreads();
-    item = sm.misc[0];
+    item = sm.misc()[0];
   } else {
     item = blockIdx.x;
   }
@@ -399,23 +409,23 @@ __global__ void __launch_bounds__(RB, 4) scan_rows_kernel(const RowParams p) {
   const float biasc = (row_ok && p.a.bias) ? p.a.bias[c] : 0.f;
 
   float S = 0.f;
-  row_pass<T, HAS_Z, VEC, kScanPass>(sm, p, b, row0, nrows, tc0, tc1, h, a2, ia, arow, precise, Dc, biasc, S);
+  row_pass<T, RB, HAS_Z, VEC, kScanPass>(sm, p, b, row0, nrows, tc0, tc1, h, a2, ia, arow, precise, Dc, biasc, S);
 
   // ---------------- carry between chunks ----------------
   float hin[NS];
 #pragma unroll
   for (int n = 0; n < NS; ++n) hin[n] = 0.f;
   if (p.nchunks > 1) {
-    const size_t slot = (size_t)per_chunk * RB * NS;
+    const size_t slot = (size_t)per_chunk * RB * NS;  // RB: this instantiation's rows per CTA
     const size_t my = ((size_t)rem * RB + threadIdx.x) * NS;
     if (chunk > 0) {
       if (threadIdx.x == 0) {
         const unsigned* f = p.flags + (size_t)(chunk - 1) * per_chunk + rem;
-        sm.misc[1] = wait_flag_rows(p, f, p.fault_lookback ? 3u : 1u) ? 1 : 0;  // 3 is never written
+        sm.misc()[1] = wait_flag_rows(p, f, p.fault_lookback ? 3u : 1u) ? 1 : 0;  // 3 is never written
       }
       __syncthreads();
       __threadfence();
-      const bool ok = sm.misc[1] != 0;
+      const bool ok = sm.misc()[1] != 0;
       const float4* prev = reinterpret_cast<const float4*>(p.incl + (size_t)(chunk - 1) * slot + my);
 #pragma unroll
       for (int q = 0; q < NS / 4; ++q) {
@@ -450,52 +460,37 @@ __global__ void __launch_bounds__(RB, 4) scan_rows_kernel(const RowParams p) {
   for (int n = 0; n < NS; ++n) any |= (hin[n] != 0.f);
   if (!__syncthreads_or(any)) return;
   float Sc = 0.f;
-  row_pass<T, HAS_Z, VEC, kCorrPass>(sm, p, b, row0, nrows, tc0, tc1, hin, a2, ia, arow, precise, Dc, biasc, Sc);
+  row_pass<T, RB, HAS_Z, VEC, kCorrPass>(sm, p, b, row0, nrows, tc0, tc1, hin, a2, ia, arow, precise, Dc, biasc, Sc);
 }
 
-int g_rows_occ[2][2] = {};  // [act][has_z]
-
-template <typename T, bool HAS_Z, bool VEC>
+template <typename T, int RB, bool HAS_Z, bool VEC>
 cudaError_t set_smem() {
-  return cudaFuncSetAttribute(scan_rows_kernel<T, HAS_Z, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)sizeof(Smem<T>));
+  return cudaFuncSetAttribute(scan_rows_kernel<T, RB, HAS_Z, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sizeof(Smem<T, RB>));
 }
 
-template <typename T, bool HAS_Z>
-int rows_occupancy() {
-  int nb = 0;
-  if (set_smem<T, HAS_Z, true>() != cudaSuccess) return 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, scan_rows_kernel<T, HAS_Z, true>, RB, sizeof(Smem<T>)) !=
-      cudaSuccess)
-    return 1;
-  return nb > 0 ? nb : 1;
-}
-
-template <typename T, bool HAS_Z>
+template <typename T, int RB, bool HAS_Z>
 cudaError_t rows_launch_t(const RowParams& p, int grid, cudaStream_t s) {
   cudaError_t e;
   if (p.vec_rows) {
-    if ((e = set_smem<T, HAS_Z, true>()) != cudaSuccess) return e;
-    scan_rows_kernel<T, HAS_Z, true><<<grid, RB, sizeof(Smem<T>), s>>>(p);
+    if ((e = set_smem<T, RB, HAS_Z, true>()) != cudaSuccess) return e;
+    scan_rows_kernel<T, RB, HAS_Z, true><<<grid, RB, sizeof(Smem<T, RB>), s>>>(p);
   } else {
-    if ((e = set_smem<T, HAS_Z, false>()) != cudaSuccess) return e;
-    scan_rows_kernel<T, HAS_Z, false><<<grid, RB, sizeof(Smem<T>), s>>>(p);
+    if ((e = set_smem<T, RB, HAS_Z, false>()) != cudaSuccess) return e;
+    scan_rows_kernel<T, RB, HAS_Z, false><<<grid, RB, sizeof(Smem<T, RB>), s>>>(p);
   }
   return cudaGetLastError();
 }
 
+template <typename T, bool HAS_Z>
+cudaError_t rows_launch_dt(const RowParams& p, int rb, int grid, cudaStream_t s) {
+  if (rb == 128) return rows_launch_t<T, 128, HAS_Z>(p, grid, s);
+  return rows_launch_t<T, (sizeof(T) == 2 ? 512 : 256), HAS_Z>(p, grid, s);
+}
+
 }  // namespace
 
-int rows_resident_ctas(int act, bool has_z) {
-  int& o = g_rows_occ[act == 1][has_z];
-  if (o == 0) {
-    if (act == 1)
-      o = has_z ? rows_occupancy<__nv_bfloat16, true>() : rows_occupancy<__nv_bfloat16, false>();
-    else
-      o = has_z ? rows_occupancy<float, true>() : rows_occupancy<float, false>();
-  }
-  return o;
-}
+int rows_big_cta_rows(int act) { return act == 1 ? 512 : 256; }
 
 cudaError_t scan_rows_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream) {
   RowParams p{};
@@ -519,9 +514,11 @@ cudaError_t scan_rows_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream
     if (e != cudaSuccess) return e;
   }
   const int grid = (int)((int64_t)plan.nchunks * a.batch * plan.ctiles);
+  const int rb = plan.threads;
   if (a.act == 1)
-    return a.z ? rows_launch_t<__nv_bfloat16, true>(p, grid, stream) : rows_launch_t<__nv_bfloat16, false>(p, grid, stream);
-  return a.z ? rows_launch_t<float, true>(p, grid, stream) : rows_launch_t<float, false>(p, grid, stream);
+    return a.z ? rows_launch_dt<__nv_bfloat16, true>(p, rb, grid, stream)
+               : rows_launch_dt<__nv_bfloat16, false>(p, rb, grid, stream);
+  return a.z ? rows_launch_dt<float, true>(p, rb, grid, stream) : rows_launch_dt<float, false>(p, rb, grid, stream);
 }
 
 }  // namespace ssm

@@ -11,7 +11,7 @@ namespace ssm {
 constexpr int kRowsPerCta = 32;
 constexpr int kTileTokens = 32;
 constexpr int kStatesPerThread = 4;  // G: states of one row held by one thread (tile kernel)
-constexpr int kRowsPerRowCta = 128;     // row kernel: rows per CTA (one thread per row, d_state <= 16)
+constexpr int kRowsPerRowCta = 128;     // row kernel, small variant: rows per CTA (four CTAs per SM)
 constexpr int kRowTokensPerStage = 32;  // row kernel: tokens per stage
 
 enum ScanKind { kScanTiles = 0, kScanRows = 1 };
@@ -63,7 +63,7 @@ RuntimeKnobs runtime_knobs();
 
 bool scan_make_plan(const ScanArgs& a, ScanPlan* plan);  // false: unsupported dims
 cudaError_t scan_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream);
-int rows_resident_ctas(int act, bool has_z);
+int rows_big_cta_rows(int act);  // rows of the one-CTA-per-SM variant of the row kernel
 cudaError_t scan_rows_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream);
 
 struct StepArgs {
