@@ -169,8 +169,18 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- timing helpers
-def flush_l2(buf):
-    buf.zero_()
+class L2Flush:
+    """Evict L2 between timed calls: write a 512 MiB buffer (4x the 126 MB L2),
+    then read another one, so that the written lines are already back in HBM
+    and the next timed call does not pay for their write-back."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
 
 
 def time_steps(fn, steps, warmup, world, stream):
@@ -250,6 +260,47 @@ def bench_e2e(args, shape, inp, out, dev, world):
     return steps, secs, h2d, d2h
 
 
+def bench_workloads(dev, runs=20):
+    """The other scan workloads, one call each timed alone with L2 flushed before
+    it (CUDA events around the call only); median of `runs`."""
+    import selective_state_space_154_b300 as ssm
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for name in ("tiny_fp32", "mamba130m_layer", "mamba2p8b_layer"):
+        shape = W.SCAN_SHAPES[name]
+        inp = W.scan_inputs(shape, device=dev, seed=0)
+        out = torch.empty_like(inp["u"])
+        fs = torch.empty((shape.batch, shape.d_inner, shape.d_state), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(16, ssm.ssm_scan_workspace_bytes(shape.batch, shape.d_inner, shape.d_state,
+                                                              shape.seqlen, shape.dtype)), dtype=torch.uint8,
+                         device=dev)
+
+        def call():
+            ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                             inp["bias"], out, fs, workspace=ws, stream=stream)
+
+        for _ in range(3):
+            call()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
+        for a, b in evs:
+            flush()
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize()
+        if ssm.ssm_scan_check(ws) != ssm.SSM_OK:
+            raise RuntimeError(f"{name}: scan reported an error")
+        secs = statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+        alg = scan_alg_bytes(shape)
+        res[name] = {"batch": shape.batch, "d_inner": shape.d_inner, "d_state": shape.d_state,
+                     "seq_len": shape.seqlen, "io_dtype": "bf16" if shape.dtype == torch.bfloat16 else "fp32",
+                     "us": secs * 1e6, "channel_tokens_per_s": shape.channel_tokens / secs,
+                     "gbs": alg / secs / 1e9, "alg_bytes": alg}
+        del inp, out, fs, ws
+    return res
+
+
 def bench_decode(dev):
     """ssm_step on the decode workload: each timed step starts with L2 flushed
     (in a model, the other layers evict this layer's state between its steps);
@@ -260,7 +311,7 @@ def bench_decode(dev):
     state = torch.zeros((shape.batch, shape.d_inner, shape.d_state), dtype=torch.float32, device=dev)
     out = torch.empty((shape.batch, shape.d_inner), dtype=shape.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
-    l2 = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def step(s):
         ssm.ssm_step(state, inp["x"][s], inp["delta"][s], inp["A"], inp["B"][s], inp["C"][s], inp["D"],
@@ -271,7 +322,7 @@ def bench_decode(dev):
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(shape.steps)]
     for s in range(shape.steps):
-        flush_l2(l2)
+        flush()
         evs[s][0].record(stream)
         step(s)
         evs[s][1].record(stream)
@@ -304,7 +355,7 @@ def bench_decode(dev):
         "us_per_step": cold / shape.steps * 1e6,
         "gbs": per_step_bytes * shape.steps / cold / 1e9,
         "alg_bytes_per_step": per_step_bytes,
-        "l2": "flushed (512 MiB write) before every timed step; steps timed one by one with CUDA events",
+        "l2": "flushed (512 MiB write, then 512 MiB read) before every timed step; steps timed one by one with CUDA events",
         "warm_l2_graph": {"value": shape.batch * shape.steps / warm, "us_per_step": warm / shape.steps * 1e6,
                           "gbs": per_step_bytes * shape.steps / warm / 1e9,
                           "note": "1000 steps replayed back to back as one CUDA graph; the 84 MB state stays in L2"},
@@ -340,23 +391,21 @@ def _oracle_call(args_list, threads):
 
 def cpu_baseline(target_s=15.0):
     """The oracle as it stands, on all host cores, over a bounded sample of the
-    workload: full-length rows are too slow, so the sample is `rows` channels ×
-    `length` tokens sized from a short calibration run to about target_s."""
+    workload: one full-length channel per thread, scanned repeatedly until about
+    target_s of work has been timed (the host memory stays at a few hundred MB)."""
     shape = W.SCAN_SHAPES[WORKLOAD]
     threads = cpu_threads()
-    calib_len = 1 << 16
-    cal = make_oracle_rows(shape, threads, calib_len)
-    _oracle_call(cal, threads)  # warm (thread pool, page faults)
-    dt = _oracle_call(cal, threads)
-    rate = threads * calib_len / max(dt, 1e-6)  # channel·tokens/s
-    length = shape.seqlen if rate * target_s >= threads * shape.seqlen else max(calib_len, int(rate * target_s / threads) // 1024 * 1024)
-    rows = threads * max(1, int(rate * target_s / (threads * length)))
+    length, rows = shape.seqlen, threads
     sample = make_oracle_rows(shape, rows, length, seed=1)
-    dt = _oracle_call(sample, threads)
-    return {"value": rows * length / dt, "unit": "channel·tokens/s", "cores": threads, "kind": "oracle",
-            "seconds": dt,
+    total, calls = 0.0, 0
+    while total < target_s and calls < 1000:
+        total += _oracle_call(sample, threads)
+        calls += 1
+    return {"value": rows * length * calls / total, "unit": "channel·tokens/s", "cores": threads, "kind": "oracle",
+            "seconds": total,
             "sample": f"{rows} channels x {length} tokens of the {WORKLOAD} workload (d_state {shape.d_state}, "
-                      f"bf16-rounded inputs, float64 arithmetic), oracle.scan threaded over channels"}
+                      f"bf16-rounded inputs, float64 arithmetic), oracle.scan threaded over channels, "
+                      f"run {calls} times"}
 
 
 # ---------------------------------------------------------------- arms
@@ -385,6 +434,7 @@ def run_ours(args):
     del inp, out
     torch.cuda.empty_cache()
     decode = bench_decode(dev) if rank == 0 else None
+    others = bench_workloads(dev) if rank == 0 else None
     cpu = cpu_baseline() if (rank == 0 and world == 1) else None
 
     if rank == 0:
@@ -412,6 +462,10 @@ def run_ours(args):
             "gpu_launches": args.steps,
             "clocks": clocks,
             "decode": decode,
+            "workloads": {"note": "other scan workloads, each call timed alone after an L2 flush (512 MiB write, then 512 MiB read), "
+                                  "median of 20; hbm_frac of the measured copy bandwidth",
+                          **({k: dict(v, hbm_frac=v["gbs"] / hbm_peak) for k, v in others.items()}
+                             if others else {})},
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -425,7 +479,7 @@ def run_profile_case(args):
     import selective_state_space_154_b300 as ssm
     dev = torch.device("cuda", 0)
     if args.only == "scan":
-        base = W.SCAN_SHAPES[WORKLOAD]
+        base = W.SCAN_SHAPES[args.workload]
         shape = W.ScanShape(base.name, base.batch, args.dinner or base.d_inner, base.d_state, args.seqlen or base.seqlen,
                             base.dtype)
         inp = W.scan_inputs(shape, device=dev, seed=0)
@@ -491,6 +545,8 @@ def main(argv=None):
                     help="profiling aid: scan another sequence length of the same workload")
     ap.add_argument("--dinner", type=int, default=None,
                     help="profiling aid: scan another number of channels of the same workload")
+    ap.add_argument("--workload", choices=sorted(W.SCAN_SHAPES), default=WORKLOAD,
+                    help="profiling aid: the scan workload --only scan runs")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":

@@ -128,6 +128,16 @@ SSM_API ssm_status ssm_step(float* state, const void* x, const void* delta, cons
  */
 SSM_API ssm_status ssm_scan_check(const void* workspace, size_t workspace_bytes);
 
+/*
+ * Synchronises `stream`, then reads and clears this library's device-side step
+ * error word on the current device: SSM_ERR_TIMEOUT if, since the last check,
+ * an ssm_step on this device gave up waiting for its state to arrive in shared
+ * memory (bounded at 1 s, or SSM_LOOKBACK_TIMEOUT_MS), in which case the state
+ * rows of the affected tiles were left unchanged and their outputs are
+ * undefined; SSM_OK otherwise.  The word is shared by all streams of the device.
+ */
+SSM_API ssm_status ssm_step_check(ssm_stream_t stream);
+
 /* Static, human-readable name of a status. */
 SSM_API const char* ssm_status_string(ssm_status s);
 

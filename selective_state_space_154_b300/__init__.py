@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "SsmError", "ssm_scan_workspace_bytes", "ssm_scan_fwd", "ssm_step", "ssm_scan_check",
     "ssm_status_string", "scan_fwd", "step", "library_path", "load_library", "ssm_scan_fwd_noalloc",
-    "SSM_NOALLOC_SCRATCH_BYTES",
+    "SSM_NOALLOC_SCRATCH_BYTES", "ssm_step_check",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -70,6 +70,8 @@ def load_library():
             lib.ssm_step.restype = i32
             lib.ssm_scan_check.argtypes = [vp, sz]
             lib.ssm_scan_check.restype = i32
+            lib.ssm_step_check.argtypes = [vp]
+            lib.ssm_step_check.restype = i32
             lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 10 + [dp, vp]
             lib.ssm_scan_fwd_noalloc.restype = i32
             lib.ssm_status_string.argtypes = [i32]
@@ -216,6 +218,13 @@ def ssm_scan_check(workspace) -> int:
     if workspace is None:
         return SSM_OK
     return int(load_library().ssm_scan_check(_ptr(workspace), workspace.numel() * workspace.element_size()))
+
+
+def ssm_step_check(stream=None, device=None) -> int:
+    """Synchronise the stream, then read and clear the device's step error word."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(load_library().ssm_step_check(_stream_handle(stream, dev)))
 
 
 def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, return_final_state=False,

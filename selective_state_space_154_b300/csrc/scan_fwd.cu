@@ -26,8 +26,9 @@
 // end state of the previous one as its carry-in h_in (bounded wait on a flag),
 // and publishes its own end state P h_in + H.  The outputs of a chunk are
 // then corrected by Σ_n C_t,n exp(A_n S_t) h_in,n,
-// S_t = Σ_{s≤t} Δ_s, for as long as that term is not exactly zero in fp32
-// for every state of the CTA.
+// S_t = Σ_{s≤t} Δ_s, for as long as exp(A_n S_t) is above 2^-24 for some
+// state of the CTA with h_in,n != 0; below that the term is under the fp32
+// rounding of h_in itself.
 #include <algorithm>
 #include <cstdio>
 
@@ -422,11 +423,9 @@ __global__ void __launch_bounds__(512, 1) scan_fwd_kernel(const KParams p) {
           }
           pyr[t * groups] = y;
         }
+        // continue while some state's carried-in term is above 2^-24 |h_in| (A log2e S > -24)
 #pragma unroll
-        for (int k = 0; k < G; ++k) {
-          const float P = precise ? expf(a_[k] * S) : ex2_approx(a2[k] * S);
-          alive |= (P != 0.f && hin[k] != 0.f);
-        }
+        for (int k = 0; k < G; ++k) alive |= (a2[k] * S > kCorrStopLog2 && hin[k] != 0.f);
       }
       __syncthreads();
 
@@ -520,6 +519,10 @@ int device_sms() {
 
 // Chunks along L: enough (rows x chunks) work items to fill the resident slots,
 // each chunk at least min_chunk tokens (the carry correction is paid per chunk).
+// Shortest chunk the row kernel splits a sequence into: the correction of a
+// chunk by its carry-in typically covers several hundred tokens.
+constexpr int64_t kMinRowChunk = 256;
+
 int64_t pick_chunks(int64_t items, int64_t slots, int64_t L, int64_t min_chunk, int64_t granule, int force) {
   int64_t nch = 1;
   if (items < slots) nch = std::min<int64_t>(slots / items, L / min_chunk);
@@ -552,13 +555,14 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
   const int sms = device_sms();
   ScanPlan pl{};
   // The row kernel (one thread per row) does the least work per state update
-  // but needs many rows or a long sequence to fill the GPU; the tile kernel
-  // splits a row's states over 4 threads and suits short sequences.
+  // but needs rows × chunks to fill the GPU, with chunks of at least
+  // kMinRowChunk tokens; the tile kernel splits a row's states over 4 threads
+  // and takes short sequences over few rows.
   const int64_t rows = a.batch * a.d_inner;
   int kind = kScanTiles;
   if (a.N <= 16) {
     const int64_t row_slots = (int64_t)sms * 4 * kRowsPerRowCta;
-    if (rows >= row_slots || a.L >= 65536) kind = kScanRows;
+    if (rows >= row_slots || a.L >= 65536 || rows * (a.L / kMinRowChunk) >= row_slots) kind = kScanRows;
   }
   if (knobs.force_kind >= 0 && !(knobs.force_kind == kScanRows && a.N > 16)) kind = knobs.force_kind;
   pl.kind = kind;
@@ -568,15 +572,20 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
     // Otherwise 128-row CTAs, four per SM, for finer load balance.
     const int big = rows_big_cta_rows(a.act);
     const int rb = (a.d_inner >= big && a.L >= 65536 && knobs.ctas_per_sm <= 0) ? big : kRowsPerRowCta;
-    const int occ = rb == kRowsPerRowCta ? 4 : 1;
+    int tpr = 1;
+    if (rb == kRowsPerRowCta && (knobs.force_tpr == 2)) tpr = 2;
+    const int occ = rb == kRowsPerRowCta ? (tpr == 2 ? 3 : 4) : 1;
     pl.npad = 16;
-    pl.groups = 1;
-    pl.threads = rb;
+    pl.groups = tpr;
+    pl.threads = rb * tpr;
+    pl.rows_per_cta = rb;
     pl.ctiles = (int)((a.d_inner + rb - 1) / rb);
     pl.smem_bytes = 0;
     const int occ_k = knobs.ctas_per_sm > 0 ? knobs.ctas_per_sm : occ;
     const int64_t items = a.batch * pl.ctiles;
-    const int64_t nch = pick_chunks(items, (int64_t)sms * occ_k, a.L, 8192, kRowTokensPerStage, knobs.force_chunks);
+    // as many chunks as fill one wave of CTAs (more would only add corrections)
+    const int64_t nch =
+        pick_chunks(items, (int64_t)sms * occ_k, a.L, kMinRowChunk, kRowTokensPerStage, knobs.force_chunks);
     finish_chunks(pl, a.L, nch, kRowTokensPerStage, items, (size_t)rb * 16 * 4);
     *plan = pl;
     return true;
@@ -584,6 +593,7 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
   pl.npad = (int)((a.N + 15) / 16) * 16;
   pl.groups = pl.npad / G;
   pl.threads = RT * pl.groups;
+  pl.rows_per_cta = RT;
   pl.ctiles = (int)((a.d_inner + RT - 1) / RT);
   const int esize = a.act == 1 ? 2 : 4;
   const Layout lay = make_layout(esize, (int)a.N, pl.npad, pl.groups);

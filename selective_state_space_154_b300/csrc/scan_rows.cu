@@ -66,10 +66,13 @@ __device__ __forceinline__ int swz(int r) {
 }
 
 // Issue the copies of stage [t0, t0 + TS) ∩ [t0, t_end): three row tiles and B, C.
-template <typename T, int RB, bool VEC, int MODE>
+template <typename T, int RB, int NT, bool VEC, int MODE>
 __device__ __forceinline__ void issue_stage(Smem<T, RB>& sm, int buf, const RowParams& p, int64_t b, int64_t row0, int nrows,
                                             int64_t t0, int64_t t_end) {
   constexpr int G = Smem<T, RB>::kGran;
+  constexpr int RSTEP = NT / G;        // rows apart of one thread's copies
+  constexpr int NPER = RB / RSTEP;     // copies per thread and tensor
+  static_assert(NT % G == 0 && RB % RSTEP == 0, "a stage splits evenly over the CTA's threads");
   constexpr int E = sizeof(T);
   const int64_t L = p.a.L;
   const T* srcs[3] = {static_cast<const T*>(MODE == 0 ? p.a.u : p.a.out), static_cast<const T*>(p.a.delta),
@@ -80,17 +83,16 @@ __device__ __forceinline__ void issue_stage(Smem<T, RB>& sm, int buf, const RowP
   const int64_t t = t0 + (int64_t)g * (16 / E);
   for (int w = 0; w < ntens; ++w) {
     const T* base = srcs[w] + (row0 + r_first) * L + t;
-    for (int k = 0; k < G; ++k) {
-      const int r = r_first + k * (RB / G);
+    for (int k = 0; k < NPER; ++k) {
+      const int r = r_first + k * RSTEP;
       uint4* dst = &sm.tile[buf][w][r][g ^ swz<T>(r)];
       const bool ok = r < nrows && t < t_end;
       if (VEC) {
-        cp_async16(dst, ok ? static_cast<const void*>(base + (int64_t)k * (RB / G) * L) : static_cast<const void*>(srcs[w]),
+        cp_async16(dst, ok ? static_cast<const void*>(base + (int64_t)k * RSTEP * L) : static_cast<const void*>(srcs[w]),
                    ok ? 16 : 0);
       } else {
         // element copies for rows that are not 16-byte aligned
         unsigned wv[4] = {0u, 0u, 0u, 0u};
-        static_assert(RB % G == 0, "rows per stage split evenly over granules");
         if (ok) {
           const T* s = srcs[w] + (row0 + r) * L;
           for (int e = 0; e < 16 / E; ++e) {
@@ -118,19 +120,19 @@ __device__ __forceinline__ void issue_stage(Smem<T, RB>& sm, int buf, const RowP
     if (p.vec_bc) {
       constexpr int VPT = 16 / E;
       const int nvec = TS * N / VPT;
-      for (int i = threadIdx.x; i < nvec; i += RB) {
+      for (int i = threadIdx.x; i < nvec; i += NT) {
         const bool ok = (int64_t)(i + 1) * VPT <= nvalid;
         cp_async16(dst + i * VPT, ok ? s0 + (int64_t)i * VPT : bcsrc[w], ok ? 16 : 0);
       }
     } else {
-      for (int i = threadIdx.x; i < TS * N; i += RB) dst[i] = (i < nvalid) ? s0[i] : T(0.f);
+      for (int i = threadIdx.x; i < TS * N; i += NT) dst[i] = (i < nvalid) ? s0[i] : T(0.f);
     }
   }
 }
 
-template <typename T, int RB>
+template <typename T, int NT>
 __device__ __forceinline__ void convert_bc(float* bc, const T* raw, int N) {
-  for (int i = threadIdx.x; i < TS * 2 * NS; i += RB) {
+  for (int i = threadIdx.x; i < TS * 2 * NS; i += NT) {
     const int t = i / (2 * NS), w = (i / NS) & 1, n = i % NS;
     bc[i] = n < N ? Act<T>::to_f(raw[(w * TS + t) * N + n]) : 0.f;
   }
@@ -203,33 +205,39 @@ enum PassMode { kScanPass = 0, kCorrPass = 1 };
 
 // One pass of the CTA over tokens [t_lo, t_hi).
 //   kScanPass: the local scan from the registers' h; writes out.
-//   kCorrPass: h holds h_in; adds Σ_n C exp(A S) h_in to out until the term is
-//              zero for every row of the CTA.
-template <typename T, int RB, bool HAS_Z, bool VEC, int MODE>
+//   kCorrPass: h holds h_in; adds Σ_n C exp(A S) h_in to out until exp(A S) has
+//              fallen below 2^-24 for every state with h_in != 0 in the CTA.
+// TPR threads share a row: thread j of the row holds states [j·SPT, (j+1)·SPT)
+// and the readout is summed over the row's threads with shuffles.
+template <typename T, int RB, int TPR, bool HAS_Z, bool VEC, int MODE>
 __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, int64_t b, int64_t row0, int nrows,
-                                         int64_t t_lo, int64_t t_hi, float (&h)[NS], const float (&a2)[NS],
-                                         const float (&ia)[NS], const float* arow, bool precise, float Dc,
+                                         int64_t t_lo, int64_t t_hi, float (&h)[NS / TPR], const float (&a2)[NS / TPR],
+                                         const float (&ia)[NS / TPR], const float* arow, bool precise, float Dc,
                                          float biasc, float& S) {
   using AT = Act<T>;
   constexpr bool FAST = AT::kFast;
+  constexpr int NT = RB * TPR;
+  constexpr int SPT = NS / TPR;
   constexpr int GPB = (8 * (int)sizeof(T)) / 16;  // granules per 8-token block
   const int N = (int)p.a.N;
-  const int r = threadIdx.x;
+  const int r = threadIdx.x / TPR;
+  const int jpart = threadIdx.x % TPR;
+  const int n0 = jpart * SPT;
   const bool row_ok = r < nrows;
   T* orow = static_cast<T*>(p.a.out) + (row0 + (row_ok ? r : 0)) * p.a.L;
   const int nst = (int)((t_hi - t_lo + TS - 1) / TS);
   if (nst <= 0) return;
-  issue_stage<T, RB, VEC, MODE>(sm, 0, p, b, row0, nrows, t_lo, t_hi);
+  issue_stage<T, RB, NT, VEC, MODE>(sm, 0, p, b, row0, nrows, t_lo, t_hi);
   cp_async_commit();
   float comp = 0.f;  // Kahan compensation of S
   for (int st = 0; st < nst; ++st) {
     const int64_t ts = t_lo + (int64_t)st * TS;
     const int buf = st & 1;
-    if (st + 1 < nst) issue_stage<T, RB, VEC, MODE>(sm, buf ^ 1, p, b, row0, nrows, ts + TS, t_hi);
+    if (st + 1 < nst) issue_stage<T, RB, NT, VEC, MODE>(sm, buf ^ 1, p, b, row0, nrows, ts + TS, t_hi);
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();  // stage st landed for every thread
-    convert_bc<T, RB>(sm.bcf, reinterpret_cast<const T*>(sm.raw_bc[buf]), N);
+    convert_bc<T, NT>(sm.bcf, reinterpret_cast<const T*>(sm.raw_bc[buf]), N);
     __syncthreads();
     const int64_t t_valid = row_ok ? t_hi : ts;  // rows past d_inner compute nothing useful
     bool any = false;
@@ -247,11 +255,17 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
       const float* bcs = sm.bcf + blk * 8 * 2 * NS;
       float yv[8];
       float Sb = 0.f;
+      float dlt8[8], gz8[8];
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
+      for (int v = 0; v < 8; ++v) {  // per-token scalars first: 8 independent MUFU chains
         const bool tok_ok = t + v < t_valid;
         const float rr = get8<T>(wd, v) + biasc;
-        const float dlt = tok_ok ? (FAST ? softplus_fast(rr) : softplus_precise(rr)) : 0.f;
+        dlt8[v] = tok_ok ? (FAST ? softplus_fast(rr) : softplus_precise(rr)) : 0.f;
+        gz8[v] = HAS_Z ? silu_t<FAST>(get8<T>(wz, v)) : 1.f;
+      }
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float dlt = dlt8[v];
         const float x = get8<T>(wu, v);  // kCorrPass: the current output value
         const float4* bc4 = reinterpret_cast<const float4*>(bcs + v * 2 * NS);
         float y;
@@ -260,9 +274,9 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
             const float2 dd = make_float2(dlt, dlt), xx = make_float2(x, x);
             float2 ya = make_float2(0.f, 0.f), yb = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int q = 0; q < NS / 4; ++q) {
-              const float4 bq = bc4[q];
-              const float4 cq = bc4[NS / 4 + q];
+            for (int q = 0; q < SPT / 4; ++q) {
+              const float4 bq = bc4[n0 / 4 + q];
+              const float4 cq = bc4[NS / 4 + n0 / 4 + q];
 #pragma unroll
               for (int k2 = 0; k2 < 2; ++k2) {
                 const int n = 4 * q + 2 * k2;
@@ -283,15 +297,15 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
           } else {
             y = 0.f;
 #pragma unroll
-            for (int q = 0; q < NS / 4; ++q) {
-              const float4 bq = bc4[q];
-              const float4 cq = bc4[NS / 4 + q];
+            for (int q = 0; q < SPT / 4; ++q) {
+              const float4 bq = bc4[n0 / 4 + q];
+              const float4 cq = bc4[NS / 4 + n0 / 4 + q];
               const float bb[4] = {bq.x, bq.y, bq.z, bq.w};
               const float cc[4] = {cq.x, cq.y, cq.z, cq.w};
 #pragma unroll
               for (int k2 = 0; k2 < 4; ++k2) {
                 const int n = 4 * q + k2;
-                const float an0 = (row_ok && n < N) ? __ldg(arow + n) : 0.f;
+                const float an0 = (row_ok && n0 + n < N) ? __ldg(arow + n) : 0.f;  // arow starts at state n0
                 const float an = fabsf(an0) < 8.673617e-19f ? 0.f : an0;
                 if (an != 0.f) {
                   const float em1 = FAST ? ex2_approx(dlt * a2[n]) - 1.f : expm1f(dlt * an);
@@ -303,8 +317,10 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
               }
             }
           }
+#pragma unroll
+          for (int off = TPR / 2; off > 0; off >>= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
           y = fmaf(Dc, x, y);
-          if (HAS_Z) y *= silu_t<FAST>(get8<T>(wz, v));
+          if (HAS_Z) y *= gz8[v];
           Sb += dlt;
         } else {
           // correction Σ_n C_n exp(A_n S_t) h_in,n (h holds h_in in this pass)
@@ -313,8 +329,8 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
           const float2 ss = make_float2(St, St);
           float2 ya = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int q = 0; q < NS / 4; ++q) {
-            const float4 cq = bc4[NS / 4 + q];
+          for (int q = 0; q < SPT / 4; ++q) {
+            const float4 cq = bc4[NS / 4 + n0 / 4 + q];
 #pragma unroll
             for (int k2 = 0; k2 < 2; ++k2) {
               const int n = 4 * q + 2 * k2;
@@ -330,7 +346,9 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
             }
           }
           y = ya.x + ya.y;
-          if (HAS_Z) y *= silu_t<FAST>(get8<T>(wz, v));
+#pragma unroll
+          for (int off = TPR / 2; off > 0; off >>= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
+          if (HAS_Z) y *= gz8[v];
           y += x;
         }
         yv[v] = y;
@@ -341,15 +359,13 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
         comp = (tk - S) - yk;
         S = tk;
       }
-      if (row_ok && t < t_hi) store8<T, VEC>(orow, t, t_hi, yv);
+      if (row_ok && jpart == 0 && t < t_hi) store8<T, VEC>(orow, t, t_hi, yv);
     }
     if (MODE == kCorrPass) {
-      // stop once exp(A S) h_in is exactly zero for every state of the CTA's rows
+      // Stop once every state's carried-in term exp(A S) h_in is below 2^-24 |h_in|
+      // (A log2e S < -24): what is left is under the fp32 rounding of h_in itself.
 #pragma unroll
-      for (int n = 0; n < NS; ++n) {
-        const float P = precise ? exp2f(a2[n] * S) : ex2_approx(a2[n] * S);
-        any |= (P != 0.f && h[n] != 0.f);
-      }
+      for (int n = 0; n < SPT; ++n) any |= (a2[n] * S > kCorrStopLog2 && h[n] != 0.f);
       if (!__syncthreads_or(any)) break;  // also orders the reuse of this stage's buffers
     } else {
       __syncthreads();  // this stage's buffers are refilled two stages later
@@ -363,8 +379,18 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
 // for bf16 / fp32).  With one CTA per SM all of an SM's rows advance in lock-step
 // through the per-stage barriers, so chunks finish together; co-resident CTAs
 // with equal work were seen to finish up to 1.6x apart.
-template <typename T, int RB, bool HAS_Z, bool VEC>
-__global__ void __launch_bounds__(RB, 512 / RB) scan_rows_kernel(const RowParams p) {
+// TPR = 2 (two threads per row, 8 states each) doubles the threads for layers
+// with too few rows to fill the GPU at one thread per row.
+template <int RB, int TPR>
+struct RowCta {
+  static constexpr int kThreads = RB * TPR;
+  static constexpr int kMinBlocks = TPR == 1 ? 512 / RB : 3;
+};
+
+template <typename T, int RB, int TPR, bool HAS_Z, bool VEC>
+__global__ void __launch_bounds__(RowCta<RB, TPR>::kThreads, RowCta<RB, TPR>::kMinBlocks)
+    scan_rows_kernel(const RowParams p) {
+  constexpr int SPT = NS / TPR;
   using AT = Act<T>;
   constexpr bool FAST = AT::kFast;
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -388,36 +414,43 @@ __global__ void __launch_bounds__(RB, 512 / RB) scan_rows_kernel(const RowParams
   const int64_t row0 = b * p.a.d_inner + c0;
   const int64_t tc0 = min64r(p.a.L, (int64_t)chunk * p.chunk_len);
   const int64_t tc1 = min64r(p.a.L, tc0 + p.chunk_len);
-  const bool row_ok = (int)threadIdx.x < nrows;
-  const int64_t c = c0 + (row_ok ? threadIdx.x : 0);
-  const int64_t row = row0 + (row_ok ? threadIdx.x : 0);
+  const int r = (int)threadIdx.x / TPR;
+  const int n0 = ((int)threadIdx.x % TPR) * SPT;
+  const bool row_ok = r < nrows;
+  const int64_t c = c0 + (row_ok ? r : 0);
+  const int64_t row = row0 + (row_ok ? r : 0);
 
-  // per-row constants; padded states (n >= N) are inert: A = 0, B = C = 0
-  float a2[NS], ia[NS], h[NS];
+  // per-row constants of this thread's states; padded states (n >= N) are inert: A = 0, B = C = 0
+  float a2[SPT], ia[SPT], h[SPT];
   bool precise = !FAST;
-  const float* arow = p.a.A + c * N;
+  const float* arow = p.a.A + c * N + n0;
 #pragma unroll
-  for (int n = 0; n < NS; ++n) {
-    const float a = (row_ok && n < N) ? arow[n] : 0.f;
+  for (int n = 0; n < SPT; ++n) {
+    const float a = (row_ok && n0 + n < N) ? arow[n] : 0.f;
     const bool tiny = fabsf(a) < 8.673617e-19f;  // |A| < 2^-60 counts as A = 0
-    if (row_ok && n < N && tiny) precise = true;
+    if (row_ok && n0 + n < N && tiny) precise = true;
     a2[n] = tiny ? 0.f : a * kLog2e;
     ia[n] = tiny ? 0.f : 1.f / a;
     h[n] = 0.f;
+  }
+  // a row's threads take the same path (the precise one if any of its states has A = 0)
+  if (TPR > 1) {
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) precise |= __shfl_xor_sync(0xffffffffu, (int)precise, off) != 0;
   }
   const float Dc = (row_ok && p.a.D) ? p.a.D[c] : 0.f;
   const float biasc = (row_ok && p.a.bias) ? p.a.bias[c] : 0.f;
 
   float S = 0.f;
-  row_pass<T, RB, HAS_Z, VEC, kScanPass>(sm, p, b, row0, nrows, tc0, tc1, h, a2, ia, arow, precise, Dc, biasc, S);
+  row_pass<T, RB, TPR, HAS_Z, VEC, kScanPass>(sm, p, b, row0, nrows, tc0, tc1, h, a2, ia, arow, precise, Dc, biasc, S);
 
   // ---------------- carry between chunks ----------------
-  float hin[NS];
+  float hin[SPT];
 #pragma unroll
-  for (int n = 0; n < NS; ++n) hin[n] = 0.f;
+  for (int n = 0; n < SPT; ++n) hin[n] = 0.f;
   if (p.nchunks > 1) {
     const size_t slot = (size_t)per_chunk * RB * NS;  // RB: this instantiation's rows per CTA
-    const size_t my = ((size_t)rem * RB + threadIdx.x) * NS;
+    const size_t my = ((size_t)rem * RB + r) * NS + n0;
     if (chunk > 0) {
       if (threadIdx.x == 0) {
         const unsigned* f = p.flags + (size_t)(chunk - 1) * per_chunk + rem;
@@ -428,12 +461,12 @@ __global__ void __launch_bounds__(RB, 512 / RB) scan_rows_kernel(const RowParams
       const bool ok = sm.misc()[1] != 0;
       const float4* prev = reinterpret_cast<const float4*>(p.incl + (size_t)(chunk - 1) * slot + my);
 #pragma unroll
-      for (int q = 0; q < NS / 4; ++q) {
+      for (int q = 0; q < SPT / 4; ++q) {
         const float4 v = ok ? __ldcg(prev + q) : make_float4(0.f, 0.f, 0.f, 0.f);
         hin[4 * q] = v.x; hin[4 * q + 1] = v.y; hin[4 * q + 2] = v.z; hin[4 * q + 3] = v.w;
       }
 #pragma unroll
-      for (int n = 0; n < NS; ++n) {
+      for (int n = 0; n < SPT; ++n) {
         const float P = precise ? exp2f(a2[n] * S) : ex2_approx(a2[n] * S);
         h[n] = fmaf(P, hin[n], h[n]);
       }
@@ -441,7 +474,7 @@ __global__ void __launch_bounds__(RB, 512 / RB) scan_rows_kernel(const RowParams
     if (chunk + 1 < p.nchunks) {
       float4* mine = reinterpret_cast<float4*>(p.incl + (size_t)chunk * slot + my);
 #pragma unroll
-      for (int q = 0; q < NS / 4; ++q) mine[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+      for (int q = 0; q < SPT / 4; ++q) mine[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
       __threadfence();
       __syncthreads();
       if (threadIdx.x == 0) st_release_gpu(p.flags + (size_t)chunk * per_chunk + rem, 1u);
@@ -449,43 +482,41 @@ __global__ void __launch_bounds__(RB, 512 / RB) scan_rows_kernel(const RowParams
   }
   if (p.a.final_state && chunk == p.nchunks - 1 && row_ok) {
 #pragma unroll
-    for (int n = 0; n < NS; ++n)
-      if (n < N) p.a.final_state[row * N + n] = h[n];
+    for (int n = 0; n < SPT; ++n)
+      if (n0 + n < N) p.a.final_state[row * N + n0 + n] = h[n];
   }
   if (chunk == 0 || p.nchunks == 1) return;
 
   // ---------------- correction of this chunk's first outputs ----------------
   bool any = false;
 #pragma unroll
-  for (int n = 0; n < NS; ++n) any |= (hin[n] != 0.f);
+  for (int n = 0; n < SPT; ++n) any |= (hin[n] != 0.f);
   if (!__syncthreads_or(any)) return;
   float Sc = 0.f;
-  row_pass<T, RB, HAS_Z, VEC, kCorrPass>(sm, p, b, row0, nrows, tc0, tc1, hin, a2, ia, arow, precise, Dc, biasc, Sc);
+  row_pass<T, RB, TPR, HAS_Z, VEC, kCorrPass>(sm, p, b, row0, nrows, tc0, tc1, hin, a2, ia, arow, precise, Dc, biasc, Sc);
 }
 
-template <typename T, int RB, bool HAS_Z, bool VEC>
-cudaError_t set_smem() {
-  return cudaFuncSetAttribute(scan_rows_kernel<T, RB, HAS_Z, VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)sizeof(Smem<T, RB>));
-}
-
-template <typename T, int RB, bool HAS_Z>
-cudaError_t rows_launch_t(const RowParams& p, int grid, cudaStream_t s) {
-  cudaError_t e;
-  if (p.vec_rows) {
-    if ((e = set_smem<T, RB, HAS_Z, true>()) != cudaSuccess) return e;
-    scan_rows_kernel<T, RB, HAS_Z, true><<<grid, RB, sizeof(Smem<T, RB>), s>>>(p);
-  } else {
-    if ((e = set_smem<T, RB, HAS_Z, false>()) != cudaSuccess) return e;
-    scan_rows_kernel<T, RB, HAS_Z, false><<<grid, RB, sizeof(Smem<T, RB>), s>>>(p);
-  }
+template <typename T, int RB, int TPR, bool HAS_Z, bool VEC>
+cudaError_t rows_launch_v(const RowParams& p, int grid, cudaStream_t s) {
+  auto kern = scan_rows_kernel<T, RB, TPR, HAS_Z, VEC>;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem<T, RB>));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, RowCta<RB, TPR>::kThreads, sizeof(Smem<T, RB>), s>>>(p);
   return cudaGetLastError();
 }
 
+template <typename T, int RB, int TPR, bool HAS_Z>
+cudaError_t rows_launch_t(const RowParams& p, int grid, cudaStream_t s) {
+  return p.vec_rows ? rows_launch_v<T, RB, TPR, HAS_Z, true>(p, grid, s)
+                    : rows_launch_v<T, RB, TPR, HAS_Z, false>(p, grid, s);
+}
+
 template <typename T, bool HAS_Z>
-cudaError_t rows_launch_dt(const RowParams& p, int rb, int grid, cudaStream_t s) {
-  if (rb == 128) return rows_launch_t<T, 128, HAS_Z>(p, grid, s);
-  return rows_launch_t<T, (sizeof(T) == 2 ? 512 : 256), HAS_Z>(p, grid, s);
+cudaError_t rows_launch_dt(const RowParams& p, int rb, int tpr, int grid, cudaStream_t s) {
+  if (tpr == 2) return rows_launch_t<T, 128, 2, HAS_Z>(p, grid, s);
+  if (rb == 128) return rows_launch_t<T, 128, 1, HAS_Z>(p, grid, s);
+  return rows_launch_t<T, (sizeof(T) == 2 ? 512 : 256), 1, HAS_Z>(p, grid, s);
 }
 
 }  // namespace
@@ -514,11 +545,12 @@ cudaError_t scan_rows_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream
     if (e != cudaSuccess) return e;
   }
   const int grid = (int)((int64_t)plan.nchunks * a.batch * plan.ctiles);
-  const int rb = plan.threads;
+  const int rb = plan.rows_per_cta, tpr = plan.threads / plan.rows_per_cta;
   if (a.act == 1)
-    return a.z ? rows_launch_dt<__nv_bfloat16, true>(p, rb, grid, stream)
-               : rows_launch_dt<__nv_bfloat16, false>(p, rb, grid, stream);
-  return a.z ? rows_launch_dt<float, true>(p, rb, grid, stream) : rows_launch_dt<float, false>(p, rb, grid, stream);
+    return a.z ? rows_launch_dt<__nv_bfloat16, true>(p, rb, tpr, grid, stream)
+               : rows_launch_dt<__nv_bfloat16, false>(p, rb, tpr, grid, stream);
+  return a.z ? rows_launch_dt<float, true>(p, rb, tpr, grid, stream)
+             : rows_launch_dt<float, false>(p, rb, tpr, grid, stream);
 }
 
 }  // namespace ssm

@@ -21,6 +21,9 @@ RuntimeKnobs runtime_knobs() {
     }
     const char* f = std::getenv("SSM_FAULT");
     r.fault_lookback = f && std::strcmp(f, "lookback") == 0;
+    r.fault_step = f && std::strcmp(f, "step") == 0;
+    const char* fs = std::getenv("SSM_FORCE_STEP");
+    r.force_step_plain = fs && std::strcmp(fs, "plain") == 0;
     if (const char* c = std::getenv("SSM_FORCE_CHUNKS")) r.force_chunks = std::atoi(c);
     r.force_kind = -1;
     if (const char* k = std::getenv("SSM_FORCE_KERNEL")) {
@@ -28,6 +31,7 @@ RuntimeKnobs runtime_knobs() {
       if (std::strcmp(k, "rows") == 0) r.force_kind = kScanRows;
     }
     if (const char* c = std::getenv("SSM_CTAS_PER_SM")) r.ctas_per_sm = std::atoi(c);
+    if (const char* c = std::getenv("SSM_FORCE_TPR")) r.force_tpr = std::atoi(c);
     return r;
   }();
 }
@@ -138,8 +142,20 @@ ssm_status ssm_step(float* state, const void* x, const void* delta, const float*
   a.state = state; a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
   a.bias = delta_bias; a.out = out;
   a.batch = dims->batch; a.d_inner = dims->d_inner; a.N = dims->d_state; a.act = dims->act;
-  const cudaError_t e = ssm::step_launch(a, reinterpret_cast<cudaStream_t>(stream));
+  const ssm::RuntimeKnobs knobs = ssm::runtime_knobs();
+  ssm::StepKnobs sk{};
+  sk.timeout_ns = knobs.lookback_timeout_ns;
+  sk.fault = knobs.fault_step;
+  sk.force_plain = knobs.force_step_plain;
+  const cudaError_t e = ssm::step_launch(a, sk, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_step_check(ssm_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return SSM_ERR_CUDA;
+  unsigned word = 0;
+  if (ssm::step_error_fetch_clear(&word) != cudaSuccess) return SSM_ERR_CUDA;
+  return word ? SSM_ERR_TIMEOUT : SSM_OK;
 }
 
 ssm_status ssm_scan_check(const void* workspace, size_t workspace_bytes) {

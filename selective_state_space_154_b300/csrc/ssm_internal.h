@@ -13,6 +13,9 @@ constexpr int kTileTokens = 32;
 constexpr int kStatesPerThread = 4;  // G: states of one row held by one thread (tile kernel)
 constexpr int kRowsPerRowCta = 128;     // row kernel, small variant: rows per CTA (four CTAs per SM)
 constexpr int kRowTokensPerStage = 32;  // row kernel: tokens per stage
+// The correction of a chunk's outputs by its carried-in state stops once
+// exp(A S) < 2^kCorrStopLog2 for every state with a nonzero carry-in.
+constexpr float kCorrStopLog2 = -24.f;
 
 enum ScanKind { kScanTiles = 0, kScanRows = 1 };
 
@@ -27,8 +30,9 @@ struct ScanPlan {
   int kind;           // ScanKind
   int npad;           // states per row rounded up to a multiple of 16 (16, 32, 48 or 64)
   int groups;         // npad / kStatesPerThread: threads per row
-  int threads;        // kRowsPerCta * groups
-  int ctiles;         // channel tiles per batch (32 channels for kScanTiles, 128 for kScanRows)
+  int threads;        // threads per CTA: kRowsPerCta * groups (tiles), rows_per_cta * threads per row (rows)
+  int rows_per_cta;   // channels per CTA
+  int ctiles;         // channel tiles per batch (d_inner / rows_per_cta, rounded up)
   int64_t chunk_len;  // tokens per chunk (multiple of kTileTokens unless one chunk)
   int nchunks;        // chunks along the sequence (1: no carry between chunks)
   size_t smem_bytes;  // dynamic shared memory per CTA
@@ -58,6 +62,9 @@ struct RuntimeKnobs {
   int force_chunks;               // >0: override the chunk count (tests)
   int force_kind;                 // -1: choose by shape; else a ScanKind (tests)
   int ctas_per_sm;                // >0: resident CTAs per SM assumed when splitting into chunks
+  int force_tpr;                  // >0: threads per row of the row kernel (1 or 2)
+  bool fault_step;                // test hook: the pipelined step's first wait never completes
+  bool force_step_plain;          // SSM_FORCE_STEP=plain: the generic step kernel only
 };
 RuntimeKnobs runtime_knobs();
 
@@ -80,6 +87,13 @@ struct StepArgs {
   int64_t batch, d_inner, N;
   int act;
 };
-cudaError_t step_launch(const StepArgs& a, cudaStream_t stream);
+struct StepKnobs {
+  long long timeout_ns;  // wait limit of the pipelined step kernel (0: 1 s)
+  bool fault;            // test hook: the pipelined kernel's first wait never completes
+  bool force_plain;      // use step_kernel even where the pipelined kernel applies
+};
+cudaError_t step_launch(const StepArgs& a, const StepKnobs& k, cudaStream_t stream);
+// Reads and clears the sticky error word of the pipelined step kernel (current device).
+cudaError_t step_error_fetch_clear(unsigned* word);
 
 }  // namespace ssm

@@ -4,12 +4,28 @@
 // とMamba" §2.4 二つのモード).
 //
 // The step is bound by memory: per row it moves the fp32 state (4·N bytes read
-// and written) plus x, Δ, z, out.  Work items are (row, quad of 4 states); a
-// warp's lanes take consecutive items, so the state moves as contiguous 16-byte
-// vectors, and the readout Σ_n C_n h_n is reduced across the lanes of a row with
-// shuffles.  Each thread handles kItems items spread over the grid and issues
-// all their loads before any arithmetic, so enough bytes are in flight per SM to
-// cover the memory latency.  The per-state arithmetic is that of the scan.
+// and written) plus x, Δ, z, out.  Two kernels:
+//
+//  * step_pipe_kernel (d_state ∈ {4, 8, 16, 32, 64}, d_inner a multiple of the
+//    tile's rows, state / x / Δ / z 16-byte aligned): a tile is 512 (row, quad
+//    of 4 states) items = 8 KB of state, 512 / (d_state / 4) consecutive
+//    channels of one batch row.  Each CTA keeps one block of channels (so A,
+//    bias and D are read once per CTA) and walks the batch.  One thread per CTA
+//    streams each tile's state, x, Δ and z into shared memory with
+//    cp.async.bulk (completion counted in bytes on an mbarrier) several tiles
+//    ahead; all threads update the tile in place in shared memory, and the same
+//    thread writes it back with a bulk store.  Loads of later tiles, the
+//    arithmetic of the current one and the stores of earlier ones overlap, so
+//    HBM stays busy without a large register footprint.
+//  * step_kernel (any shape): work items (row, quad) spread over the grid; each
+//    thread issues the loads of kItems items before any arithmetic.
+//
+// In both, a warp's lanes take consecutive items, so the state moves as
+// contiguous 16-byte vectors, and the readout Σ_n C_n h_n is reduced across the
+// lanes of a row with shuffles.  The per-state arithmetic is that of the scan.
+#include <algorithm>
+#include <cstdint>
+
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
@@ -115,6 +131,268 @@ __global__ void __launch_bounds__(kBlock) step_kernel(const StepArgs p, int64_t 
   }
 }
 
+
+// ------------------------------------------------------------ pipelined kernel
+constexpr int kPipeThreads = 512;  // items (row, quad) per tile = threads per CTA
+constexpr int kPipeStages = 4;     // tiles in shared memory per CTA
+constexpr int kPipeBarBytes = 128; // mbarriers (one per stage + one never-completed) at the front
+
+__device__ unsigned g_step_error;  // sticky: a pipelined step gave up waiting (read by ssm_step_check)
+
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+  return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(unsigned bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned bar, unsigned bytes) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned bar, unsigned parity) {
+  unsigned done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Bounded wait for the phase of `parity` to complete: false once the deadline
+// (globaltimer, ns) has passed or after 2^26 polls, whichever comes first.
+__device__ __forceinline__ bool mbar_wait(unsigned bar, unsigned parity, unsigned long long deadline) {
+  for (int it = 0; it < (1 << 26); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15) == 15 && globaltimer_ns() > deadline) return false;
+  }
+  return false;
+}
+// global -> shared bulk copy, completion signalled on `bar` (bytes: multiple of 16)
+__device__ __forceinline__ void bulk_load(unsigned dst, const void* src, unsigned bytes, unsigned bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// shared -> global bulk copy in the current bulk group
+__device__ __forceinline__ void bulk_store(void* dst, unsigned src, unsigned bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+template <typename T, int QR>
+struct PipeLayout {
+  static constexpr int kRows = kPipeThreads / QR;                  // rows per tile
+  static constexpr int kStateBytes = kPipeThreads * 16;            // 8 KB
+  static constexpr int kInBytes = kRows * (int)sizeof(T);          // one of x / Δ / z per tile
+  static constexpr int kStageBytes = kStateBytes + 3 * kInBytes;   // multiple of 16
+  static constexpr int kSmemBytes = kPipeBarBytes + kPipeStages * kStageBytes;
+};
+
+struct PipeArgs {
+  StepArgs a;
+  int64_t ncb;  // channel blocks of kRows channels: d_inner / kRows (the grid is a multiple of it)
+  unsigned long long timeout_ns;
+  int fault;  // test hook: the first wait is on a barrier that never completes
+};
+
+// CTA j owns channel block cb = j mod ncb for its whole life and walks the batch
+// rows b = j / ncb, + gridDim / ncb, ...: a tile is (b, cb), kRows consecutive
+// rows of one batch.  A, bias and D of its channels are loaded once; B and C of
+// the next tile's batch are fetched into registers while the current tile runs.
+template <typename T, int QR, bool HAS_Z>
+__global__ void __launch_bounds__(kPipeThreads) step_pipe_kernel(const PipeArgs pa) {
+  using AT = Act<T>;
+  using LY = PipeLayout<T, QR>;
+  constexpr int N = 4 * QR;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const StepArgs& p = pa.a;
+  const int t = threadIdx.x;
+  const int r = t / QR, q = t % QR;
+  const unsigned bar0 = smem_u32(smem);
+  const unsigned stage0 = bar0 + kPipeBarBytes;
+  const unsigned long long deadline = globaltimer_ns() + pa.timeout_ns;
+
+  const int64_t cb = blockIdx.x % pa.ncb;
+  const int64_t b0 = blockIdx.x / pa.ncb, bstride = gridDim.x / pa.ncb;
+  const int my_tiles = b0 < p.batch ? (int)((p.batch - 1 - b0) / bstride + 1) : 0;
+  const int64_t c = cb * LY::kRows + r;
+  auto row0_of = [&](int i) { return (b0 + (int64_t)i * bstride) * p.d_inner + cb * LY::kRows; };
+  const uint8_t* xg = static_cast<const uint8_t*>(p.x);
+  const uint8_t* dg = static_cast<const uint8_t*>(p.delta);
+  const uint8_t* zg = static_cast<const uint8_t*>(p.z);
+  auto issue = [&](int s, int64_t row0) {  // one thread
+    const unsigned st = stage0 + s * LY::kStageBytes;
+    const unsigned bar = bar0 + 8 * s;
+    mbar_expect_tx(bar, LY::kStateBytes + (HAS_Z ? 3 : 2) * LY::kInBytes);
+    bulk_load(st, p.state + row0 * N, LY::kStateBytes, bar);
+    bulk_load(st + LY::kStateBytes, xg + row0 * (int64_t)sizeof(T), LY::kInBytes, bar);
+    bulk_load(st + LY::kStateBytes + LY::kInBytes, dg + row0 * (int64_t)sizeof(T), LY::kInBytes, bar);
+    if (HAS_Z) bulk_load(st + LY::kStateBytes + 2 * LY::kInBytes, zg + row0 * (int64_t)sizeof(T), LY::kInBytes, bar);
+  };
+  auto load_bc = [&](int i, float (&bv)[4], float (&cv)[4]) {
+    const int64_t b = b0 + (int64_t)i * bstride;
+    const T* bp = static_cast<const T*>(p.B) + b * N + 4 * q;
+    const T* cp = static_cast<const T*>(p.C) + b * N + 4 * q;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      bv[k] = AT::load(bp + k);
+      cv[k] = AT::load(cp + k);
+    }
+  };
+
+  if (t == 0) {
+    for (int s = 0; s <= kPipeStages; ++s) mbar_init(bar0 + 8 * s, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (t == 0)
+    for (int i = 0; i < my_tiles && i < kPipeStages; ++i) issue(i, row0_of(i));
+
+  // per-channel constants, once per CTA
+  const float4 a4 = my_tiles > 0 ? __ldg(reinterpret_cast<const float4*>(p.A + c * N) + q)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+  const float biasc = (p.bias && my_tiles > 0) ? __ldg(p.bias + c) : 0.f;
+  const float Dc = (p.D && my_tiles > 0) ? __ldg(p.D + c) : 0.f;
+  float bn[4] = {0.f, 0.f, 0.f, 0.f}, cn[4] = {0.f, 0.f, 0.f, 0.f};
+  if (my_tiles > 0) load_bc(0, bn, cn);
+
+  int i = 0;
+  bool failed = false;
+  for (; i < my_tiles; ++i) {
+    const int s = i % kPipeStages;
+    const int64_t row0 = row0_of(i);
+    const float bv[4] = {bn[0], bn[1], bn[2], bn[3]};
+    const float cv[4] = {cn[0], cn[1], cn[2], cn[3]};
+    if (i + 1 < my_tiles) load_bc(i + 1, bn, cn);
+
+    const unsigned wait_bar = (pa.fault && i == 0) ? bar0 + 8 * kPipeStages : bar0 + 8 * s;
+    const bool ok = mbar_wait(wait_bar, (unsigned)(i / kPipeStages) & 1u, deadline);
+    unsigned char* st = smem + kPipeBarBytes + s * LY::kStageBytes;
+    float4* hp = reinterpret_cast<float4*>(st) + t;
+    const T* xs = reinterpret_cast<const T*>(st + LY::kStateBytes);
+    const T* ds = reinterpret_cast<const T*>(st + LY::kStateBytes + LY::kInBytes);
+    const T* zs = reinterpret_cast<const T*>(st + LY::kStateBytes + 2 * LY::kInBytes);
+    float4 h4 = *hp;
+    float hs[4] = {h4.x, h4.y, h4.z, h4.w};
+    const float x = AT::to_f(xs[r]);
+    const float rr = AT::to_f(ds[r]) + biasc;
+    const float dlt = AT::kFast ? softplus_fast(rr) : softplus_precise(rr);
+    float y = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float a = av[k];
+      if (fabsf(a) < 8.673617e-19f) {
+        hs[k] = fmaf(dlt * x, bv[k], hs[k]);  // A = 0: Ā = 1, B̄ = Δ B
+      } else if (AT::kFast) {
+        const float em1 = ex2_approx(dlt * (a * kLog2e)) - 1.f;
+        hs[k] = fmaf(em1, fmaf(x * (1.f / a), bv[k], hs[k]), hs[k]);
+      } else {
+        const float em1 = expm1f(dlt * a);
+        hs[k] = fmaf(em1, fmaf(x * (1.f / a), bv[k], hs[k]), hs[k]);
+      }
+      y = fmaf(cv[k], hs[k], y);
+    }
+    *hp = make_float4(hs[0], hs[1], hs[2], hs[3]);
+#pragma unroll
+    for (int off = QR / 2; off > 0; off >>= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
+    if (q == 0 && ok) {
+      y = fmaf(Dc, x, y);
+      if (HAS_Z) y *= AT::kFast ? silu_fast(AT::to_f(zs[r])) : silu_precise(AT::to_f(zs[r]));
+      static_cast<T*>(p.out)[row0 + r] = AT::from_f(y);
+    }
+    fence_async_smem();  // the bulk store below reads what the threads wrote
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
+    }
+    if (t == 0) {
+      bulk_store(p.state + row0 * N, stage0 + s * LY::kStageBytes, LY::kStateBytes);
+      bulk_commit();
+      // refill the previous tile's buffer once its store has read it
+      if (i >= 1 && i - 1 + kPipeStages < my_tiles) {
+        bulk_wait_read<1>();
+        issue((i - 1) % kPipeStages, row0_of(i - 1 + kPipeStages));
+      }
+    }
+  }
+  if (t == 0) {
+    if (failed) {
+      atomicOr(&g_step_error, 1u);
+      // let every load still in flight land before the CTA's shared memory is released
+      const int last = min(my_tiles, (i >= 1 ? i - 1 : 0) + kPipeStages);
+      for (int j = i; j < last; ++j)
+        mbar_wait(bar0 + 8 * (j % kPipeStages), (unsigned)(j / kPipeStages) & 1u,
+                  globaltimer_ns() + pa.timeout_ns);
+    }
+    bulk_wait_all();
+  }
+}
+
+template <typename T, int QR>
+cudaError_t launch_pipe_q(const PipeArgs& pa, cudaStream_t stream) {
+  using LY = PipeLayout<T, QR>;
+  // per device and instantiation: shared-memory opt-in and resident CTAs per SM, set up once
+  constexpr int kMaxDev = 64;
+  static int grid_cap[2][kMaxDev] = {};
+  const bool has_z = pa.a.z != nullptr;
+  auto kern = has_z ? step_pipe_kernel<T, QR, true> : step_pipe_kernel<T, QR, false>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  int& cap = grid_cap[has_z][dev];
+  if (!cap) {
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kSmemBytes);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPipeThreads, LY::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cap = sms * std::max(per_sm, 1);
+  }
+  // a multiple of the channel blocks, at most one CTA per (batch, channel block)
+  const int64_t per_cb = std::max<int64_t>(1, std::min<int64_t>(pa.a.batch, cap / pa.ncb));
+  const int64_t grid = pa.ncb * per_cb;
+  if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
+  kern<<<(unsigned)grid, kPipeThreads, LY::kSmemBytes, stream>>>(pa);
+  return cudaGetLastError();
+}
+
+// The pipelined kernel takes the step when its tiles fit the shape exactly and
+// every bulk-copied array is 16-byte aligned; otherwise step_kernel does.
+template <typename T>
+bool pipe_launch_dt(const StepArgs& a, const StepKnobs& k, cudaStream_t stream, cudaError_t* err) {
+  const int N = (int)a.N;
+  if (k.force_plain) return false;
+  if (N != 4 && N != 8 && N != 16 && N != 32 && N != 64) return false;
+  const int rows_per_tile = kPipeThreads / (N / 4);
+  if (a.d_inner % rows_per_tile != 0) return false;
+  auto al = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+  if (!al(a.state) || !al(a.x) || !al(a.delta) || (a.z && !al(a.z))) return false;
+  PipeArgs pa{};
+  pa.a = a;
+  pa.ncb = a.d_inner / rows_per_tile;
+  pa.timeout_ns = k.timeout_ns > 0 ? (unsigned long long)k.timeout_ns : 1000000000ull;
+  pa.fault = k.fault ? 1 : 0;
+  switch (N) {
+    case 4: *err = launch_pipe_q<T, 1>(pa, stream); break;
+    case 8: *err = launch_pipe_q<T, 2>(pa, stream); break;
+    case 16: *err = launch_pipe_q<T, 4>(pa, stream); break;
+    case 32: *err = launch_pipe_q<T, 8>(pa, stream); break;
+    default: *err = launch_pipe_q<T, 16>(pa, stream); break;
+  }
+  return true;
+}
+
 template <typename T, int QR>
 cudaError_t launch_q(const StepArgs& a, bool vec, cudaStream_t stream) {
   const int64_t items = a.batch * a.d_inner * QR;
@@ -142,8 +420,21 @@ cudaError_t launch_dt(const StepArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t step_launch(const StepArgs& a, cudaStream_t stream) {
-  return a.act == 1 ? launch_dt<__nv_bfloat16>(a, stream) : launch_dt<float>(a, stream);
+cudaError_t step_launch(const StepArgs& a, const StepKnobs& k, cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
+  if (a.act == 1) {
+    if (pipe_launch_dt<__nv_bfloat16>(a, k, stream, &e)) return e;
+    return launch_dt<__nv_bfloat16>(a, stream);
+  }
+  if (pipe_launch_dt<float>(a, k, stream, &e)) return e;
+  return launch_dt<float>(a, stream);
+}
+
+cudaError_t step_error_fetch_clear(unsigned* word) {
+  cudaError_t e = cudaMemcpyFromSymbol(word, g_step_error, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  const unsigned zero = 0;
+  return cudaMemcpyToSymbol(g_step_error, &zero, sizeof(unsigned));
 }
 
 }  // namespace ssm

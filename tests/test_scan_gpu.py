@@ -21,11 +21,14 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.fixture(params=["tiles", "rows"])
+@pytest.fixture(params=["tiles", "rows", "rows2"])
 def kernel(request, monkeypatch):
-    """Run the test through each scan kernel (the row kernel serves d_state <= 16;
-    larger d_state falls back to the tile kernel)."""
-    monkeypatch.setenv("SSM_FORCE_KERNEL", request.param)
+    """Run the test through each scan kernel: the tile kernel, the row kernel with
+    one thread per row, and the row kernel with two threads per row (the row
+    kernel serves d_state <= 16; larger d_state falls back to the tile kernel)."""
+    monkeypatch.setenv("SSM_FORCE_KERNEL", "tiles" if request.param == "tiles" else "rows")
+    if request.param == "rows2":
+        monkeypatch.setenv("SSM_FORCE_TPR", "2")
     return request.param
 
 
@@ -172,8 +175,7 @@ def test_long_1m_sampled():
 @pytest.mark.parametrize("name", ["mamba130m_layer", "long_1m"])
 def test_workload_through_other_kernel(name, monkeypatch):
     """The kernel not chosen by the planner for a workload gives the same result."""
-    other = "rows" if name == "mamba130m_layer" else "tiles"
-    monkeypatch.setenv("SSM_FORCE_KERNEL", other)
+    monkeypatch.setenv("SSM_FORCE_KERNEL", "tiles")  # both take the row kernel by default
     _workload_rows(name, 8, seed=3)
 
 

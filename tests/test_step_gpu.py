@@ -41,6 +41,63 @@ def test_step_small(dtype, batch, d, N):
         assert rel_err(to_np(state), ref_state) <= TOL[dtype]
 
 
+@pytest.fixture(params=["pipe", "plain"])
+def step_kernel(request, monkeypatch):
+    """Run a test with the pipelined step kernel where the shape allows it, or with
+    the generic one (SSM_FORCE_STEP=plain)."""
+    if request.param == "plain":
+        monkeypatch.setenv("SSM_FORCE_STEP", "plain")
+    return request.param
+
+
+# shapes the pipelined kernel takes: d_inner a multiple of 512 / (d_state / 4) rows;
+# (64, 4096, 16) gives each CTA more tiles than it has pipeline stages
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("batch,d,N", [(1, 128, 16), (3, 256, 16), (2, 512, 4), (1, 256, 8), (2, 64, 32),
+                                       (2, 64, 64), (64, 4096, 16)])
+def test_step_tiled_shapes(step_kernel, dtype, batch, d, N):
+    steps = 3
+    inp = _rand_step_inputs(batch, d, N, steps, dtype, seed=batch * 7 + d + N)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    state = torch.randn((batch, d, N), generator=g, device=DEV)
+    ref_state = to_np(state)
+    for s in range(steps):
+        z = inp["z"][s] if s != 1 else None  # one step without the gate
+        out = ssm.step(state, inp["x"][s], inp["delta"][s], inp["A"], inp["B"][s], inp["C"][s],
+                       D=inp["D"], z=z, delta_bias=inp["bias"])
+        ref_out, ref_state = oracle.step(ref_state, inp["x"][s], inp["delta"][s], inp["A"], inp["B"][s],
+                                         inp["C"][s], D=inp["D"], z=z, bias=inp["bias"])
+        torch.cuda.synchronize()
+        assert rel_err(to_np(out), ref_out) <= TOL[dtype]
+        assert rel_err(to_np(state), ref_state) <= TOL[dtype]
+    assert ssm.ssm_step_check() == ssm.SSM_OK
+
+
+def test_step_wait_timeout_is_reported_and_state_kept(monkeypatch):
+    """Test hook: the pipelined kernel's first wait is on a barrier nothing
+    completes; the bounded wait gives up, every tile is left unchanged,
+    ssm_step_check reports SSM_ERR_TIMEOUT once, and the next step is clean."""
+    batch, d, N = 4, 1024, 16
+    inp = _rand_step_inputs(batch, d, N, 1, torch.bfloat16, seed=21)
+    state = torch.randn((batch, d, N), device=DEV)
+    before = state.clone()
+    monkeypatch.setenv("SSM_FAULT", "step")
+    monkeypatch.setenv("SSM_LOOKBACK_TIMEOUT_MS", "100")
+    ssm.step(state, inp["x"][0], inp["delta"][0], inp["A"], inp["B"][0], inp["C"][0], D=inp["D"], z=inp["z"][0],
+             delta_bias=inp["bias"])
+    assert ssm.ssm_step_check() == ssm.SSM_ERR_TIMEOUT
+    assert torch.equal(state, before)
+    assert ssm.ssm_step_check() == ssm.SSM_OK  # the check cleared the word
+    monkeypatch.delenv("SSM_FAULT")
+    out = ssm.step(state, inp["x"][0], inp["delta"][0], inp["A"], inp["B"][0], inp["C"][0], D=inp["D"],
+                   z=inp["z"][0], delta_bias=inp["bias"])
+    ref_out, ref_state = oracle.step(to_np(before), inp["x"][0], inp["delta"][0], inp["A"], inp["B"][0],
+                                     inp["C"][0], D=inp["D"], z=inp["z"][0], bias=inp["bias"])
+    assert ssm.ssm_step_check() == ssm.SSM_OK
+    assert rel_err(to_np(out), ref_out) <= TOL[torch.bfloat16]
+    assert rel_err(to_np(state), ref_state) <= TOL[torch.bfloat16]
+
+
 def test_step_optional_and_zero_A():
     inp = _rand_step_inputs(2, 40, 16, 3, torch.bfloat16, seed=9)
     inp["A"][::4, 2] = 0.0
@@ -62,7 +119,7 @@ def _as_scan(inp):
                 C=inp["C"].permute(1, 0, 2).contiguous(), A=inp["A"], D=inp["D"], bias=inp["bias"])
 
 
-def test_decode_workload_matches_oracle_and_scan():
+def test_decode_workload_matches_oracle_and_scan(step_kernel):
     """256 x 5120 x 16, 1000 steps from a zero state: sampled rows against the
     oracle; every output and the final state against ssm_scan_fwd on the same
     1000-token sequences."""
@@ -94,6 +151,7 @@ def test_decode_workload_matches_oracle_and_scan():
     rms_h = fs_scan.pow(2).mean().sqrt()
     err_h = ((fs_scan - state).abs() / torch.maximum(fs_scan.abs(), rms_h)).max().item()
     assert err_h <= TOL[shape.dtype]
+    assert ssm.ssm_step_check() == ssm.SSM_OK
 
 
 def test_prefill_then_decode_continues_the_state():
