@@ -133,9 +133,10 @@ __global__ void __launch_bounds__(kBlock) step_kernel(const StepArgs p, int64_t 
 
 
 // ------------------------------------------------------------ pipelined kernel
-constexpr int kPipeThreads = 512;  // items (row, quad) per tile = threads per CTA
-constexpr int kPipeStages = 4;     // tiles in shared memory per CTA
-constexpr int kPipeBarBytes = 128; // mbarriers (one per stage + one never-completed) at the front
+constexpr int kTileFloats = 2048;   // fp32 state per tile: 8 KB
+constexpr int kPipeStages = 6;      // tiles in shared memory per CTA
+constexpr int kRefillLag = 2;       // a tile's buffer is refilled this many tiles after its store was issued
+constexpr int kPipeBarBytes = 128;  // mbarriers (one per stage + one never-completed) at the front
 
 __device__ unsigned g_step_error;  // sticky: a pipelined step gave up waiting (read by ssm_step_check)
 
@@ -187,14 +188,42 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-template <typename T, int QR>
-struct PipeLayout {
-  static constexpr int kRows = kPipeThreads / QR;                  // rows per tile
-  static constexpr int kStateBytes = kPipeThreads * 16;            // 8 KB
-  static constexpr int kInBytes = kRows * (int)sizeof(T);          // one of x / Δ / z per tile
-  static constexpr int kStageBytes = kStateBytes + 3 * kInBytes;   // multiple of 16
+// Tile geometry for d_state = N: a thread holds SPT = min(N, 16) states of one
+// row, TPR = N / SPT threads share a row, a tile is kRows = 2048 / N rows
+// (8 KB of state) of one batch row.  Per stage, shared memory holds the state
+// tile, x / Δ / z of its rows and B / C of its batch, all bulk-copied.
+template <typename T, int N>
+struct RowTile {
+  static constexpr int SPT = N < 16 ? N : 16;
+  static constexpr int TPR = N / SPT;
+  static constexpr int Q = SPT / 4;  // float4 groups per thread
+  static constexpr int kRows = kTileFloats / N;
+  static constexpr int kThreads = kRows * TPR;
+  static constexpr int kMinBlocks = 512 / kThreads > 0 ? 512 / kThreads : 1;
+  static constexpr int kStateBytes = kTileFloats * 4;
+  static constexpr int kInBytes = kRows * (int)sizeof(T);  // x, Δ or z of the tile's rows
+  static constexpr int kBCBytes = N * (int)sizeof(T);      // B or C of the tile's batch
+  static constexpr int kOffX = kStateBytes, kOffD = kOffX + kInBytes, kOffZ = kOffD + kInBytes;
+  static constexpr int kOffB = kOffZ + kInBytes, kOffC = kOffB + kBCBytes;
+  static constexpr int kStageBytes = kOffC + kBCBytes;
   static constexpr int kSmemBytes = kPipeBarBytes + kPipeStages * kStageBytes;
+  static_assert(kInBytes % 16 == 0 && kBCBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
 };
+
+// Four consecutive activation values read from shared memory as one vector.
+template <typename T>
+__device__ __forceinline__ void load4(const T* p, float (&v)[4]) {
+  if constexpr (sizeof(T) == 2) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    v[0] = __uint_as_float(w.x << 16);
+    v[1] = __uint_as_float(w.x & 0xffff0000u);
+    v[2] = __uint_as_float(w.y << 16);
+    v[3] = __uint_as_float(w.y & 0xffff0000u);
+  } else {
+    const float4 w = *reinterpret_cast<const float4*>(p);
+    v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+  }
+}
 
 struct PipeArgs {
   StepArgs a;
@@ -204,18 +233,22 @@ struct PipeArgs {
 };
 
 // CTA j owns channel block cb = j mod ncb for its whole life and walks the batch
-// rows b = j / ncb, + gridDim / ncb, ...: a tile is (b, cb), kRows consecutive
-// rows of one batch.  A, bias and D of its channels are loaded once; B and C of
-// the next tile's batch are fetched into registers while the current tile runs.
-template <typename T, int QR, bool HAS_Z>
-__global__ void __launch_bounds__(kPipeThreads) step_pipe_kernel(const PipeArgs pa) {
+// rows b = j / ncb, + gridDim / ncb, ...: a tile is (b, cb).  A, bias and D of its
+// channels are loaded once.  Thread t reads its SPT states as float4 groups in
+// the rotated order (k + rot) mod Q, so that the eight lanes of each shared-memory
+// phase hit eight different bank groups; A, B and C are taken in the same order.
+template <typename T, int N, bool HAS_Z>
+__global__ void __launch_bounds__(RowTile<T, N>::kThreads, RowTile<T, N>::kMinBlocks)
+    step_pipe_kernel(const PipeArgs pa) {
   using AT = Act<T>;
-  using LY = PipeLayout<T, QR>;
-  constexpr int N = 4 * QR;
+  using RT = RowTile<T, N>;
+  constexpr int SPT = RT::SPT, TPR = RT::TPR, Q = RT::Q;
   extern __shared__ __align__(128) unsigned char smem[];
   const StepArgs& p = pa.a;
   const int t = threadIdx.x;
-  const int r = t / QR, q = t % QR;
+  const int r = t / TPR;                   // row within the tile
+  const int n0 = (t % TPR) * SPT;          // first state of this thread
+  const int rot = (t * SPT / 32) & (Q - 1);
   const unsigned bar0 = smem_u32(smem);
   const unsigned stage0 = bar0 + kPipeBarBytes;
   const unsigned long long deadline = globaltimer_ns() + pa.timeout_ns;
@@ -223,29 +256,26 @@ __global__ void __launch_bounds__(kPipeThreads) step_pipe_kernel(const PipeArgs 
   const int64_t cb = blockIdx.x % pa.ncb;
   const int64_t b0 = blockIdx.x / pa.ncb, bstride = gridDim.x / pa.ncb;
   const int my_tiles = b0 < p.batch ? (int)((p.batch - 1 - b0) / bstride + 1) : 0;
-  const int64_t c = cb * LY::kRows + r;
-  auto row0_of = [&](int i) { return (b0 + (int64_t)i * bstride) * p.d_inner + cb * LY::kRows; };
+  const int64_t c = cb * RT::kRows + r;
+  auto batch_of = [&](int i) { return b0 + (int64_t)i * bstride; };
   const uint8_t* xg = static_cast<const uint8_t*>(p.x);
   const uint8_t* dg = static_cast<const uint8_t*>(p.delta);
   const uint8_t* zg = static_cast<const uint8_t*>(p.z);
-  auto issue = [&](int s, int64_t row0) {  // one thread
-    const unsigned st = stage0 + s * LY::kStageBytes;
+  const uint8_t* bg = static_cast<const uint8_t*>(p.B);
+  const uint8_t* cg = static_cast<const uint8_t*>(p.C);
+  auto issue = [&](int s, int i) {  // one thread: all copies of tile i into stage s
+    const unsigned st = stage0 + s * RT::kStageBytes;
     const unsigned bar = bar0 + 8 * s;
-    mbar_expect_tx(bar, LY::kStateBytes + (HAS_Z ? 3 : 2) * LY::kInBytes);
-    bulk_load(st, p.state + row0 * N, LY::kStateBytes, bar);
-    bulk_load(st + LY::kStateBytes, xg + row0 * (int64_t)sizeof(T), LY::kInBytes, bar);
-    bulk_load(st + LY::kStateBytes + LY::kInBytes, dg + row0 * (int64_t)sizeof(T), LY::kInBytes, bar);
-    if (HAS_Z) bulk_load(st + LY::kStateBytes + 2 * LY::kInBytes, zg + row0 * (int64_t)sizeof(T), LY::kInBytes, bar);
-  };
-  auto load_bc = [&](int i, float (&bv)[4], float (&cv)[4]) {
-    const int64_t b = b0 + (int64_t)i * bstride;
-    const T* bp = static_cast<const T*>(p.B) + b * N + 4 * q;
-    const T* cp = static_cast<const T*>(p.C) + b * N + 4 * q;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      bv[k] = AT::load(bp + k);
-      cv[k] = AT::load(cp + k);
-    }
+    const int64_t b = batch_of(i);
+    const int64_t row0 = b * p.d_inner + cb * RT::kRows;
+    constexpr int64_t E = sizeof(T);
+    mbar_expect_tx(bar, RT::kStateBytes + (HAS_Z ? 3 : 2) * RT::kInBytes + 2 * RT::kBCBytes);
+    bulk_load(st, p.state + row0 * N, RT::kStateBytes, bar);
+    bulk_load(st + RT::kOffX, xg + row0 * E, RT::kInBytes, bar);
+    bulk_load(st + RT::kOffD, dg + row0 * E, RT::kInBytes, bar);
+    if (HAS_Z) bulk_load(st + RT::kOffZ, zg + row0 * E, RT::kInBytes, bar);
+    bulk_load(st + RT::kOffB, bg + b * N * E, RT::kBCBytes, bar);
+    bulk_load(st + RT::kOffC, cg + b * N * E, RT::kBCBytes, bar);
   };
 
   if (t == 0) {
@@ -254,59 +284,77 @@ __global__ void __launch_bounds__(kPipeThreads) step_pipe_kernel(const PipeArgs 
   }
   __syncthreads();
   if (t == 0)
-    for (int i = 0; i < my_tiles && i < kPipeStages; ++i) issue(i, row0_of(i));
+    for (int i = 0; i < my_tiles && i < kPipeStages; ++i) issue(i, i);
 
-  // per-channel constants, once per CTA
-  const float4 a4 = my_tiles > 0 ? __ldg(reinterpret_cast<const float4*>(p.A + c * N) + q)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-  const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+  // per-channel constants, once per CTA, in this thread's rotated state order
+  float a2[SPT], ia[SPT], av[AT::kFast ? 1 : SPT];  // A·log2e, 1/A (0 where |A| < 2^-60: Ā = 1, B̄ = Δ B)
+  bool zero_a = false;
+#pragma unroll
+  for (int k = 0; k < Q; ++k) {
+    const int qq = (k + rot) & (Q - 1);
+    const float4 a4 = my_tiles > 0 ? __ldg(reinterpret_cast<const float4*>(p.A + c * N + n0) + qq)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float a[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool z0 = fabsf(a[j]) < 8.673617e-19f;
+      zero_a |= z0;
+      a2[4 * k + j] = z0 ? 0.f : a[j] * kLog2e;
+      ia[4 * k + j] = z0 ? 0.f : 1.f / a[j];
+      if constexpr (!AT::kFast) av[4 * k + j] = a[j];
+    }
+  }
   const float biasc = (p.bias && my_tiles > 0) ? __ldg(p.bias + c) : 0.f;
   const float Dc = (p.D && my_tiles > 0) ? __ldg(p.D + c) : 0.f;
-  float bn[4] = {0.f, 0.f, 0.f, 0.f}, cn[4] = {0.f, 0.f, 0.f, 0.f};
-  if (my_tiles > 0) load_bc(0, bn, cn);
 
   int i = 0;
   bool failed = false;
   for (; i < my_tiles; ++i) {
     const int s = i % kPipeStages;
-    const int64_t row0 = row0_of(i);
-    const float bv[4] = {bn[0], bn[1], bn[2], bn[3]};
-    const float cv[4] = {cn[0], cn[1], cn[2], cn[3]};
-    if (i + 1 < my_tiles) load_bc(i + 1, bn, cn);
-
+    const int64_t row0 = batch_of(i) * p.d_inner + cb * RT::kRows;
     const unsigned wait_bar = (pa.fault && i == 0) ? bar0 + 8 * kPipeStages : bar0 + 8 * s;
     const bool ok = mbar_wait(wait_bar, (unsigned)(i / kPipeStages) & 1u, deadline);
-    unsigned char* st = smem + kPipeBarBytes + s * LY::kStageBytes;
-    float4* hp = reinterpret_cast<float4*>(st) + t;
-    const T* xs = reinterpret_cast<const T*>(st + LY::kStateBytes);
-    const T* ds = reinterpret_cast<const T*>(st + LY::kStateBytes + LY::kInBytes);
-    const T* zs = reinterpret_cast<const T*>(st + LY::kStateBytes + 2 * LY::kInBytes);
-    float4 h4 = *hp;
-    float hs[4] = {h4.x, h4.y, h4.z, h4.w};
-    const float x = AT::to_f(xs[r]);
-    const float rr = AT::to_f(ds[r]) + biasc;
+    unsigned char* st = smem + kPipeBarBytes + s * RT::kStageBytes;
+    float4* hq = reinterpret_cast<float4*>(st) + t * Q;
+    const T* bs = reinterpret_cast<const T*>(st + RT::kOffB) + n0;
+    const T* cs = reinterpret_cast<const T*>(st + RT::kOffC) + n0;
+    const float x = AT::to_f(reinterpret_cast<const T*>(st + RT::kOffX)[r]);
+    const float rr = AT::to_f(reinterpret_cast<const T*>(st + RT::kOffD)[r]) + biasc;
     const float dlt = AT::kFast ? softplus_fast(rr) : softplus_precise(rr);
     float y = 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float a = av[k];
-      if (fabsf(a) < 8.673617e-19f) {
-        hs[k] = fmaf(dlt * x, bv[k], hs[k]);  // A = 0: Ā = 1, B̄ = Δ B
-      } else if (AT::kFast) {
-        const float em1 = ex2_approx(dlt * (a * kLog2e)) - 1.f;
-        hs[k] = fmaf(em1, fmaf(x * (1.f / a), bv[k], hs[k]), hs[k]);
-      } else {
-        const float em1 = expm1f(dlt * a);
-        hs[k] = fmaf(em1, fmaf(x * (1.f / a), bv[k], hs[k]), hs[k]);
-      }
-      y = fmaf(cv[k], hs[k], y);
-    }
-    *hp = make_float4(hs[0], hs[1], hs[2], hs[3]);
+    for (int k = 0; k < Q; ++k) {
+      const int qq = (k + rot) & (Q - 1);
+      const float4 h4 = hq[qq];
+      float h[4] = {h4.x, h4.y, h4.z, h4.w}, bb[4], cc[4];
+      load4<T>(bs + 4 * qq, bb);
+      load4<T>(cs + 4 * qq, cc);
 #pragma unroll
-    for (int off = QR / 2; off > 0; off >>= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
-    if (q == 0 && ok) {
+      for (int j = 0; j < 4; ++j) {
+        const int n = 4 * k + j;
+        if (AT::kFast && !zero_a) {
+          const float em1 = ex2_approx(dlt * a2[n]) - 1.f;
+          h[j] = fmaf(em1, fmaf(x * ia[n], bb[j], h[j]), h[j]);
+        } else if (a2[n] == 0.f) {
+          h[j] = fmaf(dlt * x, bb[j], h[j]);  // A = 0: Ā = 1, B̄ = Δ B
+        } else {
+          float em1;
+          if constexpr (AT::kFast) em1 = ex2_approx(dlt * a2[n]) - 1.f;
+          else em1 = expm1f(dlt * av[n]);
+          h[j] = fmaf(em1, fmaf(x * ia[n], bb[j], h[j]), h[j]);
+        }
+        y = fmaf(cc[j], h[j], y);
+      }
+      hq[qq] = make_float4(h[0], h[1], h[2], h[3]);
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
+    if (n0 == 0 && ok) {
       y = fmaf(Dc, x, y);
-      if (HAS_Z) y *= AT::kFast ? silu_fast(AT::to_f(zs[r])) : silu_precise(AT::to_f(zs[r]));
+      if (HAS_Z) {
+        const float zv = AT::to_f(reinterpret_cast<const T*>(st + RT::kOffZ)[r]);
+        y *= AT::kFast ? silu_fast(zv) : silu_precise(zv);
+      }
       static_cast<T*>(p.out)[row0 + r] = AT::from_f(y);
     }
     fence_async_smem();  // the bulk store below reads what the threads wrote
@@ -315,20 +363,22 @@ __global__ void __launch_bounds__(kPipeThreads) step_pipe_kernel(const PipeArgs 
       break;
     }
     if (t == 0) {
-      bulk_store(p.state + row0 * N, stage0 + s * LY::kStageBytes, LY::kStateBytes);
-      bulk_commit();
-      // refill the previous tile's buffer once its store has read it
-      if (i >= 1 && i - 1 + kPipeStages < my_tiles) {
-        bulk_wait_read<1>();
-        issue((i - 1) % kPipeStages, row0_of(i - 1 + kPipeStages));
+      // refill the buffer of tile j = i - kRefillLag once its store has read it,
+      // ahead of this tile's store in the copy queue
+      const int j = i - kRefillLag;
+      if (j >= 0 && j + kPipeStages < my_tiles) {
+        bulk_wait_read<kRefillLag - 1>();
+        issue(j % kPipeStages, j + kPipeStages);
       }
+      bulk_store(p.state + row0 * N, stage0 + s * RT::kStageBytes, RT::kStateBytes);
+      bulk_commit();
     }
   }
   if (t == 0) {
     if (failed) {
       atomicOr(&g_step_error, 1u);
       // let every load still in flight land before the CTA's shared memory is released
-      const int last = min(my_tiles, (i >= 1 ? i - 1 : 0) + kPipeStages);
+      const int last = min(my_tiles, max(kPipeStages, i - kRefillLag + kPipeStages));  // tiles issued so far
       for (int j = i; j < last; ++j)
         mbar_wait(bar0 + 8 * (j % kPipeStages), (unsigned)(j / kPipeStages) & 1u,
                   globaltimer_ns() + pa.timeout_ns);
@@ -337,14 +387,14 @@ __global__ void __launch_bounds__(kPipeThreads) step_pipe_kernel(const PipeArgs 
   }
 }
 
-template <typename T, int QR>
-cudaError_t launch_pipe_q(const PipeArgs& pa, cudaStream_t stream) {
-  using LY = PipeLayout<T, QR>;
+template <typename T, int N>
+cudaError_t launch_pipe_n(const PipeArgs& pa, cudaStream_t stream) {
+  using RT = RowTile<T, N>;
   // per device and instantiation: shared-memory opt-in and resident CTAs per SM, set up once
   constexpr int kMaxDev = 64;
   static int grid_cap[2][kMaxDev] = {};
   const bool has_z = pa.a.z != nullptr;
-  auto kern = has_z ? step_pipe_kernel<T, QR, true> : step_pipe_kernel<T, QR, false>;
+  auto kern = has_z ? step_pipe_kernel<T, N, true> : step_pipe_kernel<T, N, false>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -354,8 +404,9 @@ cudaError_t launch_pipe_q(const PipeArgs& pa, cudaStream_t stream) {
     int sms = 0, per_sm = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kSmemBytes);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPipeThreads, LY::kSmemBytes);
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RT::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, RT::kThreads, RT::kSmemBytes);
     if (e != cudaSuccess) return e;
     cap = sms * std::max(per_sm, 1);
   }
@@ -363,32 +414,34 @@ cudaError_t launch_pipe_q(const PipeArgs& pa, cudaStream_t stream) {
   const int64_t per_cb = std::max<int64_t>(1, std::min<int64_t>(pa.a.batch, cap / pa.ncb));
   const int64_t grid = pa.ncb * per_cb;
   if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)grid, kPipeThreads, LY::kSmemBytes, stream>>>(pa);
+  kern<<<(unsigned)grid, RT::kThreads, RT::kSmemBytes, stream>>>(pa);
   return cudaGetLastError();
 }
 
 // The pipelined kernel takes the step when its tiles fit the shape exactly and
-// every bulk-copied array is 16-byte aligned; otherwise step_kernel does.
+// every bulk-copied array is 16-byte aligned with 16-byte rows of B and C;
+// otherwise step_kernel does.
 template <typename T>
 bool pipe_launch_dt(const StepArgs& a, const StepKnobs& k, cudaStream_t stream, cudaError_t* err) {
   const int N = (int)a.N;
   if (k.force_plain) return false;
   if (N != 4 && N != 8 && N != 16 && N != 32 && N != 64) return false;
-  const int rows_per_tile = kPipeThreads / (N / 4);
+  if ((N * (int)sizeof(T)) % 16 != 0) return false;  // B, C rows of one batch
+  const int rows_per_tile = kTileFloats / N;
   if (a.d_inner % rows_per_tile != 0) return false;
   auto al = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
-  if (!al(a.state) || !al(a.x) || !al(a.delta) || (a.z && !al(a.z))) return false;
+  if (!al(a.state) || !al(a.x) || !al(a.delta) || (a.z && !al(a.z)) || !al(a.B) || !al(a.C)) return false;
   PipeArgs pa{};
   pa.a = a;
   pa.ncb = a.d_inner / rows_per_tile;
   pa.timeout_ns = k.timeout_ns > 0 ? (unsigned long long)k.timeout_ns : 1000000000ull;
   pa.fault = k.fault ? 1 : 0;
   switch (N) {
-    case 4: *err = launch_pipe_q<T, 1>(pa, stream); break;
-    case 8: *err = launch_pipe_q<T, 2>(pa, stream); break;
-    case 16: *err = launch_pipe_q<T, 4>(pa, stream); break;
-    case 32: *err = launch_pipe_q<T, 8>(pa, stream); break;
-    default: *err = launch_pipe_q<T, 16>(pa, stream); break;
+    case 4: *err = launch_pipe_n<T, (sizeof(T) == 4 ? 4 : 8)>(pa, stream); break;  // bf16 N = 4 excluded above
+    case 8: *err = launch_pipe_n<T, 8>(pa, stream); break;
+    case 16: *err = launch_pipe_n<T, 16>(pa, stream); break;
+    case 32: *err = launch_pipe_n<T, 32>(pa, stream); break;
+    default: *err = launch_pipe_n<T, 64>(pa, stream); break;
   }
   return true;
 }
