@@ -107,6 +107,25 @@ SSM_API ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A
                         size_t workspace_bytes, ssm_stream_t stream);
 
 /*
+ * ssm_scan_fwd starting from a given state instead of h = 0: the scan of a
+ * sequence that continues an earlier one (a prompt processed in pieces, or a
+ * prefill resumed from a decode state), the state being carried between the
+ * two modes as "State Space Models（SSM）とMamba" §2.4 二つのモード and
+ * "Mambaとは？Transformer以外の系列モデル", section training、prefill、decodeでは
+ * 計算の姿が違う describe.  Scanning [0, L) equals scanning [0, k) and then
+ * [k, L) from the first call's final_state.
+ *   initial_state: [batch][d_inner][d_state] float32, required, 4-byte aligned,
+ *     read only.  final_state may be the same array (the state is then updated
+ *     in place); any other overlap with an output is not allowed.
+ *   All other arguments, the workspace and the errors as for ssm_scan_fwd.
+ */
+SSM_API ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, const float* A, const void* B,
+                                   const void* C, const float* D, const void* z, const float* delta_bias,
+                                   const float* initial_state, void* out, float* final_state,
+                                   const ssm_dims* dims, void* workspace, size_t workspace_bytes,
+                                   ssm_stream_t stream);
+
+/*
  * Recurrent (decode) mode: one token for every (batch, channel) row, updating
  * `state` in place (h ← Ā h + B̄ x) and writing out = (C·h + D x) · silu(z).
  *   state, x, delta, A, B, C, out, dims: required (dims->seqlen is ignored).

@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "SsmError", "ssm_scan_workspace_bytes", "ssm_scan_fwd", "ssm_step", "ssm_scan_check",
     "ssm_status_string", "scan_fwd", "step", "library_path", "load_library", "ssm_scan_fwd_noalloc",
-    "SSM_NOALLOC_SCRATCH_BYTES", "ssm_step_check",
+    "SSM_NOALLOC_SCRATCH_BYTES", "ssm_step_check", "ssm_scan_fwd_from_state",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -66,6 +66,8 @@ def load_library():
             lib.ssm_scan_workspace_bytes.restype = sz
             lib.ssm_scan_fwd.argtypes = [vp] * 10 + [dp, vp, sz, vp]
             lib.ssm_scan_fwd.restype = i32
+            lib.ssm_scan_fwd_from_state.argtypes = [vp] * 11 + [dp, vp, sz, vp]
+            lib.ssm_scan_fwd_from_state.restype = i32
             lib.ssm_step.argtypes = [vp] * 10 + [dp, vp]
             lib.ssm_step.restype = i32
             lib.ssm_scan_check.argtypes = [vp, sz]
@@ -122,8 +124,10 @@ def ssm_scan_workspace_bytes(batch, d_inner, d_state, seqlen, dtype=torch.bfloat
     return int(load_library().ssm_scan_workspace_bytes(ctypes.byref(d)))
 
 
-def ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, out, final_state, workspace=None, stream=None):
-    """Parallel-mode scan into caller-provided ``out`` (and ``final_state``)."""
+def ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, out, final_state, workspace=None, stream=None,
+                 initial_state=None):
+    """Parallel-mode scan into caller-provided ``out`` (and ``final_state``),
+    from h = 0, or from ``initial_state`` (ssm_scan_fwd_from_state) when given."""
     lib = load_library()
     if not isinstance(u, torch.Tensor) or u.dim() != 3:
         raise ValueError("u must be a [batch, d_inner, seqlen] tensor")
@@ -144,18 +148,33 @@ def ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, out, final_state, workspac
     _check(delta_bias, "delta_bias", torch.float32, (d_inner,), dev, required=False)
     _check(out, "out", act, (batch, d_inner, L), dev)
     _check(final_state, "final_state", torch.float32, (batch, d_inner, N), dev, required=False)
+    _check(initial_state, "initial_state", torch.float32, (batch, d_inner, N), dev, required=False)
     dims = _dims(batch, d_inner, N, L, act)
     with torch.cuda.device(dev):
         need = int(lib.ssm_scan_workspace_bytes(ctypes.byref(dims)))
         if workspace is None and need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-        st = lib.ssm_scan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-                              _ptr(delta_bias), _ptr(out), _ptr(final_state), ctypes.byref(dims),
-                              _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
+        tail = (ctypes.byref(dims), _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
+        if initial_state is None:
+            st = lib.ssm_scan_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                  _ptr(delta_bias), _ptr(out), _ptr(final_state), *tail)
+        else:
+            st = lib.ssm_scan_fwd_from_state(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                             _ptr(delta_bias), _ptr(initial_state), _ptr(out), _ptr(final_state),
+                                             *tail)
     if st != SSM_OK:
-        raise SsmError(st, "ssm_scan_fwd")
+        raise SsmError(st, "ssm_scan_fwd" if initial_state is None else "ssm_scan_fwd_from_state")
     return workspace
+
+
+def ssm_scan_fwd_from_state(u, delta, A, B, C, D, z, delta_bias, initial_state, out, final_state,
+                            workspace=None, stream=None):
+    """The scan starting from ``initial_state`` (same arguments as the C call)."""
+    if initial_state is None:
+        raise ValueError("initial_state is required")
+    return ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, out, final_state, workspace=workspace,
+                        stream=stream, initial_state=initial_state)
 
 
 def ssm_scan_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, out, final_state, stream=None):
@@ -228,13 +247,15 @@ def ssm_step_check(stream=None, device=None) -> int:
 
 
 def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, return_final_state=False,
-             workspace=None, stream=None):
-    """Allocate ``out`` (and ``final_state``) and run ``ssm_scan_fwd``."""
+             workspace=None, stream=None, initial_state=None):
+    """Allocate ``out`` (and ``final_state``) and run ``ssm_scan_fwd`` (from
+    ``initial_state`` when given)."""
     out = torch.empty_like(u)
     fs = None
     if return_final_state:
         fs = torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
-    ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, out, fs, workspace=workspace, stream=stream)
+    ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, out, fs, workspace=workspace, stream=stream,
+                 initial_state=initial_state)
     return (out, fs) if return_final_state else out
 
 

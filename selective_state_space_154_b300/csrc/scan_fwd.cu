@@ -255,7 +255,8 @@ __global__ void __launch_bounds__(512, 1) scan_fwd_kernel(const KParams p) {
     a_[k] = tiny ? 0.f : av;
     a2[k] = a_[k] * kLog2e;
     ia[k] = tiny ? 0.f : 1.f / av;
-    h[k] = 0.f;
+    // the first chunk starts from the initial state; later chunks start from 0 and take their carry
+    h[k] = (chunk == 0 && p.a.h0 && row_ok && n < N) ? p.a.h0[row * N + n] : 0.f;
   }
   float S = 0.f;  // Σ Δ over the chunk so far (same for all threads of a row)
 

@@ -431,7 +431,8 @@ __global__ void __launch_bounds__(RowCta<RB, TPR>::kThreads, RowCta<RB, TPR>::kM
     if (row_ok && n0 + n < N && tiny) precise = true;
     a2[n] = tiny ? 0.f : a * kLog2e;
     ia[n] = tiny ? 0.f : 1.f / a;
-    h[n] = 0.f;
+    // the first chunk starts from the initial state; later chunks start from 0 and take their carry
+    h[n] = (chunk == 0 && p.a.h0 && row_ok && n0 + n < N) ? p.a.h0[row * N + n0 + n] : 0.f;
   }
   // a row's threads take the same path (the precise one if any of its states has A = 0)
   if (TPR > 1) {

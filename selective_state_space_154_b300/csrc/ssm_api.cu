@@ -63,10 +63,10 @@ ssm_status check_dims(const ssm_dims* d, bool need_len) {
 
 ssm::ScanArgs scan_args(const void* u, const void* delta, const float* A, const void* B, const void* C,
                         const float* D, const void* z, const float* bias, void* out, float* fs,
-                        const ssm_dims* d, void* ws) {
+                        const ssm_dims* d, void* ws, const float* h0 = nullptr) {
   ssm::ScanArgs a{};
   a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.bias = bias;
-  a.out = out; a.final_state = fs;
+  a.out = out; a.final_state = fs; a.h0 = h0;
   a.batch = d->batch; a.d_inner = d->d_inner; a.N = d->d_state; a.L = d->seqlen;
   a.act = d->act;
   a.ws = static_cast<unsigned char*>(ws);
@@ -92,10 +92,14 @@ size_t ssm_scan_workspace_bytes(const ssm_dims* dims) {
   return plan.ws_bytes > plan2.ws_bytes ? plan.ws_bytes : plan2.ws_bytes;
 }
 
-ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
-                        const float* D, const void* z, const float* delta_bias, void* out,
-                        float* final_state, const ssm_dims* dims, void* workspace, size_t workspace_bytes,
-                        ssm_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+ssm_status scan_fwd_impl(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                         const float* D, const void* z, const float* delta_bias, const float* h0, void* out,
+                         float* final_state, const ssm_dims* dims, void* workspace, size_t workspace_bytes,
+                         ssm_stream_t stream) {
   const ssm_status ds = check_dims(dims, true);
   if (ds != SSM_OK) return ds;
   if (!u || !delta || !A || !B || !C || !out) return SSM_ERR_INVALID_ARG;
@@ -104,10 +108,10 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
   const void* act_ptrs[] = {u, delta, B, C, z, out};
   for (const void* p : act_ptrs)
     if (p && !aligned(p, esz)) return SSM_ERR_ALIGNMENT;
-  const void* f32_ptrs[] = {A, D, delta_bias, final_state};
+  const void* f32_ptrs[] = {A, D, delta_bias, final_state, h0};
   for (const void* p : f32_ptrs)
     if (p && !aligned(p, 4)) return SSM_ERR_ALIGNMENT;
-  ssm::ScanArgs a = scan_args(u, delta, A, B, C, D, z, delta_bias, out, final_state, dims, workspace);
+  ssm::ScanArgs a = scan_args(u, delta, A, B, C, D, z, delta_bias, out, final_state, dims, workspace, h0);
   ssm::ScanPlan plan;
   if (!ssm::scan_make_plan(a, &plan)) return SSM_ERR_UNSUPPORTED;
   if (plan.ws_bytes > 0) {
@@ -121,6 +125,28 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
   }
   const cudaError_t e = ssm::scan_launch(a, plan, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* delta_bias, void* out,
+                        float* final_state, const ssm_dims* dims, void* workspace, size_t workspace_bytes,
+                        ssm_stream_t stream) {
+  return scan_fwd_impl(u, delta, A, B, C, D, z, delta_bias, nullptr, out, final_state, dims, workspace,
+                       workspace_bytes, stream);
+}
+
+ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, const float* A, const void* B,
+                                   const void* C, const float* D, const void* z, const float* delta_bias,
+                                   const float* initial_state, void* out, float* final_state,
+                                   const ssm_dims* dims, void* workspace, size_t workspace_bytes,
+                                   ssm_stream_t stream) {
+  if (!initial_state) return SSM_ERR_INVALID_ARG;
+  return scan_fwd_impl(u, delta, A, B, C, D, z, delta_bias, initial_state, out, final_state, dims, workspace,
+                       workspace_bytes, stream);
 }
 
 ssm_status ssm_step(float* state, const void* x, const void* delta, const float* A, const void* B,

@@ -50,6 +50,7 @@ struct ScanArgs {
   const float* bias;
   void* out;
   float* final_state;
+  const float* h0;  // initial state [batch][d_inner][N], or nullptr for h = 0
   int64_t batch, d_inner, N, L;
   int act;  // 0 fp32, 1 bf16
   unsigned char* ws;

@@ -140,3 +140,21 @@ def test_binding_fails_loudly_without_cuda_tensors():
     u = torch.zeros(1, 1, 8)
     with pytest.raises(ValueError):
         ssm.scan_fwd(u, u, torch.zeros(1, 4), torch.zeros(1, 8, 4), torch.zeros(1, 8, 4))
+
+
+def _scan_from(lib, dims, h0, ptrs=None):
+    p = dict(u=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, bias=None, out=FAKE, fs=None)
+    p.update(ptrs or {})
+    a = [ctypes.c_void_p(p[k]) if p[k] else None for k in ("u", "delta", "A", "B", "C", "D", "z", "bias")]
+    tail = [ctypes.c_void_p(p[k]) if p[k] else None for k in ("out", "fs")]
+    return lib.ssm_scan_fwd_from_state(*a, ctypes.c_void_p(h0) if h0 else None, *tail, ctypes.byref(dims),
+                                       None, 0, None)
+
+
+def test_scan_from_state_validates_the_initial_state(lib):
+    assert _scan_from(lib, _dims(), None) == ssm.SSM_ERR_INVALID_ARG       # required
+    assert _scan_from(lib, _dims(), FAKE + 2) == ssm.SSM_ERR_ALIGNMENT     # float32: 4-byte aligned
+    d = _dims()
+    d.seqlen = 0
+    assert _scan_from(lib, d, FAKE) == ssm.SSM_ERR_INVALID_ARG             # dims checked as for ssm_scan_fwd
+    assert _scan_from(lib, _dims(), FAKE, {"u": None}) == ssm.SSM_ERR_INVALID_ARG

@@ -67,6 +67,50 @@ def full_compare(inp, tol):
     return e_out, e_fs
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("chunks", [0, 3], ids=["planned", "3chunks"])
+def test_initial_state(dtype, chunks, kernel, monkeypatch):
+    """ssm_scan_fwd_from_state against the oracle started from the same h0."""
+    if chunks:
+        monkeypatch.setenv("SSM_FORCE_CHUNKS", str(chunks))
+    b, d, N, L = 2, 70, 16, 700
+    inp = W.random_scan_inputs(b, d, N, L, dtype=dtype, device=DEV, seed=31, a_kind="random")
+    g = torch.Generator(device=DEV).manual_seed(32)
+    h0 = 2.0 * torch.randn((b, d, N), generator=g, device=DEV)
+    out, fs = ssm.scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["bias"],
+                           return_final_state=True, initial_state=h0)
+    ref, href = oracle.scan(*(to_np(inp[k]) for k in ("u", "delta", "A", "B", "C")), D=to_np(inp["D"]),
+                            z=to_np(inp["z"]), bias=to_np(inp["bias"]), h0=to_np(h0))
+    assert rel_err(to_np(out), ref) <= TOL[dtype]
+    assert rel_err(to_np(fs), href) <= TOL[dtype]
+
+
+def test_split_and_continue_matches_one_scan(kernel):
+    """Scanning [0, L) equals scanning [0, k) and continuing [k, L) from its final state,
+    the state updated in place (final_state is the initial_state tensor)."""
+    b, d, N, L, k = 3, 96, 16, 2000, 613
+    inp = W.random_scan_inputs(b, d, N, L, dtype=torch.bfloat16, device=DEV, seed=41, a_kind="random")
+    whole, fs_whole = ssm.scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                   inp["bias"], return_final_state=True)
+    cut = lambda t, lo, hi, axis: t.narrow(axis, lo, hi - lo).contiguous()
+    parts, state = [], None
+    for lo, hi in ((0, k), (k, L)):
+        u, dl, z = (cut(inp[n], lo, hi, 2) for n in ("u", "delta", "z"))
+        B, C = cut(inp["B"], lo, hi, 1), cut(inp["C"], lo, hi, 1)
+        out = torch.empty_like(u)
+        if state is None:
+            state = torch.empty((b, d, N), device=DEV)
+            ssm.ssm_scan_fwd(u, dl, inp["A"], B, C, inp["D"], z, inp["bias"], out, state)
+        else:
+            ssm.ssm_scan_fwd_from_state(u, dl, inp["A"], B, C, inp["D"], z, inp["bias"], state, out, state)
+        parts.append(out)
+    torch.cuda.synchronize()
+    joined = torch.cat(parts, dim=2)
+    rms = float(whole.float().pow(2).mean().sqrt())
+    assert rel_err(to_np(joined), to_np(whole), rms_ref=rms) <= TOL[torch.bfloat16]
+    assert rel_err(to_np(state), to_np(fs_whole)) <= TOL[torch.bfloat16]
+
+
 def test_tiny_fp32_workload(kernel):
     inp = W.scan_inputs(W.SCAN_SHAPES["tiny_fp32"], device=DEV)
     full_compare(inp, TOL[torch.float32])
