@@ -63,6 +63,10 @@ def _load():
             lib.oracle_scan.restype = None
             lib.oracle_step.argtypes = [i64, i64, i64] + [dp] * 10 + [i64, i64]
             lib.oracle_step.restype = None
+            lib.oracle_conv1d.argtypes = [i64, i64, i64, i64] + [dp] * 6 + [i64, i64]
+            lib.oracle_conv1d.restype = None
+            lib.oracle_conv1d_step.argtypes = [i64, i64, i64] + [dp] * 5 + [i64, i64]
+            lib.oracle_conv1d_step.restype = None
             _lib = lib
     return _lib
 
@@ -143,4 +147,47 @@ def step(state, x, delta, A, B, C, D=None, z=None, bias=None, threads: int | Non
     else:
         with ThreadPoolExecutor(len(ranges)) as ex:
             list(ex.map(lambda rg: lib.oracle_step(*args, *rg), ranges))
+    return out, st
+
+
+def conv1d(x, w, bias=None, state0=None, threads: int | None = None):
+    """Causal depthwise Conv1D + SiLU over whole sequences.
+
+    x: [batch, d_inner, L]; w: [d_inner, W]; bias: [d_inner] or None;
+    state0: [batch, d_inner, W-1] (the W-1 inputs before x, oldest first) or None (zeros).
+    Returns (out [batch, d_inner, L], stateT [batch, d_inner, W-1]) as float64 arrays.
+    """
+    x, w, bias, state0 = (_f64(v) for v in (x, w, bias, state0))
+    batch, d_inner, L = x.shape
+    W = w.shape[1]
+    assert w.shape == (d_inner, W) and 1 <= W <= 64
+    assert bias is None or bias.shape == (d_inner,)
+    assert state0 is None or state0.shape == (batch, d_inner, W - 1)
+    out = np.empty((batch, d_inner, L), np.float64)
+    stateT = np.empty((batch, d_inner, W - 1), np.float64)
+    lib = _load()
+    args = [batch, d_inner, L, W] + [_ptr(v) for v in (x, w, bias, state0, out, stateT)]
+    ranges = _row_ranges(batch * d_inner, threads or default_threads())
+    if len(ranges) == 1:
+        lib.oracle_conv1d(*args, *ranges[0])
+    else:
+        with ThreadPoolExecutor(len(ranges)) as ex:
+            list(ex.map(lambda rg: lib.oracle_conv1d(*args, *rg), ranges))
+    return out, stateT
+
+
+def conv1d_step(state, x, w, bias=None):
+    """One decode token of the causal Conv1D + SiLU.
+
+    state: [batch, d_inner, W-1] (not modified; the new state is returned);
+    x: [batch, d_inner]; w: [d_inner, W].  Returns (out [batch, d_inner], new_state).
+    """
+    st = _f64(state).copy()
+    x, w, bias = (_f64(v) for v in (x, w, bias))
+    batch, d_inner = x.shape
+    W = w.shape[1]
+    assert st.shape == (batch, d_inner, W - 1) and w.shape == (d_inner, W)
+    out = np.empty((batch, d_inner), np.float64)
+    lib = _load()
+    lib.oracle_conv1d_step(batch, d_inner, W, *(_ptr(v) for v in (st, x, w, bias, out)), 0, batch * d_inner)
     return out, st

@@ -63,3 +63,21 @@ def step(state, x, delta, A, B, C, D=None, z=None, bias=None):
                   _arr(C)[:, None, :], D, None if z is None else _arr(z)[:, :, None], bias,
                   _arr(state))
     return out[:, :, 0], h
+
+
+def conv1d(x, w, bias=None, state0=None):
+    """Causal depthwise Conv1D + SiLU, vectorised over (batch, channel) and over
+    the W taps: the sequence is prefixed with the W-1 carried inputs (zeros when
+    state0 is None) and tap k multiplies the window shifted by W-1-k
+    ("Mambaとは？Transformer以外の系列モデル", section Mamba blockのarchitecture,
+    steps 2-3)."""
+    x, w, bias, state0 = (_arr(v) for v in (x, w, bias, state0))
+    batch, d, L = x.shape
+    W = w.shape[1]
+    pre_pad = np.zeros((batch, d, W - 1)) if state0 is None else state0
+    xt = np.concatenate([pre_pad, x], axis=2)  # x̃, length L + W - 1
+    pre = np.zeros((batch, d, L)) if bias is None else np.broadcast_to(bias[None, :, None], (batch, d, L)).copy()
+    for k in range(W):
+        pre += w[None, :, k, None] * xt[:, :, k:k + L]
+    out = pre * expit(pre)
+    return out, xt[:, :, L:].copy()

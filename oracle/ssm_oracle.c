@@ -122,3 +122,62 @@ void oracle_step(int64_t batch, int64_t d_inner, int64_t N, double* state,
                    z ? z[r] : 0.0);
   }
 }
+
+/*
+ * Causal depthwise Conv1D followed by SiLU: the short convolution of the Mamba
+ * block's main branch, in front of the selective SSM ("Mambaとは？Transformer以外の
+ * 系列モデル", section Mamba blockのarchitecture, steps 2 and 3: a short causal
+ * Conv1D mixes neighbouring tokens, then SiLU).  Per (batch, channel) row and
+ * width W (the pages give no width or formula; this is the plain reading):
+ *
+ *   pre[t] = bias + Σ_{k=0}^{W-1} w[k] · x̃[t - (W-1) + k]
+ *   out[t] = silu(pre[t])
+ *
+ * where x̃ is x extended to the left by the W-1 inputs that came before it:
+ * state0[0..W-2] (oldest first), or zeros when state0 is NULL.  The state after
+ * the sequence is the last W-1 entries of x̃ ("Mambaとは？…", section
+ * training、prefill、decodeでは計算の姿が違う: in decode each layer keeps its
+ * SSM state and a state for the short causal Conv1D).
+ *
+ * Layouts (row-major, all double): x, out [batch][d_inner][L]; w [d_inner][W];
+ * bias [d_inner] (NULL: 0); state0, stateT [batch][d_inner][W-1].
+ */
+static double conv_input(const double* xr, const double* s0r, int64_t W, int64_t p) {
+  if (p >= 0) return xr[p];
+  return s0r ? s0r[(W - 1) + p] : 0.0;
+}
+
+void oracle_conv1d(int64_t batch, int64_t d_inner, int64_t L, int64_t W, const double* x, const double* w,
+                   const double* bias, const double* state0, double* out, double* stateT, int64_t row_begin,
+                   int64_t row_end) {
+  (void)batch;
+  for (int64_t r = row_begin; r < row_end; ++r) {
+    const int64_t c = r % d_inner;
+    const double* xr = x + r * L;
+    const double* s0r = state0 ? state0 + r * (W - 1) : NULL;
+    for (int64_t t = 0; t < L; ++t) {
+      double pre = bias ? bias[c] : 0.0;
+      for (int64_t k = 0; k < W; ++k) pre += w[c * W + k] * conv_input(xr, s0r, W, t - (W - 1) + k);
+      out[r * L + t] = silu(pre);
+    }
+    if (stateT)
+      for (int64_t j = 0; j < W - 1; ++j) stateT[r * (W - 1) + j] = conv_input(xr, s0r, W, L - (W - 1) + j);
+  }
+}
+
+/* One decode token: window = (state[0..W-2], x); out = silu(bias + Σ w·window);
+ * state ← window[1..W-1].  state [batch][d_inner][W-1] is updated in place. */
+void oracle_conv1d_step(int64_t batch, int64_t d_inner, int64_t W, double* state, const double* x,
+                        const double* w, const double* bias, double* out, int64_t row_begin, int64_t row_end) {
+  (void)batch;
+  double win[64];
+  for (int64_t r = row_begin; r < row_end; ++r) {
+    const int64_t c = r % d_inner;
+    for (int64_t k = 0; k < W - 1; ++k) win[k] = state[r * (W - 1) + k];
+    win[W - 1] = x[r];
+    double pre = bias ? bias[c] : 0.0;
+    for (int64_t k = 0; k < W; ++k) pre += w[c * W + k] * win[k];
+    out[r] = silu(pre);
+    for (int64_t k = 0; k < W - 1; ++k) state[r * (W - 1) + k] = win[k + 1];
+  }
+}
