@@ -148,6 +148,39 @@ SSM_API ssm_status ssm_step(float* state, const void* x, const void* delta, cons
 SSM_API ssm_status ssm_scan_check(const void* workspace, size_t workspace_bytes);
 
 /*
+ * Causal depthwise Conv1D + SiLU over whole sequences: the short convolution of
+ * the Mamba block's main branch that feeds the selective SSM
+ * ("Mambaとは？Transformer以外の系列モデル", section Mamba blockのarchitecture,
+ * steps 2 and 3).  For every (batch, channel) row, with W = width:
+ *   out[t] = silu(bias[c] + Σ_{k<W} weight[c][k] · x̃[t - (W-1) + k])
+ * where x̃ is the row prefixed by the W-1 inputs before it, initial_conv_state
+ * (oldest first), or zeros when it is NULL.  final_conv_state (may be NULL)
+ * receives the last W-1 entries of x̃: the state ssm_conv1d_step continues from.
+ *   x, out: [batch][d_inner][seqlen], act dtype (ssm_dims.act; d_state ignored).
+ *   weight: [d_inner][width] float32; bias: [d_inner] float32 or NULL.
+ *   initial_conv_state, final_conv_state: [batch][d_inner][width-1], act dtype
+ *     (the raw inputs, so they are exact), or NULL; unused when width is 1.
+ *   1 <= width <= 8 (SSM_ERR_UNSUPPORTED above).  Element alignment as for the scan.
+ *   out and final_conv_state must not overlap x, initial_conv_state or each
+ *   other.  No workspace; stream-ordered and asynchronous like ssm_scan_fwd.
+ */
+SSM_API ssm_status ssm_conv1d_fwd(const void* x, const float* weight, const float* bias,
+                                  const void* initial_conv_state, void* out, void* final_conv_state,
+                                  const ssm_dims* dims, int32_t width, ssm_stream_t stream);
+
+/*
+ * One decode token of the same convolution ("Mambaとは？…", section training、
+ * prefill、decodeでは計算の姿が違う: each layer keeps a state for its short causal
+ * Conv1D next to the SSM state).  For every row: window = (conv_state, x);
+ * out = silu(bias + Σ_k weight[c][k] · window[k]); conv_state ← window[1..W-1].
+ *   conv_state: [batch][d_inner][width-1], act dtype, updated in place
+ *     (required unless width is 1).
+ *   x, out: [batch][d_inner], act dtype; weight, bias as for ssm_conv1d_fwd.
+ */
+SSM_API ssm_status ssm_conv1d_step(void* conv_state, const void* x, const float* weight, const float* bias,
+                                   void* out, const ssm_dims* dims, int32_t width, ssm_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears this library's device-side step
  * error word on the current device: SSM_ERR_TIMEOUT if, since the last check,
  * an ssm_step on this device gave up waiting for its state to arrive in shared

@@ -20,6 +20,7 @@ __all__ = [
     "SsmError", "ssm_scan_workspace_bytes", "ssm_scan_fwd", "ssm_step", "ssm_scan_check",
     "ssm_status_string", "scan_fwd", "step", "library_path", "load_library", "ssm_scan_fwd_noalloc",
     "SSM_NOALLOC_SCRATCH_BYTES", "ssm_step_check", "ssm_scan_fwd_from_state",
+    "ssm_conv1d_fwd", "ssm_conv1d_step", "conv1d", "conv1d_step",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -76,6 +77,10 @@ def load_library():
             lib.ssm_step_check.restype = i32
             lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 10 + [dp, vp]
             lib.ssm_scan_fwd_noalloc.restype = i32
+            lib.ssm_conv1d_fwd.argtypes = [vp] * 6 + [dp, i32, vp]
+            lib.ssm_conv1d_fwd.restype = i32
+            lib.ssm_conv1d_step.argtypes = [vp] * 5 + [dp, i32, vp]
+            lib.ssm_conv1d_step.restype = i32
             lib.ssm_status_string.argtypes = [i32]
             lib.ssm_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -230,6 +235,77 @@ def ssm_step(state, x, delta, A, B, C, D, z, delta_bias, out, stream=None):
                           _ptr(delta_bias), _ptr(out), ctypes.byref(dims), _stream_handle(stream, dev))
     if st != SSM_OK:
         raise SsmError(st, "ssm_step")
+
+
+def _conv_dims(x, batch, d_inner, seqlen):
+    return _dims(batch, d_inner, 1, seqlen, x.dtype)
+
+
+def ssm_conv1d_fwd(x, weight, bias, initial_conv_state, out, final_conv_state, stream=None):
+    """Causal depthwise Conv1D + SiLU over [batch, d_inner, L] (see include/ssm_scan.h)."""
+    lib = load_library()
+    if not isinstance(x, torch.Tensor) or x.dim() != 3:
+        raise ValueError("x must be a [batch, d_inner, seqlen] tensor")
+    if not isinstance(weight, torch.Tensor) or weight.dim() != 2:
+        raise ValueError("weight must be a [d_inner, width] tensor")
+    batch, d_inner, L = x.shape
+    width = weight.shape[1]
+    act, dev = x.dtype, x.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    _check(x, "x", act, (batch, d_inner, L), dev)
+    _check(weight, "weight", torch.float32, (d_inner, width), dev)
+    _check(bias, "bias", torch.float32, (d_inner,), dev, required=False)
+    _check(out, "out", act, (batch, d_inner, L), dev)
+    for name, t in (("initial_conv_state", initial_conv_state), ("final_conv_state", final_conv_state)):
+        if t is not None and width > 1:
+            _check(t, name, act, (batch, d_inner, width - 1), dev)
+    dims = _conv_dims(x, batch, d_inner, L)
+    with torch.cuda.device(dev):
+        st = lib.ssm_conv1d_fwd(_ptr(x), _ptr(weight), _ptr(bias), _ptr(initial_conv_state), _ptr(out),
+                                _ptr(final_conv_state), ctypes.byref(dims), int(width), _stream_handle(stream, dev))
+    if st != SSM_OK:
+        raise SsmError(st, "ssm_conv1d_fwd")
+
+
+def ssm_conv1d_step(conv_state, x, weight, bias, out, stream=None):
+    """One decode token of the causal Conv1D + SiLU; ``conv_state`` is updated in place."""
+    lib = load_library()
+    if not isinstance(x, torch.Tensor) or x.dim() != 2:
+        raise ValueError("x must be a [batch, d_inner] tensor")
+    batch, d_inner = x.shape
+    width = weight.shape[1]
+    act, dev = x.dtype, x.device
+    _check(x, "x", act, (batch, d_inner), dev)
+    _check(weight, "weight", torch.float32, (d_inner, width), dev)
+    _check(bias, "bias", torch.float32, (d_inner,), dev, required=False)
+    _check(out, "out", act, (batch, d_inner), dev)
+    if width > 1:
+        _check(conv_state, "conv_state", act, (batch, d_inner, width - 1), dev)
+    dims = _conv_dims(x, batch, d_inner, 1)
+    with torch.cuda.device(dev):
+        st = lib.ssm_conv1d_step(_ptr(conv_state), _ptr(x), _ptr(weight), _ptr(bias), _ptr(out),
+                                 ctypes.byref(dims), int(width), _stream_handle(stream, dev))
+    if st != SSM_OK:
+        raise SsmError(st, "ssm_conv1d_step")
+
+
+def conv1d(x, weight, bias=None, initial_conv_state=None, return_final_state=False, stream=None):
+    """Allocate ``out`` (and the final conv state) and run ``ssm_conv1d_fwd``."""
+    out = torch.empty_like(x)
+    fs = None
+    if return_final_state:
+        fs = torch.empty((x.shape[0], x.shape[1], max(weight.shape[1] - 1, 0)), dtype=x.dtype, device=x.device)
+    ssm_conv1d_fwd(x, weight, bias, initial_conv_state, out, fs, stream=stream)
+    return (out, fs) if return_final_state else out
+
+
+def conv1d_step(conv_state, x, weight, bias=None, out=None, stream=None):
+    """Run ``ssm_conv1d_step`` (state updated in place) and return the output."""
+    if out is None:
+        out = torch.empty_like(x)
+    ssm_conv1d_step(conv_state, x, weight, bias, out, stream=stream)
+    return out
 
 
 def ssm_scan_check(workspace) -> int:

@@ -1,0 +1,246 @@
+// Causal depthwise Conv1D + SiLU for sm_103a: the short convolution of the
+// Mamba block's main branch, in front of the selective SSM
+// ("Mambaとは？Transformer以外の系列モデル", section Mamba blockのarchitecture,
+// steps 2 and 3), and its one-token decode form with the carried state
+// (same page, section training、prefill、decodeでは計算の姿が違う).
+//
+//   pre[t] = bias + Σ_{k<W} w[k] · x̃[t - (W-1) + k],   out[t] = silu(pre[t])
+//
+// x̃ is the row prefixed by the W-1 inputs before it (the carried state, or
+// zeros).  Both kernels are bound by memory: per (row, token) one input read
+// and one output written.
+//
+// conv1d_fwd_kernel: a thread owns 8 consecutive tokens of one row (one 16-byte
+// vector in bf16, two in fp32), a warp 256 consecutive tokens.  The 8 tokens
+// before a thread's own come from the lane to its left by shuffles; lane 0
+// loads them (or takes the carried state at the start of the row).  The thread
+// holding the row's last token writes the final state.
+// conv1d_step_kernel: one thread per row shifts the W-1 carried inputs, appends
+// x and writes out.
+#include <cstdint>
+
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kTok = 8;          // tokens per thread
+constexpr int kConvBlock = 256;  // threads per CTA
+
+template <typename T>
+__device__ __forceinline__ float ld_act(const T* p) {
+  return Act<T>::to_f(*p);
+}
+
+// 8 consecutive values at p (16-byte aligned)
+template <typename T>
+__device__ __forceinline__ void load8_vec(const T* p, float (&v)[kTok]) {
+  if constexpr (sizeof(T) == 2) {
+    const uint4 w = *reinterpret_cast<const uint4*>(p);
+    const unsigned u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(u[i] << 16);
+      v[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+  } else {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void store8_vec(T* p, const float (&v)[kTok]) {
+  if constexpr (sizeof(T) == 2) {
+    unsigned u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      u[i] = *reinterpret_cast<unsigned*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(u[0], u[1], u[2], u[3]);
+  } else {
+    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+}
+
+template <bool FAST>
+__device__ __forceinline__ float silu_c(float v) {
+  return FAST ? silu_fast(v) : silu_precise(v);
+}
+
+struct ConvArgs {
+  const void* x;
+  const float* w;      // [d_inner][W]
+  const float* bias;   // [d_inner] or nullptr
+  const void* state0;  // [rows][W-1] or nullptr
+  void* out;
+  void* stateT;        // [rows][W-1] or nullptr
+  int64_t rows, d_inner, L;
+  int64_t wsegs;       // warps per row: ceil(L / 256)
+  int W;               // taps (runtime copy; the forward kernel is instantiated per width)
+};
+
+template <typename T, int W, bool VEC>
+__global__ void __launch_bounds__(kConvBlock) conv1d_fwd_kernel(const ConvArgs a) {
+  using AT = Act<T>;
+  const int lane = threadIdx.x & 31;
+  const int64_t gwarp = ((int64_t)blockIdx.x * kConvBlock + threadIdx.x) >> 5;
+  const int64_t row = gwarp / a.wsegs;
+  if (row >= a.rows) return;  // rows are warp-uniform
+  const int64_t t0 = ((gwarp % a.wsegs) * 32 + lane) * kTok;
+  const int64_t L = a.L;
+  const int64_t c = row % a.d_inner;
+  const T* xr = static_cast<const T*>(a.x) + row * L;
+  const T* sr = a.state0 ? static_cast<const T*>(a.state0) + row * (W - 1) : nullptr;
+
+  // own 8 tokens (zeros past the end of the row)
+  float cur[kTok];
+  if (VEC && t0 + kTok <= L) {
+    load8_vec<T>(xr + t0, cur);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kTok; ++i) cur[i] = (t0 + i < L) ? ld_act<T>(xr + t0 + i) : 0.f;
+  }
+  // the 8 tokens before: from the lane to the left, or loaded by lane 0
+  float prev[kTok];
+#pragma unroll
+  for (int i = 0; i < kTok; ++i) prev[i] = __shfl_up_sync(0xffffffffu, cur[i], 1);
+  if (lane == 0) {
+    if (t0 >= kTok) {
+      if (VEC) {
+        load8_vec<T>(xr + t0 - kTok, prev);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kTok; ++i) prev[i] = ld_act<T>(xr + t0 - kTok + i);
+      }
+    } else {  // t0 == 0: positions -8..-1 are the carried state (zeros before it)
+#pragma unroll
+      for (int i = 0; i < kTok; ++i) {
+        const int pos = i - kTok;
+        prev[i] = (sr && pos >= -(W - 1)) ? ld_act<T>(sr + (W - 1) + pos) : 0.f;
+      }
+    }
+  }
+  if (t0 >= L) return;
+
+  // window x̃[t0-8 .. t0+7] = (prev, cur); out[t0+j] = silu(bias + Σ_k w[k] x̃[t0+j-(W-1)+k])
+  float win[2 * kTok];
+#pragma unroll
+  for (int i = 0; i < kTok; ++i) {
+    win[i] = prev[i];
+    win[kTok + i] = cur[i];
+  }
+  const float* wc = a.w + c * W;
+  float wk[W];
+#pragma unroll
+  for (int k = 0; k < W; ++k) wk[k] = __ldg(wc + k);
+  const float b0 = a.bias ? __ldg(a.bias + c) : 0.f;
+  float y[kTok];
+#pragma unroll
+  for (int j = 0; j < kTok; ++j) {
+    float pre = b0;
+#pragma unroll
+    for (int k = 0; k < W; ++k) pre = fmaf(wk[k], win[kTok + j - (W - 1) + k], pre);  // index in [1, 15]
+    y[j] = silu_c<AT::kFast>(pre);
+  }
+  T* orow = static_cast<T*>(a.out) + row * L;
+  if (VEC && t0 + kTok <= L) {
+    store8_vec<T>(orow + t0, y);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kTok; ++j)
+      if (t0 + j < L) orow[t0 + j] = AT::from_f(y[j]);
+  }
+  // final state: x̃[L-(W-1) .. L-1], held in this window by the thread with the last token
+  if (a.stateT && t0 + kTok >= L) {
+    T* so = static_cast<T*>(a.stateT) + row * (W - 1);
+    // position L-(W-1)+j sits at window index first + j, first = kTok + (L-1-t0) - (W-2)
+    const int first = kTok + (int)(L - 1 - t0) - (W - 2);
+#pragma unroll
+    for (int idx = 0; idx < 2 * kTok; ++idx) {  // compile-time window index keeps win in registers
+      const int j = idx - first;
+      if (j >= 0 && j < W - 1) so[j] = AT::from_f(win[idx]);
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kConvBlock) conv1d_step_kernel(const ConvArgs a) {
+  using AT = Act<T>;
+  const int64_t row = (int64_t)blockIdx.x * kConvBlock + threadIdx.x;
+  if (row >= a.rows) return;
+  const int W = a.W;
+  const int64_t c = row % a.d_inner;
+  T* st = static_cast<T*>(a.stateT) + row * (W - 1);  // in-out
+  float win[kTok];
+#pragma unroll
+  for (int k = 0; k < kTok - 1; ++k) win[k] = k < W - 1 ? ld_act<T>(st + k) : 0.f;
+  const float xv = ld_act<T>(static_cast<const T*>(a.x) + row);
+  float pre = a.bias ? __ldg(a.bias + c) : 0.f;
+#pragma unroll
+  for (int k = 0; k < kTok; ++k)
+    if (k < W) pre = fmaf(__ldg(a.w + c * W + k), k == W - 1 ? xv : win[k], pre);
+  static_cast<T*>(a.out)[row] = AT::from_f(silu_c<AT::kFast>(pre));
+#pragma unroll
+  for (int k = 0; k < kTok - 1; ++k)
+    if (k < W - 1) st[k] = AT::from_f(k + 1 < W - 1 ? win[k + 1] : xv);
+}
+
+template <typename T, int W>
+cudaError_t fwd_w(const ConvArgs& a, bool vec, cudaStream_t s) {
+  const int64_t threads = a.rows * a.wsegs * 32;
+  const int64_t grid = (threads + kConvBlock - 1) / kConvBlock;
+  if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
+  if (vec)
+    conv1d_fwd_kernel<T, W, true><<<(unsigned)grid, kConvBlock, 0, s>>>(a);
+  else
+    conv1d_fwd_kernel<T, W, false><<<(unsigned)grid, kConvBlock, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t fwd_dt(const ConvArgs& a, bool vec, cudaStream_t s) {
+  switch (a.W) {
+    case 1: return fwd_w<T, 1>(a, vec, s);
+    case 2: return fwd_w<T, 2>(a, vec, s);
+    case 3: return fwd_w<T, 3>(a, vec, s);
+    case 4: return fwd_w<T, 4>(a, vec, s);
+    case 5: return fwd_w<T, 5>(a, vec, s);
+    case 6: return fwd_w<T, 6>(a, vec, s);
+    case 7: return fwd_w<T, 7>(a, vec, s);
+    case 8: return fwd_w<T, 8>(a, vec, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t conv1d_fwd_launch(const ConvCall& k, cudaStream_t stream) {
+  ConvArgs a{};
+  a.x = k.x; a.w = k.w; a.bias = k.bias; a.state0 = k.state_in; a.out = k.out; a.stateT = k.state_out;
+  a.rows = k.batch * k.d_inner; a.d_inner = k.d_inner; a.L = k.L; a.W = k.W;
+  a.wsegs = (k.L + 32 * kTok - 1) / (32 * kTok);
+  const int esz = k.act == 1 ? 2 : 4;
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const bool vec = (k.L * esz) % 16 == 0 && a16(k.x) && a16(k.out);
+  return k.act == 1 ? fwd_dt<__nv_bfloat16>(a, vec, stream) : fwd_dt<float>(a, vec, stream);
+}
+
+cudaError_t conv1d_step_launch(const ConvCall& k, cudaStream_t stream) {
+  ConvArgs a{};
+  a.x = k.x; a.w = k.w; a.bias = k.bias; a.out = k.out; a.stateT = k.state_out;
+  a.rows = k.batch * k.d_inner; a.d_inner = k.d_inner; a.L = 1; a.W = k.W;
+  const int64_t grid = (a.rows + kConvBlock - 1) / kConvBlock;
+  if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
+  if (k.act == 1)
+    conv1d_step_kernel<__nv_bfloat16><<<(unsigned)grid, kConvBlock, 0, stream>>>(a);
+  else
+    conv1d_step_kernel<float><<<(unsigned)grid, kConvBlock, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace ssm

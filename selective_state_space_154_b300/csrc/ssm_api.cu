@@ -61,6 +61,29 @@ ssm_status check_dims(const ssm_dims* d, bool need_len) {
   return SSM_OK;
 }
 
+// Validation of dims for the Conv1D calls (d_state is not used; seqlen only for the sequence form).
+ssm_status check_conv(const ssm_dims* d, bool need_len, int32_t width) {
+  if (!d) return SSM_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->d_inner < 1 || (need_len && d->seqlen < 1)) return SSM_ERR_INVALID_ARG;
+  if (d->act != SSM_DTYPE_F32 && d->act != SSM_DTYPE_BF16) return SSM_ERR_INVALID_ARG;
+  if (width < 1) return SSM_ERR_INVALID_ARG;
+  if (width > ssm::kMaxConvWidth) return SSM_ERR_UNSUPPORTED;
+  const int64_t lim = int64_t(1) << 40;  // rows and rows x tokens / 256 stay far inside the grid limits
+  if (d->batch > lim / d->d_inner) return SSM_ERR_UNSUPPORTED;
+  const int64_t rows = d->batch * d->d_inner;
+  const int64_t len = need_len ? d->seqlen : 1;
+  if (rows > (int64_t(1) << 35) || len > (int64_t(1) << 52) / rows) return SSM_ERR_UNSUPPORTED;
+  return SSM_OK;
+}
+
+ssm::ConvCall conv_call(const void* x, const float* w, const float* bias, const void* s_in, void* out,
+                        void* s_out, const ssm_dims* d, int32_t width, bool seq) {
+  ssm::ConvCall k{};
+  k.x = x; k.w = w; k.bias = bias; k.state_in = s_in; k.out = out; k.state_out = s_out;
+  k.batch = d->batch; k.d_inner = d->d_inner; k.L = seq ? d->seqlen : 1; k.W = width; k.act = d->act;
+  return k;
+}
+
 ssm::ScanArgs scan_args(const void* u, const void* delta, const float* A, const void* B, const void* C,
                         const float* D, const void* z, const float* bias, void* out, float* fs,
                         const ssm_dims* d, void* ws, const float* h0 = nullptr) {
@@ -175,6 +198,36 @@ ssm_status ssm_step(float* state, const void* x, const void* delta, const float*
   sk.force_plain = knobs.force_step_plain;
   const cudaError_t e = ssm::step_launch(a, sk, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_conv1d_fwd(const void* x, const float* weight, const float* bias, const void* initial_conv_state,
+                          void* out, void* final_conv_state, const ssm_dims* dims, int32_t width,
+                          ssm_stream_t stream) {
+  const ssm_status ds = check_conv(dims, true, width);
+  if (ds != SSM_OK) return ds;
+  if (!x || !weight || !out) return SSM_ERR_INVALID_ARG;
+  const unsigned esz = dims->act == SSM_DTYPE_BF16 ? 2u : 4u;
+  const void* act_ptrs[] = {x, out, initial_conv_state, final_conv_state};
+  for (const void* p : act_ptrs)
+    if (p && !aligned(p, esz)) return SSM_ERR_ALIGNMENT;
+  if (!aligned(weight, 4) || (bias && !aligned(bias, 4))) return SSM_ERR_ALIGNMENT;
+  const ssm::ConvCall k = conv_call(x, weight, bias, width > 1 ? initial_conv_state : nullptr, out,
+                                    width > 1 ? final_conv_state : nullptr, dims, width, true);
+  return ssm::conv1d_fwd_launch(k, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_conv1d_step(void* conv_state, const void* x, const float* weight, const float* bias, void* out,
+                           const ssm_dims* dims, int32_t width, ssm_stream_t stream) {
+  const ssm_status ds = check_conv(dims, false, width);
+  if (ds != SSM_OK) return ds;
+  if (!x || !weight || !out || (width > 1 && !conv_state)) return SSM_ERR_INVALID_ARG;
+  const unsigned esz = dims->act == SSM_DTYPE_BF16 ? 2u : 4u;
+  const void* act_ptrs[] = {x, out, conv_state};
+  for (const void* p : act_ptrs)
+    if (p && !aligned(p, esz)) return SSM_ERR_ALIGNMENT;
+  if (!aligned(weight, 4) || (bias && !aligned(bias, 4))) return SSM_ERR_ALIGNMENT;
+  const ssm::ConvCall k = conv_call(x, weight, bias, nullptr, out, conv_state, dims, width, false);
+  return ssm::conv1d_step_launch(k, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 ssm_status ssm_step_check(ssm_stream_t stream) {

@@ -94,6 +94,23 @@ struct StepKnobs {
   bool force_plain;      // use step_kernel even where the pipelined kernel applies
 };
 cudaError_t step_launch(const StepArgs& a, const StepKnobs& k, cudaStream_t stream);
+// Causal depthwise Conv1D + SiLU (conv1d.cu).  state_in / state_out: [batch][d_inner][W-1]
+// in the activation dtype; for the step, state_out is the in-out state and state_in unused.
+struct ConvCall {
+  const void* x;
+  const float* w;
+  const float* bias;
+  const void* state_in;
+  void* out;
+  void* state_out;
+  int64_t batch, d_inner, L;
+  int W;
+  int act;
+};
+constexpr int kMaxConvWidth = 8;
+cudaError_t conv1d_fwd_launch(const ConvCall& k, cudaStream_t stream);
+cudaError_t conv1d_step_launch(const ConvCall& k, cudaStream_t stream);
+
 // Reads and clears the sticky error word of the pipelined step kernel (current device).
 cudaError_t step_error_fetch_clear(unsigned* word);
 

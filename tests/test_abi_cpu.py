@@ -158,3 +158,47 @@ def test_scan_from_state_validates_the_initial_state(lib):
     d.seqlen = 0
     assert _scan_from(lib, d, FAKE) == ssm.SSM_ERR_INVALID_ARG             # dims checked as for ssm_scan_fwd
     assert _scan_from(lib, _dims(), FAKE, {"u": None}) == ssm.SSM_ERR_INVALID_ARG
+
+
+def _conv(lib, dims, width=4, ptrs=None):
+    p = dict(x=FAKE, w=FAKE, bias=None, s0=None, out=FAKE, sT=None)
+    p.update(ptrs or {})
+    a = [ctypes.c_void_p(p[k]) if p[k] else None for k in ("x", "w", "bias", "s0", "out", "sT")]
+    return lib.ssm_conv1d_fwd(*a, ctypes.byref(dims), width, None)
+
+
+def _conv_step(lib, dims, width=4, ptrs=None):
+    p = dict(state=FAKE, x=FAKE, w=FAKE, bias=None, out=FAKE)
+    p.update(ptrs or {})
+    a = [ctypes.c_void_p(p[k]) if p[k] else None for k in ("state", "x", "w", "bias", "out")]
+    return lib.ssm_conv1d_step(*a, ctypes.byref(dims), width, None)
+
+
+@pytest.mark.parametrize("width,status", [(0, ssm.SSM_ERR_INVALID_ARG), (-3, ssm.SSM_ERR_INVALID_ARG),
+                                          (9, ssm.SSM_ERR_UNSUPPORTED)])
+def test_conv_rejects_bad_width(lib, width, status):
+    assert _conv(lib, _dims(), width) == status
+    assert _conv_step(lib, _dims(), width) == status
+
+
+@pytest.mark.parametrize("missing", ["x", "w", "out"])
+def test_conv_rejects_null_required_pointer(lib, missing):
+    assert _conv(lib, _dims(), ptrs={missing: None}) == ssm.SSM_ERR_INVALID_ARG
+    assert _conv_step(lib, _dims(), ptrs={missing: None}) == ssm.SSM_ERR_INVALID_ARG
+
+
+def test_conv_step_needs_a_state_unless_width_one(lib):
+    assert _conv_step(lib, _dims(), 4, {"state": None}) == ssm.SSM_ERR_INVALID_ARG
+
+
+def test_conv_rejects_misaligned_and_bad_dims(lib):
+    assert _conv(lib, _dims(), ptrs={"x": FAKE + 1}) == ssm.SSM_ERR_ALIGNMENT
+    assert _conv(lib, _dims(), ptrs={"sT": FAKE + 1}) == ssm.SSM_ERR_ALIGNMENT
+    assert _conv(lib, _dims(), ptrs={"w": FAKE + 2}) == ssm.SSM_ERR_ALIGNMENT
+    assert _conv_step(lib, _dims(), ptrs={"state": FAKE + 1}) == ssm.SSM_ERR_ALIGNMENT
+    d = _dims()
+    d.seqlen = 0
+    assert _conv(lib, d) == ssm.SSM_ERR_INVALID_ARG
+    d = _dims()
+    d.act = 5
+    assert _conv_step(lib, d) == ssm.SSM_ERR_INVALID_ARG

@@ -153,3 +153,25 @@ def random_scan_inputs(batch, d_inner, d_state, seqlen, dtype=torch.bfloat16, de
         g = _gen(device, seed, 102)
         inp["bias"] = 0.5 * torch.randn(d_inner, generator=g, device=device)
     return inp
+
+
+# Causal Conv1D in front of the scan: width 4 as in Mamba; x, and the carried
+# state, ~ N(0, 1) in the activation dtype; weight and bias ~ U(-1/sqrt(W), 1/sqrt(W))
+# in fp32 (the usual initial range of a depthwise convolution with W taps).
+CONV_WIDTH = 4
+
+
+def conv_inputs(batch, d_inner, seqlen, width=CONV_WIDTH, dtype=torch.bfloat16, device="cpu", seed: int = 0,
+                with_bias=True, with_state=True):
+    bound = 1.0 / math.sqrt(width)
+    g = _gen(device, seed, 201)
+    w = (2.0 * torch.rand((d_inner, width), generator=g, device=device) - 1.0) * bound
+    g = _gen(device, seed, 202)
+    bias = (2.0 * torch.rand((d_inner,), generator=g, device=device) - 1.0) * bound if with_bias else None
+    g = _gen(device, seed, 203)
+    x = torch.randn((batch, d_inner, seqlen), generator=g, device=device).to(dtype)
+    state = None
+    if with_state and width > 1:
+        g = _gen(device, seed, 204)
+        state = torch.randn((batch, d_inner, width - 1), generator=g, device=device).to(dtype)
+    return dict(x=x, w=w, bias=bias, state=state)
