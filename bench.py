@@ -42,9 +42,11 @@ FP32_LANES_PER_SM = 128
 # FP32 lane operations of one state update (b, c, t, n) on the minimal path:
 # Δ·A, Ā-1, x·(1/A), (x/A)·B + h, (Ā-1)·s + h, C·h accumulate (the exp is on the MUFU pipe).
 FP32_OPS_PER_UPDATE = 6
-# ncu DRAM bytes (read + write) per launch of the scan kernel on this workload;
-# None until a capture of the current kernel is recorded (see profiles/).
-SCAN_DRAM_BYTES_PER_LAUNCH = None
+# ncu DRAM bytes (read + write) per launch of the scan kernel on this workload,
+# from a capture of the current kernel at full size (13.68 GB read + 4.58 GB
+# written; profiles/scan_rows_kernel_long_1m_dram.md).  Set back to None when
+# the kernel changes until it is captured again.
+SCAN_DRAM_BYTES_PER_LAUNCH = 18.26e9
 
 
 def measured_peaks():
@@ -301,6 +303,61 @@ def bench_workloads(dev, runs=20):
     return res
 
 
+def conv_alg_bytes(rows, L, width, esz):
+    """x read and out written once per (row, token), the carried state read and
+    the final state written once per row (weight and bias are added by the caller)."""
+    return rows * L * 2 * esz + 2 * rows * (width - 1) * esz
+
+
+def bench_conv(dev, hbm_peak, runs=20):
+    """Causal Conv1D + SiLU: the sequence form on the 2.8B-shaped layer's x (L2
+    flushed before each call) and on the 1M-token rows (larger than L2), and the
+    decode step on the decode workload's rows (L2 flushed before each step)."""
+    import selective_state_space_154_b300 as ssm
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {"width": W.CONV_WIDTH,
+           "note": "each call timed alone with CUDA events, median; hbm_frac of the measured copy bandwidth"}
+
+    def timed(call, n, flush_each=True):
+        for _ in range(3):
+            call()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            if flush_each:
+                flush()
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+
+    for name in ("mamba2p8b_layer", "long_1m"):
+        shape = W.SCAN_SHAPES[name]
+        cv = W.conv_inputs(shape.batch, shape.d_inner, shape.seqlen, device=dev, seed=0)
+        out = torch.empty_like(cv["x"])
+        fs = torch.empty_like(cv["state"])
+        call = lambda: ssm.ssm_conv1d_fwd(cv["x"], cv["w"], cv["bias"], cv["state"], out, fs, stream=stream)
+        secs = timed(call, runs if name != "long_1m" else 5, flush_each=name != "long_1m")
+        alg = conv_alg_bytes(shape.rows, shape.seqlen, W.CONV_WIDTH, 2) + shape.d_inner * (W.CONV_WIDTH + 1) * 4
+        res[f"fwd_{name}"] = {"batch": shape.batch, "d_inner": shape.d_inner, "seq_len": shape.seqlen,
+                              "us": secs * 1e6, "channel_tokens_per_s": shape.channel_tokens / secs,
+                              "gbs": alg / secs / 1e9, "hbm_frac": alg / secs / 1e9 / hbm_peak, "alg_bytes": alg}
+        del cv, out, fs
+    shape = W.DECODE_SHAPE
+    cv = W.conv_inputs(shape.batch, shape.d_inner, 1, device=dev, seed=0)
+    x = cv["x"][:, :, 0].contiguous()
+    out = torch.empty_like(x)
+    st = cv["state"]
+    secs = timed(lambda: ssm.ssm_conv1d_step(st, x, cv["w"], cv["bias"], out, stream=stream), 200)
+    rows = shape.batch * shape.d_inner
+    alg = 2 * rows * 2 + 2 * rows * (W.CONV_WIDTH - 1) * 2 + shape.d_inner * (W.CONV_WIDTH + 1) * 4
+    res["step_decode"] = {"batch": shape.batch, "d_inner": shape.d_inner, "us": secs * 1e6,
+                          "tokens_per_s": shape.batch / secs, "gbs": alg / secs / 1e9,
+                          "hbm_frac": alg / secs / 1e9 / hbm_peak, "alg_bytes": alg}
+    return res
+
+
 def bench_decode(dev):
     """ssm_step on the decode workload: each timed step starts with L2 flushed
     (in a model, the other layers evict this layer's state between its steps);
@@ -435,6 +492,7 @@ def run_ours(args):
     torch.cuda.empty_cache()
     decode = bench_decode(dev) if rank == 0 else None
     others = bench_workloads(dev) if rank == 0 else None
+    conv = bench_conv(dev, hbm_peak) if rank == 0 else None
     cpu = cpu_baseline() if (rank == 0 and world == 1) else None
 
     if rank == 0:
@@ -466,6 +524,7 @@ def run_ours(args):
                                   "median of 20; hbm_frac of the measured copy bandwidth",
                           **({k: dict(v, hbm_frac=v["gbs"] / hbm_peak) for k, v in others.items()}
                              if others else {})},
+            "conv1d": conv,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -489,6 +548,14 @@ def run_profile_case(args):
         fn = lambda: ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
                                       inp["bias"], out, None, workspace=ws)
         units = shape.channel_tokens
+    elif args.only == "conv":
+        base = W.SCAN_SHAPES[args.workload]
+        L = args.seqlen or base.seqlen
+        cv = W.conv_inputs(base.batch, args.dinner or base.d_inner, L, device=dev, seed=0)
+        out = torch.empty_like(cv["x"])
+        fs = torch.empty_like(cv["state"])
+        fn = lambda: ssm.ssm_conv1d_fwd(cv["x"], cv["w"], cv["bias"], cv["state"], out, fs)
+        units = cv["x"].numel()
     else:
         shape = W.DECODE_SHAPE
         inp = W.decode_inputs(shape, device=dev, seed=0, steps=8)
@@ -539,14 +606,14 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "scan", "decode"], default="all",
-                    help="profiling aid: run only the scan or only the decode part (no JSON line)")
+    ap.add_argument("--only", choices=["all", "scan", "decode", "conv"], default="all",
+                    help="profiling aid: run only the scan, the decode step or the Conv1D (no JSON line)")
     ap.add_argument("--seqlen", type=int, default=None,
                     help="profiling aid: scan another sequence length of the same workload")
     ap.add_argument("--dinner", type=int, default=None,
                     help="profiling aid: scan another number of channels of the same workload")
     ap.add_argument("--workload", choices=sorted(W.SCAN_SHAPES), default=WORKLOAD,
-                    help="profiling aid: the scan workload --only scan runs")
+                    help="profiling aid: the workload --only scan / --only conv runs")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":

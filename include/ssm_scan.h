@@ -160,7 +160,8 @@ SSM_API ssm_status ssm_scan_check(const void* workspace, size_t workspace_bytes)
  *   weight: [d_inner][width] float32; bias: [d_inner] float32 or NULL.
  *   initial_conv_state, final_conv_state: [batch][d_inner][width-1], act dtype
  *     (the raw inputs, so they are exact), or NULL; unused when width is 1.
- *   1 <= width <= 8 (SSM_ERR_UNSUPPORTED above).  Element alignment as for the scan.
+ *   1 <= width <= 8, batch and d_inner <= 65535 (SSM_ERR_UNSUPPORTED otherwise).
+ *   Element alignment as for the scan.
  *   out and final_conv_state must not overlap x, initial_conv_state or each
  *   other.  No workspace; stream-ordered and asynchronous like ssm_scan_fwd.
  */

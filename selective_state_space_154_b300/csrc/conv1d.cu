@@ -11,7 +11,7 @@
 // and one output written.
 //
 // conv1d_fwd_kernel: a thread owns 8 consecutive tokens of one row (one 16-byte
-// vector in bf16, two in fp32), a warp 256 consecutive tokens.  The 8 tokens
+// vector in bf16, two in fp32), a warp 256 consecutive tokens, a CTA 2048.  The 8 tokens
 // before a thread's own come from the lane to its left by shuffles; lane 0
 // loads them (or takes the carried state at the start of the row).  The thread
 // holding the row's last token writes the final state.
@@ -80,20 +80,19 @@ struct ConvArgs {
   void* out;
   void* stateT;        // [rows][W-1] or nullptr
   int64_t rows, d_inner, L;
-  int64_t wsegs;       // warps per row: ceil(L / 256)
   int W;               // taps (runtime copy; the forward kernel is instantiated per width)
 };
 
+// Grid: x = 2048-token segments of a row, y = channel, z = batch (no division per thread).
 template <typename T, int W, bool VEC>
 __global__ void __launch_bounds__(kConvBlock) conv1d_fwd_kernel(const ConvArgs a) {
   using AT = Act<T>;
   const int lane = threadIdx.x & 31;
-  const int64_t gwarp = ((int64_t)blockIdx.x * kConvBlock + threadIdx.x) >> 5;
-  const int64_t row = gwarp / a.wsegs;
-  if (row >= a.rows) return;  // rows are warp-uniform
-  const int64_t t0 = ((gwarp % a.wsegs) * 32 + lane) * kTok;
+  const int64_t c = blockIdx.y;
+  const int64_t row = (int64_t)blockIdx.z * a.d_inner + c;
+  const int64_t t0 = ((int64_t)blockIdx.x * kConvBlock + threadIdx.x) * kTok;
   const int64_t L = a.L;
-  const int64_t c = row % a.d_inner;
+  if (t0 - lane * kTok >= L) return;  // whole warp past the end of the row (lane 0 then always has t0 < L)
   const T* xr = static_cast<const T*>(a.x) + row * L;
   const T* sr = a.state0 ? static_cast<const T*>(a.state0) + row * (W - 1) : nullptr;
 
@@ -168,37 +167,56 @@ __global__ void __launch_bounds__(kConvBlock) conv1d_fwd_kernel(const ConvArgs a
   }
 }
 
-template <typename T>
+// Grid: x = blocks of kStepItems x 256 channels, y = batch.  A thread takes
+// kStepItems channels 256 apart and issues all their loads before any
+// arithmetic, so one wave of CTAs keeps enough bytes in flight.
+constexpr int kStepItems = 4;
+
+template <typename T, int W>
 __global__ void __launch_bounds__(kConvBlock) conv1d_step_kernel(const ConvArgs a) {
   using AT = Act<T>;
-  const int64_t row = (int64_t)blockIdx.x * kConvBlock + threadIdx.x;
-  if (row >= a.rows) return;
-  const int W = a.W;
-  const int64_t c = row % a.d_inner;
-  T* st = static_cast<T*>(a.stateT) + row * (W - 1);  // in-out
-  float win[kTok];
+  constexpr int S = W > 1 ? W - 1 : 1;  // carried inputs per row (storage for W = 1 unused)
+  const int64_t cbase = (int64_t)blockIdx.x * kConvBlock * kStepItems + threadIdx.x;
+  const int64_t rbase = (int64_t)blockIdx.y * a.d_inner;
+  float st[kStepItems][S], xv[kStepItems], wv[kStepItems][W], bv[kStepItems];
 #pragma unroll
-  for (int k = 0; k < kTok - 1; ++k) win[k] = k < W - 1 ? ld_act<T>(st + k) : 0.f;
-  const float xv = ld_act<T>(static_cast<const T*>(a.x) + row);
-  float pre = a.bias ? __ldg(a.bias + c) : 0.f;
+  for (int i = 0; i < kStepItems; ++i) {
+    const int64_t c = cbase + i * kConvBlock;
+    const bool ok = c < a.d_inner;
+    const int64_t row = rbase + (ok ? c : 0);
+    const T* sp = static_cast<const T*>(a.stateT) + row * (W - 1);
 #pragma unroll
-  for (int k = 0; k < kTok; ++k)
-    if (k < W) pre = fmaf(__ldg(a.w + c * W + k), k == W - 1 ? xv : win[k], pre);
-  static_cast<T*>(a.out)[row] = AT::from_f(silu_c<AT::kFast>(pre));
+    for (int k = 0; k < W - 1; ++k) st[i][k] = ok ? ld_act<T>(sp + k) : 0.f;
+    xv[i] = ok ? ld_act<T>(static_cast<const T*>(a.x) + row) : 0.f;
 #pragma unroll
-  for (int k = 0; k < kTok - 1; ++k)
-    if (k < W - 1) st[k] = AT::from_f(k + 1 < W - 1 ? win[k + 1] : xv);
+    for (int k = 0; k < W; ++k) wv[i][k] = ok ? __ldg(a.w + c * W + k) : 0.f;
+    bv[i] = (ok && a.bias) ? __ldg(a.bias + c) : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < kStepItems; ++i) {
+    const int64_t c = cbase + i * kConvBlock;
+    if (c >= a.d_inner) continue;
+    const int64_t row = rbase + c;
+    float pre = bv[i];
+#pragma unroll
+    for (int k = 0; k < W; ++k) pre = fmaf(wv[i][k], k == W - 1 ? xv[i] : st[i][k], pre);
+    static_cast<T*>(a.out)[row] = AT::from_f(silu_c<AT::kFast>(pre));
+    T* sp = static_cast<T*>(a.stateT) + row * (W - 1);
+#pragma unroll
+    for (int k = 0; k < W - 1; ++k) sp[k] = AT::from_f(k + 1 < W - 1 ? st[i][k + 1] : xv[i]);
+  }
 }
 
 template <typename T, int W>
 cudaError_t fwd_w(const ConvArgs& a, bool vec, cudaStream_t s) {
-  const int64_t threads = a.rows * a.wsegs * 32;
-  const int64_t grid = (threads + kConvBlock - 1) / kConvBlock;
-  if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
+  const int64_t segs = (a.L + kConvBlock * kTok - 1) / (kConvBlock * kTok);
+  if (segs > INT32_MAX || a.d_inner > kMaxConvGridYZ || a.rows / a.d_inner > kMaxConvGridYZ)
+    return cudaErrorInvalidConfiguration;
+  const dim3 grid((unsigned)segs, (unsigned)a.d_inner, (unsigned)(a.rows / a.d_inner));
   if (vec)
-    conv1d_fwd_kernel<T, W, true><<<(unsigned)grid, kConvBlock, 0, s>>>(a);
+    conv1d_fwd_kernel<T, W, true><<<grid, kConvBlock, 0, s>>>(a);
   else
-    conv1d_fwd_kernel<T, W, false><<<(unsigned)grid, kConvBlock, 0, s>>>(a);
+    conv1d_fwd_kernel<T, W, false><<<grid, kConvBlock, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -217,13 +235,28 @@ cudaError_t fwd_dt(const ConvArgs& a, bool vec, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
+template <typename T>
+cudaError_t step_dt(const ConvArgs& a, dim3 grid, cudaStream_t s) {
+  switch (a.W) {
+    case 1: conv1d_step_kernel<T, 1><<<grid, kConvBlock, 0, s>>>(a); break;
+    case 2: conv1d_step_kernel<T, 2><<<grid, kConvBlock, 0, s>>>(a); break;
+    case 3: conv1d_step_kernel<T, 3><<<grid, kConvBlock, 0, s>>>(a); break;
+    case 4: conv1d_step_kernel<T, 4><<<grid, kConvBlock, 0, s>>>(a); break;
+    case 5: conv1d_step_kernel<T, 5><<<grid, kConvBlock, 0, s>>>(a); break;
+    case 6: conv1d_step_kernel<T, 6><<<grid, kConvBlock, 0, s>>>(a); break;
+    case 7: conv1d_step_kernel<T, 7><<<grid, kConvBlock, 0, s>>>(a); break;
+    case 8: conv1d_step_kernel<T, 8><<<grid, kConvBlock, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t conv1d_fwd_launch(const ConvCall& k, cudaStream_t stream) {
   ConvArgs a{};
   a.x = k.x; a.w = k.w; a.bias = k.bias; a.state0 = k.state_in; a.out = k.out; a.stateT = k.state_out;
   a.rows = k.batch * k.d_inner; a.d_inner = k.d_inner; a.L = k.L; a.W = k.W;
-  a.wsegs = (k.L + 32 * kTok - 1) / (32 * kTok);
   const int esz = k.act == 1 ? 2 : 4;
   auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   const bool vec = (k.L * esz) % 16 == 0 && a16(k.x) && a16(k.out);
@@ -234,13 +267,10 @@ cudaError_t conv1d_step_launch(const ConvCall& k, cudaStream_t stream) {
   ConvArgs a{};
   a.x = k.x; a.w = k.w; a.bias = k.bias; a.out = k.out; a.stateT = k.state_out;
   a.rows = k.batch * k.d_inner; a.d_inner = k.d_inner; a.L = 1; a.W = k.W;
-  const int64_t grid = (a.rows + kConvBlock - 1) / kConvBlock;
-  if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
-  if (k.act == 1)
-    conv1d_step_kernel<__nv_bfloat16><<<(unsigned)grid, kConvBlock, 0, stream>>>(a);
-  else
-    conv1d_step_kernel<float><<<(unsigned)grid, kConvBlock, 0, stream>>>(a);
-  return cudaGetLastError();
+  if (k.batch > kMaxConvGridYZ) return cudaErrorInvalidConfiguration;
+  const int64_t per_cta = (int64_t)kConvBlock * kStepItems;
+  const dim3 grid((unsigned)((k.d_inner + per_cta - 1) / per_cta), (unsigned)k.batch);
+  return k.act == 1 ? step_dt<__nv_bfloat16>(a, grid, stream) : step_dt<float>(a, grid, stream);
 }
 
 }  // namespace ssm

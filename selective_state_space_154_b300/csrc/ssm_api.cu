@@ -68,11 +68,9 @@ ssm_status check_conv(const ssm_dims* d, bool need_len, int32_t width) {
   if (d->act != SSM_DTYPE_F32 && d->act != SSM_DTYPE_BF16) return SSM_ERR_INVALID_ARG;
   if (width < 1) return SSM_ERR_INVALID_ARG;
   if (width > ssm::kMaxConvWidth) return SSM_ERR_UNSUPPORTED;
-  const int64_t lim = int64_t(1) << 40;  // rows and rows x tokens / 256 stay far inside the grid limits
-  if (d->batch > lim / d->d_inner) return SSM_ERR_UNSUPPORTED;
-  const int64_t rows = d->batch * d->d_inner;
-  const int64_t len = need_len ? d->seqlen : 1;
-  if (rows > (int64_t(1) << 35) || len > (int64_t(1) << 52) / rows) return SSM_ERR_UNSUPPORTED;
+  // d_inner and batch are grid dimensions (at most 65535 each); tokens per row < 2^42
+  if (d->d_inner > ssm::kMaxConvGridYZ || d->batch > ssm::kMaxConvGridYZ) return SSM_ERR_UNSUPPORTED;
+  if (need_len && d->seqlen > (int64_t(1) << 42)) return SSM_ERR_UNSUPPORTED;
   return SSM_OK;
 }
 

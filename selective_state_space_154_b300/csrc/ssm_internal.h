@@ -108,6 +108,7 @@ struct ConvCall {
   int act;
 };
 constexpr int kMaxConvWidth = 8;
+constexpr int64_t kMaxConvGridYZ = 65535;  // d_inner and batch index grid dimensions y / z
 cudaError_t conv1d_fwd_launch(const ConvCall& k, cudaStream_t stream);
 cudaError_t conv1d_step_launch(const ConvCall& k, cudaStream_t stream);
 
