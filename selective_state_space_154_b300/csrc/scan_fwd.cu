@@ -26,9 +26,9 @@
 // end state of the previous one as its carry-in h_in (bounded wait on a flag),
 // and publishes its own end state P h_in + H.  The outputs of a chunk are
 // then corrected by Σ_n C_t,n exp(A_n S_t) h_in,n,
-// S_t = Σ_{s≤t} Δ_s, for as long as exp(A_n S_t) is above 2^-24 for some
-// state of the CTA with h_in,n != 0; below that the term is under the fp32
-// rounding of h_in itself.
+// S_t = Σ_{s≤t} Δ_s, for as long as exp(A_n S_t) is above 2^-24 (fp32 output)
+// or 2^-12 (bf16 output) for some state of the CTA with h_in,n != 0; below that
+// the term is under the rounding of the output relative to h_in.
 #include <algorithm>
 #include <cstdio>
 
@@ -424,9 +424,9 @@ __global__ void __launch_bounds__(512, 1) scan_fwd_kernel(const KParams p) {
           }
           pyr[t * groups] = y;
         }
-        // continue while some state's carried-in term is above 2^-24 |h_in| (A log2e S > -24)
+        // continue while some state's carried-in term is above 2^stop |h_in| (A log2e S > stop)
 #pragma unroll
-        for (int k = 0; k < G; ++k) alive |= (a2[k] * S > kCorrStopLog2 && hin[k] != 0.f);
+        for (int k = 0; k < G; ++k) alive |= (a2[k] * S > corr_stop_log2<T>() && hin[k] != 0.f);
       }
       __syncthreads();
 

@@ -206,7 +206,8 @@ enum PassMode { kScanPass = 0, kCorrPass = 1 };
 // One pass of the CTA over tokens [t_lo, t_hi).
 //   kScanPass: the local scan from the registers' h; writes out.
 //   kCorrPass: h holds h_in; adds Σ_n C exp(A S) h_in to out until exp(A S) has
-//              fallen below 2^-24 for every state with h_in != 0 in the CTA.
+//              fallen below 2^-24 (fp32 output) or 2^-12 (bf16 output) for every
+//              state with h_in != 0 in the CTA.
 // TPR threads share a row: thread j of the row holds states [j·SPT, (j+1)·SPT)
 // and the readout is summed over the row's threads with shuffles.
 template <typename T, int RB, int TPR, bool HAS_Z, bool VEC, int MODE>
@@ -362,10 +363,10 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
       if (row_ok && jpart == 0 && t < t_hi) store8<T, VEC>(orow, t, t_hi, yv);
     }
     if (MODE == kCorrPass) {
-      // Stop once every state's carried-in term exp(A S) h_in is below 2^-24 |h_in|
-      // (A log2e S < -24): what is left is under the fp32 rounding of h_in itself.
+      // Stop once every state's carried-in term exp(A S) h_in is below 2^stop |h_in|
+      // (A log2e S < stop): what is left is under the rounding of the output.
 #pragma unroll
-      for (int n = 0; n < SPT; ++n) any |= (a2[n] * S > kCorrStopLog2 && h[n] != 0.f);
+      for (int n = 0; n < SPT; ++n) any |= (a2[n] * S > corr_stop_log2<T>() && h[n] != 0.f);
       if (!__syncthreads_or(any)) break;  // also orders the reuse of this stage's buffers
     } else {
       __syncthreads();  // this stage's buffers are refilled two stages later

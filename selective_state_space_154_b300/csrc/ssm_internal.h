@@ -14,8 +14,11 @@ constexpr int kStatesPerThread = 4;  // G: states of one row held by one thread 
 constexpr int kRowsPerRowCta = 128;     // row kernel, small variant: rows per CTA (four CTAs per SM)
 constexpr int kRowTokensPerStage = 32;  // row kernel: tokens per stage
 // The correction of a chunk's outputs by its carried-in state stops once
-// exp(A S) < 2^kCorrStopLog2 for every state with a nonzero carry-in.
-constexpr float kCorrStopLog2 = -24.f;
+// exp(A S) < 2^stop for every state with a nonzero carry-in: 2^-24 (below the
+// fp32 rounding of the carry) for fp32 outputs, 2^-12 (1/8 of the half-ulp of a
+// bf16 output relative to the carried state) for bf16 outputs.
+template <typename T>
+__host__ __device__ constexpr float corr_stop_log2() { return sizeof(T) == 2 ? -12.f : -24.f; }
 
 enum ScanKind { kScanTiles = 0, kScanRows = 1 };
 
