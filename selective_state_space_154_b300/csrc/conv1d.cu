@@ -10,13 +10,15 @@
 // zeros).  Both kernels are bound by memory: per (row, token) one input read
 // and one output written.
 //
-// conv1d_fwd_kernel: a thread owns 8 consecutive tokens of one row (one 16-byte
-// vector in bf16, two in fp32), a warp 256 consecutive tokens, a CTA 2048.  The 8 tokens
-// before a thread's own come from the lane to its left by shuffles; lane 0
-// loads them (or takes the carried state at the start of the row).  The thread
+// conv1d_fwd_kernel: a thread owns 32 consecutive tokens of one row (four
+// 16-byte vectors in bf16, eight in fp32, all loaded before any arithmetic).
+// The 8 tokens before a thread's own come from the lane to its left by
+// shuffles; lane 0 loads them (or takes the carried state at the start of the
+// row).  The thread
 // holding the row's last token writes the final state.
 // conv1d_step_kernel: one thread per row shifts the W-1 carried inputs, appends
 // x and writes out.
+#include <algorithm>
 #include <cstdint>
 
 #include "ssm_device.cuh"
@@ -25,8 +27,10 @@
 namespace ssm {
 namespace {
 
-constexpr int kTok = 8;          // tokens per thread
-constexpr int kConvBlock = 256;  // threads per CTA
+constexpr int kTok = 8;            // tokens per 16-byte vector (bf16)
+constexpr int kVec = 4;            // vectors per thread in the sequence kernel
+constexpr int kSpan = kTok * kVec; // tokens per thread in the sequence kernel
+constexpr int kConvBlock = 256;    // threads per CTA (at most)
 
 template <typename T>
 __device__ __forceinline__ float ld_act(const T* p) {
@@ -35,7 +39,7 @@ __device__ __forceinline__ float ld_act(const T* p) {
 
 // 8 consecutive values at p (16-byte aligned)
 template <typename T>
-__device__ __forceinline__ void load8_vec(const T* p, float (&v)[kTok]) {
+__device__ __forceinline__ void load8_vec(const T* p, float* v) {
   if constexpr (sizeof(T) == 2) {
     const uint4 w = *reinterpret_cast<const uint4*>(p);
     const unsigned u[4] = {w.x, w.y, w.z, w.w};
@@ -52,7 +56,7 @@ __device__ __forceinline__ void load8_vec(const T* p, float (&v)[kTok]) {
 }
 
 template <typename T>
-__device__ __forceinline__ void store8_vec(T* p, const float (&v)[kTok]) {
+__device__ __forceinline__ void store8_vec(T* p, const float* v) {
   if constexpr (sizeof(T) == 2) {
     unsigned u[4];
 #pragma unroll
@@ -67,9 +71,16 @@ __device__ __forceinline__ void store8_vec(T* p, const float (&v)[kTok]) {
   }
 }
 
+// silu(v) = v·sigmoid(v); for bf16 outputs as (v/2)(1 + tanh(v/2)), one MUFU op.
 template <bool FAST>
 __device__ __forceinline__ float silu_c(float v) {
-  return FAST ? silu_fast(v) : silu_precise(v);
+  if (FAST) {
+    const float hv = 0.5f * v;
+    float th;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(hv));
+    return fmaf(hv, th, hv);
+  }
+  return silu_precise(v);
 }
 
 struct ConvArgs {
@@ -83,84 +94,88 @@ struct ConvArgs {
   int W;               // taps (runtime copy; the forward kernel is instantiated per width)
 };
 
-// Grid: x = 2048-token segments of a row, y = channel, z = batch (no division per thread).
+// Grid: x = segments of blockDim.x * kSpan tokens of a row, y = channel, z = batch
+// (no division per thread).  A thread owns kSpan consecutive tokens, loaded as
+// kVec vectors before any arithmetic.
 template <typename T, int W, bool VEC>
 __global__ void __launch_bounds__(kConvBlock) conv1d_fwd_kernel(const ConvArgs a) {
   using AT = Act<T>;
   const int lane = threadIdx.x & 31;
   const int64_t c = blockIdx.y;
   const int64_t row = (int64_t)blockIdx.z * a.d_inner + c;
-  const int64_t t0 = ((int64_t)blockIdx.x * kConvBlock + threadIdx.x) * kTok;
+  const int64_t t0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * kSpan;
   const int64_t L = a.L;
-  if (t0 - lane * kTok >= L) return;  // whole warp past the end of the row (lane 0 then always has t0 < L)
+  if (t0 - lane * kSpan >= L) return;  // whole warp past the end of the row (lane 0 then always has t0 < L)
   const T* xr = static_cast<const T*>(a.x) + row * L;
   const T* sr = a.state0 ? static_cast<const T*>(a.state0) + row * (W - 1) : nullptr;
 
-  // own 8 tokens (zeros past the end of the row)
-  float cur[kTok];
-  if (VEC && t0 + kTok <= L) {
-    load8_vec<T>(xr + t0, cur);
-  } else {
+  // window x̃[t0-8 .. t0+kSpan-1]: win[0..7] the 8 tokens before, win[8..] the thread's own
+  float win[kTok + kSpan];
 #pragma unroll
-    for (int i = 0; i < kTok; ++i) cur[i] = (t0 + i < L) ? ld_act<T>(xr + t0 + i) : 0.f;
+  for (int v = 0; v < kVec; ++v) {
+    const int64_t tv = t0 + v * kTok;
+    if (VEC && tv + kTok <= L) {
+      load8_vec<T>(xr + tv, win + kTok + v * kTok);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kTok; ++i) win[kTok + v * kTok + i] = (tv + i < L) ? ld_act<T>(xr + tv + i) : 0.f;
+    }
   }
-  // the 8 tokens before: from the lane to the left, or loaded by lane 0
-  float prev[kTok];
+  // the 8 tokens before: the last 8 of the lane to the left, or loaded by lane 0
 #pragma unroll
-  for (int i = 0; i < kTok; ++i) prev[i] = __shfl_up_sync(0xffffffffu, cur[i], 1);
+  for (int i = 0; i < kTok; ++i) win[i] = __shfl_up_sync(0xffffffffu, win[kSpan + i], 1);
   if (lane == 0) {
     if (t0 >= kTok) {
       if (VEC) {
-        load8_vec<T>(xr + t0 - kTok, prev);
+        load8_vec<T>(xr + t0 - kTok, win);
       } else {
 #pragma unroll
-        for (int i = 0; i < kTok; ++i) prev[i] = ld_act<T>(xr + t0 - kTok + i);
+        for (int i = 0; i < kTok; ++i) win[i] = ld_act<T>(xr + t0 - kTok + i);
       }
     } else {  // t0 == 0: positions -8..-1 are the carried state (zeros before it)
 #pragma unroll
       for (int i = 0; i < kTok; ++i) {
         const int pos = i - kTok;
-        prev[i] = (sr && pos >= -(W - 1)) ? ld_act<T>(sr + (W - 1) + pos) : 0.f;
+        win[i] = (sr && pos >= -(W - 1)) ? ld_act<T>(sr + (W - 1) + pos) : 0.f;
       }
     }
   }
   if (t0 >= L) return;
 
-  // window x̃[t0-8 .. t0+7] = (prev, cur); out[t0+j] = silu(bias + Σ_k w[k] x̃[t0+j-(W-1)+k])
-  float win[2 * kTok];
-#pragma unroll
-  for (int i = 0; i < kTok; ++i) {
-    win[i] = prev[i];
-    win[kTok + i] = cur[i];
-  }
+  // out[t0+j] = silu(bias + Σ_k w[k] x̃[t0+j-(W-1)+k]), window index kTok + j - (W-1) + k
   const float* wc = a.w + c * W;
   float wk[W];
 #pragma unroll
   for (int k = 0; k < W; ++k) wk[k] = __ldg(wc + k);
   const float b0 = a.bias ? __ldg(a.bias + c) : 0.f;
-  float y[kTok];
-#pragma unroll
-  for (int j = 0; j < kTok; ++j) {
-    float pre = b0;
-#pragma unroll
-    for (int k = 0; k < W; ++k) pre = fmaf(wk[k], win[kTok + j - (W - 1) + k], pre);  // index in [1, 15]
-    y[j] = silu_c<AT::kFast>(pre);
-  }
   T* orow = static_cast<T*>(a.out) + row * L;
-  if (VEC && t0 + kTok <= L) {
-    store8_vec<T>(orow + t0, y);
-  } else {
 #pragma unroll
-    for (int j = 0; j < kTok; ++j)
-      if (t0 + j < L) orow[t0 + j] = AT::from_f(y[j]);
+  for (int v = 0; v < kVec; ++v) {
+    float y[kTok];
+#pragma unroll
+    for (int i = 0; i < kTok; ++i) {
+      const int j = v * kTok + i;
+      float pre = b0;
+#pragma unroll
+      for (int k = 0; k < W; ++k) pre = fmaf(wk[k], win[kTok + j - (W - 1) + k], pre);  // index >= 1
+      y[i] = silu_c<AT::kFast>(pre);
+    }
+    const int64_t tv = t0 + v * kTok;
+    if (VEC && tv + kTok <= L) {
+      store8_vec<T>(orow + tv, y);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kTok; ++i)
+        if (tv + i < L) orow[tv + i] = AT::from_f(y[i]);
+    }
   }
   // final state: x̃[L-(W-1) .. L-1], held in this window by the thread with the last token
-  if (a.stateT && t0 + kTok >= L) {
+  if (a.stateT && t0 + kSpan >= L) {
     T* so = static_cast<T*>(a.stateT) + row * (W - 1);
     // position L-(W-1)+j sits at window index first + j, first = kTok + (L-1-t0) - (W-2)
     const int first = kTok + (int)(L - 1 - t0) - (W - 2);
 #pragma unroll
-    for (int idx = 0; idx < 2 * kTok; ++idx) {  // compile-time window index keeps win in registers
+    for (int idx = 0; idx < kTok + kSpan; ++idx) {  // compile-time window index keeps win in registers
       const int j = idx - first;
       if (j >= 0 && j < W - 1) so[j] = AT::from_f(win[idx]);
     }
@@ -209,14 +224,17 @@ __global__ void __launch_bounds__(kConvBlock) conv1d_step_kernel(const ConvArgs 
 
 template <typename T, int W>
 cudaError_t fwd_w(const ConvArgs& a, bool vec, cudaStream_t s) {
-  const int64_t segs = (a.L + kConvBlock * kTok - 1) / (kConvBlock * kTok);
+  // CTA width: enough warps for the row, at most kConvBlock threads
+  const int64_t need = (a.L + kSpan - 1) / kSpan;
+  const int threads = (int)std::min<int64_t>(kConvBlock, (need + 31) / 32 * 32);
+  const int64_t segs = (a.L + (int64_t)threads * kSpan - 1) / ((int64_t)threads * kSpan);
   if (segs > INT32_MAX || a.d_inner > kMaxConvGridYZ || a.rows / a.d_inner > kMaxConvGridYZ)
     return cudaErrorInvalidConfiguration;
   const dim3 grid((unsigned)segs, (unsigned)a.d_inner, (unsigned)(a.rows / a.d_inner));
   if (vec)
-    conv1d_fwd_kernel<T, W, true><<<grid, kConvBlock, 0, s>>>(a);
+    conv1d_fwd_kernel<T, W, true><<<grid, threads, 0, s>>>(a);
   else
-    conv1d_fwd_kernel<T, W, false><<<grid, kConvBlock, 0, s>>>(a);
+    conv1d_fwd_kernel<T, W, false><<<grid, threads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
