@@ -71,16 +71,11 @@ __device__ __forceinline__ void store8_vec(T* p, const float* v) {
   }
 }
 
-// silu(v) = v·sigmoid(v); for bf16 outputs as (v/2)(1 + tanh(v/2)), one MUFU op.
+// silu(v) = v·sigmoid(v): v / (1 + 2^(-v log2 e)) with the MUFU ex2 and rcp
+// approximations for bf16 outputs (accurate for v < 0 too), the precise form otherwise.
 template <bool FAST>
 __device__ __forceinline__ float silu_c(float v) {
-  if (FAST) {
-    const float hv = 0.5f * v;
-    float th;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(hv));
-    return fmaf(hv, th, hv);
-  }
-  return silu_precise(v);
+  return FAST ? silu_fast(v) : silu_precise(v);
 }
 
 struct ConvArgs {

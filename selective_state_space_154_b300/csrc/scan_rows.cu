@@ -17,9 +17,11 @@
 //  * chunks compose as affine maps, (A₂,b₂)∘(A₁,b₁) = (A₂A₁, A₂b₁+b₂)
 //    ("Mambaとは？…", Selective Scanは選択機構そのものではない): every chunk scans
 //    from h = 0 at once keeping S = ΣΔ, then takes the end state h_in of the
-//    previous chunk (in chunk order, bounded wait), publishes its own end state
-//    exp(A S)·h_in + h_local, and adds Σ_n C_t,n exp(A_n S_t) h_in,n to its first
-//    outputs until that term is exactly zero in fp32 for every row of the CTA.
+//    previous chunk (in chunk order, bounded wait) and publishes its own end state
+//    exp(A S)·h_in + h_local.  Its first blocks, those whose outputs the carried-in
+//    state still changes (exp(A_n S) ≥ 2^-24 for fp32 outputs, 2^-12 for bf16, for
+//    the row's slowest-decaying state), are not written by that pass: a second pass
+//    scans them again from h_in and writes them, rounding each output once.
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
 
@@ -66,7 +68,7 @@ __device__ __forceinline__ int swz(int r) {
 }
 
 // Issue the copies of stage [t0, t0 + TS) ∩ [t0, t_end): three row tiles and B, C.
-template <typename T, int RB, int NT, bool VEC, int MODE>
+template <typename T, int RB, int NT, bool VEC>
 __device__ __forceinline__ void issue_stage(Smem<T, RB>& sm, int buf, const RowParams& p, int64_t b, int64_t row0, int nrows,
                                             int64_t t0, int64_t t_end) {
   constexpr int G = Smem<T, RB>::kGran;
@@ -75,7 +77,7 @@ __device__ __forceinline__ void issue_stage(Smem<T, RB>& sm, int buf, const RowP
   static_assert(NT % G == 0 && RB % RSTEP == 0, "a stage splits evenly over the CTA's threads");
   constexpr int E = sizeof(T);
   const int64_t L = p.a.L;
-  const T* srcs[3] = {static_cast<const T*>(MODE == 0 ? p.a.u : p.a.out), static_cast<const T*>(p.a.delta),
+  const T* srcs[3] = {static_cast<const T*>(p.a.u), static_cast<const T*>(p.a.delta),
                       static_cast<const T*>(p.a.z)};
   const int ntens = p.a.z ? 3 : 2;
   const int g = threadIdx.x % G;
@@ -176,16 +178,12 @@ __device__ __forceinline__ void store8(T* row, int64_t t, int64_t t_end, const f
   }
 }
 
-// silu for bf16 outputs: z·(1 + tanh(z/2))/2 (one MUFU op); precise form otherwise.
+// silu for bf16 outputs: z / (1 + 2^(-z log2 e)) with the MUFU ex2 and rcp
+// approximations (no cancellation for z < 0, unlike (z/2)(1 + tanh(z/2)),
+// whose 1 + tanh loses all accuracy there); precise form otherwise.
 template <bool FAST>
 __device__ __forceinline__ float silu_t(float z) {
-  if (FAST) {
-    float th;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(0.5f * z));
-    const float hz = 0.5f * z;
-    return fmaf(hz, th, hz);
-  }
-  return silu_precise(z);
+  return FAST ? silu_fast(z) : silu_precise(z);
 }
 
 __device__ bool wait_flag_rows(const RowParams& p, const unsigned* flag, unsigned want) {
@@ -201,20 +199,27 @@ __device__ bool wait_flag_rows(const RowParams& p, const unsigned* flag, unsigne
   return false;
 }
 
-enum PassMode { kScanPass = 0, kCorrPass = 1 };
+// Which 8-token blocks a pass writes.  A block of a chunk after the first is
+// "settled" when exp(A_n S) < 2^stop for every state at the block's start
+// (S = ΣΔ from the chunk start, the same sequence in both passes), i.e. when
+// the chunk's carried-in state can no longer change its outputs.
+enum WritePolicy {
+  kWriteAll = 0,        // the first chunk (or the only one): every block
+  kWriteSettled = 1,    // other chunks, first pass from h = 0: the settled blocks
+  kWriteUnsettled = 2,  // other chunks, second pass from the carried-in state: the rest,
+                        // stopping once every row of the CTA is settled
+};
 
-// One pass of the CTA over tokens [t_lo, t_hi).
-//   kScanPass: the local scan from the registers' h; writes out.
-//   kCorrPass: h holds h_in; adds Σ_n C exp(A S) h_in to out until exp(A S) has
-//              fallen below 2^-24 (fp32 output) or 2^-12 (bf16 output) for every
-//              state with h_in != 0 in the CTA.
-// TPR threads share a row: thread j of the row holds states [j·SPT, (j+1)·SPT)
-// and the readout is summed over the row's threads with shuffles.
-template <typename T, int RB, int TPR, bool HAS_Z, bool VEC, int MODE>
+// One pass of the CTA over tokens [t_lo, t_hi): the scan from the registers' h,
+// writing the blocks that WP selects.  a2max = max_n A_n log2e over the row's
+// states (-inf for rows past d_inner): the slowest decay decides when a row is
+// settled.  TPR threads share a row: thread j of the row holds states
+// [j·SPT, (j+1)·SPT) and the readout is summed over the row's threads with shuffles.
+template <typename T, int RB, int TPR, bool HAS_Z, bool VEC, int WP>
 __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, int64_t b, int64_t row0, int nrows,
                                          int64_t t_lo, int64_t t_hi, float (&h)[NS / TPR], const float (&a2)[NS / TPR],
                                          const float (&ia)[NS / TPR], const float* arow, bool precise, float Dc,
-                                         float biasc, float& S) {
+                                         float biasc, float a2max, float& S) {
   using AT = Act<T>;
   constexpr bool FAST = AT::kFast;
   constexpr int NT = RB * TPR;
@@ -228,23 +233,27 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
   T* orow = static_cast<T*>(p.a.out) + (row0 + (row_ok ? r : 0)) * p.a.L;
   const int nst = (int)((t_hi - t_lo + TS - 1) / TS);
   if (nst <= 0) return;
-  issue_stage<T, RB, NT, VEC, MODE>(sm, 0, p, b, row0, nrows, t_lo, t_hi);
+  issue_stage<T, RB, NT, VEC>(sm, 0, p, b, row0, nrows, t_lo, t_hi);
   cp_async_commit();
   float comp = 0.f;  // Kahan compensation of S
   for (int st = 0; st < nst; ++st) {
     const int64_t ts = t_lo + (int64_t)st * TS;
     const int buf = st & 1;
-    if (st + 1 < nst) issue_stage<T, RB, NT, VEC, MODE>(sm, buf ^ 1, p, b, row0, nrows, ts + TS, t_hi);
+    if (st + 1 < nst) issue_stage<T, RB, NT, VEC>(sm, buf ^ 1, p, b, row0, nrows, ts + TS, t_hi);
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();  // stage st landed for every thread
     convert_bc<T, NT>(sm.bcf, reinterpret_cast<const T*>(sm.raw_bc[buf]), N);
     __syncthreads();
     const int64_t t_valid = row_ok ? t_hi : ts;  // rows past d_inner compute nothing useful
-    bool any = false;
 #pragma unroll 1
     for (int blk = 0; blk < TS / 8; ++blk) {
       const int64_t t = ts + blk * 8;
+      // S: ΣΔ before this block.  Pass two takes the threshold one power of two
+      // looser, so a block near the boundary may be written twice (pass two last)
+      // but never by neither pass.
+      const bool write_blk = WP == kWriteAll || (WP == kWriteSettled ? !(a2max * S > corr_stop_log2<T>())
+                                                                     : a2max * S > corr_stop_log2<T>() - 1.f);
       uint4 wu[GPB], wd[GPB], wz[GPB];
 #pragma unroll
       for (int j = 0; j < GPB; ++j) {
@@ -267,10 +276,10 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
         const float dlt = dlt8[v];
-        const float x = get8<T>(wu, v);  // kCorrPass: the current output value
+        const float x = get8<T>(wu, v);
         const float4* bc4 = reinterpret_cast<const float4*>(bcs + v * 2 * NS);
         float y;
-        if (MODE == kScanPass) {
+        {
           if (!precise) {
             const float2 dd = make_float2(dlt, dlt), xx = make_float2(x, x);
             float2 ya = make_float2(0.f, 0.f), yb = make_float2(0.f, 0.f);
@@ -323,34 +332,6 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
           y = fmaf(Dc, x, y);
           if (HAS_Z) y *= gz8[v];
           Sb += dlt;
-        } else {
-          // correction Σ_n C_n exp(A_n S_t) h_in,n (h holds h_in in this pass)
-          Sb += dlt;
-          const float St = S + Sb;
-          const float2 ss = make_float2(St, St);
-          float2 ya = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int q = 0; q < SPT / 4; ++q) {
-            const float4 cq = bc4[NS / 4 + n0 / 4 + q];
-#pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-              const int n = 4 * q + 2 * k2;
-              float2 P;
-              if (!precise) {
-                const float2 e = __fmul2_rn(ss, make_float2(a2[n], a2[n + 1]));
-                P = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-              } else {
-                P = make_float2(exp2f(a2[n] * St), exp2f(a2[n + 1] * St));
-              }
-              const float2 cc = k2 ? make_float2(cq.z, cq.w) : make_float2(cq.x, cq.y);
-              ya = __ffma2_rn(__fmul2_rn(cc, make_float2(h[n], h[n + 1])), P, ya);
-            }
-          }
-          y = ya.x + ya.y;
-#pragma unroll
-          for (int off = TPR / 2; off > 0; off >>= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
-          if (HAS_Z) y *= gz8[v];
-          y += x;
         }
         yv[v] = y;
       }
@@ -360,14 +341,12 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
         comp = (tk - S) - yk;
         S = tk;
       }
-      if (row_ok && jpart == 0 && t < t_hi) store8<T, VEC>(orow, t, t_hi, yv);
+      if (row_ok && jpart == 0 && t < t_hi && write_blk) store8<T, VEC>(orow, t, t_hi, yv);
     }
-    if (MODE == kCorrPass) {
-      // Stop once every state's carried-in term exp(A S) h_in is below 2^stop |h_in|
-      // (A log2e S < stop): what is left is under the rounding of the output.
-#pragma unroll
-      for (int n = 0; n < SPT; ++n) any |= (a2[n] * S > corr_stop_log2<T>() && h[n] != 0.f);
-      if (!__syncthreads_or(any)) break;  // also orders the reuse of this stage's buffers
+    if (WP == kWriteUnsettled) {
+      // stop once every row of the CTA is settled: pass one wrote the rest
+      const bool unsettled = a2max * S > corr_stop_log2<T>() - 1.f;
+      if (!__syncthreads_or(unsettled)) break;  // also orders the reuse of this stage's buffers
     } else {
       __syncthreads();  // this stage's buffers are refilled two stages later
     }
@@ -435,16 +414,31 @@ __global__ void __launch_bounds__(RowCta<RB, TPR>::kThreads, RowCta<RB, TPR>::kM
     // the first chunk starts from the initial state; later chunks start from 0 and take their carry
     h[n] = (chunk == 0 && p.a.h0 && row_ok && n0 + n < N) ? p.a.h0[row * N + n0 + n] : 0.f;
   }
+  // slowest decay of the row (its real states only): decides which blocks the carry still changes
+  float a2max = -INFINITY;
+#pragma unroll
+  for (int n = 0; n < SPT; ++n)
+    if (row_ok && n0 + n < N) a2max = fmaxf(a2max, a2[n]);
   // a row's threads take the same path (the precise one if any of its states has A = 0)
   if (TPR > 1) {
 #pragma unroll
-    for (int off = TPR / 2; off > 0; off >>= 1) precise |= __shfl_xor_sync(0xffffffffu, (int)precise, off) != 0;
+    for (int off = TPR / 2; off > 0; off >>= 1) {
+      precise |= __shfl_xor_sync(0xffffffffu, (int)precise, off) != 0;
+      a2max = fmaxf(a2max, __shfl_xor_sync(0xffffffffu, a2max, off));
+    }
   }
   const float Dc = (row_ok && p.a.D) ? p.a.D[c] : 0.f;
   const float biasc = (row_ok && p.a.bias) ? p.a.bias[c] : 0.f;
 
+  // pass one: the chunk from h = 0 (the initial state for the first chunk); later
+  // chunks write only the blocks their carried-in state can no longer change
   float S = 0.f;
-  row_pass<T, RB, TPR, HAS_Z, VEC, kScanPass>(sm, p, b, row0, nrows, tc0, tc1, h, a2, ia, arow, precise, Dc, biasc, S);
+  if (chunk > 0)
+    row_pass<T, RB, TPR, HAS_Z, VEC, kWriteSettled>(sm, p, b, row0, nrows, tc0, tc1, h, a2, ia, arow, precise, Dc,
+                                                    biasc, a2max, S);
+  else
+    row_pass<T, RB, TPR, HAS_Z, VEC, kWriteAll>(sm, p, b, row0, nrows, tc0, tc1, h, a2, ia, arow, precise, Dc,
+                                                biasc, a2max, S);
 
   // ---------------- carry between chunks ----------------
   float hin[SPT];
@@ -489,13 +483,12 @@ __global__ void __launch_bounds__(RowCta<RB, TPR>::kThreads, RowCta<RB, TPR>::kM
   }
   if (chunk == 0 || p.nchunks == 1) return;
 
-  // ---------------- correction of this chunk's first outputs ----------------
-  bool any = false;
-#pragma unroll
-  for (int n = 0; n < SPT; ++n) any |= (hin[n] != 0.f);
-  if (!__syncthreads_or(any)) return;
-  float Sc = 0.f;
-  row_pass<T, RB, TPR, HAS_Z, VEC, kCorrPass>(sm, p, b, row0, nrows, tc0, tc1, hin, a2, ia, arow, precise, Dc, biasc, Sc);
+  // ---------------- pass two: the chunk's first blocks again, from the carried-in state ----------------
+  // The same arithmetic as an unchunked scan, so these outputs are rounded once;
+  // it runs until every row of the CTA is settled.
+  float S2 = 0.f;
+  row_pass<T, RB, TPR, HAS_Z, VEC, kWriteUnsettled>(sm, p, b, row0, nrows, tc0, tc1, hin, a2, ia, arow, precise, Dc,
+                                                    biasc, a2max, S2);
 }
 
 template <typename T, int RB, int TPR, bool HAS_Z, bool VEC>
