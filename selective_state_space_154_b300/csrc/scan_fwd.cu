@@ -24,11 +24,11 @@
 // associativity of (A₂,b₂)∘(A₁,b₁) = (A₂A₁, A₂b₁+b₂)), so every chunk runs its
 // local scan from h = 0 at once; then, in chunk order, each chunk takes the
 // end state of the previous one as its carry-in h_in (bounded wait on a flag),
-// and publishes its own end state P h_in + H.  The outputs of a chunk are
-// then corrected by Σ_n C_t,n exp(A_n S_t) h_in,n,
-// S_t = Σ_{s≤t} Δ_s, for as long as exp(A_n S_t) is above 2^-24 (fp32 output)
-// or 2^-12 (bf16 output) for some state of the CTA with h_in,n != 0; below that
-// the term is under the rounding of the output relative to h_in.
+// and publishes its own end state P h_in + H.  The first pass writes only the
+// tiles that h_in can no longer change (exp(A_n S_t) below 2^-24 for fp32
+// outputs, 2^-12 for bf16, S_t = Σ_{s≤t} Δ_s, for the row's slowest-decaying
+// state); a second pass scans the chunk's first tiles again from h_in and
+// writes them, so every output is rounded once.
 #include <algorithm>
 #include <cstdio>
 
@@ -62,7 +62,7 @@ __host__ __device__ inline Layout make_layout(int esize, int N, int npad, int gr
   l.bf = o; o += align16((size_t)TT * npad * 4);
   l.cf = o; o += align16((size_t)TT * npad * 4);
   l.py = o; o += align16((size_t)RT * (TT * groups + kPyPad) * 4);
-  l.rowp = o; o += align16((size_t)2 * RT * 4);
+  l.rowp = o; o += align16((size_t)4 * RT * 4);  // D, bias, slowest decay, write flag per row
   l.misc = o; o += 64;
   l.total = o;
   return l;
@@ -80,12 +80,18 @@ struct KParams {
   int fault_lookback;
 };
 
-enum Mode { kMain = 0, kCorr = 1 };
+// Which tiles a pass writes (per row).  A tile of a chunk after the first is
+// "settled" when exp(A_n S) < 2^stop for the row's slowest-decaying state at the
+// tile's start (S = ΣΔ from the chunk start): the chunk's carried-in state can no
+// longer change its outputs.  Pass one (from h = 0) writes the settled tiles,
+// pass two (again from the carried-in state) the others, with a threshold one
+// power of two looser so that no tile is left unwritten.
+enum WritePolicy { kWriteAll = 0, kWriteSettled = 1, kWriteUnsettled = 2 };
 
 // Raw tile pointers inside one staging buffer.
 template <typename T>
 struct RawTile {
-  T* u;   // [RT][TT]   (kCorr: current out values)
+  T* u;   // [RT][TT]
   T* dr;  // [RT][TT]
   T* z;   // [RT][TT]
   T* b;   // [TT][N]
@@ -152,17 +158,13 @@ __device__ __forceinline__ void load_bc(T* dst, const T* src, const KParams& p, 
 }
 
 template <typename T, bool HAS_Z>
-__device__ void issue_tile(unsigned char* buf, const KParams& p, Mode mode, int64_t b, int64_t c0, int nrows,
+__device__ void issue_tile(unsigned char* buf, const KParams& p, int64_t b, int64_t c0, int nrows,
                            int64_t t0, int64_t t_end) {
   RawTile<T> rt = raw_tile<T>(buf, (int)p.a.N);
   const int64_t row0 = b * p.a.d_inner + c0;
   const bool vr = p.vec_rows != 0, vb = p.vec_bc != 0;
-  if (mode == kMain) {
-    load_rows<T>(rt.u, static_cast<const T*>(p.a.u), p, row0, nrows, t0, t_end, vr);
-    load_bc<T>(rt.b, static_cast<const T*>(p.a.B), p, b, t0, t_end, vb);
-  } else {
-    load_rows<T>(rt.u, static_cast<const T*>(p.a.out), p, row0, nrows, t0, t_end, vr);
-  }
+  load_rows<T>(rt.u, static_cast<const T*>(p.a.u), p, row0, nrows, t0, t_end, vr);
+  load_bc<T>(rt.b, static_cast<const T*>(p.a.B), p, b, t0, t_end, vb);
   load_rows<T>(rt.dr, static_cast<const T*>(p.a.delta), p, row0, nrows, t0, t_end, vr);
   if (HAS_Z) load_rows<T>(rt.z, static_cast<const T*>(p.a.z), p, row0, nrows, t0, t_end, vr);
   load_bc<T>(rt.c, static_cast<const T*>(p.a.C), p, b, t0, t_end, vb);
@@ -210,6 +212,8 @@ __global__ void __launch_bounds__(512, 1) scan_fwd_kernel(const KParams p) {
   float* py = reinterpret_cast<float*>(smem + lay.py);
   float* d_s = reinterpret_cast<float*>(smem + lay.rowp);
   float* bias_s = d_s + RT;
+  float* a2max_s = d_s + 2 * RT;                      // slowest decay A·log2e of each row
+  int* wflag = reinterpret_cast<int*>(d_s + 3 * RT);  // 1: this pass writes the row's current tile
   int* misc = reinterpret_cast<int*>(smem + lay.misc);
 
   // ---- work item: (chunk, batch, channel tile), chunk-major ticket order ----
@@ -241,6 +245,13 @@ __global__ void __launch_bounds__(512, 1) scan_fwd_kernel(const KParams p) {
     const bool ok = (int)threadIdx.x < nrows;
     d_s[threadIdx.x] = (ok && p.a.D) ? p.a.D[c0 + threadIdx.x] : 0.f;
     bias_s[threadIdx.x] = (ok && p.a.bias) ? p.a.bias[c0 + threadIdx.x] : 0.f;
+    float amax = -INFINITY;  // rows past d_inner are always settled
+    if (ok)
+      for (int n = 0; n < N; ++n) {
+        const float av = p.a.A[(c0 + threadIdx.x) * N + n];
+        amax = fmaxf(amax, fabsf(av) < 8.673617e-19f ? 0.f : av * kLog2e);
+      }
+    a2max_s[threadIdx.x] = amax;
   }
 
   // ---- per-thread constants: A·log2e, 1/A; padded states are inert (A = 0, B = C = 0) ----
@@ -272,8 +283,9 @@ __global__ void __launch_bounds__(512, 1) scan_fwd_kernel(const KParams p) {
 #pragma unroll
   for (int k = 0; k < G; ++k) hin[k] = 0.f;
 
-  for (int mode = kMain; mode <= kCorr; ++mode) {
-    if (mode == kCorr) {
+  for (int pass = 0; pass < 2; ++pass) {
+    int wp = (p.nchunks > 1 && chunk > 0) ? kWriteSettled : kWriteAll;
+    if (pass == 1) {
       if (p.nchunks == 1) break;
       // ---- carry between chunks: wait for the previous chunk's final state ----
       // Chunk k's end state is P_k h_in + H_k with P_k = exp(A ΣΔ) and H_k its
@@ -307,24 +319,30 @@ __global__ void __launch_bounds__(512, 1) scan_fwd_kernel(const KParams p) {
         __syncthreads();
         if (threadIdx.x == 0) st_release_gpu(myflag, 1u);
       }
-      if (chunk == 0) break;  // chunk 0 starts from h = 0: nothing to correct
-      // skip the correction when the carry-in is zero everywhere in the CTA
-      bool any = false;
+      // the last chunk's end state is the final state; pass two reuses h
+      if (p.a.final_state && chunk == p.nchunks - 1 && row_ok) {
 #pragma unroll
-      for (int k = 0; k < G; ++k) any |= (hin[k] != 0.f);
-      if (!__syncthreads_or(any)) break;
+        for (int k = 0; k < G; ++k) {
+          const int n = g * G + k;
+          if (n < N) p.a.final_state[row * N + n] = h[k];
+        }
+      }
+      if (chunk == 0) break;  // the first chunk started from its true state: all written
+      // pass two: the chunk's first tiles again, from the carried-in state
+#pragma unroll
+      for (int k = 0; k < G; ++k) h[k] = hin[k];
       S = 0.f;
+      wp = kWriteUnsettled;
     }
 
     // ---------------- tile loop ----------------
-    const Mode md = (Mode)mode;
-    issue_tile<T, HAS_Z>(raw0, p, md, b, c0, nrows, tc0, tc1);
+    issue_tile<T, HAS_Z>(raw0, p, b, c0, nrows, tc0, tc1);
     cp_async_commit();
     for (int it = 0; it < ntiles; ++it) {
       const int64_t t0 = tc0 + (int64_t)it * TT;
       unsigned char* cur = (it & 1) ? raw1 : raw0;
       unsigned char* nxt = (it & 1) ? raw0 : raw1;
-      if (it + 1 < ntiles) issue_tile<T, HAS_Z>(nxt, p, md, b, c0, nrows, t0 + TT, tc1);
+      if (it + 1 < ntiles) issue_tile<T, HAS_Z>(nxt, p, b, c0, nrows, t0 + TT, tc1);
       cp_async_commit();
       cp_async_wait<1>();
       __syncthreads();
@@ -350,7 +368,7 @@ __global__ void __launch_bounds__(512, 1) scan_fwd_kernel(const KParams p) {
       for (int i = threadIdx.x; i < TT * npad; i += blockDim.x) {
         const int t = i / npad, n = i % npad;
         const bool ok = n < N && t < nvalid_t;
-        if (md == kMain) bf[i] = ok ? AT::to_f(rt.b[t * N + n]) : 0.f;
+        bf[i] = ok ? AT::to_f(rt.b[t * N + n]) : 0.f;
         cf[i] = ok ? AT::to_f(rt.c[t * N + n]) : 0.f;
       }
       __syncthreads();
@@ -358,8 +376,12 @@ __global__ void __launch_bounds__(512, 1) scan_fwd_kernel(const KParams p) {
       // ---- sequential scan over the tile's tokens, h in registers ----
       const float2* dxr = dx + r_loc * kDxStride;
       float* pyr = py + r_loc * (TT * groups + kPyPad) + g;
-      bool alive = false;
-      if (md == kMain) {
+      const float a2max = a2max_s[r_loc];
+      if (g == 0) {  // S is the row's ΣΔ before this tile
+        const float thr = corr_stop_log2<T>();
+        wflag[r_loc] = wp == kWriteAll ? 1 : wp == kWriteSettled ? !(a2max * S > thr) : (a2max * S > thr - 1.f);
+      }
+      {
         if (!precise) {
           float2 h01 = make_float2(h[0], h[1]), h23 = make_float2(h[2], h[3]);
           const float2 A01 = make_float2(a2[0], a2[1]), A23 = make_float2(a2[2], a2[3]);
@@ -409,24 +431,6 @@ __global__ void __launch_bounds__(512, 1) scan_fwd_kernel(const KParams p) {
             S += d.x;
           }
         }
-      } else {
-        // correction: Σ_n C_t,n exp(A_n S_t) h_in,n
-        for (int t = 0; t < TT; ++t) {
-          const float2 d = dxr[t];
-          const float4 cv = cf4[t * q4 + g];
-          const float cc[4] = {cv.x, cv.y, cv.z, cv.w};
-          S += d.x;
-          float y = 0.f;
-#pragma unroll
-          for (int k = 0; k < G; ++k) {
-            const float P = precise ? expf(a_[k] * S) : ex2_approx(a2[k] * S);
-            y = fmaf(cc[k] * hin[k], P, y);
-          }
-          pyr[t * groups] = y;
-        }
-        // continue while some state's carried-in term is above 2^stop |h_in| (A log2e S > stop)
-#pragma unroll
-        for (int k = 0; k < G; ++k) alive |= (a2[k] * S > corr_stop_log2<T>() && hin[k] != 0.f);
       }
       __syncthreads();
 
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(512, 1) scan_fwd_kernel(const KParams p) {
         const int64_t L = p.a.L;
         for (int i = threadIdx.x; i < RT * (TT / VPT); i += blockDim.x) {
           const int r = i / (TT / VPT), s = i % (TT / VPT);
-          if (r >= nrows) continue;
+          if (r >= nrows || !wflag[r]) continue;
           const int64_t grow = b * p.a.d_inner + c0 + r;
           const float* pr = py + r * (TT * groups + kPyPad);
           float vals[VPT];
@@ -448,14 +452,9 @@ __global__ void __launch_bounds__(512, 1) scan_fwd_kernel(const KParams p) {
             float y = 0.f;
             for (int q = 0; q < groups; ++q) y += pr[t * groups + q];
             const float2 d = dx[r * kDxStride + t];
-            if (md == kMain) {
-              y = fmaf(d_s[r], d.y, y);
-              if (HAS_Z) y *= gt[r * kGtStride + t];
-              vals[v] = y;
-            } else {
-              if (HAS_Z) y *= gt[r * kGtStride + t];
-              vals[v] = d.y + y;  // current out value + correction
-            }
+            y = fmaf(d_s[r], d.y, y);
+            if (HAS_Z) y *= gt[r * kGtStride + t];
+            vals[v] = y;
           }
           const int64_t tb = t0 + (int64_t)s * VPT;
           T* dst = outp + grow * L + tb;
@@ -467,16 +466,17 @@ __global__ void __launch_bounds__(512, 1) scan_fwd_kernel(const KParams p) {
           }
         }
       }
-      if (md == kCorr) {
-        if (!__syncthreads_or(alive)) break;
+      if (wp == kWriteUnsettled) {
+        // stop once every row of the CTA is settled: pass one wrote the rest
+        if (!__syncthreads_or(a2max * S > corr_stop_log2<T>() - 1.f)) break;
       }
     }
     cp_async_wait<0>();
     __syncthreads();
   }
 
-  // ---- final state h_L (last chunk holds it after the carry) ----
-  if (p.a.final_state && chunk == p.nchunks - 1 && row_ok) {
+  // ---- final state h_L of an unchunked scan (chunked scans wrote it after the carry) ----
+  if (p.a.final_state && p.nchunks == 1 && row_ok) {
 #pragma unroll
     for (int k = 0; k < G; ++k) {
       const int n = g * G + k;

@@ -111,6 +111,26 @@ def test_split_and_continue_matches_one_scan(kernel):
     assert rel_err(to_np(state), to_np(fs_whole)) <= TOL[torch.bfloat16]
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+def test_chunking_does_not_change_results(dtype, kernel, monkeypatch):
+    """A chunked scan gives the unchunked scan's outputs: every output is computed
+    from its true state and rounded once (a correction added to already-rounded
+    bf16 outputs missed this by 1.1e-2 where the local output and the carried
+    term cancel)."""
+    b, d, N, L = 2, 256, 16, 4000
+    inp = W.random_scan_inputs(b, d, N, L, dtype=dtype, device=DEV, seed=51)
+    monkeypatch.setenv("SSM_FORCE_CHUNKS", "1")
+    one = ssm.scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["bias"])
+    monkeypatch.setenv("SSM_FORCE_CHUNKS", "6")
+    six = ssm.scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["bias"])
+    torch.cuda.synchronize()
+    # bf16: two output ulps; fp32: the omitted carry (< 2^-24 of the state) and the
+    # reassociated chunk boundary move outputs by a few fp32 ulps, kept 10x under the tolerance
+    bound = 2 * 2.0 ** -8 if dtype == torch.bfloat16 else 1e-5
+    e = rel_err(to_np(six), to_np(one))
+    assert e <= bound, f"chunked vs unchunked: {e:.3e}"
+
+
 def test_tiny_fp32_workload(kernel):
     inp = W.scan_inputs(W.SCAN_SHAPES["tiny_fp32"], device=DEV)
     full_compare(inp, TOL[torch.float32])
