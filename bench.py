@@ -46,7 +46,7 @@ FP32_OPS_PER_UPDATE = 6
 # from a capture of the current kernel at full size (13.49 GB read + 4.46 GB
 # written; profiles/scan_rows_kernel_long_1m_dram.md).  Set back to None when
 # the kernel changes until it is captured again.
-SCAN_DRAM_BYTES_PER_LAUNCH = 17.95e9
+SCAN_DRAM_BYTES_PER_LAUNCH = None
 
 
 def measured_peaks():

@@ -266,12 +266,34 @@ __device__ __forceinline__ void row_pass(Smem<T, RB>& sm, const RowParams& p, in
       float yv[8];
       float Sb = 0.f;
       float dlt8[8], gz8[8];
+      if (FAST) {  // per-token scalars first, two tokens per packed instruction
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {  // per-token scalars first: 8 independent MUFU chains
-        const bool tok_ok = t + v < t_valid;
-        const float rr = get8<T>(wd, v) + biasc;
-        dlt8[v] = tok_ok ? (FAST ? softplus_fast(rr) : softplus_precise(rr)) : 0.f;
-        gz8[v] = HAS_Z ? silu_t<FAST>(get8<T>(wz, v)) : 1.f;
+        for (int v = 0; v < 8; v += 2) {
+          const float2 rr = __fadd2_rn(make_float2(get8<T>(wd, v), get8<T>(wd, v + 1)), make_float2(biasc, biasc));
+          const float2 e = __fmul2_rn(rr, make_float2(kLog2e, kLog2e));
+          const float2 q = __fadd2_rn(make_float2(ex2_approx(e.x), ex2_approx(e.y)), make_float2(1.f, 1.f));
+          const float2 sp = __fmul2_rn(make_float2(lg2_approx(q.x), lg2_approx(q.y)), make_float2(kLn2, kLn2));
+          dlt8[v] = t + v < t_valid ? (rr.x > 15.f ? rr.x : sp.x) : 0.f;
+          dlt8[v + 1] = t + v + 1 < t_valid ? (rr.y > 15.f ? rr.y : sp.y) : 0.f;
+          if (HAS_Z) {
+            const float2 zz = make_float2(get8<T>(wz, v), get8<T>(wz, v + 1));
+            const float2 ez = __fmul2_rn(zz, make_float2(-kLog2e, -kLog2e));
+            const float2 dz = __fadd2_rn(make_float2(ex2_approx(ez.x), ex2_approx(ez.y)), make_float2(1.f, 1.f));
+            const float2 gz = __fmul2_rn(zz, make_float2(rcp_approx(dz.x), rcp_approx(dz.y)));
+            gz8[v] = gz.x;
+            gz8[v + 1] = gz.y;
+          } else {
+            gz8[v] = gz8[v + 1] = 1.f;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const bool tok_ok = t + v < t_valid;
+          const float rr = get8<T>(wd, v) + biasc;
+          dlt8[v] = tok_ok ? softplus_precise(rr) : 0.f;
+          gz8[v] = HAS_Z ? silu_precise(get8<T>(wz, v)) : 1.f;
+        }
       }
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
