@@ -63,6 +63,8 @@ def _load():
             lib.oracle_scan.restype = None
             lib.oracle_step.argtypes = [i64, i64, i64] + [dp] * 10 + [i64, i64]
             lib.oracle_step.restype = None
+            lib.oracle_scan_bwd.argtypes = [i64, i64, i64, i64] + [dp] * 21
+            lib.oracle_scan_bwd.restype = None
             lib.oracle_conv1d.argtypes = [i64, i64, i64, i64] + [dp] * 6 + [i64, i64]
             lib.oracle_conv1d.restype = None
             lib.oracle_conv1d_step.argtypes = [i64, i64, i64] + [dp] * 5 + [i64, i64]
@@ -123,6 +125,33 @@ def scan(u, delta, A, B, C, D=None, z=None, bias=None, h0=None, threads: int | N
         with ThreadPoolExecutor(len(ranges)) as ex:
             list(ex.map(lambda rg: lib.oracle_scan(*args, *rg), ranges))
     return out, hT
+
+
+def scan_bwd(u, delta, A, B, C, dout, D=None, z=None, bias=None, h0=None, dhT=None):
+    """Gradients of sum(dout * out) + sum(dhT * h_L) of ``scan`` with respect to
+    its inputs (plain reverse-mode loop, float64, one thread).
+
+    Returns a dict with du, ddelta, dz [batch, d_inner, L]; dA [d_inner, N];
+    dB, dC [batch, L, N]; dD, dbias [d_inner]; dh0 [batch, d_inner, N]
+    (entries for absent optional inputs are None).
+    """
+    u, delta, A, B, C, dout = (_f64(x) for x in (u, delta, A, B, C, dout))
+    D, z, bias, h0, dhT = (_f64(x) for x in (D, z, bias, h0, dhT))
+    batch, d_inner, L = u.shape
+    N = A.shape[1]
+    assert dout.shape == u.shape and delta.shape == u.shape and A.shape == (d_inner, N)
+    assert B.shape == (batch, L, N) and C.shape == (batch, L, N)
+    out = dict(du=np.empty_like(u), ddelta=np.empty_like(u), dA=np.zeros((d_inner, N)),
+               dB=np.zeros((batch, L, N)), dC=np.zeros((batch, L, N)),
+               dD=np.zeros(d_inner) if D is not None else None,
+               dz=np.empty_like(u) if z is not None else None,
+               dbias=np.zeros(d_inner), dh0=np.empty((batch, d_inner, N)))
+    work = np.empty((L + 1) * N)
+    lib = _load()
+    lib.oracle_scan_bwd(batch, d_inner, N, L, *(_ptr(v) for v in (u, delta, A, B, C, D, z, bias, h0, dout, dhT)),
+                        *(_ptr(out[k]) for k in ("du", "ddelta", "dA", "dB", "dC", "dD", "dz", "dbias", "dh0")),
+                        _ptr(work))
+    return out
 
 
 def step(state, x, delta, A, B, C, D=None, z=None, bias=None, threads: int | None = None):

@@ -81,3 +81,73 @@ def conv1d(x, w, bias=None, state0=None):
         pre += w[None, :, k, None] * xt[:, :, k:k + L]
     out = pre * expit(pre)
     return out, xt[:, :, L:].copy()
+
+
+def scan_bwd(u, delta, A, B, C, dout, D=None, z=None, bias=None, h0=None, dhT=None):
+    """Gradients of sum(dout * out) + sum(dhT * h_L) of ``scan``, written
+    independently of the C oracle: vectorised over (batch, channel, state),
+    sequential over t, with the step-size and A derivatives in factored form
+        dℓ/dΔ_t = Σ_n dh_t Ā_t (a h_{t-1} + B_t x_t)
+        dℓ/da   = Σ_t dh_t (Δ_t Ā_t h_{t-1} + B_t x_t (Δ_t Ā_t − φ_t)/a)   (a → 0: Δ h_{t-1} + B x Δ²/2)
+    (the chain rule on the zero-order hold of "State Space Models（SSM）とMamba" §2.2)."""
+    u, delta, A, B, C, dout = (_arr(x) for x in (u, delta, A, B, C, dout))
+    D, z, bias, h0, dhT = (_arr(x) for x in (D, z, bias, h0, dhT))
+    batch, d, L = u.shape
+    N = A.shape[1]
+    r = delta + (0.0 if bias is None else bias[None, :, None])
+    dt = np.logaddexp(0.0, r)                                     # [b, d, L]
+    a = A[None]                                                   # [1, d, N]
+    hs = np.zeros((L + 1, batch, d, N))
+    if h0 is not None:
+        hs[0] = h0
+    abar_all = np.empty((L, batch, d, N))
+    phi_all = np.empty((L, batch, d, N))
+    for t in range(L):
+        abar, phi = discretize(dt[:, :, t, None], a)
+        abar_all[t], phi_all[t] = abar, phi
+        hs[t + 1] = abar * hs[t] + phi * B[:, None, t, :] * u[:, :, t, None]
+    g = {k: None for k in ("du", "ddelta", "dz", "dA", "dB", "dC", "dD", "dbias", "dh0")}
+    g["du"] = np.empty_like(u)
+    g["ddelta"] = np.empty_like(u)
+    g["dB"] = np.zeros_like(B)
+    g["dC"] = np.zeros_like(C)
+    g["dA"] = np.zeros_like(A)
+    if D is not None:
+        g["dD"] = np.zeros(d)
+    if z is not None:
+        g["dz"] = np.empty_like(u)
+    dbias = np.zeros(d)
+    dh = np.zeros((batch, d, N)) if dhT is None else dhT.copy()
+    safe_a = np.where(a == 0.0, 1.0, a)
+    for t in range(L - 1, -1, -1):
+        x = u[:, :, t]
+        y = np.einsum("bdn,bn->bd", hs[t + 1], C[:, t])
+        if D is not None:
+            y = y + D[None] * x
+        dy = dout[:, :, t]
+        if z is not None:
+            s = expit(z[:, :, t])
+            g["dz"][:, :, t] = dout[:, :, t] * y * s * (1.0 + z[:, :, t] * (1.0 - s))
+            dy = dy * z[:, :, t] * s
+        dx = np.zeros_like(x) if D is None else dy * D[None]
+        if D is not None:
+            g["dD"] += (dy * x).sum(axis=0)
+        dh = dh + dy[:, :, None] * C[:, None, t, :]
+        g["dC"][:, t] += np.einsum("bd,bdn->bn", dy, hs[t + 1])
+        abar, phi = abar_all[t], phi_all[t]
+        bx = B[:, None, t, :] * x[:, :, None]                     # B x, [b, d, N]
+        g["dB"][:, t] += np.einsum("bdn,bdn,bd->bn", dh, phi, x)
+        dx = dx + np.einsum("bdn,bdn,bn->bd", dh, phi, B[:, t])
+        dtn = dt[:, :, t, None]
+        ddt = (dh * abar * (a * hs[t] + bx)).sum(axis=2)
+        da = np.where(a == 0.0, dh * (dtn * hs[t] + bx * dtn * dtn / 2.0),
+                      dh * (dtn * abar * hs[t] + bx * (dtn * abar - phi) / safe_a))
+        g["dA"] += da.sum(axis=0)
+        g["du"][:, :, t] = dx
+        dr = ddt * expit(r[:, :, t])
+        g["ddelta"][:, :, t] = dr
+        dbias += dr.sum(axis=0)
+        dh = dh * abar
+    g["dbias"] = dbias
+    g["dh0"] = dh
+    return g

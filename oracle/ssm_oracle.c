@@ -181,3 +181,103 @@ void oracle_conv1d_step(int64_t batch, int64_t d_inner, int64_t W, double* state
     for (int64_t k = 0; k < W - 1; ++k) state[r * (W - 1) + k] = win[k + 1];
   }
 }
+
+/*
+ * Backward of the scan: the gradients of the scalar loss
+ *   ℓ = Σ_{b,c,t} dout[b,c,t] · out[b,c,t]  +  Σ_{b,c,n} dhT[b,c,n] · h_L[b,c,n]
+ * with respect to every input, by reverse-mode differentiation of the loop of
+ * oracle_scan written out: the forward states h_0..h_L of a row are kept, then
+ * t runs backwards carrying dℓ/dh_t.  Per token (a = A[c,n], Ā = exp(Δa),
+ * φ = expm1(Δa)/a, or Δ when a = 0, q = φ B x, h_t = Ā h_{t-1} + q):
+ *   dy = dout·silu(z), dz = dout·y·silu'(z), dD += dy x, dx = dy D
+ *   dh_t += dy C_t;  dC_t += dy h_t
+ *   dĀ = dh_t h_{t-1}, dφ = dh_t B x;  dB_t += dh_t φ x;  dx += dh_t φ B
+ *   dΔ += dĀ a Ā + dφ Ā;  da += dĀ Δ Ā + dφ (Δ Ā − φ)/a   (a = 0: dΔ += dφ, da += dĀ Δ + dφ Δ²/2)
+ *   dh_{t-1} = Ā dh_t
+ *   dΔraw = dΔ · sigmoid(Δraw + bias);  dbias += dΔraw
+ * and dh0 = dℓ/dh_0.  This is the plain chain rule on the definition of
+ * oracle_scan; the pages describe the backward only as recomputing the states
+ * instead of storing them ("Mambaとは？…", section Selective Scanは選択機構そのもの
+ * ではない, hardware-aware parallel scan).
+ *
+ * du, ddelta, dz, dh0 are written; dA [d_inner][N], dB, dC [batch][L][N], dD and
+ * dbias [d_inner] are accumulated (the caller zeroes them).  z, D, bias, h0, dhT
+ * and the matching outputs may be NULL.  work: (L + 1) * N doubles.
+ * Rows are processed in order (the accumulations are shared).
+ */
+static double dsilu(double z) {
+  const double s = sigmoid(z);
+  return s * (1.0 + z * (1.0 - s));
+}
+
+void oracle_scan_bwd(int64_t batch, int64_t d_inner, int64_t N, int64_t L, const double* u, const double* delta,
+                     const double* A, const double* B, const double* C, const double* D, const double* z,
+                     const double* bias, const double* h0, const double* dout, const double* dhT, double* du,
+                     double* ddelta, double* dA, double* dB, double* dC, double* dD, double* dz, double* dbias,
+                     double* dh0, double* work) {
+  double dh[1024];
+  if (N > 1024) return;
+  for (int64_t r = 0; r < batch * d_inner; ++r) {
+    const int64_t b = r / d_inner, c = r % d_inner;
+    const double bc = bias ? bias[c] : 0.0;
+    double* H = work;  // H[t * N + n] = h_t[n], t = 0..L
+    for (int64_t n = 0; n < N; ++n) H[n] = h0 ? h0[r * N + n] : 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+      const int64_t i = r * L + t;
+      const double dtv = softplus(delta[i] + bc);
+      for (int64_t n = 0; n < N; ++n) {
+        const double a = A[c * N + n];
+        const double abar = exp(dtv * a);
+        const double phi = (a != 0.0) ? expm1(dtv * a) / a : dtv;
+        H[(t + 1) * N + n] = abar * H[t * N + n] + phi * B[(b * L + t) * N + n] * u[i];
+      }
+    }
+    for (int64_t n = 0; n < N; ++n) dh[n] = dhT ? dhT[r * N + n] : 0.0;
+    for (int64_t t = L - 1; t >= 0; --t) {
+      const int64_t i = r * L + t;
+      const double* Bt = B + (b * L + t) * N;
+      const double* Ct = C + (b * L + t) * N;
+      const double x = u[i];
+      const double rr = delta[i] + bc;
+      const double dtv = softplus(rr);
+      double y = 0.0;
+      for (int64_t n = 0; n < N; ++n) y += Ct[n] * H[(t + 1) * N + n];
+      if (D) y += D[c] * x;
+      double dy = dout[i];
+      if (z) {
+        dy = dout[i] * silu(z[i]);
+        if (dz) dz[i] = dout[i] * y * dsilu(z[i]);
+      }
+      double dx = 0.0, ddt = 0.0;
+      if (D) {
+        if (dD) dD[c] += dy * x;
+        dx = dy * D[c];
+      }
+      for (int64_t n = 0; n < N; ++n) {
+        const double a = A[c * N + n];
+        const double abar = exp(dtv * a);
+        const double phi = (a != 0.0) ? expm1(dtv * a) / a : dtv;
+        dh[n] += dy * Ct[n];
+        dC[(b * L + t) * N + n] += dy * H[(t + 1) * N + n];
+        const double dabar = dh[n] * H[t * N + n];
+        const double dphi = dh[n] * Bt[n] * x;
+        dB[(b * L + t) * N + n] += dh[n] * phi * x;
+        dx += dh[n] * phi * Bt[n];
+        if (a != 0.0) {
+          ddt += dabar * a * abar + dphi * abar;
+          dA[c * N + n] += dabar * dtv * abar + dphi * (dtv * abar - phi) / a;
+        } else {
+          ddt += dphi;
+          dA[c * N + n] += dabar * dtv + dphi * dtv * dtv / 2.0;
+        }
+        dh[n] *= abar;
+      }
+      du[i] = dx;
+      const double dr = ddt * sigmoid(rr);
+      ddelta[i] = dr;
+      if (dbias) dbias[c] += dr;
+    }
+    if (dh0)
+      for (int64_t n = 0; n < N; ++n) dh0[r * N + n] = dh[n];
+  }
+}
