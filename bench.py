@@ -303,6 +303,52 @@ def bench_workloads(dev, runs=20):
     return res
 
 
+def bench_scan_bwd(dev, hbm_peak, runs=10):
+    """Backward of the scan on the two training-shaped layers, each call timed
+    alone after an L2 flush (median).  Algorithmic bytes: u, delta, z, dout read and
+    du, delta and z gradients written once per (batch, channel, token), B and C read
+    and their fp32 gradients written once per (batch, token, state)."""
+    import selective_state_space_154_b300 as ssm
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {"note": "states recomputed from checkpoints every 8 tokens (workspace); rows are the only "
+                   "parallelism (no split along the sequence yet); median of 10, L2 flushed before each"}
+    for name in ("mamba130m_layer", "mamba2p8b_layer"):
+        shape = W.SCAN_SHAPES[name]
+        inp = W.scan_inputs(shape, device=dev, seed=0)
+        gen = torch.Generator(device=dev).manual_seed(1)
+        dout = torch.randn(inp["u"].shape, generator=gen, device=dev).to(shape.dtype)
+        g = dict(du=torch.empty_like(inp["u"]), ddelta=torch.empty_like(inp["u"]), dz=torch.empty_like(inp["u"]),
+                 dA=torch.empty_like(inp["A"]), dB=torch.empty(inp["B"].shape, device=dev),
+                 dC=torch.empty(inp["C"].shape, device=dev), dD=torch.empty_like(inp["D"]),
+                 dbias=torch.empty(shape.d_inner, device=dev))
+        ws = torch.empty(max(16, ssm.ssm_scan_bwd_workspace_bytes(shape.batch, shape.d_inner, shape.d_state,
+                                                                  shape.seqlen, shape.dtype)),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            ssm.ssm_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["bias"],
+                             dout, g["du"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"], g["dz"], g["dbias"],
+                             workspace=ws, stream=stream)
+
+        call()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
+        for a, b in evs:
+            flush()
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize()
+        secs = statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+        ct = shape.channel_tokens
+        alg = 7 * ct * 2 + shape.batch * shape.seqlen * shape.d_state * (2 * 2 + 2 * 4)
+        res[name] = {"batch": shape.batch, "d_inner": shape.d_inner, "d_state": shape.d_state,
+                     "seq_len": shape.seqlen, "us": secs * 1e6, "channel_tokens_per_s": ct / secs,
+                     "gbs": alg / secs / 1e9, "hbm_frac": alg / secs / 1e9 / hbm_peak, "alg_bytes": alg}
+        del inp, dout, g, ws
+    return res
+
+
 def conv_alg_bytes(rows, L, width, esz):
     """x read and out written once per (row, token), the carried state read and
     the final state written once per row (weight and bias are added by the caller)."""
@@ -493,6 +539,7 @@ def run_ours(args):
     decode = bench_decode(dev) if rank == 0 else None
     others = bench_workloads(dev) if rank == 0 else None
     conv = bench_conv(dev, hbm_peak) if rank == 0 else None
+    bwd = bench_scan_bwd(dev, hbm_peak) if rank == 0 else None
     cpu = cpu_baseline() if (rank == 0 and world == 1) else None
 
     if rank == 0:
@@ -525,6 +572,7 @@ def run_ours(args):
                           **({k: dict(v, hbm_frac=v["gbs"] / hbm_peak) for k, v in others.items()}
                              if others else {})},
             "conv1d": conv,
+            "scan_bwd": bwd,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -126,6 +126,32 @@ SSM_API ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, con
                                    ssm_stream_t stream);
 
 /*
+ * Backward of ssm_scan_fwd (from h = 0): the gradients of ℓ = Σ dout·out with
+ * respect to every input, the states being recomputed from checkpoints in the
+ * workspace instead of stored ("Mambaとは？Transformer以外の系列モデル", section
+ * Selective Scanは選択機構そのものではない: recomputation as the third
+ * hardware-aware ingredient).  d_state ≤ 16 (SSM_ERR_UNSUPPORTED above).
+ *   Inputs as for ssm_scan_fwd, plus dout [batch][d_inner][seqlen] (act dtype).
+ *   du, ddelta: [batch][d_inner][seqlen], act dtype (ddelta is dℓ/dΔraw).
+ *   dz: same shape, required when z is given (else ignored and may be NULL).
+ *   dA: [d_inner][d_state] float32; dB, dC: [batch][seqlen][d_state] float32.
+ *   dD: [d_inner] float32, required when D is given; ddelta_bias: [d_inner]
+ *     float32 or NULL (dℓ/dbias, whether or not delta_bias is given).
+ *   The call zeroes dA, dB, dC, dD and ddelta_bias, then accumulates into them
+ *   (the sums over batch and channels use atomic adds, so their last bits may
+ *   differ from call to call).
+ *   workspace: at least ssm_scan_bwd_workspace_bytes(dims) bytes, 16-byte
+ *   aligned, caller-owned; it holds the state every 8 tokens of every row.
+ * Outputs must not overlap inputs or each other.
+ */
+SSM_API size_t ssm_scan_bwd_workspace_bytes(const ssm_dims* dims);
+SSM_API ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B,
+                                const void* C, const float* D, const void* z, const float* delta_bias,
+                                const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC,
+                                float* dD, void* dz, float* ddelta_bias, const ssm_dims* dims, void* workspace,
+                                size_t workspace_bytes, ssm_stream_t stream);
+
+/*
  * Recurrent (decode) mode: one token for every (batch, channel) row, updating
  * `state` in place (h ← Ā h + B̄ x) and writing out = (C·h + D x) · silu(z).
  *   state, x, delta, A, B, C, out, dims: required (dims->seqlen is ignored).

@@ -21,6 +21,7 @@ __all__ = [
     "ssm_status_string", "scan_fwd", "step", "library_path", "load_library", "ssm_scan_fwd_noalloc",
     "SSM_NOALLOC_SCRATCH_BYTES", "ssm_step_check", "ssm_scan_fwd_from_state",
     "ssm_conv1d_fwd", "ssm_conv1d_step", "conv1d", "conv1d_step",
+    "ssm_scan_bwd_workspace_bytes", "ssm_scan_bwd", "scan_bwd",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -77,6 +78,10 @@ def load_library():
             lib.ssm_step_check.restype = i32
             lib.ssm_scan_fwd_noalloc.argtypes = [vp] * 10 + [dp, vp]
             lib.ssm_scan_fwd_noalloc.restype = i32
+            lib.ssm_scan_bwd_workspace_bytes.argtypes = [dp]
+            lib.ssm_scan_bwd_workspace_bytes.restype = sz
+            lib.ssm_scan_bwd.argtypes = [vp] * 17 + [dp, vp, sz, vp]
+            lib.ssm_scan_bwd.restype = i32
             lib.ssm_conv1d_fwd.argtypes = [vp] * 6 + [dp, i32, vp]
             lib.ssm_conv1d_fwd.restype = i32
             lib.ssm_conv1d_step.argtypes = [vp] * 5 + [dp, i32, vp]
@@ -235,6 +240,62 @@ def ssm_step(state, x, delta, A, B, C, D, z, delta_bias, out, stream=None):
                           _ptr(delta_bias), _ptr(out), ctypes.byref(dims), _stream_handle(stream, dev))
     if st != SSM_OK:
         raise SsmError(st, "ssm_step")
+
+
+def ssm_scan_bwd_workspace_bytes(batch, d_inner, d_state, seqlen, dtype=torch.bfloat16) -> int:
+    d = _dims(batch, d_inner, d_state, seqlen, dtype)
+    return int(load_library().ssm_scan_bwd_workspace_bytes(ctypes.byref(d)))
+
+
+def ssm_scan_bwd(u, delta, A, B, C, D, z, delta_bias, dout, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias,
+                 workspace=None, stream=None):
+    """Backward of the scan into caller-provided gradient tensors (see include/ssm_scan.h)."""
+    lib = load_library()
+    batch, d_inner, L = u.shape
+    N = A.shape[1]
+    act, dev = u.dtype, u.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    for name, t in (("u", u), ("delta", delta), ("dout", dout), ("du", du), ("ddelta", ddelta)):
+        _check(t, name, act, (batch, d_inner, L), dev)
+    _check(z, "z", act, (batch, d_inner, L), dev, required=False)
+    _check(dz, "dz", act, (batch, d_inner, L), dev, required=z is not None)
+    _check(A, "A", torch.float32, (d_inner, N), dev)
+    _check(dA, "dA", torch.float32, (d_inner, N), dev)
+    for name, t in (("B", B), ("C", C)):
+        _check(t, name, act, (batch, L, N), dev)
+    for name, t in (("dB", dB), ("dC", dC)):
+        _check(t, name, torch.float32, (batch, L, N), dev)
+    _check(D, "D", torch.float32, (d_inner,), dev, required=False)
+    _check(dD, "dD", torch.float32, (d_inner,), dev, required=D is not None)
+    _check(delta_bias, "delta_bias", torch.float32, (d_inner,), dev, required=False)
+    _check(ddelta_bias, "ddelta_bias", torch.float32, (d_inner,), dev, required=False)
+    dims = _dims(batch, d_inner, N, L, act)
+    with torch.cuda.device(dev):
+        need = int(lib.ssm_scan_bwd_workspace_bytes(ctypes.byref(dims)))
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        ws_bytes = workspace.numel() * workspace.element_size()
+        st = lib.ssm_scan_bwd(*(_ptr(t) for t in (u, delta, A, B, C, D, z, delta_bias, dout, du, ddelta, dA, dB, dC,
+                                                 dD, dz, ddelta_bias)),
+                              ctypes.byref(dims), _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
+    if st != SSM_OK:
+        raise SsmError(st, "ssm_scan_bwd")
+    return workspace
+
+
+def scan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None, stream=None):
+    """Allocate the gradients and run ``ssm_scan_bwd``; returns a dict like the oracle's."""
+    g = dict(du=torch.empty_like(u), ddelta=torch.empty_like(u),
+             dA=torch.empty(A.shape, dtype=torch.float32, device=u.device),
+             dB=torch.empty(B.shape, dtype=torch.float32, device=u.device),
+             dC=torch.empty(C.shape, dtype=torch.float32, device=u.device),
+             dD=torch.empty_like(D) if D is not None else None,
+             dz=torch.empty_like(u) if z is not None else None,
+             dbias=torch.empty((u.shape[1],), dtype=torch.float32, device=u.device))
+    ssm_scan_bwd(u, delta, A, B, C, D, z, delta_bias, dout, g["du"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"],
+                 g["dz"], g["dbias"], stream=stream)
+    return g
 
 
 def _conv_dims(x, batch, d_inner, seqlen):

@@ -1,6 +1,7 @@
 // C ABI of the selective-scan library: argument validation, launch planning,
 // status codes.  Declarations and the meaning of every argument are in
 // include/ssm_scan.h.
+#include <climits>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -226,6 +227,49 @@ ssm_status ssm_conv1d_step(void* conv_state, const void* x, const float* weight,
   if (!aligned(weight, 4) || (bias && !aligned(bias, 4))) return SSM_ERR_ALIGNMENT;
   const ssm::ConvCall k = conv_call(x, weight, bias, nullptr, out, conv_state, dims, width, false);
   return ssm::conv1d_step_launch(k, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+size_t ssm_scan_bwd_workspace_bytes(const ssm_dims* dims) {
+  if (check_dims(dims, true) != SSM_OK || dims->d_state > 16) return 0;
+  return ssm::scan_bwd_workspace_bytes(dims->batch, dims->d_inner, dims->seqlen);
+}
+
+ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* delta_bias, const void* dout, void* du,
+                        void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz, float* ddelta_bias,
+                        const ssm_dims* dims, void* workspace, size_t workspace_bytes, ssm_stream_t stream) {
+  const ssm_status ds = check_dims(dims, true);
+  if (ds != SSM_OK) return ds;
+  if (dims->d_state > 16) return SSM_ERR_UNSUPPORTED;
+  if (!u || !delta || !A || !B || !C || !dout || !du || !ddelta || !dA || !dB || !dC) return SSM_ERR_INVALID_ARG;
+  if ((D && !dD) || (z && !dz)) return SSM_ERR_INVALID_ARG;
+  const unsigned esz = dims->act == SSM_DTYPE_BF16 ? 2u : 4u;
+  const void* act_ptrs[] = {u, delta, B, C, z, dout, du, ddelta, dz};
+  for (const void* p : act_ptrs)
+    if (p && !aligned(p, esz)) return SSM_ERR_ALIGNMENT;
+  const void* f32_ptrs[] = {A, D, delta_bias, dA, dB, dC, dD, ddelta_bias};
+  for (const void* p : f32_ptrs)
+    if (p && !aligned(p, 4)) return SSM_ERR_ALIGNMENT;
+  const size_t need = ssm::scan_bwd_workspace_bytes(dims->batch, dims->d_inner, dims->seqlen);
+  if (!workspace || workspace_bytes < need) return SSM_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return SSM_ERR_ALIGNMENT;
+  const int64_t ctiles = (dims->d_inner + 127) / 128;
+  if (dims->batch * ctiles > INT32_MAX) return SSM_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t b = dims->batch, d = dims->d_inner, N = dims->d_state, L = dims->seqlen;
+  // accumulated gradients start at zero
+  if (cudaMemsetAsync(dA, 0, sizeof(float) * d * N, st) != cudaSuccess ||
+      cudaMemsetAsync(dB, 0, sizeof(float) * b * L * N, st) != cudaSuccess ||
+      cudaMemsetAsync(dC, 0, sizeof(float) * b * L * N, st) != cudaSuccess ||
+      (dD && cudaMemsetAsync(dD, 0, sizeof(float) * d, st) != cudaSuccess) ||
+      (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, sizeof(float) * d, st) != cudaSuccess))
+    return SSM_ERR_CUDA;
+  ssm::BwdArgs a{};
+  a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.bias = delta_bias; a.dout = dout;
+  a.du = du; a.ddelta = ddelta; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dz = dz; a.dbias = ddelta_bias;
+  a.ckpt = static_cast<float*>(workspace);
+  a.batch = b; a.d_inner = d; a.N = N; a.L = L; a.act = dims->act;
+  return ssm::scan_bwd_launch(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 ssm_status ssm_step_check(ssm_stream_t stream) {

@@ -115,6 +115,33 @@ constexpr int64_t kMaxConvGridYZ = 65535;  // d_inner and batch index grid dimen
 cudaError_t conv1d_fwd_launch(const ConvCall& k, cudaStream_t stream);
 cudaError_t conv1d_step_launch(const ConvCall& k, cudaStream_t stream);
 
+// Backward of the scan (scan_bwd.cu).  dA, dB, dC, dD, dbias are accumulated
+// (zeroed by the caller); ckpt is the workspace of scan_bwd_workspace_bytes().
+struct BwdArgs {
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* bias;
+  const void* dout;
+  void* du;
+  void* ddelta;
+  float* dA;
+  float* dB;
+  float* dC;
+  float* dD;
+  void* dz;
+  float* dbias;
+  float* ckpt;
+  int64_t batch, d_inner, N, L, nblk;
+  int ctiles, act;
+};
+size_t scan_bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L);
+cudaError_t scan_bwd_launch(BwdArgs p, cudaStream_t stream);
+
 // Reads and clears the sticky error word of the pipelined step kernel (current device).
 cudaError_t step_error_fetch_clear(unsigned* word);
 
