@@ -253,8 +253,8 @@ ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const 
   const size_t need = ssm::scan_bwd_workspace_bytes(dims->batch, dims->d_inner, dims->seqlen);
   if (!workspace || workspace_bytes < need) return SSM_ERR_WORKSPACE;
   if (!aligned16(workspace)) return SSM_ERR_ALIGNMENT;
-  const int64_t ctiles = (dims->d_inner + 127) / 128;
-  if (dims->batch * ctiles > INT32_MAX) return SSM_ERR_UNSUPPORTED;
+  const int64_t rpc = ssm::scan_bwd_rows_per_cta();
+  if (dims->batch * ((dims->d_inner + rpc - 1) / rpc) > INT32_MAX) return SSM_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int64_t b = dims->batch, d = dims->d_inner, N = dims->d_state, L = dims->seqlen;
   // accumulated gradients start at zero

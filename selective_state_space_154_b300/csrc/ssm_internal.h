@@ -140,6 +140,7 @@ struct BwdArgs {
   int ctiles, act;
 };
 size_t scan_bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L);
+int scan_bwd_rows_per_cta();
 cudaError_t scan_bwd_launch(BwdArgs p, cudaStream_t stream);
 
 // Reads and clears the sticky error word of the pipelined step kernel (current device).
