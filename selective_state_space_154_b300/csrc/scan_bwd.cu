@@ -163,6 +163,17 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
   // this thread's checkpoints: [nblk] float4 (its quad of the row's state)
   float4* ck = reinterpret_cast<float4*>(p.ckpt) + ((int64_t)blockIdx.x * kBwdThreads + threadIdx.x) * nblk;
 
+  // packed path: bf16 arithmetic and no A = 0 state among this thread's four
+  const bool packed = FAST && a[0] != 0.f && a[1] != 0.f && a[2] != 0.f && a[3] != 0.f;
+  const float2 aP[2] = {make_float2(a[0], a[1]), make_float2(a[2], a[3])};
+  const float2 iaP[2] = {make_float2(ia[0], ia[1]), make_float2(ia[2], ia[3])};
+  // Ā - 1 and Ā of states (2j, 2j+1) at step size dt (packed path)
+  auto disc2 = [&](float dt, int j, float2& abar, float2& phi) {
+    const float dl = dt * kLog2e;
+    const float2 e = __fmul2_rn(make_float2(dl, dl), aP[j]);
+    abar = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+    phi = __fmul2_rn(__fadd2_rn(abar, make_float2(-1.f, -1.f)), iaP[j]);
+  };
   auto discretise = [&](float dt, int k, float& abar, float& phi) {
     if (a[k] != 0.f) {
       abar = FAST ? ex2_approx(dt * a[k] * kLog2e) : expf(dt * a[k]);
@@ -185,11 +196,24 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     __syncthreads();
     for (int v = 0; v < nv; ++v) {
       const TokScalars s = sm.ts[v][r];
+      if (packed) {
+        const float2 xx = make_float2(s.x, s.x);
 #pragma unroll
-      for (int k = 0; k < kBwdG; ++k) {
-        float abar, phi;
-        discretise(s.dt, k, abar, phi);
-        h[k] = fmaf(abar, h[k], phi * sm.bc[v][0][kBwdG * g + k] * s.x);
+        for (int j = 0; j < 2; ++j) {
+          float2 abar, phi;
+          disc2(s.dt, j, abar, phi);
+          const float2 bb = *reinterpret_cast<const float2*>(&sm.bc[v][0][kBwdG * g + 2 * j]);
+          const float2 hh = __ffma2_rn(abar, make_float2(h[2 * j], h[2 * j + 1]), __fmul2_rn(__fmul2_rn(phi, bb), xx));
+          h[2 * j] = hh.x;
+          h[2 * j + 1] = hh.y;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < kBwdG; ++k) {
+          float abar, phi;
+          discretise(s.dt, k, abar, phi);
+          h[k] = fmaf(abar, h[k], phi * sm.bc[v][0][kBwdG * g + k] * s.x);
+        }
       }
     }
   }
@@ -210,11 +234,24 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     // recompute the block's states
     for (int v = 0; v < nv; ++v) {
       const TokScalars s = sm.ts[v][r];
+      if (packed) {
+        const float2 xx = make_float2(s.x, s.x);
 #pragma unroll
-      for (int k = 0; k < kBwdG; ++k) {
-        float abar, phi;
-        discretise(s.dt, k, abar, phi);
-        h[k] = fmaf(abar, h[k], phi * sm.bc[v][0][kBwdG * g + k] * s.x);
+        for (int j = 0; j < 2; ++j) {
+          float2 abar, phi;
+          disc2(s.dt, j, abar, phi);
+          const float2 bb = *reinterpret_cast<const float2*>(&sm.bc[v][0][kBwdG * g + 2 * j]);
+          const float2 hh = __ffma2_rn(abar, make_float2(h[2 * j], h[2 * j + 1]), __fmul2_rn(__fmul2_rn(phi, bb), xx));
+          h[2 * j] = hh.x;
+          h[2 * j + 1] = hh.y;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < kBwdG; ++k) {
+          float abar, phi;
+          discretise(s.dt, k, abar, phi);
+          h[k] = fmaf(abar, h[k], phi * sm.bc[v][0][kBwdG * g + k] * s.x);
+        }
       }
       sm.hs[v + 1][r][g] = make_float4(h[0], h[1], h[2], h[3]);
     }
@@ -235,6 +272,40 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
       const float dy = s.dy;
       float dx = 0.f, ddt = 0.f;
       float slots[8];  // [0..3] dB, [4..7] dC of this thread's states
+      if (packed) {
+        const float2 dy2 = make_float2(dy, dy), xx = make_float2(s.x, s.x), dt2 = make_float2(s.dt, s.dt);
+        float2 dx2 = make_float2(0.f, 0.f), ddt2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int n = kBwdG * g + 2 * j;
+          const float2 Bn = *reinterpret_cast<const float2*>(&sm.bc[v][0][n]);
+          const float2 Cn = *reinterpret_cast<const float2*>(&sm.bc[v][1][n]);
+          const float2 hv2 = make_float2(hv[2 * j], hv[2 * j + 1]), hp2 = make_float2(hp[2 * j], hp[2 * j + 1]);
+          const float2 gk = __ffma2_rn(dy2, Cn, make_float2(dh[2 * j], dh[2 * j + 1]));
+          const float2 sc = __fmul2_rn(dy2, hv2);
+          float2 abar, phi;
+          disc2(s.dt, j, abar, phi);
+          const float2 bx = __fmul2_rn(Bn, xx);
+          const float2 gphi = __fmul2_rn(gk, phi);
+          const float2 sb = __fmul2_rn(gphi, xx);
+          dx2 = __ffma2_rn(gphi, Bn, dx2);
+          ddt2 = __ffma2_rn(__fmul2_rn(gk, abar), __ffma2_rn(aP[j], hp2, bx), ddt2);
+          const float2 dta = __fmul2_rn(dt2, abar);
+          const float2 tb = __fmul2_rn(__fmul2_rn(bx, __fadd2_rn(dta, make_float2(-phi.x, -phi.y))), iaP[j]);
+          const float2 da = __fmul2_rn(gk, __ffma2_rn(dta, hp2, tb));
+          dA_acc[2 * j] += da.x;
+          dA_acc[2 * j + 1] += da.y;
+          const float2 dhn = __fmul2_rn(gk, abar);
+          dh[2 * j] = dhn.x;
+          dh[2 * j + 1] = dhn.y;
+          slots[2 * j] = sb.x;
+          slots[2 * j + 1] = sb.y;
+          slots[4 + 2 * j] = sc.x;
+          slots[4 + 2 * j + 1] = sc.y;
+        }
+        dx = dx2.x + dx2.y;
+        ddt = ddt2.x + ddt2.y;
+      } else
 #pragma unroll
       for (int k = 0; k < kBwdG; ++k) {
         const int n = kBwdG * g + k;
