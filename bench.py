@@ -596,6 +596,24 @@ def run_profile_case(args):
         fn = lambda: ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
                                       inp["bias"], out, None, workspace=ws)
         units = shape.channel_tokens
+    elif args.only == "bwd":
+        base = W.SCAN_SHAPES[args.workload]
+        shape = W.ScanShape(base.name, base.batch, args.dinner or base.d_inner, base.d_state, args.seqlen or base.seqlen,
+                            base.dtype)
+        inp = W.scan_inputs(shape, device=dev, seed=0)
+        gen = torch.Generator(device=dev).manual_seed(1)
+        dout = torch.randn(inp["u"].shape, generator=gen, device=dev).to(shape.dtype)
+        gr = dict(du=torch.empty_like(inp["u"]), ddelta=torch.empty_like(inp["u"]), dz=torch.empty_like(inp["u"]),
+                  dA=torch.empty_like(inp["A"]), dB=torch.empty(inp["B"].shape, device=dev),
+                  dC=torch.empty(inp["C"].shape, device=dev), dD=torch.empty_like(inp["D"]),
+                  dbias=torch.empty(shape.d_inner, device=dev))
+        ws = torch.empty(max(16, ssm.ssm_scan_bwd_workspace_bytes(shape.batch, shape.d_inner, shape.d_state,
+                                                                  shape.seqlen, shape.dtype)), dtype=torch.uint8,
+                         device=dev)
+        fn = lambda: ssm.ssm_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                      inp["bias"], dout, gr["du"], gr["ddelta"], gr["dA"], gr["dB"], gr["dC"],
+                                      gr["dD"], gr["dz"], gr["dbias"], workspace=ws)
+        units = shape.channel_tokens
     elif args.only == "conv":
         base = W.SCAN_SHAPES[args.workload]
         L = args.seqlen or base.seqlen
@@ -654,14 +672,14 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "scan", "decode", "conv"], default="all",
-                    help="profiling aid: run only the scan, the decode step or the Conv1D (no JSON line)")
+    ap.add_argument("--only", choices=["all", "scan", "decode", "conv", "bwd"], default="all",
+                    help="profiling aid: run only the scan, the decode step, the Conv1D or the backward (no JSON line)")
     ap.add_argument("--seqlen", type=int, default=None,
                     help="profiling aid: scan another sequence length of the same workload")
     ap.add_argument("--dinner", type=int, default=None,
                     help="profiling aid: scan another number of channels of the same workload")
     ap.add_argument("--workload", choices=sorted(W.SCAN_SHAPES), default=WORKLOAD,
-                    help="profiling aid: the workload --only scan / --only conv runs")
+                    help="profiling aid: the workload --only scan / conv / bwd runs")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
