@@ -43,10 +43,10 @@ FP32_LANES_PER_SM = 128
 # Δ·A, Ā-1, x·(1/A), (x/A)·B + h, (Ā-1)·s + h, C·h accumulate (the exp is on the MUFU pipe).
 FP32_OPS_PER_UPDATE = 6
 # ncu DRAM bytes (read + write) per launch of the scan kernel on this workload,
-# from a capture of the current kernel at full size (13.49 GB read + 4.46 GB
+# from a capture of the current kernel at full size (13.52 GB read + 4.45 GB
 # written; profiles/scan_rows_kernel_long_1m_dram.md).  Set back to None when
 # the kernel changes until it is captured again.
-SCAN_DRAM_BYTES_PER_LAUNCH = None
+SCAN_DRAM_BYTES_PER_LAUNCH = 17.97e9
 
 
 def measured_peaks():
