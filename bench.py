@@ -311,8 +311,9 @@ def bench_scan_bwd(dev, hbm_peak, runs=10):
     import selective_state_space_154_b300 as ssm
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
-    res = {"note": "states recomputed from checkpoints every 8 tokens (workspace); rows are the only "
-                   "parallelism (no split along the sequence yet); median of 10, L2 flushed before each"}
+    res = {"note": "states recomputed from checkpoints every 8 tokens (workspace); the sequence is split "
+                   "into chunks combined from per-chunk summaries (two launches); median of 10, L2 flushed "
+                   "before each"}
     for name in ("mamba130m_layer", "mamba2p8b_layer"):
         shape = W.SCAN_SHAPES[name]
         inp = W.scan_inputs(shape, device=dev, seed=0)

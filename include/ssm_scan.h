@@ -141,7 +141,10 @@ SSM_API ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, con
  *   (the sums over batch and channels use atomic adds, so their last bits may
  *   differ from call to call).
  *   workspace: at least ssm_scan_bwd_workspace_bytes(dims) bytes, 16-byte
- *   aligned, caller-owned; it holds the state every 8 tokens of every row.
+ *   aligned, caller-owned; it holds the state every 8 tokens of every row and,
+ *   the sequence being split into chunks that run in parallel, each chunk's
+ *   end state, Δ sum and outgoing adjoint (at most 32 chunks of ≥ 16 tokens).
+ * Two kernel launches on `stream` after the zeroing copies; no host sync.
  * Outputs must not overlap inputs or each other.
  */
 SSM_API size_t ssm_scan_bwd_workspace_bytes(const ssm_dims* dims);

@@ -13,16 +13,27 @@
 //   dΔraw = dΔ·sigmoid(Δraw + bias), dbias += dΔraw.
 //
 // Organisation: four threads per (batch, channel) row, four states each; a CTA
-// holds kBwdRows rows of one batch.  Pass one runs the scan forward and saves
-// the state every kBwdTok tokens to the workspace.  Pass two walks the
-// kBwdTok-token blocks backwards: it reloads the block's starting state,
-// recomputes the block's states into shared memory, and runs the adjoint
-// recurrence over the block in reverse.  Per (row, token) scalars (Δ, x, the
-// gate terms) are evaluated once per row into shared memory; sums over a row's
-// states take two shuffles; the sums of dB and dC over channels are reduced
-// across the warp's rows (reduce-scatter by shuffles), across the CTA's warps in
-// shared memory, and added to global memory once per CTA; dA, dD and dbias are
-// accumulated in registers over the whole sequence and added once per row.
+// holds kBwdRows rows of one batch and one chunk of the sequence, so that the
+// grid is (row tiles) × (chunks) and short batches still fill the GPU.  Two
+// launches, neither waiting on another CTA:
+//   1. scan_bwd_chunk_kernel runs each chunk forward from h = 0 and saves, every
+//      kBwdTok tokens, that local state and the Δ summed since the chunk's start;
+//      at the chunk's end it saves the local end state, the chunk's ΣΔ and the
+//      adjoint the chunk sends to its left neighbour when nothing comes in from
+//      its right, Σ_t (Π_{s≤t} Ā_s) dy_t C_t (the adjoint is linear in what
+//      comes in and needs no state, so it can be summed in forward order).
+//   2. scan_bwd_kernel first combines the chunks' summaries: the true state
+//      entering its chunk, h_in = Σ_{j<k} (Π_{j<i<k} e^{a S_i}) H_j, and the true
+//      adjoint entering from the right.  It then walks its chunk's kBwdTok-token
+//      blocks backwards: it rebuilds the block's starting state as
+//      local + e^{a ΣΔ} h_in, recomputes the block's states into shared memory,
+//      and runs the adjoint recurrence over the block in reverse.
+// Per (row, token) scalars (Δ, x, the gate terms) are evaluated once per row
+// into shared memory; sums over a row's states take two shuffles; the sums of
+// dB and dC over channels are reduced across the warp's rows (reduce-scatter by
+// shuffles), across the CTA's warps in shared memory, and added to global memory
+// once per CTA; dA, dD and dbias are accumulated in registers over the chunk and
+// added once per row and chunk.
 #include <cstdint>
 
 #include "ssm_device.cuh"
@@ -38,6 +49,28 @@ constexpr int kBwdThreads = kBwdRows * kBwdTpr; // 256
 constexpr int kBwdTok = 8;                      // tokens per block = checkpoint interval
 constexpr int kBwdN = kBwdTpr * kBwdG;          // 16 states per row
 constexpr int kWarps = kBwdThreads / 32;
+constexpr int kBwdMaxChunks = 32;               // chunk summaries kept per row tile
+constexpr int64_t kBwdMinChunkBlocks = 2;       // a chunk spans at least 16 tokens
+
+// chunks the workspace provides for nblk blocks of kBwdTok tokens
+__host__ __device__ constexpr int64_t bwd_max_chunks(int64_t nblk) {
+  return nblk / kBwdMinChunkBlocks < 1 ? 1 : (nblk / kBwdMinChunkBlocks > kBwdMaxChunks ? kBwdMaxChunks
+                                                                                           : nblk / kBwdMinChunkBlocks);
+}
+
+// The workspace, per row tile rt (batch-major, then channel tile):
+//   ck   [rt][nblk][kBwdThreads] float4  chunk-local state at each block's start
+//   scum [rt][nblk][kBwdRows]    float   ΣΔ from the chunk's start to the block's
+//   hend [rt][kmax][kBwdThreads] float4  chunk-local state after the chunk
+//   gcar [rt][kmax][kBwdThreads] float4  adjoint sent left with none coming in
+//   stot [rt][kmax][kBwdRows]    float   the chunk's ΣΔ
+struct BwdWs {
+  float4* ck;
+  float* scum;
+  float4* hend;
+  float4* gcar;
+  float* stot;
+};
 
 // per (row, token) scalars of a block
 struct TokScalars {
@@ -48,10 +81,15 @@ struct TokScalars {
   float dzf;    // dout·silu'(z): dz = dzf·y
 };
 
-struct BwdSmem {
-  float4 hs[kBwdTok + 1][kBwdRows][kBwdTpr];  // h_{t0-1} .. h_{t0+7}, [step][row][quad]
+// The per-block staging both kernels share, followed (second kernel) by the
+// recomputed states and the partial sums of dB and dC.
+struct StageSmem {
   TokScalars ts[kBwdTok][kBwdRows];
   float bc[kBwdTok][2][kBwdN];                // B | C of the block's tokens, fp32
+};
+struct BwdSmem {
+  StageSmem st;
+  float4 hs[kBwdTok + 1][kBwdRows][kBwdTpr];  // h_{t0-1} .. h_{t0+7}, [step][row][quad]
   float red[kWarps][kBwdTok][32];             // per-warp sums of the 32 (B|C, n) slots
 };
 
@@ -66,7 +104,7 @@ __device__ __forceinline__ void stf(void* base, int64_t i, float v) {
 
 // Stage B and C of tokens [t0, t0 + nv) of batch b into shared memory as fp32.
 template <typename T>
-__device__ __forceinline__ void stage_bc(BwdSmem& sm, const BwdArgs& p, int64_t b, int64_t t0, int nv) {
+__device__ __forceinline__ void stage_bc(StageSmem& sm, const BwdArgs& p, int64_t b, int64_t t0, int nv) {
   const int N = (int)p.N;
   for (int i = threadIdx.x; i < kBwdTok * 2 * kBwdN; i += kBwdThreads) {
     const int v = i / (2 * kBwdN), w = (i / kBwdN) & 1, n = i % kBwdN;
@@ -79,7 +117,7 @@ __device__ __forceinline__ void stage_bc(BwdSmem& sm, const BwdArgs& p, int64_t 
 // The per-token scalars of the block's tokens for this thread's row: thread g of
 // the row takes tokens g and g + 4.  Visible to the row's four threads after __syncwarp.
 template <typename T>
-__device__ __forceinline__ void row_scalars(BwdSmem& sm, const BwdArgs& p, int r, int g, bool row_ok, int64_t row,
+__device__ __forceinline__ void row_scalars(StageSmem& sm, const BwdArgs& p, int r, int g, bool row_ok, int64_t row,
                                             int64_t t0, int nv, float biasc, bool with_grad) {
   constexpr bool FAST = Act<T>::kFast;
 #pragma unroll
@@ -130,168 +168,278 @@ __device__ __forceinline__ float rows_reduce_scatter8(float (&v)[8]) {
   return v[0];
 }
 
+// A thread's four states n = 4g + k of its row: A and 1/A (both 0 for |A| < 2^-60
+// and for padded states), their pairs for packed f32x2 arithmetic, and whether
+// the packed path applies (bf16 arithmetic and no A = 0 state among the four).
+struct Quad {
+  float a[kBwdG], ia[kBwdG];
+  float2 aP[2], iaP[2];
+  bool packed;
+};
+
+template <bool FAST>
+__device__ __forceinline__ Quad load_quad(const float* A, int64_t c, int g, int N, bool row_ok) {
+  Quad q;
+#pragma unroll
+  for (int k = 0; k < kBwdG; ++k) {
+    const int n = kBwdG * g + k;
+    const float av = (row_ok && n < N) ? A[c * N + n] : 0.f;
+    const bool zero = fabsf(av) < 8.673617e-19f;
+    q.a[k] = zero ? 0.f : av;
+    q.ia[k] = zero ? 0.f : 1.f / av;
+  }
+  q.packed = FAST && q.a[0] != 0.f && q.a[1] != 0.f && q.a[2] != 0.f && q.a[3] != 0.f;
+  q.aP[0] = make_float2(q.a[0], q.a[1]);
+  q.aP[1] = make_float2(q.a[2], q.a[3]);
+  q.iaP[0] = make_float2(q.ia[0], q.ia[1]);
+  q.iaP[1] = make_float2(q.ia[2], q.ia[3]);
+  return q;
+}
+
+// Ā = e^{Δa} and φ = (Ā − 1)/a (Δ for a = 0) of state k
+template <bool FAST>
+__device__ __forceinline__ void discretise(const Quad& q, float dt, int k, float& abar, float& phi) {
+  if (q.a[k] != 0.f) {
+    abar = FAST ? ex2_approx(dt * q.a[k] * kLog2e) : expf(dt * q.a[k]);
+    phi = (FAST ? abar - 1.f : expm1f(dt * q.a[k])) * q.ia[k];
+  } else {
+    abar = 1.f;
+    phi = dt;
+  }
+}
+// the same for states (2j, 2j+1) on the packed path
+__device__ __forceinline__ void disc2(const Quad& q, float dt, int j, float2& abar, float2& phi) {
+  const float dl = dt * kLog2e;
+  const float2 e = __fmul2_rn(make_float2(dl, dl), q.aP[j]);
+  abar = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+  phi = __fmul2_rn(__fadd2_rn(abar, make_float2(-1.f, -1.f)), q.iaP[j]);
+}
+
+// e^{a S} for the four states (the decay over a stretch whose Δ sum to S)
+template <bool FAST>
+__device__ __forceinline__ void decay4(const Quad& q, float S, float (&e)[kBwdG]) {
+#pragma unroll
+  for (int k = 0; k < kBwdG; ++k) e[k] = FAST ? ex2_approx(q.a[k] * S * kLog2e) : expf(q.a[k] * S);
+}
+
+// One token of the recurrence h ← Ā h + φ B x for the thread's four states
+// (bq: their four B values); abar receives Ā.
+template <bool FAST>
+__device__ __forceinline__ void fwd_token(const Quad& q, float (&h)[kBwdG], float (&abar)[kBwdG], float dt, float x,
+                                          const float* bq) {
+  if (q.packed) {
+    const float2 xx = make_float2(x, x);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float2 ab, phi;
+      disc2(q, dt, j, ab, phi);
+      const float2 bb = *reinterpret_cast<const float2*>(bq + 2 * j);
+      const float2 hh = __ffma2_rn(ab, make_float2(h[2 * j], h[2 * j + 1]), __fmul2_rn(__fmul2_rn(phi, bb), xx));
+      h[2 * j] = hh.x;
+      h[2 * j + 1] = hh.y;
+      abar[2 * j] = ab.x;
+      abar[2 * j + 1] = ab.y;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kBwdG; ++k) {
+      float phi;
+      discretise<FAST>(q, dt, k, abar[k], phi);
+      h[k] = fmaf(abar[k], h[k], phi * bq[k] * x);
+    }
+  }
+}
+
+// Where this CTA sits: row tile blockIdx.x (batch-major), chunk blockIdx.y.
+struct CtaPos {
+  int64_t rt, b, c, row, blk0, blk1;
+  int chunk, r, g;
+  bool row_ok;
+};
+__device__ __forceinline__ CtaPos cta_pos(const BwdArgs& p) {
+  CtaPos o;
+  o.rt = blockIdx.x;
+  o.chunk = (int)blockIdx.y;
+  o.b = o.rt / p.ctiles;
+  const int64_t c0 = (o.rt % p.ctiles) * kBwdRows;
+  const int nrows = (int)((p.d_inner - c0) < kBwdRows ? (p.d_inner - c0) : kBwdRows);
+  o.r = threadIdx.x / kBwdTpr;
+  o.g = threadIdx.x % kBwdTpr;
+  o.row_ok = o.r < nrows;
+  o.c = c0 + (o.row_ok ? o.r : 0);
+  o.row = o.b * p.d_inner + o.c;
+  o.blk0 = o.chunk * p.cblk;
+  o.blk1 = o.blk0 + p.cblk < p.nblk ? o.blk0 + p.cblk : p.nblk;
+  return o;
+}
+
+// Launch 1: each chunk forward from h = 0, saving the local states, the prefix
+// sums of Δ and the chunk's summary (end state, ΣΔ, adjoint sent left).
 template <typename T>
-__global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs p) {
-  using AT = Act<T>;
-  constexpr bool FAST = AT::kFast;
+__global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_chunk_kernel(const BwdArgs p, const BwdWs w) {
+  constexpr bool FAST = Act<T>::kFast;
+  __shared__ StageSmem sm;
+  const CtaPos o = cta_pos(p);
+  const int r = o.r, g = o.g;
+  const Quad q = load_quad<FAST>(p.A, o.c, g, (int)p.N, o.row_ok);
+  const float biasc = (o.row_ok && p.bias) ? p.bias[o.c] : 0.f;
+  const bool want_g = o.chunk > 0;  // chunk 0 sends no adjoint further left
+  float h[kBwdG] = {0.f, 0.f, 0.f, 0.f}, P[kBwdG] = {1.f, 1.f, 1.f, 1.f}, G[kBwdG] = {0.f, 0.f, 0.f, 0.f};
+  float S = 0.f;
+  for (int64_t blk = o.blk0; blk < o.blk1; ++blk) {
+    const int64_t t0 = blk * kBwdTok;
+    const int nv = (int)(p.L - t0 < kBwdTok ? p.L - t0 : kBwdTok);
+    const int64_t slot = o.rt * p.nblk + blk;
+    w.ck[slot * kBwdThreads + threadIdx.x] = make_float4(h[0], h[1], h[2], h[3]);
+    if (g == 0) w.scum[slot * kBwdRows + r] = S;
+    __syncthreads();  // the previous block's staging is no longer read
+    stage_bc<T>(sm, p, o.b, t0, nv);
+    row_scalars<T>(sm, p, r, g, o.row_ok, o.row, t0, nv, biasc, want_g);
+    __syncthreads();
+    for (int v = 0; v < nv; ++v) {
+      const TokScalars s = sm.ts[v][r];
+      float ab[kBwdG];
+      fwd_token<FAST>(q, h, ab, s.dt, s.x, &sm.bc[v][0][kBwdG * g]);
+      if (want_g) {
+        // P = Π Ā over the chunk so far; G += P dy C
+        const float* cq = &sm.bc[v][1][kBwdG * g];
+        if (q.packed) {
+          const float2 dy2 = make_float2(s.dy, s.dy);
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float2 pp = __fmul2_rn(make_float2(P[2 * j], P[2 * j + 1]), make_float2(ab[2 * j], ab[2 * j + 1]));
+            const float2 cc = *reinterpret_cast<const float2*>(cq + 2 * j);
+            const float2 gg = __ffma2_rn(pp, __fmul2_rn(dy2, cc), make_float2(G[2 * j], G[2 * j + 1]));
+            P[2 * j] = pp.x;
+            P[2 * j + 1] = pp.y;
+            G[2 * j] = gg.x;
+            G[2 * j + 1] = gg.y;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < kBwdG; ++k) {
+            P[k] *= ab[k];
+            G[k] = fmaf(P[k], s.dy * cq[k], G[k]);
+          }
+        }
+      }
+      S += s.dt;
+    }
+  }
+  const int64_t cs = o.rt * p.kmax + o.chunk;
+  w.hend[cs * kBwdThreads + threadIdx.x] = make_float4(h[0], h[1], h[2], h[3]);
+  w.gcar[cs * kBwdThreads + threadIdx.x] = make_float4(G[0], G[1], G[2], G[3]);
+  if (g == 0) w.stot[cs * kBwdRows + r] = S;
+}
+
+// Launch 2: the gradients over one chunk, from the combined chunk summaries.
+template <typename T>
+__global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs p, const BwdWs w) {
+  constexpr bool FAST = Act<T>::kFast;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw);
   const int N = (int)p.N;
   const int64_t L = p.L;
-  const int64_t b = blockIdx.x / p.ctiles;
-  const int64_t c0 = (int64_t)(blockIdx.x % p.ctiles) * kBwdRows;
-  const int nrows = (int)((p.d_inner - c0) < kBwdRows ? (p.d_inner - c0) : kBwdRows);
-  const int r = threadIdx.x / kBwdTpr, g = threadIdx.x % kBwdTpr;
-  const bool row_ok = r < nrows;
-  const int64_t c = c0 + (row_ok ? r : 0);
-  const int64_t row = b * p.d_inner + c;
+  const CtaPos o = cta_pos(p);
+  const int r = o.r, g = o.g;
+  const bool row_ok = o.row_ok;
+  const int64_t b = o.b, c = o.c, row = o.row;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // this thread's states n = 4g + k: A and 1/A (0 for |A| < 2^-60 and padded states)
-  float a[kBwdG], ia[kBwdG];
-#pragma unroll
-  for (int k = 0; k < kBwdG; ++k) {
-    const int n = kBwdG * g + k;
-    const float av = (row_ok && n < N) ? p.A[c * N + n] : 0.f;
-    const bool zero = fabsf(av) < 8.673617e-19f;
-    a[k] = zero ? 0.f : av;
-    ia[k] = zero ? 0.f : 1.f / av;
-  }
+  const Quad q = load_quad<FAST>(p.A, c, g, N, row_ok);
   const float Dc = (row_ok && p.D) ? p.D[c] : 0.f;
   const float biasc = (row_ok && p.bias) ? p.bias[c] : 0.f;
-  const int64_t nblk = p.nblk;
-  // this thread's checkpoints: [nblk] float4 (its quad of the row's state)
-  float4* ck = reinterpret_cast<float4*>(p.ckpt) + ((int64_t)blockIdx.x * kBwdThreads + threadIdx.x) * nblk;
 
-  // packed path: bf16 arithmetic and no A = 0 state among this thread's four
-  const bool packed = FAST && a[0] != 0.f && a[1] != 0.f && a[2] != 0.f && a[3] != 0.f;
-  const float2 aP[2] = {make_float2(a[0], a[1]), make_float2(a[2], a[3])};
-  const float2 iaP[2] = {make_float2(ia[0], ia[1]), make_float2(ia[2], ia[3])};
-  // Ā - 1 and Ā of states (2j, 2j+1) at step size dt (packed path)
-  auto disc2 = [&](float dt, int j, float2& abar, float2& phi) {
-    const float dl = dt * kLog2e;
-    const float2 e = __fmul2_rn(make_float2(dl, dl), aP[j]);
-    abar = make_float2(ex2_approx(e.x), ex2_approx(e.y));
-    phi = __fmul2_rn(__fadd2_rn(abar, make_float2(-1.f, -1.f)), iaP[j]);
-  };
-  auto discretise = [&](float dt, int k, float& abar, float& phi) {
-    if (a[k] != 0.f) {
-      abar = FAST ? ex2_approx(dt * a[k] * kLog2e) : expf(dt * a[k]);
-      phi = (FAST ? abar - 1.f : expm1f(dt * a[k])) * ia[k];
-    } else {
-      abar = 1.f;
-      phi = dt;
-    }
-  };
-
-  // ---------------- pass one: forward, checkpoint every kBwdTok tokens ----------------
-  float h[kBwdG] = {0.f, 0.f, 0.f, 0.f};
-  for (int64_t blk = 0; blk < nblk; ++blk) {
-    const int64_t t0 = blk * kBwdTok;
-    const int nv = (int)(L - t0 < kBwdTok ? L - t0 : kBwdTok);
-    ck[blk] = make_float4(h[0], h[1], h[2], h[3]);
-    __syncthreads();  // the previous block's bc and ts are no longer read
-    stage_bc<T>(sm, p, b, t0, nv);
-    row_scalars<T>(sm, p, r, g, row_ok, row, t0, nv, biasc, false);
-    __syncthreads();
-    for (int v = 0; v < nv; ++v) {
-      const TokScalars s = sm.ts[v][r];
-      if (packed) {
-        const float2 xx = make_float2(s.x, s.x);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float2 abar, phi;
-          disc2(s.dt, j, abar, phi);
-          const float2 bb = *reinterpret_cast<const float2*>(&sm.bc[v][0][kBwdG * g + 2 * j]);
-          const float2 hh = __ffma2_rn(abar, make_float2(h[2 * j], h[2 * j + 1]), __fmul2_rn(__fmul2_rn(phi, bb), xx));
-          h[2 * j] = hh.x;
-          h[2 * j + 1] = hh.y;
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < kBwdG; ++k) {
-          float abar, phi;
-          discretise(s.dt, k, abar, phi);
-          h[k] = fmaf(abar, h[k], phi * sm.bc[v][0][kBwdG * g + k] * s.x);
-        }
-      }
-    }
+  // the state entering the chunk and the adjoint entering it from the right
+  float hin[kBwdG] = {0.f, 0.f, 0.f, 0.f}, dh[kBwdG] = {0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < o.chunk; ++j) {
+    const int64_t cs = o.rt * p.kmax + j;
+    const float4 H = w.hend[cs * kBwdThreads + threadIdx.x];
+    float e[kBwdG];
+    decay4<FAST>(q, w.stot[cs * kBwdRows + r], e);
+    hin[0] = fmaf(e[0], hin[0], H.x);
+    hin[1] = fmaf(e[1], hin[1], H.y);
+    hin[2] = fmaf(e[2], hin[2], H.z);
+    hin[3] = fmaf(e[3], hin[3], H.w);
+  }
+  for (int j = p.nchunks - 1; j > o.chunk; --j) {
+    const int64_t cs = o.rt * p.kmax + j;
+    const float4 Gj = w.gcar[cs * kBwdThreads + threadIdx.x];
+    float e[kBwdG];
+    decay4<FAST>(q, w.stot[cs * kBwdRows + r], e);
+    dh[0] = fmaf(e[0], dh[0], Gj.x);
+    dh[1] = fmaf(e[1], dh[1], Gj.y);
+    dh[2] = fmaf(e[2], dh[2], Gj.z);
+    dh[3] = fmaf(e[3], dh[3], Gj.w);
   }
 
-  // ---------------- pass two: blocks in reverse, adjoint recurrence ----------------
-  float dh[kBwdG] = {0.f, 0.f, 0.f, 0.f}, dA_acc[kBwdG] = {0.f, 0.f, 0.f, 0.f};
+  // blocks in reverse, adjoint recurrence
+  float h[kBwdG], dA_acc[kBwdG] = {0.f, 0.f, 0.f, 0.f};
   float dD_acc = 0.f, db_acc = 0.f;
-  for (int64_t blk = nblk - 1; blk >= 0; --blk) {
+  for (int64_t blk = o.blk1 - 1; blk >= o.blk0; --blk) {
     const int64_t t0 = blk * kBwdTok;
     const int nv = (int)(L - t0 < kBwdTok ? L - t0 : kBwdTok);
+    const int64_t slot = o.rt * p.nblk + blk;
     __syncthreads();  // bc, ts, hs and red of the previous block are no longer read
-    stage_bc<T>(sm, p, b, t0, nv);
-    row_scalars<T>(sm, p, r, g, row_ok, row, t0, nv, biasc, true);
-    const float4 h0v = ck[blk];
+    stage_bc<T>(sm.st, p, b, t0, nv);
+    row_scalars<T>(sm.st, p, r, g, row_ok, row, t0, nv, biasc, true);
+    // the block's starting state: chunk-local + decay since the chunk's start × h_in
+    float4 h0v = w.ck[slot * kBwdThreads + threadIdx.x];
+    if (o.chunk > 0) {
+      float e[kBwdG];
+      decay4<FAST>(q, w.scum[slot * kBwdRows + r], e);
+      h0v.x = fmaf(e[0], hin[0], h0v.x);
+      h0v.y = fmaf(e[1], hin[1], h0v.y);
+      h0v.z = fmaf(e[2], hin[2], h0v.z);
+      h0v.w = fmaf(e[3], hin[3], h0v.w);
+    }
     h[0] = h0v.x; h[1] = h0v.y; h[2] = h0v.z; h[3] = h0v.w;
     sm.hs[0][r][g] = h0v;
     __syncthreads();  // bc and ts staged
     // recompute the block's states
     for (int v = 0; v < nv; ++v) {
-      const TokScalars s = sm.ts[v][r];
-      if (packed) {
-        const float2 xx = make_float2(s.x, s.x);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float2 abar, phi;
-          disc2(s.dt, j, abar, phi);
-          const float2 bb = *reinterpret_cast<const float2*>(&sm.bc[v][0][kBwdG * g + 2 * j]);
-          const float2 hh = __ffma2_rn(abar, make_float2(h[2 * j], h[2 * j + 1]), __fmul2_rn(__fmul2_rn(phi, bb), xx));
-          h[2 * j] = hh.x;
-          h[2 * j + 1] = hh.y;
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < kBwdG; ++k) {
-          float abar, phi;
-          discretise(s.dt, k, abar, phi);
-          h[k] = fmaf(abar, h[k], phi * sm.bc[v][0][kBwdG * g + k] * s.x);
-        }
-      }
+      const TokScalars s = sm.st.ts[v][r];
+      float ab[kBwdG];
+      fwd_token<FAST>(q, h, ab, s.dt, s.x, &sm.st.bc[v][0][kBwdG * g]);
       sm.hs[v + 1][r][g] = make_float4(h[0], h[1], h[2], h[3]);
     }
     // adjoint over the block, last token first
     for (int v = nv - 1; v >= 0; --v) {
       const int64_t i = row * L + t0 + v;
-      const TokScalars s = sm.ts[v][r];
+      const TokScalars s = sm.st.ts[v][r];
       const float4 hv4 = sm.hs[v + 1][r][g], hp4 = sm.hs[v][r][g];
       const float hv[kBwdG] = {hv4.x, hv4.y, hv4.z, hv4.w};
       const float hp[kBwdG] = {hp4.x, hp4.y, hp4.z, hp4.w};
+      const float(&bcv)[2][kBwdN] = sm.st.bc[v];
       // y = Σ_n C h + D x over the row's four threads
       float y = 0.f;
 #pragma unroll
-      for (int k = 0; k < kBwdG; ++k) y = fmaf(sm.bc[v][1][kBwdG * g + k], hv[k], y);
+      for (int k = 0; k < kBwdG; ++k) y = fmaf(bcv[1][kBwdG * g + k], hv[k], y);
       y += __shfl_xor_sync(0xffffffffu, y, 1);
       y += __shfl_xor_sync(0xffffffffu, y, 2);
       y = fmaf(Dc, s.x, y);
       const float dy = s.dy;
       float dx = 0.f, ddt = 0.f;
       float slots[8];  // [0..3] dB, [4..7] dC of this thread's states
-      if (packed) {
+      if (q.packed) {
         const float2 dy2 = make_float2(dy, dy), xx = make_float2(s.x, s.x), dt2 = make_float2(s.dt, s.dt);
         float2 dx2 = make_float2(0.f, 0.f), ddt2 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const int n = kBwdG * g + 2 * j;
-          const float2 Bn = *reinterpret_cast<const float2*>(&sm.bc[v][0][n]);
-          const float2 Cn = *reinterpret_cast<const float2*>(&sm.bc[v][1][n]);
+          const float2 Bn = *reinterpret_cast<const float2*>(&bcv[0][n]);
+          const float2 Cn = *reinterpret_cast<const float2*>(&bcv[1][n]);
           const float2 hv2 = make_float2(hv[2 * j], hv[2 * j + 1]), hp2 = make_float2(hp[2 * j], hp[2 * j + 1]);
           const float2 gk = __ffma2_rn(dy2, Cn, make_float2(dh[2 * j], dh[2 * j + 1]));
           const float2 sc = __fmul2_rn(dy2, hv2);
           float2 abar, phi;
-          disc2(s.dt, j, abar, phi);
+          disc2(q, s.dt, j, abar, phi);
           const float2 bx = __fmul2_rn(Bn, xx);
           const float2 gphi = __fmul2_rn(gk, phi);
           const float2 sb = __fmul2_rn(gphi, xx);
           dx2 = __ffma2_rn(gphi, Bn, dx2);
-          ddt2 = __ffma2_rn(__fmul2_rn(gk, abar), __ffma2_rn(aP[j], hp2, bx), ddt2);
+          ddt2 = __ffma2_rn(__fmul2_rn(gk, abar), __ffma2_rn(q.aP[j], hp2, bx), ddt2);
           const float2 dta = __fmul2_rn(dt2, abar);
-          const float2 tb = __fmul2_rn(__fmul2_rn(bx, __fadd2_rn(dta, make_float2(-phi.x, -phi.y))), iaP[j]);
+          const float2 tb = __fmul2_rn(__fmul2_rn(bx, __fadd2_rn(dta, make_float2(-phi.x, -phi.y))), q.iaP[j]);
           const float2 da = __fmul2_rn(gk, __ffma2_rn(dta, hp2, tb));
           dA_acc[2 * j] += da.x;
           dA_acc[2 * j + 1] += da.y;
@@ -309,17 +457,17 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
 #pragma unroll
       for (int k = 0; k < kBwdG; ++k) {
         const int n = kBwdG * g + k;
-        const float Bn = sm.bc[v][0][n], Cn = sm.bc[v][1][n];
+        const float Bn = bcv[0][n], Cn = bcv[1][n];
         const float gk = fmaf(dy, Cn, dh[k]);  // dℓ/dh_t
         slots[4 + k] = dy * hv[k];
         float abar, phi;
-        discretise(s.dt, k, abar, phi);
+        discretise<FAST>(q, s.dt, k, abar, phi);
         const float bx = Bn * s.x;
         slots[k] = gk * phi * s.x;
         dx = fmaf(gk * phi, Bn, dx);
-        if (a[k] != 0.f) {
-          ddt = fmaf(gk * abar, fmaf(a[k], hp[k], bx), ddt);
-          dA_acc[k] = fmaf(gk, fmaf(s.dt * abar, hp[k], bx * (s.dt * abar - phi) * ia[k]), dA_acc[k]);
+        if (q.a[k] != 0.f) {
+          ddt = fmaf(gk * abar, fmaf(q.a[k], hp[k], bx), ddt);
+          dA_acc[k] = fmaf(gk, fmaf(s.dt * abar, hp[k], bx * (s.dt * abar - phi) * q.ia[k]), dA_acc[k]);
         } else {
           ddt = fmaf(gk, bx, ddt);
           dA_acc[k] = fmaf(gk, fmaf(s.dt, hp[k], 0.5f * bx * s.dt * s.dt), dA_acc[k]);
@@ -347,13 +495,13 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     __syncthreads();  // red complete
     for (int sidx = threadIdx.x; sidx < nv * 32; sidx += kBwdThreads) {
       const int v = sidx >> 5, l = sidx & 31;
-      const int qg = l & 3, slot = l >> 2;               // lane l held quad qg, value slot
-      const int n = kBwdG * qg + (slot & 3);
+      const int qg = l & 3, slot_id = l >> 2;            // lane l held quad qg, value slot_id
+      const int n = kBwdG * qg + (slot_id & 3);
       if (n >= N) continue;
       float sum = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) sum += sm.red[w][v][l];
-      atomicAdd((slot < 4 ? p.dB : p.dC) + (b * L + t0 + v) * N + n, sum);
+      for (int wi = 0; wi < kWarps; ++wi) sum += sm.red[wi][v][l];
+      atomicAdd((slot_id < 4 ? p.dB : p.dC) + (b * L + t0 + v) * N + n, sum);
     }
   }
   if (row_ok) {
@@ -369,12 +517,67 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
   }
 }
 
+BwdWs ws_layout(float* base, int64_t R, int64_t nblk, int64_t kmax) {
+  unsigned char* p = reinterpret_cast<unsigned char*>(base);
+  BwdWs w;
+  w.ck = reinterpret_cast<float4*>(p);
+  p += (size_t)(R * nblk * kBwdThreads) * sizeof(float4);
+  w.scum = reinterpret_cast<float*>(p);
+  p += (size_t)(R * nblk * kBwdRows) * sizeof(float);
+  w.hend = reinterpret_cast<float4*>(p);
+  p += (size_t)(R * kmax * kBwdThreads) * sizeof(float4);
+  w.gcar = reinterpret_cast<float4*>(p);
+  p += (size_t)(R * kmax * kBwdThreads) * sizeof(float4);
+  w.stot = reinterpret_cast<float*>(p);
+  return w;
+}
+
+// Chunks for R row tiles of nblk blocks on `slots` resident CTAs: fewest
+// block-steps per slot, counting whole waves and about two blocks' worth of
+// fixed cost per CTA (the summaries, the atomics at the end).
+int pick_bwd_chunks(int64_t R, int64_t nblk, int64_t slots, int64_t kmax) {
+  int best = 1;
+  int64_t best_cost = INT64_MAX;
+  for (int64_t k = 1; k <= kmax; ++k) {
+    const int64_t cb = (nblk + k - 1) / k;
+    const int64_t ke = (nblk + cb - 1) / cb;
+    const int64_t waves = (R * ke + slots - 1) / slots;
+    const int64_t cost = waves * (cb + 2);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = (int)ke;
+    }
+  }
+  return best;
+}
+
 template <typename T>
-cudaError_t bwd_launch_t(const BwdArgs& p, cudaStream_t s) {
-  const cudaError_t e =
+cudaError_t bwd_launch_t(BwdArgs p, cudaStream_t s) {
+  cudaError_t e =
       cudaFuncSetAttribute(scan_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(BwdSmem));
   if (e != cudaSuccess) return e;
-  scan_bwd_kernel<T><<<(unsigned)(p.batch * p.ctiles), kBwdThreads, sizeof(BwdSmem), s>>>(p);
+  const int64_t R = p.batch * p.ctiles;
+  if (R == 0) return cudaSuccess;
+  int64_t k = p.force_chunks;
+  if (k <= 0) {
+    int dev = 0, sms = 0, occ = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, scan_bwd_kernel<T>, kBwdThreads,
+                                                           sizeof(BwdSmem))) != cudaSuccess)
+      return e;
+    k = pick_bwd_chunks(R, p.nblk, (int64_t)(sms > 0 ? sms : 1) * (occ > 0 ? occ : 1), p.kmax);
+  }
+  if (k > p.kmax) k = p.kmax;
+  if (k > p.nblk) k = p.nblk;
+  if (k < 1) k = 1;
+  p.cblk = (p.nblk + k - 1) / k;
+  p.nchunks = p.cblk > 0 ? (int)((p.nblk + p.cblk - 1) / p.cblk) : 1;
+  const BwdWs w = ws_layout(p.ckpt, R, p.nblk, p.kmax);
+  const dim3 grid((unsigned)R, (unsigned)p.nchunks);
+  scan_bwd_chunk_kernel<T><<<grid, kBwdThreads, 0, s>>>(p, w);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  scan_bwd_kernel<T><<<grid, kBwdThreads, sizeof(BwdSmem), s>>>(p, w);
   return cudaGetLastError();
 }
 
@@ -383,14 +586,17 @@ cudaError_t bwd_launch_t(const BwdArgs& p, cudaStream_t s) {
 int scan_bwd_rows_per_cta() { return kBwdRows; }
 
 size_t scan_bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L) {
-  const int64_t ctiles = (d_inner + kBwdRows - 1) / kBwdRows;
+  const int64_t R = batch * ((d_inner + kBwdRows - 1) / kBwdRows);
   const int64_t nblk = (L + kBwdTok - 1) / kBwdTok;
-  return (size_t)(batch * ctiles * kBwdThreads) * (size_t)nblk * sizeof(float4);
+  const int64_t kmax = bwd_max_chunks(nblk);
+  return (size_t)(R * nblk) * (kBwdThreads * sizeof(float4) + kBwdRows * sizeof(float)) +
+         (size_t)(R * kmax) * (2 * kBwdThreads * sizeof(float4) + kBwdRows * sizeof(float));
 }
 
 cudaError_t scan_bwd_launch(BwdArgs p, cudaStream_t stream) {
   p.ctiles = (int)((p.d_inner + kBwdRows - 1) / kBwdRows);
   p.nblk = (p.L + kBwdTok - 1) / kBwdTok;
+  p.kmax = (int)bwd_max_chunks(p.nblk);
   return p.act == 1 ? bwd_launch_t<__nv_bfloat16>(p, stream) : bwd_launch_t<float>(p, stream);
 }
 

@@ -33,6 +33,7 @@ RuntimeKnobs runtime_knobs() {
     }
     if (const char* c = std::getenv("SSM_CTAS_PER_SM")) r.ctas_per_sm = std::atoi(c);
     if (const char* c = std::getenv("SSM_FORCE_TPR")) r.force_tpr = std::atoi(c);
+    if (const char* c = std::getenv("SSM_BWD_CHUNKS")) r.bwd_chunks = std::atoi(c);
     return r;
   }();
 }
@@ -269,6 +270,7 @@ ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const 
   a.du = du; a.ddelta = ddelta; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dz = dz; a.dbias = ddelta_bias;
   a.ckpt = static_cast<float*>(workspace);
   a.batch = b; a.d_inner = d; a.N = N; a.L = L; a.act = dims->act;
+  a.force_chunks = ssm::runtime_knobs().bwd_chunks;
   return ssm::scan_bwd_launch(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

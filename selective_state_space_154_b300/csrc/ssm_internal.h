@@ -69,6 +69,7 @@ struct RuntimeKnobs {
   int force_tpr;                  // >0: threads per row of the row kernel (1 or 2)
   bool fault_step;                // test hook: the pipelined step's first wait never completes
   bool force_step_plain;          // SSM_FORCE_STEP=plain: the generic step kernel only
+  int bwd_chunks;                 // >0: sequence chunks of the backward (tests)
 };
 RuntimeKnobs runtime_knobs();
 
@@ -117,6 +118,8 @@ cudaError_t conv1d_step_launch(const ConvCall& k, cudaStream_t stream);
 
 // Backward of the scan (scan_bwd.cu).  dA, dB, dC, dD, dbias are accumulated
 // (zeroed by the caller); ckpt is the workspace of scan_bwd_workspace_bytes().
+// force_chunks > 0 fixes the number of sequence chunks (tests); the launcher
+// fills nblk, ctiles, nchunks, cblk and kmax.
 struct BwdArgs {
   const void* u;
   const void* delta;
@@ -136,8 +139,8 @@ struct BwdArgs {
   void* dz;
   float* dbias;
   float* ckpt;
-  int64_t batch, d_inner, N, L, nblk;
-  int ctiles, act;
+  int64_t batch, d_inner, N, L, nblk, cblk;
+  int ctiles, act, nchunks, kmax, force_chunks;
 };
 size_t scan_bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L);
 int scan_bwd_rows_per_cta();

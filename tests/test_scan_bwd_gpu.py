@@ -78,3 +78,44 @@ def test_bwd_rejects_large_d_state():
     inp = W.random_scan_inputs(1, 8, 32, 16, dtype=torch.bfloat16, device=DEV, seed=1)
     with pytest.raises(ssm.SsmError):
         _run(inp, _dout(inp, 1))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("chunks", [1, 2, 5, 19])
+def test_bwd_sequence_chunks(monkeypatch, dtype, chunks):
+    """The sequence split into chunks (38 blocks of 8 tokens, the last ragged, over
+    1, 2, 5 or 19 chunks) gives the oracle's gradients."""
+    monkeypatch.setenv("SSM_BWD_CHUNKS", str(chunks))
+    inp = W.random_scan_inputs(2, 70, 16, 300, dtype=dtype, device=DEV, seed=chunks, a_kind="random")
+    _compare(inp, _dout(inp, chunks + 1), TOL[dtype])
+
+
+def test_bwd_sequence_chunks_zero_A(monkeypatch):
+    """Chunk summaries with A = 0 states (no decay across chunks) on the scalar path."""
+    monkeypatch.setenv("SSM_BWD_CHUNKS", "4")
+    inp = W.random_scan_inputs(1, 40, 16, 200, dtype=torch.float32, device=DEV, seed=9, a_kind="random")
+    inp["A"][::2, 5] = 0.0
+    _compare(inp, _dout(inp, 10), TOL[torch.float32])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+def test_bwd_few_rows_long_sequence(dtype):
+    """One row tile over 6000 tokens: the planner splits the sequence into many chunks."""
+    inp = W.random_scan_inputs(1, 64, 16, 6000, dtype=dtype, device=DEV, seed=21)
+    _compare(inp, _dout(inp, 22), TOL[dtype])
+
+
+def test_bwd_chunk_counts_agree(monkeypatch):
+    """fp32 gradients with 1 and 7 chunks agree to rounding (the chunk combine is exact
+    algebra; only the order of additions differs)."""
+    inp = W.random_scan_inputs(2, 50, 16, 500, dtype=torch.float32, device=DEV, seed=31, a_kind="random")
+    dout = _dout(inp, 32)
+    monkeypatch.setenv("SSM_BWD_CHUNKS", "1")
+    g1 = _run(inp, dout)
+    monkeypatch.setenv("SSM_BWD_CHUNKS", "7")
+    g7 = _run(inp, dout)
+    for k in GRADS:
+        if g1[k] is None:
+            continue
+        a, b = to_np(g1[k]), to_np(g7[k])
+        assert rel_err(b, a) <= 2e-5, k
