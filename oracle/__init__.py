@@ -220,3 +220,50 @@ def conv1d_step(state, x, w, bias=None):
     lib = _load()
     lib.oracle_conv1d_step(batch, d_inner, W, *(_ptr(v) for v in (st, x, w, bias, out)), 0, batch * d_inner)
     return out, st
+
+
+def ssd_scan(x, dt, A, B, C, D=None, z=None, dt_bias=None, h0=None, threads: int | None = None):
+    """The Mamba-2 layer scan (state space duality form of the selective SSM):
+    the state matrix of each head is a scalar times the identity, so each head's
+    headdim channels share their step size, their A and the B, C of their group.
+
+    x, z: [batch, L, H, P]; dt (Δraw): [batch, L, H]; A, D, dt_bias: [H];
+    B, C: [batch, L, G, N], head h reading group h // (H // G);
+    h0: [batch, H, P, N] or None.  Returns (out [batch, L, H, P], hT [batch, H, P, N]).
+
+    Channel (h, p) is the selective scan above on one row with A[c, n] = A[h] for
+    every n and Δraw = dt[..., h], so the result is ``scan`` applied group by group
+    ("Mambaとは？Transformer以外の系列モデル", section Mamba-2とTransformerとの関係性;
+    "State Space Models（SSM）とMamba" §4.6 Mamba-2: the SSM with this structure is
+    the one that coincides with masked linear attention).  Discretisation is the
+    zero-order hold of the scan, as the pages define no other.
+    """
+    x, dt, A, B, C = (_f64(v) for v in (x, dt, A, B, C))
+    D, z, dt_bias, h0 = (_f64(v) for v in (D, z, dt_bias, h0))
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    assert H % G == 0 and dt.shape == (batch, L, H) and A.shape == (H,)
+    assert B.shape == (batch, L, G, N) and C.shape == (batch, L, G, N)
+    assert z is None or z.shape == x.shape
+    assert h0 is None or h0.shape == (batch, H, P, N)
+    hpg = H // G
+
+    def rows(t):  # [batch, L, hpg, P] -> [batch, hpg * P, L]
+        return np.ascontiguousarray(t.transpose(0, 2, 3, 1).reshape(batch, hpg * P, L))
+
+    out = np.empty((batch, L, H, P))
+    hT = np.empty((batch, H, P, N))
+    for g in range(G):
+        hs = slice(g * hpg, (g + 1) * hpg)
+        u = rows(x[:, :, hs, :])
+        delta = rows(np.broadcast_to(dt[:, :, hs, None], (batch, L, hpg, P)))
+        Af = np.repeat(np.repeat(A[hs], P)[:, None], N, axis=1)
+        o, hg = scan(u, delta, Af, B[:, :, g, :], C[:, :, g, :],
+                     D=None if D is None else np.repeat(D[hs], P),
+                     z=None if z is None else rows(z[:, :, hs, :]),
+                     bias=None if dt_bias is None else np.repeat(dt_bias[hs], P),
+                     h0=None if h0 is None else np.ascontiguousarray(h0[:, hs].reshape(batch, hpg * P, N)),
+                     threads=threads)
+        out[:, :, hs, :] = o.reshape(batch, hpg, P, L).transpose(0, 3, 1, 2)
+        hT[:, hs] = hg.reshape(batch, hpg, P, N)
+    return out, hT

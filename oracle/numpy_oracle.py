@@ -151,3 +151,70 @@ def scan_bwd(u, delta, A, B, C, dout, D=None, z=None, bias=None, h0=None, dhT=No
     g["dbias"] = dbias
     g["dh0"] = dh
     return g
+
+
+def _ssd_prep(x, dt, A, B, C, D, z, dt_bias):
+    x, dt, A, B, C = (_arr(v) for v in (x, dt, A, B, C))
+    D, z, dt_bias = (_arr(v) for v in (D, z, dt_bias))
+    H, G = x.shape[2], B.shape[2]
+    r = dt + (dt_bias[None, None, :] if dt_bias is not None else 0.0)
+    delta = np.logaddexp(0.0, r)                           # [batch, L, H]
+    la = delta * A[None, None, :]                          # log Ā_t
+    safe = np.where(A == 0.0, 1.0, A)[None, None, :]
+    phi = np.where(A[None, None, :] == 0.0, delta, np.expm1(la) / safe)
+    head_group = np.arange(H) // (H // G)
+    Bh, Ch = B[:, :, head_group, :], C[:, :, head_group, :]   # [batch, L, H, N]
+    return x, D, z, la, phi, Bh, Ch
+
+
+def _gate(y, x, D, z):
+    if D is not None:
+        y = y + D[None, None, :, None] * x
+    if z is not None:
+        y = y * (z * expit(z))
+    return y
+
+
+def ssd_dual(x, dt, A, B, C, D=None, z=None, dt_bias=None):
+    """The quadratic ("attention") form of the Mamba-2 layer scan, with no
+    recurrence: y_t = Σ_{s≤t} (Π_{s<k≤t} Ā_k) φ_s (C_t·B_s) x_s + D x_t, i.e. causal
+    linear attention with queries C, keys B, values φ x and a decay mask
+    ("Mambaとは？Transformer以外の系列モデル", section Mamba-2とTransformerとの関係性).
+    Returns (out [batch, L, H, P], hT [batch, H, P, N])."""
+    x, D, z, la, phi, Bh, Ch = _ssd_prep(x, dt, A, B, C, D, z, dt_bias)
+    L = x.shape[1]
+    cum = np.cumsum(la, axis=1)                            # Σ_{k≤t} log Ā_k
+    diff = cum[:, :, None, :] - cum[:, None, :, :]         # [batch, t, s, H]
+    causal = np.tril(np.ones((L, L), bool))[None, :, :, None]
+    decay = np.where(causal, np.exp(np.where(causal, diff, 0.0)), 0.0)
+    cb = np.einsum("bthn,bshn->btsh", Ch, Bh)
+    M = decay * cb * phi[:, None, :, :]
+    y = np.einsum("btsh,bshp->bthp", M, x)
+    w = np.exp(cum[:, -1:, :] - cum) * phi                 # weight of token s in the final state
+    hT = np.einsum("bsh,bshp,bshn->bhpn", w, x, Bh)
+    return _gate(y, x, D, z), hT
+
+
+def ssd_chunked(x, dt, A, B, C, D=None, z=None, dt_bias=None, chunk=64):
+    """The chunked evaluation of the same map: inside each chunk the quadratic form,
+    between chunks the state, carried as h ← e^{Σ log Ā over the chunk} h + (the
+    chunk's own contribution), and read by every token as C_t e^{Σ log Ā since the
+    chunk's start} h.  Returns (out, hT) as ``ssd_dual``."""
+    x, D, z, la, phi, Bh, Ch = _ssd_prep(x, dt, A, B, C, D, z, dt_bias)
+    batch, L, H, P = x.shape
+    N = Bh.shape[-1]
+    y = np.zeros((batch, L, H, P))
+    h = np.zeros((batch, H, P, N))
+    for c0 in range(0, L, chunk):
+        sl = slice(c0, min(L, c0 + chunk))
+        q = sl.stop - sl.start
+        cum = np.cumsum(la[:, sl], axis=1)                 # since the chunk's start, inclusive
+        diff = cum[:, :, None, :] - cum[:, None, :, :]
+        causal = np.tril(np.ones((q, q), bool))[None, :, :, None]
+        decay = np.where(causal, np.exp(np.where(causal, diff, 0.0)), 0.0)
+        cb = np.einsum("bthn,bshn->btsh", Ch[:, sl], Bh[:, sl])
+        y[:, sl] = np.einsum("btsh,bshp->bthp", decay * cb * phi[:, None, sl, :], x[:, sl])
+        y[:, sl] += np.einsum("bth,bthn,bhpn->bthp", np.exp(cum), Ch[:, sl], h)
+        w = np.exp(cum[:, -1:, :] - cum) * phi[:, sl]
+        h = np.exp(cum[:, -1, :])[:, :, None, None] * h + np.einsum("bsh,bshp,bshn->bhpn", w, x[:, sl], Bh[:, sl])
+    return _gate(y, x, D, z), h

@@ -21,6 +21,16 @@ Distributions: A[c, n] = -(n + 1); u, z, B, C, D ~ N(0, 1); for the scans the
 step dt ~ log-uniform[1e-3, 0.1] per element, passed as Δraw = log(expm1(dt))
 with bias = 0; for decode Δraw ~ N(0, 1) and bias[c] = log(expm1(dt_c)) with
 dt_c ~ log-uniform[1e-3, 0.1] per channel.
+
+Mamba-2 (SSD) layer workloads (batch, L, heads × headdim, groups, d_state N):
+
+    mamba2_130m_layer  8 × 2048, 24 × 64, 1 group, N 128   bf16
+    mamba2_2p7b_layer  4 × 4096, 80 × 64, 1 group, N 128   bf16
+
+with x, z, B, C ~ N(0, 1) (layout [batch][L][heads][headdim] and
+[batch][L][groups][N]), A[h] ~ -U(1, 16) per head, D ~ N(0, 1) per head and the
+step dt ~ log-uniform[1e-3, 0.1] per (batch, token, head), passed as
+Δraw = log(expm1(dt)) with dt_bias = 0.
 """
 from __future__ import annotations
 
@@ -65,6 +75,28 @@ SCAN_SHAPES = {
     "long_1m": ScanShape("long_1m", 1, 2048, 16, 1 << 20, torch.bfloat16),
 }
 DECODE_SHAPE = DecodeShape("decode", 256, 5120, 16, 1000, torch.bfloat16)
+
+
+@dataclass(frozen=True)
+class SsdShape:
+    name: str
+    batch: int
+    seqlen: int
+    nheads: int
+    headdim: int
+    ngroups: int
+    d_state: int
+    dtype: torch.dtype
+
+    @property
+    def channel_tokens(self) -> int:
+        return self.batch * self.seqlen * self.nheads * self.headdim
+
+
+SSD_SHAPES = {
+    "mamba2_130m_layer": SsdShape("mamba2_130m_layer", 8, 2048, 24, 64, 1, 128, torch.bfloat16),
+    "mamba2_2p7b_layer": SsdShape("mamba2_2p7b_layer", 4, 4096, 80, 64, 1, 128, torch.bfloat16),
+}
 
 # tensor ids: each tensor is drawn from its own stream
 _IDS = dict(u=1, delta=2, z=3, B=4, C=5, D=6, A=7, bias=8, x=9, dt=10)
@@ -175,3 +207,38 @@ def conv_inputs(batch, d_inner, seqlen, width=CONV_WIDTH, dtype=torch.bfloat16, 
         g = _gen(device, seed, 204)
         state = torch.randn((batch, d_inner, width - 1), generator=g, device=device).to(dtype)
     return dict(x=x, w=w, bias=bias, state=state)
+
+
+def ssd_inputs(shape: SsdShape, device="cpu", seed: int = 0, gate: bool = True, skip: bool = True,
+               with_bias: bool = True, bias_scale: float = 0.0):
+    """Inputs of one Mamba-2 layer scan: x, z [batch, L, H, P] and B, C [batch, L, G, N]
+    (act dtype); dt (Δraw) [batch, L, H] (act dtype); A, D, dt_bias [H] (fp32).
+    bias_scale > 0 draws dt_bias ~ bias_scale·N(0, 1) instead of zeros."""
+    b, L, H, P, G, N, dt_ = (shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.ngroups,
+                             shape.d_state, shape.dtype)
+    step = _log_uniform((b, L, H), device, seed, "dt")
+    dt = torch.log(torch.expm1(step)).to(dt_)
+    del step
+    ga = _gen(device, seed, _IDS["A"])
+    A = -(1.0 + 15.0 * torch.rand((H,), generator=ga, device=device, dtype=torch.float32))
+    bias = None
+    if with_bias:
+        bias = (bias_scale * _normal((H,), device, seed, "bias", torch.float32) if bias_scale > 0
+                else torch.zeros(H, device=device, dtype=torch.float32))
+    return dict(
+        x=_normal((b, L, H, P), device, seed, "x", dt_),
+        dt=dt,
+        A=A,
+        B=_normal((b, L, G, N), device, seed, "B", dt_),
+        C=_normal((b, L, G, N), device, seed, "C", dt_),
+        D=_normal((H,), device, seed, "D", torch.float32) if skip else None,
+        z=_normal((b, L, H, P), device, seed, "z", dt_) if gate else None,
+        dt_bias=bias,
+    )
+
+
+def random_ssd_inputs(batch, seqlen, nheads, headdim, ngroups, d_state, dtype=torch.bfloat16, device="cpu",
+                      seed: int = 0, gate=True, skip=True, with_bias=True):
+    """ssd_inputs for an arbitrary shape, with dt_bias ~ 0.5·N(0, 1) when present."""
+    shape = SsdShape("custom", batch, seqlen, nheads, headdim, ngroups, d_state, dtype)
+    return ssd_inputs(shape, device, seed, gate, skip, with_bias, bias_scale=0.5 if with_bias else 0.0)
