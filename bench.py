@@ -356,6 +356,62 @@ def conv_alg_bytes(rows, L, width, esz):
     return rows * L * 2 * esz + 2 * rows * (width - 1) * esz
 
 
+
+def ssd_alg(shape):
+    """Algorithmic bytes and tensor FLOPs of one Mamba-2 layer scan: x and z read and
+    out written once per (batch, token, head, p), dt once per (batch, token, head), B
+    and C once per (batch, token, group, n) (bf16); FLOPs of the chunked evaluation
+    per (batch, head, 128-token chunk): S = C Bᵀ (2·Q·Q·N), Y = G X and Y_in = C h_inᵀ
+    (2·Q·P·Q + 2·Q·P·N) and the chunk state Bᵀ diag(w) X (2·N·P·Q), counting each
+    operand once (the second bf16 term of G and of w·x is precision, not work)."""
+    b, L, H, P, G, N = shape.batch, shape.seqlen, shape.nheads, shape.headdim, shape.ngroups, shape.d_state
+    q = 128
+    nch = (L + q - 1) // q
+    alg = 3 * 2 * b * L * H * P + 2 * b * L * H + 2 * 2 * b * L * G * N
+    flops = b * H * nch * (2 * q * q * N + 2 * q * P * q + 2 * q * P * N + 2 * N * P * q)
+    return alg, flops
+
+
+def bench_ssd(dev, hbm_peak, tc_peak, runs=20):
+    """The Mamba-2 (SSD) layer scan on the two Mamba-2-shaped layers, each call
+    timed alone after an L2 flush (median)."""
+    import selective_state_space_154_b300 as ssm
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {"note": "chunks of 128 tokens on the tensor cores (tcgen05, bf16 operands, fp32 accumulators in "
+                   "tensor memory); three launches; median of 20, L2 flushed before each; hbm_frac of the "
+                   "measured copy bandwidth, tensor_frac of the measured cuBLAS bf16 burst"}
+    for name in ("mamba2_130m_layer", "mamba2_2p7b_layer"):
+        shape = W.SSD_SHAPES[name]
+        inp = W.ssd_inputs(shape, device=dev, seed=0)
+        out = torch.empty_like(inp["x"])
+        fs = torch.empty((shape.batch, shape.nheads, shape.headdim, shape.d_state), device=dev)
+        ws = torch.empty(ssm.ssd_scan_workspace_bytes(shape.batch, shape.seqlen, shape.nheads, shape.headdim,
+                                                      shape.ngroups, shape.d_state), dtype=torch.uint8, device=dev)
+        call = lambda: ssm.ssd_scan_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                        inp["dt_bias"], None, out, fs, workspace=ws, stream=stream)
+        for _ in range(3):
+            call()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
+        for a, b in evs:
+            flush()
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize()
+        secs = statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+        if ssm.ssm_scan_check(ws) != 0:
+            raise RuntimeError("ssd_scan_fwd reported a device-side timeout")
+        alg, flops = ssd_alg(shape)
+        res[name] = {"batch": shape.batch, "seq_len": shape.seqlen, "nheads": shape.nheads,
+                     "headdim": shape.headdim, "ngroups": shape.ngroups, "d_state": shape.d_state,
+                     "us": secs * 1e6, "channel_tokens_per_s": shape.channel_tokens / secs,
+                     "gbs": alg / secs / 1e9, "hbm_frac": alg / secs / 1e9 / hbm_peak, "alg_bytes": alg,
+                     "tflops": flops / secs / 1e12, "tensor_frac": flops / secs / 1e12 / tc_peak,
+                     "workspace_bytes": ws.numel()}
+        del inp, out, fs, ws
+    return res
+
 def bench_conv(dev, hbm_peak, runs=20):
     """Causal Conv1D + SiLU: the sequence form on the 2.8B-shaped layer's x (L2
     flushed before each call) and on the 1M-token rows (larger than L2), and the
@@ -541,6 +597,7 @@ def run_ours(args):
     others = bench_workloads(dev) if rank == 0 else None
     conv = bench_conv(dev, hbm_peak) if rank == 0 else None
     bwd = bench_scan_bwd(dev, hbm_peak) if rank == 0 else None
+    ssd = bench_ssd(dev, hbm_peak, peaks.get("bf16_tflops")) if rank == 0 else None
     cpu = cpu_baseline() if (rank == 0 and world == 1) else None
 
     if rank == 0:
@@ -574,6 +631,7 @@ def run_ours(args):
                              if others else {})},
             "conv1d": conv,
             "scan_bwd": bwd,
+            "ssd": ssd,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -614,6 +672,18 @@ def run_profile_case(args):
         fn = lambda: ssm.ssm_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
                                       inp["bias"], dout, gr["du"], gr["ddelta"], gr["dA"], gr["dB"], gr["dC"],
                                       gr["dD"], gr["dz"], gr["dbias"], workspace=ws)
+        units = shape.channel_tokens
+    elif args.only == "ssd":
+        shape = W.SSD_SHAPES[args.workload if args.workload in W.SSD_SHAPES else "mamba2_2p7b_layer"]
+        if args.seqlen:
+            shape = W.SsdShape(shape.name, shape.batch, args.seqlen, shape.nheads, shape.headdim, shape.ngroups,
+                               shape.d_state, shape.dtype)
+        inp = W.ssd_inputs(shape, device=dev, seed=0)
+        out = torch.empty_like(inp["x"])
+        ws = torch.empty(ssm.ssd_scan_workspace_bytes(shape.batch, shape.seqlen, shape.nheads, shape.headdim,
+                                                      shape.ngroups, shape.d_state), dtype=torch.uint8, device=dev)
+        fn = lambda: ssm.ssd_scan_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                      inp["dt_bias"], None, out, None, workspace=ws)
         units = shape.channel_tokens
     elif args.only == "conv":
         base = W.SCAN_SHAPES[args.workload]
@@ -673,14 +743,14 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "scan", "decode", "conv", "bwd"], default="all",
+    ap.add_argument("--only", choices=["all", "scan", "decode", "conv", "bwd", "ssd"], default="all",
                     help="profiling aid: run only the scan, the decode step, the Conv1D or the backward (no JSON line)")
     ap.add_argument("--seqlen", type=int, default=None,
                     help="profiling aid: scan another sequence length of the same workload")
     ap.add_argument("--dinner", type=int, default=None,
                     help="profiling aid: scan another number of channels of the same workload")
-    ap.add_argument("--workload", choices=sorted(W.SCAN_SHAPES), default=WORKLOAD,
-                    help="profiling aid: the workload --only scan / conv / bwd runs")
+    ap.add_argument("--workload", choices=sorted(W.SCAN_SHAPES) + sorted(W.SSD_SHAPES), default=WORKLOAD,
+                    help="profiling aid: the workload --only scan / conv / bwd / ssd runs")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":

@@ -252,6 +252,51 @@ SSM_API ssm_status ssm_scan_fwd_noalloc(const void* u, const void* delta, const 
                                 const void* C, const float* D, const void* z, const float* delta_bias,
                                 void* out, float* final_state, const ssm_dims* dims, ssm_stream_t stream);
 
+/*
+ * Mamba-2 layer scan (state space duality, SSD): each head's state matrix is a
+ * scalar a_h times the identity, so the layer equals causal linear attention
+ * with queries C, keys B, values φ·x and the decay mask e^{Σ Δa}
+ * ("Mambaとは？Transformer以外の系列モデル", section Mamba-2とTransformerとの関係性;
+ * "State Space Models（SSM）とMamba" §4.6 Mamba-2).  Per head h, with
+ * Δ_t = softplus(dt[t,h] + dt_bias[h]), Ā_t = e^{Δ_t a_h}, φ_t = (Ā_t − 1)/a_h
+ * (Δ_t when a_h = 0), the state (headdim × d_state) follows
+ *   H_t = Ā_t H_{t-1} + φ_t x_t B_tᵀ,   out_t = (H_t C_t + D_h x_t) · silu(z_t)
+ * from H_0 = initial_state (zero when NULL).  Evaluated in chunks of 128
+ * tokens on the tensor cores (bf16 operands, fp32 accumulation; the state
+ * handed from one chunk to the next's tensor cores is rounded to bf16, and is
+ * carried between chunks in fp32).
+ *   x, z, out: [batch][seqlen][nheads][headdim] bf16, 16-byte aligned (z may be NULL).
+ *   dt: [batch][seqlen][nheads] bf16 (Δraw).
+ *   B, C: [batch][seqlen][ngroups][d_state] bf16, 16-byte aligned; head h
+ *     reads group h / (nheads / ngroups).
+ *   A, D, dt_bias: [nheads] float32 (D, dt_bias may be NULL).
+ *   initial_state, final_state: [batch][nheads][headdim][d_state] float32, or NULL.
+ *   workspace: at least ssd_scan_workspace_bytes(dims) bytes, 16-byte aligned,
+ *     caller-owned; its error word is read by ssm_scan_check (a tensor-core
+ *     wait that ran out of time).
+ * seqlen may be 0: x, dt, B, C, z and out may then be NULL and final_state
+ * receives the initial state.
+ * Supported: act = SSM_DTYPE_BF16, headdim = 64, d_state = 128, nheads and batch
+ * ≤ 65535 (else SSM_ERR_UNSUPPORTED); nheads a multiple of ngroups (else
+ * SSM_ERR_INVALID_ARG).  Three kernel launches on `stream`; no host sync.
+ */
+typedef struct {
+  int64_t batch;
+  int64_t seqlen;
+  int64_t nheads;
+  int64_t headdim;  /* P */
+  int64_t ngroups;  /* G: heads share B and C within a group */
+  int64_t d_state;  /* N */
+  int32_t act;      /* ssm_dtype of x, dt, z, B, C, out */
+  int32_t reserved;
+} ssd_dims;
+
+SSM_API size_t ssd_scan_workspace_bytes(const ssd_dims* dims);
+SSM_API ssm_status ssd_scan_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                                const float* D, const void* z, const float* dt_bias, const float* initial_state,
+                                void* out, float* final_state, const ssd_dims* dims, void* workspace,
+                                size_t workspace_bytes, ssm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

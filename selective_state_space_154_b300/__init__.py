@@ -22,6 +22,7 @@ __all__ = [
     "SSM_NOALLOC_SCRATCH_BYTES", "ssm_step_check", "ssm_scan_fwd_from_state",
     "ssm_conv1d_fwd", "ssm_conv1d_step", "conv1d", "conv1d_step",
     "ssm_scan_bwd_workspace_bytes", "ssm_scan_bwd", "scan_bwd",
+    "ssd_scan_workspace_bytes", "ssd_scan_fwd", "ssd_scan",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -43,6 +44,12 @@ class SsmError(RuntimeError):
 class ssm_dims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int64), ("d_inner", ctypes.c_int64), ("d_state", ctypes.c_int64),
                 ("seqlen", ctypes.c_int64), ("act", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class ssd_dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
+                ("headdim", ctypes.c_int64), ("ngroups", ctypes.c_int64), ("d_state", ctypes.c_int64),
+                ("act", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _lib = None
@@ -86,6 +93,11 @@ def load_library():
             lib.ssm_conv1d_fwd.restype = i32
             lib.ssm_conv1d_step.argtypes = [vp] * 5 + [dp, i32, vp]
             lib.ssm_conv1d_step.restype = i32
+            sdp = ctypes.POINTER(ssd_dims)
+            lib.ssd_scan_workspace_bytes.argtypes = [sdp]
+            lib.ssd_scan_workspace_bytes.restype = sz
+            lib.ssd_scan_fwd.argtypes = [vp] * 11 + [sdp, vp, sz, vp]
+            lib.ssd_scan_fwd.restype = i32
             lib.ssm_status_string.argtypes = [i32]
             lib.ssm_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -402,3 +414,63 @@ def step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, out=None, st
         out = torch.empty_like(x)
     ssm_step(state, x, delta, A, B, C, D, z, delta_bias, out, stream=stream)
     return out
+
+
+def _ssd_dims(batch, seqlen, nheads, headdim, ngroups, d_state, dtype):
+    if dtype not in _DTYPES:
+        raise TypeError(f"activation dtype must be float32 or bfloat16, got {dtype}")
+    return ssd_dims(int(batch), int(seqlen), int(nheads), int(headdim), int(ngroups), int(d_state), _DTYPES[dtype], 0)
+
+
+def ssd_scan_workspace_bytes(batch, seqlen, nheads, headdim, ngroups, d_state, dtype=torch.bfloat16) -> int:
+    d = _ssd_dims(batch, seqlen, nheads, headdim, ngroups, d_state, dtype)
+    return int(load_library().ssd_scan_workspace_bytes(ctypes.byref(d)))
+
+
+def ssd_scan_fwd(x, dt, A, B, C, D, z, dt_bias, initial_state, out, final_state, workspace=None, stream=None):
+    """Mamba-2 (SSD) layer scan into caller-provided ``out`` (and ``final_state``);
+    see include/ssm_scan.h.  x, z, out: [batch, L, H, P]; dt: [batch, L, H];
+    B, C: [batch, L, G, N]; A, D, dt_bias: [H]; states [batch, H, P, N] (fp32)."""
+    lib = load_library()
+    if not isinstance(x, torch.Tensor) or x.dim() != 4:
+        raise ValueError("x must be a [batch, seqlen, nheads, headdim] tensor")
+    if not isinstance(B, torch.Tensor) or B.dim() != 4:
+        raise ValueError("B must be a [batch, seqlen, ngroups, d_state] tensor")
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    act, dev = x.dtype, x.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    _check(x, "x", act, (batch, L, H, P), dev)
+    _check(dt, "dt", act, (batch, L, H), dev)
+    _check(A, "A", torch.float32, (H,), dev)
+    _check(B, "B", act, (batch, L, G, N), dev)
+    _check(C, "C", act, (batch, L, G, N), dev)
+    _check(D, "D", torch.float32, (H,), dev, required=False)
+    _check(z, "z", act, (batch, L, H, P), dev, required=False)
+    _check(dt_bias, "dt_bias", torch.float32, (H,), dev, required=False)
+    _check(initial_state, "initial_state", torch.float32, (batch, H, P, N), dev, required=False)
+    _check(out, "out", act, (batch, L, H, P), dev)
+    _check(final_state, "final_state", torch.float32, (batch, H, P, N), dev, required=False)
+    dims = _ssd_dims(batch, L, H, P, G, N, act)
+    with torch.cuda.device(dev):
+        need = int(lib.ssd_scan_workspace_bytes(ctypes.byref(dims)))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = lib.ssd_scan_fwd(*(_ptr(t) for t in (x, dt, A, B, C, D, z, dt_bias, initial_state, out, final_state)),
+                              ctypes.byref(dims), _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
+    if st != SSM_OK:
+        raise SsmError(st, "ssd_scan_fwd")
+    return workspace
+
+
+def ssd_scan(x, dt, A, B, C, D=None, z=None, dt_bias=None, initial_state=None, return_final_state=False,
+             workspace=None, stream=None):
+    """Allocate ``out`` (and the final state) and run ``ssd_scan_fwd``."""
+    out = torch.empty_like(x)
+    fs = None
+    if return_final_state:
+        fs = torch.empty((x.shape[0], x.shape[2], x.shape[3], B.shape[3]), dtype=torch.float32, device=x.device)
+    ssd_scan_fwd(x, dt, A, B, C, D, z, dt_bias, initial_state, out, fs, workspace=workspace, stream=stream)
+    return (out, fs) if return_final_state else out

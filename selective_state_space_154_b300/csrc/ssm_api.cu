@@ -98,6 +98,20 @@ ssm::ScanArgs scan_args(const void* u, const void* delta, const float* A, const 
 
 }  // namespace
 
+namespace {
+ssm_status check_ssd_dims(const ssd_dims* d) {
+  if (!d) return SSM_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->seqlen < 0 || d->nheads < 1 || d->headdim < 1 || d->ngroups < 1 || d->d_state < 1)
+    return SSM_ERR_INVALID_ARG;
+  if (d->act != SSM_DTYPE_BF16 && d->act != SSM_DTYPE_F32) return SSM_ERR_INVALID_ARG;
+  if (d->nheads % d->ngroups != 0) return SSM_ERR_INVALID_ARG;
+  if (d->act != SSM_DTYPE_BF16 || d->headdim != ssm::kSsdHeadDim || d->d_state != ssm::kSsdState)
+    return SSM_ERR_UNSUPPORTED;
+  if (d->nheads > 65535 || d->batch > 65535) return SSM_ERR_UNSUPPORTED;
+  return SSM_OK;
+}
+}  // namespace
+
 extern "C" {
 
 size_t ssm_scan_workspace_bytes(const ssm_dims* dims) {
@@ -279,6 +293,41 @@ ssm_status ssm_step_check(ssm_stream_t stream) {
   unsigned word = 0;
   if (ssm::step_error_fetch_clear(&word) != cudaSuccess) return SSM_ERR_CUDA;
   return word ? SSM_ERR_TIMEOUT : SSM_OK;
+}
+
+size_t ssd_scan_workspace_bytes(const ssd_dims* dims) {
+  if (check_ssd_dims(dims) != SSM_OK) return 0;
+  return ssm::ssd_workspace_bytes(dims->batch, dims->seqlen, dims->nheads);
+}
+
+ssm_status ssd_scan_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C, const float* D,
+                        const void* z, const float* dt_bias, const float* initial_state, void* out,
+                        float* final_state, const ssd_dims* dims, void* workspace, size_t workspace_bytes,
+                        ssm_stream_t stream) {
+  const ssm_status ds = check_ssd_dims(dims);
+  if (ds != SSM_OK) return ds;
+  // with seqlen = 0 there is nothing to read or write but the state
+  if (!A || (dims->seqlen > 0 && (!x || !dt || !B || !C || !out))) return SSM_ERR_INVALID_ARG;
+  const void* v16[] = {x, z, out, B, C};
+  for (const void* p : v16)
+    if (p && !aligned16(p)) return SSM_ERR_ALIGNMENT;
+  if (dt && !aligned(dt, 2)) return SSM_ERR_ALIGNMENT;
+  const void* f32_ptrs[] = {A, D, dt_bias, initial_state, final_state};
+  for (const void* p : f32_ptrs)
+    if (p && !aligned(p, 4)) return SSM_ERR_ALIGNMENT;
+  const size_t need = ssm::ssd_workspace_bytes(dims->batch, dims->seqlen, dims->nheads);
+  if (!workspace || workspace_bytes < need) return SSM_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return SSM_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // clear the error word so ssm_scan_check on this workspace reports this call
+  if (cudaMemsetAsync(workspace, 0, sizeof(unsigned) * 2, st) != cudaSuccess) return SSM_ERR_CUDA;
+  ssm::SsdArgs a{};
+  a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias;
+  a.h0 = initial_state; a.out = out; a.final_state = final_state; a.ws = workspace;
+  a.batch = dims->batch; a.L = dims->seqlen; a.H = dims->nheads; a.P = dims->headdim; a.G = dims->ngroups;
+  a.N = dims->d_state;
+  a.timeout_ns = ssm::runtime_knobs().lookback_timeout_ns;
+  return ssm::ssd_launch(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 ssm_status ssm_scan_check(const void* workspace, size_t workspace_bytes) {

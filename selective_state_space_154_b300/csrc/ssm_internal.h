@@ -146,6 +146,31 @@ size_t scan_bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L);
 int scan_bwd_rows_per_cta();
 cudaError_t scan_bwd_launch(BwdArgs p, cudaStream_t stream);
 
+// Mamba-2 (SSD) layer scan (ssd.cu): x, z, out [batch][L][H][P]; dt [batch][L][H];
+// B, C [batch][L][G][N] (bf16); A, D, dt_bias [H]; h0, final_state [batch][H][P][N]
+// (fp32).  ws: the workspace of ssd_workspace_bytes() (error word at byte 4).
+struct SsdArgs {
+  const void* x;
+  const void* dt;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* dt_bias;
+  const float* h0;
+  void* out;
+  float* final_state;
+  void* ws;
+  int64_t batch, L, H, P, G, N, nchunks;
+  long long timeout_ns;
+};
+constexpr int kSsdChunk = 128;    // tokens per chunk
+constexpr int kSsdHeadDim = 64;   // supported headdim
+constexpr int kSsdState = 128;    // supported d_state
+size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H);
+cudaError_t ssd_launch(SsdArgs p, cudaStream_t stream);
+
 // Reads and clears the sticky error word of the pipelined step kernel (current device).
 cudaError_t step_error_fetch_clear(unsigned* word);
 

@@ -202,3 +202,52 @@ def test_conv_rejects_misaligned_and_bad_dims(lib):
     d = _dims()
     d.act = 5
     assert _conv_step(lib, d) == ssm.SSM_ERR_INVALID_ARG
+
+
+def _ssd_dims(batch=2, seqlen=300, nheads=4, headdim=64, ngroups=2, d_state=128, act=ssm.SSM_DTYPE_BF16):
+    return ssm.ssd_dims(batch, seqlen, nheads, headdim, ngroups, d_state, act, 0)
+
+
+def _ssd(lib, dims, ptrs=None, ws=FAKE, ws_bytes=1 << 40):
+    p = dict(x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, bias=None, h0=None, out=FAKE, fs=None)
+    p.update(ptrs or {})
+    args = [ctypes.c_void_p(p[k]) if p[k] else None
+            for k in ("x", "dt", "A", "B", "C", "D", "z", "bias", "h0", "out", "fs")]
+    return lib.ssd_scan_fwd(*args, ctypes.byref(dims), ctypes.c_void_p(ws) if ws else None, ws_bytes, None)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("batch", 0, ssm.SSM_ERR_INVALID_ARG), ("nheads", 0, ssm.SSM_ERR_INVALID_ARG),
+    ("ngroups", 3, ssm.SSM_ERR_INVALID_ARG), ("seqlen", -1, ssm.SSM_ERR_INVALID_ARG),
+    ("act", 5, ssm.SSM_ERR_INVALID_ARG), ("act", ssm.SSM_DTYPE_F32, ssm.SSM_ERR_UNSUPPORTED),
+    ("headdim", 32, ssm.SSM_ERR_UNSUPPORTED), ("d_state", 64, ssm.SSM_ERR_UNSUPPORTED),
+    ("nheads", 1 << 17, ssm.SSM_ERR_UNSUPPORTED),
+])
+def test_ssd_rejects_bad_dims(lib, field, value, status):
+    d = _ssd_dims()
+    setattr(d, field, value)
+    assert _ssd(lib, d) == status
+    assert lib.ssd_scan_workspace_bytes(ctypes.byref(d)) == 0
+
+
+@pytest.mark.parametrize("missing", ["x", "dt", "A", "B", "C", "out"])
+def test_ssd_rejects_null_required_pointer(lib, missing):
+    assert _ssd(lib, _ssd_dims(), {missing: None}) == ssm.SSM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("which,offset", [("x", 2), ("z", 8), ("out", 2), ("B", 4), ("C", 2), ("dt", 1),
+                                          ("A", 2), ("D", 1), ("bias", 2), ("h0", 2), ("fs", 1)])
+def test_ssd_rejects_misaligned_pointer(lib, which, offset):
+    assert _ssd(lib, _ssd_dims(), {which: FAKE + offset}) == ssm.SSM_ERR_ALIGNMENT
+
+
+def test_ssd_workspace_size_and_check(lib):
+    d = _ssd_dims()
+    need = lib.ssd_scan_workspace_bytes(ctypes.byref(d))
+    # 3 chunks of 128 tokens per (batch, head): fp32 chunk states, the two bf16 terms of the
+    # incoming states and the chunk decays
+    cells = 2 * 4 * 3
+    assert need >= 256 + cells * 64 * 128 * (4 + 2 * 2) + cells * 4
+    assert _ssd(lib, d, ws_bytes=need - 1) == ssm.SSM_ERR_WORKSPACE
+    assert _ssd(lib, d, ws=None, ws_bytes=0) == ssm.SSM_ERR_WORKSPACE
+    assert _ssd(lib, d, ws=FAKE + 8, ws_bytes=need) == ssm.SSM_ERR_ALIGNMENT

@@ -1,0 +1,99 @@
+"""GPU parity of ssd_scan_fwd (the Mamba-2 layer scan on the tensor cores) with the
+float64 oracle on the same bf16-rounded inputs: whole outputs at small sizes that
+still span several 128-token chunks and a ragged tail, and sampled heads over the
+full Mamba-2-2.7B-shaped layer."""
+import pytest
+import torch
+
+import oracle
+import selective_state_space_154_b300 as ssm
+import workloads as W
+from parity import TOL, rel_err, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+BF16 = TOL[torch.bfloat16]
+
+
+def _oracle(inp, h0=None):
+    return oracle.ssd_scan(*(to_np(inp[k]) for k in ("x", "dt", "A", "B", "C")), D=to_np(inp["D"]),
+                           z=to_np(inp["z"]), dt_bias=to_np(inp["dt_bias"]), h0=to_np(h0))
+
+
+def _gpu(inp, h0=None):
+    out, fs = ssm.ssd_scan(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"], z=inp["z"],
+                           dt_bias=inp["dt_bias"], initial_state=h0, return_final_state=True)
+    torch.cuda.synchronize()
+    return out, fs
+
+
+def _compare(inp, h0=None):
+    out, fs = _gpu(inp, h0)
+    ref, href = _oracle(inp, h0)
+    assert rel_err(to_np(out), ref) <= BF16
+    assert rel_err(to_np(fs), href) <= BF16
+
+
+@pytest.mark.parametrize("shape", [(1, 128, 2, 64, 1, 128), (2, 300, 4, 64, 2, 128), (1, 1, 2, 64, 1, 128),
+                                   (1, 129, 3, 64, 3, 128), (2, 700, 2, 64, 1, 128), (1, 2048, 4, 64, 2, 128)],
+                         ids=["one_chunk", "ragged_groups", "one_token", "chunk_plus_one", "six_chunks",
+                              "sixteen_chunks"])
+def test_ssd_matches_oracle(shape):
+    _compare(W.random_ssd_inputs(*shape, device=DEV, seed=sum(shape)))
+
+
+@pytest.mark.parametrize("opts", [dict(gate=False), dict(skip=False), dict(with_bias=False),
+                                  dict(gate=False, skip=False, with_bias=False)],
+                         ids=["no_z", "no_D", "no_bias", "all_off"])
+def test_ssd_optional_inputs(opts):
+    _compare(W.random_ssd_inputs(1, 260, 2, 64, 1, 128, device=DEV, seed=5, **opts))
+
+
+def test_ssd_initial_state_continues_a_split_sequence():
+    inp = W.random_ssd_inputs(2, 400, 2, 64, 1, 128, device=DEV, seed=8)
+    g = torch.Generator(device=DEV).manual_seed(3)
+    h0 = torch.randn((2, 2, 64, 128), generator=g, device=DEV)
+    _compare(inp, h0)
+    ref, href = _oracle(inp, h0)
+    # the first 250 tokens, then the rest from the device's final state
+    first = {k: (v if k in ("A", "D", "dt_bias") or v is None else v[:, :250].contiguous()) for k, v in inp.items()}
+    rest = {k: (v if k in ("A", "D", "dt_bias") or v is None else v[:, 250:].contiguous()) for k, v in inp.items()}
+    o1, f1 = _gpu(first, h0)
+    o2, f2 = _gpu(rest, f1)
+    assert rel_err(to_np(torch.cat([o1, o2], dim=1)), ref) <= BF16
+    assert rel_err(to_np(f2), href) <= BF16
+
+
+def test_ssd_zero_A_is_linear_attention():
+    inp = W.random_ssd_inputs(1, 300, 2, 64, 1, 128, device=DEV, seed=12)
+    inp["A"].zero_()
+    _compare(inp)
+
+
+def test_ssd_empty_sequence_passes_the_state_through():
+    inp = W.random_ssd_inputs(1, 0, 2, 64, 1, 128, device=DEV, seed=2)
+    h0 = torch.randn((1, 2, 64, 128), device=DEV)
+    out, fs = _gpu(inp, h0)
+    assert out.numel() == 0
+    assert torch.equal(fs, h0)
+
+
+def test_ssd_mamba2_2p7b_layer_sampled_heads():
+    """The full 4 × 4096 × 80 × 64 (N = 128) layer on the device; the oracle recomputes
+    heads 0, 37 and 79 of every batch over the whole sequence."""
+    shape = W.SSD_SHAPES["mamba2_2p7b_layer"]
+    inp = W.ssd_inputs(shape, device=DEV, seed=0)
+    ws = torch.empty(ssm.ssd_scan_workspace_bytes(shape.batch, shape.seqlen, shape.nheads, shape.headdim,
+                                                  shape.ngroups, shape.d_state), dtype=torch.uint8, device=DEV)
+    out, fs = ssm.ssd_scan(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], D=inp["D"], z=inp["z"],
+                           dt_bias=inp["dt_bias"], return_final_state=True, workspace=ws)
+    torch.cuda.synchronize()
+    assert ssm.ssm_scan_check(ws) == ssm.SSM_OK
+    for h in (0, 37, 79):
+        sub = {k: (None if v is None else v[..., h:h + 1] if k in ("A", "D", "dt_bias", "dt") else v)
+               for k, v in inp.items()}
+        sub["x"] = inp["x"][:, :, h:h + 1]
+        sub["z"] = inp["z"][:, :, h:h + 1]
+        ref, href = _oracle(sub)
+        assert rel_err(to_np(out[:, :, h:h + 1]), ref) <= BF16, h
+        assert rel_err(to_np(fs[:, h:h + 1]), href) <= BF16, h
