@@ -43,10 +43,11 @@ namespace {
 constexpr int kQ = kSsdChunk;
 constexpr int kP = kSsdHeadDim;
 constexpr int kN = kSsdState;
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kDefaultTimeoutMs = 2000;
 
-static_assert(kQ == kThreads && kN == 128 && kP == 64, "tile shapes assume 128 tokens, 128 states, headdim 64");
+static_assert(kQ == 128 && kThreads == 2 * kQ && kN == 128 && kP == 64,
+              "tile shapes assume 128 tokens, 128 states, headdim 64, 256 threads");
 
 // Workspace: error words | H_c fp32 [b][H][nch][P][N] | Σ Δa [b][H][nch] |
 // h_in as bf16 hi and lo terms [b][H][nch][2][P][N]
@@ -81,37 +82,50 @@ SsdWs ws_layout(void* base, int64_t b, int64_t H, int64_t nch) {
 
 __device__ __forceinline__ const __nv_bfloat16* bf(const void* p) { return static_cast<const __nv_bfloat16*>(p); }
 
-// Per-token scalars of one chunk, thread i = token t0 + i.
+constexpr int kMaxHeadsPerCta = 8;
+
+// Per-token scalars of one chunk for the CTA's heads j < hb (head h0 + j).
 struct TokenSmem {
-  float cs2[kQ];   // inclusive prefix sums of Δa since the chunk's start, in log2 units
-  float phi[kQ];   // φ of the token (0 past the sequence's end)
-  float wsum[kThreads / 32];
-  float total;     // Σ Δa over the chunk (natural units)
+  float cs2[kMaxHeadsPerCta][kQ];   // inclusive prefix sums of Δa since the chunk's start, log2 units
+  float phi[kMaxHeadsPerCta][kQ];   // φ of the token (0 past the sequence's end)
+  float wsum[2][4];
+  float total[kMaxHeadsPerCta];     // Σ Δa over the chunk (natural units)
 };
 
-__device__ void chunk_tokens(const SsdArgs& p, int64_t b, int h, int64_t t0, int q, TokenSmem& ts) {
-  const int i = threadIdx.x, lane = i & 31, warp = i >> 5;
-  const float a = p.A[h];
-  float la = 0.f, ph = 0.f;
-  if (i < q) {
-    const float r = __bfloat162float(bf(p.dt)[(b * p.L + t0 + i) * p.H + h]) + (p.dt_bias ? p.dt_bias[h] : 0.f);
-    const float d = softplus_precise(r);
-    la = d * a;
-    ph = a != 0.f ? expm1f(la) / a : d;
-  }
-  float v = la;
+// Threads 0..127 take heads 0, 2, 4, ... and threads 128..255 heads 1, 3, 5, ...,
+// token i = thread % 128; a block scan over the 128 tokens per head.
+__device__ void chunk_tokens(const SsdArgs& p, int64_t b, int h0, int hb, int64_t t0, int q, TokenSmem& ts) {
+  const int i = threadIdx.x & (kQ - 1), half = threadIdx.x >> 7, lane = threadIdx.x & 31,
+            wq = (threadIdx.x >> 5) & 3;
+  for (int r = 0; r < (hb + 1) / 2; ++r) {
+    const int j = 2 * r + half;
+    const bool on = j < hb;
+    float la = 0.f, ph = 0.f;
+    if (on && i < q) {
+      const int h = h0 + j;
+      const float a = p.A[h];
+      const float rr =
+          __bfloat162float(bf(p.dt)[(b * p.L + t0 + i) * p.H + h]) + (p.dt_bias ? p.dt_bias[h] : 0.f);
+      const float d = softplus_precise(rr);
+      la = d * a;
+      ph = a != 0.f ? expm1f(la) / a : d;
+    }
+    float v = la;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float u = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += u;
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    if (lane == 31) ts.wsum[half][wq] = v;
+    __syncthreads();
+    for (int w = 0; w < wq; ++w) v += ts.wsum[half][w];
+    if (on) {
+      ts.cs2[j][i] = v * kLog2e;
+      ts.phi[j][i] = ph;
+      if (i == kQ - 1) ts.total[j] = v;
+    }
+    __syncthreads();
   }
-  if (lane == 31) ts.wsum[warp] = v;
-  __syncthreads();
-  for (int w = 0; w < warp; ++w) v += ts.wsum[w];
-  ts.cs2[i] = v * kLog2e;
-  ts.phi[i] = ph;
-  if (i == kThreads - 1) ts.total = v;
-  __syncthreads();
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
@@ -156,44 +170,62 @@ __device__ __forceinline__ void stage_rows_async(unsigned char* s, const __nv_bf
   }
 }
 
-// The transpose of a [128 tokens][R] block (token i at g + i·stride, R contiguous
-// values) as an R-row K-major operand over the tokens; tokens ≥ valid are zero.
-// With wt given, token i's row is scaled by wt[i] and written as the two terms
-// hi (to s) and lo (to s_lo).  Thread k builds core matrices k, k + 128, ...
-// (column group fastest, so a warp's loads of one token are contiguous).
-template <int R>
-__device__ __forceinline__ void stage_transposed(unsigned char* s, unsigned char* s_lo, const __nv_bfloat16* g,
-                                                 int64_t stride, int valid, const float* wt) {
-  constexpr int kCores = (R / 8) * (kQ / 8);
+// Bᵀ (N rows × 128 tokens, K-major over the tokens) from B [token][n]; one core
+// matrix (n group = thread % 16, token group = thread / 16) per thread.
+__device__ __forceinline__ void stage_bt(unsigned char* s, const __nv_bfloat16* g, int64_t stride, int valid) {
+  const int jg = threadIdx.x % (kN / 8), ig = threadIdx.x / (kN / 8);
+  uint4 in[8], out[8];
 #pragma unroll
-  for (int core = threadIdx.x; core < kCores; core += kThreads) {
-    const int jg = core % (R / 8), ig = core / (R / 8);
-    uint4 in[8], out[8];
-#pragma unroll
-    for (int ii = 0; ii < 8; ++ii) {
-      const int i = ig * 8 + ii;
-      in[ii] = i < valid ? *reinterpret_cast<const uint4*>(g + i * stride + jg * 8) : make_uint4(0, 0, 0, 0);
-    }
-    const size_t off = (size_t)((ig * (R / 8)) + jg) * 128;
-    if (wt) {
-      uint4 lo[8];
-#pragma unroll
-      for (int ii = 0; ii < 8; ++ii) {
-        const float w = wt[ig * 8 + ii];
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) scale_split_bf16x2(word_of(in[ii], m), w, h[m], l[m]);
-        in[ii] = make_uint4(h[0], h[1], h[2], h[3]);
-        lo[ii] = make_uint4(l[0], l[1], l[2], l[3]);
-      }
-      transpose8x8(lo, out);
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) *reinterpret_cast<uint4*>(s_lo + off + jj * 16) = out[jj];
-    }
-    transpose8x8(in, out);
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) *reinterpret_cast<uint4*>(s + off + jj * 16) = out[jj];
+  for (int ii = 0; ii < 8; ++ii) {
+    const int i = ig * 8 + ii;
+    in[ii] = i < valid ? *reinterpret_cast<const uint4*>(g + i * stride + jg * 8) : make_uint4(0, 0, 0, 0);
   }
+  transpose8x8(in, out);
+  unsigned char* dst = s + (size_t)((ig * (kN / 8)) + jg) * 128;
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj) *reinterpret_cast<uint4*>(dst + jj * 16) = out[jj];
+}
+
+// One head's X over the chunk, [token][p]: threads 0..127 each hold the 8 × 8 block
+// (p group = thread % 8, token group = thread / 8), read into registers ahead of use.
+__device__ __forceinline__ void load_x_block(const __nv_bfloat16* xg, int64_t stride, int valid, uint4 (&in)[8]) {
+  const int jg = threadIdx.x % (kP / 8), ig = threadIdx.x / (kP / 8);
+#pragma unroll
+  for (int ii = 0; ii < 8; ++ii) {
+    const int i = ig * 8 + ii;
+    in[ii] = i < valid ? *reinterpret_cast<const uint4*>(xg + i * stride + jg * 8) : make_uint4(0, 0, 0, 0);
+  }
+}
+// Xᵀ (P rows × 128 tokens, K-major over the tokens) from the block of load_x_block
+__device__ __forceinline__ void store_xt(unsigned char* s, const uint4 (&in)[8]) {
+  const int jg = threadIdx.x % (kP / 8), ig = threadIdx.x / (kP / 8);
+  uint4 out[8];
+  transpose8x8(in, out);
+  unsigned char* dst = s + (size_t)((ig * (kP / 8)) + jg) * 128;
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj) *reinterpret_cast<uint4*>(dst + jj * 16) = out[jj];
+}
+// (diag(w) X)ᵀ as hi and lo terms, w = token weights of the head
+__device__ __forceinline__ void store_xw(unsigned char* s_hi, unsigned char* s_lo, const uint4 (&in)[8],
+                                         const float* w) {
+  const int jg = threadIdx.x % (kP / 8), ig = threadIdx.x / (kP / 8);
+  uint4 hi[8], lo[8], out[8];
+#pragma unroll
+  for (int ii = 0; ii < 8; ++ii) {
+    const float wi = w[ig * 8 + ii];
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) scale_split_bf16x2(word_of(in[ii], m), wi, h[m], l[m]);
+    hi[ii] = make_uint4(h[0], h[1], h[2], h[3]);
+    lo[ii] = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+  const size_t off = (size_t)((ig * (kP / 8)) + jg) * 128;
+  transpose8x8(hi, out);
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj) *reinterpret_cast<uint4*>(s_hi + off + jj * 16) = out[jj];
+  transpose8x8(lo, out);
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj) *reinterpret_cast<uint4*>(s_lo + off + jj * 16) = out[jj];
 }
 
 // Bounded wait for an mbarrier phase; on timeout the error word is set.
@@ -206,69 +238,110 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
   atomicOr(err, kErrTimeout);
   return false;
 }
-
-// ---------------------------------------------------------------------------
-// Launch 1: the chunk's own end state H_c = Bᵀ diag(w) X and its Σ Δa.
-struct StateSmem {
-  unsigned char bt[kN * kQ * 2];     // Bᵀ: N rows × Q tokens, K-major
-  unsigned char xw[kP * kQ * 2];     // (diag(w) X)ᵀ, hi term: P rows × Q tokens, K-major
-  unsigned char xw_lo[kP * kQ * 2];  // its lo term
-  TokenSmem ts;
-  float w[kQ];
-  uint64_t bar;
-  uint32_t tslot;
-};
-
-__global__ void __launch_bounds__(kThreads) ssd_chunk_state_kernel(const SsdArgs p, const SsdWs ws) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  StateSmem& sm = *reinterpret_cast<StateSmem*>(smem_raw);
-  const int c = blockIdx.x, h = blockIdx.y;
-  const int64_t b = blockIdx.z;
-  const int g = (int)(h / (p.H / p.G));
-  const int64_t t0 = (int64_t)c * kQ;
-  const int q = (int)(p.L - t0 < kQ ? p.L - t0 : kQ);
-  const int warp = threadIdx.x >> 5;
-  const uint32_t bar = tc::smem_addr(&sm.bar);
-  if (threadIdx.x == 0) tc::mbar_init1(bar);
-  if (warp == 0) tc::tmem_alloc(tc::smem_addr(&sm.tslot), 64);
-  chunk_tokens(p, b, h, t0, q, sm.ts);  // (its barriers also publish the mbarrier's initialisation)
-  sm.w[threadIdx.x] = ex2_approx(sm.ts.cs2[kQ - 1] - sm.ts.cs2[threadIdx.x]) * sm.ts.phi[threadIdx.x];
-  __syncthreads();
-  stage_transposed<kN>(sm.bt, nullptr, bf(p.B) + ((b * p.L + t0) * p.G + g) * kN, p.G * kN, q, nullptr);
-  stage_transposed<kP>(sm.xw, sm.xw_lo, bf(p.x) + ((b * p.L + t0) * p.H + h) * kP, p.H * kP, q, sm.w);
+// every thread's tcgen05 work and shared-memory writes before, the elected
+// thread's tensor-core work after
+__device__ __forceinline__ void sync_for_mma() {
   tc::fence_smem_to_async();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+}
+
+// Where the CTA sits: chunk blockIdx.x, heads h0 .. h0 + hb − 1 (one group), batch blockIdx.z.
+struct CtaPos {
+  int64_t b, t0;
+  int c, h0, hb, g, q;
+};
+__device__ __forceinline__ CtaPos cta_pos(const SsdArgs& p) {
+  CtaPos o;
+  o.c = blockIdx.x;
+  o.hb = p.heads_per_cta;
+  o.h0 = blockIdx.y * o.hb;
+  o.b = blockIdx.z;
+  o.g = (int)(o.h0 / (p.H / p.G));
+  o.t0 = (int64_t)o.c * kQ;
+  o.q = (int)(p.L - o.t0 < kQ ? p.L - o.t0 : kQ);
+  return o;
+}
+
+// ---------------------------------------------------------------------------
+// Launch 1: each head's chunk end state H_c = Bᵀ diag(w) X and the chunk's Σ Δa.
+// Bᵀ is staged once for the CTA's heads; per head the (w X)ᵀ tile and the
+// tensor-memory accumulator are double-buffered, so a head's product runs while
+// the previous head's state is written out and the next head's X is read.
+struct StateSmem {
+  unsigned char bt[kN * kQ * 2];          // Bᵀ: N rows × Q tokens, K-major
+  unsigned char xw[2][2][kP * kQ * 2];    // [buffer][hi, lo] (diag(w) X)ᵀ: P rows × Q tokens
+  TokenSmem ts;
+  uint64_t bar;
+  uint32_t tslot;
+};
+constexpr int kStateCols = 128;  // two 64-column accumulators
+
+__global__ void __launch_bounds__(kThreads, 1) ssd_chunk_state_kernel(const SsdArgs p, const SsdWs ws) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  StateSmem& sm = *reinterpret_cast<StateSmem*>(smem_raw);
+  const CtaPos o = cta_pos(p);
+  const int warp = threadIdx.x >> 5, wq = warp & 3, hf = warp >> 2;
+  const uint32_t bar = tc::smem_addr(&sm.bar);
+  if (threadIdx.x == 0) tc::mbar_init1(bar);
+  if (warp == 0) tc::tmem_alloc(tc::smem_addr(&sm.tslot), kStateCols);
+  const __nv_bfloat16* xbase = bf(p.x) + (o.b * p.L + o.t0) * p.H * kP;
+  const int64_t xstride = p.H * kP;
+  uint4 xin[8];
+  if (threadIdx.x < kQ) load_x_block(xbase + (int64_t)o.h0 * kP, xstride, o.q, xin);
+  stage_bt(sm.bt, bf(p.B) + ((o.b * p.L + o.t0) * p.G + o.g) * kN, p.G * kN, o.q);
+  chunk_tokens(p, o.b, o.h0, o.hb, o.t0, o.q, sm.ts);  // (its barriers publish the mbarrier's initialisation)
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
   const uint32_t tmem = sm.tslot;
-  if (threadIdx.x == 0) {
-    const uint32_t idesc = tc::idesc_bf16_f32(kN, kP);
-    const uint32_t abase = tc::smem_addr(sm.bt), bhi = tc::smem_addr(sm.xw), blo = tc::smem_addr(sm.xw_lo);
+  const uint32_t idesc = tc::idesc_bf16_f32(kN, kP);
+  bool ok = true;
+  auto write_state = [&](int j) {  // accumulator of head j → H_c [p][n] (fp32)
+    const int n = wq * 32 + (threadIdx.x & 31);
+    float v[32];
+    tc::tmem_ld32(tc::tmem_lane_addr(tmem + (uint32_t)((j & 1) * 64), wq * 32, hf * 32), v);
+    float* dst = ws.hc + (((o.b * p.H + o.h0 + j) * p.nchunks + o.c) * kP + hf * 32) * kN + n;
 #pragma unroll
-    for (int kk = 0; kk < kQ / 16; ++kk)
-      tc::mma_bf16(tmem, tc::kslice_desc(abase, kN, kk), tc::kslice_desc(bhi, kP, kk), idesc, kk > 0);
-#pragma unroll
-    for (int kk = 0; kk < kQ / 16; ++kk)
-      tc::mma_bf16(tmem, tc::kslice_desc(abase, kN, kk), tc::kslice_desc(blo, kP, kk), idesc, true);
-    tc::mma_commit(bar);
-  }
-  if (wait_phase(bar, 0, p, ws.err)) {
-    tc::fence_after_sync();
-    // thread = state row n; columns = headdim p
-    const int n = threadIdx.x;
-    float* dst = ws.hc + (((b * p.H + h) * p.nchunks + c) * kP) * kN + n;
-#pragma unroll
-    for (int half = 0; half < kP / 32; ++half) {
-      float v[32];
-      tc::tmem_ld32(tc::tmem_lane_addr(tmem, warp * 32, half * 32), v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) dst[(half * 32 + j) * kN] = v[j];
+    for (int k = 0; k < 32; ++k) dst[k * kN] = v[k];
+    if (threadIdx.x == 0) ws.ctot[(o.b * p.H + o.h0 + j) * p.nchunks + o.c] = sm.ts.total[j];
+  };
+  for (int j = 0; j < o.hb; ++j) {
+    const int k = j & 1;
+    bool done = true;
+    if (j > 0) done = wait_phase(bar, (uint32_t)((j - 1) & 1), p, ws.err);  // head j−1's product
+    if (threadIdx.x < kQ) {
+      // token weights w_s = 2^(cs2_end − cs2_s) φ_s of head j, over φ (each thread its own token)
+      const int i = threadIdx.x;
+      sm.ts.phi[j][i] *= ex2_approx(sm.ts.cs2[j][kQ - 1] - sm.ts.cs2[j][i]);
     }
-    if (threadIdx.x == 0) ws.ctot[(b * p.H + h) * p.nchunks + c] = sm.ts.total;
+    ok = __syncthreads_and(ok && done) != 0;  // the same decision in every thread
+    if (!ok) break;
+    tc::fence_after_sync();
+    if (threadIdx.x < kQ) store_xw(sm.xw[k][0], sm.xw[k][1], xin, sm.ts.phi[j]);
+    sync_for_mma();
+    if (threadIdx.x == 0) {
+      const uint32_t abase = tc::smem_addr(sm.bt), bhi = tc::smem_addr(sm.xw[k][0]),
+                     blo = tc::smem_addr(sm.xw[k][1]), d = tmem + (uint32_t)(k * 64);
+#pragma unroll
+      for (int kk = 0; kk < kQ / 16; ++kk)
+        tc::mma_bf16(d, tc::kslice_desc(abase, kN, kk), tc::kslice_desc(bhi, kP, kk), idesc, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < kQ / 16; ++kk)
+        tc::mma_bf16(d, tc::kslice_desc(abase, kN, kk), tc::kslice_desc(blo, kP, kk), idesc, true);
+      tc::mma_commit(bar);
+    }
+    if (threadIdx.x < kQ && j + 1 < o.hb) load_x_block(xbase + (int64_t)(o.h0 + j + 1) * kP, xstride, o.q, xin);
+    if (j > 0) write_state(j - 1);
+  }
+  if (ok && o.hb > 0 && wait_phase(bar, (uint32_t)((o.hb - 1) & 1), p, ws.err)) {
+    tc::fence_after_sync();
+    write_state(o.hb - 1);
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 64);
+  if (warp == 0) tc::tmem_dealloc(tmem, kStateCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -308,170 +381,186 @@ __global__ void __launch_bounds__(256) ssd_state_pass_kernel(const SsdArgs p, co
 }
 
 // ---------------------------------------------------------------------------
-// Launch 3: the chunk's outputs.
+// Launch 3: the outputs of the CTA's heads over one chunk.  S = C Bᵀ is computed
+// once for all of them; per head j (buffers k = j & 1):
+//   Y_in = C h_inᵀ and, once head j−1's product is done, G_j → shared memory and
+//   Y = G_j X_j; head j−1's epilogue runs while head j's products do.
 struct OutSmem {
-  unsigned char c[kQ * kN * 2];    // C: Q rows × N, K-major (A of S and of Y_in); then G's lo term
-  unsigned char bg[kQ * kN * 2];   // B: Q rows × N (B of S); then G's hi term: Q rows × Q (A of Y)
-  unsigned char hin[kP * kN * 2];  // h_in, hi term: P rows × N (B of Y_in); then Xᵀ: P rows × Q (B of Y)
-  unsigned char hlo[kP * kN * 2];  // h_in, lo term
+  unsigned char c[kQ * kN * 2];          // C: Q rows × N, K-major (A of S and of every Y_in)
+  unsigned char bg[kQ * kN * 2];         // B: Q rows × N (B of S); then G's hi term (A of Y)
+  unsigned char glo[kQ * kQ * 2];        // G's lo term
+  unsigned char hin[2][2][kP * kN * 2];  // [buffer][hi, lo] h_in: P rows × N (B of Y_in)
+  unsigned char xt[2][kP * kQ * 2];      // [buffer] Xᵀ: P rows × Q tokens (B of Y)
   TokenSmem ts;
-  uint64_t bar;
+  uint64_t bar_s, bar_y;
   uint32_t tslot;
 };
-constexpr int kColS = 0, kColY = 128, kColYin = 192, kOutCols = 256;
+constexpr int kColS = 0, kOutCols = 512;
+__device__ __forceinline__ int col_y(int k) { return 128 + 128 * k; }
+__device__ __forceinline__ int col_yin(int k) { return 192 + 128 * k; }
 
-__global__ void __launch_bounds__(kThreads) ssd_chunk_out_kernel(const SsdArgs p, const SsdWs ws) {
+__global__ void __launch_bounds__(kThreads, 1) ssd_chunk_out_kernel(const SsdArgs p, const SsdWs ws) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   OutSmem& sm = *reinterpret_cast<OutSmem*>(smem_raw);
-  const int c = blockIdx.x, h = blockIdx.y;
-  const int64_t b = blockIdx.z;
-  const int g = (int)(h / (p.H / p.G));
-  const int64_t t0 = (int64_t)c * kQ;
-  const int q = (int)(p.L - t0 < kQ ? p.L - t0 : kQ);
-  const int warp = threadIdx.x >> 5;
-  const uint32_t bar = tc::smem_addr(&sm.bar);
-  if (threadIdx.x == 0) tc::mbar_init1(bar);
-  if (warp == 0) tc::tmem_alloc(tc::smem_addr(&sm.tslot), kOutCols);
-  // operands with K contiguous in global memory go by cp.async while the token scalars are computed
-  stage_rows_async<kQ>(sm.c, bf(p.C) + ((b * p.L + t0) * p.G + g) * kN, p.G * kN, q);
-  stage_rows_async<kQ>(sm.bg, bf(p.B) + ((b * p.L + t0) * p.G + g) * kN, p.G * kN, q);
-  const __nv_bfloat16* hin_g = ws.hin + ((b * p.H + h) * p.nchunks + c) * 2 * kP * kN;
-  stage_rows_async<kP>(sm.hin, hin_g, kN, kP);
-  stage_rows_async<kP>(sm.hlo, hin_g + kP * kN, kN, kP);
-  cp_async_commit();
-  // X (B of the last product, transposed) is read now and written over h_in's
-  // hi tile once the first products are done: core matrix (p group, token
-  // group) = (threadIdx % 8, threadIdx / 8)
-  uint4 xin[8];
-  const int xjg = threadIdx.x % (kP / 8), xig = threadIdx.x / (kP / 8);
-  {
-    const __nv_bfloat16* xg = bf(p.x) + ((b * p.L + t0) * p.H + h) * kP;
-#pragma unroll
-    for (int ii = 0; ii < 8; ++ii) {
-      const int i = xig * 8 + ii;
-      xin[ii] = i < q ? *reinterpret_cast<const uint4*>(xg + (int64_t)i * p.H * kP + xjg * 8) : make_uint4(0, 0, 0, 0);
-    }
-  }
-  chunk_tokens(p, b, h, t0, q, sm.ts);
-  cp_async_wait<0>();
-  tc::fence_smem_to_async();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = sm.tslot;
-  const uint32_t a_c = tc::smem_addr(sm.c), a_bg = tc::smem_addr(sm.bg), a_h = tc::smem_addr(sm.hin),
-                 a_hlo = tc::smem_addr(sm.hlo), a_x = a_h;
+  const CtaPos o = cta_pos(p);
+  const int warp = threadIdx.x >> 5, wq = warp & 3, hf = warp >> 2;
+  const int t = wq * 32 + (threadIdx.x & 31);  // this thread's token row (tensor-memory lane)
+  const uint32_t bar_s = tc::smem_addr(&sm.bar_s), bar_y = tc::smem_addr(&sm.bar_y);
   if (threadIdx.x == 0) {
-    const uint32_t id_s = tc::idesc_bf16_f32(kQ, kQ), id_y = tc::idesc_bf16_f32(kQ, kP);
+    tc::mbar_init1(bar_s);
+    tc::mbar_init1(bar_y);
+  }
+  if (warp == 0) tc::tmem_alloc(tc::smem_addr(&sm.tslot), kOutCols);
+  const __nv_bfloat16* hin_base = ws.hin + ((o.b * p.H + o.h0) * p.nchunks + o.c) * 2 * kP * kN;
+  const int64_t hin_head = p.nchunks * 2 * kP * kN;  // from one head to the next
+  auto stage_hin = [&](int j) {
+    const __nv_bfloat16* g = hin_base + (int64_t)j * hin_head;
+    stage_rows_async<kP>(sm.hin[j & 1][0], g, kN, kP);
+    stage_rows_async<kP>(sm.hin[j & 1][1], g + kP * kN, kN, kP);
+    cp_async_commit();
+  };
+  stage_rows_async<kQ>(sm.c, bf(p.C) + ((o.b * p.L + o.t0) * p.G + o.g) * kN, p.G * kN, o.q);
+  stage_rows_async<kQ>(sm.bg, bf(p.B) + ((o.b * p.L + o.t0) * p.G + o.g) * kN, p.G * kN, o.q);
+  cp_async_commit();
+  stage_hin(0);
+  const __nv_bfloat16* xbase = bf(p.x) + (o.b * p.L + o.t0) * p.H * kP;
+  const int64_t xstride = p.H * kP;
+  uint4 xin[8];
+  if (threadIdx.x < kQ) load_x_block(xbase + (int64_t)o.h0 * kP, xstride, o.q, xin);
+  chunk_tokens(p, o.b, o.h0, o.hb, o.t0, o.q, sm.ts);
+  cp_async_wait<1>();  // C and B
+  sync_for_mma();
+  const uint32_t tmem = sm.tslot;
+  const uint32_t a_c = tc::smem_addr(sm.c), a_bg = tc::smem_addr(sm.bg), a_glo = tc::smem_addr(sm.glo);
+  const uint32_t id_s = tc::idesc_bf16_f32(kQ, kQ), id_y = tc::idesc_bf16_f32(kQ, kP);
+  if (threadIdx.x == 0) {
 #pragma unroll
     for (int kk = 0; kk < kN / 16; ++kk)
       tc::mma_bf16(tmem + kColS, tc::kslice_desc(a_c, kQ, kk), tc::kslice_desc(a_bg, kQ, kk), id_s, kk > 0);
-#pragma unroll
-    for (int kk = 0; kk < kN / 16; ++kk)
-      tc::mma_bf16(tmem + kColYin, tc::kslice_desc(a_c, kQ, kk), tc::kslice_desc(a_h, kP, kk), id_y, kk > 0);
-#pragma unroll
-    for (int kk = 0; kk < kN / 16; ++kk)
-      tc::mma_bf16(tmem + kColYin, tc::kslice_desc(a_c, kQ, kk), tc::kslice_desc(a_hlo, kP, kk), id_y, true);
-    tc::mma_commit(bar);
+    tc::mma_commit(bar_s);
   }
-  bool ok = wait_phase(bar, 0, p, ws.err);
-  if (ok) {
-    tc::fence_after_sync();
-    {  // Xᵀ over h_in's hi tile (its product is complete)
-      uint4 xo[8];
-      transpose8x8(xin, xo);
-      unsigned char* dst = sm.hin + (size_t)((xig * (kP / 8)) + xjg) * 128;
+  // head j's x and z at row t, columns hf·32 .. hf·32 + 31, read ahead of its epilogue
+  uint4 xv[4], zv[4];
+  auto prefetch_xz = [&](int j) {
+    const int64_t row = ((o.b * p.L + o.t0 + t) * p.H + o.h0 + j) * kP + hf * 32;
+    const uint4* xr = reinterpret_cast<const uint4*>(bf(p.x) + row);
+    const uint4* zr = p.z ? reinterpret_cast<const uint4*>(bf(p.z) + row) : nullptr;
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) *reinterpret_cast<uint4*>(dst + jj * 16) = xo[jj];
+    for (int v4 = 0; v4 < 4; ++v4) {
+      xv[v4] = t < o.q ? xr[v4] : make_uint4(0, 0, 0, 0);
+      zv[v4] = (zr && t < o.q) ? zr[v4] : make_uint4(0, 0, 0, 0);
     }
-    // G_ts = S_ts · 2^(cs2_t − cs2_s) · φ_s for s ≤ t, written as the K-major A
-    // operand over s in two terms: hi over B's tile, lo over C's (both MMAs that
-    // read them have completed)
-    const int t = threadIdx.x;
-    const float cst = sm.ts.cs2[t];
-#pragma unroll 1
-    for (int blk = 0; blk < kQ / 32; ++blk) {
-      uint32_t hi[16], lo[16];
-      if (blk * 32 <= warp * 32 + 31) {  // warp-uniform: some s of the block is ≤ some t of the warp
-        float v[32];
-        tc::tmem_ld32(tc::tmem_lane_addr(tmem + kColS, warp * 32, blk * 32), v);
+  };
+  auto epilogue = [&](int j) {  // head j's outputs, row t, columns hf·32 .. hf·32 + 31
+    const int k = j & 1, h = o.h0 + j;
+    float y[32], yin[32];
+    tc::tmem_ld32(tc::tmem_lane_addr(tmem + (uint32_t)col_y(k), wq * 32, hf * 32), y);
+    tc::tmem_ld32(tc::tmem_lane_addr(tmem + (uint32_t)col_yin(k), wq * 32, hf * 32), yin);
+    if (t >= o.q) return;
+    const float et = ex2_approx(sm.ts.cs2[j][t]);
+    const float Dh = p.D ? p.D[h] : 0.f;
+    const bool gated = p.z != nullptr;
+    const int64_t row = ((o.b * p.L + o.t0 + t) * p.H + h) * kP + hf * 32;
+    uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row);
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const int s0 = blk * 32 + j;
-          const float g0 = s0 <= t ? v[j] * ex2_approx(cst - sm.ts.cs2[s0]) * sm.ts.phi[s0] : 0.f;
-          const float g1 = s0 + 1 <= t ? v[j + 1] * ex2_approx(cst - sm.ts.cs2[s0 + 1]) * sm.ts.phi[s0 + 1] : 0.f;
+    for (int v4 = 0; v4 < 4; ++v4) {
+      uint32_t ow[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint32_t xw = word_of(xv[v4], m), zw = word_of(zv[v4], m);
+        float r2[2];
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int jj = v4 * 8 + m * 2 + kk;
+          const float xf = __uint_as_float(kk ? (xw & 0xffff0000u) : (xw << 16));
+          float yv = fmaf(et, yin[jj], y[jj]);
+          yv = fmaf(Dh, xf, yv);
+          if (gated) yv *= silu_fast(__uint_as_float(kk ? (zw & 0xffff0000u) : (zw << 16)));
+          r2[kk] = yv;
+        }
+        ow[m] = pack_bf16x2(r2[0], r2[1]);
+      }
+      orow[v4] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    }
+  };
+  bool ok = true;
+  for (int j = 0; j < o.hb; ++j) {
+    const int k = j & 1;
+    if (j > 0) prefetch_xz(j - 1);
+    cp_async_wait<0>();  // head j's h_in
+    sync_for_mma();
+    if (threadIdx.x == 0) {
+      const uint32_t hhi = tc::smem_addr(sm.hin[k][0]), hlo = tc::smem_addr(sm.hin[k][1]),
+                     d = tmem + (uint32_t)col_yin(k);
+#pragma unroll
+      for (int kk = 0; kk < kN / 16; ++kk)
+        tc::mma_bf16(d, tc::kslice_desc(a_c, kQ, kk), tc::kslice_desc(hhi, kP, kk), id_y, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < kN / 16; ++kk)
+        tc::mma_bf16(d, tc::kslice_desc(a_c, kQ, kk), tc::kslice_desc(hlo, kP, kk), id_y, true);
+    }
+    // S (first head) or head j−1's products: G and the other buffers are free after it
+    const bool done = j == 0 ? wait_phase(bar_s, 0, p, ws.err) : wait_phase(bar_y, (uint32_t)((j - 1) & 1), p, ws.err);
+    ok = __syncthreads_and(ok && done) != 0;  // the same decision in every thread
+    if (!ok) break;
+    tc::fence_after_sync();
+    if (j + 1 < o.hb) stage_hin(j + 1);
+    if (threadIdx.x < kQ) {
+      store_xt(sm.xt[k], xin);
+      if (j + 1 < o.hb) load_x_block(xbase + (int64_t)(o.h0 + j + 1) * kP, xstride, o.q, xin);
+    }
+    // G_ts = S_ts · 2^(cs2_t − cs2_s) · φ_s for s ≤ t as hi (over B's tile) and lo terms;
+    // this thread: row t, column blocks 2·hf and 2·hf + 1
+    const float cst = sm.ts.cs2[j][t];
+    const float* cs2 = sm.ts.cs2[j];
+    const float* phi = sm.ts.phi[j];
+#pragma unroll 1
+    for (int bi = 0; bi < 2; ++bi) {
+      const int blk = 2 * hf + bi;
+      uint32_t hi[16], lo[16];
+      if (blk <= wq) {  // warp-uniform: some s of the block is ≤ some t of the warp
+        float v[32];
+        tc::tmem_ld32(tc::tmem_lane_addr(tmem + kColS, wq * 32, blk * 32), v);
+#pragma unroll
+        for (int jj = 0; jj < 32; jj += 2) {
+          const int s0 = blk * 32 + jj;
+          const float g0 = s0 <= t ? v[jj] * ex2_approx(cst - cs2[s0]) * phi[s0] : 0.f;
+          const float g1 = s0 + 1 <= t ? v[jj + 1] * ex2_approx(cst - cs2[s0 + 1]) * phi[s0 + 1] : 0.f;
           const __nv_bfloat162 gh = __floats2bfloat162_rn(g0, g1);
           const float2 ghf = __bfloat1622float2(gh);
-          hi[j / 2] = *reinterpret_cast<const uint32_t*>(&gh);
-          lo[j / 2] = pack_bf16x2(g0 - ghf.x, g1 - ghf.y);
+          hi[jj / 2] = *reinterpret_cast<const uint32_t*>(&gh);
+          lo[jj / 2] = pack_bf16x2(g0 - ghf.x, g1 - ghf.y);
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) hi[j] = lo[j] = 0u;
+        for (int jj = 0; jj < 16; ++jj) hi[jj] = lo[jj] = 0u;
       }
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const uint32_t off = tc::kmajor_offset(kQ, t, blk * 32 + m * 8);
         *reinterpret_cast<uint4*>(sm.bg + off) = make_uint4(hi[4 * m], hi[4 * m + 1], hi[4 * m + 2], hi[4 * m + 3]);
-        *reinterpret_cast<uint4*>(sm.c + off) = make_uint4(lo[4 * m], lo[4 * m + 1], lo[4 * m + 2], lo[4 * m + 3]);
+        *reinterpret_cast<uint4*>(sm.glo + off) = make_uint4(lo[4 * m], lo[4 * m + 1], lo[4 * m + 2], lo[4 * m + 3]);
       }
     }
-  }
-  tc::fence_smem_to_async();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  if (ok && threadIdx.x == 0) {
-    const uint32_t id_y = tc::idesc_bf16_f32(kQ, kP);
+    sync_for_mma();
+    if (threadIdx.x == 0) {
+      const uint32_t a_x = tc::smem_addr(sm.xt[k]), d = tmem + (uint32_t)col_y(k);
 #pragma unroll
-    for (int kk = 0; kk < kQ / 16; ++kk)
-      tc::mma_bf16(tmem + kColY, tc::kslice_desc(a_bg, kQ, kk), tc::kslice_desc(a_x, kP, kk), id_y, kk > 0);
+      for (int kk = 0; kk < kQ / 16; ++kk)
+        tc::mma_bf16(d, tc::kslice_desc(a_bg, kQ, kk), tc::kslice_desc(a_x, kP, kk), id_y, kk > 0);
 #pragma unroll
-    for (int kk = 0; kk < kQ / 16; ++kk)
-      tc::mma_bf16(tmem + kColY, tc::kslice_desc(a_c, kQ, kk), tc::kslice_desc(a_x, kP, kk), id_y, true);
-    tc::mma_commit(bar);
+      for (int kk = 0; kk < kQ / 16; ++kk)
+        tc::mma_bf16(d, tc::kslice_desc(a_glo, kQ, kk), tc::kslice_desc(a_x, kP, kk), id_y, true);
+      tc::mma_commit(bar_y);  // covers Y_in and Y of head j
+    }
+    if (j > 0) epilogue(j - 1);
   }
-  if (ok) ok = wait_phase(bar, 1, p, ws.err);
-  if (ok) {
+  if (ok && o.hb > 0) prefetch_xz(o.hb - 1);
+  if (ok && o.hb > 0 && wait_phase(bar_y, (uint32_t)((o.hb - 1) & 1), p, ws.err)) {
     tc::fence_after_sync();
-    const int t = threadIdx.x;
-    const float et = ex2_approx(sm.ts.cs2[t]);
-    const float Dh = p.D ? p.D[h] : 0.f;
-    const int64_t row = ((b * p.L + t0 + t) * p.H + h) * kP;
-#pragma unroll 1
-    for (int half = 0; half < kP / 32; ++half) {
-      float y[32], yin[32];
-      tc::tmem_ld32(tc::tmem_lane_addr(tmem + kColY, warp * 32, half * 32), y);
-      tc::tmem_ld32(tc::tmem_lane_addr(tmem + kColYin, warp * 32, half * 32), yin);
-      if (t < q) {
-        const uint4* xr = reinterpret_cast<const uint4*>(bf(p.x) + row + half * 32);
-        const uint4* zr = p.z ? reinterpret_cast<const uint4*>(bf(p.z) + row + half * 32) : nullptr;
-        uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row + half * 32);
-#pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-          const uint4 xv = xr[v4];
-          const uint4 zv = zr ? zr[v4] : make_uint4(0, 0, 0, 0);
-          uint32_t o[4];
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const uint32_t xw = word_of(xv, m), zw = word_of(zv, m);
-            float r2[2];
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const int j = v4 * 8 + m * 2 + k;
-              const float xf = __uint_as_float(k ? (xw & 0xffff0000u) : (xw << 16));
-              float yv = fmaf(et, yin[j], y[j]);
-              yv = fmaf(Dh, xf, yv);
-              if (zr) yv *= silu_fast(__uint_as_float(k ? (zw & 0xffff0000u) : (zw << 16)));
-              r2[k] = yv;
-            }
-            o[m] = pack_bf16x2(r2[0], r2[1]);
-          }
-          orow[v4] = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      }
-    }
+    epilogue(o.hb - 1);
   }
+  cp_async_wait<0>();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kOutCols);
@@ -488,6 +577,14 @@ size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H) {
 cudaError_t ssd_launch(SsdArgs p, cudaStream_t stream) {
   p.nchunks = (p.L + kQ - 1) / kQ;
   if (p.timeout_ns <= 0) p.timeout_ns = (long long)kDefaultTimeoutMs * 1000000ll;
+  // heads per CTA: the largest divisor of the heads of a group up to kMaxHeadsPerCta
+  const int64_t hpg = p.H / p.G;
+  p.heads_per_cta = 1;
+  for (int d = kMaxHeadsPerCta; d >= 1; --d)
+    if (hpg % d == 0) {
+      p.heads_per_cta = d;
+      break;
+    }
   const SsdWs ws = ws_layout(p.ws, p.batch, p.H, p.nchunks < 1 ? 1 : p.nchunks);
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(ssd_chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -496,15 +593,14 @@ cudaError_t ssd_launch(SsdArgs p, cudaStream_t stream) {
   if ((e = cudaFuncSetAttribute(ssd_chunk_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)sizeof(OutSmem))) != cudaSuccess)
     return e;
+  const dim3 grid((unsigned)p.nchunks, (unsigned)(p.H / p.heads_per_cta), (unsigned)p.batch);
   if (p.nchunks > 0) {
-    const dim3 grid((unsigned)p.nchunks, (unsigned)p.H, (unsigned)p.batch);
     ssd_chunk_state_kernel<<<grid, kThreads, sizeof(StateSmem), stream>>>(p, ws);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   ssd_state_pass_kernel<<<dim3((unsigned)(p.batch * p.H), kP * kN / 256), 256, 0, stream>>>(p, ws);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.nchunks > 0) {
-    const dim3 grid((unsigned)p.nchunks, (unsigned)p.H, (unsigned)p.batch);
     ssd_chunk_out_kernel<<<grid, kThreads, sizeof(OutSmem), stream>>>(p, ws);
     e = cudaGetLastError();
   }

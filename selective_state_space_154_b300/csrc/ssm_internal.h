@@ -164,6 +164,7 @@ struct SsdArgs {
   void* ws;
   int64_t batch, L, H, P, G, N, nchunks;
   long long timeout_ns;
+  int heads_per_cta;  // set by the launcher
 };
 constexpr int kSsdChunk = 128;    // tokens per chunk
 constexpr int kSsdHeadDim = 64;   // supported headdim

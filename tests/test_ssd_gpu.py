@@ -97,3 +97,12 @@ def test_ssd_mamba2_2p7b_layer_sampled_heads():
         ref, href = _oracle(sub)
         assert rel_err(to_np(out[:, :, h:h + 1]), ref) <= BF16, h
         assert rel_err(to_np(fs[:, h:h + 1]), href) <= BF16, h
+
+
+@pytest.mark.parametrize("shape", [(1, 300, 5, 64, 1, 128), (1, 260, 12, 64, 2, 128), (2, 150, 14, 64, 2, 128),
+                                   (1, 400, 16, 64, 1, 128)],
+                         ids=["5_heads_per_cta", "6_heads_per_cta", "7_heads_per_cta", "8_heads_per_cta_x2"])
+def test_ssd_heads_per_cta(shape):
+    """A CTA takes up to 8 heads of one group (the largest divisor of heads per group):
+    odd and even counts, several head blocks per group."""
+    _compare(W.random_ssd_inputs(*shape, device=DEV, seed=shape[2]))
