@@ -247,6 +247,14 @@ __device__ __forceinline__ void sync_for_mma() {
   tc::fence_after_sync();
 }
 
+// After giving up on a wait: one more commit, which completes once every MMA
+// this CTA's issuing thread has started is done, and a bounded wait for it, so
+// that tensor memory is not released under a running product.
+__device__ __forceinline__ void drain_mmas(uint32_t bar, const SsdArgs& p, unsigned* err) {
+  if (threadIdx.x == 0) tc::mma_commit(bar);
+  wait_phase(bar, 0, p, err);
+}
+
 // Where the CTA sits: chunk blockIdx.x, heads h0 .. h0 + hb − 1 (one group), batch blockIdx.z.
 struct CtaPos {
   int64_t b, t0;
@@ -273,7 +281,7 @@ struct StateSmem {
   unsigned char bt[kN * kQ * 2];          // Bᵀ: N rows × Q tokens, K-major
   unsigned char xw[2][2][kP * kQ * 2];    // [buffer][hi, lo] (diag(w) X)ᵀ: P rows × Q tokens
   TokenSmem ts;
-  uint64_t bar;
+  uint64_t bar, bar_drain;
   uint32_t tslot;
 };
 constexpr int kStateCols = 128;  // two 64-column accumulators
@@ -283,8 +291,11 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_state_kernel(const SsdA
   StateSmem& sm = *reinterpret_cast<StateSmem*>(smem_raw);
   const CtaPos o = cta_pos(p);
   const int warp = threadIdx.x >> 5, wq = warp & 3, hf = warp >> 2;
-  const uint32_t bar = tc::smem_addr(&sm.bar);
-  if (threadIdx.x == 0) tc::mbar_init1(bar);
+  const uint32_t bar = tc::smem_addr(&sm.bar), bar_drain = tc::smem_addr(&sm.bar_drain);
+  if (threadIdx.x == 0) {
+    tc::mbar_init1(bar);
+    tc::mbar_init1(bar_drain);
+  }
   if (warp == 0) tc::tmem_alloc(tc::smem_addr(&sm.tslot), kStateCols);
   const __nv_bfloat16* xbase = bf(p.x) + (o.b * p.L + o.t0) * p.H * kP;
   const int64_t xstride = p.H * kP;
@@ -335,10 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_state_kernel(const SsdA
     if (threadIdx.x < kQ && j + 1 < o.hb) load_x_block(xbase + (int64_t)(o.h0 + j + 1) * kP, xstride, o.q, xin);
     if (j > 0) write_state(j - 1);
   }
-  if (ok && o.hb > 0 && wait_phase(bar, (uint32_t)((o.hb - 1) & 1), p, ws.err)) {
+  if (ok && o.hb > 0) ok = __syncthreads_and(wait_phase(bar, (uint32_t)((o.hb - 1) & 1), p, ws.err)) != 0;
+  if (ok && o.hb > 0) {
     tc::fence_after_sync();
     write_state(o.hb - 1);
   }
+  if (!ok) drain_mmas(bar_drain, p, ws.err);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kStateCols);
@@ -392,7 +405,7 @@ struct OutSmem {
   unsigned char hin[2][2][kP * kN * 2];  // [buffer][hi, lo] h_in: P rows × N (B of Y_in)
   unsigned char xt[2][kP * kQ * 2];      // [buffer] Xᵀ: P rows × Q tokens (B of Y)
   TokenSmem ts;
-  uint64_t bar_s, bar_y;
+  uint64_t bar_s, bar_y, bar_drain, bar_never;  // bar_never: the test hook's wait (nothing arrives)
   uint32_t tslot;
 };
 constexpr int kColS = 0, kOutCols = 512;
@@ -405,10 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_out_kernel(const SsdArg
   const CtaPos o = cta_pos(p);
   const int warp = threadIdx.x >> 5, wq = warp & 3, hf = warp >> 2;
   const int t = wq * 32 + (threadIdx.x & 31);  // this thread's token row (tensor-memory lane)
-  const uint32_t bar_s = tc::smem_addr(&sm.bar_s), bar_y = tc::smem_addr(&sm.bar_y);
+  const uint32_t bar_s = tc::smem_addr(&sm.bar_s), bar_y = tc::smem_addr(&sm.bar_y),
+                 bar_drain = tc::smem_addr(&sm.bar_drain), bar_never = tc::smem_addr(&sm.bar_never);
   if (threadIdx.x == 0) {
     tc::mbar_init1(bar_s);
     tc::mbar_init1(bar_y);
+    tc::mbar_init1(bar_drain);
+    tc::mbar_init1(bar_never);
   }
   if (warp == 0) tc::tmem_alloc(tc::smem_addr(&sm.tslot), kOutCols);
   const __nv_bfloat16* hin_base = ws.hin + ((o.b * p.H + o.h0) * p.nchunks + o.c) * 2 * kP * kN;
@@ -500,7 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_out_kernel(const SsdArg
         tc::mma_bf16(d, tc::kslice_desc(a_c, kQ, kk), tc::kslice_desc(hlo, kP, kk), id_y, true);
     }
     // S (first head) or head j−1's products: G and the other buffers are free after it
-    const bool done = j == 0 ? wait_phase(bar_s, 0, p, ws.err) : wait_phase(bar_y, (uint32_t)((j - 1) & 1), p, ws.err);
+    const bool done = j == 0 ? wait_phase(p.fault ? bar_never : bar_s, 0, p, ws.err)
+                             : wait_phase(bar_y, (uint32_t)((j - 1) & 1), p, ws.err);
     ok = __syncthreads_and(ok && done) != 0;  // the same decision in every thread
     if (!ok) break;
     tc::fence_after_sync();
@@ -556,10 +573,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_out_kernel(const SsdArg
     if (j > 0) epilogue(j - 1);
   }
   if (ok && o.hb > 0) prefetch_xz(o.hb - 1);
-  if (ok && o.hb > 0 && wait_phase(bar_y, (uint32_t)((o.hb - 1) & 1), p, ws.err)) {
+  if (ok && o.hb > 0) ok = __syncthreads_and(wait_phase(bar_y, (uint32_t)((o.hb - 1) & 1), p, ws.err)) != 0;
+  if (ok && o.hb > 0) {
     tc::fence_after_sync();
     epilogue(o.hb - 1);
   }
+  if (!ok) drain_mmas(bar_drain, p, ws.err);
   cp_async_wait<0>();
   tc::fence_before_sync();
   __syncthreads();

@@ -23,6 +23,7 @@ RuntimeKnobs runtime_knobs() {
     const char* f = std::getenv("SSM_FAULT");
     r.fault_lookback = f && std::strcmp(f, "lookback") == 0;
     r.fault_step = f && std::strcmp(f, "step") == 0;
+    r.fault_ssd = f && std::strcmp(f, "ssd") == 0;
     const char* fs = std::getenv("SSM_FORCE_STEP");
     r.force_step_plain = fs && std::strcmp(fs, "plain") == 0;
     if (const char* c = std::getenv("SSM_FORCE_CHUNKS")) r.force_chunks = std::atoi(c);
@@ -326,7 +327,9 @@ ssm_status ssd_scan_fwd(const void* x, const void* dt, const float* A, const voi
   a.h0 = initial_state; a.out = out; a.final_state = final_state; a.ws = workspace;
   a.batch = dims->batch; a.L = dims->seqlen; a.H = dims->nheads; a.P = dims->headdim; a.G = dims->ngroups;
   a.N = dims->d_state;
-  a.timeout_ns = ssm::runtime_knobs().lookback_timeout_ns;
+  const ssm::RuntimeKnobs knobs = ssm::runtime_knobs();
+  a.timeout_ns = knobs.lookback_timeout_ns;
+  a.fault = knobs.fault_ssd ? 1 : 0;
   return ssm::ssd_launch(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

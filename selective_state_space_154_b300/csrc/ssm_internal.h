@@ -70,6 +70,7 @@ struct RuntimeKnobs {
   bool fault_step;                // test hook: the pipelined step's first wait never completes
   bool force_step_plain;          // SSM_FORCE_STEP=plain: the generic step kernel only
   int bwd_chunks;                 // >0: sequence chunks of the backward (tests)
+  bool fault_ssd;                 // test hook: the SSD output kernel's first wait never completes
 };
 RuntimeKnobs runtime_knobs();
 
@@ -165,6 +166,7 @@ struct SsdArgs {
   int64_t batch, L, H, P, G, N, nchunks;
   long long timeout_ns;
   int heads_per_cta;  // set by the launcher
+  int fault;          // test hook: the output kernel waits on an mbarrier nothing arrives on
 };
 constexpr int kSsdChunk = 128;    // tokens per chunk
 constexpr int kSsdHeadDim = 64;   // supported headdim
