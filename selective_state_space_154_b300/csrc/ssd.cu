@@ -286,7 +286,7 @@ struct StateSmem {
 };
 constexpr int kStateCols = 128;  // two 64-column accumulators
 
-__global__ void __launch_bounds__(kThreads, 1) ssd_chunk_state_kernel(const SsdArgs p, const SsdWs ws) {
+__global__ void __launch_bounds__(kThreads, 2) ssd_chunk_state_kernel(const SsdArgs p, const SsdWs ws) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   StateSmem& sm = *reinterpret_cast<StateSmem*>(smem_raw);
   const CtaPos o = cta_pos(p);
