@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_chunk_kernel(const Bw
     stage_bc<T>(sm, p, o.b, t0, nv);
     row_scalars<T>(sm, p, r, g, o.row_ok, o.row, t0, nv, biasc, want_g);
     __syncthreads();
-    for (int v = 0; v < nv; ++v) {
+    auto token = [&](int v) {
       const TokScalars s = sm.ts[v][r];
       float ab[kBwdG];
       fwd_token<FAST>(q, h, ab, s.dt, s.x, &sm.bc[v][0][kBwdG * g]);
@@ -324,6 +324,12 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_chunk_kernel(const Bw
         }
       }
       S += s.dt;
+    };
+    if (nv == kBwdTok) {  // full blocks: unrolled, shared-memory offsets fixed at compile time
+#pragma unroll
+      for (int v = 0; v < kBwdTok; ++v) token(v);
+    } else {
+      for (int v = 0; v < nv; ++v) token(v);
     }
   }
   const int64_t cs = o.rt * p.kmax + o.chunk;
@@ -396,14 +402,20 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     sm.hs[0][r][g] = h0v;
     __syncthreads();  // bc and ts staged
     // recompute the block's states
-    for (int v = 0; v < nv; ++v) {
+    auto recompute = [&](int v) {
       const TokScalars s = sm.st.ts[v][r];
       float ab[kBwdG];
       fwd_token<FAST>(q, h, ab, s.dt, s.x, &sm.st.bc[v][0][kBwdG * g]);
       sm.hs[v + 1][r][g] = make_float4(h[0], h[1], h[2], h[3]);
+    };
+    if (nv == kBwdTok) {  // full blocks: unrolled, shared-memory offsets fixed at compile time
+#pragma unroll
+      for (int v = 0; v < kBwdTok; ++v) recompute(v);
+    } else {
+      for (int v = 0; v < nv; ++v) recompute(v);
     }
     // adjoint over the block, last token first
-    for (int v = nv - 1; v >= 0; --v) {
+    auto adjoint = [&](int v) {
       const int64_t i = row * L + t0 + v;
       const TokScalars s = sm.st.ts[v][r];
       const float4 hv4 = sm.hs[v + 1][r][g], hp4 = sm.hs[v][r][g];
@@ -491,6 +503,12 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
       }
       // Σ over the CTA's rows of the 32 (B|C, n) slots: warp reduce-scatter, then shared memory
       sm.red[warp][v][lane] = rows_reduce_scatter8(slots);
+    };
+    if (nv == kBwdTok) {
+#pragma unroll
+      for (int v = kBwdTok - 1; v >= 0; --v) adjoint(v);
+    } else {
+      for (int v = nv - 1; v >= 0; --v) adjoint(v);
     }
     __syncthreads();  // red complete
     for (int sidx = threadIdx.x; sidx < nv * 32; sidx += kBwdThreads) {
