@@ -410,7 +410,33 @@ def bench_ssd(dev, hbm_peak, tc_peak, runs=20):
                      "tflops": flops / secs / 1e12, "tensor_frac": flops / secs / 1e12 / tc_peak,
                      "workspace_bytes": ws.numel()}
         del inp, out, fs, ws
+    # decode: one token for 256 sequences of the 2.7B-shaped layer (80 heads × 64 × 128 fp32 state,
+    # 671 MB > L2, so no flush is needed), steps timed one by one
+    b, H, P, N = 256, 80, 64, 128
+    dshape = W.SsdShape("decode", b, 1, H, P, 1, N, torch.bfloat16)
+    dinp = W.ssd_inputs(dshape, device=dev, seed=0)
+    state = torch.zeros((b, H, P, N), device=dev)
+    tok = dict(x=dinp["x"][:, 0].contiguous(), dt=dinp["dt"][:, 0].contiguous(), B=dinp["B"][:, 0].contiguous(),
+               C=dinp["C"][:, 0].contiguous(), z=dinp["z"][:, 0].contiguous())
+    yout = torch.empty_like(tok["x"])
+    step = lambda: ssm.ssd_step(state, tok["x"], tok["dt"], dinp["A"], tok["B"], tok["C"], D=dinp["D"], z=tok["z"],
+                                dt_bias=dinp["dt_bias"], out=yout, stream=stream)
+    for _ in range(3):
+        step()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
+    for a, e in evs:
+        a.record(stream)
+        step()
+        e.record(stream)
+    torch.cuda.synchronize()
+    secs = statistics.median(a.elapsed_time(e) for a, e in evs) / 1e3
+    alg = 2 * b * H * P * N * 4 + 3 * b * H * P * 2 + b * H * 2 + 2 * b * N * 2
+    res["decode_mamba2_2p7b"] = {"batch": b, "nheads": H, "headdim": P, "d_state": N, "us": secs * 1e6,
+                                 "tokens_per_s": b / secs, "gbs": alg / secs / 1e9,
+                                 "hbm_frac": alg / secs / 1e9 / hbm_peak, "alg_bytes": alg,
+                                 "note": "ssd_step, state read and written in place (671 MB > L2)"}
     return res
+
 
 def bench_conv(dev, hbm_peak, runs=20):
     """Causal Conv1D + SiLU: the sequence form on the 2.8B-shaped layer's x (L2

@@ -297,6 +297,25 @@ SSM_API ssm_status ssd_scan_fwd(const void* x, const void* dt, const float* A, c
                                 void* out, float* final_state, const ssd_dims* dims, void* workspace,
                                 size_t workspace_bytes, ssm_stream_t stream);
 
+/*
+ * Recurrent (decode) mode of the Mamba-2 layer: one token for every (batch, head),
+ * with `state` updated in place:
+ *   H ← Ā H + φ x Bᵀ,   out = (H C + D x) · silu(z)
+ * (Ā, φ and the step size as for ssd_scan_fwd; the two modes of the pages,
+ * "State Space Models（SSM）とMamba" §2.4 二つのモード).  Continues a prefill whose
+ * final_state it is given.
+ *   state: [batch][nheads][headdim][d_state] float32, 16-byte aligned (in-out).
+ *   x, z, out: [batch][nheads][headdim] bf16 (z may be NULL).
+ *   dt: [batch][nheads] bf16 (Δraw).
+ *   B, C: [batch][ngroups][d_state] bf16, 16-byte aligned.
+ *   A, D, dt_bias: [nheads] float32 (D, dt_bias may be NULL).
+ *   dims: as for ssd_scan_fwd (seqlen is ignored), with the same supported sizes.
+ * One kernel launch on `stream`; no workspace; out must not alias an input.
+ */
+SSM_API ssm_status ssd_step(float* state, const void* x, const void* dt, const float* A, const void* B,
+                            const void* C, const float* D, const void* z, const float* dt_bias, void* out,
+                            const ssd_dims* dims, ssm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,7 @@ __all__ = [
     "SSM_NOALLOC_SCRATCH_BYTES", "ssm_step_check", "ssm_scan_fwd_from_state",
     "ssm_conv1d_fwd", "ssm_conv1d_step", "conv1d", "conv1d_step",
     "ssm_scan_bwd_workspace_bytes", "ssm_scan_bwd", "scan_bwd",
-    "ssd_scan_workspace_bytes", "ssd_scan_fwd", "ssd_scan",
+    "ssd_scan_workspace_bytes", "ssd_scan_fwd", "ssd_scan", "ssd_step",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -98,6 +98,8 @@ def load_library():
             lib.ssd_scan_workspace_bytes.restype = sz
             lib.ssd_scan_fwd.argtypes = [vp] * 11 + [sdp, vp, sz, vp]
             lib.ssd_scan_fwd.restype = i32
+            lib.ssd_step.argtypes = [vp] * 10 + [sdp, vp]
+            lib.ssd_step.restype = i32
             lib.ssm_status_string.argtypes = [i32]
             lib.ssm_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -474,3 +476,37 @@ def ssd_scan(x, dt, A, B, C, D=None, z=None, dt_bias=None, initial_state=None, r
         fs = torch.empty((x.shape[0], x.shape[2], x.shape[3], B.shape[3]), dtype=torch.float32, device=x.device)
     ssd_scan_fwd(x, dt, A, B, C, D, z, dt_bias, initial_state, out, fs, workspace=workspace, stream=stream)
     return (out, fs) if return_final_state else out
+
+
+def ssd_step(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, out=None, stream=None):
+    """One decode token of the Mamba-2 layer (``state`` [batch, H, P, N] fp32 updated in
+    place); x, z: [batch, H, P]; dt: [batch, H]; B, C: [batch, G, N].  Returns ``out``."""
+    lib = load_library()
+    if not isinstance(state, torch.Tensor) or state.dim() != 4:
+        raise ValueError("state must be a [batch, nheads, headdim, d_state] tensor")
+    if not isinstance(B, torch.Tensor) or B.dim() != 3:
+        raise ValueError("B must be a [batch, ngroups, d_state] tensor")
+    batch, H, P, N = state.shape
+    G = B.shape[1]
+    act, dev = x.dtype, state.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    if out is None:
+        out = torch.empty_like(x)
+    _check(state, "state", torch.float32, (batch, H, P, N), dev)
+    _check(x, "x", act, (batch, H, P), dev)
+    _check(dt, "dt", act, (batch, H), dev)
+    _check(A, "A", torch.float32, (H,), dev)
+    _check(B, "B", act, (batch, G, N), dev)
+    _check(C, "C", act, (batch, G, N), dev)
+    _check(D, "D", torch.float32, (H,), dev, required=False)
+    _check(z, "z", act, (batch, H, P), dev, required=False)
+    _check(dt_bias, "dt_bias", torch.float32, (H,), dev, required=False)
+    _check(out, "out", act, (batch, H, P), dev)
+    dims = _ssd_dims(batch, 1, H, P, G, N, act)
+    with torch.cuda.device(dev):
+        st = lib.ssd_step(*(_ptr(t) for t in (state, x, dt, A, B, C, D, z, dt_bias, out)), ctypes.byref(dims),
+                          _stream_handle(stream, dev))
+    if st != SSM_OK:
+        raise SsmError(st, "ssd_step")
+    return out

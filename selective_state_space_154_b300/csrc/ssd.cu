@@ -627,3 +627,85 @@ cudaError_t ssd_launch(SsdArgs p, cudaStream_t stream) {
 }
 
 }  // namespace ssm
+
+// ---------------------------------------------------------------------------
+// Recurrent (decode) mode of the Mamba-2 layer: one token for every (batch, head),
+// the state (headdim × d_state, fp32) updated in place:
+//   H ← Ā H + φ x Bᵀ,   out = (H C + D x) · silu(z)
+// ("State Space Models（SSM）とMamba" §2.4 二つのモード; the per-head structure of
+// §4.6 Mamba-2).  One CTA of 8 warps per (batch, head); warp w takes rows
+// p = w, w + 8, ...; lane l holds states 4l .. 4l + 3 of a row (d_state 128), so a
+// row's 512 bytes are one coalesced warp access, and the readout is a warp sum.
+// Memory-bound: the state is read and written once.
+namespace ssm {
+namespace {
+
+constexpr int kStepRowsPerIter = 8;  // rows per warp whose loads are issued together
+
+__global__ void __launch_bounds__(256, 3) ssd_step_kernel(const SsdStepArgs p) {
+  const int64_t bh = blockIdx.x;  // b * H + h
+  const int64_t b = bh / p.H, h = bh % p.H, g = h / (p.H / p.G);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const __nv_bfloat16* bf_dt = static_cast<const __nv_bfloat16*>(p.dt);
+  const float a = p.A[h];
+  const float d = softplus_precise(__bfloat162float(bf_dt[bh]) + (p.dt_bias ? p.dt_bias[h] : 0.f));
+  const float abar = expf(d * a);
+  const float phi = a != 0.f ? expm1f(d * a) / a : d;
+  const float Dh = p.D ? p.D[h] : 0.f;
+  // this lane's four states of B and C (bf16 → fp32)
+  const uint2 bw = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.B) + (b * p.G + g) * kSsdState + 4 * lane);
+  const uint2 cw = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.C) + (b * p.G + g) * kSsdState + 4 * lane);
+  const float Bv[4] = {__uint_as_float(bw.x << 16), __uint_as_float(bw.x & 0xffff0000u), __uint_as_float(bw.y << 16),
+                       __uint_as_float(bw.y & 0xffff0000u)};
+  const float Cv[4] = {__uint_as_float(cw.x << 16), __uint_as_float(cw.x & 0xffff0000u), __uint_as_float(cw.y << 16),
+                       __uint_as_float(cw.y & 0xffff0000u)};
+  const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(p.x) + bh * p.P;
+  const __nv_bfloat16* zr = p.z ? static_cast<const __nv_bfloat16*>(p.z) + bh * p.P : nullptr;
+  __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + bh * p.P;
+  float4* st = reinterpret_cast<float4*>(p.state + bh * p.P * kSsdState) + lane;
+  for (int64_t base = warp; base < p.P; base += 8 * kStepRowsPerIter) {
+    float4 s[kStepRowsPerIter];
+    float xv[kStepRowsPerIter];
+#pragma unroll
+    for (int k = 0; k < kStepRowsPerIter; ++k) {
+      const int64_t row = base + 8 * k;
+      if (row < p.P) {
+        s[k] = st[row * (kSsdState / 4)];
+        xv[k] = __bfloat162float(xr[row]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kStepRowsPerIter; ++k) {
+      const int64_t row = base + 8 * k;
+      if (row >= p.P) break;
+      const float px = phi * xv[k];
+      float4 v = s[k];
+      v.x = fmaf(abar, v.x, px * Bv[0]);
+      v.y = fmaf(abar, v.y, px * Bv[1]);
+      v.z = fmaf(abar, v.z, px * Bv[2]);
+      v.w = fmaf(abar, v.w, px * Bv[3]);
+      st[row * (kSsdState / 4)] = v;
+      float y = v.x * Cv[0];
+      y = fmaf(v.y, Cv[1], y);
+      y = fmaf(v.z, Cv[2], y);
+      y = fmaf(v.w, Cv[3], y);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+      if (lane == 0) {
+        y = fmaf(Dh, xv[k], y);
+        if (zr) y *= silu_precise(__bfloat162float(zr[row]));
+        orow[row] = __float2bfloat16_rn(y);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t ssd_step_launch(const SsdStepArgs& p, cudaStream_t stream) {
+  if (p.batch * p.H == 0) return cudaSuccess;
+  ssd_step_kernel<<<(unsigned)(p.batch * p.H), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ssm

@@ -333,6 +333,28 @@ ssm_status ssd_scan_fwd(const void* x, const void* dt, const float* A, const voi
   return ssm::ssd_launch(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
+ssm_status ssd_step(float* state, const void* x, const void* dt, const float* A, const void* B, const void* C,
+                    const float* D, const void* z, const float* dt_bias, void* out, const ssd_dims* dims,
+                    ssm_stream_t stream) {
+  const ssm_status ds = check_ssd_dims(dims);
+  if (ds != SSM_OK) return ds;
+  if (!state || !x || !dt || !A || !B || !C || !out) return SSM_ERR_INVALID_ARG;
+  const void* v16[] = {state, B, C};
+  for (const void* p : v16)
+    if (!aligned16(p)) return SSM_ERR_ALIGNMENT;
+  const void* v2[] = {x, dt, z, out};
+  for (const void* p : v2)
+    if (p && !aligned(p, 2)) return SSM_ERR_ALIGNMENT;
+  const void* f32_ptrs[] = {A, D, dt_bias};
+  for (const void* p : f32_ptrs)
+    if (p && !aligned(p, 4)) return SSM_ERR_ALIGNMENT;
+  if (dims->batch * dims->nheads > INT32_MAX) return SSM_ERR_UNSUPPORTED;
+  ssm::SsdStepArgs a{};
+  a.state = state; a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias;
+  a.out = out; a.batch = dims->batch; a.H = dims->nheads; a.P = dims->headdim; a.G = dims->ngroups;
+  return ssm::ssd_step_launch(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
 ssm_status ssm_scan_check(const void* workspace, size_t workspace_bytes) {
   if (!workspace || workspace_bytes < sizeof(unsigned) * 2) return SSM_OK;
   unsigned word = 0;

@@ -174,6 +174,23 @@ constexpr int kSsdState = 128;    // supported d_state
 size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H);
 cudaError_t ssd_launch(SsdArgs p, cudaStream_t stream);
 
+// One decode token of the Mamba-2 layer (ssd.cu): state [batch][H][P][N] fp32 in place;
+// x, z, out [batch][H][P], dt [batch][H], B, C [batch][G][N] (bf16); A, D, dt_bias [H].
+struct SsdStepArgs {
+  float* state;
+  const void* x;
+  const void* dt;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* dt_bias;
+  void* out;
+  int64_t batch, H, P, G;
+};
+cudaError_t ssd_step_launch(const SsdStepArgs& p, cudaStream_t stream);
+
 // Reads and clears the sticky error word of the pipelined step kernel (current device).
 cudaError_t step_error_fetch_clear(unsigned* word);
 

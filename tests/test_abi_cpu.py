@@ -251,3 +251,26 @@ def test_ssd_workspace_size_and_check(lib):
     assert _ssd(lib, d, ws_bytes=need - 1) == ssm.SSM_ERR_WORKSPACE
     assert _ssd(lib, d, ws=None, ws_bytes=0) == ssm.SSM_ERR_WORKSPACE
     assert _ssd(lib, d, ws=FAKE + 8, ws_bytes=need) == ssm.SSM_ERR_ALIGNMENT
+
+
+def _ssd_step(lib, dims, ptrs=None):
+    p = dict(state=FAKE, x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, bias=None, out=FAKE)
+    p.update(ptrs or {})
+    args = [ctypes.c_void_p(p[k]) if p[k] else None
+            for k in ("state", "x", "dt", "A", "B", "C", "D", "z", "bias", "out")]
+    return lib.ssd_step(*args, ctypes.byref(dims), None)
+
+
+@pytest.mark.parametrize("missing", ["state", "x", "dt", "A", "B", "C", "out"])
+def test_ssd_step_rejects_null_required_pointer(lib, missing):
+    assert _ssd_step(lib, _ssd_dims(), {missing: None}) == ssm.SSM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("which,offset", [("state", 4), ("B", 8), ("C", 2), ("x", 1), ("out", 1), ("A", 2)])
+def test_ssd_step_rejects_misaligned_pointer(lib, which, offset):
+    assert _ssd_step(lib, _ssd_dims(), {which: FAKE + offset}) == ssm.SSM_ERR_ALIGNMENT
+
+
+def test_ssd_step_rejects_unsupported_dims(lib):
+    assert _ssd_step(lib, _ssd_dims(d_state=64)) == ssm.SSM_ERR_UNSUPPORTED
+    assert _ssd_step(lib, _ssd_dims(ngroups=3)) == ssm.SSM_ERR_INVALID_ARG

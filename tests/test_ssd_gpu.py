@@ -129,3 +129,67 @@ def test_ssd_wait_timeout_is_reported_and_the_context_recovers(monkeypatch):
     ref, href = _oracle(inp)
     assert rel_err(to_np(out), ref) <= BF16
     assert rel_err(to_np(fs), href) <= BF16
+
+
+def _step_inputs(inp, t):
+    """Token t of a sequence's inputs, in the decode layout."""
+    return dict(x=inp["x"][:, t].contiguous(), dt=inp["dt"][:, t].contiguous(), B=inp["B"][:, t].contiguous(),
+                C=inp["C"][:, t].contiguous(), z=None if inp["z"] is None else inp["z"][:, t].contiguous())
+
+
+@pytest.mark.parametrize("opts", [dict(), dict(gate=False, skip=False, with_bias=False)], ids=["all", "none"])
+def test_ssd_step_matches_oracle(opts):
+    """One decode token from a random state: the oracle's scan of one token from that state."""
+    inp = W.random_ssd_inputs(2, 1, 4, 64, 2, 128, device=DEV, seed=14, **opts)
+    g = torch.Generator(device=DEV).manual_seed(15)
+    state = torch.randn((2, 4, 64, 128), generator=g, device=DEV)
+    ref, href = _oracle(inp, state)
+    tok = _step_inputs(inp, 0)
+    y = ssm.ssd_step(state, tok["x"], tok["dt"], inp["A"], tok["B"], tok["C"], D=inp["D"], z=tok["z"],
+                     dt_bias=inp["dt_bias"])
+    torch.cuda.synchronize()
+    assert rel_err(to_np(y), ref[:, 0]) <= BF16
+    assert rel_err(to_np(state), href) <= 1e-5  # fp32 state: one update's rounding
+
+
+def test_ssd_prefill_then_decode():
+    """ssd_scan_fwd over the first 300 tokens, then 20 ssd_step calls from its final state:
+    the outputs and the final state match the oracle over all 320 tokens, and the device's
+    own scan of all 320."""
+    L0, L = 300, 320
+    inp = W.random_ssd_inputs(2, L, 4, 64, 2, 128, device=DEV, seed=16)
+    ref, href = _oracle(inp)
+    pre = {k: (v if k in ("A", "D", "dt_bias") or v is None else v[:, :L0].contiguous()) for k, v in inp.items()}
+    _, state = _gpu(pre)
+    ys = []
+    for t in range(L0, L):
+        tok = _step_inputs(inp, t)
+        ys.append(ssm.ssd_step(state, tok["x"], tok["dt"], inp["A"], tok["B"], tok["C"], D=inp["D"], z=tok["z"],
+                               dt_bias=inp["dt_bias"]))
+    torch.cuda.synchronize()
+    dec = torch.stack(ys, dim=1)
+    assert rel_err(to_np(dec), ref[:, L0:]) <= BF16
+    assert rel_err(to_np(state), href) <= BF16
+    full, _ = _gpu(inp)
+    assert rel_err(to_np(dec), to_np(full[:, L0:])) <= BF16
+
+
+def test_ssd_step_mamba2_2p7b_decode_sampled_heads():
+    """A 2.7B-shaped decode batch (64 × 80 heads × 64 × 128 state): heads 0, 41, 79 against the oracle."""
+    shape = W.SsdShape("decode", 64, 1, 80, 64, 1, 128, torch.bfloat16)
+    inp = W.ssd_inputs(shape, device=DEV, seed=3)
+    g = torch.Generator(device=DEV).manual_seed(4)
+    state = torch.randn((64, 80, 64, 128), generator=g, device=DEV)
+    state0 = state.clone()
+    tok = _step_inputs(inp, 0)
+    y = ssm.ssd_step(state, tok["x"], tok["dt"], inp["A"], tok["B"], tok["C"], D=inp["D"], z=tok["z"],
+                     dt_bias=inp["dt_bias"])
+    torch.cuda.synchronize()
+    for h in (0, 41, 79):
+        sub = {k: (None if v is None else v[..., h:h + 1] if k in ("A", "D", "dt_bias", "dt") else v)
+               for k, v in inp.items()}
+        sub["x"] = inp["x"][:, :, h:h + 1]
+        sub["z"] = inp["z"][:, :, h:h + 1]
+        ref, href = _oracle(sub, state0[:, h:h + 1])
+        assert rel_err(to_np(y[:, h:h + 1]), ref[:, 0]) <= BF16, h
+        assert rel_err(to_np(state[:, h:h + 1]), href) <= 1e-5, h
