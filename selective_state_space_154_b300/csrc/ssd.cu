@@ -646,6 +646,19 @@ __global__ void __launch_bounds__(256, 3) ssd_step_kernel(const SsdStepArgs p) {
   const int64_t bh = blockIdx.x;  // b * H + h
   const int64_t b = bh / p.H, h = bh % p.H, g = h / (p.H / p.G);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float4* st = reinterpret_cast<float4*>(p.state + bh * p.P * kSsdState) + lane;
+  const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(p.x) + bh * p.P;
+  // the first rows' states are requested before the per-head scalars are computed
+  float4 s[kStepRowsPerIter];
+  float xv[kStepRowsPerIter];
+#pragma unroll
+  for (int k = 0; k < kStepRowsPerIter; ++k) {
+    const int64_t row = warp + 8 * k;
+    if (row < p.P) {
+      s[k] = st[row * (kSsdState / 4)];
+      xv[k] = __bfloat162float(xr[row]);
+    }
+  }
   const __nv_bfloat16* bf_dt = static_cast<const __nv_bfloat16*>(p.dt);
   const float a = p.A[h];
   const float d = softplus_precise(__bfloat162float(bf_dt[bh]) + (p.dt_bias ? p.dt_bias[h] : 0.f));
@@ -659,19 +672,17 @@ __global__ void __launch_bounds__(256, 3) ssd_step_kernel(const SsdStepArgs p) {
                        __uint_as_float(bw.y & 0xffff0000u)};
   const float Cv[4] = {__uint_as_float(cw.x << 16), __uint_as_float(cw.x & 0xffff0000u), __uint_as_float(cw.y << 16),
                        __uint_as_float(cw.y & 0xffff0000u)};
-  const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(p.x) + bh * p.P;
   const __nv_bfloat16* zr = p.z ? static_cast<const __nv_bfloat16*>(p.z) + bh * p.P : nullptr;
   __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + bh * p.P;
-  float4* st = reinterpret_cast<float4*>(p.state + bh * p.P * kSsdState) + lane;
   for (int64_t base = warp; base < p.P; base += 8 * kStepRowsPerIter) {
-    float4 s[kStepRowsPerIter];
-    float xv[kStepRowsPerIter];
+    if (base != warp) {
 #pragma unroll
-    for (int k = 0; k < kStepRowsPerIter; ++k) {
-      const int64_t row = base + 8 * k;
-      if (row < p.P) {
-        s[k] = st[row * (kSsdState / 4)];
-        xv[k] = __bfloat162float(xr[row]);
+      for (int k = 0; k < kStepRowsPerIter; ++k) {
+        const int64_t row = base + 8 * k;
+        if (row < p.P) {
+          s[k] = st[row * (kSsdState / 4)];
+          xv[k] = __bfloat162float(xr[row]);
+        }
       }
     }
 #pragma unroll
