@@ -38,15 +38,35 @@ import workloads as W  # noqa: E402
 METRIC = "scan GB/s & channel·tokens/s (fraction of HBM roofline); ssm_step tokens/s"
 WORKLOAD = "long_1m"
 HBM_PEAK_FALLBACK = 6400.0
-FP32_LANES_PER_SM = 128
 # FP32 lane operations of one state update (b, c, t, n) on the minimal path:
 # Δ·A, Ā-1, x·(1/A), (x/A)·B + h, (Ā-1)·s + h, C·h accumulate (the exp is on the MUFU pipe).
 FP32_OPS_PER_UPDATE = 6
-# ncu DRAM bytes (read + write) per launch of the scan kernel on this workload,
-# from a capture of the current kernel at full size (13.52 GB read + 4.45 GB
-# written; profiles/scan_rows_kernel_long_1m_dram.md).  Set back to None when
-# the kernel changes until it is captured again.
-SCAN_DRAM_BYTES_PER_LAUNCH = 17.97e9
+SCAN_PROFILE = os.path.join(ROOT, "profiles", "scan_stream_kernel_long_seq.md")
+SCAN_KERNEL_SRC = os.path.join(ROOT, "selective_state_space_154_b300", "csrc", "scan_stream.cu")
+
+
+def source_digest(path):
+    import hashlib
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def scan_traffic_per_launch():
+    """DRAM bytes (read + write) per launch of the scan kernel on the 1M-token workload,
+    from the committed ncu summary of the kernel, or None when the summary was taken
+    on another version of the kernel source (its digest is recorded beside the figure)."""
+    import re
+    try:
+        text = open(SCAN_PROFILE).read()
+    except OSError:
+        return None, "no committed capture"
+    m = re.search(r"traffic_per_launch_bytes:\s*([0-9.eE+]+)", text)
+    d = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+    if not m or not d:
+        return None, "capture summary lacks the figure or the source digest"
+    if d.group(1) != source_digest(SCAN_KERNEL_SRC):
+        return None, "kernel changed since the capture"
+    return float(m.group(1)), f"ncu capture summarised in profiles/{os.path.basename(SCAN_PROFILE)}"
 
 
 def measured_peaks():
@@ -125,11 +145,11 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        import tempfile
+        self.path = os.path.join(tempfile.gettempdir(), f"ssm_bench_clocks_{os.getpid()}_{gpu_index}.csv")
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
@@ -575,23 +595,41 @@ def _oracle_call(args_list, threads):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(target_s=15.0):
-    """The oracle as it stands, on all host cores, over a bounded sample of the
-    workload: one full-length channel per thread, scanned repeatedly until about
-    target_s of work has been timed (the host memory stays at a few hundred MB)."""
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(target_s=12.0, rows=128):
+    """The oracle as it stands on the host cores: a seeded subset of `rows` channels of
+    the workload at full length, threaded over channels on every core, repeated until
+    about target_s of work has been timed; and one full-length channel on one core."""
     shape = W.SCAN_SHAPES[WORKLOAD]
     threads = cpu_threads()
-    length, rows = shape.seqlen, threads
+    length = shape.seqlen
     sample = make_oracle_rows(shape, rows, length, seed=1)
     total, calls = 0.0, 0
-    while total < target_s and calls < 1000:
+    while total < target_s and calls < 100:
         total += _oracle_call(sample, threads)
         calls += 1
+    u, delta, A, B, C, D, z, bias = sample
+    cut = lambda a, sl: None if a is None else a[sl]
+    one = [u[:, :1], delta[:, :1], A[:1], B, C, cut(D, slice(0, 1)), cut(z, (slice(None), slice(0, 1))),
+           cut(bias, slice(0, 1))]
+    single = _oracle_call(one, 1)
     return {"value": rows * length * calls / total, "unit": "channel·tokens/s", "cores": threads, "kind": "oracle",
-            "seconds": total,
-            "sample": f"{rows} channels x {length} tokens of the {WORKLOAD} workload (d_state {shape.d_state}, "
-                      f"bf16-rounded inputs, float64 arithmetic), oracle.scan threaded over channels, "
-                      f"run {calls} times"}
+            "cpu_model": cpu_model(), "seconds": total,
+            "single_core": {"value": length / single, "unit": "channel·tokens/s",
+                            "sample": f"1 channel x {length} tokens on 1 thread"},
+            "sample": f"seeded subset of {rows} channels x {length} tokens (full length) of the {WORKLOAD} workload "
+                      f"(d_state {shape.d_state}, bf16-rounded inputs, float64 arithmetic), oracle.scan threaded "
+                      f"over channels on {threads} threads, run {calls} times"}
 
 
 # ---------------------------------------------------------------- arms
@@ -610,8 +648,11 @@ def run_ours(args):
     gbs = alg / (secs / args.steps) / 1e9
     sm_mhz = clocks.get("sm_mhz") or peaks.get("sm_max_mhz", 2032.0)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    alu_peak = sms * FP32_LANES_PER_SM * sm_mhz * 1e6 / 1e12
+    rates = probe_pipe_rates(threads_list=(512,)) if rank == 0 else None
+    fp32_lanes = rates["ffma2 (packed f32x2)"]["512"] if rates else 128.0
+    alu_peak = sms * fp32_lanes * sm_mhz * 1e6 / 1e12
     alu_achieved = FP32_OPS_PER_UPDATE * ct * shape.d_state / (secs / args.steps) / 1e12
+    traffic, traffic_note = scan_traffic_per_launch()
     hbm_peak = peaks.get("hbm_gbs")
     hbm_note = "of measured" if hbm_peak else "of fallback"
     hbm_peak = hbm_peak or HBM_PEAK_FALLBACK
@@ -639,12 +680,20 @@ def run_ours(args):
                        "parallelism": "one independent problem per GPU, no collective" if world > 1 else "single GPU",
                        "l2": "inputs 17.2 GB > 126 MB L2 (no flush needed)"},
             "gbs": gbs,
-            "roofline": {"bound": "alu", "achieved": alu_achieved, "peak": alu_peak, "unit": "FP32 Tops/s",
-                         "frac": alu_achieved / alu_peak, "traffic": SCAN_DRAM_BYTES_PER_LAUNCH,
-                         "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x {sm_mhz:.0f} MHz (median SM clock sampled during the timed region)",
-                         "achieved_basis": f"{FP32_OPS_PER_UPDATE} FP32 ops per state update x {ct * shape.d_state} updates per launch",
-                         "hbm": {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
-                                 "peak_note": hbm_note, "alg_bytes_per_launch": alg}},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                         "traffic": traffic, "peak_note": hbm_note + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+                         "achieved_basis": f"algorithmic bytes {alg} per launch (u, delta, z read and out written once "
+                                           "per channel-token; B, C once per token; final state, A, D, bias once) / "
+                                           "CUDA-event time per launch",
+                         "traffic_note": traffic_note,
+                         "alu": {"achieved": alu_achieved, "peak": alu_peak, "unit": "FP32 Tops/s",
+                                 "frac": alu_achieved / alu_peak,
+                                 "achieved_basis": f"{FP32_OPS_PER_UPDATE} FP32 lane operations per state update x "
+                                                   f"{ct * shape.d_state} updates per launch",
+                                 "peak_basis": f"{sms} SMs x {fp32_lanes:.1f} FP32 lane-ops per SM-clock (measured "
+                                               f"now by the pipe-rate probe, packed FFMA2) x {sm_mhz:.0f} MHz (median SM "
+                                               "clock sampled during the timed region)",
+                                 "pipe_rates": rates}},
             "e2e": {"value": world * ct * e2e_steps / e2e_secs, "unit": "channel·tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "note": "public API: pinned host -> device copies of u, delta, z, B, C, ssm_scan_fwd, out -> pinned host; wall clock"},
@@ -731,6 +780,56 @@ def run_profile_case(args):
     print(f"{args.only}: {secs / args.steps * 1e3:.4f} ms per call, {units * args.steps / secs:.4e} units/s")
 
 
+PROBE_VARIANTS = {0: ("ffma", "FP32 lane-ops"), 1: ("ffma2 (packed f32x2)", "FP32 lane-ops"),
+                  2: ("mufu ex2", "ex2"), 3: ("scan state update, packed", "state updates"),
+                  4: ("scan state update, scalar", "state updates"), 5: ("alu prmt+lop3", "ALU lane-ops"),
+                  6: ("12 ffma2 + 4 ex2 chains", "rounds (12 ffma2 + 4 ex2 each)"),
+                  7: ("6 ffma2 + 4 ex2 chains", "rounds (6 ffma2 + 4 ex2 each)"),
+                  8: ("scan state update, packed, ex2 replaced by fmul", "state updates"),
+                  9: ("scan token, 1 thread/row, 8 tokens unrolled", "state updates"),
+                  10: ("scan token, 1 thread/row, 4 tokens unrolled", "state updates"),
+                  11: ("scan token, 2 threads/row, 8 tokens unrolled", "state updates"),
+                  12: ("scan token, 1 thread/row, ex2 one token ahead", "state updates"),
+                  13: ("scan token, 1 thread/row, ex2 one token ahead, unrolled x2", "state updates")}
+
+
+PROBE_THREADS = {3: (512, 640), 4: (512,), 8: (512,), 9: (512, 640), 10: (512, 640), 11: (512, 768, 1024),
+                 12: (512, 640), 13: (512,)}
+
+
+def probe_pipe_rates(threads_list=(512, 1024)):
+    """Per-SM throughput of the arithmetic pipes, from the probe library: one CTA per
+    SM, register-resident independent chains, each CTA timed by the SM clock counter.
+    Returns {variant: {threads: work per SM-clock (median over CTAs)}}."""
+    import ctypes
+    from selective_state_space_154_b300 import build as ssm_build
+    lib = ctypes.CDLL(ssm_build.build_probe())
+    fn = lib.ssm_probe_pipe_rates
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                   ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_double)]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    res = {}
+    for v, (name, unit) in PROBE_VARIANTS.items():
+        res[name] = {"unit": f"{unit} per SM per clock"}
+        for threads in (PROBE_THREADS.get(v, threads_list) if len(threads_list) > 1 else threads_list):
+            iters = 2000 if v not in PROBE_THREADS else 400
+            cyc = (ctypes.c_longlong * sms)()
+            work = ctypes.c_double()
+            for _ in range(2):  # the first run warms up
+                rc = fn(v, sms, threads, iters, cyc, ctypes.byref(work))
+                if rc != 0:
+                    raise RuntimeError(f"probe {name}: CUDA error {rc}")
+            per_sm = sorted(work.value * threads / c for c in cyc)
+            res[name][str(threads)] = per_sm[len(per_sm) // 2]
+    return res
+
+
+def run_peaks(args):
+    res = probe_pipe_rates()
+    print(json.dumps({"pipe_rates": res}, indent=1), flush=True)
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -769,7 +868,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--only", choices=["all", "scan", "decode", "conv", "bwd", "ssd"], default="all",
+    ap.add_argument("--only", choices=["all", "scan", "decode", "conv", "bwd", "ssd", "peaks"], default="all",
                     help="profiling aid: run only the scan, the decode step, the Conv1D or the backward (no JSON line)")
     ap.add_argument("--seqlen", type=int, default=None,
                     help="profiling aid: scan another sequence length of the same workload")
@@ -781,6 +880,8 @@ def main(argv=None):
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.only == "peaks":
+        run_peaks(args)
     elif args.only != "all":
         run_profile_case(args)
     else:

@@ -23,7 +23,11 @@
  *
  * Conventions for every call:
  *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
- *    keeps no global state, allocates nothing and never frees caller memory.
+ *    allocates nothing and never frees caller memory.  Its only global state:
+ *    the decode step's device error word (read and cleared by ssm_step_check),
+ *    the static scratch array of ssm_scan_fwd_noalloc with its cached device
+ *    address, and the test hooks read from the environment (see the end of
+ *    this header).  Every other call works only on the memory it is given.
  *  - Layouts are dense row-major:
  *        u, delta, z, out          [batch][d_inner][seqlen]   (act dtype)
  *        B, C                      [batch][seqlen][d_state]   (act dtype)
@@ -40,7 +44,13 @@
  *  - Inputs are never written.  out must not overlap any input.
  *  - NaN / Inf inputs are not checked and propagate.
  *  - Limits: 1 ≤ d_state ≤ 64; batch, d_inner, seqlen ≥ 1;
- *    batch·d_inner·seqlen < 2^62.  Pointers must be 16-byte aligned.
+ *    batch·d_inner·seqlen < 2^62.
+ *  - Alignment: every pointer must be aligned to its element (2 bytes for bf16,
+ *    4 for float32 arrays), else SSM_ERR_ALIGNMENT.  16-byte alignment of u,
+ *    delta, z, B, C and out, with rows whose byte length is a multiple of 16,
+ *    selects the vectorised kernels (for bf16 with d_state 16 and seqlen a
+ *    multiple of 8, the tensor-copy kernel); other inputs take element copies.
+ *    The Mamba-2 calls below state their own, stricter, alignment.
  */
 #ifndef SSM_SCAN_H_
 #define SSM_SCAN_H_
@@ -124,6 +134,35 @@ SSM_API ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, con
                                    const float* initial_state, void* out, float* final_state,
                                    const ssm_dims* dims, void* workspace, size_t workspace_bytes,
                                    ssm_stream_t stream);
+
+/*
+ * ssm_scan_fwd for a sequence held in HOST memory, the copies to and from the
+ * device overlapped with the scan: the sequence is cut into pieces of piece_len
+ * tokens; each piece's u, delta, z, B and C are copied to device staging memory on
+ * h2d_stream, scanned on `stream` from the state the previous piece left
+ * (initial_state, or 0, for the first), and its output copied back on d2h_stream.
+ * Two staging slots alternate, so one piece's copies run while another is scanned.
+ * Scanning in pieces equals one scan of the whole sequence (the state carries
+ * across, as for ssm_scan_fwd_from_state).
+ *   u, delta, z, out: [batch][d_inner][seqlen] and B, C: [batch][seqlen][d_state]
+ *     in HOST memory (page-locked for the copies to overlap); z may be NULL.
+ *   A, D, delta_bias, initial_state (NULL: h = 0), final_state (NULL: not
+ *     written): DEVICE memory, as for ssm_scan_fwd_from_state.
+ *   staging: device memory of ssm_scan_fwd_host_staging_bytes(dims, piece_len)
+ *     bytes, 256-byte aligned, caller-owned; its first bytes are the pieces' scan
+ *     workspace, so ssm_scan_check(staging, bytes) reports their device-side waits.
+ *   stream, h2d_stream, d2h_stream: may be the same stream (then nothing overlaps).
+ *     The call returns once everything is queued; `stream` is made to wait for the
+ *     last output copy, so synchronising `stream` completes the call.
+ * Errors: as for ssm_scan_fwd, plus SSM_ERR_INVALID_ARG for piece_len < 1 and
+ * SSM_ERR_WORKSPACE for missing or small staging memory.
+ */
+SSM_API size_t ssm_scan_fwd_host_staging_bytes(const ssm_dims* dims, int64_t piece_len);
+SSM_API ssm_status ssm_scan_fwd_host(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                                     const float* D, const void* z, const float* delta_bias,
+                                     const float* initial_state, void* out, float* final_state,
+                                     const ssm_dims* dims, int64_t piece_len, void* staging, size_t staging_bytes,
+                                     ssm_stream_t stream, ssm_stream_t h2d_stream, ssm_stream_t d2h_stream);
 
 /*
  * Backward of ssm_scan_fwd (from h = 0): the gradients of ℓ = Σ dout·out with
@@ -224,6 +263,13 @@ SSM_API ssm_status ssm_step_check(ssm_stream_t stream);
 SSM_API const char* ssm_status_string(ssm_status s);
 
 /*
+ * The error behind the calling thread's most recent SSM_ERR_CUDA: the CUDA
+ * runtime's cudaError_t code, or 10000 + the driver's CUresult when a driver
+ * call failed (the encoding of a tensor-copy descriptor).  0 if none occurred.
+ */
+SSM_API int ssm_last_cuda_error(void);
+
+/*
  * ssm_scan_fwd for callers that cannot allocate device memory: a plug-in whose
  * host framework owns every allocation, a serving loop that may not call
  * cudaMalloc after start-up, or any caller with a fixed device-memory budget.
@@ -238,8 +284,10 @@ SSM_API const char* ssm_status_string(ssm_status s);
  *  - Returns SSM_ERR_WORKSPACE when ssm_scan_workspace_bytes(dims) exceeds
  *    SSM_NOALLOC_SCRATCH_BYTES; use ssm_scan_fwd with your own workspace then.
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) and caches it; make that first call before any
- *    stream capture.
+ *    (cudaGetSymbolAddress) and caches it with the id of the current context;
+ *    make that first call before any stream capture.  After cudaDeviceReset, or
+ *    under another context on the same device, the next call looks the address
+ *    up again (that call, too, must not be captured).
  *  - All calls share the one array, and each call resets what must start at
  *    zero.  Calls whose work overlaps on the GPU (concurrent streams, or other
  *    threads) race on the array: serialise them.
@@ -248,6 +296,8 @@ SSM_API const char* ssm_status_string(ssm_status s);
  *    use ssm_scan_fwd.
  */
 #define SSM_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+/* SSM_NOALLOC_SCRATCH_BYTES as built into this library (for callers without the header). */
+SSM_API size_t ssm_noalloc_scratch_bytes(void);
 SSM_API ssm_status ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* A, const void* B,
                                 const void* C, const float* D, const void* z, const float* delta_bias,
                                 void* out, float* final_state, const ssm_dims* dims, ssm_stream_t stream);
@@ -315,6 +365,26 @@ SSM_API ssm_status ssd_scan_fwd(const void* x, const void* dt, const float* A, c
 SSM_API ssm_status ssd_step(float* state, const void* x, const void* dt, const float* A, const void* B,
                             const void* C, const float* D, const void* z, const float* dt_bias, void* out,
                             const ssd_dims* dims, ssm_stream_t stream);
+
+/*
+ * Test hooks.  The library reads these environment variables once, at the first
+ * call that needs them, and again only inside ssm_test_hooks_reload(); no other
+ * call reads the environment.  They exist for the test suite (forcing a kernel,
+ * a chunk count, or a device-side wait that never completes) and are not part of
+ * the supported interface:
+ *   SSM_FORCE_KERNEL = tiles | rows | stream   scan kernel, where the shape allows it
+ *   SSM_FORCE_CHUNKS = n        sequence chunks of the scan
+ *   SSM_FORCE_TPR = 2           two threads per row in the row kernel
+ *   SSM_CTAS_PER_SM = n         resident CTAs per SM assumed by the row kernel's planner
+ *   SSM_STREAM_ROWS = 512 | 128 rows per CTA of the streamed row kernel
+ *   SSM_STREAM_TOKENS = 8       8-token pipeline stages in the streamed row kernel (default 16)
+ *   SSM_BWD_CHUNKS = n          sequence chunks of ssm_scan_bwd
+ *   SSM_FORCE_STEP = plain      the generic decode-step kernel only
+ *   SSM_FAULT = lookback | step | ssd   the named device-side wait never completes
+ *                               (the call reports SSM_ERR_TIMEOUT; nothing faults)
+ *   SSM_LOOKBACK_TIMEOUT_MS = n limit of the device-side waits
+ */
+SSM_API void ssm_test_hooks_reload(void);
 
 #ifdef __cplusplus
 }

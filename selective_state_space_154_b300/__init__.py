@@ -21,6 +21,7 @@ __all__ = [
     "ssm_status_string", "scan_fwd", "step", "library_path", "load_library", "ssm_scan_fwd_noalloc",
     "SSM_NOALLOC_SCRATCH_BYTES", "ssm_step_check", "ssm_scan_fwd_from_state",
     "ssm_conv1d_fwd", "ssm_conv1d_step", "conv1d", "conv1d_step",
+    "ssm_scan_fwd_host", "ssm_scan_fwd_host_staging_bytes", "reload_test_hooks",
     "ssm_scan_bwd_workspace_bytes", "ssm_scan_bwd", "scan_bwd",
     "ssd_scan_workspace_bytes", "ssd_scan_fwd", "ssd_scan", "ssd_step",
 ]
@@ -31,14 +32,22 @@ _LIB_PATH = os.path.join(_PKG, "_lib", "libssm_b300.so")
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_ALIGNMENT, SSM_ERR_WORKSPACE, \
     SSM_ERR_CUDA, SSM_ERR_TIMEOUT = range(7)
 SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
-SSM_NOALLOC_SCRATCH_BYTES = 8 << 20  # size of the library's static scratch (include/ssm_scan.h)
+def __getattr__(name):
+    # SSM_NOALLOC_SCRATCH_BYTES: the size of the library's static scratch, read from the library
+    if name == "SSM_NOALLOC_SCRATCH_BYTES":
+        return int(load_library().ssm_noalloc_scratch_bytes())
+    raise AttributeError(name)
 _DTYPES = {torch.float32: SSM_DTYPE_F32, torch.bfloat16: SSM_DTYPE_BF16}
 
 
 class SsmError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {ssm_status_string(status)}")
+        msg = f"{where}: {ssm_status_string(status)}"
+        if status == SSM_ERR_CUDA:
+            code = int(load_library().ssm_last_cuda_error())
+            msg += (f" (driver error {code - 10000})" if code >= 10000 else f" (CUDA error {code})")
+        super().__init__(msg)
 
 
 class ssm_dims(ctypes.Structure):
@@ -102,12 +111,28 @@ def load_library():
             lib.ssd_step.restype = i32
             lib.ssm_status_string.argtypes = [i32]
             lib.ssm_status_string.restype = ctypes.c_char_p
+            lib.ssm_test_hooks_reload.argtypes = []
+            lib.ssm_test_hooks_reload.restype = None
+            lib.ssm_scan_fwd_host_staging_bytes.argtypes = [dp, ctypes.c_int64]
+            lib.ssm_scan_fwd_host_staging_bytes.restype = sz
+            lib.ssm_scan_fwd_host.argtypes = [vp] * 11 + [dp, ctypes.c_int64, vp, sz, vp, vp, vp]
+            lib.ssm_scan_fwd_host.restype = i32
+            lib.ssm_last_cuda_error.argtypes = []
+            lib.ssm_last_cuda_error.restype = i32
+            lib.ssm_noalloc_scratch_bytes.argtypes = []
+            lib.ssm_noalloc_scratch_bytes.restype = sz
             _lib = lib
     return _lib
 
 
 def ssm_status_string(status: int) -> str:
     return load_library().ssm_status_string(int(status)).decode()
+
+
+def reload_test_hooks() -> None:
+    """Make the library read its SSM_* test-hook environment variables again (it reads
+    them once otherwise)."""
+    load_library().ssm_test_hooks_reload()
 
 
 def _ptr(t):
@@ -190,6 +215,55 @@ def ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, out, final_state, workspac
     if st != SSM_OK:
         raise SsmError(st, "ssm_scan_fwd" if initial_state is None else "ssm_scan_fwd_from_state")
     return workspace
+
+
+def ssm_scan_fwd_host_staging_bytes(batch, d_inner, d_state, seqlen, piece_len, dtype=torch.bfloat16) -> int:
+    d = _dims(batch, d_inner, d_state, seqlen, dtype)
+    return int(load_library().ssm_scan_fwd_host_staging_bytes(ctypes.byref(d), int(piece_len)))
+
+
+def ssm_scan_fwd_host(u, delta, A, B, C, D, z, delta_bias, out, final_state=None, initial_state=None,
+                      piece_len=1 << 16, staging=None, stream=None, h2d_stream=None, d2h_stream=None):
+    """ssm_scan_fwd over host tensors (u, delta, z, B, C, out; page-locked for overlap),
+    A, D, delta_bias, initial_state and final_state on the device: the C call pipelines
+    the copies with the scan in pieces of ``piece_len`` tokens.  Allocates the device
+    staging memory when it is not given.  Returns the staging tensor."""
+    lib = load_library()
+    if not isinstance(u, torch.Tensor) or u.dim() != 3:
+        raise ValueError("u must be a [batch, d_inner, seqlen] tensor")
+    batch, d_inner, L = u.shape
+    if not isinstance(A, torch.Tensor) or A.dim() != 2:
+        raise ValueError("A must be a [d_inner, d_state] tensor")
+    N = A.shape[1]
+    act, dev, host = u.dtype, A.device, torch.device("cpu")
+    if dev.type != "cuda":
+        raise ValueError("A must be on a CUDA device")
+    _check(u, "u", act, (batch, d_inner, L), host)
+    _check(delta, "delta", act, (batch, d_inner, L), host)
+    _check(B, "B", act, (batch, L, N), host)
+    _check(C, "C", act, (batch, L, N), host)
+    _check(z, "z", act, (batch, d_inner, L), host, required=False)
+    _check(out, "out", act, (batch, d_inner, L), host)
+    _check(A, "A", torch.float32, (d_inner, N), dev)
+    _check(D, "D", torch.float32, (d_inner,), dev, required=False)
+    _check(delta_bias, "delta_bias", torch.float32, (d_inner,), dev, required=False)
+    _check(final_state, "final_state", torch.float32, (batch, d_inner, N), dev, required=False)
+    _check(initial_state, "initial_state", torch.float32, (batch, d_inner, N), dev, required=False)
+    dims = _dims(batch, d_inner, N, L, act)
+    with torch.cuda.device(dev):
+        need = int(lib.ssm_scan_fwd_host_staging_bytes(ctypes.byref(dims), int(piece_len)))
+        if staging is None:
+            staging = torch.empty(need, dtype=torch.uint8, device=dev)
+        sbytes = staging.numel() * staging.element_size()
+        main = _stream_handle(stream, dev)
+        h2d = main if h2d_stream is None else ctypes.c_void_p(h2d_stream.cuda_stream)
+        d2h = main if d2h_stream is None else ctypes.c_void_p(d2h_stream.cuda_stream)
+        st = lib.ssm_scan_fwd_host(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                   _ptr(delta_bias), _ptr(initial_state), _ptr(out), _ptr(final_state),
+                                   ctypes.byref(dims), int(piece_len), _ptr(staging), sbytes, main, h2d, d2h)
+    if st != SSM_OK:
+        raise SsmError(st, "ssm_scan_fwd_host")
+    return staging
 
 
 def ssm_scan_fwd_from_state(u, delta, A, B, C, D, z, delta_bias, initial_state, out, final_state,

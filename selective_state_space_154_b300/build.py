@@ -15,6 +15,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libssm_b300.so")
+# a separate throughput probe of the arithmetic pipes, loaded only by the benchmark
+PROBE_SRC = os.path.join(CSRC, "probe", "pipe_rates.cu")
+PROBE_PATH = os.path.join(LIB_DIR, "libssm_probe.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 
 NVCC_FLAGS = [
@@ -38,18 +41,34 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def build_probe(force: bool = False) -> str:
+    if not force and os.path.exists(PROBE_PATH) and os.path.getmtime(PROBE_PATH) > os.path.getmtime(PROBE_SRC):
+        return PROBE_PATH
+    os.makedirs(LIB_DIR, exist_ok=True)
+    tmp = PROBE_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call([NVCC, "-shared", *NVCC_FLAGS, PROBE_SRC, "-o", tmp,
+                           "-Xlinker", "-rpath,/usr/local/cuda/lib64"])
+    os.replace(tmp, PROBE_PATH)
+    return PROBE_PATH
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
+    build_probe(force)
     if not force and not _stale():
         return LIB_PATH
     os.makedirs(LIB_DIR, exist_ok=True)
-    objs = []
-    for src in sources():
+    from concurrent.futures import ThreadPoolExecutor
+
+    def compile_one(src):
         obj = os.path.join(LIB_DIR, os.path.basename(src) + ".o")
         cmd = [NVCC, *NVCC_FLAGS, "-I", INCLUDE, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         subprocess.check_call(cmd)
-        objs.append(obj)
+        return obj
+
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        objs = list(ex.map(compile_one, sources()))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     subprocess.check_call([NVCC, "-shared", *NVCC_FLAGS, *objs, "-o", tmp,
                            "-Xlinker", "-rpath,/usr/local/cuda/lib64"])

@@ -565,8 +565,40 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
     const int64_t row_slots = (int64_t)sms * 4 * kRowsPerRowCta;
     if (rows >= row_slots || a.L >= 65536 || rows * (a.L / kMinRowChunk) >= row_slots) kind = kScanRows;
   }
-  if (knobs.force_kind >= 0 && !(knobs.force_kind == kScanRows && a.N > 16)) kind = knobs.force_kind;
+  // The streamed row kernel (tensor-copied stages; bf16, 16 states, 16-byte aligned
+  // rows) is taken only when asked for: measured slower than the row kernel so far.
+  if (knobs.force_kind >= 0) {
+    const bool ok = knobs.force_kind == kScanTiles || (knobs.force_kind == kScanRows && a.N <= 16) ||
+                    (knobs.force_kind == kScanStream && stream_supported(a));
+    if (ok) kind = knobs.force_kind;
+  }
   pl.kind = kind;
+  if (kind == kScanStream) {
+    // CTAs of 512 rows (one per SM) over wide layers, else 128 (three per SM)
+    const int rb = knobs.stream_rows == 128 || (knobs.stream_rows != 512 && a.d_inner < 512) ? 128 : 512;
+    const int occ = rb == 512 ? 1 : 3;
+    pl.stage_tokens = knobs.stream_stage_tokens == 8 ? 8 : 16;
+    pl.npad = 16;
+    pl.groups = 1;
+    pl.threads = rb + 32;
+    pl.rows_per_cta = rb;
+    pl.ctiles = (int)((a.d_inner + rb - 1) / rb);
+    pl.smem_bytes = stream_smem_bytes_for(rb, pl.stage_tokens);
+    const int64_t items = a.batch * pl.ctiles;
+    const int64_t nch = pick_chunks(items, (int64_t)sms * occ, a.L, kMinRowChunk, pl.stage_tokens, knobs.force_chunks);
+    int64_t clen = (a.L + nch - 1) / nch;
+    clen = (clen + pl.stage_tokens - 1) / pl.stage_tokens * pl.stage_tokens;
+    pl.chunk_len = clen;
+    pl.nchunks = (int)((a.L + clen - 1) / clen);
+    size_t total = 0;
+    stream_ws_layout(nullptr, pl.nchunks, items, rb, &total);
+    pl.ws_flags_off = kWsHeaderBytes;
+    pl.ws_agg_off = 0;
+    // one chunk needs no workspace; a workspace given anyway receives the error word
+    pl.ws_bytes = pl.nchunks > 1 ? total : 0;
+    *plan = pl;
+    return true;
+  }
   if (kind == kScanRows) {
     // Long sequences over wide layers: one CTA per SM holding rows_big_cta_rows() rows,
     // so that chunks advance in lock-step and the carry between them resolves at once.
@@ -616,6 +648,7 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
 
 cudaError_t scan_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream) {
   if (plan.kind == kScanRows) return scan_rows_launch(a, plan, stream);
+  if (plan.kind == kScanStream) return scan_stream_launch(a, plan, stream);
   KParams p{};
   p.a = a;
   p.npad = plan.npad;

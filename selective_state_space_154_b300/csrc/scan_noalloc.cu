@@ -6,7 +6,11 @@
 // is loaded on each device and kept until the process exits.  Host code cannot
 // use the array's name as a device address (it names a host-side shadow), so the
 // first call on each device looks up the real address with
-// cudaGetSymbolAddress while that device is current, and caches it.
+// cudaGetSymbolAddress while that device is current, and caches it together with
+// the id of the context it belongs to; a call in another context (after a device
+// reset, say) looks it up again.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "ssm_internal.h"
@@ -17,23 +21,57 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SSM_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchEntry {
+  unsigned long long ctx_id;  // the context the address belongs to (0: none yet)
+  void* ptr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
-// Device address of g_noalloc_scratch on the current device (nullptr on failure).
+// Unique id of the current context (0 if none is current or the driver cannot say).
+// A device reset, or another context made current on the same device, changes it,
+// and with it the device address of g_noalloc_scratch.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_noalloc_scratch in the current context (nullptr on failure),
+// looked up with that device current on the first call in each context and cached.
 void* scratch_address() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = ptr;
-  }
-  return g_scratch_ptr[dev];
+  unsigned long long id = current_context_id();
+  if (id != 0 && g_scratch[dev].ctx_id == id && g_scratch[dev].ptr) return g_scratch[dev].ptr;
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+  id = current_context_id();  // the lookup above made the device's context current if none was
+  g_scratch[dev] = ScratchEntry{id, ptr};
+  return ptr;
 }
 
 }  // namespace
+
+extern "C" size_t ssm_noalloc_scratch_bytes(void) { return SSM_NOALLOC_SCRATCH_BYTES; }
 
 extern "C" ssm_status ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* A, const void* B,
                                            const void* C, const float* D, const void* z, const float* delta_bias,

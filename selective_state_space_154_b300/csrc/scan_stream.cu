@@ -1,0 +1,676 @@
+// Selective-scan forward, bf16 activations, d_state 16: the streamed row kernel (sm_103a).
+//
+// The operation is the one of scan_fwd.cu ("State Space Models（SSM）とMamba" §2.2 離散化;
+// "Mambaとは？Transformer以外の系列モデル", sections 状態空間モデルを一つの式から理解する
+// and Mamba blockのarchitecture).  Organisation:
+//  * one thread per (batch, channel) row holds the row's 16 states, A and 1/A in
+//    registers; the readout Σ_n C_n h_n needs no other thread;
+//  * a CTA owns RB rows of one batch over one chunk of the sequence.  One producer
+//    warp streams the chunk through shared memory in stages of TS = 32 (or 16) tokens
+//    with tensor (TMA) copies: per stage an [RB rows × 2·TS bytes] tile of each of u,
+//    Δraw and z (swizzled, so that lanes reading 8 bytes of their own rows are
+//    conflict-free) and the [TS tokens × 16] tiles of B and C, which it converts to
+//    fp32 once for all rows.  Completion is counted in bytes on a "full" mbarrier per
+//    stage; each consumer warp releases a stage on an "empty" mbarrier.  Consumer
+//    warps never wait for one another;
+//  * the step size enters the exponent in base 2: Δ' = log2(1 + 2^{(Δraw+bias)·log2 e})
+//    = Δ / ln 2, so Ā_n = 2^{Δ'·A_n} with no further scaling, and Σ Δ' is the chunk's
+//    decay exponent;
+//  * chunks compose as affine maps, (A₂,b₂)∘(A₁,b₁) = (A₂A₁, A₂b₁+b₂) ("Mambaとは？…",
+//    Selective Scanは選択機構そのものではない).  Every chunk first scans from h = 0
+//    keeping S = ΣΔ', then each warp publishes (S, h_local) for its 32 rows and
+//    combines those of all preceding chunks, in a fixed order, into its carried-in
+//    state h_in; its end state is 2^{A S}·h_in + h_local.  The chunk's first blocks, those whose
+//    outputs h_in still changes (2^{A_n S} ≥ 2^-12 for the slowest-decaying state, bf16
+//    outputs), are not written by the first pass: a second pass scans them again from
+//    h_in and writes them, so every output is rounded once.  The number of stages the
+//    second pass needs is known from the first pass, so the producer streams them
+//    while the consumers look back.
+#include "async_copy.cuh"
+#include "ssm_device.cuh"
+#include "ssm_internal.h"
+
+#include <mutex>
+
+namespace ssm {
+
+namespace {
+thread_local int g_driver_error = 0;  // CUresult of this thread's last failed driver call
+}  // namespace
+
+int take_driver_error() {
+  const int e = g_driver_error;
+  g_driver_error = 0;
+  return e;
+}
+
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+  using Fn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*, const cuuint64_t*,
+                          const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                          CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(f);
+  });
+  if (!fn) {
+    g_driver_error = (int)CUDA_ERROR_NOT_FOUND;
+    return false;
+  }
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  const CUresult r = fn(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, s, b, e,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) g_driver_error = (int)r;
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+constexpr int NS = 16;        // states per row
+// rows per tensor copy of a row tile: the CTA's rows, at most 256 (the largest box)
+__host__ __device__ constexpr int box_rows(int rb) { return rb < 256 ? rb : 256; }
+
+// Stage geometry: TS tokens per stage, NSTG = 64 / TS stages in the ring (64 tokens
+// of every row in shared memory).  A stage's B and C are converted to fp32 kAhead
+// stages before its use.  TS = 16: 32-byte rows with the 32-byte swizzle; TS = 8:
+// 16-byte rows, no swizzle.
+template <int TS_>
+struct Geo {
+  static constexpr int NSTG = 64 / TS_;
+  static constexpr int kAhead = NSTG / 2;
+  static constexpr int kRowBytes = TS_ * 2;
+  // 16-byte granule g of row r of a swizzled tile: the TMA swizzle of R-byte rows
+  // XORs the granule bits of the address with the bits above bit 7, i.e. with
+  // (r · R / 128) mod (R / 16)
+  __device__ static __forceinline__ int swz(int r, int g) {
+    return g ^ ((r * kRowBytes / 128) & (kRowBytes / 16 - 1));
+  }
+};
+
+struct StreamParams {
+  CUtensorMap tm_u, tm_d, tm_z, tm_b, tm_c;
+  ScanArgs a;
+  int rtiles, nchunks;
+  int64_t chunk_len;
+  StreamWs ws;
+  long long timeout_ns;
+  int fault_lookback;
+};
+
+// Shared memory of one CTA (the dynamic allocation is aligned up to 1024 bytes).
+template <int RB, int TS>
+struct StreamSmem {
+  using G = Geo<TS>;
+  uint8_t tile[G::NSTG][3][RB * G::kRowBytes];  // [stage][u|Δraw|z][row][TS tokens], swizzled
+  uint16_t bc_raw[G::NSTG][2][TS * NS];         // [stage][B|C][token][state] bf16
+  float bcf[G::NSTG][TS][2 * NS];               // [stage][token][B 0..15 | C 0..15] fp32
+  uint64_t full[G::NSTG];  // the stage's tensor copies landed (bytes counted)
+  uint64_t conv[G::NSTG];  // every warp converted its share of the stage's B and C
+  uint64_t settled;        // every warp knows how far pass two must go
+  int done[G::NSTG];       // warps that released the stage's buffer
+  int n2;                  // stages of the second pass (max over warps)
+  int issued;              // stages issued so far (the last one + 1)
+  int ticket;              // this CTA's work item
+};
+template <int RB, int TS>
+constexpr size_t stream_smem_bytes() {
+  return sizeof(StreamSmem<RB, TS>) + 1024;
+}
+
+__device__ __forceinline__ float bf_lo(unsigned w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(unsigned w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ bool wait_flag(const unsigned* flag, unsigned want, long long timeout_ns,
+                                          unsigned* value) {
+  const unsigned long long start = ac::globaltimer();
+  unsigned ns = 32;
+  for (long long it = 0; it < (1ll << 28); ++it) {
+    const unsigned v = ld_acquire_gpu(flag);
+    if (v >= want) {
+      *value = v;
+      return true;
+    }
+    if ((long long)(ac::globaltimer() - start) > timeout_ns) break;
+    __nanosleep(ns);
+    ns = ns < 256 ? ns * 2 : ns;
+  }
+  return false;
+}
+
+enum StreamPass {
+  kAll = 0,        // the first chunk: every block written, S not needed
+  kSettled = 1,    // other chunks, pass one from h = 0: the settled blocks
+  kUnsettled = 2,  // other chunks, pass two from h_in: the rest
+};
+
+// Per-thread (row) constants.
+struct RowConst {
+  float a2[NS], ia[NS];  // A (the exponent base is 2: Ā = 2^{Δ' A}) and 1/A; 0 for A = 0
+  float a2max, Dc, bl2;  // slowest decay, D, bias · log2 e
+  bool precise;          // a row of this warp has an A = 0 state: the exact branch
+  bool row_ok;
+};
+
+// What every warp knows about the CTA's ring: its chunk's tokens and stage counts.
+// Stage k < n1 is pass one's stage k, stage n1 + i pass two's stage i (tokens from
+// the chunk start again).  The first min(NSTG, n1) stages of pass two are issued
+// before pass two's length is known (every chunk after the first re-scans at least
+// its first stage); the rest once it is.
+struct Ring {
+  const StreamParams* p;
+  unsigned long long deadline;
+  int c0, b, tc0, n1;
+  int spec_end;  // stages that may be issued without knowing pass two's length
+};
+
+// Issue the tensor copies of stage j (one thread).
+template <int RB, int TS, bool HAS_Z>
+__device__ __forceinline__ void ring_issue(StreamSmem<RB, TS>& sm, const Ring& g, int j) {
+  using G = Geo<TS>;
+  const int s = j % G::NSTG;
+  const int t0 = g.tc0 + (j < g.n1 ? j : j - g.n1) * TS;
+  const StreamParams& p = *g.p;
+  constexpr int ntens = HAS_Z ? 3 : 2;
+  const uint32_t fb = ac::smem_u32(&sm.full[s]);
+  ac::mbar_arrive_expect_tx(fb, (uint32_t)(ntens * RB * G::kRowBytes + 2 * TS * NS * 2));
+  ac::tma_load_3d(ac::smem_u32(sm.bc_raw[s][0]), &p.tm_b, 0, t0, g.b, fb);
+  ac::tma_load_3d(ac::smem_u32(sm.bc_raw[s][1]), &p.tm_c, 0, t0, g.b, fb);
+  const CUtensorMap* maps[3] = {&p.tm_u, &p.tm_d, &p.tm_z};
+  constexpr int kBox = box_rows(RB);
+#pragma unroll
+  for (int w = 0; w < ntens; ++w) {
+#pragma unroll
+    for (int hb = 0; hb < RB / kBox; ++hb)
+      ac::tma_load_3d(ac::smem_u32(sm.tile[s][w] + hb * kBox * G::kRowBytes), maps[w], t0, g.c0 + hb * kBox, g.b,
+                      fb);
+  }
+  atomicMax(&sm.issued, j + 1);
+}
+
+// This warp's share of stage j's B and C to fp32: [B|C][token][state] -> [token][B | C].
+template <int RB, int TS>
+__device__ __forceinline__ void ring_convert(StreamSmem<RB, TS>& sm, const Ring& g, int j, int warp, int lane,
+                                             int& err) {
+  using G = Geo<TS>;
+  constexpr int NW = RB / 32;
+  constexpr int kWords = TS * NS;       // 32-bit words of B and C together
+  constexpr int kShare = kWords / NW;   // words per warp
+  const int s = j % G::NSTG;
+  if (!ac::mbar_wait(ac::smem_u32(&sm.full[s]), (uint32_t)(j / G::NSTG) & 1u, g.deadline)) err = 1;
+  const unsigned* raw = reinterpret_cast<const unsigned*>(sm.bc_raw[s][0]);
+#pragma unroll
+  for (int q = 0; q < (kShare + 31) / 32; ++q) {
+    const int k = lane + 32 * q;
+    if (kShare % 32 == 0 || k < kShare) {
+      const int i = warp * kShare + k;  // word i: tensor i / (kWords / 2), token (i mod kWords/2) / 8, pair i mod 8
+      const unsigned wv = raw[i];
+      const int w = i / (kWords / 2), tok = (i % (kWords / 2)) / (NS / 2), np = i % (NS / 2);
+      *reinterpret_cast<float2*>(&sm.bcf[s][tok][w * NS + 2 * np]) = make_float2(bf_lo(wv), bf_hi(wv));
+    }
+  }
+  __syncwarp();
+  if (lane == 0) ac::mbar_arrive(ac::smem_u32(&sm.conv[s]));
+}
+
+// Whether stage j is ever issued: pass one, the first stages of pass two, or pass
+// two's remaining stages once its length n2 (< 0: unknown) is known.
+__device__ __forceinline__ bool ring_has(const Ring& g, int j, int n2) {
+  return j < g.spec_end || (n2 >= 0 && j < g.n1 + n2);
+}
+
+// After this warp finished stage k: release its buffer (the warp releasing it last
+// issues the copies of stage k + NSTG into it) and convert its share of stage k + kAhead.
+template <int RB, int TS, bool HAS_Z>
+__device__ __forceinline__ void ring_advance(StreamSmem<RB, TS>& sm, const Ring& g, int k, int n2, int warp, int lane,
+                                             int& err) {
+  using G = Geo<TS>;
+  constexpr int NW = RB / 32;
+  const int s = k % G::NSTG;
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence_block();  // this warp's reads of the buffer precede its release
+    if (atomicAdd(&sm.done[s], 1) == NW - 1) {
+      sm.done[s] = 0;
+      // stage k + NSTG > k ≥ n1 only once pass two runs, when n2 is known to every warp
+      if (ring_has(g, k + G::NSTG, n2)) ring_issue<RB, TS, HAS_Z>(sm, g, k + G::NSTG);
+    }
+  }
+  if (ring_has(g, k + G::kAhead, n2)) ring_convert<RB, TS>(sm, g, k + G::kAhead, warp, lane, err);
+}
+
+// One pass of a thread over ring stages [k0, k0 + nst), tokens from t_lo, writing the
+// 4-token groups that P selects.  h: the row's states; S: ΣΔ' since the chunk start
+// (P != kAll), with Kahan compensation `comp`.  In pass one (kSettled), lane 0
+// publishes the warp's stage count for pass two as soon as it is known.
+template <int RB, int TS, bool HAS_Z, int P, bool PRECISE>
+__device__ __forceinline__ void consume(StreamSmem<RB, TS>& sm, const Ring& g, const RowConst& c,
+                                        __nv_bfloat16* orow, int r, int warp, int lane, int k0, int nst, int t_lo,
+                                        int t_hi, int n2, float (&h)[NS], float& S, float& comp, int& err) {
+  using G = Geo<TS>;
+  constexpr float kStop = corr_stop_log2<__nv_bfloat16>();
+  const int t_valid = c.row_ok ? t_hi : t_lo;  // rows past d_inner compute nothing useful
+  bool published = P != kSettled;
+#pragma unroll 1
+  for (int kk = 0; kk < nst; ++kk) {
+    const int k = k0 + kk;
+    const int s = k % G::NSTG;
+    const uint32_t ph = (uint32_t)(k / G::NSTG) & 1u;
+    if (!ac::mbar_wait(ac::smem_u32(&sm.full[s]), ph, g.deadline)) err = 1;
+    if (!ac::mbar_wait(ac::smem_u32(&sm.conv[s]), ph, g.deadline)) err = 1;
+    const int ts = t_lo + kk * TS;
+    const uint2* tu = reinterpret_cast<const uint2*>(sm.tile[s][0] + r * G::kRowBytes);
+    const uint2* td = reinterpret_cast<const uint2*>(sm.tile[s][1] + r * G::kRowBytes);
+    const uint2* tz = reinterpret_cast<const uint2*>(sm.tile[s][2] + r * G::kRowBytes);
+#pragma unroll 1
+    for (int q4 = 0; q4 < TS / 4; ++q4) {
+      // four tokens per iteration: 8 bytes of each of u, Δraw, z (half a swizzled granule)
+      const int t = ts + q4 * 4;
+      const bool write_blk =
+          P == kAll || (P == kSettled ? !(c.a2max * S > kStop) : c.a2max * S > kStop - 1.f);
+      const int gi = G::swz(r, q4 >> 1) * 2 + (q4 & 1);  // 8-byte unit of the row
+      const uint2 wu = tu[gi], wd = td[gi];
+      uint2 wz = make_uint2(0u, 0u);
+      if (HAS_Z) wz = tz[gi];
+      const float* bcs = sm.bcf[s][q4 * 4];
+      unsigned packed0 = 0u, packed1 = 0u;
+      float Sb = 0.f;
+#pragma unroll
+      for (int v = 0; v < 4; v += 2) {
+        const unsigned uw = v ? wu.y : wu.x, dw = v ? wd.y : wd.x;
+        // Δ' = log2(1 + 2^{r log2 e}) for two tokens (r = Δraw + bias); r log2 e above 15 log2 e
+        const float2 rl = __ffma2_rn(make_float2(bf_lo(dw), bf_hi(dw)), make_float2(kLog2e, kLog2e),
+                                     make_float2(c.bl2, c.bl2));
+        const float2 q = __fadd2_rn(make_float2(ex2_approx(rl.x), ex2_approx(rl.y)), make_float2(1.f, 1.f));
+        float d0 = rl.x > 15.f * kLog2e ? rl.x : lg2_approx(q.x);
+        float d1 = rl.y > 15.f * kLog2e ? rl.y : lg2_approx(q.y);
+        d0 = t + v < t_valid ? d0 : 0.f;
+        d1 = t + v + 1 < t_valid ? d1 : 0.f;
+        float2 gz = make_float2(1.f, 1.f);
+        if (HAS_Z) {
+          const unsigned zw = v ? wz.y : wz.x;
+          const float2 zz = make_float2(bf_lo(zw), bf_hi(zw));
+          const float2 ez = __fmul2_rn(zz, make_float2(-kLog2e, -kLog2e));
+          const float2 dz = __fadd2_rn(make_float2(ex2_approx(ez.x), ex2_approx(ez.y)), make_float2(1.f, 1.f));
+          gz = __fmul2_rn(zz, make_float2(rcp_approx(dz.x), rcp_approx(dz.y)));
+        }
+        const float xs[2] = {bf_lo(uw), bf_hi(uw)};
+        const float ds[2] = {d0, d1};
+        float ys[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float dlt = ds[j], x = xs[j];
+          const float4* bc4 = reinterpret_cast<const float4*>(bcs + (v + j) * 2 * NS);
+          const float2 dd = make_float2(dlt, dlt), xx = make_float2(x, x);
+          // rows with an A = 0 state (PRECISE): Ā = 1, B̄ = Δ B exactly there (Δ = Δ' ln 2)
+          const float2 dx = PRECISE ? make_float2(dlt * kLn2 * x, dlt * kLn2 * x) : make_float2(0.f, 0.f);
+          float2 ya = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int qd = 0; qd < NS / 4; ++qd) {
+            const float4 bq = bc4[qd];
+            const float4 cq = bc4[NS / 4 + qd];
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+              const int n = 4 * qd + 2 * k2;
+              const float2 e = __fmul2_rn(dd, make_float2(c.a2[n], c.a2[n + 1]));
+              const float2 em = __fadd2_rn(make_float2(ex2_approx(e.x), ex2_approx(e.y)), make_float2(-1.f, -1.f));
+              const float2 xp = __fmul2_rn(xx, make_float2(c.ia[n], c.ia[n + 1]));
+              const float2 hb = make_float2(h[n], h[n + 1]);
+              const float2 bb = k2 ? make_float2(bq.z, bq.w) : make_float2(bq.x, bq.y);
+              const float2 cc = k2 ? make_float2(cq.z, cq.w) : make_float2(cq.x, cq.y);
+              float2 hn = __ffma2_rn(em, __ffma2_rn(xp, bb, hb), hb);
+              if (PRECISE) {
+                const float2 h0 = __ffma2_rn(dx, bb, hb);
+                hn.x = c.ia[n] != 0.f ? hn.x : h0.x;
+                hn.y = c.ia[n + 1] != 0.f ? hn.y : h0.y;
+              }
+              h[n] = hn.x;
+              h[n + 1] = hn.y;
+              ya = __ffma2_rn(cc, hn, ya);
+            }
+          }
+          ys[j] = fmaf(c.Dc, x, ya.x + ya.y);
+        }
+        const float2 yo = __fmul2_rn(make_float2(ys[0], ys[1]), gz);
+        __nv_bfloat162 p2 = __floats2bfloat162_rn(yo.x, yo.y);
+        const unsigned pw = *reinterpret_cast<unsigned*>(&p2);
+        packed0 = v ? packed0 : pw;
+        packed1 = v ? pw : packed1;
+        if (P != kAll) Sb += d0 + d1;
+      }
+      if (P != kAll) {  // S += Sb with Kahan compensation (S feeds 2^{A S} over long chunks)
+        const float yk = Sb - comp;
+        const float tk = S + yk;
+        comp = (tk - S) - yk;
+        S = tk;
+      }
+      if (c.row_ok && t < t_hi && write_blk) {
+        if (t + 4 <= t_hi) {
+          *reinterpret_cast<uint2*>(orow + t) = make_uint2(packed0, packed1);
+        } else {
+          unsigned short* o16 = reinterpret_cast<unsigned short*>(orow);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (t + i < t_hi) o16[t + i] = (unsigned short)((i < 2 ? packed0 : packed1) >> (16 * (i & 1)));
+        }
+      }
+    }
+    if (!published) {
+      // pass two must cover this stage unless every row of the warp is settled after it
+      const bool settled = !c.row_ok || !(c.a2max * S > kStop - 1.f);
+      if (__all_sync(0xffffffffu, settled)) {
+        published = true;
+        if (lane == 0) {
+          atomicMax(&sm.n2, kk + 1);
+          ac::mbar_arrive(ac::smem_u32(&sm.settled));
+        }
+      }
+    }
+    ring_advance<RB, TS, HAS_Z>(sm, g, k, n2, warp, lane, err);
+  }
+  if (!published && lane == 0) {  // never settled: pass two covers the whole chunk
+    atomicMax(&sm.n2, nst);
+    ac::mbar_arrive(ac::smem_u32(&sm.settled));
+  }
+}
+
+// Threads of a CTA: one per row (an SM's 16 warps of 128 registers fill its register
+// file).  RB 512: one CTA per SM; RB 128: three.
+template <int RB>
+struct StreamCta {
+  static_assert(RB == 512 || RB == 128, "rows per CTA");
+  static constexpr int kThreads = RB;
+  static constexpr int kMaxRegs = 128;
+};
+
+template <int RB, int TS, bool HAS_Z, bool PRECISE>
+__device__ __forceinline__ void row_program(StreamSmem<RB, TS>& sm, const StreamParams& p, const Ring& g,
+                                            const RowConst& cs, __nv_bfloat16* orow, float (&h)[NS], int chunk,
+                                            int rem, int per_chunk, int64_t row, int r, int warp, int lane,
+                                            int tc1, int& err) {
+  constexpr int NW = RB / 32;
+  const int n1 = g.n1;
+  float S = 0.f, comp = 0.f;
+  if (chunk == 0)
+    consume<RB, TS, HAS_Z, kAll, PRECISE>(sm, g, cs, orow, r, warp, lane, 0, n1, g.tc0, tc1, 0, h, S, comp, err);
+  else
+    consume<RB, TS, HAS_Z, kSettled, PRECISE>(sm, g, cs, orow, r, warp, lane, 0, n1, g.tc0, tc1, -1, h, S, comp,
+                                              err);
+
+  // ---------------- carry between chunks ----------------
+  // Each warp publishes its rows' aggregate (S, h from h = 0; the first chunk's h is
+  // its end state from the initial state) and combines those of all preceding
+  // chunks in a fixed order, h_in = Σ_j 2^{A (S_{j+1} + … + S_{chunk-1})} h_j, so the
+  // result does not depend on which chunk finished first.  The aggregates are
+  // published right after pass one, so no chunk waits for another's carry.
+  float hin[NS];
+#pragma unroll
+  for (int n = 0; n < NS; ++n) hin[n] = 0.f;
+  if (p.nchunks > 1) {
+    const int64_t rows_chunk = (int64_t)per_chunk * RB;
+    const int64_t my = (int64_t)rem * RB + r;
+    const int64_t flags_chunk = (int64_t)per_chunk * NW;
+    const int64_t fw = (int64_t)rem * NW + warp;
+    if (chunk + 1 < p.nchunks) {
+      float4* ah = reinterpret_cast<float4*>(p.ws.agg_h + ((int64_t)chunk * rows_chunk + my) * NS);
+#pragma unroll
+      for (int q = 0; q < NS / 4; ++q) ah[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+      p.ws.agg_s[(int64_t)chunk * rows_chunk + my] = S;
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) st_release_gpu(p.ws.flags + (int64_t)chunk * flags_chunk + fw, 1u);
+    }
+    if (chunk > 0) {
+      // every preceding chunk's aggregate: lanes wait on different chunks' flags
+      const unsigned want = p.fault_lookback ? 3u : 1u;  // 3 is never written
+      bool all_ok = true;
+      for (int base = 0; base < chunk; base += 32) {
+        const int j = base + lane;
+        unsigned v = 0;
+        const bool ok = j >= chunk || wait_flag(p.ws.flags + (int64_t)j * flags_chunk + fw, want, p.timeout_ns, &v);
+        all_ok = __all_sync(0xffffffffu, ok) && all_ok;
+      }
+      __syncwarp();
+      if (!all_ok) {
+        err = 1;  // the carry is left out; the error word reports it
+      } else {
+        float acc = 0.f;
+        for (int j = chunk - 1; j >= 0; --j) {
+          const float4* src = reinterpret_cast<const float4*>(p.ws.agg_h + ((int64_t)j * rows_chunk + my) * NS);
+#pragma unroll
+          for (int q = 0; q < NS / 4; ++q) {
+            const float4 x = __ldcg(src + q);
+            const float xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int n = 4 * q + i;
+              hin[n] = fmaf(PRECISE ? exp2f(cs.a2[n] * acc) : ex2_approx(cs.a2[n] * acc), xv[i], hin[n]);
+            }
+          }
+          acc += __ldcg(p.ws.agg_s + (int64_t)j * rows_chunk + my);
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < NS; ++n)
+        h[n] = fmaf(PRECISE ? exp2f(cs.a2[n] * S) : ex2_approx(cs.a2[n] * S), hin[n], h[n]);
+    }
+  }
+  if (p.a.final_state && chunk == p.nchunks - 1 && cs.row_ok) {
+    float4* fs = reinterpret_cast<float4*>(p.a.final_state + row * NS);
+#pragma unroll
+    for (int q = 0; q < NS / 4; ++q) fs[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+  }
+
+  // ---------------- pass two: the chunk's first stages again, from h_in ----------------
+  if (chunk > 0) {
+    if (!ac::mbar_wait(ac::smem_u32(&sm.settled), 0u, g.deadline)) err = 1;
+    const int n2 = *reinterpret_cast<volatile int*>(&sm.n2);
+    float S2 = 0.f, comp2 = 0.f;
+    consume<RB, TS, HAS_Z, kUnsettled, PRECISE>(sm, g, cs, orow, r, warp, lane, n1, n2, g.tc0, tc1, n2, hin, S2,
+                                                comp2, err);
+  }
+}
+
+template <int RB, int TS, bool HAS_Z>
+__global__ void __launch_bounds__(StreamCta<RB>::kThreads) __maxnreg__(StreamCta<RB>::kMaxRegs)
+    scan_stream_kernel(const __grid_constant__ StreamParams p) {
+  using G = Geo<TS>;
+  constexpr int NW = RB / 32;
+  extern __shared__ unsigned char smem_raw[];
+  // aligned by offsetting the shared array itself, so that the compiler keeps
+  // shared-memory (32-bit) addressing
+  StreamSmem<RB, TS>& sm = *reinterpret_cast<StreamSmem<RB, TS>*>(
+      smem_raw + ((1024u - (ac::smem_u32(smem_raw) & 1023u)) & 1023u));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < G::NSTG; ++s) {
+      ac::mbar_init(ac::smem_u32(&sm.full[s]), 1);  // the issuing thread's arrival + the copies' bytes
+      ac::mbar_init(ac::smem_u32(&sm.conv[s]), NW);
+      sm.done[s] = 0;
+    }
+    ac::mbar_init(ac::smem_u32(&sm.settled), NW);
+    ac::fence_mbar_init();
+    sm.n2 = 0;
+    sm.issued = 0;
+    sm.ticket = p.nchunks > 1 ? (int)atomicAdd(p.ws.hdr, 1u) : (int)blockIdx.x;
+  }
+  __syncthreads();
+  const int per_chunk = (int)p.a.batch * p.rtiles;
+  const int item = sm.ticket;
+  const int chunk = item / per_chunk;  // chunk-major tickets: a chunk's predecessors started earlier
+  const int rem = item % per_chunk;
+  Ring g;
+  g.p = &p;
+  g.deadline = ac::globaltimer() + (unsigned long long)p.timeout_ns;
+  g.b = rem / p.rtiles;
+  g.c0 = (rem % p.rtiles) * RB;
+  g.tc0 = (int)min((int64_t)p.a.L, (int64_t)chunk * p.chunk_len);
+  const int tc1 = (int)min((int64_t)p.a.L, (int64_t)g.tc0 + p.chunk_len);
+  g.n1 = (tc1 - g.tc0 + TS - 1) / TS;
+  g.spec_end = g.n1 + (chunk > 0 ? min(G::NSTG, g.n1) : 0);
+  int err = 0;
+
+  // fill the ring, then every warp converts its share of the first kAhead stages
+  if (threadIdx.x == 0) {
+    ac::prefetch_tensormap(&p.tm_u);
+    ac::prefetch_tensormap(&p.tm_d);
+    if (HAS_Z) ac::prefetch_tensormap(&p.tm_z);
+    ac::prefetch_tensormap(&p.tm_b);
+    ac::prefetch_tensormap(&p.tm_c);
+    for (int j = 0; j < G::NSTG && j < g.spec_end; ++j) ring_issue<RB, TS, HAS_Z>(sm, g, j);
+  }
+  for (int j = 0; j < G::kAhead && j < g.spec_end; ++j) ring_convert<RB, TS>(sm, g, j, warp, lane, err);
+
+  // ---------------- thread r owns row c0 + r ----------------
+  const int r = threadIdx.x;
+  RowConst cs;
+  const int nrows = min(RB, (int)p.a.d_inner - g.c0);
+  cs.row_ok = r < nrows;
+  const int64_t ch = g.c0 + (cs.row_ok ? r : 0);
+  const int64_t row = (int64_t)g.b * p.a.d_inner + ch;
+  __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.a.out) + row * p.a.L;
+  float h[NS];
+  cs.precise = false;
+  cs.a2max = -INFINITY;
+  const float* arow = p.a.A + ch * NS;
+#pragma unroll
+  for (int n = 0; n < NS; ++n) {
+    const float a = cs.row_ok ? arow[n] : 0.f;
+    const bool tiny = fabsf(a) < 8.673617e-19f;  // |A| < 2^-60 counts as A = 0
+    if (cs.row_ok && tiny) cs.precise = true;
+    cs.a2[n] = tiny ? 0.f : a;
+    cs.ia[n] = tiny ? 0.f : 1.f / a;
+    if (cs.row_ok) cs.a2max = fmaxf(cs.a2max, cs.a2[n]);
+    h[n] = (chunk == 0 && p.a.h0 && cs.row_ok) ? p.a.h0[row * NS + n] : 0.f;
+  }
+  cs.precise = __any_sync(0xffffffffu, cs.precise);  // warp-uniform: the exact branch serves every row
+  cs.Dc = (cs.row_ok && p.a.D) ? p.a.D[ch] : 0.f;
+  cs.bl2 = (cs.row_ok && p.a.bias) ? p.a.bias[ch] * kLog2e : 0.f;
+
+  if (cs.precise)
+    row_program<RB, TS, HAS_Z, true>(sm, p, g, cs, orow, h, chunk, rem, per_chunk, row, r, warp, lane, tc1, err);
+  else
+    row_program<RB, TS, HAS_Z, false>(sm, p, g, cs, orow, h, chunk, rem, per_chunk, row, r, warp, lane, tc1, err);
+
+  // copies issued ahead of a pass two shorter than the ring, never consumed, must land
+  // before the CTA exits
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int issued = sm.issued;
+    for (int j = issued - G::NSTG < 0 ? 0 : issued - G::NSTG; j < issued; ++j)
+      if (!ac::mbar_wait(ac::smem_u32(&sm.full[j % G::NSTG]), (uint32_t)(j / G::NSTG) & 1u,
+                         g.deadline + 1000000000ull))
+        err = 1;
+  }
+  if (err && p.ws.hdr) atomicOr(p.ws.hdr + 1, kErrTimeout);
+}
+
+template <int RB, int TS, bool HAS_Z>
+cudaError_t stream_launch_t(const StreamParams& p, int grid, cudaStream_t s) {
+  auto kern = scan_stream_kernel<RB, TS, HAS_Z>;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stream_smem_bytes<RB, TS>());
+  if (e != cudaSuccess) return e;
+  kern<<<grid, StreamCta<RB>::kThreads, stream_smem_bytes<RB, TS>(), s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int RB, int TS>
+cudaError_t stream_launch_z(const StreamParams& p, bool has_z, int grid, cudaStream_t s) {
+  return has_z ? stream_launch_t<RB, TS, true>(p, grid, s) : stream_launch_t<RB, TS, false>(p, grid, s);
+}
+
+}  // namespace
+
+size_t stream_smem_bytes_for(int rb, int ts) {
+  if (ts == 8) return rb == 512 ? stream_smem_bytes<512, 8>() : stream_smem_bytes<128, 8>();
+  return rb == 512 ? stream_smem_bytes<512, 16>() : stream_smem_bytes<128, 16>();
+}
+
+StreamWs stream_ws_layout(unsigned char* ws, int64_t nchunks, int64_t items, int rb, size_t* total) {
+  // [header][flags: nchunks × items × warps][aggregate h: nchunks × rows × 16][aggregate S: nchunks × rows]
+  StreamWs w{};
+  const int64_t rows = items * rb, warps = items * (rb / 32);
+  size_t off = kWsHeaderBytes;
+  const size_t flags_off = off;
+  off += ((size_t)nchunks * warps * 4 + 255) & ~size_t(255);
+  w.flags_bytes = off;
+  const size_t aggh_off = off;
+  off += (size_t)nchunks * rows * NS * 4;
+  const size_t aggs_off = off;
+  off += ((size_t)nchunks * rows * 4 + 255) & ~size_t(255);
+  *total = off;
+  if (ws) {
+    w.hdr = reinterpret_cast<unsigned*>(ws);
+    w.flags = reinterpret_cast<unsigned*>(ws + flags_off);
+    w.agg_h = reinterpret_cast<float*>(ws + aggh_off);
+    w.agg_s = reinterpret_cast<float*>(ws + aggs_off);
+  }
+  return w;
+}
+
+bool stream_supported(const ScanArgs& a) {
+  if (a.act != 1 || a.N != NS) return false;
+  if (a.L % 8 != 0 || a.L > (int64_t)INT32_MAX - 64 || a.d_inner > (int64_t)INT32_MAX - 512 || a.batch > 65535)
+    return false;
+  auto a16 = [](const void* q) { return q == nullptr || (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  return a16(a.u) && a16(a.delta) && a16(a.z) && a16(a.B) && a16(a.C) && a16(a.out);
+}
+
+cudaError_t scan_stream_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream) {
+  StreamParams p{};
+  p.a = a;
+  p.rtiles = plan.ctiles;
+  p.nchunks = plan.nchunks;
+  p.chunk_len = plan.chunk_len;
+  const RuntimeKnobs knobs = runtime_knobs();
+  p.timeout_ns = knobs.lookback_timeout_ns > 0 ? knobs.lookback_timeout_ns
+                                               : 1000ll * 1000 * 1000 + plan.chunk_len * 100ll;
+  p.fault_lookback = knobs.fault_lookback ? 1 : 0;
+  const int rb = plan.rows_per_cta;
+  size_t total = 0;
+  // one chunk: no workspace is required; if one is given its header takes the error word
+  p.ws = stream_ws_layout(plan.nchunks > 1 ? a.ws : nullptr, plan.nchunks, a.batch * plan.ctiles, rb, &total);
+  if (plan.nchunks == 1) p.ws.hdr = reinterpret_cast<unsigned*>(a.ws);
+  // tensor maps: u, Δraw, z as [batch][d_inner][L], B and C as [batch][L][16], bf16
+  const uint64_t L = (uint64_t)a.L, D = (uint64_t)a.d_inner, Bt = (uint64_t)a.batch;
+  const uint64_t dims_row[3] = {L, D, Bt}, str_row[2] = {L * 2, L * D * 2};
+  const int ts = plan.stage_tokens;
+  const uint32_t box_row[3] = {(uint32_t)ts, (uint32_t)box_rows(rb), 1};
+  const uint64_t dims_bc[3] = {(uint64_t)NS, L, Bt}, str_bc[2] = {NS * 2, L * NS * 2};
+  const uint32_t box_bc[3] = {(uint32_t)NS, (uint32_t)ts, 1};
+  const CUtensorMapSwizzle swz = ts == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+  bool ok = encode_tensor_map(&p.tm_u, bf, 3, a.u, dims_row, str_row, box_row, swz, promo) &&
+            encode_tensor_map(&p.tm_d, bf, 3, a.delta, dims_row, str_row, box_row, swz, promo) &&
+            encode_tensor_map(&p.tm_b, bf, 3, a.B, dims_bc, str_bc, box_bc, CU_TENSOR_MAP_SWIZZLE_NONE, promo) &&
+            encode_tensor_map(&p.tm_c, bf, 3, a.C, dims_bc, str_bc, box_bc, CU_TENSOR_MAP_SWIZZLE_NONE, promo);
+  if (ok && a.z)
+    ok = encode_tensor_map(&p.tm_z, bf, 3, a.z, dims_row, str_row, box_row, swz, promo);
+  if (!ok) return cudaErrorInvalidValue;
+  if (plan.nchunks > 1) {
+    const cudaError_t e = cudaMemsetAsync(a.ws, 0, p.ws.flags_bytes, stream);
+    if (e != cudaSuccess) return e;
+  }
+  const int grid = (int)((int64_t)plan.nchunks * a.batch * plan.ctiles);
+  const bool hz = a.z != nullptr;
+  if (ts == 8) return rb == 512 ? stream_launch_z<512, 8>(p, hz, grid, stream)
+                                : stream_launch_z<128, 8>(p, hz, grid, stream);
+  return rb == 512 ? stream_launch_z<512, 16>(p, hz, grid, stream) : stream_launch_z<128, 16>(p, hz, grid, stream);
+}
+
+}  // namespace ssm

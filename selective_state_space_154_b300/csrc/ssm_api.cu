@@ -1,8 +1,10 @@
 // C ABI of the selective-scan library: argument validation, launch planning,
 // status codes.  Declarations and the meaning of every argument are in
 // include/ssm_scan.h.
+#include <atomic>
 #include <climits>
 #include <cstdint>
+#include <mutex>
 #include <cstdlib>
 #include <cstring>
 
@@ -11,37 +13,80 @@
 
 namespace ssm {
 
-// Read on every call (a getenv per launch) so that tests can change them per call.
+namespace {
+
+// The test hooks (SSM_* environment variables, listed in include/ssm_scan.h) are
+// read once, at the first call that needs them, and again only when the
+// application calls ssm_test_hooks_reload(): no call reads the environment on
+// its own.  Each load publishes an immutable copy.
+RuntimeKnobs* load_knobs() {
+  RuntimeKnobs* r = new RuntimeKnobs{};
+  r->lookback_timeout_ns = 0;  // 0: 1 s + 100 ns per token of a chunk (set at launch)
+  if (const char* s = std::getenv("SSM_LOOKBACK_TIMEOUT_MS")) {
+    const long long ms = std::atoll(s);
+    if (ms > 0) r->lookback_timeout_ns = ms * 1000ll * 1000;
+  }
+  const char* f = std::getenv("SSM_FAULT");
+  r->fault_lookback = f && std::strcmp(f, "lookback") == 0;
+  r->fault_step = f && std::strcmp(f, "step") == 0;
+  r->fault_ssd = f && std::strcmp(f, "ssd") == 0;
+  const char* fs = std::getenv("SSM_FORCE_STEP");
+  r->force_step_plain = fs && std::strcmp(fs, "plain") == 0;
+  if (const char* c = std::getenv("SSM_FORCE_CHUNKS")) r->force_chunks = std::atoi(c);
+  r->force_kind = -1;
+  if (const char* k = std::getenv("SSM_FORCE_KERNEL")) {
+    if (std::strcmp(k, "tiles") == 0) r->force_kind = kScanTiles;
+    if (std::strcmp(k, "rows") == 0) r->force_kind = kScanRows;
+    if (std::strcmp(k, "stream") == 0) r->force_kind = kScanStream;
+  }
+  if (const char* c = std::getenv("SSM_CTAS_PER_SM")) r->ctas_per_sm = std::atoi(c);
+  if (const char* c = std::getenv("SSM_FORCE_TPR")) r->force_tpr = std::atoi(c);
+  if (const char* c = std::getenv("SSM_BWD_CHUNKS")) r->bwd_chunks = std::atoi(c);
+  if (const char* c = std::getenv("SSM_STREAM_ROWS")) {
+    const int v = std::atoi(c);
+    r->stream_rows = (v == 512 || v == 128) ? v : 0;
+  }
+  if (const char* c = std::getenv("SSM_STREAM_TOKENS")) r->stream_stage_tokens = std::atoi(c);
+  return r;
+}
+
+std::atomic<RuntimeKnobs*> g_knobs{nullptr};
+std::mutex g_knobs_mu;
+
+}  // namespace
+
 RuntimeKnobs runtime_knobs() {
-  return [] {
-    RuntimeKnobs r{};
-    r.lookback_timeout_ns = 0;  // 0: 1 s + 100 ns per token of a chunk (set at launch)
-    if (const char* s = std::getenv("SSM_LOOKBACK_TIMEOUT_MS")) {
-      const long long ms = std::atoll(s);
-      if (ms > 0) r.lookback_timeout_ns = ms * 1000ll * 1000;
+  RuntimeKnobs* k = g_knobs.load(std::memory_order_acquire);
+  if (!k) {
+    std::lock_guard<std::mutex> lock(g_knobs_mu);
+    k = g_knobs.load(std::memory_order_acquire);
+    if (!k) {
+      k = load_knobs();
+      g_knobs.store(k, std::memory_order_release);
     }
-    const char* f = std::getenv("SSM_FAULT");
-    r.fault_lookback = f && std::strcmp(f, "lookback") == 0;
-    r.fault_step = f && std::strcmp(f, "step") == 0;
-    r.fault_ssd = f && std::strcmp(f, "ssd") == 0;
-    const char* fs = std::getenv("SSM_FORCE_STEP");
-    r.force_step_plain = fs && std::strcmp(fs, "plain") == 0;
-    if (const char* c = std::getenv("SSM_FORCE_CHUNKS")) r.force_chunks = std::atoi(c);
-    r.force_kind = -1;
-    if (const char* k = std::getenv("SSM_FORCE_KERNEL")) {
-      if (std::strcmp(k, "tiles") == 0) r.force_kind = kScanTiles;
-      if (std::strcmp(k, "rows") == 0) r.force_kind = kScanRows;
-    }
-    if (const char* c = std::getenv("SSM_CTAS_PER_SM")) r.ctas_per_sm = std::atoi(c);
-    if (const char* c = std::getenv("SSM_FORCE_TPR")) r.force_tpr = std::atoi(c);
-    if (const char* c = std::getenv("SSM_BWD_CHUNKS")) r.bwd_chunks = std::atoi(c);
-    return r;
-  }();
+  }
+  return *k;
+}
+
+void reload_knobs() {
+  std::lock_guard<std::mutex> lock(g_knobs_mu);
+  // the previous copy stays allocated: a concurrent reader may still hold it
+  g_knobs.store(load_knobs(), std::memory_order_release);
 }
 
 }  // namespace ssm
 
 namespace {
+
+// The error behind the calling thread's last SSM_ERR_CUDA (see ssm_last_cuda_error).
+thread_local int g_last_cuda_error = 0;
+
+ssm_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return SSM_OK;
+  const int drv = ssm::take_driver_error();
+  g_last_cuda_error = drv ? 10000 + drv : (int)e;
+  return SSM_ERR_CUDA;
+}
 
 bool aligned(const void* p, unsigned bytes) { return (reinterpret_cast<uintptr_t>(p) & (bytes - 1u)) == 0; }
 bool aligned16(const void* p) { return aligned(p, 16); }
@@ -156,13 +201,15 @@ ssm_status scan_fwd_impl(const void* u, const void* delta, const float* A, const
     if (!workspace || workspace_bytes < plan.ws_bytes) return SSM_ERR_WORKSPACE;
     if (!aligned16(workspace)) return SSM_ERR_ALIGNMENT;
   }
+  if (plan.ws_bytes == 0 && workspace_bytes < sizeof(unsigned) * 2) a.ws = nullptr;  // too small for the error word
   if (plan.ws_bytes == 0 && workspace && workspace_bytes >= sizeof(unsigned) * 2) {
     // clear the error word so ssm_scan_check on this workspace reports this call
-    if (cudaMemsetAsync(workspace, 0, sizeof(unsigned) * 2, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-      return SSM_ERR_CUDA;
+    const ssm_status ms =
+        cuda_status(cudaMemsetAsync(workspace, 0, sizeof(unsigned) * 2, reinterpret_cast<cudaStream_t>(stream)));
+    if (ms != SSM_OK) return ms;
   }
   const cudaError_t e = ssm::scan_launch(a, plan, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  return cuda_status(e);
 }
 
 }  // namespace
@@ -212,7 +259,7 @@ ssm_status ssm_step(float* state, const void* x, const void* delta, const float*
   sk.fault = knobs.fault_step;
   sk.force_plain = knobs.force_step_plain;
   const cudaError_t e = ssm::step_launch(a, sk, reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  return cuda_status(e);
 }
 
 ssm_status ssm_conv1d_fwd(const void* x, const float* weight, const float* bias, const void* initial_conv_state,
@@ -228,7 +275,7 @@ ssm_status ssm_conv1d_fwd(const void* x, const float* weight, const float* bias,
   if (!aligned(weight, 4) || (bias && !aligned(bias, 4))) return SSM_ERR_ALIGNMENT;
   const ssm::ConvCall k = conv_call(x, weight, bias, width > 1 ? initial_conv_state : nullptr, out,
                                     width > 1 ? final_conv_state : nullptr, dims, width, true);
-  return ssm::conv1d_fwd_launch(k, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  return cuda_status(ssm::conv1d_fwd_launch(k, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 ssm_status ssm_conv1d_step(void* conv_state, const void* x, const float* weight, const float* bias, void* out,
@@ -242,7 +289,7 @@ ssm_status ssm_conv1d_step(void* conv_state, const void* x, const float* weight,
     if (p && !aligned(p, esz)) return SSM_ERR_ALIGNMENT;
   if (!aligned(weight, 4) || (bias && !aligned(bias, 4))) return SSM_ERR_ALIGNMENT;
   const ssm::ConvCall k = conv_call(x, weight, bias, nullptr, out, conv_state, dims, width, false);
-  return ssm::conv1d_step_launch(k, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  return cuda_status(ssm::conv1d_step_launch(k, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t ssm_scan_bwd_workspace_bytes(const ssm_dims* dims) {
@@ -274,25 +321,27 @@ ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int64_t b = dims->batch, d = dims->d_inner, N = dims->d_state, L = dims->seqlen;
   // accumulated gradients start at zero
-  if (cudaMemsetAsync(dA, 0, sizeof(float) * d * N, st) != cudaSuccess ||
-      cudaMemsetAsync(dB, 0, sizeof(float) * b * L * N, st) != cudaSuccess ||
-      cudaMemsetAsync(dC, 0, sizeof(float) * b * L * N, st) != cudaSuccess ||
-      (dD && cudaMemsetAsync(dD, 0, sizeof(float) * d, st) != cudaSuccess) ||
-      (ddelta_bias && cudaMemsetAsync(ddelta_bias, 0, sizeof(float) * d, st) != cudaSuccess))
-    return SSM_ERR_CUDA;
+  cudaError_t me = cudaMemsetAsync(dA, 0, sizeof(float) * d * N, st);
+  if (me == cudaSuccess) me = cudaMemsetAsync(dB, 0, sizeof(float) * b * L * N, st);
+  if (me == cudaSuccess) me = cudaMemsetAsync(dC, 0, sizeof(float) * b * L * N, st);
+  if (me == cudaSuccess && dD) me = cudaMemsetAsync(dD, 0, sizeof(float) * d, st);
+  if (me == cudaSuccess && ddelta_bias) me = cudaMemsetAsync(ddelta_bias, 0, sizeof(float) * d, st);
+  if (me != cudaSuccess) return cuda_status(me);
   ssm::BwdArgs a{};
   a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.bias = delta_bias; a.dout = dout;
   a.du = du; a.ddelta = ddelta; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dz = dz; a.dbias = ddelta_bias;
   a.ckpt = static_cast<float*>(workspace);
   a.batch = b; a.d_inner = d; a.N = N; a.L = L; a.act = dims->act;
   a.force_chunks = ssm::runtime_knobs().bwd_chunks;
-  return ssm::scan_bwd_launch(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  return cuda_status(ssm::scan_bwd_launch(a, st));
 }
 
 ssm_status ssm_step_check(ssm_stream_t stream) {
-  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return SSM_ERR_CUDA;
+  const ssm_status ss = cuda_status(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+  if (ss != SSM_OK) return ss;
   unsigned word = 0;
-  if (ssm::step_error_fetch_clear(&word) != cudaSuccess) return SSM_ERR_CUDA;
+  const ssm_status fs = cuda_status(ssm::step_error_fetch_clear(&word));
+  if (fs != SSM_OK) return fs;
   return word ? SSM_ERR_TIMEOUT : SSM_OK;
 }
 
@@ -321,7 +370,8 @@ ssm_status ssd_scan_fwd(const void* x, const void* dt, const float* A, const voi
   if (!aligned16(workspace)) return SSM_ERR_ALIGNMENT;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // clear the error word so ssm_scan_check on this workspace reports this call
-  if (cudaMemsetAsync(workspace, 0, sizeof(unsigned) * 2, st) != cudaSuccess) return SSM_ERR_CUDA;
+  const ssm_status ms = cuda_status(cudaMemsetAsync(workspace, 0, sizeof(unsigned) * 2, st));
+  if (ms != SSM_OK) return ms;
   ssm::SsdArgs a{};
   a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias;
   a.h0 = initial_state; a.out = out; a.final_state = final_state; a.ws = workspace;
@@ -330,7 +380,7 @@ ssm_status ssd_scan_fwd(const void* x, const void* dt, const float* A, const voi
   const ssm::RuntimeKnobs knobs = ssm::runtime_knobs();
   a.timeout_ns = knobs.lookback_timeout_ns;
   a.fault = knobs.fault_ssd ? 1 : 0;
-  return ssm::ssd_launch(a, st) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  return cuda_status(ssm::ssd_launch(a, st));
 }
 
 ssm_status ssd_step(float* state, const void* x, const void* dt, const float* A, const void* B, const void* C,
@@ -352,15 +402,15 @@ ssm_status ssd_step(float* state, const void* x, const void* dt, const float* A,
   ssm::SsdStepArgs a{};
   a.state = state; a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias;
   a.out = out; a.batch = dims->batch; a.H = dims->nheads; a.P = dims->headdim; a.G = dims->ngroups;
-  return ssm::ssd_step_launch(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+  return cuda_status(ssm::ssd_step_launch(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 ssm_status ssm_scan_check(const void* workspace, size_t workspace_bytes) {
   if (!workspace || workspace_bytes < sizeof(unsigned) * 2) return SSM_OK;
   unsigned word = 0;
-  if (cudaMemcpy(&word, static_cast<const unsigned char*>(workspace) + sizeof(unsigned), sizeof(word),
-                 cudaMemcpyDeviceToHost) != cudaSuccess)
-    return SSM_ERR_CUDA;
+  const ssm_status cs = cuda_status(cudaMemcpy(&word, static_cast<const unsigned char*>(workspace) + sizeof(unsigned),
+                                                sizeof(word), cudaMemcpyDeviceToHost));
+  if (cs != SSM_OK) return cs;
   return (word & ssm::kErrTimeout) ? SSM_ERR_TIMEOUT : SSM_OK;
 }
 
@@ -376,5 +426,9 @@ const char* ssm_status_string(ssm_status s) {
   }
   return "SSM_ERR_UNKNOWN";
 }
+
+void ssm_test_hooks_reload(void) { ssm::reload_knobs(); }
+
+int ssm_last_cuda_error(void) { return g_last_cuda_error; }
 
 }  // extern "C"

@@ -20,7 +20,7 @@ constexpr int kRowTokensPerStage = 32;  // row kernel: tokens per stage
 template <typename T>
 __host__ __device__ constexpr float corr_stop_log2() { return sizeof(T) == 2 ? -12.f : -24.f; }
 
-enum ScanKind { kScanTiles = 0, kScanRows = 1 };
+enum ScanKind { kScanTiles = 0, kScanRows = 1, kScanStream = 2 };
 
 // Workspace header (bytes): [0] ticket counter, [1] error word.
 constexpr size_t kWsHeaderBytes = 256;
@@ -40,6 +40,7 @@ struct ScanPlan {
   int nchunks;        // chunks along the sequence (1: no carry between chunks)
   size_t smem_bytes;  // dynamic shared memory per CTA
   size_t ws_flags_off, ws_agg_off, ws_bytes;  // workspace layout (0 bytes when nchunks == 1)
+  int stage_tokens;   // streamed row kernel: tokens per pipeline stage (16 or 8)
 };
 
 struct ScanArgs {
@@ -59,7 +60,7 @@ struct ScanArgs {
   unsigned char* ws;
 };
 
-// Host-side knobs read from the environment at every call (see ssm_api.cu).
+// Host-side test hooks from the SSM_* environment variables (see ssm_api.cu).
 struct RuntimeKnobs {
   long long lookback_timeout_ns;  // device-side wait limit between chunks (0: default)
   bool fault_lookback;            // test hook: chunk waits on a flag nothing sets
@@ -71,13 +72,32 @@ struct RuntimeKnobs {
   bool force_step_plain;          // SSM_FORCE_STEP=plain: the generic step kernel only
   int bwd_chunks;                 // >0: sequence chunks of the backward (tests)
   bool fault_ssd;                 // test hook: the SSD output kernel's first wait never completes
+  int stream_rows;                // >0: rows per CTA of the streamed row kernel (512, 256 or 128)
+  int stream_stage_tokens;        // 8: 8-token stages in the streamed row kernel (default 16)
 };
-RuntimeKnobs runtime_knobs();
+RuntimeKnobs runtime_knobs();  // the test hooks as last loaded (first use, or ssm_test_hooks_reload)
+void reload_knobs();
 
 bool scan_make_plan(const ScanArgs& a, ScanPlan* plan);  // false: unsupported dims
 cudaError_t scan_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream);
 int rows_big_cta_rows(int act);  // rows of the one-CTA-per-SM variant of the row kernel
 cudaError_t scan_rows_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream);
+
+// Streamed row kernel (scan_stream.cu): bf16, d_state 16, tensor-copied stages.
+// Workspace: [header][flags: chunks × CTAs × warps][chunk aggregates h: chunks ×
+// rows × 16][aggregate ΣΔ': chunks × rows].
+struct StreamWs {
+  unsigned* hdr;
+  unsigned* flags;
+  float* agg_h;
+  float* agg_s;
+  size_t flags_bytes;  // bytes from the start that are cleared per call (header + flags)
+};
+StreamWs stream_ws_layout(unsigned char* ws, int64_t nchunks, int64_t items, int rows_per_cta, size_t* total);
+bool stream_supported(const ScanArgs& a);
+int take_driver_error();  // CUresult of the calling thread's last failed driver call (then cleared), or 0  // dtype, d_state, alignment and size limits
+size_t stream_smem_bytes_for(int rows_per_cta, int stage_tokens);
+cudaError_t scan_stream_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream);
 
 struct StepArgs {
   float* state;

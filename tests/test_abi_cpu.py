@@ -96,6 +96,27 @@ def test_scan_rejects_misaligned_activation_pointer(lib, which):
     assert _scan(lib, _dims(act=ssm.SSM_DTYPE_F32), {which: FAKE + 2}) == ssm.SSM_ERR_ALIGNMENT
 
 
+@pytest.mark.parametrize("which", ["u", "delta", "B", "C", "z", "out"])
+def test_scan_accepts_element_aligned_pointers(lib, which):
+    """Element alignment is the rule: a bf16 pointer 2 bytes past a 16-byte boundary
+    (an fp32 one 4 bytes past) passes validation and reaches the launch, which here,
+    with no GPU, fails as a CUDA error rather than as an alignment error."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("the fake pointers would be dereferenced by a real launch")
+    for act, off in ((ssm.SSM_DTYPE_BF16, 2), (ssm.SSM_DTYPE_F32, 4)):
+        st = _scan(lib, _dims(act=act), {which: FAKE + off})
+        assert st == ssm.SSM_ERR_CUDA, ssm.ssm_status_string(st)
+
+
+def test_noalloc_scratch_size_matches_the_header(lib):
+    text = open(os.path.join(ROOT, "include", "ssm_scan.h")).read()
+    m = re.search(r"#define SSM_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", text)
+    assert m
+    assert lib.ssm_noalloc_scratch_bytes() == int(m.group(1)) << int(m.group(2))
+    assert ssm.SSM_NOALLOC_SCRATCH_BYTES == lib.ssm_noalloc_scratch_bytes()
+
+
 @pytest.mark.parametrize("which", ["A", "D", "bias", "fs"])
 def test_scan_rejects_misaligned_fp32_pointer(lib, which):
     assert _scan(lib, _dims(), {which: FAKE + 2}) == ssm.SSM_ERR_ALIGNMENT
@@ -274,3 +295,29 @@ def test_ssd_step_rejects_misaligned_pointer(lib, which, offset):
 def test_ssd_step_rejects_unsupported_dims(lib):
     assert _ssd_step(lib, _ssd_dims(d_state=64)) == ssm.SSM_ERR_UNSUPPORTED
     assert _ssd_step(lib, _ssd_dims(ngroups=3)) == ssm.SSM_ERR_INVALID_ARG
+
+
+def _host_scan(lib, dims, piece, staging=None, staging_bytes=0, ptrs=None):
+    p = dict(u=FAKE, delta=FAKE, A=FAKE, B=FAKE, C=FAKE, D=None, z=None, bias=None, h0=None, out=FAKE, fs=None)
+    p.update(ptrs or {})
+    a = [ctypes.c_void_p(p[k]) if p[k] else None for k in ("u", "delta", "A", "B", "C", "D", "z", "bias", "h0",
+                                                          "out", "fs")]
+    return lib.ssm_scan_fwd_host(*a, ctypes.byref(dims), piece, staging, staging_bytes, None, None, None)
+
+
+def test_host_scan_validates_before_any_copy(lib):
+    d = _dims(batch=1, d_inner=64, d_state=16, seqlen=10000)
+    need = lib.ssm_scan_fwd_host_staging_bytes(ctypes.byref(d), 4096)
+    assert need > 0
+    # a larger piece needs more staging; pieces longer than the sequence count as the sequence
+    assert lib.ssm_scan_fwd_host_staging_bytes(ctypes.byref(d), 8192) > need
+    assert lib.ssm_scan_fwd_host_staging_bytes(ctypes.byref(d), 1 << 30) == \
+        lib.ssm_scan_fwd_host_staging_bytes(ctypes.byref(d), 10000)
+    assert lib.ssm_scan_fwd_host_staging_bytes(ctypes.byref(d), 0) == 0
+    assert _host_scan(lib, d, 0) == ssm.SSM_ERR_INVALID_ARG
+    assert _host_scan(lib, d, 4096) == ssm.SSM_ERR_WORKSPACE
+    assert _host_scan(lib, d, 4096, ctypes.c_void_p(FAKE), need - 1) == ssm.SSM_ERR_WORKSPACE
+    assert _host_scan(lib, d, 4096, ctypes.c_void_p(FAKE + 16), need) == ssm.SSM_ERR_ALIGNMENT
+    assert _host_scan(lib, d, 4096, ctypes.c_void_p(FAKE), need, {"out": None}) == ssm.SSM_ERR_INVALID_ARG
+    bad = _dims(d_state=65)
+    assert _host_scan(lib, bad, 16, ctypes.c_void_p(FAKE), 1 << 30) == ssm.SSM_ERR_UNSUPPORTED

@@ -82,17 +82,17 @@ def test_bwd_rejects_large_d_state():
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
 @pytest.mark.parametrize("chunks", [1, 2, 5, 19])
-def test_bwd_sequence_chunks(monkeypatch, dtype, chunks):
+def test_bwd_sequence_chunks(hooks, dtype, chunks):
     """The sequence split into chunks (38 blocks of 8 tokens, the last ragged, over
     1, 2, 5 or 19 chunks) gives the oracle's gradients."""
-    monkeypatch.setenv("SSM_BWD_CHUNKS", str(chunks))
+    hooks.set("SSM_BWD_CHUNKS", str(chunks))
     inp = W.random_scan_inputs(2, 70, 16, 300, dtype=dtype, device=DEV, seed=chunks, a_kind="random")
     _compare(inp, _dout(inp, chunks + 1), TOL[dtype])
 
 
-def test_bwd_sequence_chunks_zero_A(monkeypatch):
+def test_bwd_sequence_chunks_zero_A(hooks):
     """Chunk summaries with A = 0 states (no decay across chunks) on the scalar path."""
-    monkeypatch.setenv("SSM_BWD_CHUNKS", "4")
+    hooks.set("SSM_BWD_CHUNKS", "4")
     inp = W.random_scan_inputs(1, 40, 16, 200, dtype=torch.float32, device=DEV, seed=9, a_kind="random")
     inp["A"][::2, 5] = 0.0
     _compare(inp, _dout(inp, 10), TOL[torch.float32])
@@ -105,14 +105,14 @@ def test_bwd_few_rows_long_sequence(dtype):
     _compare(inp, _dout(inp, 22), TOL[dtype])
 
 
-def test_bwd_chunk_counts_agree(monkeypatch):
+def test_bwd_chunk_counts_agree(hooks):
     """fp32 gradients with 1 and 7 chunks agree to rounding (the chunk combine is exact
     algebra; only the order of additions differs)."""
     inp = W.random_scan_inputs(2, 50, 16, 500, dtype=torch.float32, device=DEV, seed=31, a_kind="random")
     dout = _dout(inp, 32)
-    monkeypatch.setenv("SSM_BWD_CHUNKS", "1")
+    hooks.set("SSM_BWD_CHUNKS", "1")
     g1 = _run(inp, dout)
-    monkeypatch.setenv("SSM_BWD_CHUNKS", "7")
+    hooks.set("SSM_BWD_CHUNKS", "7")
     g7 = _run(inp, dout)
     for k in GRADS:
         if g1[k] is None:

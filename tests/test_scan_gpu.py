@@ -21,14 +21,16 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.fixture(params=["tiles", "rows", "rows2"])
-def kernel(request, monkeypatch):
+@pytest.fixture(params=["tiles", "rows", "rows2", "stream"])
+def kernel(request, hooks):
     """Run the test through each scan kernel: the tile kernel, the row kernel with
-    one thread per row, and the row kernel with two threads per row (the row
-    kernel serves d_state <= 16; larger d_state falls back to the tile kernel)."""
-    monkeypatch.setenv("SSM_FORCE_KERNEL", "tiles" if request.param == "tiles" else "rows")
+    one thread per row, the row kernel with two threads per row, and the streamed
+    row kernel (the row kernels serve d_state <= 16, the streamed one bf16 with
+    d_state 16, 16-byte aligned rows and L a multiple of 8; other shapes fall back
+    to the planner's choice)."""
+    hooks.set("SSM_FORCE_KERNEL", {"tiles": "tiles", "stream": "stream"}.get(request.param, "rows"))
     if request.param == "rows2":
-        monkeypatch.setenv("SSM_FORCE_TPR", "2")
+        hooks.set("SSM_FORCE_TPR", "2")
     return request.param
 
 
@@ -69,10 +71,10 @@ def full_compare(inp, tol):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
 @pytest.mark.parametrize("chunks", [0, 3], ids=["planned", "3chunks"])
-def test_initial_state(dtype, chunks, kernel, monkeypatch):
+def test_initial_state(dtype, chunks, kernel, hooks):
     """ssm_scan_fwd_from_state against the oracle started from the same h0."""
     if chunks:
-        monkeypatch.setenv("SSM_FORCE_CHUNKS", str(chunks))
+        hooks.set("SSM_FORCE_CHUNKS", str(chunks))
     b, d, N, L = 2, 70, 16, 700
     inp = W.random_scan_inputs(b, d, N, L, dtype=dtype, device=DEV, seed=31, a_kind="random")
     g = torch.Generator(device=DEV).manual_seed(32)
@@ -112,16 +114,16 @@ def test_split_and_continue_matches_one_scan(kernel):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
-def test_chunking_does_not_change_results(dtype, kernel, monkeypatch):
+def test_chunking_does_not_change_results(dtype, kernel, hooks):
     """A chunked scan gives the unchunked scan's outputs: every output is computed
     from its true state and rounded once (a correction added to already-rounded
     bf16 outputs missed this by 1.1e-2 where the local output and the carried
     term cancel)."""
     b, d, N, L = 2, 256, 16, 4000
     inp = W.random_scan_inputs(b, d, N, L, dtype=dtype, device=DEV, seed=51)
-    monkeypatch.setenv("SSM_FORCE_CHUNKS", "1")
+    hooks.set("SSM_FORCE_CHUNKS", "1")
     one = ssm.scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["bias"])
-    monkeypatch.setenv("SSM_FORCE_CHUNKS", "6")
+    hooks.set("SSM_FORCE_CHUNKS", "6")
     six = ssm.scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["bias"])
     torch.cuda.synchronize()
     # bf16: two output ulps; fp32: the omitted carry (< 2^-24 of the state) and the
@@ -171,37 +173,37 @@ def test_zero_and_tiny_A(dtype, kernel):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
 @pytest.mark.parametrize("chunks", [2, 3, 7])
-def test_chunked_carry(dtype, chunks, kernel, monkeypatch):
+def test_chunked_carry(dtype, chunks, kernel, hooks):
     """Force the split along L so the look-back carry and the correction run on
     a problem the oracle checks in full (ragged last chunk, ragged channels)."""
-    monkeypatch.setenv("SSM_FORCE_CHUNKS", str(chunks))
+    hooks.set("SSM_FORCE_CHUNKS", str(chunks))
     inp = W.random_scan_inputs(2, 45, 16, 64 * 23 + 5, dtype=dtype, device=DEV, seed=chunks,
                                a_kind="random")
     full_compare(inp, TOL[dtype])
 
 
-def test_chunked_carry_slow_decay(kernel, monkeypatch):
+def test_chunked_carry_slow_decay(kernel, hooks):
     """Tiny |A|·Δ keeps the carry alive across whole chunks (correction never stops early)."""
-    monkeypatch.setenv("SSM_FORCE_CHUNKS", "4")
+    hooks.set("SSM_FORCE_CHUNKS", "4")
     inp = W.random_scan_inputs(1, 33, 16, 2048, dtype=torch.float32, device=DEV, seed=8, a_kind="random")
     inp["A"] = inp["A"] * 1e-3
     full_compare(inp, TOL[torch.float32])
 
 
-def test_lookback_timeout_is_reported_and_context_survives(kernel, monkeypatch):
+def test_lookback_timeout_is_reported_and_context_survives(kernel, hooks):
     """Test hook: every chunk after the first waits on a flag nothing sets; the
     bounded wait gives up, the error word reads SSM_ERR_TIMEOUT and the device
     stays usable."""
-    monkeypatch.setenv("SSM_FORCE_CHUNKS", "2")
-    monkeypatch.setenv("SSM_FAULT", "lookback")
-    monkeypatch.setenv("SSM_LOOKBACK_TIMEOUT_MS", "200")
+    hooks.set("SSM_FORCE_CHUNKS", "2")
+    hooks.set("SSM_FAULT", "lookback")
+    hooks.set("SSM_LOOKBACK_TIMEOUT_MS", "200")
     inp = W.random_scan_inputs(1, 32, 16, 1024, dtype=torch.bfloat16, device=DEV, seed=1)
     out = torch.empty_like(inp["u"])
     ws = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
                           inp["bias"], out, None)
     torch.cuda.synchronize()
     assert ssm.ssm_scan_check(ws) == ssm.SSM_ERR_TIMEOUT
-    monkeypatch.delenv("SSM_FAULT")
+    hooks.unset("SSM_FAULT")
     full_compare(inp, TOL[torch.bfloat16])  # same workspace layout, clean run
 
 
@@ -237,9 +239,9 @@ def test_long_1m_sampled():
 
 
 @pytest.mark.parametrize("name", ["mamba130m_layer", "long_1m"])
-def test_workload_through_other_kernel(name, monkeypatch):
+def test_workload_through_other_kernel(name, hooks):
     """The kernel not chosen by the planner for a workload gives the same result."""
-    monkeypatch.setenv("SSM_FORCE_KERNEL", "tiles")  # both take the row kernel by default
+    hooks.set("SSM_FORCE_KERNEL", "tiles")  # both take the row kernel by default
     _workload_rows(name, 8, seed=3)
 
 

@@ -108,7 +108,7 @@ def test_ssd_heads_per_cta(shape):
     _compare(W.random_ssd_inputs(*shape, device=DEV, seed=shape[2]))
 
 
-def test_ssd_wait_timeout_is_reported_and_the_context_recovers(monkeypatch):
+def test_ssd_wait_timeout_is_reported_and_the_context_recovers(hooks):
     """Test hook: the output kernel's first tensor-core wait is on an mbarrier that nothing
     arrives on.  The wait gives up after 200 ms, lets its issued products finish, frees its
     tensor memory and sets the workspace's error word; the next clean call is correct."""
@@ -116,13 +116,13 @@ def test_ssd_wait_timeout_is_reported_and_the_context_recovers(monkeypatch):
     ws = torch.empty(ssm.ssd_scan_workspace_bytes(1, 300, 2, 64, 1, 128), dtype=torch.uint8, device=DEV)
     args = (inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"])
     kw = dict(D=inp["D"], z=inp["z"], dt_bias=inp["dt_bias"], return_final_state=True, workspace=ws)
-    monkeypatch.setenv("SSM_FAULT", "ssd")
-    monkeypatch.setenv("SSM_LOOKBACK_TIMEOUT_MS", "200")
+    hooks.set("SSM_FAULT", "ssd")
+    hooks.set("SSM_LOOKBACK_TIMEOUT_MS", "200")
     ssm.ssd_scan(*args, **kw)
     torch.cuda.synchronize()
     assert ssm.ssm_scan_check(ws) == ssm.SSM_ERR_TIMEOUT
-    monkeypatch.delenv("SSM_FAULT")
-    monkeypatch.delenv("SSM_LOOKBACK_TIMEOUT_MS")
+    hooks.unset("SSM_FAULT")
+    hooks.unset("SSM_LOOKBACK_TIMEOUT_MS")
     out, fs = ssm.ssd_scan(*args, **kw)
     torch.cuda.synchronize()
     assert ssm.ssm_scan_check(ws) == ssm.SSM_OK

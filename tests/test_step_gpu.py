@@ -42,11 +42,11 @@ def test_step_small(dtype, batch, d, N):
 
 
 @pytest.fixture(params=["pipe", "plain"])
-def step_kernel(request, monkeypatch):
+def step_kernel(request, hooks):
     """Run a test with the pipelined step kernel where the shape allows it, or with
     the generic one (SSM_FORCE_STEP=plain)."""
     if request.param == "plain":
-        monkeypatch.setenv("SSM_FORCE_STEP", "plain")
+        hooks.set("SSM_FORCE_STEP", "plain")
     return request.param
 
 
@@ -73,7 +73,7 @@ def test_step_tiled_shapes(step_kernel, dtype, batch, d, N):
     assert ssm.ssm_step_check() == ssm.SSM_OK
 
 
-def test_step_wait_timeout_is_reported_and_state_kept(monkeypatch):
+def test_step_wait_timeout_is_reported_and_state_kept(hooks):
     """Test hook: the pipelined kernel's first wait is on a barrier nothing
     completes; the bounded wait gives up, every tile is left unchanged,
     ssm_step_check reports SSM_ERR_TIMEOUT once, and the next step is clean."""
@@ -81,14 +81,14 @@ def test_step_wait_timeout_is_reported_and_state_kept(monkeypatch):
     inp = _rand_step_inputs(batch, d, N, 1, torch.bfloat16, seed=21)
     state = torch.randn((batch, d, N), device=DEV)
     before = state.clone()
-    monkeypatch.setenv("SSM_FAULT", "step")
-    monkeypatch.setenv("SSM_LOOKBACK_TIMEOUT_MS", "100")
+    hooks.set("SSM_FAULT", "step")
+    hooks.set("SSM_LOOKBACK_TIMEOUT_MS", "100")
     ssm.step(state, inp["x"][0], inp["delta"][0], inp["A"], inp["B"][0], inp["C"][0], D=inp["D"], z=inp["z"][0],
              delta_bias=inp["bias"])
     assert ssm.ssm_step_check() == ssm.SSM_ERR_TIMEOUT
     assert torch.equal(state, before)
     assert ssm.ssm_step_check() == ssm.SSM_OK  # the check cleared the word
-    monkeypatch.delenv("SSM_FAULT")
+    hooks.unset("SSM_FAULT")
     out = ssm.step(state, inp["x"][0], inp["delta"][0], inp["A"], inp["B"][0], inp["C"][0], D=inp["D"],
                    z=inp["z"][0], delta_bias=inp["bias"])
     ref_out, ref_state = oracle.step(to_np(before), inp["x"][0], inp["delta"][0], inp["A"], inp["B"][0],

@@ -52,9 +52,9 @@ def test_noalloc_matches_workspace_call_twice(shape):
         assert rel_err(to_np(fs), to_np(ref_fs)) <= tol, f"call {call}"
 
 
-def test_noalloc_refuses_scratch_beyond_the_static_array(monkeypatch):
+def test_noalloc_refuses_scratch_beyond_the_static_array(hooks):
     """A forced split into many chunks needs more scratch than the static array holds."""
-    monkeypatch.setenv("SSM_FORCE_CHUNKS", "4096")
+    hooks.set("SSM_FORCE_CHUNKS", "4096")
     b, d, N, L = 1, 1024, 16, 1 << 17
     need = ssm.ssm_scan_workspace_bytes(b, d, N, L, torch.bfloat16)
     assert need > ssm.SSM_NOALLOC_SCRATCH_BYTES
