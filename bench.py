@@ -721,8 +721,8 @@ def run_profile_case(args):
     dev = torch.device("cuda", 0)
     if args.only == "scan":
         base = W.SCAN_SHAPES[args.workload]
-        shape = W.ScanShape(base.name, base.batch, args.dinner or base.d_inner, base.d_state, args.seqlen or base.seqlen,
-                            base.dtype)
+        shape = W.ScanShape(base.name, args.batch or base.batch, args.dinner or base.d_inner, base.d_state,
+                            args.seqlen or base.seqlen, base.dtype)
         inp = W.scan_inputs(shape, device=dev, seed=0)
         out = torch.empty_like(inp["u"])
         ws = torch.empty(max(16, ssm.ssm_scan_workspace_bytes(shape.batch, shape.d_inner, shape.d_state,
@@ -872,6 +872,8 @@ def main(argv=None):
                     help="profiling aid: run only the scan, the decode step, the Conv1D or the backward (no JSON line)")
     ap.add_argument("--seqlen", type=int, default=None,
                     help="profiling aid: scan another sequence length of the same workload")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="profiling aid: scan another batch size of the same workload")
     ap.add_argument("--dinner", type=int, default=None,
                     help="profiling aid: scan another number of channels of the same workload")
     ap.add_argument("--workload", choices=sorted(W.SCAN_SHAPES) + sorted(W.SSD_SHAPES), default=WORKLOAD,

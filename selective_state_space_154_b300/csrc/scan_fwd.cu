@@ -565,8 +565,8 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
     const int64_t row_slots = (int64_t)sms * 4 * kRowsPerRowCta;
     if (rows >= row_slots || a.L >= 65536 || rows * (a.L / kMinRowChunk) >= row_slots) kind = kScanRows;
   }
-  // The streamed row kernel (tensor-copied stages; bf16, 16 states, 16-byte aligned
-  // rows) is taken only when asked for: measured slower than the row kernel so far.
+  // bf16, 16 states, 16-byte aligned rows, L a multiple of 8: the streamed row kernel
+  if (kind == kScanRows && stream_supported(a)) kind = kScanStream;
   if (knobs.force_kind >= 0) {
     const bool ok = knobs.force_kind == kScanTiles || (knobs.force_kind == kScanRows && a.N <= 16) ||
                     (knobs.force_kind == kScanStream && stream_supported(a));
@@ -577,17 +577,17 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
     // CTAs of 512 rows (one per SM) over wide layers, else 128 (three per SM)
     const int rb = knobs.stream_rows == 128 || (knobs.stream_rows != 512 && a.d_inner < 512) ? 128 : 512;
     const int occ = rb == 512 ? 1 : 3;
-    pl.stage_tokens = knobs.stream_stage_tokens == 8 ? 8 : 16;
     pl.npad = 16;
     pl.groups = 1;
     pl.threads = rb + 32;
     pl.rows_per_cta = rb;
     pl.ctiles = (int)((a.d_inner + rb - 1) / rb);
-    pl.smem_bytes = stream_smem_bytes_for(rb, pl.stage_tokens);
+    pl.smem_bytes = stream_smem_bytes_for(rb);
     const int64_t items = a.batch * pl.ctiles;
-    const int64_t nch = pick_chunks(items, (int64_t)sms * occ, a.L, kMinRowChunk, pl.stage_tokens, knobs.force_chunks);
+    const int64_t nch =
+        pick_chunks(items, (int64_t)sms * occ, a.L, kMinRowChunk, kStreamTokensPerStage, knobs.force_chunks);
     int64_t clen = (a.L + nch - 1) / nch;
-    clen = (clen + pl.stage_tokens - 1) / pl.stage_tokens * pl.stage_tokens;
+    clen = (clen + kStreamTokensPerStage - 1) / kStreamTokensPerStage * kStreamTokensPerStage;
     pl.chunk_len = clen;
     pl.nchunks = (int)((a.L + clen - 1) / clen);
     size_t total = 0;

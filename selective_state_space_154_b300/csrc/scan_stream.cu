@@ -5,14 +5,16 @@
 // and Mamba blockのarchitecture).  Organisation:
 //  * one thread per (batch, channel) row holds the row's 16 states, A and 1/A in
 //    registers; the readout Σ_n C_n h_n needs no other thread;
-//  * a CTA owns RB rows of one batch over one chunk of the sequence.  One producer
-//    warp streams the chunk through shared memory in stages of TS = 32 (or 16) tokens
-//    with tensor (TMA) copies: per stage an [RB rows × 2·TS bytes] tile of each of u,
-//    Δraw and z (swizzled, so that lanes reading 8 bytes of their own rows are
-//    conflict-free) and the [TS tokens × 16] tiles of B and C, which it converts to
-//    fp32 once for all rows.  Completion is counted in bytes on a "full" mbarrier per
-//    stage; each consumer warp releases a stage on an "empty" mbarrier.  Consumer
-//    warps never wait for one another;
+//  * a CTA owns RB rows of one batch over one chunk of the sequence, walked in stages
+//    of 32 tokens, and no warp ever waits for another warp's rows:
+//      - each warp copies its own 32 rows' u, Δraw and z tiles (64 bytes of a row per
+//        tensor, four lanes per row) into a double buffer of its own with cp.async, one
+//        stage ahead, and writes its outputs back the same way: in place of u in shared
+//        memory, then out in 64-byte row segments;
+//      - B and C of a stage, shared by all rows, come by tensor (TMA) copy into a ring of
+//        four stages; the warp that releases a stage last refills it, and every warp
+//        converts a share of each stage to fp32 two stages before its use (an mbarrier
+//        counts the shares);
 //  * the step size enters the exponent in base 2: Δ' = log2(1 + 2^{(Δraw+bias)·log2 e})
 //    = Δ / ln 2, so Ā_n = 2^{Δ'·A_n} with no further scaling, and Σ Δ' is the chunk's
 //    decay exponent;
@@ -20,12 +22,12 @@
 //    Selective Scanは選択機構そのものではない).  Every chunk first scans from h = 0
 //    keeping S = ΣΔ', then each warp publishes (S, h_local) for its 32 rows and
 //    combines those of all preceding chunks, in a fixed order, into its carried-in
-//    state h_in; its end state is 2^{A S}·h_in + h_local.  The chunk's first blocks, those whose
-//    outputs h_in still changes (2^{A_n S} ≥ 2^-12 for the slowest-decaying state, bf16
-//    outputs), are not written by the first pass: a second pass scans them again from
-//    h_in and writes them, so every output is rounded once.  The number of stages the
-//    second pass needs is known from the first pass, so the producer streams them
-//    while the consumers look back.
+//    state h_in; its end state is 2^{A S}·h_in + h_local.  The chunk's first blocks,
+//    those whose outputs h_in still changes (2^{A_n S} ≥ 2^-12 for the slowest-decaying
+//    state, bf16 outputs), are not written by the first pass: a second pass scans them
+//    again from h_in and writes them, so every output is rounded once.  How many
+//    stages the second pass needs is known during the first, so its copies start
+//    before the carry is combined.
 #include "async_copy.cuh"
 #include "ssm_device.cuh"
 #include "ssm_internal.h"
@@ -83,25 +85,20 @@ constexpr int NS = 16;        // states per row
 // rows per tensor copy of a row tile: the CTA's rows, at most 256 (the largest box)
 __host__ __device__ constexpr int box_rows(int rb) { return rb < 256 ? rb : 256; }
 
-// Stage geometry: TS tokens per stage, NSTG = 64 / TS stages in the ring (64 tokens
-// of every row in shared memory).  A stage's B and C are converted to fp32 kAhead
-// stages before its use.  TS = 16: 32-byte rows with the 32-byte swizzle; TS = 8:
-// 16-byte rows, no swizzle.
-template <int TS_>
-struct Geo {
-  static constexpr int NSTG = 64 / TS_;
-  static constexpr int kAhead = NSTG / 2;
-  static constexpr int kRowBytes = TS_ * 2;
-  // 16-byte granule g of row r of a swizzled tile: the TMA swizzle of R-byte rows
-  // XORs the granule bits of the address with the bits above bit 7, i.e. with
-  // (r · R / 128) mod (R / 16)
-  __device__ static __forceinline__ int swz(int r, int g) {
-    return g ^ ((r * kRowBytes / 128) & (kRowBytes / 16 - 1));
-  }
-};
+// Stage geometry: TS = 32 tokens per stage.  Each warp double-buffers its own 32 rows'
+// tiles (64 bytes of a row per tensor and stage, copied by the warp itself); B and C
+// of a stage, shared by all rows, sit in a ring of NB = 4 stages filled by tensor
+// copies and converted to fp32 kAhead = 2 stages before their use.
+constexpr int TS = kStreamTokensPerStage;
+constexpr int NB = 4;
+constexpr int kAhead = 2;
+constexpr int kRowBytes = TS * 2;
+// 16-byte granule g of row r of a tile: XOR-swizzled by (r / 2) mod 4, so that eight
+// lanes reading the same granule of eight consecutive rows hit different banks
+__device__ __forceinline__ int swz(int r, int g) { return g ^ ((r >> 1) & 3); }
 
 struct StreamParams {
-  CUtensorMap tm_u, tm_d, tm_z, tm_b, tm_c;
+  CUtensorMap tm_b, tm_c;
   ScanArgs a;
   int rtiles, nchunks;
   int64_t chunk_len;
@@ -111,23 +108,22 @@ struct StreamParams {
 };
 
 // Shared memory of one CTA (the dynamic allocation is aligned up to 1024 bytes).
-template <int RB, int TS>
+template <int RB>
 struct StreamSmem {
-  using G = Geo<TS>;
-  uint8_t tile[G::NSTG][3][RB * G::kRowBytes];  // [stage][u|Δraw|z][row][TS tokens], swizzled
-  uint16_t bc_raw[G::NSTG][2][TS * NS];         // [stage][B|C][token][state] bf16
-  float bcf[G::NSTG][TS][2 * NS];               // [stage][token][B 0..15 | C 0..15] fp32
-  uint64_t full[G::NSTG];  // the stage's tensor copies landed (bytes counted)
-  uint64_t conv[G::NSTG];  // every warp converted its share of the stage's B and C
-  uint64_t settled;        // every warp knows how far pass two must go
-  int done[G::NSTG];       // warps that released the stage's buffer
-  int n2;                  // stages of the second pass (max over warps)
-  int issued;              // stages issued so far (the last one + 1)
-  int ticket;              // this CTA's work item
+  uint8_t tile[2][3][RB * kRowBytes];  // [buffer][u|Δraw|z][row][TS tokens], swizzled; warp w owns rows 32w..32w+31
+  uint16_t bc_raw[NB][2][TS * NS];     // [stage][B|C][token][state] bf16
+  float bcf[NB][TS][2 * NS];           // [stage][token][B 0..15 | C 0..15] fp32
+  uint64_t full[NB];  // the stage's B and C copies landed (bytes counted)
+  uint64_t conv[NB];  // every warp converted its share of the stage's B and C
+  uint64_t settled;   // every warp knows how far pass two must go
+  int done[NB];       // warps that released the stage's B and C
+  int n2;             // stages of the second pass (max over warps)
+  int issued;         // B/C stages issued so far (the last one + 1)
+  int ticket;         // this CTA's work item
 };
-template <int RB, int TS>
+template <int RB>
 constexpr size_t stream_smem_bytes() {
-  return sizeof(StreamSmem<RB, TS>) + 1024;
+  return sizeof(StreamSmem<RB>) + 1024;
 }
 
 __device__ __forceinline__ float bf_lo(unsigned w) { return __uint_as_float(w << 16); }
@@ -164,52 +160,68 @@ struct RowConst {
   bool row_ok;
 };
 
-// What every warp knows about the CTA's ring: its chunk's tokens and stage counts.
-// Stage k < n1 is pass one's stage k, stage n1 + i pass two's stage i (tokens from
-// the chunk start again).  The first min(NSTG, n1) stages of pass two are issued
-// before pass two's length is known (every chunk after the first re-scans at least
-// its first stage); the rest once it is.
+// What every warp knows about its CTA's stages: the chunk's tokens and stage counts.
+// Stage k < n1 is pass one's stage k, stage n1 + i pass two's stage i (tokens from the
+// chunk start again).  Copies for the first stages of pass two are issued before pass
+// two's length is known (every chunk after the first re-scans at least one stage);
+// later ones once it is.
 struct Ring {
   const StreamParams* p;
   unsigned long long deadline;
-  int c0, b, tc0, n1;
-  int spec_end;  // stages that may be issued without knowing pass two's length
+  int c0, b, tc0, tc1, n1;
+  int spec_rows;  // row-tile stages a warp may copy without knowing pass two's length
+  int spec_bc;    // B/C stages that may be issued without knowing it
 };
 
-// Issue the tensor copies of stage j (one thread).
-template <int RB, int TS, bool HAS_Z>
-__device__ __forceinline__ void ring_issue(StreamSmem<RB, TS>& sm, const Ring& g, int j) {
-  using G = Geo<TS>;
-  const int s = j % G::NSTG;
-  const int t0 = g.tc0 + (j < g.n1 ? j : j - g.n1) * TS;
-  const StreamParams& p = *g.p;
+__device__ __forceinline__ int stage_t0(const Ring& g, int k) { return g.tc0 + (k < g.n1 ? k : k - g.n1) * TS; }
+
+// This warp's 32 rows of stage k's u, Δraw, z tiles into row buffer k % 2, one
+// cp.async group (four lanes per 64-byte row segment; rows past d_inner and tokens
+// past the sequence are zero-filled).
+template <int RB, bool HAS_Z>
+__device__ __forceinline__ void rows_issue(StreamSmem<RB>& sm, const Ring& g, int k, int warp, int lane) {
+  const ScanArgs& a = g.p->a;
+  const int t0 = stage_t0(g, k);
+  const int gi = lane & 3;
+  const int t = t0 + gi * 8;
+  const bool t_ok = t < g.tc1;  // a granule is all in or all out (L % 8 == 0)
+  const __nv_bfloat16* srcs[3] = {static_cast<const __nv_bfloat16*>(a.u), static_cast<const __nv_bfloat16*>(a.delta),
+                                  static_cast<const __nv_bfloat16*>(a.z)};
   constexpr int ntens = HAS_Z ? 3 : 2;
-  const uint32_t fb = ac::smem_u32(&sm.full[s]);
-  ac::mbar_arrive_expect_tx(fb, (uint32_t)(ntens * RB * G::kRowBytes + 2 * TS * NS * 2));
-  ac::tma_load_3d(ac::smem_u32(sm.bc_raw[s][0]), &p.tm_b, 0, t0, g.b, fb);
-  ac::tma_load_3d(ac::smem_u32(sm.bc_raw[s][1]), &p.tm_c, 0, t0, g.b, fb);
-  const CUtensorMap* maps[3] = {&p.tm_u, &p.tm_d, &p.tm_z};
-  constexpr int kBox = box_rows(RB);
 #pragma unroll
   for (int w = 0; w < ntens; ++w) {
 #pragma unroll
-    for (int hb = 0; hb < RB / kBox; ++hb)
-      ac::tma_load_3d(ac::smem_u32(sm.tile[s][w] + hb * kBox * G::kRowBytes), maps[w], t0, g.c0 + hb * kBox, g.b,
-                      fb);
+    for (int i = 0; i < 4; ++i) {
+      const int r = 32 * warp + (lane >> 2) + 8 * i;  // row within the CTA
+      const int c = g.c0 + r;
+      const bool ok = t_ok && c < a.d_inner;
+      const __nv_bfloat16* src = srcs[w] + ((int64_t)g.b * a.d_inner + (ok ? c : 0)) * a.L + (ok ? t : 0);
+      cp_async16(sm.tile[k & 1][w] + r * kRowBytes + swz(r, gi) * 16, src, ok ? 16 : 0);
+    }
   }
+}
+
+// Issue the tensor copies of stage j's B and C (one thread).
+template <int RB>
+__device__ __forceinline__ void bc_issue(StreamSmem<RB>& sm, const Ring& g, int j) {
+  const int s = j % NB;
+  const int t0 = stage_t0(g, j);
+  const StreamParams& p = *g.p;
+  const uint32_t fb = ac::smem_u32(&sm.full[s]);
+  ac::mbar_arrive_expect_tx(fb, (uint32_t)(2 * TS * NS * 2));
+  ac::tma_load_3d(ac::smem_u32(sm.bc_raw[s][0]), &p.tm_b, 0, t0, g.b, fb);
+  ac::tma_load_3d(ac::smem_u32(sm.bc_raw[s][1]), &p.tm_c, 0, t0, g.b, fb);
   atomicMax(&sm.issued, j + 1);
 }
 
 // This warp's share of stage j's B and C to fp32: [B|C][token][state] -> [token][B | C].
-template <int RB, int TS>
-__device__ __forceinline__ void ring_convert(StreamSmem<RB, TS>& sm, const Ring& g, int j, int warp, int lane,
-                                             int& err) {
-  using G = Geo<TS>;
+template <int RB>
+__device__ __forceinline__ void bc_convert(StreamSmem<RB>& sm, const Ring& g, int j, int warp, int lane, int& err) {
   constexpr int NW = RB / 32;
-  constexpr int kWords = TS * NS;       // 32-bit words of B and C together
-  constexpr int kShare = kWords / NW;   // words per warp
-  const int s = j % G::NSTG;
-  if (!ac::mbar_wait(ac::smem_u32(&sm.full[s]), (uint32_t)(j / G::NSTG) & 1u, g.deadline)) err = 1;
+  constexpr int kWords = TS * NS;      // 32-bit words of B and C together
+  constexpr int kShare = kWords / NW;  // words per warp
+  const int s = j % NB;
+  if (!ac::mbar_wait(ac::smem_u32(&sm.full[s]), (uint32_t)(j / NB) & 1u, g.deadline)) err = 1;
   const unsigned* raw = reinterpret_cast<const unsigned*>(sm.bc_raw[s][0]);
 #pragma unroll
   for (int q = 0; q < (kShare + 31) / 32; ++q) {
@@ -225,62 +237,66 @@ __device__ __forceinline__ void ring_convert(StreamSmem<RB, TS>& sm, const Ring&
   if (lane == 0) ac::mbar_arrive(ac::smem_u32(&sm.conv[s]));
 }
 
-// Whether stage j is ever issued: pass one, the first stages of pass two, or pass
-// two's remaining stages once its length n2 (< 0: unknown) is known.
-__device__ __forceinline__ bool ring_has(const Ring& g, int j, int n2) {
-  return j < g.spec_end || (n2 >= 0 && j < g.n1 + n2);
+// Whether stage j is ever used: pass one, the first stages of pass two, or pass two's
+// remaining stages once its length n2 (< 0: unknown) is known.
+__device__ __forceinline__ bool stage_has(int j, int spec_end, int n1, int n2) {
+  return j < spec_end || (n2 >= 0 && j < n1 + n2);
 }
 
-// After this warp finished stage k: release its buffer (the warp releasing it last
-// issues the copies of stage k + NSTG into it) and convert its share of stage k + kAhead.
-template <int RB, int TS, bool HAS_Z>
-__device__ __forceinline__ void ring_advance(StreamSmem<RB, TS>& sm, const Ring& g, int k, int n2, int warp, int lane,
-                                             int& err) {
-  using G = Geo<TS>;
+// After this warp finished stage k: copy its rows of stage k + 2 into the row buffer
+// just freed; release stage k's B and C (the warp releasing them last issues the copies
+// of stage k + NB into that slot) and convert its share of stage k + kAhead.
+template <int RB, bool HAS_Z>
+__device__ __forceinline__ void stage_advance(StreamSmem<RB>& sm, const Ring& g, int k, int n2, int warp, int lane,
+                                              int& err) {
   constexpr int NW = RB / 32;
-  const int s = k % G::NSTG;
+  if (stage_has(k + 2, g.spec_rows, g.n1, n2)) rows_issue<RB, HAS_Z>(sm, g, k + 2, warp, lane);
+  cp_async_commit();  // one group per stage, empty or not, keeps the wait counts fixed
+  const int s = k % NB;
   __syncwarp();
   if (lane == 0) {
-    __threadfence_block();  // this warp's reads of the buffer precede its release
+    __threadfence_block();  // this warp's reads of the slot precede its release
     if (atomicAdd(&sm.done[s], 1) == NW - 1) {
       sm.done[s] = 0;
-      // stage k + NSTG > k ≥ n1 only once pass two runs, when n2 is known to every warp
-      if (ring_has(g, k + G::NSTG, n2)) ring_issue<RB, TS, HAS_Z>(sm, g, k + G::NSTG);
+      // stage k + NB > k ≥ n1 only once pass two runs, when n2 is known to every warp
+      if (stage_has(k + NB, g.spec_bc, g.n1, n2)) bc_issue<RB>(sm, g, k + NB);
     }
   }
-  if (ring_has(g, k + G::kAhead, n2)) ring_convert<RB, TS>(sm, g, k + G::kAhead, warp, lane, err);
+  if (stage_has(k + kAhead, g.spec_bc, g.n1, n2)) bc_convert<RB>(sm, g, k + kAhead, warp, lane, err);
 }
 
-// One pass of a thread over ring stages [k0, k0 + nst), tokens from t_lo, writing the
+// One pass of a thread over stages [k0, k0 + nst), tokens from t_lo, writing the
 // 4-token groups that P selects.  h: the row's states; S: ΣΔ' since the chunk start
 // (P != kAll), with Kahan compensation `comp`.  In pass one (kSettled), lane 0
 // publishes the warp's stage count for pass two as soon as it is known.
-template <int RB, int TS, bool HAS_Z, int P, bool PRECISE>
-__device__ __forceinline__ void consume(StreamSmem<RB, TS>& sm, const Ring& g, const RowConst& c,
-                                        __nv_bfloat16* orow, int r, int warp, int lane, int k0, int nst, int t_lo,
-                                        int t_hi, int n2, float (&h)[NS], float& S, float& comp, int& err) {
-  using G = Geo<TS>;
+template <int RB, bool HAS_Z, int P, bool PRECISE>
+__device__ __forceinline__ void consume(StreamSmem<RB>& sm, const Ring& g, const RowConst& c, __nv_bfloat16* outb,
+                                        int r, int warp, int lane, int k0, int nst, int n2, float (&h)[NS],
+                                        float& S, float& comp, int& err) {
   constexpr float kStop = corr_stop_log2<__nv_bfloat16>();
+  const int t_lo = g.tc0, t_hi = g.tc1;
   const int t_valid = c.row_ok ? t_hi : t_lo;  // rows past d_inner compute nothing useful
   bool published = P != kSettled;
 #pragma unroll 1
   for (int kk = 0; kk < nst; ++kk) {
     const int k = k0 + kk;
-    const int s = k % G::NSTG;
-    const uint32_t ph = (uint32_t)(k / G::NSTG) & 1u;
-    if (!ac::mbar_wait(ac::smem_u32(&sm.full[s]), ph, g.deadline)) err = 1;
+    const int s = k % NB;
+    const uint32_t ph = (uint32_t)(k / NB) & 1u;
+    cp_async_wait<1>();  // this warp's rows of stage k (stage k + 1's may still be in flight)
+    __syncwarp();
     if (!ac::mbar_wait(ac::smem_u32(&sm.conv[s]), ph, g.deadline)) err = 1;
     const int ts = t_lo + kk * TS;
-    const uint2* tu = reinterpret_cast<const uint2*>(sm.tile[s][0] + r * G::kRowBytes);
-    const uint2* td = reinterpret_cast<const uint2*>(sm.tile[s][1] + r * G::kRowBytes);
-    const uint2* tz = reinterpret_cast<const uint2*>(sm.tile[s][2] + r * G::kRowBytes);
+    uint2* tu = reinterpret_cast<uint2*>(sm.tile[k & 1][0] + r * kRowBytes);  // outputs replace u in place
+    const uint2* td = reinterpret_cast<const uint2*>(sm.tile[k & 1][1] + r * kRowBytes);
+    const uint2* tz = reinterpret_cast<const uint2*>(sm.tile[k & 1][2] + r * kRowBytes);
+    unsigned wmask = 0;  // 4-token groups of this stage whose outputs this row writes
 #pragma unroll 1
     for (int q4 = 0; q4 < TS / 4; ++q4) {
       // four tokens per iteration: 8 bytes of each of u, Δraw, z (half a swizzled granule)
       const int t = ts + q4 * 4;
       const bool write_blk =
           P == kAll || (P == kSettled ? !(c.a2max * S > kStop) : c.a2max * S > kStop - 1.f);
-      const int gi = G::swz(r, q4 >> 1) * 2 + (q4 & 1);  // 8-byte unit of the row
+      const int gi = swz(r, q4 >> 1) * 2 + (q4 & 1);  // 8-byte unit of the row
       const uint2 wu = tu[gi], wd = td[gi];
       uint2 wz = make_uint2(0u, 0u);
       if (HAS_Z) wz = tz[gi];
@@ -356,14 +372,26 @@ __device__ __forceinline__ void consume(StreamSmem<RB, TS>& sm, const Ring& g, c
         comp = (tk - S) - yk;
         S = tk;
       }
-      if (c.row_ok && t < t_hi && write_blk) {
-        if (t + 4 <= t_hi) {
-          *reinterpret_cast<uint2*>(orow + t) = make_uint2(packed0, packed1);
-        } else {
-          unsigned short* o16 = reinterpret_cast<unsigned short*>(orow);
+      tu[gi] = make_uint2(packed0, packed1);
+      if (c.row_ok && t < t_hi && write_blk) wmask |= 1u << q4;  // groups lie wholly inside [0, L) (L % 8 == 0)
+    }
+    // the stage's outputs leave in 64-byte row segments, four lanes per row (as the
+    // inputs arrive): far fewer distinct rows per store than one row per lane
+    __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (t + i < t_hi) o16[t + i] = (unsigned short)((i < 2 ? packed0 : packed1) >> (16 * (i & 1)));
+    for (int i = 0; i < 4; ++i) {
+      const int rr = 32 * warp + (lane >> 2) + 8 * i;
+      const int gg = lane & 3;  // 16-byte granule: 4-token groups 2 gg and 2 gg + 1
+      const unsigned bits = (__shfl_sync(0xffffffffu, wmask, rr & 31) >> (2 * gg)) & 3u;
+      if (bits) {
+        const uint4 v = *reinterpret_cast<const uint4*>(sm.tile[k & 1][0] + rr * kRowBytes + swz(rr, gg) * 16);
+        __nv_bfloat16* dst = outb + (int64_t)rr * g.p->a.L + ts + gg * 8;
+        if (bits == 3u) {
+          *reinterpret_cast<uint4*>(dst) = v;
+        } else if (bits == 1u) {
+          *reinterpret_cast<uint2*>(dst) = make_uint2(v.x, v.y);
+        } else {
+          *reinterpret_cast<uint2*>(dst + 4) = make_uint2(v.z, v.w);
         }
       }
     }
@@ -378,7 +406,7 @@ __device__ __forceinline__ void consume(StreamSmem<RB, TS>& sm, const Ring& g, c
         }
       }
     }
-    ring_advance<RB, TS, HAS_Z>(sm, g, k, n2, warp, lane, err);
+    stage_advance<RB, HAS_Z>(sm, g, k, n2, warp, lane, err);
   }
   if (!published && lane == 0) {  // never settled: pass two covers the whole chunk
     atomicMax(&sm.n2, nst);
@@ -395,19 +423,18 @@ struct StreamCta {
   static constexpr int kMaxRegs = 128;
 };
 
-template <int RB, int TS, bool HAS_Z, bool PRECISE>
-__device__ __forceinline__ void row_program(StreamSmem<RB, TS>& sm, const StreamParams& p, const Ring& g,
-                                            const RowConst& cs, __nv_bfloat16* orow, float (&h)[NS], int chunk,
+template <int RB, bool HAS_Z, bool PRECISE>
+__device__ __forceinline__ void row_program(StreamSmem<RB>& sm, const StreamParams& p, const Ring& g,
+                                            const RowConst& cs, __nv_bfloat16* outb, float (&h)[NS], int chunk,
                                             int rem, int per_chunk, int64_t row, int r, int warp, int lane,
-                                            int tc1, int& err) {
+                                            int& err) {
   constexpr int NW = RB / 32;
   const int n1 = g.n1;
   float S = 0.f, comp = 0.f;
   if (chunk == 0)
-    consume<RB, TS, HAS_Z, kAll, PRECISE>(sm, g, cs, orow, r, warp, lane, 0, n1, g.tc0, tc1, 0, h, S, comp, err);
+    consume<RB, HAS_Z, kAll, PRECISE>(sm, g, cs, outb, r, warp, lane, 0, n1, 0, h, S, comp, err);
   else
-    consume<RB, TS, HAS_Z, kSettled, PRECISE>(sm, g, cs, orow, r, warp, lane, 0, n1, g.tc0, tc1, -1, h, S, comp,
-                                              err);
+    consume<RB, HAS_Z, kSettled, PRECISE>(sm, g, cs, outb, r, warp, lane, 0, n1, -1, h, S, comp, err);
 
   // ---------------- carry between chunks ----------------
   // Each warp publishes its rows' aggregate (S, h from h = 0; the first chunk's h is
@@ -478,25 +505,23 @@ __device__ __forceinline__ void row_program(StreamSmem<RB, TS>& sm, const Stream
     if (!ac::mbar_wait(ac::smem_u32(&sm.settled), 0u, g.deadline)) err = 1;
     const int n2 = *reinterpret_cast<volatile int*>(&sm.n2);
     float S2 = 0.f, comp2 = 0.f;
-    consume<RB, TS, HAS_Z, kUnsettled, PRECISE>(sm, g, cs, orow, r, warp, lane, n1, n2, g.tc0, tc1, n2, hin, S2,
-                                                comp2, err);
+    consume<RB, HAS_Z, kUnsettled, PRECISE>(sm, g, cs, outb, r, warp, lane, n1, n2, n2, hin, S2, comp2, err);
   }
 }
 
-template <int RB, int TS, bool HAS_Z>
+template <int RB, bool HAS_Z>
 __global__ void __launch_bounds__(StreamCta<RB>::kThreads) __maxnreg__(StreamCta<RB>::kMaxRegs)
     scan_stream_kernel(const __grid_constant__ StreamParams p) {
-  using G = Geo<TS>;
   constexpr int NW = RB / 32;
   extern __shared__ unsigned char smem_raw[];
   // aligned by offsetting the shared array itself, so that the compiler keeps
   // shared-memory (32-bit) addressing
-  StreamSmem<RB, TS>& sm = *reinterpret_cast<StreamSmem<RB, TS>*>(
+  StreamSmem<RB>& sm = *reinterpret_cast<StreamSmem<RB>*>(
       smem_raw + ((1024u - (ac::smem_u32(smem_raw) & 1023u)) & 1023u));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < G::NSTG; ++s) {
+    for (int s = 0; s < NB; ++s) {
       ac::mbar_init(ac::smem_u32(&sm.full[s]), 1);  // the issuing thread's arrival + the copies' bytes
       ac::mbar_init(ac::smem_u32(&sm.conv[s]), NW);
       sm.done[s] = 0;
@@ -518,21 +543,24 @@ __global__ void __launch_bounds__(StreamCta<RB>::kThreads) __maxnreg__(StreamCta
   g.b = rem / p.rtiles;
   g.c0 = (rem % p.rtiles) * RB;
   g.tc0 = (int)min((int64_t)p.a.L, (int64_t)chunk * p.chunk_len);
-  const int tc1 = (int)min((int64_t)p.a.L, (int64_t)g.tc0 + p.chunk_len);
-  g.n1 = (tc1 - g.tc0 + TS - 1) / TS;
-  g.spec_end = g.n1 + (chunk > 0 ? min(G::NSTG, g.n1) : 0);
+  g.tc1 = (int)min((int64_t)p.a.L, (int64_t)g.tc0 + p.chunk_len);
+  g.n1 = (g.tc1 - g.tc0 + TS - 1) / TS;
+  g.spec_rows = g.n1 + (chunk > 0 ? min(2, g.n1) : 0);
+  g.spec_bc = g.n1 + (chunk > 0 ? min(NB, g.n1) : 0);
   int err = 0;
 
-  // fill the ring, then every warp converts its share of the first kAhead stages
+  // the first two stages of this warp's rows; the B/C ring filled; every warp converts
+  // its share of the first kAhead stages
+  for (int k = 0; k < 2; ++k) {
+    if (k < g.spec_rows) rows_issue<RB, HAS_Z>(sm, g, k, warp, lane);
+    cp_async_commit();
+  }
   if (threadIdx.x == 0) {
-    ac::prefetch_tensormap(&p.tm_u);
-    ac::prefetch_tensormap(&p.tm_d);
-    if (HAS_Z) ac::prefetch_tensormap(&p.tm_z);
     ac::prefetch_tensormap(&p.tm_b);
     ac::prefetch_tensormap(&p.tm_c);
-    for (int j = 0; j < G::NSTG && j < g.spec_end; ++j) ring_issue<RB, TS, HAS_Z>(sm, g, j);
+    for (int j = 0; j < NB && j < g.spec_bc; ++j) bc_issue<RB>(sm, g, j);
   }
-  for (int j = 0; j < G::kAhead && j < g.spec_end; ++j) ring_convert<RB, TS>(sm, g, j, warp, lane, err);
+  for (int j = 0; j < kAhead && j < g.spec_bc; ++j) bc_convert<RB>(sm, g, j, warp, lane, err);
 
   // ---------------- thread r owns row c0 + r ----------------
   const int r = threadIdx.x;
@@ -541,7 +569,8 @@ __global__ void __launch_bounds__(StreamCta<RB>::kThreads) __maxnreg__(StreamCta
   cs.row_ok = r < nrows;
   const int64_t ch = g.c0 + (cs.row_ok ? r : 0);
   const int64_t row = (int64_t)g.b * p.a.d_inner + ch;
-  __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.a.out) + row * p.a.L;
+  // output of the CTA's first row (rows past d_inner are never stored)
+  __nv_bfloat16* outb = static_cast<__nv_bfloat16*>(p.a.out) + ((int64_t)g.b * p.a.d_inner + g.c0) * p.a.L;
   float h[NS];
   cs.precise = false;
   cs.a2max = -INFINITY;
@@ -561,44 +590,36 @@ __global__ void __launch_bounds__(StreamCta<RB>::kThreads) __maxnreg__(StreamCta
   cs.bl2 = (cs.row_ok && p.a.bias) ? p.a.bias[ch] * kLog2e : 0.f;
 
   if (cs.precise)
-    row_program<RB, TS, HAS_Z, true>(sm, p, g, cs, orow, h, chunk, rem, per_chunk, row, r, warp, lane, tc1, err);
+    row_program<RB, HAS_Z, true>(sm, p, g, cs, outb, h, chunk, rem, per_chunk, row, r, warp, lane, err);
   else
-    row_program<RB, TS, HAS_Z, false>(sm, p, g, cs, orow, h, chunk, rem, per_chunk, row, r, warp, lane, tc1, err);
+    row_program<RB, HAS_Z, false>(sm, p, g, cs, outb, h, chunk, rem, per_chunk, row, r, warp, lane, err);
 
   // copies issued ahead of a pass two shorter than the ring, never consumed, must land
   // before the CTA exits
+  cp_async_wait<0>();
   __syncthreads();
   if (threadIdx.x == 0) {
     const int issued = sm.issued;
-    for (int j = issued - G::NSTG < 0 ? 0 : issued - G::NSTG; j < issued; ++j)
-      if (!ac::mbar_wait(ac::smem_u32(&sm.full[j % G::NSTG]), (uint32_t)(j / G::NSTG) & 1u,
-                         g.deadline + 1000000000ull))
+    for (int j = issued - NB < 0 ? 0 : issued - NB; j < issued; ++j)
+      if (!ac::mbar_wait(ac::smem_u32(&sm.full[j % NB]), (uint32_t)(j / NB) & 1u, g.deadline + 1000000000ull))
         err = 1;
   }
   if (err && p.ws.hdr) atomicOr(p.ws.hdr + 1, kErrTimeout);
 }
 
-template <int RB, int TS, bool HAS_Z>
+template <int RB, bool HAS_Z>
 cudaError_t stream_launch_t(const StreamParams& p, int grid, cudaStream_t s) {
-  auto kern = scan_stream_kernel<RB, TS, HAS_Z>;
+  auto kern = scan_stream_kernel<RB, HAS_Z>;
   const cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stream_smem_bytes<RB, TS>());
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)stream_smem_bytes<RB>());
   if (e != cudaSuccess) return e;
-  kern<<<grid, StreamCta<RB>::kThreads, stream_smem_bytes<RB, TS>(), s>>>(p);
+  kern<<<grid, StreamCta<RB>::kThreads, stream_smem_bytes<RB>(), s>>>(p);
   return cudaGetLastError();
-}
-
-template <int RB, int TS>
-cudaError_t stream_launch_z(const StreamParams& p, bool has_z, int grid, cudaStream_t s) {
-  return has_z ? stream_launch_t<RB, TS, true>(p, grid, s) : stream_launch_t<RB, TS, false>(p, grid, s);
 }
 
 }  // namespace
 
-size_t stream_smem_bytes_for(int rb, int ts) {
-  if (ts == 8) return rb == 512 ? stream_smem_bytes<512, 8>() : stream_smem_bytes<128, 8>();
-  return rb == 512 ? stream_smem_bytes<512, 16>() : stream_smem_bytes<128, 16>();
-}
+size_t stream_smem_bytes_for(int rb) { return rb == 512 ? stream_smem_bytes<512>() : stream_smem_bytes<128>(); }
 
 StreamWs stream_ws_layout(unsigned char* ws, int64_t nchunks, int64_t items, int rb, size_t* total) {
   // [header][flags: nchunks × items × warps][aggregate h: nchunks × rows × 16][aggregate S: nchunks × rows]
@@ -645,32 +666,24 @@ cudaError_t scan_stream_launch(const ScanArgs& a, const ScanPlan& plan, cudaStre
   // one chunk: no workspace is required; if one is given its header takes the error word
   p.ws = stream_ws_layout(plan.nchunks > 1 ? a.ws : nullptr, plan.nchunks, a.batch * plan.ctiles, rb, &total);
   if (plan.nchunks == 1) p.ws.hdr = reinterpret_cast<unsigned*>(a.ws);
-  // tensor maps: u, Δraw, z as [batch][d_inner][L], B and C as [batch][L][16], bf16
-  const uint64_t L = (uint64_t)a.L, D = (uint64_t)a.d_inner, Bt = (uint64_t)a.batch;
-  const uint64_t dims_row[3] = {L, D, Bt}, str_row[2] = {L * 2, L * D * 2};
-  const int ts = plan.stage_tokens;
-  const uint32_t box_row[3] = {(uint32_t)ts, (uint32_t)box_rows(rb), 1};
+  // tensor maps of B and C as [batch][L][16] bf16 (tokens past L read as zero)
+  const uint64_t L = (uint64_t)a.L, Bt = (uint64_t)a.batch;
   const uint64_t dims_bc[3] = {(uint64_t)NS, L, Bt}, str_bc[2] = {NS * 2, L * NS * 2};
-  const uint32_t box_bc[3] = {(uint32_t)NS, (uint32_t)ts, 1};
-  const CUtensorMapSwizzle swz = ts == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  const uint32_t box_bc[3] = {(uint32_t)NS, (uint32_t)TS, 1};
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
   const auto promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
-  bool ok = encode_tensor_map(&p.tm_u, bf, 3, a.u, dims_row, str_row, box_row, swz, promo) &&
-            encode_tensor_map(&p.tm_d, bf, 3, a.delta, dims_row, str_row, box_row, swz, promo) &&
-            encode_tensor_map(&p.tm_b, bf, 3, a.B, dims_bc, str_bc, box_bc, CU_TENSOR_MAP_SWIZZLE_NONE, promo) &&
-            encode_tensor_map(&p.tm_c, bf, 3, a.C, dims_bc, str_bc, box_bc, CU_TENSOR_MAP_SWIZZLE_NONE, promo);
-  if (ok && a.z)
-    ok = encode_tensor_map(&p.tm_z, bf, 3, a.z, dims_row, str_row, box_row, swz, promo);
-  if (!ok) return cudaErrorInvalidValue;
+  if (!encode_tensor_map(&p.tm_b, bf, 3, a.B, dims_bc, str_bc, box_bc, none, promo) ||
+      !encode_tensor_map(&p.tm_c, bf, 3, a.C, dims_bc, str_bc, box_bc, none, promo))
+    return cudaErrorInvalidValue;
   if (plan.nchunks > 1) {
     const cudaError_t e = cudaMemsetAsync(a.ws, 0, p.ws.flags_bytes, stream);
     if (e != cudaSuccess) return e;
   }
   const int grid = (int)((int64_t)plan.nchunks * a.batch * plan.ctiles);
   const bool hz = a.z != nullptr;
-  if (ts == 8) return rb == 512 ? stream_launch_z<512, 8>(p, hz, grid, stream)
-                                : stream_launch_z<128, 8>(p, hz, grid, stream);
-  return rb == 512 ? stream_launch_z<512, 16>(p, hz, grid, stream) : stream_launch_z<128, 16>(p, hz, grid, stream);
+  if (rb == 512) return hz ? stream_launch_t<512, true>(p, grid, stream) : stream_launch_t<512, false>(p, grid, stream);
+  return hz ? stream_launch_t<128, true>(p, grid, stream) : stream_launch_t<128, false>(p, grid, stream);
 }
 
 }  // namespace ssm

@@ -46,7 +46,6 @@ RuntimeKnobs* load_knobs() {
     const int v = std::atoi(c);
     r->stream_rows = (v == 512 || v == 128) ? v : 0;
   }
-  if (const char* c = std::getenv("SSM_STREAM_TOKENS")) r->stream_stage_tokens = std::atoi(c);
   return r;
 }
 

@@ -40,7 +40,6 @@ struct ScanPlan {
   int nchunks;        // chunks along the sequence (1: no carry between chunks)
   size_t smem_bytes;  // dynamic shared memory per CTA
   size_t ws_flags_off, ws_agg_off, ws_bytes;  // workspace layout (0 bytes when nchunks == 1)
-  int stage_tokens;   // streamed row kernel: tokens per pipeline stage (16 or 8)
 };
 
 struct ScanArgs {
@@ -73,7 +72,6 @@ struct RuntimeKnobs {
   int bwd_chunks;                 // >0: sequence chunks of the backward (tests)
   bool fault_ssd;                 // test hook: the SSD output kernel's first wait never completes
   int stream_rows;                // >0: rows per CTA of the streamed row kernel (512, 256 or 128)
-  int stream_stage_tokens;        // 8: 8-token stages in the streamed row kernel (default 16)
 };
 RuntimeKnobs runtime_knobs();  // the test hooks as last loaded (first use, or ssm_test_hooks_reload)
 void reload_knobs();
@@ -96,7 +94,8 @@ struct StreamWs {
 StreamWs stream_ws_layout(unsigned char* ws, int64_t nchunks, int64_t items, int rows_per_cta, size_t* total);
 bool stream_supported(const ScanArgs& a);
 int take_driver_error();  // CUresult of the calling thread's last failed driver call (then cleared), or 0  // dtype, d_state, alignment and size limits
-size_t stream_smem_bytes_for(int rows_per_cta, int stage_tokens);
+size_t stream_smem_bytes_for(int rows_per_cta);
+constexpr int kStreamTokensPerStage = 32;  // streamed row kernel: tokens per stage
 cudaError_t scan_stream_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream);
 
 struct StepArgs {
