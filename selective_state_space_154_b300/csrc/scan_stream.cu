@@ -82,8 +82,6 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, co
 namespace {
 
 constexpr int NS = 16;        // states per row
-// rows per tensor copy of a row tile: the CTA's rows, at most 256 (the largest box)
-__host__ __device__ constexpr int box_rows(int rb) { return rb < 256 ? rb : 256; }
 
 // Stage geometry: TS = 32 tokens per stage.  Each warp double-buffers its own 32 rows'
 // tiles (64 bytes of a row per tensor and stage, copied by the warp itself); B and C
@@ -98,7 +96,7 @@ constexpr int kRowBytes = TS * 2;
 __device__ __forceinline__ int swz(int r, int g) { return g ^ ((r >> 1) & 3); }
 
 struct StreamParams {
-  CUtensorMap tm_b, tm_c;
+  CUtensorMap tm_b, tm_c, tm_out;
   ScanArgs a;
   int rtiles, nchunks;
   int64_t chunk_len;
@@ -250,6 +248,8 @@ template <int RB, bool HAS_Z>
 __device__ __forceinline__ void stage_advance(StreamSmem<RB>& sm, const Ring& g, int k, int n2, int warp, int lane,
                                               int& err) {
   constexpr int NW = RB / 32;
+  if (lane == 0) ac::bulk_wait_read0();  // the tensor store has read stage k's outputs out of the buffer
+  __syncwarp();
   if (stage_has(k + 2, g.spec_rows, g.n1, n2)) rows_issue<RB, HAS_Z>(sm, g, k + 2, warp, lane);
   cp_async_commit();  // one group per stage, empty or not, keeps the wait counts fixed
   const int s = k % NB;
@@ -265,12 +265,24 @@ __device__ __forceinline__ void stage_advance(StreamSmem<RB>& sm, const Ring& g,
   if (stage_has(k + kAhead, g.spec_bc, g.n1, n2)) bc_convert<RB>(sm, g, k + kAhead, warp, lane, err);
 }
 
+// The warp's outputs of a stage, written in place of u in shared memory, to HBM by one
+// tensor store (lane 0), after the lanes' shared-memory writes are made visible to it.
+__device__ __forceinline__ void fence_store_and_issue(const Ring& g, const uint8_t* slice, int ts, int warp,
+                                                      int lane) {
+  ac::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    ac::tma_store_3d(&g.p->tm_out, ac::smem_u32(slice), ts, g.c0 + 32 * warp, g.b);
+    ac::bulk_commit();
+  }
+}
+
 // One pass of a thread over stages [k0, k0 + nst), tokens from t_lo, writing the
 // 4-token groups that P selects.  h: the row's states; S: ΣΔ' since the chunk start
 // (P != kAll), with Kahan compensation `comp`.  In pass one (kSettled), lane 0
 // publishes the warp's stage count for pass two as soon as it is known.
 template <int RB, bool HAS_Z, int P, bool PRECISE>
-__device__ __forceinline__ void consume(StreamSmem<RB>& sm, const Ring& g, const RowConst& c, __nv_bfloat16* outb,
+__device__ __forceinline__ void consume(StreamSmem<RB>& sm, const Ring& g, const RowConst& c,
                                         int r, int warp, int lane, int k0, int nst, int n2, float (&h)[NS],
                                         float& S, float& comp, int& err) {
   constexpr float kStop = corr_stop_log2<__nv_bfloat16>();
@@ -289,13 +301,10 @@ __device__ __forceinline__ void consume(StreamSmem<RB>& sm, const Ring& g, const
     uint2* tu = reinterpret_cast<uint2*>(sm.tile[k & 1][0] + r * kRowBytes);  // outputs replace u in place
     const uint2* td = reinterpret_cast<const uint2*>(sm.tile[k & 1][1] + r * kRowBytes);
     const uint2* tz = reinterpret_cast<const uint2*>(sm.tile[k & 1][2] + r * kRowBytes);
-    unsigned wmask = 0;  // 4-token groups of this stage whose outputs this row writes
 #pragma unroll 1
     for (int q4 = 0; q4 < TS / 4; ++q4) {
       // four tokens per iteration: 8 bytes of each of u, Δraw, z (half a swizzled granule)
       const int t = ts + q4 * 4;
-      const bool write_blk =
-          P == kAll || (P == kSettled ? !(c.a2max * S > kStop) : c.a2max * S > kStop - 1.f);
       const int gi = swz(r, q4 >> 1) * 2 + (q4 & 1);  // 8-byte unit of the row
       const uint2 wu = tu[gi], wd = td[gi];
       uint2 wz = make_uint2(0u, 0u);
@@ -373,28 +382,12 @@ __device__ __forceinline__ void consume(StreamSmem<RB>& sm, const Ring& g, const
         S = tk;
       }
       tu[gi] = make_uint2(packed0, packed1);
-      if (c.row_ok && t < t_hi && write_blk) wmask |= 1u << q4;  // groups lie wholly inside [0, L) (L % 8 == 0)
     }
-    // the stage's outputs leave in 64-byte row segments, four lanes per row (as the
-    // inputs arrive): far fewer distinct rows per store than one row per lane
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int rr = 32 * warp + (lane >> 2) + 8 * i;
-      const int gg = lane & 3;  // 16-byte granule: 4-token groups 2 gg and 2 gg + 1
-      const unsigned bits = (__shfl_sync(0xffffffffu, wmask, rr & 31) >> (2 * gg)) & 3u;
-      if (bits) {
-        const uint4 v = *reinterpret_cast<const uint4*>(sm.tile[k & 1][0] + rr * kRowBytes + swz(rr, gg) * 16);
-        __nv_bfloat16* dst = outb + (int64_t)rr * g.p->a.L + ts + gg * 8;
-        if (bits == 3u) {
-          *reinterpret_cast<uint4*>(dst) = v;
-        } else if (bits == 1u) {
-          *reinterpret_cast<uint2*>(dst) = make_uint2(v.x, v.y);
-        } else {
-          *reinterpret_cast<uint2*>(dst + 4) = make_uint2(v.z, v.w);
-        }
-      }
-    }
+    // the stage's outputs, in place of u, leave by one tensor store of the warp's
+    // [32 rows × 32 tokens] (rows past d_inner and tokens past L are clipped).  Pass one
+    // of a chunk after the first stores every token too: pass two later stores its
+    // stages again, computed from the carried-in state.
+    fence_store_and_issue(g, sm.tile[k & 1][0] + 32 * warp * kRowBytes, ts, warp, lane);
     if (!published) {
       // pass two must cover this stage unless every row of the warp is settled after it
       const bool settled = !c.row_ok || !(c.a2max * S > kStop - 1.f);
@@ -425,16 +418,18 @@ struct StreamCta {
 
 template <int RB, bool HAS_Z, bool PRECISE>
 __device__ __forceinline__ void row_program(StreamSmem<RB>& sm, const StreamParams& p, const Ring& g,
-                                            const RowConst& cs, __nv_bfloat16* outb, float (&h)[NS], int chunk,
+                                            const RowConst& cs, float (&h)[NS], int chunk,
                                             int rem, int per_chunk, int64_t row, int r, int warp, int lane,
                                             int& err) {
   constexpr int NW = RB / 32;
   const int n1 = g.n1;
   float S = 0.f, comp = 0.f;
   if (chunk == 0)
-    consume<RB, HAS_Z, kAll, PRECISE>(sm, g, cs, outb, r, warp, lane, 0, n1, 0, h, S, comp, err);
+    consume<RB, HAS_Z, kAll, PRECISE>(sm, g, cs, r, warp, lane, 0, n1, 0, h, S, comp, err);
   else
-    consume<RB, HAS_Z, kSettled, PRECISE>(sm, g, cs, outb, r, warp, lane, 0, n1, -1, h, S, comp, err);
+    consume<RB, HAS_Z, kSettled, PRECISE>(sm, g, cs, r, warp, lane, 0, n1, -1, h, S, comp, err);
+  // pass one's stores complete before pass two stores its stages again
+  if (lane == 0) ac::bulk_wait0();
 
   // ---------------- carry between chunks ----------------
   // Each warp publishes its rows' aggregate (S, h from h = 0; the first chunk's h is
@@ -505,7 +500,7 @@ __device__ __forceinline__ void row_program(StreamSmem<RB>& sm, const StreamPara
     if (!ac::mbar_wait(ac::smem_u32(&sm.settled), 0u, g.deadline)) err = 1;
     const int n2 = *reinterpret_cast<volatile int*>(&sm.n2);
     float S2 = 0.f, comp2 = 0.f;
-    consume<RB, HAS_Z, kUnsettled, PRECISE>(sm, g, cs, outb, r, warp, lane, n1, n2, n2, hin, S2, comp2, err);
+    consume<RB, HAS_Z, kUnsettled, PRECISE>(sm, g, cs, r, warp, lane, n1, n2, n2, hin, S2, comp2, err);
   }
 }
 
@@ -569,8 +564,6 @@ __global__ void __launch_bounds__(StreamCta<RB>::kThreads) __maxnreg__(StreamCta
   cs.row_ok = r < nrows;
   const int64_t ch = g.c0 + (cs.row_ok ? r : 0);
   const int64_t row = (int64_t)g.b * p.a.d_inner + ch;
-  // output of the CTA's first row (rows past d_inner are never stored)
-  __nv_bfloat16* outb = static_cast<__nv_bfloat16*>(p.a.out) + ((int64_t)g.b * p.a.d_inner + g.c0) * p.a.L;
   float h[NS];
   cs.precise = false;
   cs.a2max = -INFINITY;
@@ -590,13 +583,14 @@ __global__ void __launch_bounds__(StreamCta<RB>::kThreads) __maxnreg__(StreamCta
   cs.bl2 = (cs.row_ok && p.a.bias) ? p.a.bias[ch] * kLog2e : 0.f;
 
   if (cs.precise)
-    row_program<RB, HAS_Z, true>(sm, p, g, cs, outb, h, chunk, rem, per_chunk, row, r, warp, lane, err);
+    row_program<RB, HAS_Z, true>(sm, p, g, cs, h, chunk, rem, per_chunk, row, r, warp, lane, err);
   else
-    row_program<RB, HAS_Z, false>(sm, p, g, cs, outb, h, chunk, rem, per_chunk, row, r, warp, lane, err);
+    row_program<RB, HAS_Z, false>(sm, p, g, cs, h, chunk, rem, per_chunk, row, r, warp, lane, err);
 
-  // copies issued ahead of a pass two shorter than the ring, never consumed, must land
-  // before the CTA exits
+  // copies issued ahead of a pass two shorter than the ring, never consumed, must land,
+  // and the tensor stores complete, before the CTA exits
   cp_async_wait<0>();
+  if (lane == 0) ac::bulk_wait0();
   __syncthreads();
   if (threadIdx.x == 0) {
     const int issued = sm.issued;
@@ -673,8 +667,15 @@ cudaError_t scan_stream_launch(const ScanArgs& a, const ScanPlan& plan, cudaStre
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto none = CU_TENSOR_MAP_SWIZZLE_NONE;
   const auto promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+  // out as [batch][d_inner][L] bf16, stored in [32 rows × 32 tokens] boxes with the
+  // 64-byte swizzle of the row tiles (rows past d_inner, tokens past L clipped)
+  const uint64_t D = (uint64_t)a.d_inner;
+  const uint64_t dims_row[3] = {L, D, Bt}, str_row[2] = {L * 2, L * D * 2};
+  const uint32_t box_row[3] = {(uint32_t)TS, 32u, 1u};
   if (!encode_tensor_map(&p.tm_b, bf, 3, a.B, dims_bc, str_bc, box_bc, none, promo) ||
-      !encode_tensor_map(&p.tm_c, bf, 3, a.C, dims_bc, str_bc, box_bc, none, promo))
+      !encode_tensor_map(&p.tm_c, bf, 3, a.C, dims_bc, str_bc, box_bc, none, promo) ||
+      !encode_tensor_map(&p.tm_out, bf, 3, a.out, dims_row, str_row, box_row, CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE))
     return cudaErrorInvalidValue;
   if (plan.nchunks > 1) {
     const cudaError_t e = cudaMemsetAsync(a.ws, 0, p.ws.flags_bytes, stream);
