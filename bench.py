@@ -337,7 +337,8 @@ def bench_scan_bwd(dev, hbm_peak, runs=10):
     stream = torch.cuda.current_stream(dev)
     res = {"note": "states recomputed from checkpoints every 8 tokens (workspace); the sequence is split "
                    "into chunks combined from per-chunk summaries (two launches); median of 10, L2 flushed "
-                   "before each"}
+                   "before each; deterministic_us: ssm_scan_bwd_deterministic (partial sums reduced in a fixed "
+                   "order by a third launch)"}
     for name in ("mamba130m_layer", "mamba2p8b_layer"):
         shape = W.SCAN_SHAPES[name]
         inp = W.scan_inputs(shape, device=dev, seed=0)
@@ -347,29 +348,33 @@ def bench_scan_bwd(dev, hbm_peak, runs=10):
                  dA=torch.empty_like(inp["A"]), dB=torch.empty(inp["B"].shape, device=dev),
                  dC=torch.empty(inp["C"].shape, device=dev), dD=torch.empty_like(inp["D"]),
                  dbias=torch.empty(shape.d_inner, device=dev))
-        ws = torch.empty(max(16, ssm.ssm_scan_bwd_workspace_bytes(shape.batch, shape.d_inner, shape.d_state,
-                                                                  shape.seqlen, shape.dtype)),
-                         dtype=torch.uint8, device=dev)
+        ws = torch.empty(max(16, ssm.ssm_scan_bwd_deterministic_workspace_bytes(
+            shape.batch, shape.d_inner, shape.d_state, shape.seqlen, shape.dtype)), dtype=torch.uint8, device=dev)
 
-        def call():
-            ssm.ssm_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["bias"],
-                             dout, g["du"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"], g["dz"], g["dbias"],
-                             workspace=ws, stream=stream)
+        def timed(det):
+            def call():
+                ssm.ssm_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                 inp["bias"], dout, g["du"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"], g["dz"],
+                                 g["dbias"], workspace=ws, stream=stream, deterministic=det)
 
-        call()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
-        for a, b in evs:
-            flush()
-            a.record(stream)
             call()
-            b.record(stream)
-        torch.cuda.synchronize()
-        secs = statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(runs)]
+            for a, b in evs:
+                flush()
+                a.record(stream)
+                call()
+                b.record(stream)
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+
+        secs = timed(False)
+        secs_det = timed(True)
         ct = shape.channel_tokens
         alg = 7 * ct * 2 + shape.batch * shape.seqlen * shape.d_state * (2 * 2 + 2 * 4)
         res[name] = {"batch": shape.batch, "d_inner": shape.d_inner, "d_state": shape.d_state,
                      "seq_len": shape.seqlen, "us": secs * 1e6, "channel_tokens_per_s": ct / secs,
-                     "gbs": alg / secs / 1e9, "hbm_frac": alg / secs / 1e9 / hbm_peak, "alg_bytes": alg}
+                     "gbs": alg / secs / 1e9, "hbm_frac": alg / secs / 1e9 / hbm_peak, "alg_bytes": alg,
+                     "deterministic_us": secs_det * 1e6}
         del inp, dout, g, ws
     return res
 

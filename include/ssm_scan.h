@@ -107,8 +107,9 @@ SSM_API size_t ssm_scan_workspace_bytes(const ssm_dims* dims);
  *   D, z, delta_bias: may be NULL (no skip term / no gate / zero bias).
  *   final_state: may be NULL; otherwise receives h_L.
  *   workspace: device memory of at least ssm_scan_workspace_bytes(dims) bytes,
- *     caller-owned, contents on entry irrelevant, not shared with a concurrent
- *     call.  It also holds a device error word read by ssm_scan_check.
+ *     16-byte aligned when any is needed, caller-owned, contents on entry
+ *     irrelevant, not shared with a concurrent call.  It also holds a device
+ *     error word read by ssm_scan_check.
  * Returns SSM_OK when the work was queued.
  */
 SSM_API ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
@@ -178,7 +179,7 @@ SSM_API ssm_status ssm_scan_fwd_host(const void* u, const void* delta, const flo
  *     float32 or NULL (dℓ/dbias, whether or not delta_bias is given).
  *   The call zeroes dA, dB, dC, dD and ddelta_bias, then accumulates into them
  *   (the sums over batch and channels use atomic adds, so their last bits may
- *   differ from call to call).
+ *   differ from call to call; ssm_scan_bwd_deterministic below does not).
  *   workspace: at least ssm_scan_bwd_workspace_bytes(dims) bytes, 16-byte
  *   aligned, caller-owned; it holds the state every 8 tokens of every row and,
  *   the sequence being split into chunks that run in parallel, each chunk's
@@ -192,6 +193,25 @@ SSM_API ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A
                                 const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC,
                                 float* dD, void* dz, float* ddelta_bias, const ssm_dims* dims, void* workspace,
                                 size_t workspace_bytes, ssm_stream_t stream);
+
+/*
+ * The same gradients, bitwise reproducible: the sums over channels (dB, dC) and over
+ * batch rows and sequence chunks (dA, dD, ddelta_bias) are not accumulated by atomic
+ * adds but written as per-CTA partial sums into the workspace and added by a third
+ * launch in a fixed order.  Arguments as for ssm_scan_bwd; the workspace must hold
+ * ssm_scan_bwd_deterministic_workspace_bytes(dims) bytes (the checkpoints, plus
+ * 4·2·d_state bytes per (64-channel tile, batch, token) and 4·(d_state + 2) bytes
+ * per (batch, chunk, channel) of partials).  dA, dB, dC, dD, ddelta_bias need not be
+ * zeroed.  Three kernel launches on `stream`; no host sync.  Repeated calls on the same
+ * inputs, device and dims return identical bits.
+ */
+SSM_API size_t ssm_scan_bwd_deterministic_workspace_bytes(const ssm_dims* dims);
+SSM_API ssm_status ssm_scan_bwd_deterministic(const void* u, const void* delta, const float* A, const void* B,
+                                              const void* C, const float* D, const void* z,
+                                              const float* delta_bias, const void* dout, void* du, void* ddelta,
+                                              float* dA, float* dB, float* dC, float* dD, void* dz,
+                                              float* ddelta_bias, const ssm_dims* dims, void* workspace,
+                                              size_t workspace_bytes, ssm_stream_t stream);
 
 /*
  * Recurrent (decode) mode: one token for every (batch, channel) row, updating

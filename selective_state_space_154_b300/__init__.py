@@ -23,6 +23,7 @@ __all__ = [
     "ssm_conv1d_fwd", "ssm_conv1d_step", "conv1d", "conv1d_step",
     "ssm_scan_fwd_host", "ssm_scan_fwd_host_staging_bytes", "reload_test_hooks",
     "ssm_scan_bwd_workspace_bytes", "ssm_scan_bwd", "scan_bwd",
+    "ssm_scan_bwd_deterministic_workspace_bytes",
     "ssd_scan_workspace_bytes", "ssd_scan_fwd", "ssd_scan", "ssd_step",
 ]
 
@@ -98,6 +99,10 @@ def load_library():
             lib.ssm_scan_bwd_workspace_bytes.restype = sz
             lib.ssm_scan_bwd.argtypes = [vp] * 17 + [dp, vp, sz, vp]
             lib.ssm_scan_bwd.restype = i32
+            lib.ssm_scan_bwd_deterministic_workspace_bytes.argtypes = [dp]
+            lib.ssm_scan_bwd_deterministic_workspace_bytes.restype = sz
+            lib.ssm_scan_bwd_deterministic.argtypes = [vp] * 17 + [dp, vp, sz, vp]
+            lib.ssm_scan_bwd_deterministic.restype = i32
             lib.ssm_conv1d_fwd.argtypes = [vp] * 6 + [dp, i32, vp]
             lib.ssm_conv1d_fwd.restype = i32
             lib.ssm_conv1d_step.argtypes = [vp] * 5 + [dp, i32, vp]
@@ -335,9 +340,15 @@ def ssm_scan_bwd_workspace_bytes(batch, d_inner, d_state, seqlen, dtype=torch.bf
     return int(load_library().ssm_scan_bwd_workspace_bytes(ctypes.byref(d)))
 
 
+def ssm_scan_bwd_deterministic_workspace_bytes(batch, d_inner, d_state, seqlen, dtype=torch.bfloat16) -> int:
+    d = _dims(batch, d_inner, d_state, seqlen, dtype)
+    return int(load_library().ssm_scan_bwd_deterministic_workspace_bytes(ctypes.byref(d)))
+
+
 def ssm_scan_bwd(u, delta, A, B, C, D, z, delta_bias, dout, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias,
-                 workspace=None, stream=None):
-    """Backward of the scan into caller-provided gradient tensors (see include/ssm_scan.h)."""
+                 workspace=None, stream=None, deterministic=False):
+    """Backward of the scan into caller-provided gradient tensors (see include/ssm_scan.h);
+    ``deterministic`` selects ssm_scan_bwd_deterministic (bitwise reproducible sums)."""
     lib = load_library()
     batch, d_inner, L = u.shape
     N = A.shape[1]
@@ -360,19 +371,21 @@ def ssm_scan_bwd(u, delta, A, B, C, D, z, delta_bias, dout, du, ddelta, dA, dB, 
     _check(ddelta_bias, "ddelta_bias", torch.float32, (d_inner,), dev, required=False)
     dims = _dims(batch, d_inner, N, L, act)
     with torch.cuda.device(dev):
-        need = int(lib.ssm_scan_bwd_workspace_bytes(ctypes.byref(dims)))
+        size_fn = lib.ssm_scan_bwd_deterministic_workspace_bytes if deterministic else lib.ssm_scan_bwd_workspace_bytes
+        need = int(size_fn(ctypes.byref(dims)))
         if workspace is None:
             workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         ws_bytes = workspace.numel() * workspace.element_size()
-        st = lib.ssm_scan_bwd(*(_ptr(t) for t in (u, delta, A, B, C, D, z, delta_bias, dout, du, ddelta, dA, dB, dC,
-                                                 dD, dz, ddelta_bias)),
-                              ctypes.byref(dims), _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
+        fn = lib.ssm_scan_bwd_deterministic if deterministic else lib.ssm_scan_bwd
+        st = fn(*(_ptr(t) for t in (u, delta, A, B, C, D, z, delta_bias, dout, du, ddelta, dA, dB, dC, dD, dz,
+                                    ddelta_bias)),
+                ctypes.byref(dims), _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
     if st != SSM_OK:
-        raise SsmError(st, "ssm_scan_bwd")
+        raise SsmError(st, "ssm_scan_bwd_deterministic" if deterministic else "ssm_scan_bwd")
     return workspace
 
 
-def scan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None, stream=None):
+def scan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None, stream=None, deterministic=False):
     """Allocate the gradients and run ``ssm_scan_bwd``; returns a dict like the oracle's."""
     g = dict(du=torch.empty_like(u), ddelta=torch.empty_like(u),
              dA=torch.empty(A.shape, dtype=torch.float32, device=u.device),
@@ -382,7 +395,7 @@ def scan_bwd(u, delta, A, B, C, dout, D=None, z=None, delta_bias=None, stream=No
              dz=torch.empty_like(u) if z is not None else None,
              dbias=torch.empty((u.shape[1],), dtype=torch.float32, device=u.device))
     ssm_scan_bwd(u, delta, A, B, C, D, z, delta_bias, dout, g["du"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"],
-                 g["dz"], g["dbias"], stream=stream)
+                 g["dz"], g["dbias"], stream=stream, deterministic=deterministic)
     return g
 
 

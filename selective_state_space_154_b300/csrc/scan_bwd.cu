@@ -519,10 +519,25 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
       float sum = 0.f;
 #pragma unroll
       for (int wi = 0; wi < kWarps; ++wi) sum += sm.red[wi][v][l];
-      atomicAdd((slot_id < 4 ? p.dB : p.dC) + (b * L + t0 + v) * N + n, sum);
+      const int w = slot_id < 4 ? 0 : 1;
+      if (p.det)  // this CTA's channel tile's share, summed over the tiles by the reduce launch
+        p.part_bc[(((o.rt % p.ctiles) * p.batch + b) * L + t0 + v) * 2 * N + w * N + n] = sum;
+      else
+        atomicAdd((w ? p.dC : p.dB) + (b * L + t0 + v) * N + n, sum);
     }
   }
-  if (row_ok) {
+  if (row_ok && p.det) {
+    float* pr = p.part_row + ((b * p.nchunks + o.chunk) * p.d_inner + c) * (N + 2);
+#pragma unroll
+    for (int k = 0; k < kBwdG; ++k) {
+      const int n = kBwdG * g + k;
+      if (n < N) pr[n] = dA_acc[k];
+    }
+    if (g == 0) {
+      pr[N] = dD_acc;
+      pr[N + 1] = db_acc;
+    }
+  } else if (row_ok) {
 #pragma unroll
     for (int k = 0; k < kBwdG; ++k) {
       const int n = kBwdG * g + k;
@@ -531,6 +546,37 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     if (g == 0) {
       if (p.dD) atomicAdd(p.dD + c, dD_acc);
       if (p.dbias) atomicAdd(p.dbias + c, db_acc);
+    }
+  }
+}
+
+// Launch 3 (deterministic mode): the sums over channel tiles (dB, dC) and over batch and
+// chunks (dA, dD, dbias) of the partials, each in ascending index order, so that the result
+// does not depend on which CTA ran first.
+__global__ void __launch_bounds__(256) scan_bwd_reduce_kernel(const BwdArgs p) {
+  const int64_t N = p.N;
+  const int64_t nbc = p.batch * p.L * 2 * N;  // one channel tile's partials
+  const int64_t nrow = p.d_inner * (N + 2);
+  const int64_t nparts = p.batch * p.nchunks;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nbc + nrow;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    if (i < nbc) {
+      float s = 0.f;
+      for (int ct = 0; ct < p.ctiles; ++ct) s += __ldcs(p.part_bc + ct * nbc + i);
+      const int64_t n = i % N, w = (i / N) & 1, bt = i / (2 * N);
+      (w ? p.dC : p.dB)[bt * N + n] = s;
+    } else {
+      const int64_t j = i - nbc;
+      float s = 0.f;
+      for (int64_t q = 0; q < nparts; ++q) s += __ldcs(p.part_row + q * nrow + j);
+      const int64_t c = j / (N + 2), k = j % (N + 2);
+      if (k < N)
+        p.dA[c * N + k] = s;
+      else if (k == N) {
+        if (p.dD) p.dD[c] = s;
+      } else if (p.dbias) {
+        p.dbias[c] = s;
+      }
     }
   }
 }
@@ -596,6 +642,10 @@ cudaError_t bwd_launch_t(BwdArgs p, cudaStream_t s) {
   scan_bwd_chunk_kernel<T><<<grid, kBwdThreads, 0, s>>>(p, w);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   scan_bwd_kernel<T><<<grid, kBwdThreads, sizeof(BwdSmem), s>>>(p, w);
+  if ((e = cudaGetLastError()) != cudaSuccess || !p.det) return e;
+  const int64_t items = p.batch * p.L * 2 * p.N + p.d_inner * (p.N + 2);
+  const int64_t blocks = (items + 255) / 256;
+  scan_bwd_reduce_kernel<<<(unsigned)(blocks < 148 * 16 ? blocks : 148 * 16), 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -603,18 +653,41 @@ cudaError_t bwd_launch_t(BwdArgs p, cudaStream_t s) {
 
 int scan_bwd_rows_per_cta() { return kBwdRows; }
 
-size_t scan_bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L) {
-  const int64_t R = batch * ((d_inner + kBwdRows - 1) / kBwdRows);
+namespace {
+// Workspace: [checkpoints and chunk summaries][partials of dB, dC][partials of dA, dD, dbias]
+struct BwdWsSizes {
+  size_t base, part_bc, part_row;
+};
+size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+BwdWsSizes bwd_ws_sizes(int64_t batch, int64_t d_inner, int64_t N, int64_t L) {
+  const int64_t ctiles = (d_inner + kBwdRows - 1) / kBwdRows;
+  const int64_t R = batch * ctiles;
   const int64_t nblk = (L + kBwdTok - 1) / kBwdTok;
   const int64_t kmax = bwd_max_chunks(nblk);
-  return (size_t)(R * nblk) * (kBwdThreads * sizeof(float4) + kBwdRows * sizeof(float)) +
-         (size_t)(R * kmax) * (2 * kBwdThreads * sizeof(float4) + kBwdRows * sizeof(float));
+  BwdWsSizes z;
+  z.base = round256((size_t)(R * nblk) * (kBwdThreads * sizeof(float4) + kBwdRows * sizeof(float)) +
+                    (size_t)(R * kmax) * (2 * kBwdThreads * sizeof(float4) + kBwdRows * sizeof(float)));
+  z.part_bc = round256((size_t)(ctiles * batch * L * 2 * N) * sizeof(float));
+  z.part_row = round256((size_t)(batch * kmax * d_inner * (N + 2)) * sizeof(float));
+  return z;
+}
+}  // namespace
+
+size_t scan_bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t N, int64_t L, bool deterministic) {
+  const BwdWsSizes z = bwd_ws_sizes(batch, d_inner, N, L);
+  return deterministic ? z.base + z.part_bc + z.part_row : z.base;
 }
 
 cudaError_t scan_bwd_launch(BwdArgs p, cudaStream_t stream) {
   p.ctiles = (int)((p.d_inner + kBwdRows - 1) / kBwdRows);
   p.nblk = (p.L + kBwdTok - 1) / kBwdTok;
   p.kmax = (int)bwd_max_chunks(p.nblk);
+  if (p.det) {
+    const BwdWsSizes z = bwd_ws_sizes(p.batch, p.d_inner, p.N, p.L);
+    unsigned char* base = reinterpret_cast<unsigned char*>(p.ckpt);
+    p.part_bc = reinterpret_cast<float*>(base + z.base);
+    p.part_row = reinterpret_cast<float*>(base + z.base + z.part_bc);
+  }
   return p.act == 1 ? bwd_launch_t<__nv_bfloat16>(p, stream) : bwd_launch_t<float>(p, stream);
 }
 

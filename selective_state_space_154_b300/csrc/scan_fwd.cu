@@ -579,7 +579,7 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
     const int occ = rb == 512 ? 1 : 3;
     pl.npad = 16;
     pl.groups = 1;
-    pl.threads = rb + 32;
+    pl.threads = rb;  // one thread per row
     pl.rows_per_cta = rb;
     pl.ctiles = (int)((a.d_inner + rb - 1) / rb);
     pl.smem_bytes = stream_smem_bytes_for(rb);

@@ -293,13 +293,23 @@ ssm_status ssm_conv1d_step(void* conv_state, const void* x, const float* weight,
 
 size_t ssm_scan_bwd_workspace_bytes(const ssm_dims* dims) {
   if (check_dims(dims, true) != SSM_OK || dims->d_state > 16) return 0;
-  return ssm::scan_bwd_workspace_bytes(dims->batch, dims->d_inner, dims->seqlen);
+  return ssm::scan_bwd_workspace_bytes(dims->batch, dims->d_inner, dims->d_state, dims->seqlen, false);
 }
 
-ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
-                        const float* D, const void* z, const float* delta_bias, const void* dout, void* du,
-                        void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz, float* ddelta_bias,
-                        const ssm_dims* dims, void* workspace, size_t workspace_bytes, ssm_stream_t stream) {
+size_t ssm_scan_bwd_deterministic_workspace_bytes(const ssm_dims* dims) {
+  if (check_dims(dims, true) != SSM_OK || dims->d_state > 16) return 0;
+  return ssm::scan_bwd_workspace_bytes(dims->batch, dims->d_inner, dims->d_state, dims->seqlen, true);
+}
+
+}  // extern "C"
+
+namespace {
+
+ssm_status scan_bwd_impl(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                         const float* D, const void* z, const float* delta_bias, const void* dout, void* du,
+                         void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz, float* ddelta_bias,
+                         const ssm_dims* dims, void* workspace, size_t workspace_bytes, ssm_stream_t stream,
+                         bool det) {
   const ssm_status ds = check_dims(dims, true);
   if (ds != SSM_OK) return ds;
   if (dims->d_state > 16) return SSM_ERR_UNSUPPORTED;
@@ -312,27 +322,51 @@ ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const 
   const void* f32_ptrs[] = {A, D, delta_bias, dA, dB, dC, dD, ddelta_bias};
   for (const void* p : f32_ptrs)
     if (p && !aligned(p, 4)) return SSM_ERR_ALIGNMENT;
-  const size_t need = ssm::scan_bwd_workspace_bytes(dims->batch, dims->d_inner, dims->seqlen);
+  const size_t need = ssm::scan_bwd_workspace_bytes(dims->batch, dims->d_inner, dims->d_state, dims->seqlen, det);
   if (!workspace || workspace_bytes < need) return SSM_ERR_WORKSPACE;
   if (!aligned16(workspace)) return SSM_ERR_ALIGNMENT;
   const int64_t rpc = ssm::scan_bwd_rows_per_cta();
   if (dims->batch * ((dims->d_inner + rpc - 1) / rpc) > INT32_MAX) return SSM_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int64_t b = dims->batch, d = dims->d_inner, N = dims->d_state, L = dims->seqlen;
-  // accumulated gradients start at zero
-  cudaError_t me = cudaMemsetAsync(dA, 0, sizeof(float) * d * N, st);
-  if (me == cudaSuccess) me = cudaMemsetAsync(dB, 0, sizeof(float) * b * L * N, st);
-  if (me == cudaSuccess) me = cudaMemsetAsync(dC, 0, sizeof(float) * b * L * N, st);
-  if (me == cudaSuccess && dD) me = cudaMemsetAsync(dD, 0, sizeof(float) * d, st);
-  if (me == cudaSuccess && ddelta_bias) me = cudaMemsetAsync(ddelta_bias, 0, sizeof(float) * d, st);
-  if (me != cudaSuccess) return cuda_status(me);
+  if (!det) {
+    // accumulated gradients start at zero (the deterministic mode writes them whole)
+    cudaError_t me = cudaMemsetAsync(dA, 0, sizeof(float) * d * N, st);
+    if (me == cudaSuccess) me = cudaMemsetAsync(dB, 0, sizeof(float) * b * L * N, st);
+    if (me == cudaSuccess) me = cudaMemsetAsync(dC, 0, sizeof(float) * b * L * N, st);
+    if (me == cudaSuccess && dD) me = cudaMemsetAsync(dD, 0, sizeof(float) * d, st);
+    if (me == cudaSuccess && ddelta_bias) me = cudaMemsetAsync(ddelta_bias, 0, sizeof(float) * d, st);
+    if (me != cudaSuccess) return cuda_status(me);
+  }
   ssm::BwdArgs a{};
   a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.bias = delta_bias; a.dout = dout;
   a.du = du; a.ddelta = ddelta; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dz = dz; a.dbias = ddelta_bias;
   a.ckpt = static_cast<float*>(workspace);
   a.batch = b; a.d_inner = d; a.N = N; a.L = L; a.act = dims->act;
+  a.det = det ? 1 : 0;
   a.force_chunks = ssm::runtime_knobs().bwd_chunks;
   return cuda_status(ssm::scan_bwd_launch(a, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* delta_bias, const void* dout, void* du,
+                        void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz, float* ddelta_bias,
+                        const ssm_dims* dims, void* workspace, size_t workspace_bytes, ssm_stream_t stream) {
+  return scan_bwd_impl(u, delta, A, B, C, D, z, delta_bias, dout, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias, dims,
+                       workspace, workspace_bytes, stream, false);
+}
+
+ssm_status ssm_scan_bwd_deterministic(const void* u, const void* delta, const float* A, const void* B,
+                                      const void* C, const float* D, const void* z, const float* delta_bias,
+                                      const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC,
+                                      float* dD, void* dz, float* ddelta_bias, const ssm_dims* dims,
+                                      void* workspace, size_t workspace_bytes, ssm_stream_t stream) {
+  return scan_bwd_impl(u, delta, A, B, C, D, z, delta_bias, dout, du, ddelta, dA, dB, dC, dD, dz, ddelta_bias, dims,
+                       workspace, workspace_bytes, stream, true);
 }
 
 ssm_status ssm_step_check(ssm_stream_t stream) {

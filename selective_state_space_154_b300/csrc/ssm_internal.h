@@ -159,10 +159,14 @@ struct BwdArgs {
   void* dz;
   float* dbias;
   float* ckpt;
+  // deterministic mode: per-CTA partial sums, reduced in a fixed order by a third launch
+  float* part_bc;   // [ctile][batch][L][B | C][N]
+  float* part_row;  // [batch][chunk][d_inner][dA 0..N-1 | dD | dbias]
   int64_t batch, d_inner, N, L, nblk, cblk;
-  int ctiles, act, nchunks, kmax, force_chunks;
+  int ctiles, act, nchunks, kmax, force_chunks, det;
 };
-size_t scan_bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t L);
+// deterministic = false: the checkpoints and chunk summaries; true: those plus the partial sums
+size_t scan_bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t N, int64_t L, bool deterministic);
 int scan_bwd_rows_per_cta();
 cudaError_t scan_bwd_launch(BwdArgs p, cudaStream_t stream);
 

@@ -119,3 +119,39 @@ def test_bwd_chunk_counts_agree(hooks):
             continue
         a, b = to_np(g1[k]), to_np(g7[k])
         assert rel_err(b, a) <= 2e-5, k
+
+
+@pytest.mark.parametrize("chunks", [0, 3])
+def test_bwd_deterministic_bitwise_and_parity(hooks, chunks):
+    """ssm_scan_bwd_deterministic: two calls return the same bits for every gradient, they
+    match the oracle like the atomic mode, and the two modes agree to rounding."""
+    if chunks:
+        hooks.set("SSM_BWD_CHUNKS", chunks)
+    inp = W.random_scan_inputs(3, 150, 16, 300, dtype=torch.bfloat16, device=DEV, seed=21, a_kind="random")
+    dout = _dout(inp, 22)
+    kw = dict(D=inp["D"], z=inp["z"], delta_bias=inp["bias"])
+    g1 = ssm.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dout, deterministic=True, **kw)
+    g2 = ssm.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dout, deterministic=True, **kw)
+    ga = ssm.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dout, **kw)
+    torch.cuda.synchronize()
+    r = _ref(inp, dout)
+    for k in GRADS:
+        assert torch.equal(g1[k], g2[k]), f"{k}: deterministic mode differs between calls"
+        e = rel_err(to_np(g1[k]), r[k])
+        assert e <= TOL[torch.bfloat16], f"{k}: rel err {e:.3e}"
+        e2 = rel_err(to_np(g1[k]), to_np(ga[k]).astype(np.float64))
+        assert e2 <= 1e-3, f"{k}: deterministic vs atomic {e2:.3e}"
+
+
+def test_bwd_deterministic_fp32_no_optional():
+    inp = W.random_scan_inputs(2, 70, 13, 90, dtype=torch.float32, device=DEV, seed=23, a_kind="random",
+                               gate=False, skip=False, with_bias=False)
+    dout = _dout(inp, 24)
+    g = ssm.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dout, deterministic=True)
+    torch.cuda.synchronize()
+    r = _ref(inp, dout)
+    for k in GRADS:
+        if r[k] is None or g[k] is None:
+            continue
+        e = rel_err(to_np(g[k]), r[k])
+        assert e <= TOL[torch.float32], f"{k}: rel err {e:.3e}"
