@@ -277,6 +277,97 @@ __device__ __forceinline__ void fence_store_and_issue(const Ring& g, const uint8
   }
 }
 
+// The 32 tokens of one stage for one row, in groups of four: steps, updates, readout,
+// gate; outputs (bf16) replace u in the tile; returns the stage's ΣΔ' (P != kAll).
+// MASKED: tokens past t_valid (the sequence's or chunk's end, or a row past d_inner)
+// take Δ' = 0; a stage the whole warp has inside needs no mask.
+template <int RB, bool HAS_Z, int P, bool PRECISE, bool MASKED>
+__device__ __forceinline__ float stage_tokens(const StreamSmem<RB>& sm, int s, const RowConst& c, int r, uint2* tu,
+                                              const uint2* td, const uint2* tz, int ts, int t_valid,
+                                              float (&h)[NS]) {
+  float Sst = 0.f;
+#pragma unroll 1
+  for (int q4 = 0; q4 < TS / 4; ++q4) {
+    // four tokens per iteration: 8 bytes of each of u, Δraw, z (half a swizzled granule)
+    const int t = ts + q4 * 4;
+    const int gi = swz(r, q4 >> 1) * 2 + (q4 & 1);  // 8-byte unit of the row
+    const uint2 wu = tu[gi], wd = td[gi];
+    uint2 wz = make_uint2(0u, 0u);
+    if (HAS_Z) wz = tz[gi];
+    const float* bcs = sm.bcf[s][q4 * 4];
+    unsigned packed0 = 0u, packed1 = 0u;
+    float Sb = 0.f;
+#pragma unroll
+    for (int v = 0; v < 4; v += 2) {
+      const unsigned uw = v ? wu.y : wu.x, dw = v ? wd.y : wd.x;
+      // Δ' = log2(1 + 2^{r log2 e}) for two tokens (r = Δraw + bias); r log2 e above 15 log2 e
+      const float2 rl = __ffma2_rn(make_float2(bf_lo(dw), bf_hi(dw)), make_float2(kLog2e, kLog2e),
+                                   make_float2(c.bl2, c.bl2));
+      const float2 q = __fadd2_rn(make_float2(ex2_approx(rl.x), ex2_approx(rl.y)), make_float2(1.f, 1.f));
+      float d0 = rl.x > 15.f * kLog2e ? rl.x : lg2_approx(q.x);
+      float d1 = rl.y > 15.f * kLog2e ? rl.y : lg2_approx(q.y);
+      if (MASKED) {
+        d0 = t + v < t_valid ? d0 : 0.f;
+        d1 = t + v + 1 < t_valid ? d1 : 0.f;
+      }
+      float2 gz = make_float2(1.f, 1.f);
+      if (HAS_Z) {
+        const unsigned zw = v ? wz.y : wz.x;
+        const float2 zz = make_float2(bf_lo(zw), bf_hi(zw));
+        const float2 ez = __fmul2_rn(zz, make_float2(-kLog2e, -kLog2e));
+        const float2 dz = __fadd2_rn(make_float2(ex2_approx(ez.x), ex2_approx(ez.y)), make_float2(1.f, 1.f));
+        gz = __fmul2_rn(zz, make_float2(rcp_approx(dz.x), rcp_approx(dz.y)));
+      }
+      const float xs[2] = {bf_lo(uw), bf_hi(uw)};
+      const float ds[2] = {d0, d1};
+      float ys[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float dlt = ds[j], x = xs[j];
+        const float4* bc4 = reinterpret_cast<const float4*>(bcs + (v + j) * 2 * NS);
+        const float2 dd = make_float2(dlt, dlt), xx = make_float2(x, x);
+        // rows with an A = 0 state (PRECISE): Ā = 1, B̄ = Δ B exactly there (Δ = Δ' ln 2)
+        const float2 dx = PRECISE ? make_float2(dlt * kLn2 * x, dlt * kLn2 * x) : make_float2(0.f, 0.f);
+        float2 ya = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int qd = 0; qd < NS / 4; ++qd) {
+          const float4 bq = bc4[qd];
+          const float4 cq = bc4[NS / 4 + qd];
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int n = 4 * qd + 2 * k2;
+            const float2 e = __fmul2_rn(dd, make_float2(c.a2[n], c.a2[n + 1]));
+            const float2 em = __fadd2_rn(make_float2(ex2_approx(e.x), ex2_approx(e.y)), make_float2(-1.f, -1.f));
+            const float2 xp = __fmul2_rn(xx, make_float2(c.ia[n], c.ia[n + 1]));
+            const float2 hb = make_float2(h[n], h[n + 1]);
+            const float2 bb = k2 ? make_float2(bq.z, bq.w) : make_float2(bq.x, bq.y);
+            const float2 cc = k2 ? make_float2(cq.z, cq.w) : make_float2(cq.x, cq.y);
+            float2 hn = __ffma2_rn(em, __ffma2_rn(xp, bb, hb), hb);
+            if (PRECISE) {
+              const float2 h0 = __ffma2_rn(dx, bb, hb);
+              hn.x = c.ia[n] != 0.f ? hn.x : h0.x;
+              hn.y = c.ia[n + 1] != 0.f ? hn.y : h0.y;
+            }
+            h[n] = hn.x;
+            h[n + 1] = hn.y;
+            ya = __ffma2_rn(cc, hn, ya);
+          }
+        }
+        ys[j] = fmaf(c.Dc, x, ya.x + ya.y);
+      }
+      const float2 yo = __fmul2_rn(make_float2(ys[0], ys[1]), gz);
+      __nv_bfloat162 p2 = __floats2bfloat162_rn(yo.x, yo.y);
+      const unsigned pw = *reinterpret_cast<unsigned*>(&p2);
+      packed0 = v ? packed0 : pw;
+      packed1 = v ? pw : packed1;
+      if (P != kAll) Sb += d0 + d1;
+    }
+    if (P != kAll) Sst += Sb;
+    tu[gi] = make_uint2(packed0, packed1);
+  }
+  return Sst;
+}
+
 // One pass of a thread over stages [k0, k0 + nst), tokens from t_lo, writing the
 // 4-token groups that P selects.  h: the row's states; S: ΣΔ' since the chunk start
 // (P != kAll), with Kahan compensation `comp`.  In pass one (kSettled), lane 0
@@ -301,87 +392,16 @@ __device__ __forceinline__ void consume(StreamSmem<RB>& sm, const Ring& g, const
     uint2* tu = reinterpret_cast<uint2*>(sm.tile[k & 1][0] + r * kRowBytes);  // outputs replace u in place
     const uint2* td = reinterpret_cast<const uint2*>(sm.tile[k & 1][1] + r * kRowBytes);
     const uint2* tz = reinterpret_cast<const uint2*>(sm.tile[k & 1][2] + r * kRowBytes);
-#pragma unroll 1
-    for (int q4 = 0; q4 < TS / 4; ++q4) {
-      // four tokens per iteration: 8 bytes of each of u, Δraw, z (half a swizzled granule)
-      const int t = ts + q4 * 4;
-      const int gi = swz(r, q4 >> 1) * 2 + (q4 & 1);  // 8-byte unit of the row
-      const uint2 wu = tu[gi], wd = td[gi];
-      uint2 wz = make_uint2(0u, 0u);
-      if (HAS_Z) wz = tz[gi];
-      const float* bcs = sm.bcf[s][q4 * 4];
-      unsigned packed0 = 0u, packed1 = 0u;
-      float Sb = 0.f;
-#pragma unroll
-      for (int v = 0; v < 4; v += 2) {
-        const unsigned uw = v ? wu.y : wu.x, dw = v ? wd.y : wd.x;
-        // Δ' = log2(1 + 2^{r log2 e}) for two tokens (r = Δraw + bias); r log2 e above 15 log2 e
-        const float2 rl = __ffma2_rn(make_float2(bf_lo(dw), bf_hi(dw)), make_float2(kLog2e, kLog2e),
-                                     make_float2(c.bl2, c.bl2));
-        const float2 q = __fadd2_rn(make_float2(ex2_approx(rl.x), ex2_approx(rl.y)), make_float2(1.f, 1.f));
-        float d0 = rl.x > 15.f * kLog2e ? rl.x : lg2_approx(q.x);
-        float d1 = rl.y > 15.f * kLog2e ? rl.y : lg2_approx(q.y);
-        d0 = t + v < t_valid ? d0 : 0.f;
-        d1 = t + v + 1 < t_valid ? d1 : 0.f;
-        float2 gz = make_float2(1.f, 1.f);
-        if (HAS_Z) {
-          const unsigned zw = v ? wz.y : wz.x;
-          const float2 zz = make_float2(bf_lo(zw), bf_hi(zw));
-          const float2 ez = __fmul2_rn(zz, make_float2(-kLog2e, -kLog2e));
-          const float2 dz = __fadd2_rn(make_float2(ex2_approx(ez.x), ex2_approx(ez.y)), make_float2(1.f, 1.f));
-          gz = __fmul2_rn(zz, make_float2(rcp_approx(dz.x), rcp_approx(dz.y)));
-        }
-        const float xs[2] = {bf_lo(uw), bf_hi(uw)};
-        const float ds[2] = {d0, d1};
-        float ys[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float dlt = ds[j], x = xs[j];
-          const float4* bc4 = reinterpret_cast<const float4*>(bcs + (v + j) * 2 * NS);
-          const float2 dd = make_float2(dlt, dlt), xx = make_float2(x, x);
-          // rows with an A = 0 state (PRECISE): Ā = 1, B̄ = Δ B exactly there (Δ = Δ' ln 2)
-          const float2 dx = PRECISE ? make_float2(dlt * kLn2 * x, dlt * kLn2 * x) : make_float2(0.f, 0.f);
-          float2 ya = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int qd = 0; qd < NS / 4; ++qd) {
-            const float4 bq = bc4[qd];
-            const float4 cq = bc4[NS / 4 + qd];
-#pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-              const int n = 4 * qd + 2 * k2;
-              const float2 e = __fmul2_rn(dd, make_float2(c.a2[n], c.a2[n + 1]));
-              const float2 em = __fadd2_rn(make_float2(ex2_approx(e.x), ex2_approx(e.y)), make_float2(-1.f, -1.f));
-              const float2 xp = __fmul2_rn(xx, make_float2(c.ia[n], c.ia[n + 1]));
-              const float2 hb = make_float2(h[n], h[n + 1]);
-              const float2 bb = k2 ? make_float2(bq.z, bq.w) : make_float2(bq.x, bq.y);
-              const float2 cc = k2 ? make_float2(cq.z, cq.w) : make_float2(cq.x, cq.y);
-              float2 hn = __ffma2_rn(em, __ffma2_rn(xp, bb, hb), hb);
-              if (PRECISE) {
-                const float2 h0 = __ffma2_rn(dx, bb, hb);
-                hn.x = c.ia[n] != 0.f ? hn.x : h0.x;
-                hn.y = c.ia[n + 1] != 0.f ? hn.y : h0.y;
-              }
-              h[n] = hn.x;
-              h[n + 1] = hn.y;
-              ya = __ffma2_rn(cc, hn, ya);
-            }
-          }
-          ys[j] = fmaf(c.Dc, x, ya.x + ya.y);
-        }
-        const float2 yo = __fmul2_rn(make_float2(ys[0], ys[1]), gz);
-        __nv_bfloat162 p2 = __floats2bfloat162_rn(yo.x, yo.y);
-        const unsigned pw = *reinterpret_cast<unsigned*>(&p2);
-        packed0 = v ? packed0 : pw;
-        packed1 = v ? pw : packed1;
-        if (P != kAll) Sb += d0 + d1;
-      }
-      if (P != kAll) {  // S += Sb with Kahan compensation (S feeds 2^{A S} over long chunks)
-        const float yk = Sb - comp;
-        const float tk = S + yk;
-        comp = (tk - S) - yk;
-        S = tk;
-      }
-      tu[gi] = make_uint2(packed0, packed1);
+    float Sst;
+    if (__all_sync(0xffffffffu, ts + TS <= t_valid))
+      Sst = stage_tokens<RB, HAS_Z, P, PRECISE, false>(sm, s, c, r, tu, td, tz, ts, t_valid, h);
+    else
+      Sst = stage_tokens<RB, HAS_Z, P, PRECISE, true>(sm, s, c, r, tu, td, tz, ts, t_valid, h);
+    if (P != kAll) {  // S += the stage's sum with Kahan compensation (S feeds 2^{A S} over long chunks)
+      const float yk = Sst - comp;
+      const float tk = S + yk;
+      comp = (tk - S) - yk;
+      S = tk;
     }
     // the stage's outputs, in place of u, leave by one tensor store of the warp's
     // [32 rows × 32 tokens] (rows past d_inner and tokens past L are clipped).  Pass one
