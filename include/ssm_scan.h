@@ -397,6 +397,7 @@ SSM_API ssm_status ssd_step(float* state, const void* x, const void* dt, const f
  *   SSM_FORCE_TPR = 2           two threads per row in the row kernel
  *   SSM_CTAS_PER_SM = n         resident CTAs per SM assumed by the row kernel's planner
  *   SSM_STREAM_ROWS = 512 | 128 rows per CTA of the streamed row kernel
+ *   SSM_STREAM_CTAS = n         work items (CTAs) of the streamed row kernel
  *   SSM_BWD_CHUNKS = n          sequence chunks of ssm_scan_bwd
  *   SSM_FORCE_STEP = plain      the generic decode-step kernel only
  *   SSM_FAULT = lookback | step | ssd   the named device-side wait never completes

@@ -583,19 +583,30 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
     pl.rows_per_cta = rb;
     pl.ctiles = (int)((a.d_inner + rb - 1) / rb);
     pl.smem_bytes = stream_smem_bytes_for(rb);
-    const int64_t items = a.batch * pl.ctiles;
-    const int64_t nch =
-        pick_chunks(items, (int64_t)sms * occ, a.L, kMinRowChunk, kStreamTokensPerStage, knobs.force_chunks);
-    int64_t clen = (a.L + nch - 1) / nch;
-    clen = (clen + kStreamTokensPerStage - 1) / kStreamTokensPerStage * kStreamTokensPerStage;
-    pl.chunk_len = clen;
-    pl.nchunks = (int)((a.L + clen - 1) / clen);
+    // Work items: the tiles' stages, flattened tile after tile, cut into nearly equal
+    // ranges, one per resident CTA when the tiles alone do not fill the GPU (a range may
+    // end one tile's sequence and start the next's), each of at least kMinRowChunk tokens
+    // on average.  SSM_FORCE_CHUNKS = n makes n equal segments per tile, SSM_STREAM_CTAS
+    // sets the item count itself.
+    const int64_t tiles = a.batch * pl.ctiles;
+    const int64_t sl = (a.L + kStreamTokensPerStage - 1) / kStreamTokensPerStage;
+    const int64_t min_st = kMinRowChunk / kStreamTokensPerStage;
+    int64_t items = tiles;
+    if (knobs.force_chunks > 0)
+      items = tiles * std::min<int64_t>(knobs.force_chunks, sl);
+    else if (knobs.stream_ctas > 0)
+      items = std::min<int64_t>(std::max<int64_t>(knobs.stream_ctas, tiles), tiles * sl);
+    else if (tiles < (int64_t)sms * occ)
+      items = std::max<int64_t>(tiles, std::min<int64_t>((int64_t)sms * occ, tiles * sl / min_st));
+    const int64_t per_item = (tiles * sl + items - 1) / items;  // stages
+    pl.chunk_len = per_item * kStreamTokensPerStage;
+    pl.nchunks = (int)items;
     size_t total = 0;
-    stream_ws_layout(nullptr, pl.nchunks, items, rb, &total);
+    stream_ws_layout(nullptr, items, rb, &total);
     pl.ws_flags_off = kWsHeaderBytes;
     pl.ws_agg_off = 0;
-    // one chunk needs no workspace; a workspace given anyway receives the error word
-    pl.ws_bytes = pl.nchunks > 1 ? total : 0;
+    // one segment per tile needs no workspace; a workspace given anyway receives the error word
+    pl.ws_bytes = items > tiles ? total : 0;
     *plan = pl;
     return true;
   }

@@ -95,14 +95,31 @@ constexpr int kRowBytes = TS * 2;
 // lanes reading the same granule of eight consecutive rows hit different banks
 __device__ __forceinline__ int swz(int r, int g) { return g ^ ((r >> 1) & 3); }
 
+// Work items: the (row tile, stage) pairs of all tiles, tile after tile, cut into `items`
+// ranges of nearly equal length; item j holds flattened stages [j·ptot/items,
+// (j+1)·ptot/items).  A range lies in one tile or straddles two; the part of a range in
+// one tile is a segment of that tile's sequence (a chunk), and the segments of a tile,
+// in order, belong to consecutive items.
 struct StreamParams {
   CUtensorMap tm_b, tm_c, tm_out;
   ScanArgs a;
-  int rtiles, nchunks;
-  int64_t chunk_len;
+  int rtiles;   // row tiles per batch
+  int sl;       // stages per tile (ceil(L / 32))
+  int items;    // work items (CTAs)
+  int multi;    // some tile has more than one segment (the carry and the workspace are used)
+  int64_t ptot; // flattened stages: batch · rtiles · sl
   StreamWs ws;
   long long timeout_ns;
   int fault_lookback;
+};
+
+// A segment of one tile's sequence as one work item sees it.
+struct Segment {
+  int tile;      // row tile, batch-major
+  int s0, s1;    // its stages [s0, s1) of the tile's sequence
+  int q;         // its index among the tile's segments (0: starts from the initial state)
+  int64_t slot;  // where its aggregate is published
+  int64_t item;  // the work item holding it
 };
 
 // Shared memory of one CTA (the dynamic allocation is aligned up to 1024 bytes).
@@ -117,7 +134,8 @@ struct StreamSmem {
   int done[NB];       // warps that released the stage's B and C
   int n2;             // stages of the second pass (max over warps)
   int issued;         // B/C stages issued so far (the last one + 1)
-  int ticket;         // this CTA's work item
+  int nseg;           // this CTA's segments: 1, or 2 (the next tile's first one runs first)
+  Segment seg[2];
 };
 template <int RB>
 constexpr size_t stream_smem_bytes() {
@@ -167,11 +185,14 @@ struct Ring {
   const StreamParams* p;
   unsigned long long deadline;
   int c0, b, tc0, tc1, n1;
+  int kb;         // ring stages the CTA used before this segment (the ring's slots and phases run on)
   int spec_rows;  // row-tile stages a warp may copy without knowing pass two's length
   int spec_bc;    // B/C stages that may be issued without knowing it
 };
 
 __device__ __forceinline__ int stage_t0(const Ring& g, int k) { return g.tc0 + (k < g.n1 ? k : k - g.n1) * TS; }
+// position of the segment's stage k in the CTA's ring (buffer k & 1, B/C slot k % NB)
+__device__ __forceinline__ int ring(const Ring& g, int k) { return g.kb + k; }
 
 // This warp's 32 rows of stage k's u, Δraw, z tiles into row buffer k % 2, one
 // cp.async group (four lanes per 64-byte row segment; rows past d_inner and tokens
@@ -194,7 +215,7 @@ __device__ __forceinline__ void rows_issue(StreamSmem<RB>& sm, const Ring& g, in
       const int c = g.c0 + r;
       const bool ok = t_ok && c < a.d_inner;
       const __nv_bfloat16* src = srcs[w] + ((int64_t)g.b * a.d_inner + (ok ? c : 0)) * a.L + (ok ? t : 0);
-      cp_async16(sm.tile[k & 1][w] + r * kRowBytes + swz(r, gi) * 16, src, ok ? 16 : 0);
+      cp_async16(sm.tile[ring(g, k) & 1][w] + r * kRowBytes + swz(r, gi) * 16, src, ok ? 16 : 0);
     }
   }
 }
@@ -202,14 +223,14 @@ __device__ __forceinline__ void rows_issue(StreamSmem<RB>& sm, const Ring& g, in
 // Issue the tensor copies of stage j's B and C (one thread).
 template <int RB>
 __device__ __forceinline__ void bc_issue(StreamSmem<RB>& sm, const Ring& g, int j) {
-  const int s = j % NB;
+  const int s = ring(g, j) % NB;
   const int t0 = stage_t0(g, j);
   const StreamParams& p = *g.p;
   const uint32_t fb = ac::smem_u32(&sm.full[s]);
   ac::mbar_arrive_expect_tx(fb, (uint32_t)(2 * TS * NS * 2));
   ac::tma_load_3d(ac::smem_u32(sm.bc_raw[s][0]), &p.tm_b, 0, t0, g.b, fb);
   ac::tma_load_3d(ac::smem_u32(sm.bc_raw[s][1]), &p.tm_c, 0, t0, g.b, fb);
-  atomicMax(&sm.issued, j + 1);
+  atomicMax(&sm.issued, ring(g, j) + 1);
 }
 
 // This warp's share of stage j's B and C to fp32: [B|C][token][state] -> [token][B | C].
@@ -218,8 +239,8 @@ __device__ __forceinline__ void bc_convert(StreamSmem<RB>& sm, const Ring& g, in
   constexpr int NW = RB / 32;
   constexpr int kWords = TS * NS;      // 32-bit words of B and C together
   constexpr int kShare = kWords / NW;  // words per warp
-  const int s = j % NB;
-  if (!ac::mbar_wait(ac::smem_u32(&sm.full[s]), (uint32_t)(j / NB) & 1u, g.deadline)) err = 1;
+  const int s = ring(g, j) % NB;
+  if (!ac::mbar_wait(ac::smem_u32(&sm.full[s]), (uint32_t)(ring(g, j) / NB) & 1u, g.deadline)) err = 1;
   const unsigned* raw = reinterpret_cast<const unsigned*>(sm.bc_raw[s][0]);
 #pragma unroll
   for (int q = 0; q < (kShare + 31) / 32; ++q) {
@@ -252,7 +273,7 @@ __device__ __forceinline__ void stage_advance(StreamSmem<RB>& sm, const Ring& g,
   __syncwarp();
   if (stage_has(k + 2, g.spec_rows, g.n1, n2)) rows_issue<RB, HAS_Z>(sm, g, k + 2, warp, lane);
   cp_async_commit();  // one group per stage, empty or not, keeps the wait counts fixed
-  const int s = k % NB;
+  const int s = ring(g, k) % NB;
   __syncwarp();
   if (lane == 0) {
     __threadfence_block();  // this warp's reads of the slot precede its release
@@ -383,15 +404,16 @@ __device__ __forceinline__ void consume(StreamSmem<RB>& sm, const Ring& g, const
 #pragma unroll 1
   for (int kk = 0; kk < nst; ++kk) {
     const int k = k0 + kk;
-    const int s = k % NB;
-    const uint32_t ph = (uint32_t)(k / NB) & 1u;
+    const int s = ring(g, k) % NB;
+    const uint32_t ph = (uint32_t)(ring(g, k) / NB) & 1u;
     cp_async_wait<1>();  // this warp's rows of stage k (stage k + 1's may still be in flight)
     __syncwarp();
     if (!ac::mbar_wait(ac::smem_u32(&sm.conv[s]), ph, g.deadline)) err = 1;
     const int ts = t_lo + kk * TS;
-    uint2* tu = reinterpret_cast<uint2*>(sm.tile[k & 1][0] + r * kRowBytes);  // outputs replace u in place
-    const uint2* td = reinterpret_cast<const uint2*>(sm.tile[k & 1][1] + r * kRowBytes);
-    const uint2* tz = reinterpret_cast<const uint2*>(sm.tile[k & 1][2] + r * kRowBytes);
+    const int buf = ring(g, k) & 1;
+    uint2* tu = reinterpret_cast<uint2*>(sm.tile[buf][0] + r * kRowBytes);  // outputs replace u in place
+    const uint2* td = reinterpret_cast<const uint2*>(sm.tile[buf][1] + r * kRowBytes);
+    const uint2* tz = reinterpret_cast<const uint2*>(sm.tile[buf][2] + r * kRowBytes);
     float Sst;
     if (__all_sync(0xffffffffu, ts + TS <= t_valid))
       Sst = stage_tokens<RB, HAS_Z, P, PRECISE, false>(sm, s, c, r, tu, td, tz, ts, t_valid, h);
@@ -407,7 +429,7 @@ __device__ __forceinline__ void consume(StreamSmem<RB>& sm, const Ring& g, const
     // [32 rows × 32 tokens] (rows past d_inner and tokens past L are clipped).  Pass one
     // of a chunk after the first stores every token too: pass two later stores its
     // stages again, computed from the carried-in state.
-    fence_store_and_issue(g, sm.tile[k & 1][0] + 32 * warp * kRowBytes, ts, warp, lane);
+    fence_store_and_issue(g, sm.tile[buf][0] + 32 * warp * kRowBytes, ts, warp, lane);
     if (!published) {
       // pass two must cover this stage unless every row of the warp is settled after it
       const bool settled = !c.row_ok || !(c.a2max * S > kStop - 1.f);
@@ -436,52 +458,66 @@ struct StreamCta {
   static constexpr int kMaxRegs = 128;
 };
 
+// Work-item geometry (see StreamParams): the first flattened stage of item j, and the
+// item whose range holds flattened stage P.
+__device__ __forceinline__ int64_t item_start(const StreamParams& p, int64_t j) { return j * p.ptot / p.items; }
+__device__ __forceinline__ int64_t item_owner(const StreamParams& p, int64_t P) {
+  return ((P + 1) * p.items - 1) / p.ptot;
+}
+// Workspace slot of an item's segment: 2j for the segment its range starts in, 2j + 1 for
+// the first segment of the next tile where its range ends.
+__device__ __forceinline__ int64_t seg_slot(const StreamParams& p, int64_t owner, int tile, int m) {
+  return (m == 0 && item_start(p, owner) < (int64_t)tile * p.sl) ? 2 * owner + 1 : 2 * owner;
+}
+
+
 template <int RB, bool HAS_Z, bool PRECISE>
 __device__ __forceinline__ void row_program(StreamSmem<RB>& sm, const StreamParams& p, const Ring& g,
-                                            const RowConst& cs, float (&h)[NS], int chunk,
-                                            int rem, int per_chunk, int64_t row, int r, int warp, int lane,
-                                            int& err) {
+                                            const RowConst& cs, float (&h)[NS], const Segment& sg, int64_t row,
+                                            int r, int warp, int lane, int& err) {
   constexpr int NW = RB / 32;
   const int n1 = g.n1;
+  const bool last = sg.s1 == p.sl;  // no later segment in this tile
   float S = 0.f, comp = 0.f;
-  if (chunk == 0)
+  if (sg.q == 0)
     consume<RB, HAS_Z, kAll, PRECISE>(sm, g, cs, r, warp, lane, 0, n1, 0, h, S, comp, err);
   else
     consume<RB, HAS_Z, kSettled, PRECISE>(sm, g, cs, r, warp, lane, 0, n1, -1, h, S, comp, err);
   // pass one's stores complete before pass two stores its stages again
   if (lane == 0) ac::bulk_wait0();
 
-  // ---------------- carry between chunks ----------------
-  // Each warp publishes its rows' aggregate (S, h from h = 0; the first chunk's h is
+  // ---------------- carry between the segments of a tile ----------------
+  // Each warp publishes its rows' aggregate (S, h from h = 0; the first segment's h is
   // its end state from the initial state) and combines those of all preceding
-  // chunks in a fixed order, h_in = Σ_j 2^{A (S_{j+1} + … + S_{chunk-1})} h_j, so the
-  // result does not depend on which chunk finished first.  The aggregates are
-  // published right after pass one, so no chunk waits for another's carry.
+  // segments in a fixed order, h_in = Σ_m 2^{A (S_{m+1} + … + S_{q-1})} h_m, so the
+  // result does not depend on which segment finished first.  The aggregates are
+  // published right after pass one, so no segment waits for another's carry.
   float hin[NS];
 #pragma unroll
   for (int n = 0; n < NS; ++n) hin[n] = 0.f;
-  if (p.nchunks > 1) {
-    const int64_t rows_chunk = (int64_t)per_chunk * RB;
-    const int64_t my = (int64_t)rem * RB + r;
-    const int64_t flags_chunk = (int64_t)per_chunk * NW;
-    const int64_t fw = (int64_t)rem * NW + warp;
-    if (chunk + 1 < p.nchunks) {
-      float4* ah = reinterpret_cast<float4*>(p.ws.agg_h + ((int64_t)chunk * rows_chunk + my) * NS);
+  if (p.multi) {
+    if (!last) {
+      float4* ah = reinterpret_cast<float4*>(p.ws.agg_h + (sg.slot * RB + r) * NS);
 #pragma unroll
       for (int q = 0; q < NS / 4; ++q) ah[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-      p.ws.agg_s[(int64_t)chunk * rows_chunk + my] = S;
+      p.ws.agg_s[sg.slot * RB + r] = S;
       __threadfence();
       __syncwarp();
-      if (lane == 0) st_release_gpu(p.ws.flags + (int64_t)chunk * flags_chunk + fw, 1u);
+      if (lane == 0) st_release_gpu(p.ws.flags + sg.slot * NW + warp, 1u);
     }
-    if (chunk > 0) {
-      // every preceding chunk's aggregate: lanes wait on different chunks' flags
+    if (sg.q > 0) {
+      // every preceding segment's aggregate (segment m belongs to item sg.item - q + m):
+      // lanes wait on different segments' flags
       const unsigned want = p.fault_lookback ? 3u : 1u;  // 3 is never written
       bool all_ok = true;
-      for (int base = 0; base < chunk; base += 32) {
-        const int j = base + lane;
+      for (int base = 0; base < sg.q; base += 32) {
+        const int m = base + lane;
         unsigned v = 0;
-        const bool ok = j >= chunk || wait_flag(p.ws.flags + (int64_t)j * flags_chunk + fw, want, p.timeout_ns, &v);
+        bool ok = true;
+        if (m < sg.q) {
+          const int64_t sl_m = seg_slot(p, sg.item - sg.q + m, sg.tile, m);
+          ok = wait_flag(p.ws.flags + sl_m * NW + warp, want, p.timeout_ns, &v);
+        }
         all_ok = __all_sync(0xffffffffu, ok) && all_ok;
       }
       __syncwarp();
@@ -489,8 +525,9 @@ __device__ __forceinline__ void row_program(StreamSmem<RB>& sm, const StreamPara
         err = 1;  // the carry is left out; the error word reports it
       } else {
         float acc = 0.f;
-        for (int j = chunk - 1; j >= 0; --j) {
-          const float4* src = reinterpret_cast<const float4*>(p.ws.agg_h + ((int64_t)j * rows_chunk + my) * NS);
+        for (int m = sg.q - 1; m >= 0; --m) {
+          const int64_t sl_m = seg_slot(p, sg.item - sg.q + m, sg.tile, m);
+          const float4* src = reinterpret_cast<const float4*>(p.ws.agg_h + (sl_m * RB + r) * NS);
 #pragma unroll
           for (int q = 0; q < NS / 4; ++q) {
             const float4 x = __ldcg(src + q);
@@ -501,7 +538,7 @@ __device__ __forceinline__ void row_program(StreamSmem<RB>& sm, const StreamPara
               hin[n] = fmaf(PRECISE ? exp2f(cs.a2[n] * acc) : ex2_approx(cs.a2[n] * acc), xv[i], hin[n]);
             }
           }
-          acc += __ldcg(p.ws.agg_s + (int64_t)j * rows_chunk + my);
+          acc += __ldcg(p.ws.agg_s + sl_m * RB + r);
         }
       }
 #pragma unroll
@@ -509,19 +546,83 @@ __device__ __forceinline__ void row_program(StreamSmem<RB>& sm, const StreamPara
         h[n] = fmaf(PRECISE ? exp2f(cs.a2[n] * S) : ex2_approx(cs.a2[n] * S), hin[n], h[n]);
     }
   }
-  if (p.a.final_state && chunk == p.nchunks - 1 && cs.row_ok) {
+  if (p.a.final_state && last && cs.row_ok) {
     float4* fs = reinterpret_cast<float4*>(p.a.final_state + row * NS);
 #pragma unroll
     for (int q = 0; q < NS / 4; ++q) fs[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
   }
 
-  // ---------------- pass two: the chunk's first stages again, from h_in ----------------
-  if (chunk > 0) {
+  // ---------------- pass two: the segment's first stages again, from h_in ----------------
+  if (sg.q > 0) {
     if (!ac::mbar_wait(ac::smem_u32(&sm.settled), 0u, g.deadline)) err = 1;
     const int n2 = *reinterpret_cast<volatile int*>(&sm.n2);
     float S2 = 0.f, comp2 = 0.f;
     consume<RB, HAS_Z, kUnsettled, PRECISE>(sm, g, cs, r, warp, lane, n1, n2, n2, hin, S2, comp2, err);
   }
+}
+
+// The row's constants (channel ch); `precise` is made warp-uniform: the exact branch
+// serves every row of a warp that has an A = 0 state.
+__device__ __forceinline__ RowConst row_const(const StreamParams& p, int64_t ch, bool row_ok) {
+  RowConst c;
+  c.row_ok = row_ok;
+  c.precise = false;
+  c.a2max = -INFINITY;
+  const float* arow = p.a.A + ch * NS;
+#pragma unroll
+  for (int n = 0; n < NS; ++n) {
+    const float a = row_ok ? arow[n] : 0.f;
+    const bool tiny = fabsf(a) < 8.673617e-19f;  // |A| < 2^-60 counts as A = 0
+    if (row_ok && tiny) c.precise = true;
+    c.a2[n] = tiny ? 0.f : a;
+    c.ia[n] = tiny ? 0.f : 1.f / a;
+    if (row_ok) c.a2max = fmaxf(c.a2max, c.a2[n]);
+  }
+  c.precise = __any_sync(0xffffffffu, c.precise);
+  c.Dc = (row_ok && p.a.D) ? p.a.D[ch] : 0.f;
+  c.bl2 = (row_ok && p.a.bias) ? p.a.bias[ch] * kLog2e : 0.f;
+  return c;
+}
+
+// One segment, from the ring's prologue to its last store: thread r owns row c0 + r.
+template <int RB, bool HAS_Z>
+__device__ __forceinline__ void run_segment(StreamSmem<RB>& sm, const StreamParams& p, const Segment& sg, int kb,
+                                            unsigned long long deadline, int warp, int lane, int& err) {
+  Ring g;
+  g.p = &p;
+  g.deadline = deadline;
+  g.kb = kb;
+  g.b = sg.tile / p.rtiles;
+  g.c0 = (sg.tile % p.rtiles) * RB;
+  g.tc0 = sg.s0 * TS;
+  g.tc1 = (int)min((int64_t)p.a.L, (int64_t)sg.s1 * TS);
+  g.n1 = sg.s1 - sg.s0;
+  g.spec_rows = g.n1 + (sg.q > 0 ? min(2, g.n1) : 0);
+  g.spec_bc = g.n1 + (sg.q > 0 ? min(NB, g.n1) : 0);
+
+  // the first two stages of this warp's rows; the B/C ring filled; every warp converts
+  // its share of the first kAhead stages
+  for (int k = 0; k < 2; ++k) {
+    if (k < g.spec_rows) rows_issue<RB, HAS_Z>(sm, g, k, warp, lane);
+    cp_async_commit();
+  }
+  if (threadIdx.x == 0)
+    for (int j = 0; j < NB && j < g.spec_bc; ++j) bc_issue<RB>(sm, g, j);
+  for (int j = 0; j < kAhead && j < g.spec_bc; ++j) bc_convert<RB>(sm, g, j, warp, lane, err);
+
+  const int r = threadIdx.x;
+  const int nrows = min(RB, (int)p.a.d_inner - g.c0);
+  const bool row_ok = r < nrows;
+  const int64_t ch = g.c0 + (row_ok ? r : 0);
+  const int64_t row = (int64_t)g.b * p.a.d_inner + ch;
+  const RowConst cs = row_const(p, ch, row_ok);
+  float h[NS];
+#pragma unroll
+  for (int n = 0; n < NS; ++n) h[n] = (sg.q == 0 && p.a.h0 && row_ok) ? p.a.h0[row * NS + n] : 0.f;
+  if (cs.precise)
+    row_program<RB, HAS_Z, true>(sm, p, g, cs, h, sg, row, r, warp, lane, err);
+  else
+    row_program<RB, HAS_Z, false>(sm, p, g, cs, h, sg, row, r, warp, lane, err);
 }
 
 template <int RB, bool HAS_Z>
@@ -545,67 +646,48 @@ __global__ void __launch_bounds__(StreamCta<RB>::kThreads) __maxnreg__(StreamCta
     ac::fence_mbar_init();
     sm.n2 = 0;
     sm.issued = 0;
-    sm.ticket = p.nchunks > 1 ? (int)atomicAdd(p.ws.hdr, 1u) : (int)blockIdx.x;
-  }
-  __syncthreads();
-  const int per_chunk = (int)p.a.batch * p.rtiles;
-  const int item = sm.ticket;
-  const int chunk = item / per_chunk;  // chunk-major tickets: a chunk's predecessors started earlier
-  const int rem = item % per_chunk;
-  Ring g;
-  g.p = &p;
-  g.deadline = ac::globaltimer() + (unsigned long long)p.timeout_ns;
-  g.b = rem / p.rtiles;
-  g.c0 = (rem % p.rtiles) * RB;
-  g.tc0 = (int)min((int64_t)p.a.L, (int64_t)chunk * p.chunk_len);
-  g.tc1 = (int)min((int64_t)p.a.L, (int64_t)g.tc0 + p.chunk_len);
-  g.n1 = (g.tc1 - g.tc0 + TS - 1) / TS;
-  g.spec_rows = g.n1 + (chunk > 0 ? min(2, g.n1) : 0);
-  g.spec_bc = g.n1 + (chunk > 0 ? min(NB, g.n1) : 0);
-  int err = 0;
-
-  // the first two stages of this warp's rows; the B/C ring filled; every warp converts
-  // its share of the first kAhead stages
-  for (int k = 0; k < 2; ++k) {
-    if (k < g.spec_rows) rows_issue<RB, HAS_Z>(sm, g, k, warp, lane);
-    cp_async_commit();
-  }
-  if (threadIdx.x == 0) {
+    // tickets in start order: the items a segment's carry waits on started earlier
+    const int64_t item = p.multi ? (int64_t)atomicAdd(p.ws.hdr, 1u) : (int64_t)blockIdx.x;
+    // the item's range of flattened stages, in one tile or across the end of one tile
+    // and the start of the next; with two segments, the next tile's first segment runs
+    // first: it waits for nothing, and later items wait on it
+    const int64_t P0 = item_start(p, item), P1 = item_start(p, item + 1);
+    const int ta = (int)(P0 / p.sl), tb = (int)((P1 - 1) / p.sl);
+    sm.nseg = tb > ta ? 2 : 1;
+    Segment& sa = sm.seg[sm.nseg - 1];
+    sa.item = item;
+    sa.tile = ta;
+    sa.s0 = (int)(P0 - (int64_t)ta * p.sl);
+    sa.s1 = tb > ta ? p.sl : (int)(P1 - (int64_t)ta * p.sl);
+    sa.q = (int)(item - item_owner(p, (int64_t)ta * p.sl));
+    sa.slot = 2 * item;
+    if (tb > ta) {
+      Segment& sb = sm.seg[0];
+      sb.item = item;
+      sb.tile = tb;
+      sb.s0 = 0;
+      sb.s1 = (int)(P1 - (int64_t)tb * p.sl);
+      sb.q = 0;
+      sb.slot = 2 * item + 1;
+    }
     ac::prefetch_tensormap(&p.tm_b);
     ac::prefetch_tensormap(&p.tm_c);
-    for (int j = 0; j < NB && j < g.spec_bc; ++j) bc_issue<RB>(sm, g, j);
   }
-  for (int j = 0; j < kAhead && j < g.spec_bc; ++j) bc_convert<RB>(sm, g, j, warp, lane, err);
-
-  // ---------------- thread r owns row c0 + r ----------------
-  const int r = threadIdx.x;
-  RowConst cs;
-  const int nrows = min(RB, (int)p.a.d_inner - g.c0);
-  cs.row_ok = r < nrows;
-  const int64_t ch = g.c0 + (cs.row_ok ? r : 0);
-  const int64_t row = (int64_t)g.b * p.a.d_inner + ch;
-  float h[NS];
-  cs.precise = false;
-  cs.a2max = -INFINITY;
-  const float* arow = p.a.A + ch * NS;
-#pragma unroll
-  for (int n = 0; n < NS; ++n) {
-    const float a = cs.row_ok ? arow[n] : 0.f;
-    const bool tiny = fabsf(a) < 8.673617e-19f;  // |A| < 2^-60 counts as A = 0
-    if (cs.row_ok && tiny) cs.precise = true;
-    cs.a2[n] = tiny ? 0.f : a;
-    cs.ia[n] = tiny ? 0.f : 1.f / a;
-    if (cs.row_ok) cs.a2max = fmaxf(cs.a2max, cs.a2[n]);
-    h[n] = (chunk == 0 && p.a.h0 && cs.row_ok) ? p.a.h0[row * NS + n] : 0.f;
+  __syncthreads();
+  const unsigned long long deadline = ac::globaltimer() + (unsigned long long)p.timeout_ns;
+  int err = 0;
+  const int nseg = sm.nseg;
+  int kb = 0;
+#pragma unroll 1
+  for (int sgi = 0; sgi < nseg; ++sgi) {
+    run_segment<RB, HAS_Z>(sm, p, sm.seg[sgi], kb, deadline, warp, lane, err);
+    if (sgi + 1 < nseg) {
+      kb = sm.seg[sgi].s1;  // every ring stage of a first segment was issued and consumed
+      cp_async_wait<0>();
+      if (lane == 0) ac::bulk_wait0();
+      __syncthreads();  // the ring and the row buffers are free for the next segment
+    }
   }
-  cs.precise = __any_sync(0xffffffffu, cs.precise);  // warp-uniform: the exact branch serves every row
-  cs.Dc = (cs.row_ok && p.a.D) ? p.a.D[ch] : 0.f;
-  cs.bl2 = (cs.row_ok && p.a.bias) ? p.a.bias[ch] * kLog2e : 0.f;
-
-  if (cs.precise)
-    row_program<RB, HAS_Z, true>(sm, p, g, cs, h, chunk, rem, per_chunk, row, r, warp, lane, err);
-  else
-    row_program<RB, HAS_Z, false>(sm, p, g, cs, h, chunk, rem, per_chunk, row, r, warp, lane, err);
 
   // copies issued ahead of a pass two shorter than the ring, never consumed, must land,
   // and the tensor stores complete, before the CTA exits
@@ -615,7 +697,7 @@ __global__ void __launch_bounds__(StreamCta<RB>::kThreads) __maxnreg__(StreamCta
   if (threadIdx.x == 0) {
     const int issued = sm.issued;
     for (int j = issued - NB < 0 ? 0 : issued - NB; j < issued; ++j)
-      if (!ac::mbar_wait(ac::smem_u32(&sm.full[j % NB]), (uint32_t)(j / NB) & 1u, g.deadline + 1000000000ull))
+      if (!ac::mbar_wait(ac::smem_u32(&sm.full[j % NB]), (uint32_t)(j / NB) & 1u, deadline + 1000000000ull))
         err = 1;
   }
   if (err && p.ws.hdr) atomicOr(p.ws.hdr + 1, kErrTimeout);
@@ -635,18 +717,19 @@ cudaError_t stream_launch_t(const StreamParams& p, int grid, cudaStream_t s) {
 
 size_t stream_smem_bytes_for(int rb) { return rb == 512 ? stream_smem_bytes<512>() : stream_smem_bytes<128>(); }
 
-StreamWs stream_ws_layout(unsigned char* ws, int64_t nchunks, int64_t items, int rb, size_t* total) {
-  // [header][flags: nchunks × items × warps][aggregate h: nchunks × rows × 16][aggregate S: nchunks × rows]
+StreamWs stream_ws_layout(unsigned char* ws, int64_t items, int rb, size_t* total) {
+  // [header][flags: 2 items × warps][aggregate h: 2 items × rows × 16][aggregate S: 2 items × rows]
+  // (an item publishes at most two segments: the one its range starts in and the next tile's first)
   StreamWs w{};
-  const int64_t rows = items * rb, warps = items * (rb / 32);
+  const int64_t slots = 2 * items;
   size_t off = kWsHeaderBytes;
   const size_t flags_off = off;
-  off += ((size_t)nchunks * warps * 4 + 255) & ~size_t(255);
+  off += ((size_t)slots * (rb / 32) * 4 + 255) & ~size_t(255);
   w.flags_bytes = off;
   const size_t aggh_off = off;
-  off += (size_t)nchunks * rows * NS * 4;
+  off += (size_t)slots * rb * NS * 4;
   const size_t aggs_off = off;
-  off += ((size_t)nchunks * rows * 4 + 255) & ~size_t(255);
+  off += ((size_t)slots * rb * 4 + 255) & ~size_t(255);
   *total = off;
   if (ws) {
     w.hdr = reinterpret_cast<unsigned*>(ws);
@@ -658,7 +741,7 @@ StreamWs stream_ws_layout(unsigned char* ws, int64_t nchunks, int64_t items, int
 }
 
 bool stream_supported(const ScanArgs& a) {
-  if (a.act != 1 || a.N != NS) return false;
+  if (a.act != 1 || a.N != NS || a.L < 1) return false;
   if (a.L % 8 != 0 || a.L > (int64_t)INT32_MAX - 64 || a.d_inner > (int64_t)INT32_MAX - 512 || a.batch > 65535)
     return false;
   auto a16 = [](const void* q) { return q == nullptr || (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
@@ -669,17 +752,20 @@ cudaError_t scan_stream_launch(const ScanArgs& a, const ScanPlan& plan, cudaStre
   StreamParams p{};
   p.a = a;
   p.rtiles = plan.ctiles;
-  p.nchunks = plan.nchunks;
-  p.chunk_len = plan.chunk_len;
+  p.sl = (int)((a.L + TS - 1) / TS);
+  p.items = plan.nchunks;
+  const int64_t tiles = a.batch * plan.ctiles;
+  p.ptot = tiles * p.sl;
+  p.multi = p.items > tiles ? 1 : 0;
   const RuntimeKnobs knobs = runtime_knobs();
   p.timeout_ns = knobs.lookback_timeout_ns > 0 ? knobs.lookback_timeout_ns
                                                : 1000ll * 1000 * 1000 + plan.chunk_len * 100ll;
   p.fault_lookback = knobs.fault_lookback ? 1 : 0;
   const int rb = plan.rows_per_cta;
   size_t total = 0;
-  // one chunk: no workspace is required; if one is given its header takes the error word
-  p.ws = stream_ws_layout(plan.nchunks > 1 ? a.ws : nullptr, plan.nchunks, a.batch * plan.ctiles, rb, &total);
-  if (plan.nchunks == 1) p.ws.hdr = reinterpret_cast<unsigned*>(a.ws);
+  // one segment per tile: no workspace is required; if one is given its header takes the error word
+  p.ws = stream_ws_layout(p.multi ? a.ws : nullptr, p.items, rb, &total);
+  if (!p.multi) p.ws.hdr = reinterpret_cast<unsigned*>(a.ws);
   // tensor maps of B and C as [batch][L][16] bf16 (tokens past L read as zero)
   const uint64_t L = (uint64_t)a.L, Bt = (uint64_t)a.batch;
   const uint64_t dims_bc[3] = {(uint64_t)NS, L, Bt}, str_bc[2] = {NS * 2, L * NS * 2};
@@ -697,11 +783,11 @@ cudaError_t scan_stream_launch(const ScanArgs& a, const ScanPlan& plan, cudaStre
       !encode_tensor_map(&p.tm_out, bf, 3, a.out, dims_row, str_row, box_row, CU_TENSOR_MAP_SWIZZLE_64B,
                          CU_TENSOR_MAP_L2_PROMOTION_NONE))
     return cudaErrorInvalidValue;
-  if (plan.nchunks > 1) {
+  if (p.multi) {
     const cudaError_t e = cudaMemsetAsync(a.ws, 0, p.ws.flags_bytes, stream);
     if (e != cudaSuccess) return e;
   }
-  const int grid = (int)((int64_t)plan.nchunks * a.batch * plan.ctiles);
+  const int grid = p.items;
   const bool hz = a.z != nullptr;
   if (rb == 512) return hz ? stream_launch_t<512, true>(p, grid, stream) : stream_launch_t<512, false>(p, grid, stream);
   return hz ? stream_launch_t<128, true>(p, grid, stream) : stream_launch_t<128, false>(p, grid, stream);

@@ -46,6 +46,7 @@ RuntimeKnobs* load_knobs() {
     const int v = std::atoi(c);
     r->stream_rows = (v == 512 || v == 128) ? v : 0;
   }
+  if (const char* c = std::getenv("SSM_STREAM_CTAS")) r->stream_ctas = std::atoi(c);
   return r;
 }
 

@@ -72,6 +72,7 @@ struct RuntimeKnobs {
   int bwd_chunks;                 // >0: sequence chunks of the backward (tests)
   bool fault_ssd;                 // test hook: the SSD output kernel's first wait never completes
   int stream_rows;                // >0: rows per CTA of the streamed row kernel (512, 256 or 128)
+  int stream_ctas;                // >0: work items (CTAs) of the streamed row kernel
 };
 RuntimeKnobs runtime_knobs();  // the test hooks as last loaded (first use, or ssm_test_hooks_reload)
 void reload_knobs();
@@ -91,7 +92,7 @@ struct StreamWs {
   float* agg_s;
   size_t flags_bytes;  // bytes from the start that are cleared per call (header + flags)
 };
-StreamWs stream_ws_layout(unsigned char* ws, int64_t nchunks, int64_t items, int rows_per_cta, size_t* total);
+StreamWs stream_ws_layout(unsigned char* ws, int64_t work_items, int rows_per_cta, size_t* total);
 bool stream_supported(const ScanArgs& a);
 int take_driver_error();  // CUresult of the calling thread's last failed driver call (then cleared), or 0  // dtype, d_state, alignment and size limits
 size_t stream_smem_bytes_for(int rows_per_cta);

@@ -111,6 +111,34 @@ def test_initial_state(stream, chunks):
     compare(inp, h0=h0)
 
 
+@pytest.mark.parametrize("ctas", [3, 5, 7, 11])
+def test_work_items_across_tiles(stream, ctas):
+    """Item counts that are not a multiple of the row tiles: ranges end one tile's
+    sequence and start the next's, so segments differ in length and a CTA runs two (the
+    next tile's first segment, then the end of its own)."""
+    stream.set("SSM_STREAM_CTAS", ctas)
+    inp = W.random_scan_inputs(2, 130, 16, 32 * 37 + 8, dtype=torch.bfloat16, device=DEV, seed=80 + ctas,
+                               a_kind="random")
+    compare(inp)
+    h0 = torch.randn((2, 130, 16), generator=torch.Generator(device=DEV).manual_seed(ctas), device=DEV)
+    compare(inp, h0=h0)
+
+
+def test_item_count_does_not_change_results(stream):
+    """The same scan cut into 1, 5 and 9 work items per tile-sequence agrees to the output
+    rounding, and so do its final states."""
+    inp = W.random_scan_inputs(3, 200, 16, 3000, dtype=torch.bfloat16, device=DEV, seed=90)
+    res = []
+    for ctas in (1, 5, 9):
+        stream.set("SSM_STREAM_CTAS", ctas * 3)
+        res.append(ssm.scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                inp["bias"], return_final_state=True))
+    torch.cuda.synchronize()
+    for out, fs in res[1:]:
+        assert rel_err(to_np(out), to_np(res[0][0])) <= 2 * 2.0 ** -8
+        assert rel_err(to_np(fs), to_np(res[0][1])) <= 1e-5
+
+
 def test_chunking_does_not_change_results(stream):
     """Every output is computed from its true state and rounded once, chunked or not."""
     inp = W.random_scan_inputs(2, 256, 16, 4000, dtype=torch.bfloat16, device=DEV, seed=51)
