@@ -17,7 +17,8 @@
 // row).  The thread
 // holding the row's last token writes the final state.
 // conv1d_step_kernel: one thread per row shifts the W-1 carried inputs, appends
-// x and writes out.
+// x and writes out; conv1d_step4_kernel does the same for four consecutive channels
+// with vector accesses (bf16, width 4).
 #include <algorithm>
 #include <cstdint>
 
@@ -217,6 +218,52 @@ __global__ void __launch_bounds__(kConvBlock) conv1d_step_kernel(const ConvArgs 
   }
 }
 
+// Decode step for bf16 and width 4 (Mamba's): a thread owns four consecutive channels of
+// one batch row, so that x and out (8 bytes), the carried inputs (24 bytes), the taps
+// (64 bytes) and the bias (16 bytes) move as whole vectors; the taps are applied in the
+// order of conv1d_step_kernel, so both give the same bits.
+__device__ __forceinline__ float bf16_at(const unsigned (&w)[6], int i) {
+  return __uint_as_float((i & 1) ? (w[i >> 1] & 0xffff0000u) : (w[i >> 1] << 16));
+}
+__device__ __forceinline__ unsigned pack2_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<unsigned*>(&h);
+}
+__global__ void __launch_bounds__(kConvBlock) conv1d_step4_kernel(const ConvArgs a) {
+  const int64_t c = 4 * ((int64_t)blockIdx.x * kConvBlock + threadIdx.x);
+  if (c >= a.d_inner) return;
+  const int64_t row = (int64_t)blockIdx.y * a.d_inner + c;
+  const uint2 xw = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.x) + row);
+  uint2* sp = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.stateT) + row * 3);
+  const uint2 s0 = sp[0], s1 = sp[1], s2 = sp[2];  // channel k's three carried inputs: values 3k .. 3k + 2
+  const float4* w4 = reinterpret_cast<const float4*>(a.w + c * 4);
+  const float4 wq[4] = {__ldg(w4), __ldg(w4 + 1), __ldg(w4 + 2), __ldg(w4 + 3)};
+  const float4 bq = a.bias ? __ldg(reinterpret_cast<const float4*>(a.bias + c)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const unsigned sw[6] = {s0.x, s0.y, s1.x, s1.y, s2.x, s2.y};
+  const float xs[4] = {__uint_as_float(xw.x << 16), __uint_as_float(xw.x & 0xffff0000u),
+                       __uint_as_float(xw.y << 16), __uint_as_float(xw.y & 0xffff0000u)};
+  const float bs[4] = {bq.x, bq.y, bq.z, bq.w};
+  float y[4], ns[12];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float s_0 = bf16_at(sw, 3 * k), s_1 = bf16_at(sw, 3 * k + 1), s_2 = bf16_at(sw, 3 * k + 2);
+    float pre = bs[k];
+    pre = fmaf(wq[k].x, s_0, pre);
+    pre = fmaf(wq[k].y, s_1, pre);
+    pre = fmaf(wq[k].z, s_2, pre);
+    pre = fmaf(wq[k].w, xs[k], pre);
+    y[k] = silu_c<true>(pre);
+    ns[3 * k] = s_1;
+    ns[3 * k + 1] = s_2;
+    ns[3 * k + 2] = xs[k];
+  }
+  *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + row) =
+      make_uint2(pack2_bf16(y[0], y[1]), pack2_bf16(y[2], y[3]));
+  sp[0] = make_uint2(pack2_bf16(ns[0], ns[1]), pack2_bf16(ns[2], ns[3]));
+  sp[1] = make_uint2(pack2_bf16(ns[4], ns[5]), pack2_bf16(ns[6], ns[7]));
+  sp[2] = make_uint2(pack2_bf16(ns[8], ns[9]), pack2_bf16(ns[10], ns[11]));
+}
+
 template <typename T, int W>
 cudaError_t fwd_w(const ConvArgs& a, bool vec, cudaStream_t s) {
   // CTA width: enough warps for the row, at most kConvBlock threads
@@ -281,6 +328,14 @@ cudaError_t conv1d_step_launch(const ConvCall& k, cudaStream_t stream) {
   a.x = k.x; a.w = k.w; a.bias = k.bias; a.out = k.out; a.stateT = k.state_out;
   a.rows = k.batch * k.d_inner; a.d_inner = k.d_inner; a.L = 1; a.W = k.W;
   if (k.batch > kMaxConvGridYZ) return cudaErrorInvalidConfiguration;
+  auto al = [](const void* q, unsigned n) { return (reinterpret_cast<uintptr_t>(q) & (n - 1u)) == 0; };
+  if (k.act == 1 && k.W == 4 && k.d_inner % 4 == 0 && al(k.x, 8) && al(k.out, 8) && al(k.state_out, 8) &&
+      al(k.w, 16) && (!k.bias || al(k.bias, 16))) {
+    const int64_t per_cta = (int64_t)kConvBlock * 4;
+    const dim3 grid((unsigned)((k.d_inner + per_cta - 1) / per_cta), (unsigned)k.batch);
+    conv1d_step4_kernel<<<grid, kConvBlock, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
   const int64_t per_cta = (int64_t)kConvBlock * kStepItems;
   const dim3 grid((unsigned)((k.d_inner + per_cta - 1) / per_cta), (unsigned)k.batch);
   return k.act == 1 ? step_dt<__nv_bfloat16>(a, grid, stream) : step_dt<float>(a, grid, stream);

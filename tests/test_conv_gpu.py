@@ -64,10 +64,14 @@ def test_conv_unaligned_views(dtype):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
 @pytest.mark.parametrize("width", [1, 2, 4, 8])
-def test_conv_step_matches_oracle_and_fwd(dtype, width):
-    inp = W.conv_inputs(3, 50, 12, width, dtype=dtype, device=DEV, seed=width)
+@pytest.mark.parametrize("d_inner", [50, 1028])
+def test_conv_step_matches_oracle_and_fwd(dtype, width, d_inner):
+    """d_inner 1028 with bf16 and width 4 takes the four-channels-per-thread vector kernel,
+    the other cases the per-channel one; both match the oracle and the sequence form bit
+    for bit."""
+    inp = W.conv_inputs(3, d_inner, 12, width, dtype=dtype, device=DEV, seed=width)
     state = inp["state"].clone() if width > 1 else None
-    ref_state = to_np(inp["state"]) if width > 1 else np.zeros((3, 50, 0))
+    ref_state = to_np(inp["state"]) if width > 1 else np.zeros((3, d_inner, 0))
     outs = []
     for t in range(12):
         x = inp["x"][:, :, t].contiguous()
