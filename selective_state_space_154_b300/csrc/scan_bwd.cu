@@ -148,6 +148,80 @@ __device__ __forceinline__ void row_scalars(StageSmem& sm, const BwdArgs& p, int
   }
 }
 
+// The next block's raw inputs, copied by cp.async while the current block computes
+// (bf16, d_state 16, rows of 16-byte aligned 8-token pieces: L % 8 == 0); the block's
+// scalars are then formed from shared memory instead of waiting on global loads.
+struct RawBlock {
+  uint4 act[4][kBwdRows];   // u, Δraw, dout, z: a row's 8 tokens (bf16)
+  uint4 bc[2][16];          // B, C: 8 tokens × 16 states (bf16)
+  float4 ck[kBwdThreads];   // the block's chunk-local starting state (gradient kernel)
+  float scum[kBwdRows];     // ΣΔ from the chunk's start to the block (gradient kernel)
+};
+
+__device__ __forceinline__ void raw_issue(RawBlock& rb, const BwdArgs& p, const BwdWs& w, int64_t b, int64_t c0,
+                                          int64_t rt, int64_t blk, bool with_grad, bool with_ck) {
+  const int64_t t0 = blk * kBwdTok;
+  const int tid = threadIdx.x;
+  {  // 4 tensors × 64 rows: one 16-byte piece per thread
+    const int wt = tid / kBwdRows, rr = tid % kBwdRows;
+    const void* base = wt == 0 ? p.u : (wt == 1 ? p.delta : (wt == 2 ? p.dout : p.z));
+    const int64_t c = c0 + rr;
+    const bool ok = c < p.d_inner && base != nullptr && (wt < 2 || with_grad);
+    const __nv_bfloat16* src =
+        static_cast<const __nv_bfloat16*>(ok ? base : p.u) + (ok ? (b * p.d_inner + c) * p.L + t0 : 0);
+    cp_async16(&rb.act[wt][rr], src, ok ? 16 : 0);
+  }
+  if (tid < 32) {  // B and C: 256 bytes each
+    const int wt = tid / 16, qq = tid % 16;
+    cp_async16(&rb.bc[wt][qq], static_cast<const __nv_bfloat16*>(wt ? p.C : p.B) + (b * p.L + t0) * kBwdN + qq * 8,
+               16);
+  }
+  if (with_ck) {
+    const int64_t slot = rt * p.nblk + blk;
+    cp_async16(&rb.ck[tid], w.ck + slot * kBwdThreads + tid, 16);
+    if (tid < kBwdRows / 4) cp_async16(&rb.scum[tid * 4], w.scum + slot * kBwdRows + tid * 4, 16);
+  }
+}
+
+// stage_bc and row_scalars from a raw copy (bf16, full blocks)
+__device__ __forceinline__ void stage_bc_raw(StageSmem& sm, const RawBlock& rb) {
+  for (int i = threadIdx.x; i < kBwdTok * 2 * kBwdN; i += kBwdThreads) {
+    const int v = i / (2 * kBwdN), wt = (i / kBwdN) & 1, n = i % kBwdN;
+    sm.bc[v][wt][n] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(rb.bc[wt])[v * kBwdN + n]);
+  }
+}
+__device__ __forceinline__ void row_scalars_raw(StageSmem& sm, const RawBlock& rb, const BwdArgs& p, int r, int g,
+                                                bool row_ok, float biasc, bool with_grad) {
+  const __nv_bfloat16* U = reinterpret_cast<const __nv_bfloat16*>(&rb.act[0][r]);
+  const __nv_bfloat16* Dr = reinterpret_cast<const __nv_bfloat16*>(&rb.act[1][r]);
+  const __nv_bfloat16* Go = reinterpret_cast<const __nv_bfloat16*>(&rb.act[2][r]);
+  const __nv_bfloat16* Z = reinterpret_cast<const __nv_bfloat16*>(&rb.act[3][r]);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int v = g + 4 * k;
+    TokScalars s{};
+    if (row_ok) {
+      s.x = __bfloat162float(U[v]);
+      const float rr = __bfloat162float(Dr[v]) + biasc;
+      s.dt = softplus_fast(rr);
+      if (with_grad) {
+        s.sig = rcp_approx(1.f + ex2_approx(-rr * kLog2e));
+        const float go = __bfloat162float(Go[v]);
+        if (p.z) {
+          const float zv = __bfloat162float(Z[v]);
+          const float sz = rcp_approx(1.f + ex2_approx(-zv * kLog2e));
+          s.dy = go * zv * sz;
+          s.dzf = go * sz * (1.f + zv * (1.f - sz));
+        } else {
+          s.dy = go;
+          s.dzf = 0.f;
+        }
+      }
+    }
+    sm.ts[v][r] = s;
+  }
+}
+
 // Reduce-scatter over the warp's 8 rows (lane bits 2..4) of 8 values per lane:
 // afterwards lane l holds, for its quad g = l & 3, the sum over the rows of
 // value (l >> 2).
@@ -275,10 +349,11 @@ __device__ __forceinline__ CtaPos cta_pos(const BwdArgs& p) {
 
 // Launch 1: each chunk forward from h = 0, saving the local states, the prefix
 // sums of Δ and the chunk's summary (end state, ΣΔ, adjoint sent left).
-template <typename T>
+template <typename T, bool PF>
 __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_chunk_kernel(const BwdArgs p, const BwdWs w) {
   constexpr bool FAST = Act<T>::kFast;
   __shared__ StageSmem sm;
+  __shared__ RawBlock raw[PF ? 2 : 1];
   const CtaPos o = cta_pos(p);
   const int r = o.r, g = o.g;
   const Quad q = load_quad<FAST>(p.A, o.c, g, (int)p.N, o.row_ok);
@@ -286,6 +361,11 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_chunk_kernel(const Bw
   const bool want_g = o.chunk > 0;  // chunk 0 sends no adjoint further left
   float h[kBwdG] = {0.f, 0.f, 0.f, 0.f}, P[kBwdG] = {1.f, 1.f, 1.f, 1.f}, G[kBwdG] = {0.f, 0.f, 0.f, 0.f};
   float S = 0.f;
+  const int64_t c0 = (o.rt % p.ctiles) * kBwdRows;
+  if (PF && o.blk0 < o.blk1) {
+    raw_issue(raw[0], p, w, o.b, c0, o.rt, o.blk0, want_g, false);
+    cp_async_commit();
+  }
   for (int64_t blk = o.blk0; blk < o.blk1; ++blk) {
     const int64_t t0 = blk * kBwdTok;
     const int nv = (int)(p.L - t0 < kBwdTok ? p.L - t0 : kBwdTok);
@@ -293,8 +373,18 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_chunk_kernel(const Bw
     w.ck[slot * kBwdThreads + threadIdx.x] = make_float4(h[0], h[1], h[2], h[3]);
     if (g == 0) w.scum[slot * kBwdRows + r] = S;
     __syncthreads();  // the previous block's staging is no longer read
-    stage_bc<T>(sm, p, o.b, t0, nv);
-    row_scalars<T>(sm, p, r, g, o.row_ok, o.row, t0, nv, biasc, want_g);
+    if (PF) {
+      const int i = (int)(blk - o.blk0);
+      if (blk + 1 < o.blk1) raw_issue(raw[(i + 1) & 1], p, w, o.b, c0, o.rt, blk + 1, want_g, false);
+      cp_async_commit();
+      cp_async_wait<1>();  // this block's copies (the next block's may still be in flight)
+      __syncthreads();
+      stage_bc_raw(sm, raw[i & 1]);
+      row_scalars_raw(sm, raw[i & 1], p, r, g, o.row_ok, biasc, want_g);
+    } else {
+      stage_bc<T>(sm, p, o.b, t0, nv);
+      row_scalars<T>(sm, p, r, g, o.row_ok, o.row, t0, nv, biasc, want_g);
+    }
     __syncthreads();
     auto token = [&](int v) {
       const TokScalars s = sm.ts[v][r];
@@ -339,11 +429,12 @@ __global__ void __launch_bounds__(kBwdThreads, 4) scan_bwd_chunk_kernel(const Bw
 }
 
 // Launch 2: the gradients over one chunk, from the combined chunk summaries.
-template <typename T>
+template <typename T, bool PF>
 __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs p, const BwdWs w) {
   constexpr bool FAST = Act<T>::kFast;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw);
+  RawBlock* raw = reinterpret_cast<RawBlock*>(smem_raw + sizeof(BwdSmem));  // [2] when PF
   const int N = (int)p.N;
   const int64_t L = p.L;
   const CtaPos o = cta_pos(p);
@@ -381,18 +472,38 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
   // blocks in reverse, adjoint recurrence
   float h[kBwdG], dA_acc[kBwdG] = {0.f, 0.f, 0.f, 0.f};
   float dD_acc = 0.f, db_acc = 0.f;
+  const int64_t c0 = (o.rt % p.ctiles) * kBwdRows;
+  if (PF && o.blk0 < o.blk1) {
+    raw_issue(raw[0], p, w, b, c0, o.rt, o.blk1 - 1, true, true);
+    cp_async_commit();
+  }
   for (int64_t blk = o.blk1 - 1; blk >= o.blk0; --blk) {
     const int64_t t0 = blk * kBwdTok;
     const int nv = (int)(L - t0 < kBwdTok ? L - t0 : kBwdTok);
     const int64_t slot = o.rt * p.nblk + blk;
     __syncthreads();  // bc, ts, hs and red of the previous block are no longer read
-    stage_bc<T>(sm.st, p, b, t0, nv);
-    row_scalars<T>(sm.st, p, r, g, row_ok, row, t0, nv, biasc, true);
+    float4 h0v;
+    float scum;
+    if (PF) {
+      const int i = (int)(o.blk1 - 1 - blk);
+      if (blk - 1 >= o.blk0) raw_issue(raw[(i + 1) & 1], p, w, b, c0, o.rt, blk - 1, true, true);
+      cp_async_commit();
+      cp_async_wait<1>();  // this block's copies (the next block's may still be in flight)
+      __syncthreads();
+      stage_bc_raw(sm.st, raw[i & 1]);
+      row_scalars_raw(sm.st, raw[i & 1], p, r, g, row_ok, biasc, true);
+      h0v = raw[i & 1].ck[threadIdx.x];
+      scum = raw[i & 1].scum[r];
+    } else {
+      stage_bc<T>(sm.st, p, b, t0, nv);
+      row_scalars<T>(sm.st, p, r, g, row_ok, row, t0, nv, biasc, true);
+      h0v = w.ck[slot * kBwdThreads + threadIdx.x];
+      scum = w.scum[slot * kBwdRows + r];
+    }
     // the block's starting state: chunk-local + decay since the chunk's start × h_in
-    float4 h0v = w.ck[slot * kBwdThreads + threadIdx.x];
     if (o.chunk > 0) {
       float e[kBwdG];
-      decay4<FAST>(q, w.scum[slot * kBwdRows + r], e);
+      decay4<FAST>(q, scum, e);
       h0v.x = fmaf(e[0], hin[0], h0v.x);
       h0v.y = fmaf(e[1], hin[1], h0v.y);
       h0v.z = fmaf(e[2], hin[2], h0v.z);
@@ -615,10 +726,10 @@ int pick_bwd_chunks(int64_t R, int64_t nblk, int64_t slots, int64_t kmax) {
   return best;
 }
 
-template <typename T>
+template <typename T, bool PF>
 cudaError_t bwd_launch_t(BwdArgs p, cudaStream_t s) {
-  cudaError_t e =
-      cudaFuncSetAttribute(scan_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(BwdSmem));
+  const size_t smem = sizeof(BwdSmem) + (PF ? 2 * sizeof(RawBlock) : 0);
+  cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<T, PF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t R = p.batch * p.ctiles;
   if (R == 0) return cudaSuccess;
@@ -627,8 +738,8 @@ cudaError_t bwd_launch_t(BwdArgs p, cudaStream_t s) {
     int dev = 0, sms = 0, occ = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, scan_bwd_kernel<T>, kBwdThreads,
-                                                           sizeof(BwdSmem))) != cudaSuccess)
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, scan_bwd_kernel<T, PF>, kBwdThreads, smem)) !=
+        cudaSuccess)
       return e;
     k = pick_bwd_chunks(R, p.nblk, (int64_t)(sms > 0 ? sms : 1) * (occ > 0 ? occ : 1), p.kmax);
   }
@@ -639,14 +750,22 @@ cudaError_t bwd_launch_t(BwdArgs p, cudaStream_t s) {
   p.nchunks = p.cblk > 0 ? (int)((p.nblk + p.cblk - 1) / p.cblk) : 1;
   const BwdWs w = ws_layout(p.ckpt, R, p.nblk, p.kmax);
   const dim3 grid((unsigned)R, (unsigned)p.nchunks);
-  scan_bwd_chunk_kernel<T><<<grid, kBwdThreads, 0, s>>>(p, w);
+  scan_bwd_chunk_kernel<T, PF><<<grid, kBwdThreads, 0, s>>>(p, w);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  scan_bwd_kernel<T><<<grid, kBwdThreads, sizeof(BwdSmem), s>>>(p, w);
+  scan_bwd_kernel<T, PF><<<grid, kBwdThreads, smem, s>>>(p, w);
   if ((e = cudaGetLastError()) != cudaSuccess || !p.det) return e;
   const int64_t items = p.batch * p.L * 2 * p.N + p.d_inner * (p.N + 2);
   const int64_t blocks = (items + 255) / 256;
   scan_bwd_reduce_kernel<<<(unsigned)(blocks < 148 * 16 ? blocks : 148 * 16), 256, 0, s>>>(p);
   return cudaGetLastError();
+}
+
+// The raw-copy prefetch needs bf16 rows of whole 16-byte pieces: d_state 16, L % 8 == 0
+// and every activation array 16-byte aligned.
+bool bwd_prefetch_ok(const BwdArgs& p) {
+  auto a16 = [](const void* q) { return q == nullptr || (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  return p.act == 1 && p.N == kBwdN && p.L % kBwdTok == 0 && a16(p.u) && a16(p.delta) && a16(p.dout) &&
+         a16(p.z) && a16(p.B) && a16(p.C);
 }
 
 }  // namespace
@@ -688,7 +807,9 @@ cudaError_t scan_bwd_launch(BwdArgs p, cudaStream_t stream) {
     p.part_bc = reinterpret_cast<float*>(base + z.base);
     p.part_row = reinterpret_cast<float*>(base + z.base + z.part_bc);
   }
-  return p.act == 1 ? bwd_launch_t<__nv_bfloat16>(p, stream) : bwd_launch_t<float>(p, stream);
+  if (p.act != 1) return bwd_launch_t<float, false>(p, stream);
+  return bwd_prefetch_ok(p) ? bwd_launch_t<__nv_bfloat16, true>(p, stream)
+                            : bwd_launch_t<__nv_bfloat16, false>(p, stream);
 }
 
 }  // namespace ssm

@@ -155,3 +155,25 @@ def test_bwd_deterministic_fp32_no_optional():
             continue
         e = rel_err(to_np(g[k]), r[k])
         assert e <= TOL[torch.float32], f"{k}: rel err {e:.3e}"
+
+
+@pytest.mark.parametrize("chunks", [1, 3, 7])
+@pytest.mark.parametrize("gate", [True, False], ids=["z", "no_z"])
+def test_bwd_prefetched_blocks(hooks, chunks, gate):
+    """bf16 with d_state 16 and L a multiple of 8: both kernels copy the next block's raw
+    inputs (and the gradient kernel its checkpoint) by cp.async while the current block
+    computes; across chunk counts, with and without the gate, in both modes."""
+    hooks.set("SSM_BWD_CHUNKS", str(chunks))
+    inp = W.random_scan_inputs(2, 150, 16, 512, dtype=torch.bfloat16, device=DEV, seed=40 + chunks, a_kind="random",
+                               gate=gate)
+    dout = _dout(inp, 41)
+    _compare(inp, dout, TOL[torch.bfloat16])
+    g = ssm.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dout, D=inp.get("D"), z=inp.get("z"),
+                     delta_bias=inp.get("bias"), deterministic=True)
+    torch.cuda.synchronize()
+    r = _ref(inp, dout)
+    for k in GRADS:
+        if r[k] is None or g[k] is None:
+            continue
+        e = rel_err(to_np(g[k]), r[k])
+        assert e <= TOL[torch.bfloat16], f"{k}: rel err {e:.3e}"
