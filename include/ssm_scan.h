@@ -392,7 +392,7 @@ SSM_API ssm_status ssd_step(float* state, const void* x, const void* dt, const f
  * call reads the environment.  They exist for the test suite (forcing a kernel,
  * a chunk count, or a device-side wait that never completes) and are not part of
  * the supported interface:
- *   SSM_FORCE_KERNEL = tiles | rows | stream   scan kernel, where the shape allows it
+ *   SSM_FORCE_KERNEL = tiles | rows | stream | tiny   scan kernel, where the shape allows it
  *   SSM_FORCE_CHUNKS = n        sequence chunks of the scan
  *   SSM_FORCE_TPR = 2           two threads per row in the row kernel
  *   SSM_CTAS_PER_SM = n         resident CTAs per SM assumed by the row kernel's planner

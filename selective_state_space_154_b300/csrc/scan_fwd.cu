@@ -567,12 +567,29 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
   }
   // bf16, 16 states, 16-byte aligned rows, L a multiple of 8: the streamed row kernel
   if (kind == kScanRows && stream_supported(a)) kind = kScanStream;
+  // a handful of rows × states over a short sequence: the token-parallel kernel
+  if (tiny_supported(a) && rows * a.N <= kTinyMaxItems) kind = kScanTiny;
   if (knobs.force_kind >= 0) {
     const bool ok = knobs.force_kind == kScanTiles || (knobs.force_kind == kScanRows && a.N <= 16) ||
-                    (knobs.force_kind == kScanStream && stream_supported(a));
+                    (knobs.force_kind == kScanStream && stream_supported(a)) ||
+                    (knobs.force_kind == kScanTiny && tiny_supported(a));
     if (ok) kind = knobs.force_kind;
   }
   pl.kind = kind;
+  if (kind == kScanTiny) {
+    // one CTA of 32·N threads per row, no chunks, no workspace
+    pl.npad = (int)a.N;
+    pl.groups = 1;
+    pl.threads = 32 * (int)a.N;
+    pl.rows_per_cta = 1;
+    pl.ctiles = (int)a.d_inner;
+    pl.nchunks = 1;
+    pl.chunk_len = a.L;
+    pl.smem_bytes = (size_t)a.N * (size_t)a.L * sizeof(float);
+    pl.ws_flags_off = pl.ws_agg_off = pl.ws_bytes = 0;
+    *plan = pl;
+    return true;
+  }
   if (kind == kScanStream) {
     // CTAs of 512 rows (one per SM) over wide layers, else 128 (three per SM)
     const int rb = knobs.stream_rows == 128 || (knobs.stream_rows != 512 && a.d_inner < 512) ? 128 : 512;
@@ -660,6 +677,7 @@ bool scan_make_plan(const ScanArgs& a, ScanPlan* plan) {
 cudaError_t scan_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream) {
   if (plan.kind == kScanRows) return scan_rows_launch(a, plan, stream);
   if (plan.kind == kScanStream) return scan_stream_launch(a, plan, stream);
+  if (plan.kind == kScanTiny) return scan_tiny_launch(a, stream);
   KParams p{};
   p.a = a;
   p.npad = plan.npad;

@@ -38,6 +38,7 @@ RuntimeKnobs* load_knobs() {
     if (std::strcmp(k, "tiles") == 0) r->force_kind = kScanTiles;
     if (std::strcmp(k, "rows") == 0) r->force_kind = kScanRows;
     if (std::strcmp(k, "stream") == 0) r->force_kind = kScanStream;
+    if (std::strcmp(k, "tiny") == 0) r->force_kind = kScanTiny;
   }
   if (const char* c = std::getenv("SSM_CTAS_PER_SM")) r->ctas_per_sm = std::atoi(c);
   if (const char* c = std::getenv("SSM_FORCE_TPR")) r->force_tpr = std::atoi(c);

@@ -20,7 +20,12 @@ constexpr int kRowTokensPerStage = 32;  // row kernel: tokens per stage
 template <typename T>
 __host__ __device__ constexpr float corr_stop_log2() { return sizeof(T) == 2 ? -12.f : -24.f; }
 
-enum ScanKind { kScanTiles = 0, kScanRows = 1, kScanStream = 2 };
+enum ScanKind { kScanTiles = 0, kScanRows = 1, kScanStream = 2, kScanTiny = 3 };
+
+// Small problems (rows × states ≤ kTinyMaxItems, L ≤ kTinyMaxSeq, d_state ≤ 32): the
+// token-parallel kernel of scan_tiny.cu.
+constexpr int kTinyMaxSeq = 256;
+constexpr int64_t kTinyMaxItems = 2048;
 
 // Workspace header (bytes): [0] ticket counter, [1] error word.
 constexpr size_t kWsHeaderBytes = 256;
@@ -98,6 +103,8 @@ int take_driver_error();  // CUresult of the calling thread's last failed driver
 size_t stream_smem_bytes_for(int rows_per_cta);
 constexpr int kStreamTokensPerStage = 32;  // streamed row kernel: tokens per stage
 cudaError_t scan_stream_launch(const ScanArgs& a, const ScanPlan& plan, cudaStream_t stream);
+bool tiny_supported(const ScanArgs& a);
+cudaError_t scan_tiny_launch(const ScanArgs& a, cudaStream_t stream);
 
 struct StepArgs {
   float* state;

@@ -21,14 +21,15 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.fixture(params=["tiles", "rows", "rows2", "stream"])
+@pytest.fixture(params=["tiles", "rows", "rows2", "stream", "tiny"])
 def kernel(request, hooks):
     """Run the test through each scan kernel: the tile kernel, the row kernel with
-    one thread per row, the row kernel with two threads per row, and the streamed
-    row kernel (the row kernels serve d_state <= 16, the streamed one bf16 with
-    d_state 16, 16-byte aligned rows and L a multiple of 8; other shapes fall back
-    to the planner's choice)."""
-    hooks.set("SSM_FORCE_KERNEL", {"tiles": "tiles", "stream": "stream"}.get(request.param, "rows"))
+    one thread per row, the row kernel with two threads per row, the streamed
+    row kernel and the token-parallel kernel for small problems (the row kernels
+    serve d_state <= 16, the streamed one bf16 with d_state 16, 16-byte aligned rows
+    and L a multiple of 8, the token-parallel one d_state <= 32 and L <= 256; other
+    shapes fall back to the planner's choice)."""
+    hooks.set("SSM_FORCE_KERNEL", {"tiles": "tiles", "stream": "stream", "tiny": "tiny"}.get(request.param, "rows"))
     if request.param == "rows2":
         hooks.set("SSM_FORCE_TPR", "2")
     return request.param
