@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(kBlock) step_kernel(const StepArgs p, int64_t 
 
 // ------------------------------------------------------------ pipelined kernel
 constexpr int kTileFloats = 2048;   // fp32 state per tile: 8 KB
-constexpr int kPipeStages = 6;      // tiles in shared memory per CTA
-constexpr int kRefillLag = 2;       // a tile's buffer is refilled this many tiles after its store was issued
+constexpr int kPipeStages = 5;      // tiles in shared memory per CTA
+constexpr int kRefillLag = 1;       // a tile's buffer is refilled this many tiles after its store was issued
 constexpr int kPipeBarBytes = 128;  // mbarriers (one per stage + one never-completed) at the front
 
 __device__ unsigned g_step_error;  // sticky: a pipelined step gave up waiting (read by ssm_step_check)
