@@ -7,10 +7,10 @@
 //    registers; the readout Σ_n C_n h_n needs no other thread;
 //  * a CTA owns RB rows of one batch over one chunk of the sequence, walked in stages
 //    of 32 tokens, and no warp ever waits for another warp's rows:
-//      - each warp copies its own 32 rows' u, Δraw and z tiles (64 bytes of a row per
-//        tensor, four lanes per row) into a double buffer of its own with cp.async, one
-//        stage ahead, and writes its outputs back the same way: in place of u in shared
-//        memory, then out in 64-byte row segments;
+//      - each warp copies its own 32 rows' u, Δraw and z tiles ([32 rows × 32 tokens]
+//        tensor copies issued by its lane 0, counted on an mbarrier of its own) into a
+//        double buffer of its own, one stage ahead, and writes its outputs back the same
+//        way: in place of u in shared memory, then one tensor store;
 //      - B and C of a stage, shared by all rows, come by tensor (TMA) copy into a ring of
 //        four stages; the warp that releases a stage last refills it, and every warp
 //        converts a share of each stage to fp32 two stages before its use (an mbarrier
@@ -102,6 +102,7 @@ __device__ __forceinline__ int swz(int r, int g) { return g ^ ((r >> 1) & 3); }
 // in order, belong to consecutive items.
 struct StreamParams {
   CUtensorMap tm_b, tm_c, tm_out;
+  CUtensorMap tm_u, tm_d, tm_z;  // the row tensors, [32 rows × 32 tokens] boxes in the tiles' swizzle
   ScanArgs a;
   int rtiles;   // row tiles per batch
   int sl;       // stages per tile (ceil(L / 32))
@@ -131,6 +132,8 @@ struct StreamSmem {
   uint64_t full[NB];  // the stage's B and C copies landed (bytes counted)
   uint64_t conv[NB];  // every warp converted its share of the stage's B and C
   uint64_t settled;   // every warp knows how far pass two must go
+  uint64_t rowbar[RB / 32][2];  // [warp][buffer]: the warp's row tiles of a stage landed (bytes counted)
+  int rissued[RB / 32];         // ring stages whose row tiles the warp has requested (the last + 1)
   int done[NB];       // warps that released the stage's B and C
   int n2;             // stages of the second pass (max over warps)
   int issued;         // B/C stages issued so far (the last one + 1)
@@ -194,30 +197,34 @@ __device__ __forceinline__ int stage_t0(const Ring& g, int k) { return g.tc0 + (
 // position of the segment's stage k in the CTA's ring (buffer k & 1, B/C slot k % NB)
 __device__ __forceinline__ int ring(const Ring& g, int k) { return g.kb + k; }
 
-// This warp's 32 rows of stage k's u, Δraw, z tiles into row buffer k % 2, one
-// cp.async group (four lanes per 64-byte row segment; rows past d_inner and tokens
-// past the sequence are zero-filled).
+// This warp's 32 rows of stage k's u, Δraw, z tiles into row buffer k % 2: three tensor
+// copies of [32 rows × 32 tokens] issued by lane 0, completion counted in bytes on the
+// warp's mbarrier of that buffer (rows past d_inner and tokens past the sequence are
+// zero-filled).  The boxes land in the tiles' 64-byte swizzle, the layout swz() reads.
 template <int RB, bool HAS_Z>
 __device__ __forceinline__ void rows_issue(StreamSmem<RB>& sm, const Ring& g, int k, int warp, int lane) {
-  const ScanArgs& a = g.p->a;
-  const int t0 = stage_t0(g, k);
-  const int gi = lane & 3;
-  const int t = t0 + gi * 8;
-  const bool t_ok = t < g.tc1;  // a granule is all in or all out (L % 8 == 0)
-  const __nv_bfloat16* srcs[3] = {static_cast<const __nv_bfloat16*>(a.u), static_cast<const __nv_bfloat16*>(a.delta),
-                                  static_cast<const __nv_bfloat16*>(a.z)};
+  if (lane != 0) return;
+  const StreamParams& p = *g.p;
+  const int rk = ring(g, k), buf = rk & 1;
+  const uint32_t bar = ac::smem_u32(&sm.rowbar[warp][buf]);
   constexpr int ntens = HAS_Z ? 3 : 2;
-#pragma unroll
-  for (int w = 0; w < ntens; ++w) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = 32 * warp + (lane >> 2) + 8 * i;  // row within the CTA
-      const int c = g.c0 + r;
-      const bool ok = t_ok && c < a.d_inner;
-      const __nv_bfloat16* src = srcs[w] + ((int64_t)g.b * a.d_inner + (ok ? c : 0)) * a.L + (ok ? t : 0);
-      cp_async16(sm.tile[ring(g, k) & 1][w] + r * kRowBytes + swz(r, gi) * 16, src, ok ? 16 : 0);
-    }
-  }
+  ac::mbar_arrive_expect_tx(bar, (uint32_t)(ntens * 32 * kRowBytes));
+  const int t0 = stage_t0(g, k), y = g.c0 + 32 * warp;
+  ac::tma_load_3d(ac::smem_u32(sm.tile[buf][0] + 32 * warp * kRowBytes), &p.tm_u, t0, y, g.b, bar);
+  ac::tma_load_3d(ac::smem_u32(sm.tile[buf][1] + 32 * warp * kRowBytes), &p.tm_d, t0, y, g.b, bar);
+  if (HAS_Z) ac::tma_load_3d(ac::smem_u32(sm.tile[buf][2] + 32 * warp * kRowBytes), &p.tm_z, t0, y, g.b, bar);
+  sm.rissued[warp] = rk + 1;
+}
+
+// Lane 0: wait until every row-tile copy this warp requested has landed (the ones a
+// second pass shorter than its speculation never consumed included).
+template <int RB>
+__device__ __forceinline__ bool rows_drain(StreamSmem<RB>& sm, int warp, unsigned long long deadline) {
+  bool ok = true;
+  const int n = sm.rissued[warp];
+  for (int j = n - 2 < 0 ? 0 : n - 2; j < n; ++j)
+    ok = ac::mbar_wait(ac::smem_u32(&sm.rowbar[warp][j & 1]), (uint32_t)(j >> 1) & 1u, deadline) && ok;
+  return ok;
 }
 
 // Issue the tensor copies of stage j's B and C (one thread).
@@ -272,7 +279,6 @@ __device__ __forceinline__ void stage_advance(StreamSmem<RB>& sm, const Ring& g,
   if (lane == 0) ac::bulk_wait_read0();  // the tensor store has read stage k's outputs out of the buffer
   __syncwarp();
   if (stage_has(k + 2, g.spec_rows, g.n1, n2)) rows_issue<RB, HAS_Z>(sm, g, k + 2, warp, lane);
-  cp_async_commit();  // one group per stage, empty or not, keeps the wait counts fixed
   const int s = ring(g, k) % NB;
   __syncwarp();
   if (lane == 0) {
@@ -406,8 +412,10 @@ __device__ __forceinline__ void consume(StreamSmem<RB>& sm, const Ring& g, const
     const int k = k0 + kk;
     const int s = ring(g, k) % NB;
     const uint32_t ph = (uint32_t)(ring(g, k) / NB) & 1u;
-    cp_async_wait<1>();  // this warp's rows of stage k (stage k + 1's may still be in flight)
-    __syncwarp();
+    // this warp's rows of stage k (stage k + 1's may still be in flight), then its B and C
+    if (!ac::mbar_wait(ac::smem_u32(&sm.rowbar[warp][ring(g, k) & 1]), (uint32_t)(ring(g, k) >> 1) & 1u,
+                       g.deadline))
+      err = 1;
     if (!ac::mbar_wait(ac::smem_u32(&sm.conv[s]), ph, g.deadline)) err = 1;
     const int ts = t_lo + kk * TS;
     const int buf = ring(g, k) & 1;
@@ -602,10 +610,8 @@ __device__ __forceinline__ void run_segment(StreamSmem<RB>& sm, const StreamPara
 
   // the first two stages of this warp's rows; the B/C ring filled; every warp converts
   // its share of the first kAhead stages
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 0; k < 2; ++k)
     if (k < g.spec_rows) rows_issue<RB, HAS_Z>(sm, g, k, warp, lane);
-    cp_async_commit();
-  }
   if (threadIdx.x == 0)
     for (int j = 0; j < NB && j < g.spec_bc; ++j) bc_issue<RB>(sm, g, j);
   for (int j = 0; j < kAhead && j < g.spec_bc; ++j) bc_convert<RB>(sm, g, j, warp, lane, err);
@@ -643,6 +649,11 @@ __global__ void __launch_bounds__(StreamCta<RB>::kThreads) __maxnreg__(StreamCta
       sm.done[s] = 0;
     }
     ac::mbar_init(ac::smem_u32(&sm.settled), NW);
+    for (int w = 0; w < NW; ++w) {
+      ac::mbar_init(ac::smem_u32(&sm.rowbar[w][0]), 1);  // the issuing lane's arrival + the copies' bytes
+      ac::mbar_init(ac::smem_u32(&sm.rowbar[w][1]), 1);
+      sm.rissued[w] = 0;
+    }
     ac::fence_mbar_init();
     sm.n2 = 0;
     sm.issued = 0;
@@ -672,6 +683,9 @@ __global__ void __launch_bounds__(StreamCta<RB>::kThreads) __maxnreg__(StreamCta
     }
     ac::prefetch_tensormap(&p.tm_b);
     ac::prefetch_tensormap(&p.tm_c);
+    ac::prefetch_tensormap(&p.tm_u);
+    ac::prefetch_tensormap(&p.tm_d);
+    if (HAS_Z) ac::prefetch_tensormap(&p.tm_z);
   }
   __syncthreads();
   const unsigned long long deadline = ac::globaltimer() + (unsigned long long)p.timeout_ns;
@@ -683,16 +697,20 @@ __global__ void __launch_bounds__(StreamCta<RB>::kThreads) __maxnreg__(StreamCta
     run_segment<RB, HAS_Z>(sm, p, sm.seg[sgi], kb, deadline, warp, lane, err);
     if (sgi + 1 < nseg) {
       kb = sm.seg[sgi].s1;  // every ring stage of a first segment was issued and consumed
-      cp_async_wait<0>();
-      if (lane == 0) ac::bulk_wait0();
+      if (lane == 0) {
+        if (!rows_drain(sm, warp, deadline + 1000000000ull)) err = 1;
+        ac::bulk_wait0();
+      }
       __syncthreads();  // the ring and the row buffers are free for the next segment
     }
   }
 
   // copies issued ahead of a pass two shorter than the ring, never consumed, must land,
   // and the tensor stores complete, before the CTA exits
-  cp_async_wait<0>();
-  if (lane == 0) ac::bulk_wait0();
+  if (lane == 0) {
+    if (!rows_drain(sm, warp, deadline + 1000000000ull)) err = 1;
+    ac::bulk_wait0();
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     const int issued = sm.issued;
@@ -778,10 +796,13 @@ cudaError_t scan_stream_launch(const ScanArgs& a, const ScanPlan& plan, cudaStre
   const uint64_t D = (uint64_t)a.d_inner;
   const uint64_t dims_row[3] = {L, D, Bt}, str_row[2] = {L * 2, L * D * 2};
   const uint32_t box_row[3] = {(uint32_t)TS, 32u, 1u};
+  const auto sw64 = CU_TENSOR_MAP_SWIZZLE_64B;
   if (!encode_tensor_map(&p.tm_b, bf, 3, a.B, dims_bc, str_bc, box_bc, none, promo) ||
       !encode_tensor_map(&p.tm_c, bf, 3, a.C, dims_bc, str_bc, box_bc, none, promo) ||
-      !encode_tensor_map(&p.tm_out, bf, 3, a.out, dims_row, str_row, box_row, CU_TENSOR_MAP_SWIZZLE_64B,
-                         CU_TENSOR_MAP_L2_PROMOTION_NONE))
+      !encode_tensor_map(&p.tm_out, bf, 3, a.out, dims_row, str_row, box_row, sw64, CU_TENSOR_MAP_L2_PROMOTION_NONE) ||
+      !encode_tensor_map(&p.tm_u, bf, 3, a.u, dims_row, str_row, box_row, sw64, promo) ||
+      !encode_tensor_map(&p.tm_d, bf, 3, a.delta, dims_row, str_row, box_row, sw64, promo) ||
+      (a.z && !encode_tensor_map(&p.tm_z, bf, 3, a.z, dims_row, str_row, box_row, sw64, promo)))
     return cudaErrorInvalidValue;
   if (p.multi) {
     const cudaError_t e = cudaMemsetAsync(a.ws, 0, p.ws.flags_bytes, stream);
