@@ -341,9 +341,9 @@ __device__ __forceinline__ float stage_tokens(const StreamSmem<RB>& sm, int s, c
       if (HAS_Z) {
         const unsigned zw = v ? wz.y : wz.x;
         const float2 zz = make_float2(bf_lo(zw), bf_hi(zw));
-        const float2 ez = __fmul2_rn(zz, make_float2(-kLog2e, -kLog2e));
-        const float2 dz = __fadd2_rn(make_float2(ex2_approx(ez.x), ex2_approx(ez.y)), make_float2(1.f, 1.f));
-        gz = __fmul2_rn(zz, make_float2(rcp_approx(dz.x), rcp_approx(dz.y)));
+        // silu(z) = z/2 + (z/2)·tanh(z/2): one MUFU operation per token
+        const float2 hz = __fmul2_rn(zz, make_float2(0.5f, 0.5f));
+        gz = __ffma2_rn(hz, make_float2(tanh_approx(hz.x), tanh_approx(hz.y)), hz);
       }
       const float xs[2] = {bf_lo(uw), bf_hi(uw)};
       const float ds[2] = {d0, d1};

@@ -34,6 +34,12 @@ __device__ __forceinline__ float rcp_approx(float x) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// hardware tanh (one MUFU operation; absolute error about 2^-11)
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // softplus(r) = log(1 + e^r).  Fast form, without branches:
 // ln2 · log2(1 + 2^{r log2 e}) for r ≤ 15 and r itself above (relative error < e^-15).
