@@ -587,13 +587,26 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_out_kernel(const SsdArg
 
 }  // namespace
 
+// The walking form (ssd_walk.cu) needs batch · heads CTAs to fill the GPU; below
+// that the chunk-parallel form runs.
+bool ssd_use_walk(int64_t batch, int64_t L, int64_t H) {
+  const int f = runtime_knobs().force_ssd;
+  if (f == 1) return true;
+  if (f == 2) return false;
+  (void)L;
+  return batch * H >= kSsdWalkMinPairs;
+}
+
 size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H) {
+  if (ssd_use_walk(batch, L, H)) return 256;  // the error words only
   const int64_t nch = (L + kQ - 1) / kQ;
   const WsSizes z = ws_sizes(batch, H, nch < 1 ? 1 : nch);
   return 256 + z.hc + z.ctot + z.hin;
 }
 
 cudaError_t ssd_launch(SsdArgs p, cudaStream_t stream) {
+  if (ssd_use_walk(p.batch, p.L, p.H))
+    return ssd_walk_launch(p, reinterpret_cast<unsigned*>(p.ws) + 1, stream);
   p.nchunks = (p.L + kQ - 1) / kQ;
   if (p.timeout_ns <= 0) p.timeout_ns = (long long)kDefaultTimeoutMs * 1000000ll;
   // heads per CTA: the largest divisor of the heads of a group up to kMaxHeadsPerCta

@@ -39,6 +39,8 @@ RuntimeKnobs* load_knobs() {
     if (std::strcmp(k, "rows") == 0) r->force_kind = kScanRows;
     if (std::strcmp(k, "stream") == 0) r->force_kind = kScanStream;
     if (std::strcmp(k, "tiny") == 0) r->force_kind = kScanTiny;
+    if (std::strcmp(k, "ssd_walk") == 0) r->force_ssd = 1;
+    if (std::strcmp(k, "ssd_chunks") == 0) r->force_ssd = 2;
   }
   if (const char* c = std::getenv("SSM_CTAS_PER_SM")) r->ctas_per_sm = std::atoi(c);
   if (const char* c = std::getenv("SSM_FORCE_TPR")) r->force_tpr = std::atoi(c);

@@ -78,6 +78,7 @@ struct RuntimeKnobs {
   bool fault_ssd;                 // test hook: the SSD output kernel's first wait never completes
   int stream_rows;                // >0: rows per CTA of the streamed row kernel (512, 256 or 128)
   int stream_ctas;                // >0: work items (CTAs) of the streamed row kernel
+  int force_ssd;                  // SSD form: 0 by shape, 1 one CTA per (batch, head), 2 chunk-parallel
 };
 RuntimeKnobs runtime_knobs();  // the test hooks as last loaded (first use, or ssm_test_hooks_reload)
 void reload_knobs();
@@ -202,8 +203,13 @@ struct SsdArgs {
 constexpr int kSsdChunk = 128;    // tokens per chunk
 constexpr int kSsdHeadDim = 64;   // supported headdim
 constexpr int kSsdState = 128;    // supported d_state
+constexpr int kSsdWalkMinPairs = 64;  // batch · heads from which one CTA walks each (batch, head)
 size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H);
 cudaError_t ssd_launch(SsdArgs p, cudaStream_t stream);
+// the sequence-walking form (ssd_walk.cu): one CTA per (batch, head), no workspace
+// beyond the error word
+bool ssd_use_walk(int64_t batch, int64_t L, int64_t H);
+cudaError_t ssd_walk_launch(SsdArgs p, unsigned* err, cudaStream_t stream);
 
 // One decode token of the Mamba-2 layer (ssd.cu): state [batch][H][P][N] fp32 in place;
 // x, z, out [batch][H][P], dt [batch][H], B, C [batch][G][N] (bf16); A, D, dt_bias [H].

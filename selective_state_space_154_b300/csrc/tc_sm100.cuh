@@ -43,6 +43,37 @@ __device__ __forceinline__ uint64_t kslice_desc(uint32_t base, int R, int kk) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// The same with either operand MN-major (bit 15: A, bit 16: B).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_major(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_bf16_f32(M, N) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
+}
+
+// 128-byte swizzle (layout type 2 in bits 61-63): rows of 128 bytes, the 16-byte
+// chunk j of row r stored at chunk j ^ (r % 8), 8-row groups of 1024 bytes — the
+// layout a tensor copy with CU_TENSOR_MAP_SWIZZLE_128B writes.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(addr, lbo, sbo) | (2ull << 61);
+}
+// K-major, 128-byte swizzle: R rows × 128 K stored as two column blocks (K 0..63,
+// 64..127) of R × 128 bytes; the K = 16 slice kk starts 32 bytes into its block's rows.
+__device__ __forceinline__ uint64_t sw128_kslice_desc(uint32_t base, int R, int kk) {
+  return sw128_desc(base + (uint32_t)((kk >> 2) * R * 128 + (kk & 3) * 32), 16u, 1024u);
+}
+// MN-major, 128-byte swizzle: K rows of 128 bytes (64 elements of M or N) per atom
+// column, atom columns `atom_stride` bytes apart; the K = 16 slice kk is 16 rows in.
+__device__ __forceinline__ uint64_t sw128_mn_kslice_desc(uint32_t base, uint32_t atom_stride, int kk) {
+  return sw128_desc(base + (uint32_t)(kk * 2048), atom_stride, 1024u);
+}
+
+// MN-major operands (no swizzle): the core matrix is 8 rows along K, each 16
+// bytes (8 elements) along M or N.  A tile with 16 groups of 8 along K, stored
+// with core matrix (mn group i, k group j) at byte (i · 16 + j) · 128 — the same
+// bytes as kmajor_offset(128, k, mn) — has K-direction neighbours 128 bytes apart
+// (leading byte offset) and M/N-direction neighbours 2048 bytes apart (stride
+// byte offset); its K = 16 slice kk starts at byte 256 · kk.
+__device__ __forceinline__ uint64_t mn_kslice_desc(uint32_t base, int kk) {
+  return smem_desc(base + (uint32_t)(kk * 256), 128u, 2048u);
+}
 
 // D[tmem] (+)= A · Bᵀ for one K = 16 slice; issued by a single thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -92,6 +123,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+// 16 consecutive fp32 columns of this thread's lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
 __device__ __forceinline__ uint32_t tmem_lane_addr(uint32_t base, int lane0, int col) {
   return base + ((uint32_t)lane0 << 16) + (uint32_t)col;

@@ -15,6 +15,14 @@ DEV = "cuda"
 BF16 = TOL[torch.bfloat16]
 
 
+@pytest.fixture(params=["ssd_walk", "ssd_chunks"], ids=["walk", "chunks"])
+def form(request, hooks):
+    """Both forms of the layer scan: one CTA walking the sequence of each (batch, head),
+    and the chunk-parallel launches."""
+    hooks.set("SSM_FORCE_KERNEL", request.param)
+    return hooks
+
+
 def _oracle(inp, h0=None):
     return oracle.ssd_scan(*(to_np(inp[k]) for k in ("x", "dt", "A", "B", "C")), D=to_np(inp["D"]),
                            z=to_np(inp["z"]), dt_bias=to_np(inp["dt_bias"]), h0=to_np(h0))
@@ -38,18 +46,18 @@ def _compare(inp, h0=None):
                                    (1, 129, 3, 64, 3, 128), (2, 700, 2, 64, 1, 128), (1, 2048, 4, 64, 2, 128)],
                          ids=["one_chunk", "ragged_groups", "one_token", "chunk_plus_one", "six_chunks",
                               "sixteen_chunks"])
-def test_ssd_matches_oracle(shape):
+def test_ssd_matches_oracle(shape, form):
     _compare(W.random_ssd_inputs(*shape, device=DEV, seed=sum(shape)))
 
 
 @pytest.mark.parametrize("opts", [dict(gate=False), dict(skip=False), dict(with_bias=False),
                                   dict(gate=False, skip=False, with_bias=False)],
                          ids=["no_z", "no_D", "no_bias", "all_off"])
-def test_ssd_optional_inputs(opts):
+def test_ssd_optional_inputs(opts, form):
     _compare(W.random_ssd_inputs(1, 260, 2, 64, 1, 128, device=DEV, seed=5, **opts))
 
 
-def test_ssd_initial_state_continues_a_split_sequence():
+def test_ssd_initial_state_continues_a_split_sequence(form):
     inp = W.random_ssd_inputs(2, 400, 2, 64, 1, 128, device=DEV, seed=8)
     g = torch.Generator(device=DEV).manual_seed(3)
     h0 = torch.randn((2, 2, 64, 128), generator=g, device=DEV)
@@ -64,13 +72,13 @@ def test_ssd_initial_state_continues_a_split_sequence():
     assert rel_err(to_np(f2), href) <= BF16
 
 
-def test_ssd_zero_A_is_linear_attention():
+def test_ssd_zero_A_is_linear_attention(form):
     inp = W.random_ssd_inputs(1, 300, 2, 64, 1, 128, device=DEV, seed=12)
     inp["A"].zero_()
     _compare(inp)
 
 
-def test_ssd_empty_sequence_passes_the_state_through():
+def test_ssd_empty_sequence_passes_the_state_through(form):
     inp = W.random_ssd_inputs(1, 0, 2, 64, 1, 128, device=DEV, seed=2)
     h0 = torch.randn((1, 2, 64, 128), device=DEV)
     out, fs = _gpu(inp, h0)
@@ -102,27 +110,37 @@ def test_ssd_mamba2_2p7b_layer_sampled_heads():
 @pytest.mark.parametrize("shape", [(1, 300, 5, 64, 1, 128), (1, 260, 12, 64, 2, 128), (2, 150, 14, 64, 2, 128),
                                    (1, 400, 16, 64, 1, 128)],
                          ids=["5_heads_per_cta", "6_heads_per_cta", "7_heads_per_cta", "8_heads_per_cta_x2"])
-def test_ssd_heads_per_cta(shape):
-    """A CTA takes up to 8 heads of one group (the largest divisor of heads per group):
-    odd and even counts, several head blocks per group."""
+def test_ssd_heads_per_cta(shape, hooks):
+    """Chunk-parallel form: a CTA takes up to 8 heads of one group (the largest divisor
+    of heads per group): odd and even counts, several head blocks per group."""
+    hooks.set("SSM_FORCE_KERNEL", "ssd_chunks")
     _compare(W.random_ssd_inputs(*shape, device=DEV, seed=shape[2]))
 
 
-def test_ssd_wait_timeout_is_reported_and_the_context_recovers(hooks):
-    """Test hook: the output kernel's first tensor-core wait is on an mbarrier that nothing
-    arrives on.  The wait gives up after 200 ms, lets its issued products finish, frees its
+def test_ssd_walk_is_chosen_for_many_heads_and_matches():
+    """2 × 40 heads reach the planner's threshold for the walking form (its workspace is
+    the error words alone); four groups, a ragged last chunk, an initial state."""
+    assert ssm.ssd_scan_workspace_bytes(2, 333, 40, 64, 4, 128) == 256
+    inp = W.random_ssd_inputs(2, 333, 40, 64, 4, 128, device=DEV, seed=77)
+    h0 = torch.randn((2, 40, 64, 128), generator=torch.Generator(device=DEV).manual_seed(78), device=DEV)
+    _compare(inp, h0)
+
+
+def test_ssd_wait_timeout_is_reported_and_the_context_recovers(form):
+    """Test hook: the first tensor-core wait (of the output kernel, or of the walking
+    kernel) is on an mbarrier that nothing arrives on.  The wait gives up after 200 ms, lets its issued products finish, frees its
     tensor memory and sets the workspace's error word; the next clean call is correct."""
     inp = W.random_ssd_inputs(1, 300, 2, 64, 1, 128, device=DEV, seed=4)
     ws = torch.empty(ssm.ssd_scan_workspace_bytes(1, 300, 2, 64, 1, 128), dtype=torch.uint8, device=DEV)
     args = (inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"])
     kw = dict(D=inp["D"], z=inp["z"], dt_bias=inp["dt_bias"], return_final_state=True, workspace=ws)
-    hooks.set("SSM_FAULT", "ssd")
-    hooks.set("SSM_LOOKBACK_TIMEOUT_MS", "200")
+    form.set("SSM_FAULT", "ssd")
+    form.set("SSM_LOOKBACK_TIMEOUT_MS", "200")
     ssm.ssd_scan(*args, **kw)
     torch.cuda.synchronize()
     assert ssm.ssm_scan_check(ws) == ssm.SSM_ERR_TIMEOUT
-    hooks.unset("SSM_FAULT")
-    hooks.unset("SSM_LOOKBACK_TIMEOUT_MS")
+    form.unset("SSM_FAULT")
+    form.unset("SSM_LOOKBACK_TIMEOUT_MS")
     out, fs = ssm.ssd_scan(*args, **kw)
     torch.cuda.synchronize()
     assert ssm.ssm_scan_check(ws) == ssm.SSM_OK
