@@ -11,9 +11,10 @@
 // launch.  The chunk-parallel form of ssd.cu is kept for problems with too few
 // (batch, head) pairs to fill the GPU this way.
 //
-// Warp roles (17 warps):
-//  * the control warp (one lane) issues the tensor copies of each chunk's C, B and
-//    X tiles and the tensor-core products, and waits on mbarriers only;
+// Warp roles (18 warps):
+//  * the MMA warp (one lane) issues the tensor-core products, and the load warp (one
+//    lane) the tensor copies of each chunk's C, B and X tiles, each as soon as the
+//    previous chunk's last reader of the tile is done; both wait on mbarriers only;
 //  * 16 compute warps (tensor-memory lane quarter = warp % 4, column quarter =
 //    warp / 4) build the operands the kernel computes, read the accumulators and
 //    write the outputs.  Per chunk c, in order: diag(w) X (the warps with no block
@@ -59,8 +60,9 @@ constexpr int kQ = kSsdChunk;
 constexpr int kP = kSsdHeadDim;
 constexpr int kN = kSsdState;
 constexpr int kComputeWarps = 16;
-constexpr int kCtrlWarp = kComputeWarps;
-constexpr int kThreads = (kComputeWarps + 1) * 32;
+constexpr int kCtrlWarp = kComputeWarps;      // issues the tensor-core products
+constexpr int kLoadWarp = kComputeWarps + 1;  // issues the tensor copies
+constexpr int kThreads = (kComputeWarps + 2) * 32;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kDefaultTimeoutMs = 2000;
 constexpr uint32_t kBoxBytes = kQ * 128;                  // one [128 tokens × 64 elements] copy
@@ -131,16 +133,16 @@ __device__ __forceinline__ bool aborted(const WalkSmem& sm) {
 }
 // Bounded wait for the phase of `parity`; gives up at once if another thread has
 // given up (abort flag), or sets the error word and the flag after `timeout_ns`.
+// Waiting threads sleep in the barrier (up to kSleepNs per try) rather than spin.
+constexpr uint32_t kSleepNs = 20000;
 __device__ __forceinline__ bool wait_bar(WalkSmem& sm, uint32_t bar, uint32_t parity, long long timeout_ns,
                                          unsigned* err) {
   if (tc::mbar_test(bar, parity)) return true;
   const unsigned long long start = globaltimer_ns();
   for (int it = 0; it < (1 << 28); ++it) {
-    if (tc::mbar_test(bar, parity)) return true;
-    if ((it & 15) == 15) {
-      if (aborted(sm)) return false;
-      if ((long long)(globaltimer_ns() - start) > timeout_ns) break;
-    }
+    if (tc::mbar_test_sleep(bar, parity, kSleepNs)) return true;
+    if (aborted(sm)) return false;
+    if ((long long)(globaltimer_ns() - start) > timeout_ns) break;
   }
   atomicOr(err, kErrTimeout);
   *reinterpret_cast<volatile int*>(&sm.abort) = 1;
@@ -232,6 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
     }
   };
   const float a = p.A[h];
+  const float inv_a = a != 0.f ? 1.f / a : 0.f;
   const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
   const float Dh = p.D ? p.D[h] : 0.f;
   auto chunk_len = [&](int64_t c) { return (int)(p.L - c * kQ < kQ ? p.L - c * kQ : kQ); };
@@ -244,9 +247,18 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
     const int i = threadIdx.x, par = (int)(c & 1);
     float la = 0.f, ph = 0.f;
     if (c < nch && i < chunk_len(c)) {
-      const float d = softplus_precise(dtv + bias);
+      // Δ = softplus(Δraw + bias) and φ = (e^{Δa} − 1)/a with the MUFU ex2 / lg2: e^x − 1
+      // as 2^{x log2 e} − 1 for |x| ≥ 1/16 (relative error below 2^-18), by its series
+      // to x^6 below (truncation below 2^-36)
+      const float r = dtv + bias;
+      const float d = r > 15.f ? r : kLn2 * lg2_approx(1.f + ex2_approx(r * kLog2e));
       la = d * a;
-      ph = a != 0.f ? expm1f(la) / a : d;
+      if (fabsf(la) < 0.0625f) {
+        const float ser = 1.f + la * (0.5f + la * (1.f / 6 + la * (1.f / 24 + la * (1.f / 120 + la * (1.f / 720)))));
+        ph = d * ser;
+      } else {
+        ph = (ex2_approx(la * kLog2e) - 1.f) * inv_a;
+      }
     }
     float v = la;
 #pragma unroll
@@ -286,14 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
   tc::fence_after_sync();
   const uint32_t tmem = sm.tslot;
 
-  if (!compute) {
-    // ------------------------------------------------------------ control warp, one lane
+  if (warp == kCtrlWarp) {
+    // ------------------------------------------------------------ MMA warp, one lane
     if (lane == 0) {
-      if (nch > 0) {
-        ac::prefetch_tensormap(&w.tm_c);
-        ac::prefetch_tensormap(&w.tm_b);
-        ac::prefetch_tensormap(&w.tm_x);
-      }
       const uint32_t a_c = tc::smem_addr(sm.c), a_b = tc::smem_addr(sm.b), a_x = tc::smem_addr(sm.x);
       const uint32_t a_g0 = tc::smem_addr(sm.g[0]), a_g1 = tc::smem_addr(sm.g[1]);
       const uint32_t a_w0 = tc::smem_addr(sm.wx[0]);  // hi, then lo: one N = 128 operand
@@ -302,20 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
       const uint32_t id_yin = tc::idesc_bf16_f32_major(kQ, kP, false, true);  // C · h_inᵀ
       const uint32_t id_hc = tc::idesc_bf16_f32_major(kN, 2 * kP, true, true);  // Bᵀ · (diag(w) X), hi | lo
       const uint32_t id_y = tc::idesc_bf16_f32_major(kQ, kP, false, true);    // G · X
-      // copies issued and awaited: C and B on bar_ldcb, X on bar_ldx (a copy issued but
-      // never awaited, after a timeout, lands before the CTA leaves)
-      int64_t cb_issued = 0, cb_seen = 0, x_issued = 0;
-      if (nch > 0) {
-        issue_cb(sm, w, 0, (int)b, (int)g);
-        issue_x(sm, w, 0, (int)b, (int)h);
-        cb_issued = x_issued = 1;
-      }
       for (int64_t c = 0; c < nch; ++c) {
         const uint32_t par = (uint32_t)(c & 1), prev = (uint32_t)((c - 1) & 1);
         const int k = (int)(c & 1);
         // S: C and B of chunk c landed (chunk c − 1's G has read S: bar_g awaited before its Y)
         if (!wait_bar(sm, p.fault && c == 0 ? bar_never : bar_ldcb, par, tmo, w.err)) break;
-        cb_seen = c + 1;
         tc::fence_after_sync();
 #pragma unroll 1
         for (int kk = 0; kk < kN / 16; ++kk)
@@ -323,10 +321,6 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
                        kk > 0);
         tc::mma_commit(bar_a);
         if (c > 0) {
-          // chunk c − 1's G X done: X takes chunk c
-          if (!wait_bar(sm, bar_c, prev, tmo, w.err)) break;
-          issue_x(sm, w, c, (int)b, (int)h);
-          x_issued = c + 1;
           // h_in of chunk c written (and chunk c − 2's outputs have read Y[k], Y_in[k])
           if (!wait_bar(sm, bar_h, prev, tmo, w.err)) break;
           tc::fence_after_sync();
@@ -358,15 +352,32 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
           tc::mma_bf16(tmem + col_y(k), tc::kslice_desc(a_g1, kQ, kk), tc::sw128_mn_kslice_desc(a_x, kBoxBytes, kk), id_y,
                        true);
         tc::mma_commit(bar_c);  // covers Y_in, the chunk state and Y
-        if (c + 1 < nch) {  // the next chunk's C and B land while G X runs
-          if (!wait_bar(sm, bar_cb, par, tmo, w.err)) break;
-          issue_cb(sm, w, c + 1, (int)b, (int)g);
-          cb_issued = c + 2;
-        }
       }
-      if (cb_issued > cb_seen) wait_bar_drain(bar_ldcb, (uint32_t)((cb_issued - 1) & 1), tmo);
-      // every X copy is awaited by the compute warps, or by this drain
-      if (x_issued > 0) wait_bar_drain(bar_ldx, (uint32_t)((x_issued - 1) & 1), tmo);
+    }
+    __syncwarp();
+  } else if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ load warp, one lane
+    if (lane == 0 && nch > 0) {
+      ac::prefetch_tensormap(&w.tm_c);
+      ac::prefetch_tensormap(&w.tm_b);
+      ac::prefetch_tensormap(&w.tm_x);
+      issue_cb(sm, w, 0, (int)b, (int)g);
+      issue_x(sm, w, 0, (int)b, (int)h);
+      int64_t cb_issued = 1, x_issued = 1;
+      for (int64_t c = 1; c < nch; ++c) {
+        const uint32_t prev = (uint32_t)((c - 1) & 1);
+        // C and B take chunk c once chunk c − 1's S, C h_inᵀ and chunk state are done
+        if (!wait_bar(sm, bar_cb, prev, tmo, w.err)) break;
+        issue_cb(sm, w, c, (int)b, (int)g);
+        cb_issued = c + 1;
+        // X takes chunk c once chunk c − 1's G X (and diag(w) X, before it) are done
+        if (!wait_bar(sm, bar_c, prev, tmo, w.err)) break;
+        issue_x(sm, w, c, (int)b, (int)h);
+        x_issued = c + 1;
+      }
+      // the last copies have landed before the CTA leaves (at once unless a wait timed out)
+      wait_bar_drain(bar_ldcb, (uint32_t)((cb_issued - 1) & 1), tmo);
+      wait_bar_drain(bar_ldx, (uint32_t)((x_issued - 1) & 1), tmo);
     }
     __syncwarp();
   } else {
@@ -375,11 +386,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
     unsigned char* stage = sm.stage[warp];
     // Outputs of chunk oc: token rows 32·wq .., p = 16·cq .. 16·cq + 15 of this warp,
     // through its staging tile and one tensor store (rows past L are clipped).
-    auto outputs = [&](int64_t oc, bool ok) {
-      const int ok_k = (int)(oc & 1), t0 = (int)(oc * kQ), q = chunk_len(oc);
-      const int64_t off = ((b * p.L + t0 + row) * p.H + h) * kP + 16 * cq;
-      const bool in = row < q;
-      uint4 xv[2], zv[2];
+    // x and z of this thread's outputs of chunk oc (token row, p = 16·cq ..), zero past the end
+    auto load_xz = [&](int64_t oc, uint4 (&xv)[2], uint4 (&zv)[2]) {
+      const int64_t off = ((b * p.L + oc * kQ + row) * p.H + h) * kP + 16 * cq;
+      const bool in = oc >= 0 && row < chunk_len(oc);
       const uint4* xr = reinterpret_cast<const uint4*>(bf(p.x) + off);
       const uint4* zr = p.z ? reinterpret_cast<const uint4*>(bf(p.z) + off) : nullptr;
 #pragma unroll
@@ -387,6 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         xv[m] = in ? xr[m] : make_uint4(0, 0, 0, 0);
         zv[m] = (in && zr) ? zr[m] : make_uint4(0, 0, 0, 0);
       }
+    };
+    auto outputs = [&](int64_t oc, bool ok, const uint4 (&xv)[2], const uint4 (&zv)[2]) {
+      const int ok_k = (int)(oc & 1), t0 = (int)(oc * kQ);
       float y[16], yi[16];
       tc::tmem_ld16(tc::tmem_lane_addr(tmem + col_y(ok_k), wq * 32, cq * 16), y);
       tc::tmem_ld16(tc::tmem_lane_addr(tmem + col_yin(ok_k), wq * 32, cq * 16), yi);
@@ -427,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
       const float* cs2 = sm.cs2[c % 3];
       const float* phi = sm.phi[c & 1];
       const float cs_end = cs2[kQ - 1];
+      uint4 xv[2], zv[2];
       if (widx >= 0) {
         // diag(w) X as hi and lo terms, w_s = 2^(cs2_end − cs2_s) φ_s; 16-byte granules
         // (8 p of token s), consecutive threads on consecutive tokens
@@ -452,8 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         }
         warp_arrive(bar_wx);
         warp_arrive_plain(bar_g);
+        load_xz(c - 1, xv, zv);
       } else {
         warp_arrive_plain(bar_wx);
+        load_xz(c - 1, xv, zv);  // read ahead of the wait for S
         // G_ts for this thread's token row t and tokens s = 32·cq .. 32·cq + 31 (s ≤ t)
         const bool ok = __all_sync(0xffffffffu, wait_bar(sm, bar_a, par, tmo, w.err));
         tc::fence_after_sync();
@@ -488,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         warp_arrive(bar_g);
       }
       // while G X runs: the previous chunk's outputs, the next chunk's token scalars
-      if (c > 0) outputs(c - 1, true);
+      if (c > 0) outputs(c - 1, true, xv, zv);
       if (warp < 4) {
         token_scalars(c + 1, dt_next);
         dt_next = load_dt(c + 2);
@@ -506,7 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         put_state();
       }
       warp_arrive(bar_h);  // h_in of chunk c + 1 written; chunk c − 1's outputs read Y, Y_in
-      if (c + 1 == nch) outputs(c, okc);
+      if (c + 1 == nch) {
+        load_xz(c, xv, zv);
+        outputs(c, okc, xv, zv);
+      }
     }
     // every tensor store of this warp has completed before the CTA leaves
     if (lane == 0) ac::bulk_wait0();
