@@ -92,9 +92,11 @@ struct WalkSmem {
   unsigned char g[2][kQ * kQ * 2];   // hi, lo
   unsigned char wx[2][kQ * kP * 2];  // hi, lo
   unsigned char h[2][kN * kP * 2];   // hi, lo
-  unsigned char stage[kComputeWarps][32 * 32];  // each warp's outputs: 32 tokens × 16 p (bf16)
+  unsigned char stage[kComputeWarps][16 * 32];  // each warp's outputs: 16 tokens × 16 p (bf16)
   float cs2[3][kQ];                  // by chunk mod 3: inclusive prefix sums of Δa, log2 units
   float phi[2][kQ];                  // by chunk parity: φ of the token (0 past the sequence's end)
+  float ep[2][kQ];                   // by chunk parity: 2^(cs2 at the end of the token's 32-block − cs2) φ
+  float wgt[2][kQ];                  // by chunk parity: w = 2^(cs2 at the chunk's end − cs2) φ
   float wsum[2][4];
   uint64_t bar_ldcb, bar_ldx, bar_a, bar_cb, bar_c, bar_wx, bar_g, bar_h, bar_drain, bar_never;
   uint32_t tslot;
@@ -268,9 +270,19 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
     }
     if (lane == 31) sm.wsum[par][warp] = v;
     named_sync(kBarTokens, 128);
-    for (int k = 0; k < warp; ++k) v += sm.wsum[par][k];
-    sm.cs2[c % 3][i] = v * kLog2e;
+    float before = 0.f, total = 0.f;
+    for (int k = 0; k < 4; ++k) {
+      before += k < warp ? sm.wsum[par][k] : 0.f;
+      total += sm.wsum[par][k];
+    }
+    v += before;
+    const float c2 = v * kLog2e;
+    // the token's 32-block is this warp's: its last prefix sum is lane 31's
+    const float block_end = __shfl_sync(0xffffffffu, c2, 31);
+    sm.cs2[c % 3][i] = c2;
     sm.phi[par][i] = ph;
+    sm.ep[par][i] = ex2_approx(block_end - c2) * ph;
+    sm.wgt[par][i] = ex2_approx(total * kLog2e - c2) * ph;
   };
 
   float dt_next = 0.f;
@@ -309,48 +321,53 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
       const uint32_t id_yin = tc::idesc_bf16_f32_major(kQ, kP, false, true);  // C · h_inᵀ
       const uint32_t id_hc = tc::idesc_bf16_f32_major(kN, 2 * kP, true, true);  // Bᵀ · (diag(w) X), hi | lo
       const uint32_t id_y = tc::idesc_bf16_f32_major(kQ, kP, false, true);    // G · X
+      // The tiles never move, so every descriptor is its tile's K-slice-0 descriptor
+      // plus a constant byte offset (the start address is the descriptor's low field).
+      const uint64_t dc = tc::sw128_kslice_desc(a_c, kQ, 0), db = tc::sw128_kslice_desc(a_b, kQ, 0);
+      const uint64_t dbt = tc::sw128_mn_kslice_desc(a_b, kBoxBytes, 0), dx = tc::sw128_mn_kslice_desc(a_x, kBoxBytes, 0);
+      const uint64_t dh0 = tc::mn_kslice_desc(a_h0, 0), dh1 = tc::mn_kslice_desc(a_h1, 0);
+      const uint64_t dw = tc::mn_kslice_desc(a_w0, 0);
+      const uint64_t dg0 = tc::kslice_desc(a_g0, kQ, 0), dg1 = tc::kslice_desc(a_g1, kQ, 0);
+      auto at = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
+      constexpr uint32_t kSw = (uint32_t)kQ * 128;  // 128-byte swizzle: K 64..127 column block
       for (int64_t c = 0; c < nch; ++c) {
         const uint32_t par = (uint32_t)(c & 1), prev = (uint32_t)((c - 1) & 1);
         const int k = (int)(c & 1);
         // S: C and B of chunk c landed (chunk c − 1's G has read S: bar_g awaited before its Y)
         if (!wait_bar(sm, p.fault && c == 0 ? bar_never : bar_ldcb, par, tmo, w.err)) break;
         tc::fence_after_sync();
-#pragma unroll 1
-        for (int kk = 0; kk < kN / 16; ++kk)
-          tc::mma_bf16(tmem + kColS, tc::sw128_kslice_desc(a_c, kQ, kk), tc::sw128_kslice_desc(a_b, kQ, kk), id_s,
-                       kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < kN / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * kSw + (kk & 3) * 32;
+          tc::mma_bf16(tmem + kColS, at(dc, o), at(db, o), id_s, kk > 0);
+        }
         tc::mma_commit(bar_a);
         if (c > 0) {
           // h_in of chunk c written (and chunk c − 2's outputs have read Y[k], Y_in[k])
           if (!wait_bar(sm, bar_h, prev, tmo, w.err)) break;
           tc::fence_after_sync();
         }
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < kN / 16; ++kk)
-          tc::mma_bf16(tmem + col_yin(k), tc::sw128_kslice_desc(a_c, kQ, kk), tc::mn_kslice_desc(a_h0, kk), id_yin,
-                       kk > 0);
-#pragma unroll 1
+          tc::mma_bf16(tmem + col_yin(k), at(dc, (kk >> 2) * kSw + (kk & 3) * 32), at(dh0, kk * 256), id_yin, kk > 0);
+#pragma unroll
         for (int kk = 0; kk < kN / 16; ++kk)
-          tc::mma_bf16(tmem + col_yin(k), tc::sw128_kslice_desc(a_c, kQ, kk), tc::mn_kslice_desc(a_h1, kk), id_yin,
-                       true);
+          tc::mma_bf16(tmem + col_yin(k), at(dc, (kk >> 2) * kSw + (kk & 3) * 32), at(dh1, kk * 256), id_yin, true);
         // the chunk state, hi and lo terms of diag(w) X side by side (N = 128)
         if (!wait_bar(sm, bar_wx, par, tmo, w.err)) break;
         tc::fence_after_sync();
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < kQ / 16; ++kk)
-          tc::mma_bf16(tmem + kColHc, tc::sw128_mn_kslice_desc(a_b, kBoxBytes, kk), tc::mn_kslice_desc(a_w0, kk), id_hc,
-                       kk > 0);
+          tc::mma_bf16(tmem + kColHc, at(dbt, kk * 2048), at(dw, kk * 256), id_hc, kk > 0);
         tc::mma_commit(bar_cb);  // C and B are free once S, Y_in and the chunk state are done
         if (!wait_bar(sm, bar_g, par, tmo, w.err)) break;
         tc::fence_after_sync();
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < kQ / 16; ++kk)
-          tc::mma_bf16(tmem + col_y(k), tc::kslice_desc(a_g0, kQ, kk), tc::sw128_mn_kslice_desc(a_x, kBoxBytes, kk), id_y,
-                       kk > 0);
-#pragma unroll 1
+          tc::mma_bf16(tmem + col_y(k), at(dg0, kk * 4096), at(dx, kk * 2048), id_y, kk > 0);
+#pragma unroll
         for (int kk = 0; kk < kQ / 16; ++kk)
-          tc::mma_bf16(tmem + col_y(k), tc::kslice_desc(a_g1, kQ, kk), tc::sw128_mn_kslice_desc(a_x, kBoxBytes, kk), id_y,
-                       true);
+          tc::mma_bf16(tmem + col_y(k), at(dg1, kk * 4096), at(dx, kk * 2048), id_y, true);
         tc::mma_commit(bar_c);  // covers Y_in, the chunk state and Y
       }
     }
@@ -422,16 +439,23 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         }
         ow[m] = pack2(r2[0], r2[1]);
       }
-      // the staging tile is free once this warp's previous store has read it
-      if (lane == 0) ac::bulk_wait_read0();
-      __syncwarp();
-      *reinterpret_cast<uint4*>(stage + lane * 32) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-      *reinterpret_cast<uint4*>(stage + lane * 32 + 16) = make_uint4(ow[4], ow[5], ow[6], ow[7]);
-      ac::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0 && ok && t0 + 32 * wq < p.L && !aborted(sm)) {
-        ac::tma_store_4d(&w.tm_out, ac::smem_u32(stage), 16 * cq, (int)h, t0 + 32 * wq, (int)b);
-        ac::bulk_commit();
+      // two stores of 16 token rows each through the warp's staging tile, which is free
+      // once the previous store has read it
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        if (lane == 0) ac::bulk_wait_read0();
+        __syncwarp();
+        if ((lane >> 4) == half) {
+          *reinterpret_cast<uint4*>(stage + (lane & 15) * 32) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+          *reinterpret_cast<uint4*>(stage + (lane & 15) * 32 + 16) = make_uint4(ow[4], ow[5], ow[6], ow[7]);
+        }
+        ac::fence_proxy_async_smem();
+        __syncwarp();
+        const int r0 = t0 + 32 * wq + 16 * half;
+        if (lane == 0 && ok && r0 < p.L && !aborted(sm)) {
+          ac::tma_store_4d(&w.tm_out, ac::smem_u32(stage), 16 * cq, (int)h, r0, (int)b);
+          ac::bulk_commit();
+        }
       }
     };
     for (int64_t c = 0; c < nch; ++c) {
@@ -451,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
             const uint32_t off = tc::kmajor_offset(kQ, s, pg * 8);
             // X granule pg of token s in the 128-byte swizzle of its tensor copy
             const uint4 xw = *reinterpret_cast<const uint4*>(sm.x + s * 128 + ((pg ^ (s & 7)) << 4));
-            const float wgt = ex2_approx(cs_end - cs2[s]) * phi[s];
+            const float wgt = sm.wgt[c & 1][s];
             float f[8];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -479,20 +503,29 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
           const int t = row;
           const float cst = cs2[t];
           const bool diag = cq == wq;
+          // below the diagonal every s of the block is before t:
+          // 2^(cs2_t − cs2_s) φ_s = 2^(cs2_t − cs2_end(block)) · ep_s, both factors ≤ 1
+          const float ft = ex2_approx(cst - cs2[cq * 32 + 31]);
+          const float* ep = sm.ep[c & 1];
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             const int s0 = cq * 32 + m * 8;
-            const float4 ca = *reinterpret_cast<const float4*>(cs2 + s0);
-            const float4 cb = *reinterpret_cast<const float4*>(cs2 + s0 + 4);
-            const float4 pa = *reinterpret_cast<const float4*>(phi + s0);
-            const float4 pb = *reinterpret_cast<const float4*>(phi + s0 + 4);
-            const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
-            const float pv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
             float f[8];
+            if (diag) {
+              const float4 ca = *reinterpret_cast<const float4*>(cs2 + s0);
+              const float4 cb = *reinterpret_cast<const float4*>(cs2 + s0 + 4);
+              const float4 pa = *reinterpret_cast<const float4*>(phi + s0);
+              const float4 pb = *reinterpret_cast<const float4*>(phi + s0 + 4);
+              const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+              const float pv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float gv = sv[m * 8 + e] * ex2_approx(cst - cv[e]) * pv[e];
-              f[e] = (!diag || s0 + e <= t) ? gv : 0.f;
+              for (int e = 0; e < 8; ++e) f[e] = s0 + e <= t ? sv[m * 8 + e] * ex2_approx(cst - cv[e]) * pv[e] : 0.f;
+            } else {
+              const float4 ea = *reinterpret_cast<const float4*>(ep + s0);
+              const float4 eb = *reinterpret_cast<const float4*>(ep + s0 + 4);
+              const float ev[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = sv[m * 8 + e] * ft * ev[e];
             }
             uint4 hi, lo;
             split8(f, hi, lo);
@@ -568,7 +601,7 @@ cudaError_t ssd_walk_launch(SsdArgs p, unsigned* err, cudaStream_t stream) {
     const uint64_t dims_x[4] = {(uint64_t)kP, (uint64_t)p.H, (uint64_t)p.L, (uint64_t)p.batch};
     const uint64_t str_x[3] = {(uint64_t)kP * 2, (uint64_t)(p.H * kP * 2), (uint64_t)(p.L * p.H * kP * 2)};
     const uint32_t box[4] = {64, 1, (uint32_t)kQ, 1};
-    const uint32_t box_out[4] = {16, 1, 32, 1};  // a compute warp's 32 tokens × 16 p
+    const uint32_t box_out[4] = {16, 1, 16, 1};  // 16 tokens × 16 p of a compute warp
     if (!encode_tensor_map(&w.tm_c, bf16, 4, p.C, dims_bc, str_bc, box, sw, promo) ||
         !encode_tensor_map(&w.tm_b, bf16, 4, p.B, dims_bc, str_bc, box, sw, promo) ||
         !encode_tensor_map(&w.tm_x, bf16, 4, p.x, dims_x, str_x, box, sw, promo) ||
