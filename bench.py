@@ -408,7 +408,8 @@ def bench_ssd(dev, hbm_peak, tc_peak, runs=20):
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     res = {"note": "chunks of 128 tokens on the tensor cores (tcgen05, bf16 operands, fp32 accumulators in "
-                   "tensor memory); three launches; median of 20, L2 flushed before each; hbm_frac of the "
+                   "tensor memory); one launch, one CTA walking the sequence of each (batch, head) with the "
+                   "state in registers; median of 20, L2 flushed before each; hbm_frac of the "
                    "measured copy bandwidth, tensor_frac of the measured cuBLAS bf16 burst"}
     for name in ("mamba2_130m_layer", "mamba2_2p7b_layer"):
         shape = W.SSD_SHAPES[name]

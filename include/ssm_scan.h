@@ -332,9 +332,13 @@ SSM_API ssm_status ssm_scan_fwd_noalloc(const void* u, const void* delta, const 
  * (Δ_t when a_h = 0), the state (headdim × d_state) follows
  *   H_t = Ā_t H_{t-1} + φ_t x_t B_tᵀ,   out_t = (H_t C_t + D_h x_t) · silu(z_t)
  * from H_0 = initial_state (zero when NULL).  Evaluated in chunks of 128
- * tokens on the tensor cores (bf16 operands, fp32 accumulation; the state
- * handed from one chunk to the next's tensor cores is rounded to bf16, and is
- * carried between chunks in fp32).
+ * tokens on the tensor cores (bf16 operands, fp32 accumulation; the operands
+ * the library computes — the masked decay-weighted C·Bᵀ, the weighted x of a
+ * chunk's state and the state entering a chunk — go in as two bf16 terms each,
+ * and the state is carried between chunks in fp32).  With batch · nheads ≥ 64
+ * one CTA walks the whole sequence of each (batch, head), the state in
+ * registers; below that the chunks run in parallel with a chunk-state pass
+ * through the workspace.
  *   x, z, out: [batch][seqlen][nheads][headdim] bf16, 16-byte aligned (z may be NULL).
  *   dt: [batch][seqlen][nheads] bf16 (Δraw).
  *   B, C: [batch][seqlen][ngroups][d_state] bf16, 16-byte aligned; head h
@@ -343,12 +347,14 @@ SSM_API ssm_status ssm_scan_fwd_noalloc(const void* u, const void* delta, const 
  *   initial_state, final_state: [batch][nheads][headdim][d_state] float32, or NULL.
  *   workspace: at least ssd_scan_workspace_bytes(dims) bytes, 16-byte aligned,
  *     caller-owned; its error word is read by ssm_scan_check (a tensor-core
- *     wait that ran out of time).
+ *     wait that ran out of time).  256 bytes (the error words) for the
+ *     sequence-walking form; the chunk states besides for the chunk-parallel one.
  * seqlen may be 0: x, dt, B, C, z and out may then be NULL and final_state
  * receives the initial state.
  * Supported: act = SSM_DTYPE_BF16, headdim = 64, d_state = 128, nheads and batch
  * ≤ 65535 (else SSM_ERR_UNSUPPORTED); nheads a multiple of ngroups (else
- * SSM_ERR_INVALID_ARG).  Three kernel launches on `stream`; no host sync.
+ * SSM_ERR_INVALID_ARG).  One kernel launch on `stream` (three in the
+ * chunk-parallel form); no host sync.
  */
 typedef struct {
   int64_t batch;
@@ -393,6 +399,7 @@ SSM_API ssm_status ssd_step(float* state, const void* x, const void* dt, const f
  * a chunk count, or a device-side wait that never completes) and are not part of
  * the supported interface:
  *   SSM_FORCE_KERNEL = tiles | rows | stream | tiny   scan kernel, where the shape allows it
+ *   SSM_FORCE_KERNEL = ssd_walk | ssd_chunks           form of ssd_scan_fwd (and its workspace size)
  *   SSM_FORCE_CHUNKS = n        sequence chunks of the scan
  *   SSM_FORCE_TPR = 2           two threads per row in the row kernel
  *   SSM_CTAS_PER_SM = n         resident CTAs per SM assumed by the row kernel's planner

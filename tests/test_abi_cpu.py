@@ -321,3 +321,18 @@ def test_host_scan_validates_before_any_copy(lib):
     assert _host_scan(lib, d, 4096, ctypes.c_void_p(FAKE), need, {"out": None}) == ssm.SSM_ERR_INVALID_ARG
     bad = _dims(d_state=65)
     assert _host_scan(lib, bad, 16, ctypes.c_void_p(FAKE), 1 << 30) == ssm.SSM_ERR_UNSUPPORTED
+
+
+def test_ssd_walking_form_needs_only_the_error_words(lib, hooks):
+    """batch · nheads ≥ 64 selects the form where one CTA walks each (batch, head): its
+    workspace is the 256 bytes of error words; the chunk-parallel form (forced, or below
+    the threshold) needs the chunk states besides."""
+    many = _ssd_dims(batch=2, nheads=40, ngroups=4)
+    few = _ssd_dims()
+    assert lib.ssd_scan_workspace_bytes(ctypes.byref(many)) == 256
+    assert lib.ssd_scan_workspace_bytes(ctypes.byref(few)) > 256
+    assert _ssd(lib, many, ws_bytes=255) == ssm.SSM_ERR_WORKSPACE
+    hooks.set("SSM_FORCE_KERNEL", "ssd_chunks")
+    assert lib.ssd_scan_workspace_bytes(ctypes.byref(many)) > 256
+    hooks.set("SSM_FORCE_KERNEL", "ssd_walk")
+    assert lib.ssd_scan_workspace_bytes(ctypes.byref(few)) == 256
