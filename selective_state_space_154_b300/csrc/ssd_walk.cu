@@ -17,9 +17,11 @@
 //    previous chunk's last reader of the tile is done; both wait on mbarriers only;
 //  * 16 compute warps (tensor-memory lane quarter = warp % 4, column quarter =
 //    warp / 4) build the operands the kernel computes, read the accumulators and
-//    write the outputs.  Per chunk c, in order: diag(w) X (the warps with no block
-//    of G below the diagonal), G (the others), then, while G X runs, chunk c − 1's
-//    outputs and chunk c + 1's token scalars, then the state update.  Each warp
+//    write the outputs.  Per chunk c, in order: diag(w) X (the six warps whose block
+//    of G lies above the diagonal, all zeros), G (the other ten), then, while G X
+//    runs, chunk c − 1's outputs and chunk c + 1's token scalars (with the decay
+//    weights that spare G below the diagonal and diag(w) X an exponential per
+//    element), then the state update.  Each warp
 //    writes its outputs to a staging tile of its own and stores it with one tensor
 //    store, so no global store of a compute thread is in flight at its next fence.
 // The tensor cores run, per chunk: S, then C h_inᵀ and the chunk state Bᵀ diag(w) X
