@@ -400,6 +400,7 @@ SSM_API ssm_status ssd_step(float* state, const void* x, const void* dt, const f
  * the supported interface:
  *   SSM_FORCE_KERNEL = tiles | rows | stream | tiny   scan kernel, where the shape allows it
  *   SSM_FORCE_KERNEL = ssd_walk | ssd_chunks           form of ssd_scan_fwd (and its workspace size)
+ *   SSM_SSD_SPLIT = k           the walking form cuts every (batch, head) into k segments
  *   SSM_FORCE_CHUNKS = n        sequence chunks of the scan
  *   SSM_FORCE_TPR = 2           two threads per row in the row kernel
  *   SSM_CTAS_PER_SM = n         resident CTAs per SM assumed by the row kernel's planner

@@ -46,6 +46,7 @@
 // Every wait is bounded.  A timeout sets the error word (workspace byte 4) and a
 // shared abort flag; from then on no wait blocks, every warp runs its loop to the
 // end, the issued copies and products are drained and the CTA leaves.
+#include <algorithm>
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -81,10 +82,17 @@ __device__ __forceinline__ uint32_t col_yin(int k) { return 320u + 128u * (uint3
 // named barriers (0 is __syncthreads): all compute warps; the token-scalar warps 0..3
 constexpr int kBarCompute = 1, kBarTokens = 2;
 
+// Work: CTA i < full_units walks (batch, head) unit i over the whole sequence.  The
+// units left over after the launch's full rounds of CTAs are cut into seg_k segments
+// of chunks each: the CTA of segment s walks the chunks before its segment with the
+// state update alone (the chunk state, no S, G or outputs), then its own chunks in
+// full, so that the last round's few units use every SM.
 struct WalkParams {
   CUtensorMap tm_c, tm_b, tm_x, tm_out;
   SsdArgs a;
   unsigned* err;
+  int64_t full_units;
+  int seg_k;
 };
 
 struct WalkSmem {
@@ -176,14 +184,15 @@ __device__ __forceinline__ void warp_arrive_plain(uint32_t bar) {
   if ((threadIdx.x & 31) == 0) ac::mbar_arrive(bar);
 }
 
-// Chunk c's C and B, two boxes each (n 0..63 and 64..127), 65,536 bytes on bar_ldcb.
-__device__ __forceinline__ void issue_cb(WalkSmem& sm, const WalkParams& w, int64_t c, int b, int g) {
+// Chunk c's C and B, two boxes each (n 0..63 and 64..127), 65,536 bytes on bar_ldcb
+// (B alone for a chunk walked for its state only).
+__device__ __forceinline__ void issue_cb(WalkSmem& sm, const WalkParams& w, int64_t c, int b, int g, bool with_c) {
   const uint32_t bar = ac::smem_u32(&sm.bar_ldcb);
   const int t0 = (int)(c * kQ);
-  ac::mbar_arrive_expect_tx(bar, 4 * kBoxBytes);
+  ac::mbar_arrive_expect_tx(bar, (with_c ? 4 : 2) * kBoxBytes);
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    ac::tma_load_4d(ac::smem_u32(sm.c + j * kBoxBytes), &w.tm_c, j * 64, g, t0, b, bar);
+    if (with_c) ac::tma_load_4d(ac::smem_u32(sm.c + j * kBoxBytes), &w.tm_c, j * 64, g, t0, b, bar);
     ac::tma_load_4d(ac::smem_u32(sm.b + j * kBoxBytes), &w.tm_b, j * 64, g, t0, b, bar);
   }
 }
@@ -198,14 +207,22 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   WalkSmem& sm = *reinterpret_cast<WalkSmem*>(smem_raw);
   const SsdArgs& p = w.a;
-  const int64_t bh = blockIdx.x, b = bh / p.H, h = bh % p.H, g = h / (p.H / p.G);
+  const int64_t nch = p.nchunks;
+  // this CTA's (batch, head) and its chunks [c_begin, c_end), walked from chunk 0
+  int64_t bh = blockIdx.x, c_begin = 0, c_end = nch;
+  if (bh >= w.full_units) {
+    const int64_t j = bh - w.full_units, sgi = j % w.seg_k;
+    bh = w.full_units + j / w.seg_k;
+    c_begin = sgi * nch / w.seg_k;
+    c_end = (sgi + 1) * nch / w.seg_k;
+  }
+  const int64_t b = bh / p.H, h = bh % p.H, g = h / (p.H / p.G);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wq = warp & 3, cq = warp >> 2;
   const int row = wq * 32 + lane;  // a compute thread's tensor-memory lane: token t or state n
   const uint32_t bar_ldcb = ac::smem_u32(&sm.bar_ldcb), bar_ldx = ac::smem_u32(&sm.bar_ldx),
                  bar_a = ac::smem_u32(&sm.bar_a), bar_cb = ac::smem_u32(&sm.bar_cb), bar_c = ac::smem_u32(&sm.bar_c),
                  bar_wx = ac::smem_u32(&sm.bar_wx), bar_g = ac::smem_u32(&sm.bar_g), bar_h = ac::smem_u32(&sm.bar_h),
                  bar_drain = ac::smem_u32(&sm.bar_drain), bar_never = ac::smem_u32(&sm.bar_never);
-  const int64_t nch = p.nchunks;
   const long long tmo = p.timeout_ns;
   const bool compute = warp < kComputeWarps;
   if (threadIdx.x == 0) {
@@ -244,13 +261,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
   auto chunk_len = [&](int64_t c) { return (int)(p.L - c * kQ < kQ ? p.L - c * kQ : kQ); };
   auto load_dt = [&](int64_t c) {  // token threadIdx.x of chunk c (warps 0..3), 0 past the end
     const int64_t t = c * kQ + threadIdx.x;
-    return (c < nch && t < p.L) ? __bfloat162float(bf(p.dt)[(b * p.L + t) * p.H + h]) : 0.f;
+    return (c < c_end && t < p.L) ? __bfloat162float(bf(p.dt)[(b * p.L + t) * p.H + h]) : 0.f;
   };
   // token scalars of chunk c into buffers c % 3 (cs2) and c & 1 (phi) (warps 0..3, token = threadIdx.x)
   auto token_scalars = [&](int64_t c, float dtv) {
     const int i = threadIdx.x, par = (int)(c & 1);
     float la = 0.f, ph = 0.f;
-    if (c < nch && i < chunk_len(c)) {
+    if (c < c_end && i < chunk_len(c)) {
       // Δ = softplus(Δraw + bias) and φ = (e^{Δa} − 1)/a with the MUFU ex2 / lg2: e^x − 1
       // as 2^{x log2 e} − 1 for |x| ≥ 1/16 (relative error below 2^-18), by its series
       // to x^6 below (truncation below 2^-36)
@@ -332,16 +349,19 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
       const uint64_t dg0 = tc::kslice_desc(a_g0, kQ, 0), dg1 = tc::kslice_desc(a_g1, kQ, 0);
       auto at = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
       constexpr uint32_t kSw = (uint32_t)kQ * 128;  // 128-byte swizzle: K 64..127 column block
-      for (int64_t c = 0; c < nch; ++c) {
+      for (int64_t c = 0; c < c_end; ++c) {
         const uint32_t par = (uint32_t)(c & 1), prev = (uint32_t)((c - 1) & 1);
         const int k = (int)(c & 1);
+        const bool full = c >= c_begin;  // else the chunk state alone
         // S: C and B of chunk c landed (chunk c − 1's G has read S: bar_g awaited before its Y)
         if (!wait_bar(sm, p.fault && c == 0 ? bar_never : bar_ldcb, par, tmo, w.err)) break;
         tc::fence_after_sync();
+        if (full) {
 #pragma unroll
-        for (int kk = 0; kk < kN / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * kSw + (kk & 3) * 32;
-          tc::mma_bf16(tmem + kColS, at(dc, o), at(db, o), id_s, kk > 0);
+          for (int kk = 0; kk < kN / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * kSw + (kk & 3) * 32;
+            tc::mma_bf16(tmem + kColS, at(dc, o), at(db, o), id_s, kk > 0);
+          }
         }
         tc::mma_commit(bar_a);
         if (c > 0) {
@@ -349,12 +369,16 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
           if (!wait_bar(sm, bar_h, prev, tmo, w.err)) break;
           tc::fence_after_sync();
         }
+        if (full) {
 #pragma unroll
-        for (int kk = 0; kk < kN / 16; ++kk)
-          tc::mma_bf16(tmem + col_yin(k), at(dc, (kk >> 2) * kSw + (kk & 3) * 32), at(dh0, kk * 256), id_yin, kk > 0);
+          for (int kk = 0; kk < kN / 16; ++kk)
+            tc::mma_bf16(tmem + col_yin(k), at(dc, (kk >> 2) * kSw + (kk & 3) * 32), at(dh0, kk * 256), id_yin,
+                         kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < kN / 16; ++kk)
-          tc::mma_bf16(tmem + col_yin(k), at(dc, (kk >> 2) * kSw + (kk & 3) * 32), at(dh1, kk * 256), id_yin, true);
+          for (int kk = 0; kk < kN / 16; ++kk)
+            tc::mma_bf16(tmem + col_yin(k), at(dc, (kk >> 2) * kSw + (kk & 3) * 32), at(dh1, kk * 256), id_yin,
+                         true);
+        }
         // the chunk state, hi and lo terms of diag(w) X side by side (N = 128)
         if (!wait_bar(sm, bar_wx, par, tmo, w.err)) break;
         tc::fence_after_sync();
@@ -364,12 +388,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         tc::mma_commit(bar_cb);  // C and B are free once S, Y_in and the chunk state are done
         if (!wait_bar(sm, bar_g, par, tmo, w.err)) break;
         tc::fence_after_sync();
+        if (full) {
 #pragma unroll
-        for (int kk = 0; kk < kQ / 16; ++kk)
-          tc::mma_bf16(tmem + col_y(k), at(dg0, kk * 4096), at(dx, kk * 2048), id_y, kk > 0);
+          for (int kk = 0; kk < kQ / 16; ++kk)
+            tc::mma_bf16(tmem + col_y(k), at(dg0, kk * 4096), at(dx, kk * 2048), id_y, kk > 0);
 #pragma unroll
-        for (int kk = 0; kk < kQ / 16; ++kk)
-          tc::mma_bf16(tmem + col_y(k), at(dg1, kk * 4096), at(dx, kk * 2048), id_y, true);
+          for (int kk = 0; kk < kQ / 16; ++kk)
+            tc::mma_bf16(tmem + col_y(k), at(dg1, kk * 4096), at(dx, kk * 2048), id_y, true);
+        }
         tc::mma_commit(bar_c);  // covers Y_in, the chunk state and Y
       }
     }
@@ -380,14 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
       ac::prefetch_tensormap(&w.tm_c);
       ac::prefetch_tensormap(&w.tm_b);
       ac::prefetch_tensormap(&w.tm_x);
-      issue_cb(sm, w, 0, (int)b, (int)g);
+      issue_cb(sm, w, 0, (int)b, (int)g, c_begin == 0);
       issue_x(sm, w, 0, (int)b, (int)h);
       int64_t cb_issued = 1, x_issued = 1;
-      for (int64_t c = 1; c < nch; ++c) {
+      for (int64_t c = 1; c < c_end; ++c) {
         const uint32_t prev = (uint32_t)((c - 1) & 1);
         // C and B take chunk c once chunk c − 1's S, C h_inᵀ and chunk state are done
         if (!wait_bar(sm, bar_cb, prev, tmo, w.err)) break;
-        issue_cb(sm, w, c, (int)b, (int)g);
+        issue_cb(sm, w, c, (int)b, (int)g, c >= c_begin);
         cb_issued = c + 1;
         // X takes chunk c once chunk c − 1's G X (and diag(w) X, before it) are done
         if (!wait_bar(sm, bar_c, prev, tmo, w.err)) break;
@@ -460,8 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         }
       }
     };
-    for (int64_t c = 0; c < nch; ++c) {
+    for (int64_t c = 0; c < c_end; ++c) {
       const uint32_t par = (uint32_t)(c & 1);
+      const bool full = c >= c_begin, prev_out = c - 1 >= c_begin;
       named_sync(kBarCompute, kComputeThreads);  // chunk c's scalars visible
       const float* cs2 = sm.cs2[c % 3];
       const float* phi = sm.phi[c & 1];
@@ -492,10 +519,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         }
         warp_arrive(bar_wx);
         warp_arrive_plain(bar_g);
-        load_xz(c - 1, xv, zv);
+        if (prev_out) load_xz(c - 1, xv, zv);
+      } else if (!full) {  // a chunk walked for its state: no G (bar_a still awaited, phase by phase)
+        warp_arrive_plain(bar_wx);
+        (void)__all_sync(0xffffffffu, wait_bar(sm, bar_a, par, tmo, w.err));
+        warp_arrive_plain(bar_g);
       } else {
         warp_arrive_plain(bar_wx);
-        load_xz(c - 1, xv, zv);  // read ahead of the wait for S
+        if (prev_out) load_xz(c - 1, xv, zv);  // read ahead of the wait for S
         // G_ts for this thread's token row t and tokens s = 32·cq .. 32·cq + 31 (s ≤ t)
         const bool ok = __all_sync(0xffffffffu, wait_bar(sm, bar_a, par, tmo, w.err));
         tc::fence_after_sync();
@@ -539,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         warp_arrive(bar_g);
       }
       // while G X runs: the previous chunk's outputs, the next chunk's token scalars
-      if (c > 0) outputs(c - 1, true, xv, zv);
+      if (prev_out) outputs(c - 1, true, xv, zv);
       if (warp < 4) {
         token_scalars(c + 1, dt_next);
         dt_next = load_dt(c + 2);
@@ -557,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         put_state();
       }
       warp_arrive(bar_h);  // h_in of chunk c + 1 written; chunk c − 1's outputs read Y, Y_in
-      if (c + 1 == nch) {
+      if (c + 1 == c_end) {
         load_xz(c, xv, zv);
         outputs(c, okc, xv, zv);
       }
@@ -565,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
     // every tensor store of this warp has completed before the CTA leaves
     if (lane == 0) ac::bulk_wait0();
     __syncwarp();
-    if (!aborted(sm) && p.final_state) {
+    if (!aborted(sm) && p.final_state && c_end == nch) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) p.final_state[sbase + j * kN] = hs[j];
     }
@@ -614,7 +645,27 @@ cudaError_t ssd_walk_launch(SsdArgs p, unsigned* err, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(ssd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)sizeof(WalkSmem));
   if (e != cudaSuccess) return e;
-  ssd_walk_kernel<<<(unsigned)(p.batch * p.H), kThreads, sizeof(WalkSmem), stream>>>(w);
+  // one CTA per SM: the units beyond the last full round of SMs are cut into segments
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int64_t units = p.batch * p.H;
+  w.full_units = units;
+  w.seg_k = 1;
+  const int force = runtime_knobs().ssd_split;
+  if (force > 0) {
+    w.full_units = 0;
+    w.seg_k = (int)(force < p.nchunks ? force : (p.nchunks > 0 ? p.nchunks : 1));
+  } else if (sms > 0 && p.nchunks >= 2) {
+    const int64_t rem = units % sms;
+    const int64_t k = rem > 0 ? std::min<int64_t>(p.nchunks, sms / rem) : 1;
+    if (k > 1) {
+      w.full_units = units - rem;
+      w.seg_k = (int)k;
+    }
+  }
+  const int64_t grid = w.full_units + (units - w.full_units) * w.seg_k;
+  ssd_walk_kernel<<<(unsigned)grid, kThreads, sizeof(WalkSmem), stream>>>(w);
   return cudaGetLastError();
 }
 

@@ -50,6 +50,7 @@ RuntimeKnobs* load_knobs() {
     r->stream_rows = (v == 512 || v == 128) ? v : 0;
   }
   if (const char* c = std::getenv("SSM_STREAM_CTAS")) r->stream_ctas = std::atoi(c);
+  if (const char* c = std::getenv("SSM_SSD_SPLIT")) r->ssd_split = std::atoi(c);
   return r;
 }
 

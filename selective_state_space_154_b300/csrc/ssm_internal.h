@@ -79,6 +79,7 @@ struct RuntimeKnobs {
   int stream_rows;                // >0: rows per CTA of the streamed row kernel (512, 256 or 128)
   int stream_ctas;                // >0: work items (CTAs) of the streamed row kernel
   int force_ssd;                  // SSD form: 0 by shape, 1 one CTA per (batch, head), 2 chunk-parallel
+  int ssd_split;                  // >0: the walking SSD form cuts every (batch, head) into this many segments
 };
 RuntimeKnobs runtime_knobs();  // the test hooks as last loaded (first use, or ssm_test_hooks_reload)
 void reload_knobs();

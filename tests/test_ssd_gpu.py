@@ -211,3 +211,30 @@ def test_ssd_step_mamba2_2p7b_decode_sampled_heads():
         ref, href = _oracle(sub, state0[:, h:h + 1])
         assert rel_err(to_np(y[:, h:h + 1]), ref[:, 0]) <= BF16, h
         assert rel_err(to_np(state[:, h:h + 1]), href) <= 1e-5, h
+
+
+@pytest.mark.parametrize("split", [2, 3, 5])
+def test_ssd_walk_segments_from_a_state_only_prefix(hooks, split):
+    """Every (batch, head) cut into `split` segments of chunks: each segment's CTA walks the
+    chunks before it for the state alone, then its own in full; outputs and the final
+    state (written by the last segment) match the oracle, from a nonzero initial state."""
+    hooks.set("SSM_FORCE_KERNEL", "ssd_walk")
+    hooks.set("SSM_SSD_SPLIT", split)
+    inp = W.random_ssd_inputs(2, 700, 3, 64, 1, 128, device=DEV, seed=60 + split)
+    h0 = torch.randn((2, 3, 64, 128), generator=torch.Generator(device=DEV).manual_seed(split), device=DEV)
+    _compare(inp, h0)
+
+
+def test_ssd_walk_remainder_units_split_across_the_gpu():
+    """2 × 80 heads: one full round of CTAs, and the units left over cut into segments
+    (the default split); sampled heads of both kinds against the oracle."""
+    inp = W.random_ssd_inputs(2, 1000, 80, 64, 4, 128, device=DEV, seed=71)
+    out, fs = _gpu(inp)
+    for b_, h_ in ((0, 3), (1, 60), (1, 68), (1, 79)):
+        # head h_ of batch b_, with its group's B and C (20 heads per group)
+        sub = {k: (None if v is None else v[b_:b_ + 1, :, h_:h_ + 1] if k in ("x", "z", "dt")
+                   else v[h_:h_ + 1] if k in ("A", "D", "dt_bias") else v[b_:b_ + 1, :, (h_ // 20):(h_ // 20) + 1])
+               for k, v in inp.items()}
+        ref, href = _oracle(sub)
+        assert rel_err(to_np(out[b_:b_ + 1, :, h_:h_ + 1]), ref) <= BF16, (b_, h_)
+        assert rel_err(to_np(fs[b_:b_ + 1, h_:h_ + 1]), href) <= BF16, (b_, h_)
