@@ -598,7 +598,7 @@ bool ssd_use_walk(int64_t batch, int64_t L, int64_t H) {
 }
 
 size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H) {
-  if (ssd_use_walk(batch, L, H)) return 256;  // the error words only
+  if (ssd_use_walk(batch, L, H)) return ssd_walk_workspace_bytes(ssd_walk_split(batch, H, L));
   const int64_t nch = (L + kQ - 1) / kQ;
   const WsSizes z = ws_sizes(batch, H, nch < 1 ? 1 : nch);
   return 256 + z.hc + z.ctot + z.hin;
@@ -606,7 +606,7 @@ size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H) {
 
 cudaError_t ssd_launch(SsdArgs p, cudaStream_t stream) {
   if (ssd_use_walk(p.batch, p.L, p.H))
-    return ssd_walk_launch(p, reinterpret_cast<unsigned*>(p.ws) + 1, stream);
+    return ssd_walk_launch(p, p.ws, stream);
   p.nchunks = (p.L + kQ - 1) / kQ;
   if (p.timeout_ns <= 0) p.timeout_ns = (long long)kDefaultTimeoutMs * 1000000ll;
   // heads per CTA: the largest divisor of the heads of a group up to kMaxHeadsPerCta

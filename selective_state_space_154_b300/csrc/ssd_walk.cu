@@ -84,15 +84,23 @@ constexpr int kBarCompute = 1, kBarTokens = 2;
 
 // Work: CTA i < full_units walks (batch, head) unit i over the whole sequence.  The
 // units left over after the launch's full rounds of CTAs are cut into seg_k segments
-// of chunks each: the CTA of segment s walks the chunks before its segment with the
-// state update alone (the chunk state, no S, G or outputs), then its own chunks in
-// full, so that the last round's few units use every SM.
+// of chunks each, so that the last round's few units use every SM.  The CTA of
+// segment s walks its chunks twice: first for the state alone (the chunk-state
+// products, no S, G or outputs; from the initial state for s = 0, from zero else),
+// and publishes that end state and its total log decay in the workspace behind a
+// release flag (s < seg_k − 1); then it combines the published states of segments
+// 0 .. s − 1 in order (decoupled look-back: each is 2^{decay}·(state so far) + its
+// own) into the state entering its chunks, and walks them in full.  The last segment
+// needs no first walk.
 struct WalkParams {
   CUtensorMap tm_c, tm_b, tm_x, tm_out;
   SsdArgs a;
   unsigned* err;
   int64_t full_units;
   int seg_k;
+  unsigned* seg_flag;  // [slot] 1 once the segment's state is published
+  float* seg_decay;    // [slot] Σ Δa over the segment, log2 units
+  float* seg_state;    // [slot][P][N] the segment's end state (fp32)
 };
 
 struct WalkSmem {
@@ -208,14 +216,25 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
   WalkSmem& sm = *reinterpret_cast<WalkSmem*>(smem_raw);
   const SsdArgs& p = w.a;
   const int64_t nch = p.nchunks;
-  // this CTA's (batch, head) and its chunks [c_begin, c_end), walked from chunk 0
-  int64_t bh = blockIdx.x, c_begin = 0, c_end = nch;
+  // this CTA's (batch, head) and its chunks [c0, c0 + m); a split unit's segment seg
+  int64_t bh = blockIdx.x, c0 = 0, c1 = nch, slot0 = 0;
+  int seg = 0, nseg = 1;
   if (bh >= w.full_units) {
-    const int64_t j = bh - w.full_units, sgi = j % w.seg_k;
+    const int64_t j = bh - w.full_units;
+    seg = (int)(j % w.seg_k);
+    nseg = w.seg_k;
+    slot0 = j - seg;  // slot of the unit's segment 0
     bh = w.full_units + j / w.seg_k;
-    c_begin = sgi * nch / w.seg_k;
-    c_end = (sgi + 1) * nch / w.seg_k;
+    c0 = (int64_t)seg * nch / nseg;
+    c1 = (int64_t)(seg + 1) * nch / nseg;
   }
+  const int64_t m = c1 - c0;
+  const bool pre = seg < nseg - 1;   // a first walk for the state alone, then publish
+  const bool need_in = seg > 0;      // the state entering the chunks comes from the others
+  // steps: the first walk (m chunks, state alone) if pre, then the full walk
+  const int64_t nv = pre ? 2 * m : m;
+  auto chunk_of = [&](int64_t v) { return c0 + (pre && v >= m ? v - m : v); };
+  auto full_of = [&](int64_t v) { return !pre || v >= m; };
   const int64_t b = bh / p.H, h = bh % p.H, g = h / (p.H / p.G);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wq = warp & 3, cq = warp >> 2;
   const int row = wq * 32 + lane;  // a compute thread's tensor-memory lane: token t or state n
@@ -254,20 +273,46 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
       *reinterpret_cast<uint4*>(sm.h[1] + off) = lo;
     }
   };
+  // The state entering this segment: the published end states of segments 0 .. seg − 1
+  // folded in order (segment 0's is its true end state, each later one its own end state
+  // from zero, added to the state so far decayed over it).  Bounded waits on the flags.
+  auto combine_in = [&](float (&out)[16]) {
+    for (int j = 0; j < seg; ++j) {
+      const int64_t slot = slot0 + j;
+      const unsigned long long start = globaltimer_ns();
+      for (int it = 0; it < (1 << 28); ++it) {
+        if (ld_acquire_gpu(w.seg_flag + slot) != 0u) break;
+        if ((it & 15) == 15) {
+          if (aborted(sm)) break;
+          if ((long long)(globaltimer_ns() - start) > p.timeout_ns) {
+            atomicOr(w.err, kErrTimeout);
+            *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+            break;
+          }
+        }
+        __nanosleep(200);
+      }
+      const float dec = ex2_approx(w.seg_decay[slot]);
+      const float* st = w.seg_state + slot * kP * kN + (int64_t)(16 * cq) * kN + row;
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) out[jj] = j == 0 ? st[jj * kN] : fmaf(dec, out[jj], st[jj * kN]);
+    }
+  };
   const float a = p.A[h];
   const float inv_a = a != 0.f ? 1.f / a : 0.f;
   const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
   const float Dh = p.D ? p.D[h] : 0.f;
   auto chunk_len = [&](int64_t c) { return (int)(p.L - c * kQ < kQ ? p.L - c * kQ : kQ); };
-  auto load_dt = [&](int64_t c) {  // token threadIdx.x of chunk c (warps 0..3), 0 past the end
-    const int64_t t = c * kQ + threadIdx.x;
-    return (c < c_end && t < p.L) ? __bfloat162float(bf(p.dt)[(b * p.L + t) * p.H + h]) : 0.f;
+  auto load_dt = [&](int64_t v) {  // token threadIdx.x of step v's chunk (warps 0..3), 0 past the end
+    const int64_t t = chunk_of(v) * kQ + threadIdx.x;
+    return (v < nv && t < p.L) ? __bfloat162float(bf(p.dt)[(b * p.L + t) * p.H + h]) : 0.f;
   };
-  // token scalars of chunk c into buffers c % 3 (cs2) and c & 1 (phi) (warps 0..3, token = threadIdx.x)
-  auto token_scalars = [&](int64_t c, float dtv) {
-    const int i = threadIdx.x, par = (int)(c & 1);
+  // token scalars of step v's chunk into buffers v % 3 (cs2) and v & 1 (the others)
+  // (warps 0..3, token = threadIdx.x)
+  auto token_scalars = [&](int64_t step, float dtv) {
+    const int i = threadIdx.x, par = (int)(step & 1);
     float la = 0.f, ph = 0.f;
-    if (c < c_end && i < chunk_len(c)) {
+    if (step < nv && i < chunk_len(chunk_of(step))) {
       // Δ = softplus(Δraw + bias) and φ = (e^{Δa} − 1)/a with the MUFU ex2 / lg2: e^x − 1
       // as 2^{x log2 e} − 1 for |x| ≥ 1/16 (relative error below 2^-18), by its series
       // to x^6 below (truncation below 2^-36)
@@ -298,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
     const float c2 = v * kLog2e;
     // the token's 32-block is this warp's: its last prefix sum is lane 31's
     const float block_end = __shfl_sync(0xffffffffu, c2, 31);
-    sm.cs2[c % 3][i] = c2;
+    sm.cs2[step % 3][i] = c2;
     sm.phi[par][i] = ph;
     sm.ep[par][i] = ex2_approx(block_end - c2) * ph;
     sm.wgt[par][i] = ex2_approx(total * kLog2e - c2) * ph;
@@ -306,8 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
 
   float dt_next = 0.f;
   if (compute) {
+    if (!pre && need_in) {
+      combine_in(hs);  // the last segment of a split unit walks once, from the others' states
+    } else {
+      // the initial state, or zero for the first walk of a later segment
 #pragma unroll
-    for (int j = 0; j < 16; ++j) hs[j] = p.h0 ? p.h0[sbase + j * kN] : 0.f;
+      for (int j = 0; j < 16; ++j) hs[j] = (p.h0 && !need_in) ? p.h0[sbase + j * kN] : 0.f;
+    }
     put_state();
     // G blocks above the diagonal (tokens s of column block cq all after the warp's t) stay zero
     if (cq > wq) {
@@ -349,12 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
       const uint64_t dg0 = tc::kslice_desc(a_g0, kQ, 0), dg1 = tc::kslice_desc(a_g1, kQ, 0);
       auto at = [](uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); };
       constexpr uint32_t kSw = (uint32_t)kQ * 128;  // 128-byte swizzle: K 64..127 column block
-      for (int64_t c = 0; c < c_end; ++c) {
-        const uint32_t par = (uint32_t)(c & 1), prev = (uint32_t)((c - 1) & 1);
-        const int k = (int)(c & 1);
-        const bool full = c >= c_begin;  // else the chunk state alone
-        // S: C and B of chunk c landed (chunk c − 1's G has read S: bar_g awaited before its Y)
-        if (!wait_bar(sm, p.fault && c == 0 ? bar_never : bar_ldcb, par, tmo, w.err)) break;
+      for (int64_t v = 0; v < nv; ++v) {
+        const uint32_t par = (uint32_t)(v & 1), prev = (uint32_t)((v - 1) & 1);
+        const int k = (int)(v & 1);
+        const bool full = full_of(v);  // else the chunk state alone
+        // S: C and B of the chunk landed (the previous step's G has read S: bar_g awaited before its Y)
+        if (!wait_bar(sm, p.fault && v == 0 ? bar_never : bar_ldcb, par, tmo, w.err)) break;
         tc::fence_after_sync();
         if (full) {
 #pragma unroll
@@ -364,8 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
           }
         }
         tc::mma_commit(bar_a);
-        if (c > 0) {
-          // h_in of chunk c written (and chunk c − 2's outputs have read Y[k], Y_in[k])
+        if (v > 0) {
+          // h_in of the chunk written (and step v − 2's outputs have read Y[k], Y_in[k])
           if (!wait_bar(sm, bar_h, prev, tmo, w.err)) break;
           tc::fence_after_sync();
         }
@@ -406,19 +456,19 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
       ac::prefetch_tensormap(&w.tm_c);
       ac::prefetch_tensormap(&w.tm_b);
       ac::prefetch_tensormap(&w.tm_x);
-      issue_cb(sm, w, 0, (int)b, (int)g, c_begin == 0);
-      issue_x(sm, w, 0, (int)b, (int)h);
+      issue_cb(sm, w, chunk_of(0), (int)b, (int)g, full_of(0));
+      issue_x(sm, w, chunk_of(0), (int)b, (int)h);
       int64_t cb_issued = 1, x_issued = 1;
-      for (int64_t c = 1; c < c_end; ++c) {
-        const uint32_t prev = (uint32_t)((c - 1) & 1);
-        // C and B take chunk c once chunk c − 1's S, C h_inᵀ and chunk state are done
+      for (int64_t v = 1; v < nv; ++v) {
+        const uint32_t prev = (uint32_t)((v - 1) & 1);
+        // C and B take step v's chunk once step v − 1's S, C h_inᵀ and chunk state are done
         if (!wait_bar(sm, bar_cb, prev, tmo, w.err)) break;
-        issue_cb(sm, w, c, (int)b, (int)g, c >= c_begin);
-        cb_issued = c + 1;
-        // X takes chunk c once chunk c − 1's G X (and diag(w) X, before it) are done
+        issue_cb(sm, w, chunk_of(v), (int)b, (int)g, full_of(v));
+        cb_issued = v + 1;
+        // X takes it once step v − 1's G X (and diag(w) X, before it) are done
         if (!wait_bar(sm, bar_c, prev, tmo, w.err)) break;
-        issue_x(sm, w, c, (int)b, (int)h);
-        x_issued = c + 1;
+        issue_x(sm, w, chunk_of(v), (int)b, (int)h);
+        x_issued = v + 1;
       }
       // the last copies have landed before the CTA leaves (at once unless a wait timed out)
       wait_bar_drain(bar_ldcb, (uint32_t)((cb_issued - 1) & 1), tmo);
@@ -432,9 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
     // Outputs of chunk oc: token rows 32·wq .., p = 16·cq .. 16·cq + 15 of this warp,
     // through its staging tile and one tensor store (rows past L are clipped).
     // x and z of this thread's outputs of chunk oc (token row, p = 16·cq ..), zero past the end
-    auto load_xz = [&](int64_t oc, uint4 (&xv)[2], uint4 (&zv)[2]) {
+    auto load_xz = [&](int64_t ov, uint4 (&xv)[2], uint4 (&zv)[2]) {
+      const int64_t oc = chunk_of(ov);
       const int64_t off = ((b * p.L + oc * kQ + row) * p.H + h) * kP + 16 * cq;
-      const bool in = oc >= 0 && row < chunk_len(oc);
+      const bool in = row < chunk_len(oc);
       const uint4* xr = reinterpret_cast<const uint4*>(bf(p.x) + off);
       const uint4* zr = p.z ? reinterpret_cast<const uint4*>(bf(p.z) + off) : nullptr;
 #pragma unroll
@@ -443,12 +494,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         zv[m] = (in && zr) ? zr[m] : make_uint4(0, 0, 0, 0);
       }
     };
-    auto outputs = [&](int64_t oc, bool ok, const uint4 (&xv)[2], const uint4 (&zv)[2]) {
-      const int ok_k = (int)(oc & 1), t0 = (int)(oc * kQ);
+    auto outputs = [&](int64_t ov, bool ok, const uint4 (&xv)[2], const uint4 (&zv)[2]) {
+      const int ok_k = (int)(ov & 1), t0 = (int)(chunk_of(ov) * kQ);
       float y[16], yi[16];
       tc::tmem_ld16(tc::tmem_lane_addr(tmem + col_y(ok_k), wq * 32, cq * 16), y);
       tc::tmem_ld16(tc::tmem_lane_addr(tmem + col_yin(ok_k), wq * 32, cq * 16), yi);
-      const float et = ex2_approx(sm.cs2[oc % 3][row]);
+      const float et = ex2_approx(sm.cs2[ov % 3][row]);
       uint32_t ow[8];
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
@@ -486,12 +537,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         }
       }
     };
-    for (int64_t c = 0; c < c_end; ++c) {
-      const uint32_t par = (uint32_t)(c & 1);
-      const bool full = c >= c_begin, prev_out = c - 1 >= c_begin;
-      named_sync(kBarCompute, kComputeThreads);  // chunk c's scalars visible
-      const float* cs2 = sm.cs2[c % 3];
-      const float* phi = sm.phi[c & 1];
+    float logdec = 0.f;  // Σ Δa over the first walk so far, log2 units
+    for (int64_t v = 0; v < nv; ++v) {
+      const uint32_t par = (uint32_t)(v & 1);
+      const bool full = full_of(v), prev_out = v > 0 && full_of(v - 1);
+      named_sync(kBarCompute, kComputeThreads);  // step v's scalars visible
+      const float* cs2 = sm.cs2[v % 3];
+      const float* phi = sm.phi[v & 1];
       const float cs_end = cs2[kQ - 1];
       uint4 xv[2], zv[2];
       if (widx >= 0) {
@@ -504,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
             const uint32_t off = tc::kmajor_offset(kQ, s, pg * 8);
             // X granule pg of token s in the 128-byte swizzle of its tensor copy
             const uint4 xw = *reinterpret_cast<const uint4*>(sm.x + s * 128 + ((pg ^ (s & 7)) << 4));
-            const float wgt = sm.wgt[c & 1][s];
+            const float wgt = sm.wgt[v & 1][s];
             float f[8];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -519,14 +571,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         }
         warp_arrive(bar_wx);
         warp_arrive_plain(bar_g);
-        if (prev_out) load_xz(c - 1, xv, zv);
+        if (prev_out) load_xz(v - 1, xv, zv);
       } else if (!full) {  // a chunk walked for its state: no G (bar_a still awaited, phase by phase)
         warp_arrive_plain(bar_wx);
         (void)__all_sync(0xffffffffu, wait_bar(sm, bar_a, par, tmo, w.err));
         warp_arrive_plain(bar_g);
       } else {
         warp_arrive_plain(bar_wx);
-        if (prev_out) load_xz(c - 1, xv, zv);  // read ahead of the wait for S
+        if (prev_out) load_xz(v - 1, xv, zv);  // read ahead of the wait for S
         // G_ts for this thread's token row t and tokens s = 32·cq .. 32·cq + 31 (s ≤ t)
         const bool ok = __all_sync(0xffffffffu, wait_bar(sm, bar_a, par, tmo, w.err));
         tc::fence_after_sync();
@@ -539,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
           // below the diagonal every s of the block is before t:
           // 2^(cs2_t − cs2_s) φ_s = 2^(cs2_t − cs2_end(block)) · ep_s, both factors ≤ 1
           const float ft = ex2_approx(cst - cs2[cq * 32 + 31]);
-          const float* ep = sm.ep[c & 1];
+          const float* ep = sm.ep[v & 1];
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             const int s0 = cq * 32 + m * 8;
@@ -570,10 +622,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         warp_arrive(bar_g);
       }
       // while G X runs: the previous chunk's outputs, the next chunk's token scalars
-      if (prev_out) outputs(c - 1, true, xv, zv);
+      if (prev_out) outputs(v - 1, true, xv, zv);
       if (warp < 4) {
-        token_scalars(c + 1, dt_next);
-        dt_next = load_dt(c + 2);
+        token_scalars(v + 1, dt_next);
+        dt_next = load_dt(v + 2);
       }
       // chunk c's products done: the state entering chunk c + 1
       const bool okc = __all_sync(0xffffffffu, wait_bar(sm, bar_c, par, tmo, w.err));
@@ -585,18 +637,36 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
         const float dec = ex2_approx(cs_end);
 #pragma unroll
         for (int j = 0; j < 16; ++j) hs[j] = fmaf(dec, hs[j], hc[j] + hl[j]);
+        if (!full) logdec += cs_end;
+        if (pre && v == m - 1) {
+          // the first walk is done: publish its end state, then start the full walk from the
+          // initial state (segment 0) or from the combined states of the segments before
+          const int64_t slot = slot0 + seg;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) w.seg_state[slot * kP * kN + (16 * cq + j) * kN + row] = hs[j];
+          if (threadIdx.x == 0) w.seg_decay[slot] = logdec;
+          __threadfence();
+          named_sync(kBarCompute, kComputeThreads);
+          if (threadIdx.x == 0) st_release_gpu(w.seg_flag + slot, 1u);
+          if (need_in) {
+            combine_in(hs);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) hs[j] = p.h0 ? p.h0[sbase + j * kN] : 0.f;
+          }
+        }
         put_state();
       }
-      warp_arrive(bar_h);  // h_in of chunk c + 1 written; chunk c − 1's outputs read Y, Y_in
-      if (c + 1 == c_end) {
-        load_xz(c, xv, zv);
-        outputs(c, okc, xv, zv);
+      warp_arrive(bar_h);  // h_in of the next step written; step v − 1's outputs read Y, Y_in
+      if (v + 1 == nv) {
+        load_xz(v, xv, zv);
+        outputs(v, okc, xv, zv);
       }
     }
     // every tensor store of this warp has completed before the CTA leaves
     if (lane == 0) ac::bulk_wait0();
     __syncwarp();
-    if (!aborted(sm) && p.final_state && c_end == nch) {
+    if (!aborted(sm) && p.final_state && seg == nseg - 1) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) p.final_state[sbase + j * kN] = hs[j];
     }
@@ -617,12 +687,56 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
 
 }  // namespace
 
-cudaError_t ssd_walk_launch(SsdArgs p, unsigned* err, cudaStream_t stream) {
+WalkSplit ssd_walk_split(int64_t batch, int64_t H, int64_t L) {
+  WalkSplit sp{};
+  const int64_t units = batch * H, nch = (L + kQ - 1) / kQ;
+  sp.full_units = units;
+  sp.seg_k = 1;
+  const int force = runtime_knobs().ssd_split;
+  if (force > 0) {
+    sp.full_units = 0;
+    sp.seg_k = (int)(force < nch ? force : (nch > 0 ? nch : 1));
+  } else if (nch >= 2) {
+    // one CTA per SM: the units beyond the last full round of SMs are cut into segments
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms <= 0) {
+      (void)cudaGetLastError();
+      sms = 148;  // no device to ask (sizing only): a B300
+    }
+    const int64_t rem = units % sms;
+    const int64_t k = rem > 0 ? std::min<int64_t>(nch, sms / rem) : 1;
+    if (k > 1) {
+      sp.full_units = units - rem;
+      sp.seg_k = (int)k;
+    }
+  }
+  sp.slots = sp.seg_k > 1 ? (units - sp.full_units) * sp.seg_k : 0;
+  return sp;
+}
+
+// Workspace: 256 bytes of error words | flags [slots] | decays [slots] | states [slots][P][N]
+size_t ssd_walk_workspace_bytes(const WalkSplit& sp) {
+  auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  return 256 + al((size_t)sp.slots * 4) + al((size_t)sp.slots * 4) + (size_t)sp.slots * kP * kN * 4;
+}
+
+cudaError_t ssd_walk_launch(SsdArgs p, void* ws, cudaStream_t stream) {
   p.nchunks = (p.L + kQ - 1) / kQ;
   if (p.timeout_ns <= 0) p.timeout_ns = (long long)kDefaultTimeoutMs * 1000000ll;
   WalkParams w{};
   w.a = p;
-  w.err = err;
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  w.err = reinterpret_cast<unsigned*>(base) + 1;
+  const WalkSplit sp = ssd_walk_split(p.batch, p.H, p.L);
+  w.full_units = sp.full_units;
+  w.seg_k = sp.seg_k;
+  auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  w.seg_flag = reinterpret_cast<unsigned*>(base + 256);
+  w.seg_decay = reinterpret_cast<float*>(base + 256 + al((size_t)sp.slots * 4));
+  w.seg_state = reinterpret_cast<float*>(base + 256 + 2 * al((size_t)sp.slots * 4));
+  cudaError_t e;
+  if (sp.slots > 0 && (e = cudaMemsetAsync(w.seg_flag, 0, (size_t)sp.slots * 4, stream)) != cudaSuccess) return e;
   if (p.L > 0) {
     const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -642,29 +756,10 @@ cudaError_t ssd_walk_launch(SsdArgs p, unsigned* err, cudaStream_t stream) {
                            CU_TENSOR_MAP_L2_PROMOTION_NONE))
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(ssd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)sizeof(WalkSmem));
-  if (e != cudaSuccess) return e;
-  // one CTA per SM: the units beyond the last full round of SMs are cut into segments
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int64_t units = p.batch * p.H;
-  w.full_units = units;
-  w.seg_k = 1;
-  const int force = runtime_knobs().ssd_split;
-  if (force > 0) {
-    w.full_units = 0;
-    w.seg_k = (int)(force < p.nchunks ? force : (p.nchunks > 0 ? p.nchunks : 1));
-  } else if (sms > 0 && p.nchunks >= 2) {
-    const int64_t rem = units % sms;
-    const int64_t k = rem > 0 ? std::min<int64_t>(p.nchunks, sms / rem) : 1;
-    if (k > 1) {
-      w.full_units = units - rem;
-      w.seg_k = (int)k;
-    }
-  }
-  const int64_t grid = w.full_units + (units - w.full_units) * w.seg_k;
+  if ((e = cudaFuncSetAttribute(ssd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sizeof(WalkSmem))) != cudaSuccess)
+    return e;
+  const int64_t grid = sp.full_units + (p.batch * p.H - sp.full_units) * sp.seg_k;
   ssd_walk_kernel<<<(unsigned)grid, kThreads, sizeof(WalkSmem), stream>>>(w);
   return cudaGetLastError();
 }

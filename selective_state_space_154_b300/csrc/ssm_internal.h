@@ -210,7 +210,16 @@ cudaError_t ssd_launch(SsdArgs p, cudaStream_t stream);
 // the sequence-walking form (ssd_walk.cu): one CTA per (batch, head), no workspace
 // beyond the error word
 bool ssd_use_walk(int64_t batch, int64_t L, int64_t H);
-cudaError_t ssd_walk_launch(SsdArgs p, unsigned* err, cudaStream_t stream);
+// How the walking form splits the work: units [0, full_units) whole, the rest in seg_k
+// segments each, handing states over through `slots` workspace slots.
+struct WalkSplit {
+  int64_t full_units;
+  int seg_k;
+  int64_t slots;
+};
+WalkSplit ssd_walk_split(int64_t batch, int64_t H, int64_t L);
+size_t ssd_walk_workspace_bytes(const WalkSplit& sp);
+cudaError_t ssd_walk_launch(SsdArgs p, void* ws, cudaStream_t stream);
 
 // One decode token of the Mamba-2 layer (ssd.cu): state [batch][H][P][N] fp32 in place;
 // x, z, out [batch][H][P], dt [batch][H], B, C [batch][G][N] (bf16); A, D, dt_bias [H].

@@ -323,11 +323,12 @@ def test_host_scan_validates_before_any_copy(lib):
     assert _host_scan(lib, bad, 16, ctypes.c_void_p(FAKE), 1 << 30) == ssm.SSM_ERR_UNSUPPORTED
 
 
-def test_ssd_walking_form_needs_only_the_error_words(lib, hooks):
-    """batch · nheads ≥ 64 selects the form where one CTA walks each (batch, head): its
-    workspace is the 256 bytes of error words; the chunk-parallel form (forced, or below
-    the threshold) needs the chunk states besides."""
-    many = _ssd_dims(batch=2, nheads=40, ngroups=4)
+def test_ssd_walking_form_workspace(lib, hooks):
+    """batch · nheads ≥ 64 selects the form where one CTA walks each (batch, head): with
+    every unit walked whole its workspace is the 256 bytes of error words; units cut into
+    segments add a flag, a decay and a 64 × 128 fp32 state per segment; the chunk-parallel
+    form (forced, or below the threshold) needs the chunk states besides."""
+    many = _ssd_dims(batch=2, nheads=40, ngroups=4)  # 80 units, 3 chunks: each walked whole
     few = _ssd_dims()
     assert lib.ssd_scan_workspace_bytes(ctypes.byref(many)) == 256
     assert lib.ssd_scan_workspace_bytes(ctypes.byref(few)) > 256
@@ -335,4 +336,5 @@ def test_ssd_walking_form_needs_only_the_error_words(lib, hooks):
     hooks.set("SSM_FORCE_KERNEL", "ssd_chunks")
     assert lib.ssd_scan_workspace_bytes(ctypes.byref(many)) > 256
     hooks.set("SSM_FORCE_KERNEL", "ssd_walk")
-    assert lib.ssd_scan_workspace_bytes(ctypes.byref(few)) == 256
+    hooks.set("SSM_SSD_SPLIT", 3)  # 8 units × 3 segments
+    assert lib.ssd_scan_workspace_bytes(ctypes.byref(few)) == 256 + 256 + 256 + 24 * 64 * 128 * 4
