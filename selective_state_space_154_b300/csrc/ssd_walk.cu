@@ -91,14 +91,15 @@ constexpr int kBarCompute = 1, kBarTokens = 2;
 // release flag (s < seg_k − 1); then it combines the published states of segments
 // 0 .. s − 1 in order (decoupled look-back: each is 2^{decay}·(state so far) + its
 // own) into the state entering its chunks, and walks them in full.  The last segment
-// needs no first walk.
+// needs no first walk.  CTAs then take their work by ticket, in the order they start.
 struct WalkParams {
   CUtensorMap tm_c, tm_b, tm_x, tm_out;
   SsdArgs a;
   unsigned* err;
   int64_t full_units;
   int seg_k;
-  unsigned* seg_flag;  // [slot] 1 once the segment's state is published
+  int64_t slots;
+  unsigned* seg_flag;  // [slot] 1 once the segment's state is published; then the ticket counter
   float* seg_decay;    // [slot] Σ Δa over the segment, log2 units
   float* seg_state;    // [slot][P][N] the segment's end state (fp32)
 };
@@ -119,6 +120,7 @@ struct WalkSmem {
   uint64_t bar_ldcb, bar_ldx, bar_a, bar_cb, bar_c, bar_wx, bar_g, bar_h, bar_drain, bar_never;
   uint32_t tslot;
   int abort;
+  long long ticket;
 };
 
 __device__ __forceinline__ const __nv_bfloat16* bf(const void* p) { return static_cast<const __nv_bfloat16*>(p); }
@@ -216,8 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_walk_kernel(const __grid_cons
   WalkSmem& sm = *reinterpret_cast<WalkSmem*>(smem_raw);
   const SsdArgs& p = w.a;
   const int64_t nch = p.nchunks;
+  // With split units, CTAs take their work in the order they start (a ticket), so the
+  // segments a segment waits for have started before it; else by index.
+  if (threadIdx.x == 0)
+    sm.ticket = w.seg_k > 1 ? (long long)atomicAdd(w.seg_flag + w.slots, 1u) : (long long)blockIdx.x;
+  __syncthreads();
   // this CTA's (batch, head) and its chunks [c0, c0 + m); a split unit's segment seg
-  int64_t bh = blockIdx.x, c0 = 0, c1 = nch, slot0 = 0;
+  int64_t bh = sm.ticket, c0 = 0, c1 = nch, slot0 = 0;
   int seg = 0, nseg = 1;
   if (bh >= w.full_units) {
     const int64_t j = bh - w.full_units;
@@ -715,10 +722,12 @@ WalkSplit ssd_walk_split(int64_t batch, int64_t H, int64_t L) {
   return sp;
 }
 
-// Workspace: 256 bytes of error words | flags [slots] | decays [slots] | states [slots][P][N]
+// Workspace: 256 bytes of error words | flags [slots] and the ticket counter | decays
+// [slots] | states [slots][P][N]; only the error words when no unit is split
 size_t ssd_walk_workspace_bytes(const WalkSplit& sp) {
+  if (sp.slots == 0) return 256;
   auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
-  return 256 + al((size_t)sp.slots * 4) + al((size_t)sp.slots * 4) + (size_t)sp.slots * kP * kN * 4;
+  return 256 + al((size_t)(sp.slots + 1) * 4) + al((size_t)sp.slots * 4) + (size_t)sp.slots * kP * kN * 4;
 }
 
 cudaError_t ssd_walk_launch(SsdArgs p, void* ws, cudaStream_t stream) {
@@ -731,12 +740,14 @@ cudaError_t ssd_walk_launch(SsdArgs p, void* ws, cudaStream_t stream) {
   const WalkSplit sp = ssd_walk_split(p.batch, p.H, p.L);
   w.full_units = sp.full_units;
   w.seg_k = sp.seg_k;
+  w.slots = sp.slots;
   auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
   w.seg_flag = reinterpret_cast<unsigned*>(base + 256);
-  w.seg_decay = reinterpret_cast<float*>(base + 256 + al((size_t)sp.slots * 4));
-  w.seg_state = reinterpret_cast<float*>(base + 256 + 2 * al((size_t)sp.slots * 4));
+  w.seg_decay = reinterpret_cast<float*>(base + 256 + al((size_t)(sp.slots + 1) * 4));
+  w.seg_state = reinterpret_cast<float*>(base + 256 + al((size_t)(sp.slots + 1) * 4) + al((size_t)sp.slots * 4));
   cudaError_t e;
-  if (sp.slots > 0 && (e = cudaMemsetAsync(w.seg_flag, 0, (size_t)sp.slots * 4, stream)) != cudaSuccess) return e;
+  if (sp.slots > 0 && (e = cudaMemsetAsync(w.seg_flag, 0, (size_t)(sp.slots + 1) * 4, stream)) != cudaSuccess)
+    return e;
   if (p.L > 0) {
     const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;

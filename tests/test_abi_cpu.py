@@ -337,4 +337,4 @@ def test_ssd_walking_form_workspace(lib, hooks):
     assert lib.ssd_scan_workspace_bytes(ctypes.byref(many)) > 256
     hooks.set("SSM_FORCE_KERNEL", "ssd_walk")
     hooks.set("SSM_SSD_SPLIT", 3)  # 8 units × 3 segments
-    assert lib.ssd_scan_workspace_bytes(ctypes.byref(few)) == 256 + 256 + 256 + 24 * 64 * 128 * 4
+    assert lib.ssd_scan_workspace_bytes(ctypes.byref(few)) == 256 + 256 + 256 + 24 * 64 * 128 * 4  # 25 words fit
