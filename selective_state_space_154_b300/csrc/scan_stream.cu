@@ -307,8 +307,9 @@ __device__ __forceinline__ void fence_store_and_issue(const Ring& g, const uint8
 // The 32 tokens of one stage for one row, in groups of four: steps, updates, readout,
 // gate; outputs (bf16) replace u in the tile; returns the stage's ΣΔ' (P != kAll).
 // MASKED: tokens past t_valid (the sequence's or chunk's end, or a row past d_inner)
-// take Δ' = 0; a stage the whole warp has inside needs no mask.
-template <int RB, bool HAS_Z, int P, bool PRECISE, bool MASKED>
+// take Δ' = 0; a stage the whole warp has inside needs no mask.  OUT = false: the
+// state updates alone (no readout, gate or outputs), for a stage pass two writes.
+template <int RB, bool HAS_Z, int P, bool PRECISE, bool MASKED, bool OUT>
 __device__ __forceinline__ float stage_tokens(const StreamSmem<RB>& sm, int s, const RowConst& c, int r, uint2* tu,
                                               const uint2* td, const uint2* tz, int ts, int t_valid,
                                               float (&h)[NS]) {
@@ -320,7 +321,7 @@ __device__ __forceinline__ float stage_tokens(const StreamSmem<RB>& sm, int s, c
     const int gi = swz(r, q4 >> 1) * 2 + (q4 & 1);  // 8-byte unit of the row
     const uint2 wu = tu[gi], wd = td[gi];
     uint2 wz = make_uint2(0u, 0u);
-    if (HAS_Z) wz = tz[gi];
+    if (HAS_Z && OUT) wz = tz[gi];
     const float* bcs = sm.bcf[s][q4 * 4];
     unsigned packed0 = 0u, packed1 = 0u;
     float Sb = 0.f;
@@ -338,7 +339,7 @@ __device__ __forceinline__ float stage_tokens(const StreamSmem<RB>& sm, int s, c
         d1 = t + v + 1 < t_valid ? d1 : 0.f;
       }
       float2 gz = make_float2(1.f, 1.f);
-      if (HAS_Z) {
+      if (HAS_Z && OUT) {
         const unsigned zw = v ? wz.y : wz.x;
         const float2 zz = make_float2(bf_lo(zw), bf_hi(zw));
         // silu(z) = z/2 + (z/2)·tanh(z/2): one MUFU operation per token
@@ -359,7 +360,7 @@ __device__ __forceinline__ float stage_tokens(const StreamSmem<RB>& sm, int s, c
 #pragma unroll
         for (int qd = 0; qd < NS / 4; ++qd) {
           const float4 bq = bc4[qd];
-          const float4 cq = bc4[NS / 4 + qd];
+          const float4 cq = OUT ? bc4[NS / 4 + qd] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int k2 = 0; k2 < 2; ++k2) {
             const int n = 4 * qd + 2 * k2;
@@ -377,7 +378,7 @@ __device__ __forceinline__ float stage_tokens(const StreamSmem<RB>& sm, int s, c
             }
             h[n] = hn.x;
             h[n + 1] = hn.y;
-            ya = __ffma2_rn(cc, hn, ya);
+            if (OUT) ya = __ffma2_rn(cc, hn, ya);
           }
         }
         ys[j] = fmaf(c.Dc, x, ya.x + ya.y);
@@ -390,7 +391,7 @@ __device__ __forceinline__ float stage_tokens(const StreamSmem<RB>& sm, int s, c
       if (P != kAll) Sb += d0 + d1;
     }
     if (P != kAll) Sst += Sb;
-    tu[gi] = make_uint2(packed0, packed1);
+    if (OUT) tu[gi] = make_uint2(packed0, packed1);
   }
   return Sst;
 }
@@ -423,10 +424,16 @@ __device__ __forceinline__ void consume(StreamSmem<RB>& sm, const Ring& g, const
     const uint2* td = reinterpret_cast<const uint2*>(sm.tile[buf][1] + r * kRowBytes);
     const uint2* tz = reinterpret_cast<const uint2*>(sm.tile[buf][2] + r * kRowBytes);
     float Sst;
-    if (__all_sync(0xffffffffu, ts + TS <= t_valid))
-      Sst = stage_tokens<RB, HAS_Z, P, PRECISE, false>(sm, s, c, r, tu, td, tz, ts, t_valid, h);
+    // in pass one, a stage that starts with the warp's rows unsettled is one pass two
+    // writes again (its stage count only grows): the state updates alone
+    const bool out = published;
+    const bool whole = __all_sync(0xffffffffu, ts + TS <= t_valid);
+    if (P == kSettled && !out)
+      Sst = whole ? stage_tokens<RB, HAS_Z, P, PRECISE, false, false>(sm, s, c, r, tu, td, tz, ts, t_valid, h)
+                  : stage_tokens<RB, HAS_Z, P, PRECISE, true, false>(sm, s, c, r, tu, td, tz, ts, t_valid, h);
     else
-      Sst = stage_tokens<RB, HAS_Z, P, PRECISE, true>(sm, s, c, r, tu, td, tz, ts, t_valid, h);
+      Sst = whole ? stage_tokens<RB, HAS_Z, P, PRECISE, false, true>(sm, s, c, r, tu, td, tz, ts, t_valid, h)
+                  : stage_tokens<RB, HAS_Z, P, PRECISE, true, true>(sm, s, c, r, tu, td, tz, ts, t_valid, h);
     if (P != kAll) {  // S += the stage's sum with Kahan compensation (S feeds 2^{A S} over long chunks)
       const float yk = Sst - comp;
       const float tk = S + yk;
@@ -435,9 +442,9 @@ __device__ __forceinline__ void consume(StreamSmem<RB>& sm, const Ring& g, const
     }
     // the stage's outputs, in place of u, leave by one tensor store of the warp's
     // [32 rows × 32 tokens] (rows past d_inner and tokens past L are clipped).  Pass one
-    // of a chunk after the first stores every token too: pass two later stores its
-    // stages again, computed from the carried-in state.
-    fence_store_and_issue(g, sm.tile[buf][0] + 32 * warp * kRowBytes, ts, warp, lane);
+    // of a chunk after the first stores the stages after its rows settled; pass two
+    // stores the others, computed from the carried-in state.
+    if (out) fence_store_and_issue(g, sm.tile[buf][0] + 32 * warp * kRowBytes, ts, warp, lane);
     if (!published) {
       // pass two must cover this stage unless every row of the warp is settled after it
       const bool settled = !c.row_ok || !(c.a2max * S > kStop - 1.f);
