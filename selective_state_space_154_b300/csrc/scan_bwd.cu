@@ -661,6 +661,555 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
   }
 }
 
+// ---------------------------------------------------------------------------
+// The gradient pass with one thread per row (bf16, d_state 16, L % 8 == 0, 16-byte
+// aligned rows): a thread holds all 16 states of its row, so the readout and the sums
+// over states stay in registers, and the state arithmetic runs on packed f32x2 pairs.
+// A CTA is the same 64-row tile as above (two warps), over one chunk, reading the same
+// checkpoints and chunk summaries.
+//  * Per 8-token block: the block's raw inputs arrive by cp.async into one buffer,
+//    which is refilled with the next block's as soon as they are converted (the
+//    per-token scalars of each row to shared memory); the forward is recomputed from
+//    the block's starting state, each h_{t-1} kept in shared memory ([token][quad][row],
+//    conflict-free); the adjoint then runs over the block in reverse.
+//  * dA uses a·∂h/∂a = Δ·∂h/∂Δ − φ B x (a ≠ 0): per state one sum over the chunk,
+//    Σ [Δ dh Ā (a h_{t-1} + B x) − dh φ x · B x], which times 1/a is the same
+//    Σ dh (Δ Ā h_{t-1} + B x (Δ Ā − φ)/a) as the general form, with 1/a factored out of
+//    the time sum.  The fast path carries −1/a, so that the terms with −φ come out of
+//    fused multiply-adds.  A CTA with an A = 0 state takes the general form per state
+//    (PRECISE).
+//  * dB and dC, sums over the rows: each thread writes its 32 (B | C, n) terms of a
+//    token to a padded [32 rows][36] tile; lane j sums 8 rows × 4 terms from it
+//    (four 128-bit loads give 8 lanes 128 contiguous bytes each), and two exchanges
+//    over lane bits 4 and 3 finish the warp's sum of one term per lane; the two
+//    warps' sums meet in shared memory and leave once per (token, term) per CTA.
+constexpr int kLaneThreads = kBwdRows;  // one thread per row
+constexpr int kXsPitch = 36;            // floats per row of the dB | dC tile
+
+struct LaneRaw {
+  uint4 act[4][kBwdRows];     // u, Δraw, dout, z: a row's 8 tokens (bf16)
+  uint4 bc[2][16];            // B, C: 8 tokens × 16 states (bf16)
+  float4 ck[kBwdRows][4];     // the block's chunk-local starting state, 16 floats per row
+  float scum[kBwdRows];       // ΣΔ from the chunk's start to the block
+};
+struct LaneTok {              // a row's per-token scalars, [token][row]
+  float x[kBwdTok][kBwdRows];    // u
+  float dt[kBwdTok][kBwdRows];   // Δ
+  float sig[kBwdTok][kBwdRows];  // sigmoid(Δraw + bias)
+  float dy[kBwdTok][kBwdRows];   // dout·silu(z)
+  float dzf[kBwdTok][kBwdRows];  // dout·silu'(z)
+};
+struct LaneSmem {
+  float4 hp[kBwdTok][4][kBwdRows];   // h_{t-1} of the block's tokens, [token][quad][row]
+  float4 hin[4][kBwdRows];           // the state entering the chunk
+  float bc[kBwdTok][2][kBwdN];       // B | C of the block's tokens, fp32
+  float xs[2][32][kXsPitch];         // per warp: a token's dB | dC terms, [row][term]
+  float red[2][kBwdTok][32];         // per warp: the warp's sums, [token][term]
+  LaneTok ts;
+  LaneRaw raw;
+};
+
+template <bool CK>
+__device__ __forceinline__ void lane_issue(LaneRaw& rb, const BwdArgs& p, const BwdWs& w, int64_t b, int64_t c0,
+                                           int64_t rt, int64_t blk) {
+  const int64_t t0 = blk * kBwdTok;
+  const int r = threadIdx.x;
+  const int64_t c = c0 + r;
+  const bool row_ok = c < p.d_inner;
+#pragma unroll
+  for (int wt = 0; wt < 4; ++wt) {
+    const void* base = wt == 0 ? p.u : (wt == 1 ? p.delta : (wt == 2 ? p.dout : p.z));
+    const bool ok = row_ok && base != nullptr;
+    const __nv_bfloat16* src =
+        static_cast<const __nv_bfloat16*>(ok ? base : p.u) + (ok ? (b * p.d_inner + c) * p.L + t0 : 0);
+    cp_async16(&rb.act[wt][r], src, ok ? 16 : 0);
+  }
+  if (r < 32) {  // B and C: 256 bytes each
+    const int wt = r / 16, qq = r % 16;
+    cp_async16(&rb.bc[wt][qq], static_cast<const __nv_bfloat16*>(wt ? p.C : p.B) + (b * p.L + t0) * kBwdN + qq * 8,
+               16);
+  }
+  if (CK) {
+    const int64_t slot = rt * p.nblk + blk;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cp_async16(&rb.ck[r][q], w.ck + slot * kBwdThreads + 4 * r + q, 16);
+    if (r < kBwdRows / 4) cp_async16(&rb.scum[r * 4], w.scum + slot * kBwdRows + r * 4, 16);
+  }
+}
+
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+// na: −1/a (fast path) or 1/a (PRECISE); both 0 where a = 0
+template <bool PRECISE>
+__device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const BwdWs& w, const CtaPos& o,
+                                          const float (&a)[kBwdN], const float (&na)[kBwdN], float Dc, float biasc) {
+  const int r = threadIdx.x, warp = r >> 5, lane = r & 31;
+  const bool row_ok = o.row_ok;
+  const int64_t b = o.b, L = p.L;
+  const int64_t c0 = (o.rt % p.ctiles) * kBwdRows;
+
+  // the state entering the chunk (to shared memory) and the adjoint entering it from the right
+  float dh[kBwdN];
+  {
+    float hin[kBwdN];
+#pragma unroll
+    for (int n = 0; n < kBwdN; ++n) hin[n] = dh[n] = 0.f;
+    for (int j = 0; j < o.chunk; ++j) {
+      const int64_t cs = o.rt * p.kmax + j;
+      const float st = w.stot[cs * kBwdRows + r] * kLog2e;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 H = w.hend[cs * kBwdThreads + 4 * r + q];
+        const float hv[4] = {H.x, H.y, H.z, H.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) hin[4 * q + k] = fmaf(ex2_approx(a[4 * q + k] * st), hin[4 * q + k], hv[k]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) sm.hin[q][r] = make_float4(hin[4 * q], hin[4 * q + 1], hin[4 * q + 2], hin[4 * q + 3]);
+  }
+  for (int j = p.nchunks - 1; j > o.chunk; --j) {
+    const int64_t cs = o.rt * p.kmax + j;
+    const float st = w.stot[cs * kBwdRows + r] * kLog2e;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 G = w.gcar[cs * kBwdThreads + 4 * r + q];
+      const float gv[4] = {G.x, G.y, G.z, G.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) dh[4 * q + k] = fmaf(ex2_approx(a[4 * q + k] * st), dh[4 * q + k], gv[k]);
+    }
+  }
+
+  // dA before the factor 1/a (fast path), or dA itself (PRECISE)
+  float dAs[kBwdN];
+#pragma unroll
+  for (int n = 0; n < kBwdN; ++n) dAs[n] = 0.f;
+  float dD_acc = 0.f, db_acc = 0.f;
+
+  if (o.blk0 < o.blk1) {
+    lane_issue<true>(sm.raw, p, w, b, c0, o.rt, o.blk1 - 1);
+    cp_async_commit();
+  }
+  for (int64_t blk = o.blk1 - 1; blk >= o.blk0; --blk) {
+    const int64_t t0 = blk * kBwdTok;
+    cp_async_wait<0>();
+    __syncthreads();  // the raw copy is in; red of the previous block has been read
+    // B and C to fp32 (4 values per thread)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = r * 4 + k;  // [token][B|C][n]
+      const int v = i / (2 * kBwdN), wt = (i / kBwdN) & 1, n = i % kBwdN;
+      sm.bc[v][wt][n] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(&sm.raw.bc[wt][0])[v * kBwdN + n]);
+    }
+    // this row's per-token scalars
+    {
+      const uint4 U = sm.raw.act[0][r], Dr = sm.raw.act[1][r], Go = sm.raw.act[2][r], Z = sm.raw.act[3][r];
+      const __nv_bfloat16* u8 = reinterpret_cast<const __nv_bfloat16*>(&U);
+      const __nv_bfloat16* d8 = reinterpret_cast<const __nv_bfloat16*>(&Dr);
+      const __nv_bfloat16* g8 = reinterpret_cast<const __nv_bfloat16*>(&Go);
+      const __nv_bfloat16* z8 = reinterpret_cast<const __nv_bfloat16*>(&Z);
+#pragma unroll
+      for (int v = 0; v < kBwdTok; ++v) {
+        sm.ts.x[v][r] = __bfloat162float(u8[v]);
+        const float rr = __bfloat162float(d8[v]) + biasc;
+        sm.ts.dt[v][r] = softplus_fast(rr);
+        sm.ts.sig[v][r] = rcp_approx(1.f + ex2_approx(-rr * kLog2e));
+        const float go = __bfloat162float(g8[v]);
+        if (p.z) {
+          const float zv = __bfloat162float(z8[v]);
+          const float sz = rcp_approx(1.f + ex2_approx(-zv * kLog2e));
+          sm.ts.dy[v][r] = go * zv * sz;
+          sm.ts.dzf[v][r] = go * sz * (1.f + zv * (1.f - sz));
+        } else {
+          sm.ts.dy[v][r] = go;
+          sm.ts.dzf[v][r] = 0.f;
+        }
+      }
+    }
+    // the block's starting state: chunk-local + decay since the chunk's start × h_in
+    float h[kBwdN];
+    {
+      const float sc = sm.raw.scum[r] * kLog2e;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 c4 = sm.raw.ck[r][q];
+        const float4 i4 = sm.hin[q][r];
+        const float cv[4] = {c4.x, c4.y, c4.z, c4.w}, iv[4] = {i4.x, i4.y, i4.z, i4.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) h[4 * q + k] = fmaf(ex2_approx(a[4 * q + k] * sc), iv[k], cv[k]);
+      }
+    }
+    __syncthreads();  // bc converted, the raw buffer read: the next block's copy may land
+    if (blk - 1 >= o.blk0) {
+      lane_issue<true>(sm.raw, p, w, b, c0, o.rt, blk - 1);
+      cp_async_commit();
+    }
+
+    // recompute the block's states, keeping each token's h_{t-1}
+#pragma unroll
+    for (int v = 0; v < kBwdTok; ++v) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sm.hp[v][q][r] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+      const float dtv = sm.ts.dt[v][r], x = sm.ts.x[v][r];
+      const float dl = dtv * kLog2e;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 B4 = *reinterpret_cast<const float4*>(&sm.bc[v][0][4 * q]);
+        const float bq[4] = {B4.x, B4.y, B4.z, B4.w};
+        if (PRECISE) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int n = 4 * q + k;
+            const float ab = a[n] != 0.f ? ex2_approx(dl * a[n]) : 1.f;
+            const float phi = a[n] != 0.f ? (ab - 1.f) * na[n] : dtv;
+            h[n] = fmaf(ab, h[n], phi * bq[k] * x);
+          }
+        } else {
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int n = 4 * q + 2 * k2;
+            // h ← (Ā − 1)(h + x B/a) + h
+            const float2 e = __fmul2_rn(f2(dl, dl), f2(a[n], a[n + 1]));
+            const float2 em = __fadd2_rn(f2(ex2_approx(e.x), ex2_approx(e.y)), f2(-1.f, -1.f));
+            const float2 xp = __fmul2_rn(f2(-x, -x), f2(na[n], na[n + 1]));
+            const float2 hb = f2(h[n], h[n + 1]);
+            const float2 hn = __ffma2_rn(em, __ffma2_rn(xp, f2(bq[2 * k2], bq[2 * k2 + 1]), hb), hb);
+            h[n] = hn.x;
+            h[n + 1] = hn.y;
+          }
+        }
+      }
+    }
+
+    // the adjoint over the block, last token first; h = h_t, hp = h_{t-1}
+    float* xsw = &sm.xs[warp][0][0];
+    float* xrow = xsw + lane * kXsPitch;  // this row's 32 terms: dB, then dC
+    const int64_t i0 = o.row * L + t0;
+#pragma unroll 1
+    for (int v = kBwdTok - 1; v >= 0; --v) {
+      float hp[kBwdN];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 t4 = sm.hp[v][q][r];
+        hp[4 * q] = t4.x; hp[4 * q + 1] = t4.y; hp[4 * q + 2] = t4.z; hp[4 * q + 3] = t4.w;
+      }
+      const float x = sm.ts.x[v][r], dtv = sm.ts.dt[v][r], dyv = sm.ts.dy[v][r];
+      const float dl = dtv * kLog2e;
+      float y = 0.f, dx = 0.f, ddt = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 B4 = *reinterpret_cast<const float4*>(&sm.bc[v][0][4 * q]);
+        const float4 C4 = *reinterpret_cast<const float4*>(&sm.bc[v][1][4 * q]);
+        const float bq[4] = {B4.x, B4.y, B4.z, B4.w}, cq[4] = {C4.x, C4.y, C4.z, C4.w};
+        float slot[8];  // the quad's dB terms, then its dC terms
+        if (PRECISE) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int n = 4 * q + k;
+            const float ab = a[n] != 0.f ? ex2_approx(dl * a[n]) : 1.f;
+            const float phi = a[n] != 0.f ? (ab - 1.f) * na[n] : dtv;
+            y = fmaf(cq[k], h[n], y);
+            const float g = fmaf(dyv, cq[k], dh[n]);
+            slot[4 + k] = dyv * h[n];
+            slot[k] = g * phi * x;
+            dx = fmaf(g * phi, bq[k], dx);
+            const float bx = bq[k] * x;
+            if (a[n] != 0.f) {
+              ddt = fmaf(g * ab, fmaf(a[n], hp[n], bx), ddt);
+              dAs[n] = fmaf(g, fmaf(dtv * ab, hp[n], bx * (dtv * ab - phi) * na[n]), dAs[n]);
+            } else {
+              ddt = fmaf(g, bx, ddt);
+              dAs[n] = fmaf(g, fmaf(dtv, hp[n], 0.5f * bx * dtv * dtv), dAs[n]);
+            }
+            dh[n] = g * ab;
+          }
+        } else {
+          // with nphi = −φ: dB term = (g nphi)(−x); dx = −Σ (g nphi) B;
+          // dAs += Δ gd + (g nphi) B x
+          float2 y2 = f2(0.f, 0.f), ndx2 = f2(0.f, 0.f), ddt2 = f2(0.f, 0.f);
+          const float2 xx = f2(x, x), nxx = f2(-x, -x), dt2 = f2(dtv, dtv), dy2 = f2(dyv, dyv);
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int n = 4 * q + 2 * k2;
+            const float2 bb = f2(bq[2 * k2], bq[2 * k2 + 1]), cc = f2(cq[2 * k2], cq[2 * k2 + 1]);
+            const float2 hv2 = f2(h[n], h[n + 1]), hp2 = f2(hp[n], hp[n + 1]);
+            const float2 an = f2(a[n], a[n + 1]);
+            y2 = __ffma2_rn(cc, hv2, y2);
+            const float2 g = __ffma2_rn(dy2, cc, f2(dh[n], dh[n + 1]));
+            const float2 e = __fmul2_rn(f2(dl, dl), an);
+            const float2 ab = f2(ex2_approx(e.x), ex2_approx(e.y));
+            const float2 nphi = __fmul2_rn(__fadd2_rn(ab, f2(-1.f, -1.f)), f2(na[n], na[n + 1]));
+            const float2 gnp = __fmul2_rn(g, nphi);
+            const float2 sb = __fmul2_rn(gnp, nxx);
+            const float2 sc = __fmul2_rn(dy2, hv2);
+            ndx2 = __ffma2_rn(gnp, bb, ndx2);
+            const float2 ga = __fmul2_rn(g, ab);
+            const float2 bx = __fmul2_rn(bb, xx);
+            const float2 gd = __fmul2_rn(ga, __ffma2_rn(an, hp2, bx));
+            ddt2 = __fadd2_rn(ddt2, gd);
+            const float2 da = __ffma2_rn(gnp, bx, __ffma2_rn(dt2, gd, f2(dAs[n], dAs[n + 1])));
+            dAs[n] = da.x; dAs[n + 1] = da.y;
+            dh[n] = ga.x; dh[n + 1] = ga.y;
+            slot[2 * k2] = sb.x; slot[2 * k2 + 1] = sb.y;
+            slot[4 + 2 * k2] = sc.x; slot[4 + 2 * k2 + 1] = sc.y;
+          }
+          y += y2.x + y2.y;
+          dx -= ndx2.x + ndx2.y;
+          ddt += ddt2.x + ddt2.y;
+        }
+        *reinterpret_cast<float4*>(xrow + 4 * q) = make_float4(slot[0], slot[1], slot[2], slot[3]);
+        *reinterpret_cast<float4*>(xrow + kBwdN + 4 * q) = make_float4(slot[4], slot[5], slot[6], slot[7]);
+      }
+      y = fmaf(Dc, x, y);
+      dx = fmaf(dyv, Dc, dx);
+      const float dr = ddt * sm.ts.sig[v][r];
+      if (row_ok) {
+        static_cast<__nv_bfloat16*>(p.du)[i0 + v] = __float2bfloat16_rn(dx);
+        static_cast<__nv_bfloat16*>(p.ddelta)[i0 + v] = __float2bfloat16_rn(dr);
+        if (p.z) static_cast<__nv_bfloat16*>(p.dz)[i0 + v] = __float2bfloat16_rn(sm.ts.dzf[v][r] * y);
+      }
+      dD_acc = fmaf(dyv, x, dD_acc);
+      db_acc += dr;
+      // Σ over the warp's rows of the 32 terms
+      __syncwarp();
+      const int sg = lane & 7, rg = lane >> 3;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 t4 = *reinterpret_cast<const float4*>(xsw + (8 * rg + i) * kXsPitch + 4 * sg);
+        acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
+      }
+      __syncwarp();  // the tile is read before the next token's terms overwrite it
+      // over lane bit 4, then bit 3: lane keeps term 4 sg + 2 b4 + b3
+      const bool up4 = (lane & 16) != 0, up3 = (lane & 8) != 0;
+      const float s0 = up4 ? acc.x : acc.z, s1 = up4 ? acc.y : acc.w;
+      const float k0 = up4 ? acc.z : acc.x, k1 = up4 ? acc.w : acc.y;
+      const float m0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 16);
+      const float m1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 16);
+      const float sfin = (up3 ? m1 : m0) + __shfl_xor_sync(0xffffffffu, up3 ? m0 : m1, 8);
+      sm.red[warp][v][4 * sg + 2 * (up4 ? 1 : 0) + (up3 ? 1 : 0)] = sfin;
+#pragma unroll
+      for (int n = 0; n < kBwdN; ++n) h[n] = hp[n];
+    }
+    __syncthreads();  // both warps' sums are in red
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int idx = r + kLaneThreads * k;  // [token][term]
+      const int v = idx >> 5, term = idx & 31;
+      const float sum = sm.red[0][v][term] + sm.red[1][v][term];
+      const int wt = term >> 4, n = term & 15;
+      if (p.det)
+        p.part_bc[(((o.rt % p.ctiles) * p.batch + b) * L + t0 + v) * 2 * kBwdN + wt * kBwdN + n] = sum;
+      else
+        atomicAdd((wt ? p.dC : p.dB) + (b * L + t0 + v) * kBwdN + n, sum);
+    }
+  }
+  if (!row_ok) return;
+  float dA[kBwdN];
+#pragma unroll
+  for (int n = 0; n < kBwdN; ++n) dA[n] = PRECISE ? dAs[n] : -na[n] * dAs[n];
+  if (p.det) {
+    float* pr = p.part_row + ((b * p.nchunks + o.chunk) * p.d_inner + o.c) * (kBwdN + 2);
+#pragma unroll
+    for (int n = 0; n < kBwdN; ++n) pr[n] = dA[n];
+    pr[kBwdN] = dD_acc;
+    pr[kBwdN + 1] = db_acc;
+  } else {
+#pragma unroll
+    for (int n = 0; n < kBwdN; ++n) atomicAdd(p.dA + o.c * kBwdN + n, dA[n]);
+    if (p.dD) atomicAdd(p.dD + o.c, dD_acc);
+    if (p.dbias) atomicAdd(p.dbias + o.c, db_acc);
+  }
+}
+
+__device__ __forceinline__ CtaPos lane_pos(const BwdArgs& p) {
+  CtaPos o;
+  o.rt = blockIdx.x;
+  o.chunk = (int)blockIdx.y;
+  o.b = o.rt / p.ctiles;
+  const int64_t c0 = (o.rt % p.ctiles) * kBwdRows;
+  o.r = threadIdx.x;
+  o.g = 0;
+  o.row_ok = c0 + o.r < p.d_inner;
+  o.c = c0 + (o.row_ok ? o.r : 0);
+  o.row = o.b * p.d_inner + o.c;
+  o.blk0 = o.chunk * p.cblk;
+  o.blk1 = o.blk0 + p.cblk < p.nblk ? o.blk0 + p.cblk : p.nblk;
+  return o;
+}
+// A of the row (0 for |A| < 2^-60; rows past d_inner take A = -1); true if a state has A = 0
+__device__ __forceinline__ bool lane_a(const BwdArgs& p, const CtaPos& o, float (&a)[kBwdN]) {
+  bool zero = false;
+#pragma unroll
+  for (int n = 0; n < kBwdN; ++n) {
+    const float av = o.row_ok ? p.A[o.c * kBwdN + n] : -1.f;
+    const bool tiny = fabsf(av) < 8.673617e-19f;
+    zero = zero || tiny;
+    a[n] = tiny ? 0.f : av;
+  }
+  return zero;
+}
+
+__global__ void __launch_bounds__(kLaneThreads, 3) scan_bwd_lane_kernel(const BwdArgs p, const BwdWs w) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  LaneSmem& sm = *reinterpret_cast<LaneSmem*>(smem_raw);
+  const CtaPos o = lane_pos(p);
+  float a[kBwdN];
+  const bool zero = lane_a(p, o, a);
+  const float Dc = (o.row_ok && p.D) ? p.D[o.c] : 0.f;
+  const float biasc = (o.row_ok && p.bias) ? p.bias[o.c] : 0.f;
+  float na[kBwdN];
+  if (__syncthreads_or(zero)) {
+#pragma unroll
+    for (int n = 0; n < kBwdN; ++n) na[n] = a[n] != 0.f ? 1.f / a[n] : 0.f;
+    lane_body<true>(sm, p, w, o, a, na, Dc, biasc);
+  } else {
+#pragma unroll
+    for (int n = 0; n < kBwdN; ++n) na[n] = -1.f / a[n];
+    lane_body<false>(sm, p, w, o, a, na, Dc, biasc);
+  }
+}
+
+// Launch 1 in one thread per row: each chunk forward from h = 0, saving the local states
+// every block, the prefix sums of Δ and the chunk's summary (end state, ΣΔ and the adjoint
+// sent left, G = Σ_t (Π_{s≤t} Ā_s) dy_t C_t), in the layout the gradient passes read.  Only
+// the block's raw inputs, its B, C and the rows' per-token scalars live in shared memory
+// (16 KB): eight CTAs per SM.
+struct LaneChunkSmem {
+  float bc[kBwdTok][2][kBwdN];
+  float x[kBwdTok][kBwdRows], dt[kBwdTok][kBwdRows], dy[kBwdTok][kBwdRows];  // per token, per row
+  LaneRaw raw;  // the checkpoint fields stay unused
+};
+
+template <bool PRECISE>
+__device__ __forceinline__ void lane_chunk_body(LaneChunkSmem& sm, const BwdArgs& p, const BwdWs& w,
+                                                const CtaPos& o, const float (&a)[kBwdN], const float (&na)[kBwdN],
+                                                float biasc) {
+  const int r = threadIdx.x;
+  const int64_t c0 = (o.rt % p.ctiles) * kBwdRows;
+  const bool want_g = o.chunk > 0;  // chunk 0 sends no adjoint further left
+  float h[kBwdN], P[kBwdN], G[kBwdN];
+#pragma unroll
+  for (int n = 0; n < kBwdN; ++n) {
+    h[n] = 0.f;
+    P[n] = 1.f;
+    G[n] = 0.f;
+  }
+  float S = 0.f;
+  if (o.blk0 < o.blk1) {
+    lane_issue<false>(sm.raw, p, w, o.b, c0, o.rt, o.blk0);
+    cp_async_commit();
+  }
+  for (int64_t blk = o.blk0; blk < o.blk1; ++blk) {
+    const int64_t slot = o.rt * p.nblk + blk;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w.ck[slot * kBwdThreads + 4 * r + q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+    w.scum[slot * kBwdRows + r] = S;
+    cp_async_wait<0>();
+    __syncthreads();  // the raw copy is in; the previous block's B, C are no longer read
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = r * 4 + k;  // [token][B|C][n]
+      const int v = i / (2 * kBwdN), wt = (i / kBwdN) & 1, n = i % kBwdN;
+      sm.bc[v][wt][n] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(&sm.raw.bc[wt][0])[v * kBwdN + n]);
+    }
+    {
+      const uint4 U = sm.raw.act[0][r], Dr = sm.raw.act[1][r], Go = sm.raw.act[2][r], Z = sm.raw.act[3][r];
+      const __nv_bfloat16* u8 = reinterpret_cast<const __nv_bfloat16*>(&U);
+      const __nv_bfloat16* d8 = reinterpret_cast<const __nv_bfloat16*>(&Dr);
+      const __nv_bfloat16* g8 = reinterpret_cast<const __nv_bfloat16*>(&Go);
+      const __nv_bfloat16* z8 = reinterpret_cast<const __nv_bfloat16*>(&Z);
+#pragma unroll
+      for (int v = 0; v < kBwdTok; ++v) {
+        sm.x[v][r] = __bfloat162float(u8[v]);
+        sm.dt[v][r] = softplus_fast(__bfloat162float(d8[v]) + biasc);
+        const float go = __bfloat162float(g8[v]);
+        if (p.z) {
+          const float zv = __bfloat162float(z8[v]);
+          sm.dy[v][r] = go * zv * rcp_approx(1.f + ex2_approx(-zv * kLog2e));
+        } else {
+          sm.dy[v][r] = go;
+        }
+      }
+    }
+    __syncthreads();  // B, C converted and the raw buffer read: the next block's copy may land
+    if (blk + 1 < o.blk1) {
+      lane_issue<false>(sm.raw, p, w, o.b, c0, o.rt, blk + 1);
+      cp_async_commit();
+    }
+#pragma unroll 1
+    for (int v = 0; v < kBwdTok; ++v) {
+      const float xv = sm.x[v][r], dtv = sm.dt[v][r], dyv = sm.dy[v][r], dl = dtv * kLog2e;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 B4 = *reinterpret_cast<const float4*>(&sm.bc[v][0][4 * q]);
+        const float4 C4 = *reinterpret_cast<const float4*>(&sm.bc[v][1][4 * q]);
+        const float bq[4] = {B4.x, B4.y, B4.z, B4.w}, cq[4] = {C4.x, C4.y, C4.z, C4.w};
+        if (PRECISE) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int n = 4 * q + k;
+            const float ab = a[n] != 0.f ? ex2_approx(dl * a[n]) : 1.f;
+            const float phi = a[n] != 0.f ? (ab - 1.f) * na[n] : dtv;
+            h[n] = fmaf(ab, h[n], phi * bq[k] * xv);
+            if (want_g) {
+              P[n] *= ab;
+              G[n] = fmaf(P[n], dyv * cq[k], G[n]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int n = 4 * q + 2 * k2;
+            const float2 e = __fmul2_rn(f2(dl, dl), f2(a[n], a[n + 1]));
+            const float2 em = __fadd2_rn(f2(ex2_approx(e.x), ex2_approx(e.y)), f2(-1.f, -1.f));
+            const float2 xp = __fmul2_rn(f2(-xv, -xv), f2(na[n], na[n + 1]));
+            const float2 hb = f2(h[n], h[n + 1]);
+            const float2 hn = __ffma2_rn(em, __ffma2_rn(xp, f2(bq[2 * k2], bq[2 * k2 + 1]), hb), hb);
+            h[n] = hn.x;
+            h[n + 1] = hn.y;
+            if (want_g) {  // P ← P Ā = P + P (Ā − 1); G += P dy C
+              const float2 pb = f2(P[n], P[n + 1]);
+              const float2 pp = __ffma2_rn(pb, em, pb);
+              const float2 gg = __ffma2_rn(pp, __fmul2_rn(f2(dyv, dyv), f2(cq[2 * k2], cq[2 * k2 + 1])),
+                                           f2(G[n], G[n + 1]));
+              P[n] = pp.x; P[n + 1] = pp.y;
+              G[n] = gg.x; G[n + 1] = gg.y;
+            }
+          }
+        }
+      }
+      S += dtv;
+    }
+  }
+  const int64_t cs = o.rt * p.kmax + o.chunk;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    w.hend[cs * kBwdThreads + 4 * r + q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+    w.gcar[cs * kBwdThreads + 4 * r + q] = make_float4(G[4 * q], G[4 * q + 1], G[4 * q + 2], G[4 * q + 3]);
+  }
+  w.stot[cs * kBwdRows + r] = S;
+}
+
+__global__ void __launch_bounds__(kLaneThreads, 8) scan_bwd_lane_chunk_kernel(const BwdArgs p, const BwdWs w) {
+  __shared__ __align__(16) LaneChunkSmem sm;
+  const CtaPos o = lane_pos(p);
+  float a[kBwdN];
+  const bool zero = lane_a(p, o, a);
+  const float biasc = (o.row_ok && p.bias) ? p.bias[o.c] : 0.f;
+  float na[kBwdN];
+  if (__syncthreads_or(zero)) {
+#pragma unroll
+    for (int n = 0; n < kBwdN; ++n) na[n] = a[n] != 0.f ? 1.f / a[n] : 0.f;
+    lane_chunk_body<true>(sm, p, w, o, a, na, biasc);
+  } else {
+#pragma unroll
+    for (int n = 0; n < kBwdN; ++n) na[n] = -1.f / a[n];
+    lane_chunk_body<false>(sm, p, w, o, a, na, biasc);
+  }
+}
+
 // Launch 3 (deterministic mode): the sums over channel tiles (dB, dC) and over batch and
 // chunks (dA, dD, dbias) of the partials, each in ascending index order, so that the result
 // does not depend on which CTA ran first.
@@ -726,10 +1275,14 @@ int pick_bwd_chunks(int64_t R, int64_t nblk, int64_t slots, int64_t kmax) {
   return best;
 }
 
+// lane: the gradient pass with one thread per row (bf16 with the raw-copy prefetch only)
 template <typename T, bool PF>
-cudaError_t bwd_launch_t(BwdArgs p, cudaStream_t s) {
-  const size_t smem = sizeof(BwdSmem) + (PF ? 2 * sizeof(RawBlock) : 0);
-  cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<T, PF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+cudaError_t bwd_launch_t(BwdArgs p, cudaStream_t s, bool lane) {
+  const void* grad = lane ? reinterpret_cast<const void*>(scan_bwd_lane_kernel)
+                          : reinterpret_cast<const void*>(scan_bwd_kernel<T, PF>);
+  const size_t smem = lane ? sizeof(LaneSmem) : sizeof(BwdSmem) + (PF ? 2 * sizeof(RawBlock) : 0);
+  const int threads = lane ? kLaneThreads : kBwdThreads;
+  cudaError_t e = cudaFuncSetAttribute(grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t R = p.batch * p.ctiles;
   if (R == 0) return cudaSuccess;
@@ -738,9 +1291,7 @@ cudaError_t bwd_launch_t(BwdArgs p, cudaStream_t s) {
     int dev = 0, sms = 0, occ = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, scan_bwd_kernel<T, PF>, kBwdThreads, smem)) !=
-        cudaSuccess)
-      return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, grad, threads, smem)) != cudaSuccess) return e;
     k = pick_bwd_chunks(R, p.nblk, (int64_t)(sms > 0 ? sms : 1) * (occ > 0 ? occ : 1), p.kmax);
   }
   if (k > p.kmax) k = p.kmax;
@@ -750,9 +1301,15 @@ cudaError_t bwd_launch_t(BwdArgs p, cudaStream_t s) {
   p.nchunks = p.cblk > 0 ? (int)((p.nblk + p.cblk - 1) / p.cblk) : 1;
   const BwdWs w = ws_layout(p.ckpt, R, p.nblk, p.kmax);
   const dim3 grid((unsigned)R, (unsigned)p.nchunks);
-  scan_bwd_chunk_kernel<T, PF><<<grid, kBwdThreads, 0, s>>>(p, w);
+  if (lane)
+    scan_bwd_lane_chunk_kernel<<<grid, kLaneThreads, 0, s>>>(p, w);
+  else
+    scan_bwd_chunk_kernel<T, PF><<<grid, kBwdThreads, 0, s>>>(p, w);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  scan_bwd_kernel<T, PF><<<grid, kBwdThreads, smem, s>>>(p, w);
+  if (lane)
+    scan_bwd_lane_kernel<<<grid, kLaneThreads, smem, s>>>(p, w);
+  else
+    scan_bwd_kernel<T, PF><<<grid, kBwdThreads, smem, s>>>(p, w);
   if ((e = cudaGetLastError()) != cudaSuccess || !p.det) return e;
   const int64_t items = p.batch * p.L * 2 * p.N + p.d_inner * (p.N + 2);
   const int64_t blocks = (items + 255) / 256;
@@ -766,6 +1323,12 @@ bool bwd_prefetch_ok(const BwdArgs& p) {
   auto a16 = [](const void* q) { return q == nullptr || (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
   return p.act == 1 && p.N == kBwdN && p.L % kBwdTok == 0 && a16(p.u) && a16(p.delta) && a16(p.dout) &&
          a16(p.z) && a16(p.B) && a16(p.C);
+}
+// The one-thread-per-row gradient pass also stores whole 16-byte row pieces of du, the Δraw
+// gradient and dz.
+bool bwd_lane_ok(const BwdArgs& p) {
+  auto a16 = [](const void* q) { return q == nullptr || (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  return bwd_prefetch_ok(p) && a16(p.du) && a16(p.ddelta) && a16(p.dz);
 }
 
 }  // namespace
@@ -807,9 +1370,9 @@ cudaError_t scan_bwd_launch(BwdArgs p, cudaStream_t stream) {
     p.part_bc = reinterpret_cast<float*>(base + z.base);
     p.part_row = reinterpret_cast<float*>(base + z.base + z.part_bc);
   }
-  if (p.act != 1) return bwd_launch_t<float, false>(p, stream);
-  return bwd_prefetch_ok(p) ? bwd_launch_t<__nv_bfloat16, true>(p, stream)
-                            : bwd_launch_t<__nv_bfloat16, false>(p, stream);
+  if (p.act != 1) return bwd_launch_t<float, false>(p, stream, false);
+  if (!bwd_prefetch_ok(p)) return bwd_launch_t<__nv_bfloat16, false>(p, stream, false);
+  return bwd_launch_t<__nv_bfloat16, true>(p, stream, p.form != 1 && bwd_lane_ok(p));
 }
 
 }  // namespace ssm

@@ -45,6 +45,7 @@ RuntimeKnobs* load_knobs() {
   if (const char* c = std::getenv("SSM_CTAS_PER_SM")) r->ctas_per_sm = std::atoi(c);
   if (const char* c = std::getenv("SSM_FORCE_TPR")) r->force_tpr = std::atoi(c);
   if (const char* c = std::getenv("SSM_BWD_CHUNKS")) r->bwd_chunks = std::atoi(c);
+  if (const char* c = std::getenv("SSM_BWD_FORM")) r->bwd_form = std::strcmp(c, "quad") == 0 ? 1 : 0;
   if (const char* c = std::getenv("SSM_STREAM_ROWS")) {
     const int v = std::atoi(c);
     r->stream_rows = (v == 512 || v == 128) ? v : 0;
@@ -350,6 +351,7 @@ ssm_status scan_bwd_impl(const void* u, const void* delta, const float* A, const
   a.batch = b; a.d_inner = d; a.N = N; a.L = L; a.act = dims->act;
   a.det = det ? 1 : 0;
   a.force_chunks = ssm::runtime_knobs().bwd_chunks;
+  a.form = ssm::runtime_knobs().bwd_form;
   return cuda_status(ssm::scan_bwd_launch(a, st));
 }
 

@@ -75,6 +75,7 @@ struct RuntimeKnobs {
   bool fault_step;                // test hook: the pipelined step's first wait never completes
   bool force_step_plain;          // SSM_FORCE_STEP=plain: the generic step kernel only
   int bwd_chunks;                 // >0: sequence chunks of the backward (tests)
+  int bwd_form;                   // 1: the backward's four-threads-per-row gradient pass (tests)
   bool fault_ssd;                 // test hook: the SSD output kernel's first wait never completes
   int stream_rows;                // >0: rows per CTA of the streamed row kernel (512, 256 or 128)
   int stream_ctas;                // >0: work items (CTAs) of the streamed row kernel
@@ -174,6 +175,7 @@ struct BwdArgs {
   float* part_row;  // [batch][chunk][d_inner][dA 0..N-1 | dD | dbias]
   int64_t batch, d_inner, N, L, nblk, cblk;
   int ctiles, act, nchunks, kmax, force_chunks, det;
+  int form;  // gradient pass: 0 by shape, 1 four threads per row (test hook)
 };
 // deterministic = false: the checkpoints and chunk summaries; true: those plus the partial sums
 size_t scan_bwd_workspace_bytes(int64_t batch, int64_t d_inner, int64_t N, int64_t L, bool deterministic);

@@ -157,13 +157,17 @@ def test_bwd_deterministic_fp32_no_optional():
         assert e <= TOL[torch.float32], f"{k}: rel err {e:.3e}"
 
 
+@pytest.mark.parametrize("form", ["lane", "quad"])
 @pytest.mark.parametrize("chunks", [1, 3, 7])
 @pytest.mark.parametrize("gate", [True, False], ids=["z", "no_z"])
-def test_bwd_prefetched_blocks(hooks, chunks, gate):
+def test_bwd_prefetched_blocks(hooks, chunks, gate, form):
     """bf16 with d_state 16 and L a multiple of 8: both kernels copy the next block's raw
     inputs (and the gradient kernel its checkpoint) by cp.async while the current block
-    computes; across chunk counts, with and without the gate, in both modes."""
+    computes; across chunk counts, with and without the gate, in both modes, with the
+    gradient pass at one thread per row (the default here) and at four."""
     hooks.set("SSM_BWD_CHUNKS", str(chunks))
+    if form == "quad":
+        hooks.set("SSM_BWD_FORM", "quad")
     inp = W.random_scan_inputs(2, 150, 16, 512, dtype=torch.bfloat16, device=DEV, seed=40 + chunks, a_kind="random",
                                gate=gate)
     dout = _dout(inp, 41)
@@ -177,3 +181,33 @@ def test_bwd_prefetched_blocks(hooks, chunks, gate):
             continue
         e = rel_err(to_np(g[k]), r[k])
         assert e <= TOL[torch.bfloat16], f"{k}: rel err {e:.3e}"
+
+
+@pytest.mark.parametrize("chunks", [1, 4])
+def test_bwd_lane_zero_A_and_padding_rows(hooks, chunks):
+    """The one-thread-per-row gradient pass with A = 0 states in some rows (the tile that
+    holds them takes the general per-state form, the others the fused one) and a last tile
+    of 36 rows past d_inner (100 channels in 64-row tiles)."""
+    hooks.set("SSM_BWD_CHUNKS", str(chunks))
+    inp = W.random_scan_inputs(2, 100, 16, 96, dtype=torch.bfloat16, device=DEV, seed=50 + chunks,
+                               a_kind="random")
+    inp["A"][70::5, 3] = 0.0
+    inp["A"][80, :] = 0.0
+    _compare(inp, _dout(inp, 51), TOL[torch.bfloat16])
+
+
+def test_bwd_lane_and_quad_forms_agree(hooks):
+    """The two gradient passes give the same gradients to rounding on the same inputs
+    (the 130M-shaped layer's rows over a shorter sequence, five chunks)."""
+    hooks.set("SSM_BWD_CHUNKS", "5")
+    inp = W.random_scan_inputs(2, 192, 16, 800, dtype=torch.bfloat16, device=DEV, seed=61)
+    dout = _dout(inp, 62)
+    gl = _run(inp, dout)
+    hooks.set("SSM_BWD_FORM", "quad")
+    gq = _run(inp, dout)
+    r = _ref(inp, dout)
+    for k in GRADS:
+        if gl[k] is None:
+            continue
+        el, eq = rel_err(to_np(gl[k]), r[k]), rel_err(to_np(gq[k]), r[k])
+        assert el <= TOL[torch.bfloat16] and eq <= TOL[torch.bfloat16], f"{k}: {el:.3e} / {eq:.3e}"
