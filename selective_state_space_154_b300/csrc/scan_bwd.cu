@@ -679,12 +679,11 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
 //    fused multiply-adds.  A CTA with an A = 0 state takes the general form per state
 //    (PRECISE).
 //  * dB and dC, sums over the rows: each thread writes its 32 (B | C, n) terms of a
-//    token to a padded [32 rows][36] tile; lane j sums 8 rows × 4 terms from it
-//    (four 128-bit loads give 8 lanes 128 contiguous bytes each), and two exchanges
+//    token to a [32 rows][32] tile (16-byte groups XOR-swizzled by row); lane j sums
+//    8 rows × 4 terms from it (every 8 lanes of a 128-bit access hit distinct banks), and two exchanges
 //    over lane bits 4 and 3 finish the warp's sum of one term per lane; the two
 //    warps' sums meet in shared memory and leave once per (token, term) per CTA.
 constexpr int kLaneThreads = kBwdRows;  // one thread per row
-constexpr int kXsPitch = 36;            // floats per row of the dB | dC tile
 
 struct LaneRaw {
   uint4 act[4][kBwdRows];     // u, Δraw, dout, z: a row's 8 tokens (bf16)
@@ -699,15 +698,25 @@ struct LaneTok {              // a row's per-token scalars, [token][row]
   float dy[kBwdTok][kBwdRows];   // dout·silu(z)
   float dzf[kBwdTok][kBwdRows];  // dout·silu'(z)
 };
+// 56 KB: four CTAs fill an SM's 228 KB with their reserved kilobyte each.
 struct LaneSmem {
-  float4 hp[kBwdTok][4][kBwdRows];   // h_{t-1} of the block's tokens, [token][quad][row]
-  float4 hin[4][kBwdRows];           // the state entering the chunk
+  // h_{t-1} of tokens 1..7, [token - 1][quad][row] (token 0's stays in registers); once a
+  // token's adjoint has read its slot, the slot's first quad holds each warp's sums of the
+  // token's 32 terms
+  float4 hp[kBwdTok - 1][4][kBwdRows];
   float bc[kBwdTok][2][kBwdN];       // B | C of the block's tokens, fp32
-  float xs[2][32][kXsPitch];         // per warp: a token's dB | dC terms, [row][term]
-  float red[2][kBwdTok][32];         // per warp: the warp's sums, [token][term]
+  float xs[2][32][32];               // per warp: a token's dB | dC terms, [row][term], the
+                                     // 16-byte groups of row j at group g ^ (j & 7)
+  float red0[2][32];                 // per warp: token 0's sums
   LaneTok ts;
   LaneRaw raw;
 };
+static_assert(sizeof(LaneSmem) <= 56 * 1024, "four CTAs per SM");
+
+// where warp w's sums of token v's 32 terms go
+__device__ __forceinline__ float* lane_red(LaneSmem& sm, int v, int w) {
+  return v > 0 ? reinterpret_cast<float*>(&sm.hp[v - 1][0][32 * w]) : &sm.red0[w][0];
+}
 
 template <bool CK>
 __device__ __forceinline__ void lane_issue(LaneRaw& rb, const BwdArgs& p, const BwdWs& w, int64_t b, int64_t c0,
@@ -748,10 +757,9 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
   const int64_t b = o.b, L = p.L;
   const int64_t c0 = (o.rt % p.ctiles) * kBwdRows;
 
-  // the state entering the chunk (to shared memory) and the adjoint entering it from the right
-  float dh[kBwdN];
+  // the state entering the chunk and the adjoint entering it from the right
+  float hin[kBwdN], dh[kBwdN];
   {
-    float hin[kBwdN];
 #pragma unroll
     for (int n = 0; n < kBwdN; ++n) hin[n] = dh[n] = 0.f;
     for (int j = 0; j < o.chunk; ++j) {
@@ -765,8 +773,6 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
         for (int k = 0; k < 4; ++k) hin[4 * q + k] = fmaf(ex2_approx(a[4 * q + k] * st), hin[4 * q + k], hv[k]);
       }
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) sm.hin[q][r] = make_float4(hin[4 * q], hin[4 * q + 1], hin[4 * q + 2], hin[4 * q + 3]);
   }
   for (int j = p.nchunks - 1; j > o.chunk; --j) {
     const int64_t cs = o.rt * p.kmax + j;
@@ -827,16 +833,15 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
       }
     }
     // the block's starting state: chunk-local + decay since the chunk's start × h_in
-    float h[kBwdN];
+    float h[kBwdN], h0[kBwdN];
     {
       const float sc = sm.raw.scum[r] * kLog2e;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float4 c4 = sm.raw.ck[r][q];
-        const float4 i4 = sm.hin[q][r];
-        const float cv[4] = {c4.x, c4.y, c4.z, c4.w}, iv[4] = {i4.x, i4.y, i4.z, i4.w};
+        const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) h[4 * q + k] = fmaf(ex2_approx(a[4 * q + k] * sc), iv[k], cv[k]);
+        for (int k = 0; k < 4; ++k) h0[4 * q + k] = h[4 * q + k] = fmaf(ex2_approx(a[4 * q + k] * sc), hin[4 * q + k], cv[k]);
       }
     }
     __syncthreads();  // bc converted, the raw buffer read: the next block's copy may land
@@ -848,8 +853,11 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
     // recompute the block's states, keeping each token's h_{t-1}
 #pragma unroll
     for (int v = 0; v < kBwdTok; ++v) {
+      if (v > 0) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sm.hp[v][q][r] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+        for (int q = 0; q < 4; ++q)
+          sm.hp[v - 1][q][r] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+      }
       const float dtv = sm.ts.dt[v][r], x = sm.ts.x[v][r];
       const float dl = dtv * kLog2e;
 #pragma unroll
@@ -883,15 +891,21 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
 
     // the adjoint over the block, last token first; h = h_t, hp = h_{t-1}
     float* xsw = &sm.xs[warp][0][0];
-    float* xrow = xsw + lane * kXsPitch;  // this row's 32 terms: dB, then dC
+    float* xrow = xsw + lane * 32;  // this row's 32 terms: dB, then dC (groups swizzled)
+    const int sw = lane & 7;
     const int64_t i0 = o.row * L + t0;
 #pragma unroll 1
     for (int v = kBwdTok - 1; v >= 0; --v) {
       float hp[kBwdN];
+      if (v > 0) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 t4 = sm.hp[v][q][r];
-        hp[4 * q] = t4.x; hp[4 * q + 1] = t4.y; hp[4 * q + 2] = t4.z; hp[4 * q + 3] = t4.w;
+        for (int q = 0; q < 4; ++q) {
+          const float4 t4 = sm.hp[v - 1][q][r];
+          hp[4 * q] = t4.x; hp[4 * q + 1] = t4.y; hp[4 * q + 2] = t4.z; hp[4 * q + 3] = t4.w;
+        }
+      } else {
+#pragma unroll
+        for (int n = 0; n < kBwdN; ++n) hp[n] = h0[n];
       }
       const float x = sm.ts.x[v][r], dtv = sm.ts.dt[v][r], dyv = sm.ts.dy[v][r];
       const float dl = dtv * kLog2e;
@@ -957,8 +971,8 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
           dx -= ndx2.x + ndx2.y;
           ddt += ddt2.x + ddt2.y;
         }
-        *reinterpret_cast<float4*>(xrow + 4 * q) = make_float4(slot[0], slot[1], slot[2], slot[3]);
-        *reinterpret_cast<float4*>(xrow + kBwdN + 4 * q) = make_float4(slot[4], slot[5], slot[6], slot[7]);
+        *reinterpret_cast<float4*>(xrow + 4 * (q ^ sw)) = make_float4(slot[0], slot[1], slot[2], slot[3]);
+        *reinterpret_cast<float4*>(xrow + 4 * ((4 + q) ^ sw)) = make_float4(slot[4], slot[5], slot[6], slot[7]);
       }
       y = fmaf(Dc, x, y);
       dx = fmaf(dyv, Dc, dx);
@@ -976,7 +990,7 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float4 t4 = *reinterpret_cast<const float4*>(xsw + (8 * rg + i) * kXsPitch + 4 * sg);
+        const float4 t4 = *reinterpret_cast<const float4*>(xsw + (8 * rg + i) * 32 + 4 * (sg ^ i));
         acc.x += t4.x; acc.y += t4.y; acc.z += t4.z; acc.w += t4.w;
       }
       __syncwarp();  // the tile is read before the next token's terms overwrite it
@@ -987,7 +1001,7 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
       const float m0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 16);
       const float m1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 16);
       const float sfin = (up3 ? m1 : m0) + __shfl_xor_sync(0xffffffffu, up3 ? m0 : m1, 8);
-      sm.red[warp][v][4 * sg + 2 * (up4 ? 1 : 0) + (up3 ? 1 : 0)] = sfin;
+      lane_red(sm, v, warp)[4 * sg + 2 * (up4 ? 1 : 0) + (up3 ? 1 : 0)] = sfin;
 #pragma unroll
       for (int n = 0; n < kBwdN; ++n) h[n] = hp[n];
     }
@@ -996,7 +1010,7 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
     for (int k = 0; k < 4; ++k) {
       const int idx = r + kLaneThreads * k;  // [token][term]
       const int v = idx >> 5, term = idx & 31;
-      const float sum = sm.red[0][v][term] + sm.red[1][v][term];
+      const float sum = lane_red(sm, v, 0)[term] + lane_red(sm, v, 1)[term];
       const int wt = term >> 4, n = term & 15;
       if (p.det)
         p.part_bc[(((o.rt % p.ctiles) * p.batch + b) * L + t0 + v) * 2 * kBwdN + wt * kBwdN + n] = sum;
@@ -1050,7 +1064,7 @@ __device__ __forceinline__ bool lane_a(const BwdArgs& p, const CtaPos& o, float 
   return zero;
 }
 
-__global__ void __launch_bounds__(kLaneThreads, 3) scan_bwd_lane_kernel(const BwdArgs p, const BwdWs w) {
+__global__ void __launch_bounds__(kLaneThreads, 4) scan_bwd_lane_kernel(const BwdArgs p, const BwdWs w) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   LaneSmem& sm = *reinterpret_cast<LaneSmem*>(smem_raw);
   const CtaPos o = lane_pos(p);
