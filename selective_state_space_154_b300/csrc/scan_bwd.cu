@@ -718,7 +718,6 @@ __device__ __forceinline__ float* lane_red(LaneSmem& sm, int v, int w) {
   return v > 0 ? reinterpret_cast<float*>(&sm.hp[v - 1][0][32 * w]) : &sm.red0[w][0];
 }
 
-template <bool CK>
 __device__ __forceinline__ void lane_issue(LaneRaw& rb, const BwdArgs& p, const BwdWs& w, int64_t b, int64_t c0,
                                            int64_t rt, int64_t blk) {
   const int64_t t0 = blk * kBwdTok;
@@ -738,12 +737,10 @@ __device__ __forceinline__ void lane_issue(LaneRaw& rb, const BwdArgs& p, const 
     cp_async16(&rb.bc[wt][qq], static_cast<const __nv_bfloat16*>(wt ? p.C : p.B) + (b * p.L + t0) * kBwdN + qq * 8,
                16);
   }
-  if (CK) {
-    const int64_t slot = rt * p.nblk + blk;
+  const int64_t slot = rt * p.nblk + blk;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) cp_async16(&rb.ck[r][q], w.ck + slot * kBwdThreads + 4 * r + q, 16);
-    if (r < kBwdRows / 4) cp_async16(&rb.scum[r * 4], w.scum + slot * kBwdRows + r * 4, 16);
-  }
+  for (int q = 0; q < 4; ++q) cp_async16(&rb.ck[r][q], w.ck + slot * kBwdThreads + 4 * r + q, 16);
+  if (r < kBwdRows / 4) cp_async16(&rb.scum[r * 4], w.scum + slot * kBwdRows + r * 4, 16);
 }
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
@@ -793,7 +790,7 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
   float dD_acc = 0.f, db_acc = 0.f;
 
   if (o.blk0 < o.blk1) {
-    lane_issue<true>(sm.raw, p, w, b, c0, o.rt, o.blk1 - 1);
+    lane_issue(sm.raw, p, w, b, c0, o.rt, o.blk1 - 1);
     cp_async_commit();
   }
   for (int64_t blk = o.blk1 - 1; blk >= o.blk0; --blk) {
@@ -846,7 +843,7 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
     }
     __syncthreads();  // bc converted, the raw buffer read: the next block's copy may land
     if (blk - 1 >= o.blk0) {
-      lane_issue<true>(sm.raw, p, w, b, c0, o.rt, blk - 1);
+      lane_issue(sm.raw, p, w, b, c0, o.rt, blk - 1);
       cp_async_commit();
     }
 
@@ -1036,13 +1033,14 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
   }
 }
 
-__device__ __forceinline__ CtaPos lane_pos(const BwdArgs& p) {
+// split: CTAs per 64-row tile (thread t of CTA x serves row (x % split) · 64/split + t)
+__device__ __forceinline__ CtaPos lane_pos(const BwdArgs& p, int split) {
   CtaPos o;
-  o.rt = blockIdx.x;
+  o.rt = blockIdx.x / split;
   o.chunk = (int)blockIdx.y;
   o.b = o.rt / p.ctiles;
   const int64_t c0 = (o.rt % p.ctiles) * kBwdRows;
-  o.r = threadIdx.x;
+  o.r = threadIdx.x + (int)(blockIdx.x % split) * (kBwdRows / split);
   o.g = 0;
   o.row_ok = c0 + o.r < p.d_inner;
   o.c = c0 + (o.row_ok ? o.r : 0);
@@ -1067,7 +1065,7 @@ __device__ __forceinline__ bool lane_a(const BwdArgs& p, const CtaPos& o, float 
 __global__ void __launch_bounds__(kLaneThreads, 4) scan_bwd_lane_kernel(const BwdArgs p, const BwdWs w) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   LaneSmem& sm = *reinterpret_cast<LaneSmem*>(smem_raw);
-  const CtaPos o = lane_pos(p);
+  const CtaPos o = lane_pos(p, 1);
   float a[kBwdN];
   const bool zero = lane_a(p, o, a);
   const float Dc = (o.row_ok && p.D) ? p.D[o.c] : 0.f;
@@ -1086,21 +1084,42 @@ __global__ void __launch_bounds__(kLaneThreads, 4) scan_bwd_lane_kernel(const Bw
 
 // Launch 1 in one thread per row: each chunk forward from h = 0, saving the local states
 // every block, the prefix sums of Δ and the chunk's summary (end state, ΣΔ and the adjoint
-// sent left, G = Σ_t (Π_{s≤t} Ā_s) dy_t C_t), in the layout the gradient passes read.  Only
-// the block's raw inputs, its B, C and the rows' per-token scalars live in shared memory
-// (16 KB): eight CTAs per SM.
+// sent left, G = Σ_t (Π_{s≤t} Ā_s) dy_t C_t), in the layout the gradient passes read.  A CTA
+// is one warp over half a tile (the grid has twice the CTAs of the gradient pass, so that
+// short grids still fill the SMs); only the block's raw inputs, its B, C and the rows'
+// per-token scalars live in shared memory (6.5 KB).
+constexpr int kLaneChunkRows = 32;
 struct LaneChunkSmem {
   float bc[kBwdTok][2][kBwdN];
-  float x[kBwdTok][kBwdRows], dt[kBwdTok][kBwdRows], dy[kBwdTok][kBwdRows];  // per token, per row
-  LaneRaw raw;  // the checkpoint fields stay unused
+  float x[kBwdTok][kLaneChunkRows], dt[kBwdTok][kLaneChunkRows], dy[kBwdTok][kLaneChunkRows];
+  uint4 act[4][kLaneChunkRows];  // u, Δraw, dout, z: a row's 8 tokens (bf16)
+  uint4 bcr[2][16];              // B, C: 8 tokens × 16 states (bf16)
 };
+
+// the raw inputs of block blk for the CTA's rows (thread l: row o.r = first + l)
+__device__ __forceinline__ void lane_chunk_issue(LaneChunkSmem& sm, const BwdArgs& p, const CtaPos& o, int64_t blk) {
+  const int64_t t0 = blk * kBwdTok;
+  const int l = threadIdx.x;
+  const bool row_ok = o.row_ok;
+#pragma unroll
+  for (int wt = 0; wt < 4; ++wt) {
+    const void* base = wt == 0 ? p.u : (wt == 1 ? p.delta : (wt == 2 ? p.dout : p.z));
+    const bool ok = row_ok && base != nullptr;
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(ok ? base : p.u) + (ok ? o.row * p.L + t0 : 0);
+    cp_async16(&sm.act[wt][l], src, ok ? 16 : 0);
+  }
+  {  // B and C: 256 bytes each
+    const int wt = l / 16, qq = l % 16;
+    cp_async16(&sm.bcr[wt][qq], static_cast<const __nv_bfloat16*>(wt ? p.C : p.B) + (o.b * p.L + t0) * kBwdN + qq * 8,
+               16);
+  }
+}
 
 template <bool PRECISE>
 __device__ __forceinline__ void lane_chunk_body(LaneChunkSmem& sm, const BwdArgs& p, const BwdWs& w,
                                                 const CtaPos& o, const float (&a)[kBwdN], const float (&na)[kBwdN],
                                                 float biasc) {
-  const int r = threadIdx.x;
-  const int64_t c0 = (o.rt % p.ctiles) * kBwdRows;
+  const int l = threadIdx.x, r = o.r;  // r: the row within the 64-row tile
   const bool want_g = o.chunk > 0;  // chunk 0 sends no adjoint further left
   float h[kBwdN], P[kBwdN], G[kBwdN];
 #pragma unroll
@@ -1111,7 +1130,7 @@ __device__ __forceinline__ void lane_chunk_body(LaneChunkSmem& sm, const BwdArgs
   }
   float S = 0.f;
   if (o.blk0 < o.blk1) {
-    lane_issue<false>(sm.raw, p, w, o.b, c0, o.rt, o.blk0);
+    lane_chunk_issue(sm, p, o, o.blk0);
     cp_async_commit();
   }
   for (int64_t blk = o.blk0; blk < o.blk1; ++blk) {
@@ -1123,38 +1142,38 @@ __device__ __forceinline__ void lane_chunk_body(LaneChunkSmem& sm, const BwdArgs
     cp_async_wait<0>();
     __syncthreads();  // the raw copy is in; the previous block's B, C are no longer read
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = r * 4 + k;  // [token][B|C][n]
+    for (int k = 0; k < 8; ++k) {
+      const int i = l * 8 + k;  // [token][B|C][n]
       const int v = i / (2 * kBwdN), wt = (i / kBwdN) & 1, n = i % kBwdN;
-      sm.bc[v][wt][n] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(&sm.raw.bc[wt][0])[v * kBwdN + n]);
+      sm.bc[v][wt][n] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(&sm.bcr[wt][0])[v * kBwdN + n]);
     }
     {
-      const uint4 U = sm.raw.act[0][r], Dr = sm.raw.act[1][r], Go = sm.raw.act[2][r], Z = sm.raw.act[3][r];
+      const uint4 U = sm.act[0][l], Dr = sm.act[1][l], Go = sm.act[2][l], Z = sm.act[3][l];
       const __nv_bfloat16* u8 = reinterpret_cast<const __nv_bfloat16*>(&U);
       const __nv_bfloat16* d8 = reinterpret_cast<const __nv_bfloat16*>(&Dr);
       const __nv_bfloat16* g8 = reinterpret_cast<const __nv_bfloat16*>(&Go);
       const __nv_bfloat16* z8 = reinterpret_cast<const __nv_bfloat16*>(&Z);
 #pragma unroll
       for (int v = 0; v < kBwdTok; ++v) {
-        sm.x[v][r] = __bfloat162float(u8[v]);
-        sm.dt[v][r] = softplus_fast(__bfloat162float(d8[v]) + biasc);
+        sm.x[v][l] = __bfloat162float(u8[v]);
+        sm.dt[v][l] = softplus_fast(__bfloat162float(d8[v]) + biasc);
         const float go = __bfloat162float(g8[v]);
         if (p.z) {
           const float zv = __bfloat162float(z8[v]);
-          sm.dy[v][r] = go * zv * rcp_approx(1.f + ex2_approx(-zv * kLog2e));
+          sm.dy[v][l] = go * zv * rcp_approx(1.f + ex2_approx(-zv * kLog2e));
         } else {
-          sm.dy[v][r] = go;
+          sm.dy[v][l] = go;
         }
       }
     }
     __syncthreads();  // B, C converted and the raw buffer read: the next block's copy may land
     if (blk + 1 < o.blk1) {
-      lane_issue<false>(sm.raw, p, w, o.b, c0, o.rt, blk + 1);
+      lane_chunk_issue(sm, p, o, blk + 1);
       cp_async_commit();
     }
 #pragma unroll 1
     for (int v = 0; v < kBwdTok; ++v) {
-      const float xv = sm.x[v][r], dtv = sm.dt[v][r], dyv = sm.dy[v][r], dl = dtv * kLog2e;
+      const float xv = sm.x[v][l], dtv = sm.dt[v][l], dyv = sm.dy[v][l], dl = dtv * kLog2e;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float4 B4 = *reinterpret_cast<const float4*>(&sm.bc[v][0][4 * q]);
@@ -1206,9 +1225,9 @@ __device__ __forceinline__ void lane_chunk_body(LaneChunkSmem& sm, const BwdArgs
   w.stot[cs * kBwdRows + r] = S;
 }
 
-__global__ void __launch_bounds__(kLaneThreads, 8) scan_bwd_lane_chunk_kernel(const BwdArgs p, const BwdWs w) {
+__global__ void __launch_bounds__(kLaneChunkRows, 16) scan_bwd_lane_chunk_kernel(const BwdArgs p, const BwdWs w) {
   __shared__ __align__(16) LaneChunkSmem sm;
-  const CtaPos o = lane_pos(p);
+  const CtaPos o = lane_pos(p, kBwdRows / kLaneChunkRows);
   float a[kBwdN];
   const bool zero = lane_a(p, o, a);
   const float biasc = (o.row_ok && p.bias) ? p.bias[o.c] : 0.f;
@@ -1316,7 +1335,7 @@ cudaError_t bwd_launch_t(BwdArgs p, cudaStream_t s, bool lane) {
   const BwdWs w = ws_layout(p.ckpt, R, p.nblk, p.kmax);
   const dim3 grid((unsigned)R, (unsigned)p.nchunks);
   if (lane)
-    scan_bwd_lane_chunk_kernel<<<grid, kLaneThreads, 0, s>>>(p, w);
+    scan_bwd_lane_chunk_kernel<<<dim3(grid.x * (kBwdRows / kLaneChunkRows), grid.y), kLaneChunkRows, 0, s>>>(p, w);
   else
     scan_bwd_chunk_kernel<T, PF><<<grid, kBwdThreads, 0, s>>>(p, w);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
