@@ -211,3 +211,31 @@ def test_bwd_lane_and_quad_forms_agree(hooks):
             continue
         el, eq = rel_err(to_np(gl[k]), r[k]), rel_err(to_np(gq[k]), r[k])
         assert el <= TOL[torch.bfloat16] and eq <= TOL[torch.bfloat16], f"{k}: {el:.3e} / {eq:.3e}"
+
+
+def test_bwd_unaligned_gradient_views():
+    """bf16, d_state 16, L a multiple of 8, but du, the Δraw gradient and dz 2-byte aligned
+    only: the call takes the four-threads-per-row gradient pass (the one-thread-per-row
+    pass stores whole 16-byte row pieces) and matches the oracle like the aligned call."""
+    b, d, N, L = 2, 70, 16, 96
+    inp = W.random_scan_inputs(b, d, N, L, dtype=torch.bfloat16, device=DEV, seed=71, a_kind="random")
+    dout = _dout(inp, 72)
+
+    def off_view(shape, dtype):
+        n = int(np.prod(shape))
+        return torch.empty(n + 1, dtype=dtype, device=DEV)[1:].view(shape)
+
+    g = dict(du=off_view(inp["u"].shape, torch.bfloat16), ddelta=off_view(inp["u"].shape, torch.bfloat16),
+             dz=off_view(inp["u"].shape, torch.bfloat16),
+             dA=torch.empty(inp["A"].shape, dtype=torch.float32, device=DEV),
+             dB=torch.empty(inp["B"].shape, dtype=torch.float32, device=DEV),
+             dC=torch.empty(inp["C"].shape, dtype=torch.float32, device=DEV),
+             dD=torch.empty_like(inp["D"]), dbias=torch.empty((d,), dtype=torch.float32, device=DEV))
+    assert g["du"].data_ptr() % 16 != 0
+    ssm.ssm_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["bias"], dout,
+                     g["du"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"], g["dz"], g["dbias"])
+    torch.cuda.synchronize()
+    r = _ref(inp, dout)
+    for k in GRADS:
+        e = rel_err(to_np(g[k]), r[k])
+        assert e <= TOL[torch.bfloat16], f"{k}: rel err {e:.3e}"
