@@ -12,10 +12,11 @@
 //   da += dh_t (Δ Ā h_{t-1} + B x (Δ Ā − φ)/a), dh_{t-1} = Ā dh_t
 //   dΔraw = dΔ·sigmoid(Δraw + bias), dbias += dΔraw.
 //
-// Organisation: four threads per (batch, channel) row, four states each; a CTA
-// holds kBwdRows rows of one batch and one chunk of the sequence, so that the
-// grid is (row tiles) × (chunks) and short batches still fill the GPU.  Two
-// launches, neither waiting on another CTA:
+// Organisation: a CTA holds kBwdRows rows of one batch and one chunk of the sequence,
+// so that the grid is (row tiles) × (chunks) and short batches still fill the GPU;
+// four threads per (batch, channel) row, four states each, in general, and one
+// thread per row for bf16 rows of 16 states (the kernels further below, which keep
+// the same workspace layout).  Two launches, neither waiting on another CTA:
 //   1. scan_bwd_chunk_kernel runs each chunk forward from h = 0 and saves, every
 //      kBwdTok tokens, that local state and the Δ summed since the chunk's start;
 //      at the chunk's end it saves the local end state, the chunk's ΣΔ and the
@@ -679,10 +680,11 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
 //    fused multiply-adds.  A CTA with an A = 0 state takes the general form per state
 //    (PRECISE).
 //  * dB and dC, sums over the rows: each thread writes its 32 (B | C, n) terms of a
-//    token to a [32 rows][32] tile (16-byte groups XOR-swizzled by row); lane j sums
-//    8 rows × 4 terms from it (every 8 lanes of a 128-bit access hit distinct banks), and two exchanges
-//    over lane bits 4 and 3 finish the warp's sum of one term per lane; the two
-//    warps' sums meet in shared memory and leave once per (token, term) per CTA.
+//    token to a [32 rows][32] tile (16-byte groups XOR-swizzled by row, so that the 8
+//    lanes of each 128-bit access hit distinct banks); lane j sums 8 rows × 4 terms
+//    from it, and two exchanges over lane bits 4 and 3 finish the warp's sum of one
+//    term per lane; the two warps' sums meet in shared memory and leave once per
+//    (token, term) per CTA.
 constexpr int kLaneThreads = kBwdRows;  // one thread per row
 
 struct LaneRaw {
