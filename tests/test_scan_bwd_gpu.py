@@ -239,3 +239,40 @@ def test_bwd_unaligned_gradient_views():
     for k in GRADS:
         e = rel_err(to_np(g[k]), r[k])
         assert e <= TOL[torch.bfloat16], f"{k}: rel err {e:.3e}"
+
+
+@pytest.mark.parametrize("name", ["mamba130m_layer", "mamba2p8b_layer"])
+def test_bwd_layer_full_size_sampled(name):
+    """The Mamba-shaped layers at full size (8 × 1536 × 16 × 2048 and 4 × 5120 × 16 × 4096,
+    bf16), with the benchmark's inputs and launch (the planner's chunk count, one thread per
+    row): du, the Δraw gradient and dz of six channels in every batch row, and those
+    channels' dA, dD and dbias (sums over the batch), against the oracle run on those
+    channels alone; on the 130M-shaped layer also dB and dC of batch row 0 (sums over all
+    1536 channels) against the oracle run on that batch row (the 2.8B-shaped layer's would
+    take the single-threaded oracle about a minute)."""
+    shape = W.SCAN_SHAPES[name]
+    inp = W.scan_inputs(shape, device=DEV, seed=0)
+    gen = torch.Generator(device=DEV).manual_seed(1)
+    dout = torch.randn(inp["u"].shape, generator=gen, device=DEV).to(shape.dtype)
+    g = _run(inp, dout)
+    tol = TOL[torch.bfloat16]
+    d = shape.d_inner
+    chans = [0, 1, d // 3, d // 2, d - 2, d - 1]
+    pick = lambda t: to_np(t[:, chans])
+    r = oracle.scan_bwd(pick(inp["u"]), pick(inp["delta"]), to_np(inp["A"][chans]), to_np(inp["B"]),
+                        to_np(inp["C"]), pick(dout), D=to_np(inp["D"][chans]), z=pick(inp["z"]),
+                        bias=to_np(inp["bias"][chans]))
+    for k in ("du", "ddelta", "dz"):
+        e = rel_err(to_np(g[k][:, chans]), r[k])
+        assert e <= tol, f"{k}: rel err {e:.3e}"
+    for k in ("dA", "dD", "dbias"):
+        e = rel_err(to_np(g[k][chans]), r[k])
+        assert e <= tol, f"{k}: rel err {e:.3e}"
+    if name != "mamba130m_layer":
+        return
+    row0 = lambda t: to_np(t[:1])
+    r0 = oracle.scan_bwd(row0(inp["u"]), row0(inp["delta"]), to_np(inp["A"]), row0(inp["B"]), row0(inp["C"]),
+                         row0(dout), D=to_np(inp["D"]), z=row0(inp["z"]), bias=to_np(inp["bias"]))
+    for k in ("dB", "dC"):
+        e = rel_err(to_np(g[k][:1]), r0[k])
+        assert e <= tol, f"{k}: rel err {e:.3e}"
