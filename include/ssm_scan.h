@@ -203,10 +203,10 @@ SSM_API ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A
  * 4·2·d_state bytes per (64-channel tile, batch, token) and 4·(d_state + 2) bytes
  * per (batch, chunk, channel) of partials).  dA, dB, dC, dD, ddelta_bias need not be
  * zeroed.  Three kernel launches on `stream`; no host sync.  Repeated calls on the same
- * inputs, device and dims return identical bits, provided the arrays keep their 16-byte
- * alignment or lack of it (bf16 rows at d_state 16 with L a multiple of 8 take a kernel
- * with one thread per row when every row array is 16-byte aligned, else one with four,
- * and the two add in different orders).
+ * inputs, device and dims return identical bits, provided the input arrays keep their
+ * 16-byte alignment or lack of it (bf16 rows at d_state 16 with L a multiple of 8 take a
+ * kernel with one thread per row when u, delta, dout, z, B and C are 16-byte aligned,
+ * else one with four, and the two add in different orders).
  */
 SSM_API size_t ssm_scan_bwd_deterministic_workspace_bytes(const ssm_dims* dims);
 SSM_API ssm_status ssm_scan_bwd_deterministic(const void* u, const void* delta, const float* A, const void* B,

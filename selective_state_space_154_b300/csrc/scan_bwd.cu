@@ -1359,12 +1359,7 @@ bool bwd_prefetch_ok(const BwdArgs& p) {
   return p.act == 1 && p.N == kBwdN && p.L % kBwdTok == 0 && a16(p.u) && a16(p.delta) && a16(p.dout) &&
          a16(p.z) && a16(p.B) && a16(p.C);
 }
-// The one-thread-per-row gradient pass also stores whole 16-byte row pieces of du, the Δraw
-// gradient and dz.
-bool bwd_lane_ok(const BwdArgs& p) {
-  auto a16 = [](const void* q) { return q == nullptr || (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
-  return bwd_prefetch_ok(p) && a16(p.du) && a16(p.ddelta) && a16(p.dz);
-}
+
 
 }  // namespace
 
@@ -1407,7 +1402,7 @@ cudaError_t scan_bwd_launch(BwdArgs p, cudaStream_t stream) {
   }
   if (p.act != 1) return bwd_launch_t<float, false>(p, stream, false);
   if (!bwd_prefetch_ok(p)) return bwd_launch_t<__nv_bfloat16, false>(p, stream, false);
-  return bwd_launch_t<__nv_bfloat16, true>(p, stream, p.form != 1 && bwd_lane_ok(p));
+  return bwd_launch_t<__nv_bfloat16, true>(p, stream, p.form != 1);
 }
 
 }  // namespace ssm

@@ -214,9 +214,9 @@ def test_bwd_lane_and_quad_forms_agree(hooks):
 
 
 def test_bwd_unaligned_gradient_views():
-    """bf16, d_state 16, L a multiple of 8, but du, the Δraw gradient and dz 2-byte aligned
-    only: the call takes the four-threads-per-row gradient pass (the one-thread-per-row
-    pass stores whole 16-byte row pieces) and matches the oracle like the aligned call."""
+    """bf16, d_state 16, L a multiple of 8, with du, the Δraw gradient and dz 2-byte aligned
+    only (the gradient passes store them one element at a time): the result matches the
+    oracle like the aligned call's."""
     b, d, N, L = 2, 70, 16, 96
     inp = W.random_scan_inputs(b, d, N, L, dtype=torch.bfloat16, device=DEV, seed=71, a_kind="random")
     dout = _dout(inp, 72)
