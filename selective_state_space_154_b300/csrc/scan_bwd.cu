@@ -756,24 +756,15 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
   const int64_t b = o.b, L = p.L;
   const int64_t c0 = (o.rt % p.ctiles) * kBwdRows;
 
-  // the state entering the chunk and the adjoint entering it from the right
+  // The chunk pass's chunks ("fine") f_lo..f_hi make up this chunk.  The adjoint entering
+  // it from the right comes from the fine chunks after f_hi; the state entering each fine
+  // chunk, h_in, is formed when the walk reaches it.
+  const int f_hi = min((o.chunk + 1) * p.sub, p.nfine) - 1;
   float hin[kBwdN], dh[kBwdN];
-  {
 #pragma unroll
-    for (int n = 0; n < kBwdN; ++n) hin[n] = dh[n] = 0.f;
-    for (int j = 0; j < o.chunk; ++j) {
-      const int64_t cs = o.rt * p.kmax + j;
-      const float st = w.stot[cs * kBwdRows + r] * kLog2e;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 H = w.hend[cs * kBwdThreads + 4 * r + q];
-        const float hv[4] = {H.x, H.y, H.z, H.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) hin[4 * q + k] = fmaf(ex2_approx(a[4 * q + k] * st), hin[4 * q + k], hv[k]);
-      }
-    }
-  }
-  for (int j = p.nchunks - 1; j > o.chunk; --j) {
+  for (int n = 0; n < kBwdN; ++n) hin[n] = dh[n] = 0.f;
+  int f_cur = -1;
+  for (int j = p.nfine - 1; j > f_hi; --j) {
     const int64_t cs = o.rt * p.kmax + j;
     const float st = w.stot[cs * kBwdRows + r] * kLog2e;
 #pragma unroll
@@ -797,6 +788,23 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
   }
   for (int64_t blk = o.blk1 - 1; blk >= o.blk0; --blk) {
     const int64_t t0 = blk * kBwdTok;
+    const int f = (int)(blk / p.cblk_f);
+    if (f != f_cur) {  // h_in = Σ_{j<f} (Π_{j<i<f} e^{a S_i}) H_j over the fine chunks
+      f_cur = f;
+#pragma unroll
+      for (int n = 0; n < kBwdN; ++n) hin[n] = 0.f;
+      for (int j = 0; j < f; ++j) {
+        const int64_t cs = o.rt * p.kmax + j;
+        const float st = w.stot[cs * kBwdRows + r] * kLog2e;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 H = w.hend[cs * kBwdThreads + 4 * r + q];
+          const float hv[4] = {H.x, H.y, H.z, H.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) hin[4 * q + k] = fmaf(ex2_approx(a[4 * q + k] * st), hin[4 * q + k], hv[k]);
+        }
+      }
+    }
     cp_async_wait<0>();
     __syncthreads();  // the raw copy is in; red of the previous block has been read
     // B and C to fp32 (4 values per thread)
@@ -1036,7 +1044,7 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
 }
 
 // split: CTAs per 64-row tile (thread t of CTA x serves row (x % split) · 64/split + t)
-__device__ __forceinline__ CtaPos lane_pos(const BwdArgs& p, int split) {
+__device__ __forceinline__ CtaPos lane_pos(const BwdArgs& p, int split, int64_t cblk) {
   CtaPos o;
   o.rt = blockIdx.x / split;
   o.chunk = (int)blockIdx.y;
@@ -1047,8 +1055,8 @@ __device__ __forceinline__ CtaPos lane_pos(const BwdArgs& p, int split) {
   o.row_ok = c0 + o.r < p.d_inner;
   o.c = c0 + (o.row_ok ? o.r : 0);
   o.row = o.b * p.d_inner + o.c;
-  o.blk0 = o.chunk * p.cblk;
-  o.blk1 = o.blk0 + p.cblk < p.nblk ? o.blk0 + p.cblk : p.nblk;
+  o.blk0 = o.chunk * cblk;
+  o.blk1 = o.blk0 + cblk < p.nblk ? o.blk0 + cblk : p.nblk;
   return o;
 }
 // A of the row (0 for |A| < 2^-60; rows past d_inner take A = -1); true if a state has A = 0
@@ -1067,7 +1075,7 @@ __device__ __forceinline__ bool lane_a(const BwdArgs& p, const CtaPos& o, float 
 __global__ void __launch_bounds__(kLaneThreads, 4) scan_bwd_lane_kernel(const BwdArgs p, const BwdWs w) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   LaneSmem& sm = *reinterpret_cast<LaneSmem*>(smem_raw);
-  const CtaPos o = lane_pos(p, 1);
+  const CtaPos o = lane_pos(p, 1, p.cblk);
   float a[kBwdN];
   const bool zero = lane_a(p, o, a);
   const float Dc = (o.row_ok && p.D) ? p.D[o.c] : 0.f;
@@ -1229,7 +1237,7 @@ __device__ __forceinline__ void lane_chunk_body(LaneChunkSmem& sm, const BwdArgs
 
 __global__ void __launch_bounds__(kLaneChunkRows, 16) scan_bwd_lane_chunk_kernel(const BwdArgs p, const BwdWs w) {
   __shared__ __align__(16) LaneChunkSmem sm;
-  const CtaPos o = lane_pos(p, kBwdRows / kLaneChunkRows);
+  const CtaPos o = lane_pos(p, kBwdRows / kLaneChunkRows, p.cblk_f);
   float a[kBwdN];
   const bool zero = lane_a(p, o, a);
   const float biasc = (o.row_ok && p.bias) ? p.bias[o.c] : 0.f;
@@ -1334,10 +1342,25 @@ cudaError_t bwd_launch_t(BwdArgs p, cudaStream_t s, bool lane) {
   if (k < 1) k = 1;
   p.cblk = (p.nblk + k - 1) / k;
   p.nchunks = p.cblk > 0 ? (int)((p.nblk + p.cblk - 1) / p.cblk) : 1;
+  // The one-thread-per-row chunk pass runs two one-warp CTAs per tile and chunk, sixteen
+  // per SM; when the gradient pass's chunks leave it under half of those slots, it takes
+  // each of them as two chunks of its own.
+  p.sub = 1;
+  if (lane && p.cblk >= 2 && 2 * p.nchunks <= p.kmax) {
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (R * p.nchunks * (kBwdRows / kLaneChunkRows) * 2 <= (int64_t)sms * 16) p.sub = 2;
+  }
+  p.cblk_f = (p.cblk + p.sub - 1) / p.sub;
+  p.cblk = p.cblk_f * p.sub;
+  p.nchunks = (int)((p.nblk + p.cblk - 1) / p.cblk);
+  p.nfine = (int)((p.nblk + p.cblk_f - 1) / p.cblk_f);
   const BwdWs w = ws_layout(p.ckpt, R, p.nblk, p.kmax);
   const dim3 grid((unsigned)R, (unsigned)p.nchunks);
   if (lane)
-    scan_bwd_lane_chunk_kernel<<<dim3(grid.x * (kBwdRows / kLaneChunkRows), grid.y), kLaneChunkRows, 0, s>>>(p, w);
+    scan_bwd_lane_chunk_kernel<<<dim3(grid.x * (kBwdRows / kLaneChunkRows), (unsigned)p.nfine), kLaneChunkRows, 0,
+                                 s>>>(p, w);
   else
     scan_bwd_chunk_kernel<T, PF><<<grid, kBwdThreads, 0, s>>>(p, w);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;

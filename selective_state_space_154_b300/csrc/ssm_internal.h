@@ -175,6 +175,10 @@ struct BwdArgs {
   float* part_row;  // [batch][chunk][d_inner][dA 0..N-1 | dD | dbias]
   int64_t batch, d_inner, N, L, nblk, cblk;
   int ctiles, act, nchunks, kmax, force_chunks, det;
+  // the chunk pass's chunks: each of the gradient pass's chunks is `sub` of them, of cblk_f
+  // blocks (nfine in all); sub = 1 except for the one-thread-per-row form
+  int64_t cblk_f;
+  int nfine, sub;
   int form;  // gradient pass: 0 by shape, 1 four threads per row (test hook)
 };
 // deterministic = false: the checkpoints and chunk summaries; true: those plus the partial sums
