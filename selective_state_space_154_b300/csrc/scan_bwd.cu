@@ -901,6 +901,7 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
     float* xrow = xsw + lane * 32;  // this row's 32 terms: dB, then dC (groups swizzled)
     const int sw = lane & 7;
     const int64_t i0 = o.row * L + t0;
+    float4 o0 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
     for (int v = kBwdTok - 1; v >= 0; --v) {
       float hp[kBwdN];
@@ -984,11 +985,13 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
       y = fmaf(Dc, x, y);
       dx = fmaf(dyv, Dc, dx);
       const float dr = ddt * sm.ts.sig[v][r];
-      if (row_ok) {
-        static_cast<__nv_bfloat16*>(p.du)[i0 + v] = __float2bfloat16_rn(dx);
-        static_cast<__nv_bfloat16*>(p.ddelta)[i0 + v] = __float2bfloat16_rn(dr);
-        if (p.z) static_cast<__nv_bfloat16*>(p.dz)[i0 + v] = __float2bfloat16_rn(sm.ts.dzf[v][r] * y);
-      }
+      // the token's du, Δraw gradient and dz wait in the row's spent state slot (token 0's in
+      // registers) and leave with the block's other tokens
+      const float dzv = sm.ts.dzf[v][r] * y;
+      if (v > 0)
+        sm.hp[v - 1][1][r] = make_float4(dx, dr, dzv, 0.f);
+      else
+        o0 = make_float4(dx, dr, dzv, 0.f);
       dD_acc = fmaf(dyv, x, dD_acc);
       db_acc += dr;
       // Σ over the warp's rows of the 32 terms
@@ -1011,6 +1014,34 @@ __device__ __forceinline__ void lane_body(LaneSmem& sm, const BwdArgs& p, const 
       lane_red(sm, v, warp)[4 * sg + 2 * (up4 ? 1 : 0) + (up3 ? 1 : 0)] = sfin;
 #pragma unroll
       for (int n = 0; n < kBwdN; ++n) h[n] = hp[n];
+    }
+    if (row_ok) {  // the block's 8 tokens of du, the Δraw gradient and dz of this row
+      float ov[3][kBwdTok];
+      ov[0][0] = o0.x; ov[1][0] = o0.y; ov[2][0] = o0.z;
+#pragma unroll
+      for (int v = 1; v < kBwdTok; ++v) {
+        const float4 t4 = sm.hp[v - 1][1][r];
+        ov[0][v] = t4.x; ov[1][v] = t4.y; ov[2][v] = t4.z;
+      }
+      void* dst[3] = {p.du, p.ddelta, p.dz};
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        if (k == 2 && !p.z) break;
+        __nv_bfloat16* d = static_cast<__nv_bfloat16*>(dst[k]) + i0;
+        if ((reinterpret_cast<uintptr_t>(d) & 15u) == 0) {
+          uint4 pk;
+          unsigned* pw = &pk.x;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            __nv_bfloat162 t = __floats2bfloat162_rn(ov[k][2 * j], ov[k][2 * j + 1]);
+            pw[j] = *reinterpret_cast<unsigned*>(&t);
+          }
+          *reinterpret_cast<uint4*>(d) = pk;
+        } else {
+#pragma unroll
+          for (int v = 0; v < kBwdTok; ++v) d[v] = __float2bfloat16_rn(ov[k][v]);
+        }
+      }
     }
     __syncthreads();  // both warps' sums are in red
 #pragma unroll
