@@ -528,7 +528,6 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     }
     // adjoint over the block, last token first
     auto adjoint = [&](int v) {
-      const int64_t i = row * L + t0 + v;
       const TokScalars s = sm.st.ts[v][r];
       const float4 hv4 = sm.hs[v + 1][r][g], hp4 = sm.hs[v][r][g];
       const float hv[kBwdG] = {hv4.x, hv4.y, hv4.z, hv4.w};
@@ -607,11 +606,9 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
       if (g == 0) {
         dD_acc = fmaf(dy, s.x, dD_acc);
         db_acc += dr;
-        if (row_ok) {
-          stf<T>(p.du, i, dx);
-          stf<T>(p.ddelta, i, dr);
-          if (p.z) stf<T>(p.dz, i, s.dzf * y);
-        }
+        // the token's du, Δraw gradient and dz wait in this thread's slot of h_t, which no
+        // later (earlier-in-time) token reads, until the block's end
+        sm.hs[v + 1][r][0] = make_float4(dx, dr, s.dzf * y, 0.f);
       }
       // Σ over the CTA's rows of the 32 (B|C, n) slots: warp reduce-scatter, then shared memory
       sm.red[warp][v][lane] = rows_reduce_scatter8(slots);
@@ -621,6 +618,35 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
       for (int v = kBwdTok - 1; v >= 0; --v) adjoint(v);
     } else {
       for (int v = nv - 1; v >= 0; --v) adjoint(v);
+    }
+    __syncwarp();  // the row's staged outputs are visible to its four threads
+    if (row_ok && g < (p.z ? 3 : 2)) {  // thread g stores the block's tokens of du, dΔraw, dz
+      T* d = static_cast<T*>(g == 0 ? p.du : (g == 1 ? p.ddelta : p.dz)) + row * L + t0;
+      auto staged = [&](int v) {
+        const float4 t4 = sm.hs[v + 1][r][0];
+        return g == 0 ? t4.x : (g == 1 ? t4.y : t4.z);
+      };
+      if (nv == kBwdTok && (reinterpret_cast<uintptr_t>(d) & 15u) == 0) {
+        float ov[kBwdTok];
+#pragma unroll
+        for (int v = 0; v < kBwdTok; ++v) ov[v] = staged(v);
+        if (sizeof(T) == 2) {
+          uint4 pk;
+          unsigned* pw = &pk.x;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            __nv_bfloat162 t = __floats2bfloat162_rn(ov[2 * j], ov[2 * j + 1]);
+            pw[j] = *reinterpret_cast<unsigned*>(&t);
+          }
+          *reinterpret_cast<uint4*>(d) = pk;
+        } else {
+          float4* d4 = reinterpret_cast<float4*>(d);
+          d4[0] = make_float4(ov[0], ov[1], ov[2], ov[3]);
+          d4[1] = make_float4(ov[4], ov[5], ov[6], ov[7]);
+        }
+      } else {
+        for (int v = 0; v < nv; ++v) stf<T>(d, v, staged(v));
+      }
     }
     __syncthreads();  // red complete
     for (int sidx = threadIdx.x; sidx < nv * 32; sidx += kBwdThreads) {
